@@ -1,0 +1,148 @@
+"""Oracle for the GLA forward pass — TEST INFRASTRUCTURE ONLY.
+
+A plain fp64 CPU implementation (``gla_oracle.c``) of the gated linear attention recurrence and of the
+chunk-local gate cumsum, wrapped with ctypes over numpy arrays.  Only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
+neither imports nor links it; the two share no code.
+
+Method citations (page "fla/ops/gla/fused_chunk.py"):
+  * recurrence / state carry: ``fused_chunk_gla_fwd_kernel`` (state update ``h*exp(G_last) + k_g^T v``,
+    output ``q_g h``, initial state load and final state store);
+  * intra-chunk term with inclusive diagonal: ``fwd_inner_chunk``;
+  * gated operands ``q*exp(G)*scale`` and ``k*exp(G_last-G)``: ``prepare_qg_kg``;
+  * chunk-local cumsum in fp32: ``FusedChunkGLAFunction.forward``.
+Varlen convention (offsets, per-sequence states): page "fla/ops/ttt/fused_chunk.py",
+``fused_chunk_ttt_linear_fwd_kernel`` and ``fused_chunk_ttt_linear``.
+
+Pins: every function here is checked in ``tests/test_oracle.py`` against quantities that do not come from
+the oracle itself (brute-force quadratic form, the g == 0 closed form, scalar closed forms, state-split
+invariance, varlen == separate runs, symmetry invariances, and hand-derived golden fixtures).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gla_oracle.c`` into ``oracle/_build/liboracle.so`` (portable flags, no -march)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            p = ctypes.c_void_p
+            i = ctypes.c_int
+            lib.oracle_gla_fwd.argtypes = [p, p, p, p, i, p, p, p, p, i, i, i, i, i, i,
+                                           ctypes.c_double, i]
+            lib.oracle_gla_fwd.restype = i
+            lib.oracle_chunk_local_cumsum.argtypes = [p, i, p, p, i, i, i, i, i, i]
+            lib.oracle_chunk_local_cumsum.restype = i
+            _lib = lib
+    return _lib
+
+
+def _as_stored(x: np.ndarray):
+    """Return (contiguous array, dtype code).  bf16 tensors are passed as their raw uint16 words."""
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, F32
+    if x.dtype == np.uint16:
+        return x, BF16
+    raise TypeError(f"oracle inputs must be float32 or bf16 words (uint16), got {x.dtype}")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def load_variant(path: str):
+    """Load a separately compiled copy of ``gla_oracle.c`` (the tests plant mistakes in such copies to
+    show that the pins catch them).  Pass the handle as ``lib=`` to :func:`gla_fwd`."""
+    lib = ctypes.CDLL(path)
+    p, i = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_gla_fwd.argtypes = [p, p, p, p, i, p, p, p, p, i, i, i, i, i, i, ctypes.c_double, i]
+    lib.oracle_gla_fwd.restype = i
+    return lib
+
+
+def gla_fwd(q, k, v, g, scale, h0=None, cu_seqlens=None, want_ht=True, nthreads=0, lib=None):
+    """fp64 step-by-step GLA forward.
+
+    q, k, g: [B, T, H, K]; v: [B, T, H, V]; all float32 or all bf16 words (uint16).
+    h0: optional [N, H, K, V] (float32 or float64; widened to float64).  cu_seqlens: optional int32 [N+1] (host), requires B == 1.
+    Returns (o float64 [B, T, H, V], ht float64 [N, H, K, V] or None, threads used).
+    """
+    (q, dt), (k, dk), (v, dv), (g, dg) = map(_as_stored, (q, k, v, g))
+    if len({dt, dk, dv, dg}) != 1:
+        raise TypeError("q, k, v, g must share one stored type")
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError("shape mismatch between q, k, v, g")
+    cu = None
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        N = cu.size - 1
+        if cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+            raise ValueError("cu_seqlens must be non-decreasing from 0 to T")
+    else:
+        N = B
+    if h0 is not None:
+        h0 = np.ascontiguousarray(h0, dtype=np.float64)  # fp32 widens exactly
+        if h0.shape != (N, H, K, V):
+            raise ValueError(f"h0 must be [N, H, K, V] = {(N, H, K, V)}, got {h0.shape}")
+    o = np.zeros((B, T, H, V), dtype=np.float64)
+    ht = np.zeros((N, H, K, V), dtype=np.float64) if want_ht else None
+    rc = (lib or _load()).oracle_gla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), dt, _ptr(h0), _ptr(o), _ptr(ht),
+                                _ptr(cu), N, B, T, H, K, V, float(scale), int(nthreads))
+    if rc < 0:
+        raise RuntimeError(f"oracle_gla_fwd failed ({rc})")
+    return o, ht, rc
+
+
+def chunk_local_cumsum(g, chunk, cu_seqlens=None):
+    """fp64 chunk-local inclusive cumsum of g [B, T, H, K], chunks aligned to each sequence start."""
+    g, dt = _as_stored(g)
+    B, T, H, K = g.shape
+    cu = None
+    N = B
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        N = cu.size - 1
+    G = np.zeros(g.shape, dtype=np.float64)
+    rc = _load().oracle_chunk_local_cumsum(_ptr(g), dt, _ptr(G), _ptr(cu), N, B, T, H, K, int(chunk))
+    if rc != 0:
+        raise RuntimeError("oracle_chunk_local_cumsum failed")
+    return G
+
+
+def bf16_words_to_f64(x: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 words (uint16) to float64, independent of torch."""
+    return (np.ascontiguousarray(x, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -1,0 +1,205 @@
+/*
+ * Oracle for the gated linear attention (GLA) forward pass — TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, slow, step-by-step fp64 CPU implementation.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library; the CUDA library never links or calls it and
+ * shares no code with it.
+ *
+ * What it computes (the GLA recurrence; the chunked kernels of
+ * "fla/ops/gla/fused_chunk.py" (fused_chunk_gla_fwd_kernel, fwd_inner_chunk) are an exact
+ * re-association of it):
+ *
+ *     S_0     = h0[n,h]            (or 0)                          K x V state
+ *     S_t     = diag(exp(g_t)) S_{t-1} + k_t^T v_t                 decay first, then the token's own term
+ *     o_t     = scale * q_t S_t
+ *     ht[n,h] = S_last
+ *
+ * Inputs are read in their stored type (fp32, or bf16 stored as raw 16-bit words) and widened exactly
+ * to double element by element; nothing is rounded on the way.  Layouts are time-major with interleaved
+ * heads: q, k, g are [rows, H, K] and v, o are [rows, H, V] where rows = B*T (dense) or the packed
+ * total length (varlen, B == 1).  h0 / ht are [N, H, K, V] in double (an fp32 h0 widens exactly).
+ *
+ * Readings of the pages taken here (each one also listed in the design notes):
+ *   - decay is applied before the token's own k^T v is added, and q_t sees S_t including token t
+ *     (the inclusive diagonal of fwd_inner_chunk, and k*exp(G_last-G) being k at the last position in
+ *     prepare_qg_kg);
+ *   - scale multiplies q only, so ht carries no scale;
+ *   - h0 is decayed by the first token's gate like any carried state (fused_chunk_gla_fwd_kernel);
+ *   - varlen sequences are independent, a zero-length sequence gives ht = h0 (or 0).
+ * The chunk size does not enter: the result is the same for every chunking in exact arithmetic.
+ *
+ * Also here: the chunk-local inclusive cumsum of g (chunk_local_cumsum as called by
+ * FusedChunkGLAFunction.forward), with chunks aligned to each sequence's first token.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* Exact widening of one stored element to double. bf16 is the high half of an IEEE binary32. */
+static double widen(const void *base, size_t idx, int dtype)
+{
+    if (dtype == ORACLE_F32)
+        return (double)((const float *)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+typedef struct {
+    const void *q, *k, *v, *g;
+    int dtype;
+    const double *h0;         /* [N,H,K,V] or NULL */
+    double *o;                /* [rows,H,V] */
+    double *ht;               /* [N,H,K,V] or NULL */
+    const int32_t *cu;        /* host [N+1] */
+    int N, H, K, V;
+    double scale;
+    int next;                 /* shared work counter, guarded by mu */
+    pthread_mutex_t mu;
+} fwd_job;
+
+static void run_one(fwd_job *J, int item, double *S)
+{
+    const int n = item / J->H, h = item % J->H;
+    const int H = J->H, K = J->K, V = J->V;
+    const long bos = J->cu[n], eos = J->cu[n + 1];
+
+    for (int i = 0; i < K; ++i)
+        for (int j = 0; j < V; ++j)
+            S[(size_t)i * V + j] = J->h0 ? J->h0[(((size_t)n * H + h) * K + i) * V + j] : 0.0;
+
+    for (long t = bos; t < eos; ++t) {
+        const size_t kb = ((size_t)t * H + h) * K, vb = ((size_t)t * H + h) * V;
+        for (int i = 0; i < K; ++i) {
+            const double decay = exp(widen(J->g, kb + i, J->dtype));
+            const double ki = widen(J->k, kb + i, J->dtype);
+            double *row = S + (size_t)i * V;
+            for (int j = 0; j < V; ++j)
+                row[j] = decay * row[j] + ki * widen(J->v, vb + j, J->dtype);
+        }
+        for (int j = 0; j < V; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < K; ++i)
+                acc += widen(J->q, kb + i, J->dtype) * S[(size_t)i * V + j];
+            J->o[vb + j] = J->scale * acc;
+        }
+    }
+    if (J->ht)
+        memcpy(J->ht + ((size_t)n * H + h) * K * V, S, sizeof(double) * (size_t)K * V);
+}
+
+static void *worker(void *arg)
+{
+    fwd_job *J = (fwd_job *)arg;
+    double *S = (double *)malloc(sizeof(double) * (size_t)J->K * J->V);
+    if (!S)
+        return (void *)1;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int item = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (item >= J->N * J->H)
+            break;
+        run_one(J, item, S);
+    }
+    free(S);
+    return NULL;
+}
+
+static int resolve_threads(int nthreads, int items)
+{
+    if (nthreads <= 0) {
+        long c = sysconf(_SC_NPROCESSORS_ONLN);
+        nthreads = c > 0 ? (int)c : 1;
+    }
+    if (nthreads > items)
+        nthreads = items;
+    return nthreads < 1 ? 1 : nthreads;
+}
+
+/*
+ * Step-by-step fp64 recurrence.  cu_seqlens is a HOST array of N+1 offsets into the packed rows; pass
+ * NULL for the dense batch (then N = B sequences of T rows each).  Returns the number of threads used,
+ * or a negative value on bad arguments / allocation failure.
+ */
+int oracle_gla_fwd(const void *q, const void *k, const void *v, const void *g, int dtype,
+                   const double *h0, double *o, double *ht, const int32_t *cu_seqlens, int N,
+                   int B, int T, int H, int K, int V, double scale, int nthreads)
+{
+    if (!q || !k || !v || !g || !o || H <= 0 || K <= 0 || V <= 0 || B < 0 || T < 0)
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+        return -1;
+    int32_t *dense = NULL;
+    const int32_t *cu = cu_seqlens;
+    if (!cu) {
+        N = B;
+        dense = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N + 1));
+        if (!dense)
+            return -2;
+        for (int n = 0; n <= N; ++n)
+            dense[n] = n * T;
+        cu = dense;
+    }
+    if (N == 0) {
+        free(dense);
+        return 0;
+    }
+    fwd_job J = {q, k, v, g, dtype, h0, o, ht, cu, N, H, K, V, scale, 0, PTHREAD_MUTEX_INITIALIZER};
+    const int nt = resolve_threads(nthreads, N * H);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    int rc = nt;
+    if (!tid) {
+        free(dense);
+        return -2;
+    }
+    int started = 0;
+    for (; started < nt; ++started)
+        if (pthread_create(&tid[started], NULL, worker, &J) != 0)
+            break;
+    if (started == 0)
+        worker(&J);
+    for (int i = 0; i < started; ++i) {
+        void *res = NULL;
+        pthread_join(tid[i], &res);
+        if (res)
+            rc = -2;
+    }
+    free(tid);
+    free(dense);
+    return started ? rc : 1;
+}
+
+/*
+ * Chunk-local inclusive cumsum of the log-decay: G[t] = sum of g[u] for u from the start of t's chunk
+ * to t, where chunks of `chunk` rows start at each sequence's first row.  Single-threaded fp64.
+ */
+int oracle_chunk_local_cumsum(const void *g, int dtype, double *G, const int32_t *cu_seqlens, int N,
+                              int B, int T, int H, int K, int chunk)
+{
+    if (!g || !G || H <= 0 || K <= 0 || chunk <= 0)
+        return -1;
+    const int nseq = cu_seqlens ? N : B;
+    for (int n = 0; n < nseq; ++n) {
+        const long bos = cu_seqlens ? cu_seqlens[n] : (long)n * T;
+        const long eos = cu_seqlens ? cu_seqlens[n + 1] : (long)n * T + T;
+        for (int h = 0; h < H; ++h)
+            for (int i = 0; i < K; ++i) {
+                double run = 0.0;
+                for (long t = bos; t < eos; ++t) {
+                    if ((t - bos) % chunk == 0)
+                        run = 0.0;
+                    const size_t idx = ((size_t)t * H + h) * K + i;
+                    run += widen(g, idx, dtype);
+                    G[idx] = run;
+                }
+            }
+    }
+    return 0;
+}
