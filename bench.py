@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark of the GLA forward on GB300: one JSON line per run (rank 0).
+
+A step is one gla_fwd over one batch of the workload (every kernel of the path), inputs resident in HBM.
+L2 is flushed (a write of a buffer twice the L2 size) before each timed step, outside the timed events.
+Per-kernel times come from CUDA events that libgla records around each of its launches on the call's
+stream (gla_profile_events).  ``e2e`` repeats the measurement through the same public call with the inputs
+copied host->device from pinned memory and o/ht copied back inside the timed region.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this method has) on a bounded sample of
+the same workload instead.
+
+Multi-GPU (torchrun): the workload's sequences are independent problems, so each rank runs its own copy
+(weak scaling, no collective on the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GLA fwd tokens/s on 1 GB300; % of BF16 tensor peak or HBM roofline"
+DEFAULT_WORKLOAD = "b4_t2k_h8"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# kernel name -> source file that defines it (a traffic figure is only reused while that file is unchanged)
+KERNEL_SOURCES = {"out_ffma": "csrc/ffma_kernels.cu", "state_ffma": "csrc/ffma_kernels.cu",
+                  "scan_segments": "csrc/ffma_kernels.cu", "plan_varlen": "csrc/ffma_kernels.cu"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------------------------
+# workload arithmetic (algorithmic bytes / flops)
+# ------------------------------------------------------------------------------------------------
+
+def work_units(inp):
+    rows = inp.q.shape[0] * inp.q.shape[1]
+    esz = 4 if inp.dtype == "f32" else 2
+    K, V, H = inp.K, inp.V, inp.H
+    token_heads = rows * H
+    in_bytes = token_heads * esz * (3 * K + V)
+    out_bytes = token_heads * 4 * V
+    state = inp.N * H * K * V * 4
+    state_bytes = (state if inp.h0 is not None else 0) + state   # h0 read (if any) + ht write
+    flops = token_heads * (2 * inp.chunk * K + 2 * inp.chunk * V + 4 * K * V)
+    return dict(tokens=rows, token_heads=token_heads, bytes=in_bytes + out_bytes + state_bytes,
+                in_bytes=in_bytes, out_bytes=out_bytes, state_bytes=state_bytes, flops=flops)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_hbm(peaks):
+    for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+        if key in peaks and peaks[key]:
+            return float(peaks[key])
+    return FALLBACK_PEAKS["hbm_gbs"]
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = KERNEL_SOURCES.get(kernel)
+    if not os.path.exists(path) or src is None:
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    ent = table.get(f"{kernel}@{workload}")
+    if not ent:
+        return None
+    with open(os.path.join(ROOT, "chunkwise_gated_linear_chunked_gb300", src), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return ent["dram_bytes_per_launch"] if ent.get("src_sha") == sha else None
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="gla_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle sample (cpu_baseline and the reference arm)
+# ------------------------------------------------------------------------------------------------
+
+def oracle_sample(inp, seconds, head_start=0):
+    """Run the fp64 oracle over groups of heads (all sequences of each head) until about `seconds` of wall
+    time; return (tokens/s in the workload's unit, threads used, description).  A token of the metric is
+    one row with all H heads, so each (sequence, head) item of length L counts L / H tokens."""
+    import oracle
+    from chunkwise_gated_linear_chunked_gb300.inputs import stored_numpy
+    cores = os.cpu_count() or 1
+    H = inp.H
+    per_group = max(1, min(H, -(-cores // max(inp.N, 1))))
+    t0 = time.perf_counter()
+    token_heads, threads, groups, h = 0, 1, 0, head_start % H
+    while True:
+        heads = [(h + i) % H for i in range(per_group)]
+        sel = lambda x: x[:, :, heads].contiguous()
+        args = [stored_numpy(sel(x)) for x in (inp.q, inp.k, inp.v, inp.g)]
+        h0 = None if inp.h0 is None else inp.h0[:, heads].contiguous().numpy()
+        cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
+        ts = time.perf_counter()
+        _, _, threads = oracle.gla_fwd(*args, inp.scale, h0=h0, cu_seqlens=cu, nthreads=cores)
+        token_heads += inp.q.shape[0] * inp.q.shape[1] * len(heads)
+        groups += 1
+        h = (h + per_group) % H
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    desc = (f"fp64 oracle over {groups} group(s) of {per_group} head(s) x all {inp.N} sequence(s) "
+            f"({token_heads} token-heads, {el:.1f} s wall)")
+    return token_heads / H / el, threads, desc
+
+
+# ------------------------------------------------------------------------------------------------
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import torch
+    from chunkwise_gated_linear_chunked_gb300.inputs import WORKLOADS, workload_inputs
+
+    if args.workload not in WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {list(WORKLOADS)}")
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from chunkwise_gated_linear_chunked_gb300 import binding
+
+    inp = workload_inputs(args.workload)
+    wu = work_units(inp)
+    q, k, v, g = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.g))
+    h0 = None if inp.h0 is None else inp.h0.to(dev)
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
+    B, T, H, K, V, N = inp.q.shape[0], inp.q.shape[1], inp.H, inp.K, inp.V, inp.N
+    code = binding.GLA_F32 if inp.dtype == "f32" else binding.GLA_BF16
+    o = torch.empty(B, T, H, V, dtype=torch.float32, device=dev)
+    ht = torch.empty(N, H, K, V, dtype=torch.float32, device=dev)
+    ws = torch.zeros(max(256, binding.workspace_size(B, T, H, K, V, N, inp.chunk, code)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        rc = binding.fwd_into(q, k, v, g, o, inp.scale, h0, ht, cu, N, B, T, H, K, V, inp.chunk, code, ws,
+                              stream)
+        if rc != 0:
+            raise binding.GlaError(rc)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if binding.get_status(ws) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    timer = binding.KernelTimer()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms, per_kernel = [], {}
+    launches = 0
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        for _ in range(args.steps):
+            flush.zero_()
+            with timer:
+                start.record(stream)
+                step()
+                end.record(stream)
+            torch.cuda.synchronize()
+            step_ms.append(start.elapsed_time(end))
+            res = timer.results()
+            launches += len(res)
+            for name, ms in res:
+                per_kernel.setdefault(name, []).append(ms)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = binding.get_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {binding.strerror(status)} in the timed region")
+
+    value = wu["tokens"] * args.steps * world / (total_ms / 1e3)
+    ms_per_step = total_ms / args.steps
+
+    # dominant kernel and its roofline
+    peaks, peak_src = load_peaks()
+    kern_tot = {n: sum(v) for n, v in per_kernel.items()}
+    dom = max(kern_tot, key=kern_tot.get)
+    dom_ms = statistics.mean(per_kernel[dom])
+    dom_bytes = kernel_algorithmic_bytes(dom, wu)
+    hbm = peak_hbm(peaks)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                "traffic": traffic_for(dom, args.workload),
+                "algorithmic_bytes_per_launch": dom_bytes,
+                "tensor_tflops_algorithmic": round(wu["flops"] / (ms_per_step / 1e3) / 1e12, 2)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, inp, binding, dev, stream, flush)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, threads, desc = oracle_sample(inp, args.cpu_seconds)
+        cpu = {"value": round(val, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "desc": w.note, "B": B, "T": T, "H": H, "K": K, "V": V,
+                       "N": N, "chunk": inp.chunk, "input_dtype": inp.dtype, "h0": inp.h0 is not None,
+                       "tokens_per_step": wu["tokens"], "algorithmic_bytes_per_step": wu["bytes"],
+                       "l2": "flushed before every timed step (zero-fill of a 2x L2 buffer, outside the events)",
+                       "parallelism": "replicas" if world == 1 else f"weak x{world} (independent sequences)"},
+            "roofline": roofline,
+            "kernels_ms": {n: round(statistics.mean(v), 5) for n, v in per_kernel.items()},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def kernel_algorithmic_bytes(name, wu):
+    if name == "out_ffma":
+        return wu["bytes"]
+    if name == "state_ffma":
+        return wu["in_bytes"]   # upper bound: k, g, v of the non-final segments are a subset
+    return wu["state_bytes"]
+
+
+def measure_e2e(args, inp, binding, dev, stream, flush):
+    """Same metric through the public call with host inputs: pinned H2D copies, gla_fwd, D2H of o and ht,
+    all inside the timed events."""
+    import torch
+    host = [x.pin_memory() for x in (inp.q, inp.k, inp.v, inp.g)]
+    host_h0 = None if inp.h0 is None else inp.h0.pin_memory()
+    host_cu = None if inp.cu_seqlens is None else inp.cu_seqlens.pin_memory()
+    dq, dk, dv, dg = (torch.empty_like(x, device=dev) for x in host)
+    dh0 = None if host_h0 is None else torch.empty_like(host_h0, device=dev)
+    dcu = None if host_cu is None else torch.empty_like(host_cu, device=dev)
+    B, T, H, K, V, N = inp.q.shape[0], inp.q.shape[1], inp.H, inp.K, inp.V, inp.N
+    o = torch.empty(B, T, H, V, dtype=torch.float32, device=dev)
+    ht = torch.empty(N, H, K, V, dtype=torch.float32, device=dev)
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hht = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
+    code = binding.GLA_F32 if inp.dtype == "f32" else binding.GLA_BF16
+    ws = torch.zeros(max(256, binding.workspace_size(B, T, H, K, V, N, inp.chunk, code)), dtype=torch.uint8,
+                     device=dev)
+    h2d = sum(x.numel() * x.element_size() for x in host) + \
+        sum(x.numel() * x.element_size() for x in (host_h0, host_cu) if x is not None)
+    d2h = ho.numel() * ho.element_size() + hht.numel() * hht.element_size()
+
+    def e2e_step():
+        for d, h_ in zip((dq, dk, dv, dg, dh0, dcu), (*host, host_h0, host_cu)):
+            if h_ is not None:
+                d.copy_(h_, non_blocking=True)
+        rc = binding.fwd_into(dq, dk, dv, dg, o, inp.scale, dh0, ht, dcu, N, B, T, H, K, V, inp.chunk, code,
+                              ws, stream)
+        if rc != 0:
+            raise binding.GlaError(rc)
+        ho.copy_(o, non_blocking=True)
+        hht.copy_(ht, non_blocking=True)
+
+    for _ in range(max(args.warmup, 1)):
+        e2e_step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tot = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        s.record(stream)
+        e2e_step()
+        e.record(stream)
+        torch.cuda.synchronize()
+        tot += s.elapsed_time(e)
+    tokens = B * T
+    return {"value": round(tokens * args.steps / (tot / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(tot / args.steps, 4)}
+
+
+def run_reference(args, w, world, rank):
+    """The fp64 CPU oracle as the reference arm: each step times a bounded sample of the workload."""
+    if rank != 0:
+        return
+    from chunkwise_gated_linear_chunked_gb300.inputs import workload_inputs
+    inp = workload_inputs(args.workload)
+    per_step = max(1.0, min(args.cpu_seconds, 150.0 / max(args.steps + args.warmup, 1)))
+    for i in range(args.warmup):
+        oracle_sample(inp, 0.0, head_start=i)
+    vals, threads, desc = [], 1, ""
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        val, threads, desc = oracle_sample(inp, per_step, head_start=i)
+        vals.append(val)
+    el = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    wu = work_units(inp)
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "desc": w.note, "tokens_per_step": wu["tokens"],
+                       "sample": "each step: heads of the workload, all sequences, ~%.1f s of oracle time"
+                                 % per_step},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

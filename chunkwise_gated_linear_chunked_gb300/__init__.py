@@ -1,18 +1,6 @@
 """GB300-native chunkwise gated linear attention (GLA) forward.
 
-The compute path lives in ``csrc/`` (sm_103a CUDA kernels behind a C ABI, ``libgla.so``); ``binding`` is a
-thin ctypes layer over that ABI; ``inputs`` draws the seeded synthetic workloads.  The binding is imported
-lazily so that ``inputs`` can be used without the compiled library.
+The compute path lives in ``csrc/`` (sm_103a CUDA kernels behind a C ABI, ``libgla.so``, declared in
+``include/gla.h``); ``binding`` is a thin ctypes layer over that ABI (import it explicitly; it requires the
+built library); ``inputs`` draws the seeded synthetic workloads; ``build`` compiles the library in-tree.
 """
-
-__all__ = ["binding", "inputs"]
-
-
-def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
-    if name == "inputs":
-        from . import inputs
-        return inputs
-    raise AttributeError(name)

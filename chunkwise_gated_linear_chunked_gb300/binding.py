@@ -1,0 +1,175 @@
+"""Thin ctypes binding of libgla (``include/gla.h``): argument marshalling only.
+
+Every step of the forward runs in libgla's CUDA kernels; torch supplies device memory and streams.  There is
+no CPU fallback: if ``_build/libgla.so`` is missing the import fails loudly (run
+``chunkwise_gated_linear_chunked_gb300.build.build()`` or ``__graft_entry__.build()`` first).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB
+
+GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_ALIGNMENT, GLA_ERR_WORKSPACE, GLA_ERR_CUDA, \
+    GLA_ERR_TIMEOUT = range(7)
+GLA_F32, GLA_BF16, GLA_BF16_OBF16 = 0, 1, 2
+
+EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",
+           "gla_profile_events", "gla_profile_launches", "gla_kernel_name")
+
+if not os.path.exists(LIB):
+    raise ImportError(f"libgla.so not built ({LIB}); call chunkwise_gated_linear_chunked_gb300.build.build()")
+
+_lib = ctypes.CDLL(LIB)
+_p, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_lib.gla_fwd.argtypes = [_p, _p, _p, _p, _p, _f, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _sz, _p]
+_lib.gla_fwd.restype = _i
+_lib.gla_fwd_workspace_size.argtypes = [_i] * 8
+_lib.gla_fwd_workspace_size.restype = _sz
+_lib.gla_get_status.argtypes = [_p, _p]
+_lib.gla_get_status.restype = _i
+_lib.gla_strerror.argtypes = [_i]
+_lib.gla_strerror.restype = ctypes.c_char_p
+_lib.gla_chunk_local_cumsum.argtypes = [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p]
+_lib.gla_chunk_local_cumsum.restype = _i
+_lib.gla_profile_events.argtypes = [_p, _i, _p]
+_lib.gla_profile_events.restype = _i
+_lib.gla_profile_launches.argtypes = []
+_lib.gla_profile_launches.restype = _i
+_lib.gla_kernel_name.argtypes = [_i]
+_lib.gla_kernel_name.restype = ctypes.c_char_p
+
+
+class GlaError(RuntimeError):
+    def __init__(self, code: int, what: str = "gla_fwd"):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} (code {code})")
+
+
+def lib():
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return _lib.gla_strerror(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+DTYPE_CODE = {(torch.float32, torch.float32): GLA_F32, (torch.bfloat16, torch.float32): GLA_BF16,
+              (torch.bfloat16, torch.bfloat16): GLA_BF16_OBF16}
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def workspace_size(B, T, H, K, V, N, chunk=64, dtype=GLA_BF16) -> int:
+    return int(_lib.gla_fwd_workspace_size(B, T, H, K, V, N, chunk, dtype))
+
+
+def get_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-initialised, cached device workspace of at least ``nbytes`` (one per device and stream use)."""
+    device = torch.device(device)
+    key = (device.index if device.index is not None else torch.cuda.current_device())
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+        return ws
+
+
+def fwd_into(q, k, v, g, o, scale, h0, ht, cu_seqlens, N, B, T, H, K, V, chunk, dtype, workspace,
+             stream=None) -> int:
+    """Raw call: tensors (or None) are passed as device pointers, sizes as given.  Returns the code."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return int(_lib.gla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(o), float(scale), _ptr(h0), _ptr(ht),
+                            _ptr(cu_seqlens), int(N), int(B), int(T), int(H), int(K), int(V), int(chunk),
+                            int(dtype), _ptr(workspace), nbytes, _stream_handle(stream)))
+
+
+def gla_fwd(q, k, v, g, scale=None, initial_state=None, output_final_state=True, cu_seqlens=None,
+            chunk=64, out_dtype=None, stream=None, workspace=None):
+    """GLA forward on the GPU.
+
+    q, k, g: [B, T, H, K]; v: [B, T, H, V] (cuda, contiguous, all fp32 or all bf16).
+    initial_state: optional fp32 [N, H, K, V].  cu_seqlens: optional int32 [N+1] cuda offsets (B == 1).
+    out_dtype: fp32 (default) or, for bf16 inputs, bf16.  Returns (o, final_state or None).
+    """
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    out_dtype = out_dtype or torch.float32
+    code = DTYPE_CODE.get((q.dtype, out_dtype))
+    if code is None:
+        raise GlaError(GLA_ERR_UNSUPPORTED, f"gla_fwd dtype {q.dtype} -> {out_dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
+        if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise GlaError(GLA_ERR_INVALID_ARG, f"gla_fwd: {name} must be a contiguous cuda {q.dtype} tensor")
+    o = torch.empty(B, T, H, V, dtype=out_dtype, device=q.device)
+    ht = torch.empty(N, H, K, V, dtype=torch.float32, device=q.device) if output_final_state else None
+    h0 = initial_state
+    if h0 is not None and (h0.dtype != torch.float32 or not h0.is_contiguous()):
+        raise GlaError(GLA_ERR_INVALID_ARG, "gla_fwd: initial_state must be a contiguous fp32 tensor")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise GlaError(GLA_ERR_INVALID_ARG, "gla_fwd: cu_seqlens must be int32")
+    if workspace is None:
+        workspace = get_workspace(workspace_size(B, T, H, K, V, N, chunk, code), q.device)
+    rc = fwd_into(q, k, v, g, o, scale, h0, ht, cu_seqlens, N, B, T, H, K, V, chunk, code, workspace,
+                  stream)
+    if rc != GLA_OK:
+        raise GlaError(rc)
+    return o, ht
+
+
+def get_status(workspace, stream=None) -> int:
+    return int(_lib.gla_get_status(_ptr(workspace), _stream_handle(stream)))
+
+
+def chunk_local_cumsum(g, chunk=64, cu_seqlens=None, stream=None):
+    B, T, H, K = g.shape
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    code = GLA_F32 if g.dtype == torch.float32 else GLA_BF16
+    G = torch.empty(B, T, H, K, dtype=torch.float32, device=g.device)
+    rc = int(_lib.gla_chunk_local_cumsum(_ptr(g), _ptr(G), _ptr(cu_seqlens), N, B, T, H, K, chunk, code,
+                                         _stream_handle(stream)))
+    if rc != GLA_OK:
+        raise GlaError(rc, "gla_chunk_local_cumsum")
+    return G
+
+
+class KernelTimer:
+    """Arms gla_profile_events with CUDA events so each kernel launch of the next gla_fwd calls on this
+    thread is bracketed by events on its stream.  ``results()`` (after a synchronize) gives
+    [(kernel name, milliseconds)] for the last call."""
+
+    def __init__(self, max_launches=16):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_launches)]
+        self._handles = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        self._ids = (ctypes.c_int * max_launches)()
+
+    def __enter__(self):
+        _lib.gla_profile_events(self._handles, len(self.events), self._ids)
+        return self
+
+    def __exit__(self, *exc):
+        _lib.gla_profile_events(None, 0, None)
+
+    def results(self):
+        n = int(_lib.gla_profile_launches())
+        return [(_lib.gla_kernel_name(self._ids[i]).decode(), self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
+                for i in range(min(n, len(self.events) // 2))]

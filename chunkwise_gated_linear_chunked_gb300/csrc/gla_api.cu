@@ -1,0 +1,337 @@
+// libgla C ABI: argument validation, the segment planner, the workspace layout and the launch sequence
+// of the chunkwise GLA forward.  Declarations and contracts: include/gla.h.
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "gla_internal.h"
+
+namespace gla {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int sm_count()
+{
+    static std::mutex mu;
+    static int cache[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
+        return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool supported_k(int K) { return K == 64 || K == 128; }
+bool supported_v(int V) { return V == 64 || V == 128 || V == 256; }
+
+int check_shape(int B, int T, int H, int K, int V, int N, int chunk, int dtype, bool varlen)
+{
+    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_BF16_OBF16)
+        return GLA_ERR_UNSUPPORTED;
+    if (B < 0 || T < 0 || H <= 0 || N < 0 || K <= 0 || V <= 0)
+        return GLA_ERR_INVALID_ARG;
+    if (varlen ? B != 1 : N != B)
+        return GLA_ERR_INVALID_ARG;
+    if (chunk != kChunk || !supported_k(K) || !supported_v(V))
+        return GLA_ERR_UNSUPPORTED;
+    const long long rows = varlen ? (long long)T : (long long)B * T;
+    if (rows * H * (K > V ? K : V) >= (1LL << 31) || (long long)N * H * K * V >= (1LL << 31))
+        return GLA_ERR_UNSUPPORTED;
+    return GLA_OK;
+}
+
+// Segment plan.  One segment per sequence when sequences x heads x value tiles already give about two
+// CTAs per SM; otherwise segments of L rows (a multiple of the chunk, at least 4 chunks) sized so the
+// output pass has about that many CTAs.
+void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, int dtype, bool varlen)
+{
+    std::memset(&pl, 0, sizeof pl);
+    pl.B = B; pl.T = T; pl.H = H; pl.K = K; pl.V = V; pl.N = N; pl.chunk = chunk; pl.dtype = dtype;
+    pl.varlen = varlen;
+    pl.BV = 64;
+    pl.NV = V / pl.BV;
+    const long long rows = varlen ? (long long)T : (long long)B * T;
+    const int nseq = varlen ? N : B;
+    const long long target = 2LL * sm_count();
+    const long long base = (long long)nseq * H * pl.NV;
+    const int C = chunk;
+    long long whole = varlen ? (long long)T : (long long)T;   // longest possible sequence
+    whole = (whole + C - 1) / C * C;
+    if (whole < C)
+        whole = C;
+    long long L = whole;
+    if (base < target && rows > 0) {
+        long long per = (rows * H * pl.NV + target - 1) / target;   // rows per CTA
+        per = (per + C - 1) / C;
+        if (per < 4)
+            per = 4;
+        L = per * C;
+        if (L > whole)
+            L = whole;
+    }
+    pl.L = (int)L;
+    if (varlen) {
+        pl.P = 0;
+        pl.J = N + (int)((T + L - 1) / L);
+        pl.multi = L < T;
+    } else {
+        pl.P = T > 0 ? (int)((T + L - 1) / L) : 1;
+        pl.J = B * pl.P;
+        pl.multi = pl.P > 1;
+    }
+    size_t off = 0;
+    pl.off_status = off;
+    off += kAlign;
+    pl.off_table = off;
+    if (varlen)
+        off += align_up(sizeof(int4) * (size_t)pl.J);
+    pl.off_seq = off;
+    if (varlen)
+        off += align_up(sizeof(int2) * (size_t)N);
+    pl.off_ss = off;
+    if (pl.multi)
+        off += align_up(sizeof(float) * (size_t)pl.J * H * K * V);
+    pl.off_gtot = off;
+    if (pl.multi)
+        off += align_up(sizeof(float) * (size_t)pl.J * H * K);
+    pl.total = off;
+}
+
+// Per-thread measurement hook state (gla_profile_events).
+struct Profile {
+    cudaEvent_t *events = nullptr;
+    int n_events = 0;
+    int *ids = nullptr;
+    int launches = 0;
+};
+thread_local Profile g_prof;
+
+enum KernelId { K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4 };
+
+// Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
+template <typename Fn>
+cudaError_t profiled(int id, cudaStream_t s, Fn fn)
+{
+    Profile &p = g_prof;
+    const int i = p.launches++;
+    const bool rec = p.events && 2 * i + 1 < p.n_events;
+    if (rec && cudaEventRecord(p.events[2 * i], s) != cudaSuccess)
+        return cudaErrorUnknown;
+    cudaError_t e = fn();
+    if (e != cudaSuccess)
+        return e;
+    if (rec) {
+        if (p.ids)
+            p.ids[i] = id;
+        return cudaEventRecord(p.events[2 * i + 1], s);
+    }
+    return cudaSuccess;
+}
+
+bool misaligned(const void *p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u); }
+
+struct Range {
+    uintptr_t lo, hi;
+};
+Range range_of(const void *p, size_t bytes)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, a + bytes};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+}  // namespace
+}  // namespace gla
+
+using namespace gla;
+
+extern "C" size_t gla_fwd_workspace_size(int B, int T, int H, int K, int V, int N, int chunk, int dtype)
+{
+    // The workspace size does not depend on whether cu_seqlens is given except through N; size for the
+    // larger of the two layouts so one query serves both.
+    const bool varlen_ok = check_shape(B, T, H, K, V, N, chunk, dtype, B == 1) == GLA_OK;
+    const bool dense_ok = check_shape(B, T, H, K, V, N, chunk, dtype, false) == GLA_OK;
+    size_t best = 0;
+    Plan pl;
+    if (varlen_ok && B == 1) {
+        make_plan(pl, B, T, H, K, V, N, chunk, dtype, true);
+        best = pl.total;
+    }
+    if (dense_ok) {
+        make_plan(pl, B, T, H, K, V, N, chunk, dtype, false);
+        if (pl.total > best)
+            best = pl.total;
+    }
+    return best;
+}
+
+extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *g, void *o, float scale,
+                       const float *h0, float *ht, const int32_t *cu_seqlens, int N, int B, int T, int H,
+                       int K, int V, int chunk, int dtype, void *workspace, size_t workspace_bytes,
+                       void *stream)
+{
+    const bool varlen = cu_seqlens != nullptr;
+    int rc = check_shape(B, T, H, K, V, N, chunk, dtype, varlen);
+    if (rc != GLA_OK)
+        return rc;
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return GLA_ERR_INVALID_ARG;
+    const size_t rows = varlen ? (size_t)T : (size_t)B * T;
+    const size_t esz = dtype == GLA_F32 ? 4 : 2, osz = dtype == GLA_BF16_OBF16 ? 2 : 4;
+    if (rows > 0 && (!q || !k || !v || !g || !o))
+        return GLA_ERR_INVALID_ARG;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(g) || misaligned(o) ||
+        misaligned(h0) || misaligned(ht) || misaligned(cu_seqlens))
+        return GLA_ERR_ALIGNMENT;
+    Plan pl;
+    make_plan(pl, B, T, H, K, V, N, chunk, dtype, varlen);
+    if (!workspace)
+        return GLA_ERR_WORKSPACE;
+    if (workspace_bytes < pl.total)
+        return GLA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
+        return GLA_ERR_ALIGNMENT;
+    // aliasing: outputs overlap no input and no other output (h0 == ht exactly is allowed)
+    const Range rq = range_of(q, rows * H * K * esz), rk = range_of(k, rows * H * K * esz);
+    const Range rg = range_of(g, rows * H * K * esz), rv = range_of(v, rows * H * V * esz);
+    const Range ro = range_of(o, rows * H * V * osz);
+    const size_t sbytes = (size_t)N * H * K * V * 4;
+    const Range rh0 = range_of(h0, h0 ? sbytes : 0), rht = range_of(ht, ht ? sbytes : 0);
+    const Range rws = range_of(workspace, pl.total);
+    const Range rcu = range_of(cu_seqlens, varlen ? sizeof(int32_t) * (size_t)(N + 1) : 0);
+    for (Range in : {rq, rk, rg, rv, rh0, rcu, rws})
+        if (overlap(ro, in))
+            return GLA_ERR_INVALID_ARG;
+    for (Range in : {rq, rk, rg, rv, rcu, rws, ro})
+        if (overlap(rht, in))
+            return GLA_ERR_INVALID_ARG;
+    if (h0 && ht && h0 != ht && overlap(rh0, rht))
+        return GLA_ERR_INVALID_ARG;
+    for (Range in : {rq, rk, rg, rv, rh0, rcu})
+        if (overlap(rws, in))
+            return GLA_ERR_INVALID_ARG;
+    if (pl.J == 0) {
+        g_prof.launches = 0;
+        return GLA_OK;
+    }
+
+    char *ws = static_cast<char *>(workspace);
+    Args a;
+    std::memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.g = g; a.o = o; a.h0 = h0; a.ht = ht; a.cu = cu_seqlens;
+    a.scale = scale;
+    a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.N = N; a.L = pl.L; a.P = pl.P; a.J = pl.J;
+    a.status = reinterpret_cast<int *>(ws + pl.off_status);
+    if (varlen) {
+        a.table = reinterpret_cast<const int4 *>(ws + pl.off_table);
+        a.seqinfo = reinterpret_cast<const int2 *>(ws + pl.off_seq);
+    }
+    if (pl.multi) {
+        a.ss = reinterpret_cast<float *>(ws + pl.off_ss);
+        a.gtot = reinterpret_cast<float *>(ws + pl.off_gtot);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    g_prof.launches = 0;
+    if (varlen && profiled(K_PLAN, s, [&] { return launch_plan_varlen(pl, a, s); }) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    if (pl.multi) {
+        if (profiled(K_STATE_FFMA, s, [&] { return launch_state_ffma(pl, a, s); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+        if (profiled(K_SCAN, s, [&] { return launch_scan(pl, a, s); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+    }
+    if (profiled(K_OUT_FFMA, s, [&] { return launch_out_ffma(pl, a, s); }) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    return GLA_OK;
+}
+
+extern "C" int gla_get_status(void *workspace, void *stream)
+{
+    if (!workspace)
+        return GLA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return GLA_ERR_CUDA;
+    }
+    return word;
+}
+
+extern "C" const char *gla_strerror(int code)
+{
+    switch (code) {
+    case GLA_OK: return "ok";
+    case GLA_ERR_INVALID_ARG: return "invalid argument";
+    case GLA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case GLA_ERR_ALIGNMENT: return "device pointer not 16-byte aligned (workspace: 256-byte)";
+    case GLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case GLA_ERR_CUDA: return "CUDA runtime or launch failure";
+    case GLA_ERR_TIMEOUT: return "a bounded device wait ran out";
+    default: return "unknown status code";
+    }
+}
+
+extern "C" int gla_chunk_local_cumsum(const void *g, float *G, const int32_t *cu_seqlens, int N, int B,
+                                      int T, int H, int K, int chunk, int dtype, void *stream)
+{
+    const bool varlen = cu_seqlens != nullptr;
+    if (dtype != GLA_F32 && dtype != GLA_BF16)
+        return GLA_ERR_UNSUPPORTED;
+    if (B < 0 || T < 0 || H <= 0 || K <= 0 || N < 0 || (varlen ? B != 1 : false))
+        return GLA_ERR_INVALID_ARG;
+    if (chunk != 16 && chunk != 32 && chunk != 64 && chunk != 128)
+        return GLA_ERR_UNSUPPORTED;
+    const size_t rows = varlen ? (size_t)T : (size_t)B * T;
+    if (rows > 0 && (!g || !G))
+        return GLA_ERR_INVALID_ARG;
+    if (rows * H * K >= (1ull << 31))
+        return GLA_ERR_UNSUPPORTED;
+    if (misaligned(g) || misaligned(G) || misaligned(cu_seqlens))
+        return GLA_ERR_ALIGNMENT;
+    const size_t esz = dtype == GLA_F32 ? 4 : 2;
+    if (overlap(range_of(g, rows * H * K * esz), range_of(G, rows * H * K * 4)))
+        return GLA_ERR_INVALID_ARG;
+    if (launch_chunk_cumsum(g, G, cu_seqlens, N, B, T, H, K, chunk, dtype,
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    return GLA_OK;
+}
+
+extern "C" int gla_profile_events(void **events, int n_events, int *kernel_ids)
+{
+    if (n_events < 0)
+        return GLA_ERR_INVALID_ARG;
+    g_prof.events = events ? reinterpret_cast<cudaEvent_t *>(events) : nullptr;
+    g_prof.n_events = events ? n_events : 0;
+    g_prof.ids = events ? kernel_ids : nullptr;
+    return GLA_OK;
+}
+
+extern "C" int gla_profile_launches(void) { return g_prof.launches; }
+
+extern "C" const char *gla_kernel_name(int kernel_id)
+{
+    switch (kernel_id) {
+    case K_PLAN: return "plan_varlen";
+    case K_STATE_FFMA: return "state_ffma";
+    case K_SCAN: return "scan_segments";
+    case K_OUT_FFMA: return "out_ffma";
+    default: return "unknown";
+    }
+}

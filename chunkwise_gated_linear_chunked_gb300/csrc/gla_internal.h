@@ -1,0 +1,83 @@
+// Internal declarations shared by the translation units of libgla (host planner + kernels).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/gla.h"
+
+namespace gla {
+
+constexpr int kChunk = 64;   // chunk length C (rows per intra-chunk tile)
+
+// One forward call's launch plan.  Segments of L rows (L a multiple of the chunk) split each sequence
+// so that long sequences with few heads still fill the GPU; a "slot" is one (sequence, segment) pair and
+// carries all H heads.  Slots of one sequence are contiguous.
+struct Plan {
+    int B, T, H, K, V, N, chunk, dtype;
+    bool varlen;
+    int L;        // segment length in rows (multiple of chunk)
+    int P;        // dense: segments per sequence (>= 1); varlen: 0 (per sequence, from the plan kernel)
+    int J;        // slots: exact (dense) or an upper bound (varlen)
+    bool multi;   // some sequence may span more than one segment: state + scan passes are needed
+    int BV, NV;   // value-tile width and count for the CUDA-core kernels
+    // workspace layout (byte offsets)
+    size_t off_status, off_table, off_seq, off_ss, off_gtot, total;
+};
+
+// Kernel arguments (passed by value).
+struct Args {
+    const void *q, *k, *v, *g;
+    void *o;
+    const float *h0;
+    float *ht;
+    const int32_t *cu;     // device offsets or nullptr
+    float scale;
+    int B, T, H, K, V, N, L, P, J;
+    const int4 *table;     // varlen: per slot {n, p, bos, eos}; n < 0 marks an unused slot
+    const int2 *seqinfo;   // varlen: per sequence {first slot, slot count}
+    float *ss;             // [J][H][K][V]: segment contributions, then segment start states
+    float *gtot;           // [J][H][K]: total log-decay of each segment
+    int *status;           // sticky device status word
+};
+
+// Map slot j to (sequence n, segment p, rows [bos, eos), sequence end).  False for an unused slot.
+__device__ __forceinline__ bool resolve_slot(const Args &a, int j, int &n, int &p, int &bos, int &eos,
+                                             int &send)
+{
+    if (a.table) {
+        const int4 e = a.table[j];
+        if (e.x < 0)
+            return false;
+        n = e.x;
+        p = e.y;
+        bos = e.z;
+        eos = e.w;
+        send = a.cu[n + 1];
+        return true;
+    }
+    n = j / a.P;
+    p = j - n * a.P;
+    const int sb = n * a.T;
+    bos = sb + p * a.L;
+    send = sb + a.T;
+    eos = min(bos + a.L, send);
+    return true;
+}
+
+__device__ __forceinline__ void report(int *status, int code)
+{
+    if (status)
+        atomicCAS(status, 0, code);
+}
+
+// Launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_plan_varlen(const Plan &pl, const Args &a, cudaStream_t s);
+cudaError_t launch_state_ffma(const Plan &pl, const Args &a, cudaStream_t s);
+cudaError_t launch_scan(const Plan &pl, const Args &a, cudaStream_t s);
+cudaError_t launch_out_ffma(const Plan &pl, const Args &a, cudaStream_t s);
+cudaError_t launch_chunk_cumsum(const void *g, float *G, const int32_t *cu, int N, int B, int T, int H,
+                                int K, int chunk, int dtype, cudaStream_t s);
+
+}  // namespace gla

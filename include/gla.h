@@ -1,0 +1,135 @@
+/*
+ * gla.h — C ABI of libgla: the chunkwise-parallel forward pass of gated linear attention (GLA) on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method (page "fla/ops/gla/fused_chunk.py": fused_chunk_gla_fwd_kernel, fwd_inner_chunk,
+ * prepare_qg_kg, FusedChunkGLAFunction.forward) is the recurrence, per sequence n and head h,
+ *
+ *     S_0 = h0[n,h] (or 0),   S_t = diag(exp(g_t)) S_{t-1} + k_t^T v_t,   o_t = scale * q_t S_t,
+ *     ht[n,h] = S_{last}
+ *
+ * with a per-key-dimension log-decay g_t <= 0 and a K x V state.  The library computes it chunkwise: a
+ * chunk-local cumsum of g, per-segment state contributions, a decayed scan over segments, and a fused
+ * output kernel that adds the inter-chunk term q~ S to the causally masked intra-chunk term.
+ *
+ * Conventions shared by every entry point
+ *   - Layout: time-major with interleaved heads, contiguous, no strides (page
+ *     "fla/ops/ttt/fused_chunk.py", fused_chunk_ttt_linear: [B, T, H, K] inputs).
+ *       q, k, g : [B, T, H, K]        v, o : [B, T, H, V]        h0, ht : [N, H, K, V] fp32, row-major
+ *     (K rows, V columns: the state layout of fused_chunk_gla_fwd_kernel's h0/ht blocks).
+ *   - Varlen packing: cu_seqlens != NULL is a DEVICE array of N+1 int32 offsets (page
+ *     "fla/ops/ttt/fused_chunk.py", fused_chunk_ttt_linear_fwd_kernel: bos/eos from cu_seqlens); then
+ *     B must be 1, T is the packed total and cu_seqlens must run non-decreasing from 0 to T.  Because the
+ *     offsets live on the device they are checked there; a violation is reported through
+ *     gla_get_status() as GLA_ERR_INVALID_ARG and no output is written.  Zero-length sequences are
+ *     allowed (their ht is h0, or 0).  Without cu_seqlens, N must equal B.
+ *   - Pointers: every device pointer must be 16-byte aligned (GLA_ERR_ALIGNMENT otherwise).  The
+ *     caller owns every buffer, including o, ht and the workspace; the library allocates nothing.
+ *     No input may alias an output, except h0 == ht (in-place state streaming), which is allowed.
+ *   - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call is
+ *     stream-ordered and returns once its kernels are enqueued; nothing synchronises the host.
+ *   - Errors: synchronous validation returns a gla_status code and enqueues nothing.  Device-side
+ *     conditions (bad cu_seqlens, a bounded wait that ran out) are recorded in the workspace's status
+ *     word, read with gla_get_status().
+ */
+#ifndef GLA_H
+#define GLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gla_status {
+    GLA_OK = 0,
+    GLA_ERR_INVALID_ARG = 1,   /* NULL/negative/inconsistent argument, bad cu_seqlens, bad scale   */
+    GLA_ERR_UNSUPPORTED = 2,   /* shape or dtype outside the supported set                          */
+    GLA_ERR_ALIGNMENT = 3,     /* a device pointer is not 16-byte aligned                           */
+    GLA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than gla_fwd_workspace_size()           */
+    GLA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed                       */
+    GLA_ERR_TIMEOUT = 6        /* (device) a bounded wait inside a kernel ran out; outputs invalid  */
+} gla_status;
+
+typedef enum gla_dtype {
+    GLA_F32 = 0,        /* q, k, v, g fp32; o fp32                                                  */
+    GLA_BF16 = 1,       /* q, k, v, g bf16; o fp32 (default for bf16 inputs, see below)             */
+    GLA_BF16_OBF16 = 2  /* q, k, v, g bf16; o bf16 (the pages' o.to(v) convention)                  */
+} gla_dtype;
+/* o is fp32 for bf16 inputs by default: at the benchmark magnitudes (|o| up to ~20) a bf16-rounded o
+ * alone carries up to 0.06 of rounding error, above the 2e-2 max-abs parity bound.  State h0/ht is fp32
+ * for every dtype (fused_chunk_gla_fwd_kernel keeps the state in fp32 and stores ht as fp32). */
+
+/*
+ * gla_fwd — GLA forward over a batch (or a varlen pack) of sequences.
+ *
+ *   q, k, g     [B,T,H,K] input dtype (device).  g is the per-step log-decay (expected <= 0).
+ *   v           [B,T,H,V] input dtype (device).
+ *   o           [B,T,H,V] output (device), fp32 for GLA_F32 / GLA_BF16, bf16 for GLA_BF16_OBF16.
+ *   scale       multiplies q only (prepare_qg_kg); must be finite and > 0.  ht carries no scale.
+ *   h0          [N,H,K,V] fp32 initial state (device) or NULL for zeros.  It is decayed by the first
+ *               token's gate like any carried state (fused_chunk_gla_fwd_kernel).
+ *   ht          [N,H,K,V] fp32 final state (device) or NULL to skip it.  May equal h0.
+ *   cu_seqlens  int32 [N+1] device offsets or NULL (dense: N == B sequences of T rows).
+ *   chunk       chunk length; 64 is supported.  The result does not depend on it in exact arithmetic.
+ *   K           64 or 128.          V  64, 128 or 256.          B, T, H, N >= 0 (T*H*max(K,V) < 2^31).
+ *   workspace   device scratch of at least gla_fwd_workspace_size() bytes, 256-byte aligned, ZEROED
+ *               BEFORE ITS FIRST USE (it carries the sticky status word between calls).  One workspace
+ *               must not be used by two calls that may run concurrently.
+ *
+ * Valid domain of the fast intra-chunk factorisation: for every chunk and key dimension the gate sum
+ * over half a chunk (32 steps) must stay above about -80; outside it results may overflow to inf/NaN.
+ * Returns GLA_OK once enqueued, else a synchronous gla_status.
+ */
+int gla_fwd(const void *q, const void *k, const void *v, const void *g, void *o, float scale,
+            const float *h0, float *ht, const int32_t *cu_seqlens, int N, int B, int T, int H,
+            int K, int V, int chunk, int dtype, void *workspace, size_t workspace_bytes,
+            void *stream);
+
+/*
+ * Bytes of device workspace gla_fwd needs for this problem on the CURRENT device (the segment plan
+ * depends on its SM count).  Returns 0 for arguments gla_fwd would reject.  Never fails otherwise.
+ */
+size_t gla_fwd_workspace_size(int B, int T, int H, int K, int V, int N, int chunk, int dtype);
+
+/*
+ * Synchronises `stream`, then returns and clears the sticky device status word of `workspace`
+ * (GLA_OK if no enqueued call since the last read reported a device-side error).  Returns
+ * GLA_ERR_CUDA if the synchronisation itself failed, GLA_ERR_INVALID_ARG for a NULL workspace.
+ */
+int gla_get_status(void *workspace, void *stream);
+
+/* Static description of a gla_status code (never NULL). */
+const char *gla_strerror(int code);
+
+/*
+ * gla_chunk_local_cumsum — the chunk-local inclusive cumsum of the log-decay as a standalone pass
+ * (FusedChunkGLAFunction.forward computes it in fp32 before everything else):
+ *     G[t] = sum of g[u] for u from the first row of t's chunk to t,
+ * chunks of `chunk` rows starting at every sequence start (cu_seqlens, or every T rows when NULL).
+ * g [B,T,H,K] in the input dtype (GLA_F32 or GLA_BF16), G [B,T,H,K] fp32, both device.  gla_fwd does
+ * not call this: its kernels form the same sums on chip.  Device-side cu_seqlens errors are not
+ * checked here (pass valid offsets).  chunk in {16, 32, 64, 128}.
+ */
+int gla_chunk_local_cumsum(const void *g, float *G, const int32_t *cu_seqlens, int N, int B, int T,
+                           int H, int K, int chunk, int dtype, void *stream);
+
+/*
+ * Measurement hook (no counterpart on the pages; it exists so a benchmark can time each kernel of the
+ * path with CUDA events on the stream the kernels run on).  While `events` is non-NULL, every later
+ * gla_fwd call made from this host thread records events[2i] right before and events[2i+1] right after
+ * its i-th kernel launch (for i < n_events / 2), on the call's stream, and stores that launch's kernel id
+ * in kernel_ids[i] (host array of n_events / 2 ints, may be NULL).  `events` are cudaEvent_t handles
+ * created by the caller.  Pass events == NULL to stop.  Returns GLA_OK, or GLA_ERR_INVALID_ARG for
+ * n_events < 0.  gla_profile_launches() returns how many kernels the last gla_fwd call on this thread
+ * launched, and gla_kernel_name() names a kernel id.
+ */
+int gla_profile_events(void **events, int n_events, int *kernel_ids);
+int gla_profile_launches(void);
+const char *gla_kernel_name(int kernel_id);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GLA_H */

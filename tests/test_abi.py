@@ -1,0 +1,122 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function include/gla.h declares, and
+rejects bad arguments synchronously (before any CUDA work).  Pointers here are fake addresses that the
+library only inspects (alignment, overlap) and never dereferences."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gla():
+    from chunkwise_gated_linear_chunked_gb300 import build
+    build.build()
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(gla_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(gla):
+    names = declared_functions()
+    assert {"gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror"} <= names
+    lib = gla.lib()
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    assert set(gla.EXPORTS) == names
+
+
+def test_strerror_total(gla):
+    for code in range(-1, 9):
+        assert isinstance(gla.strerror(code), str) and gla.strerror(code)
+
+
+A = 1 << 20   # fake, 16-byte-aligned device addresses far apart
+
+
+def call(gla, q=A, k=2 * A, v=3 * A, g=4 * A, o=8 * A, scale=0.125, h0=None, ht=None, cu=None, N=2, B=2,
+         T=100, H=2, K=64, V=64, chunk=64, dtype=1, ws=64 * A, wsb=1 << 40):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return gla.lib().gla_fwd(p(q), p(k), p(v), p(g), p(o), scale, p(h0), p(ht), p(cu), N, B, T, H, K, V,
+                             chunk, dtype, p(ws), wsb, None)
+
+
+def test_rejects_unsupported_shapes(gla):
+    assert call(gla, K=96) == gla.GLA_ERR_UNSUPPORTED
+    assert call(gla, V=32) == gla.GLA_ERR_UNSUPPORTED
+    assert call(gla, chunk=48) == gla.GLA_ERR_UNSUPPORTED
+    assert call(gla, dtype=7) == gla.GLA_ERR_UNSUPPORTED
+
+
+def test_rejects_invalid_arguments(gla):
+    assert call(gla, scale=0.0) == gla.GLA_ERR_INVALID_ARG
+    assert call(gla, scale=-1.0) == gla.GLA_ERR_INVALID_ARG
+    assert call(gla, scale=float("nan")) == gla.GLA_ERR_INVALID_ARG
+    assert call(gla, scale=float("inf")) == gla.GLA_ERR_INVALID_ARG
+    assert call(gla, N=3) == gla.GLA_ERR_INVALID_ARG                 # dense: N must equal B
+    assert call(gla, cu=40 * A, B=2) == gla.GLA_ERR_INVALID_ARG      # varlen needs B == 1
+    assert call(gla, H=0) == gla.GLA_ERR_INVALID_ARG
+    assert call(gla, T=-1) == gla.GLA_ERR_INVALID_ARG
+    assert call(gla, q=None) == gla.GLA_ERR_INVALID_ARG
+
+
+def test_rejects_misaligned_pointers(gla):
+    assert call(gla, q=A + 8) == gla.GLA_ERR_ALIGNMENT
+    assert call(gla, o=8 * A + 4) == gla.GLA_ERR_ALIGNMENT
+    assert call(gla, h0=20 * A + 2) == gla.GLA_ERR_ALIGNMENT
+    assert call(gla, ws=64 * A + 16) == gla.GLA_ERR_ALIGNMENT        # workspace wants 256 bytes
+
+
+def test_rejects_missing_or_small_workspace(gla):
+    assert call(gla, ws=None) == gla.GLA_ERR_WORKSPACE
+    need = gla.workspace_size(2, 100, 2, 64, 64, 2, 64, 1)
+    assert need >= 256
+    assert call(gla, wsb=need - 1) == gla.GLA_ERR_WORKSPACE
+
+
+def test_rejects_aliasing(gla):
+    assert call(gla, o=A + 256) == gla.GLA_ERR_INVALID_ARG            # o overlaps q
+    assert call(gla, h0=20 * A, ht=20 * A + 256) == gla.GLA_ERR_INVALID_ARG   # partial state overlap
+    assert call(gla, ht=8 * A + 1024) == gla.GLA_ERR_INVALID_ARG      # ht overlaps o
+    assert call(gla, ws=A) == gla.GLA_ERR_INVALID_ARG                 # workspace overlaps inputs
+
+
+def test_workspace_size_rejects_and_grows(gla):
+    assert gla.workspace_size(1, 100, 2, 96, 64, 1, 64, 1) == 0
+    small = gla.workspace_size(1, 4096, 1, 128, 128, 1, 64, 1)
+    assert small > 256   # one long sequence with one head is split into segments
+    assert gla.workspace_size(1, 4096, 1, 128, 128, 8, 64, 1) >= 256
+
+
+def test_cumsum_rejects(gla):
+    f = gla.lib().gla_chunk_local_cumsum
+    p = ctypes.c_void_p
+    assert f(p(A), p(2 * A), None, 1, 1, 10, 1, 64, 48, 0, None) == gla.GLA_ERR_UNSUPPORTED
+    assert f(p(A), p(2 * A), None, 1, 1, 10, 1, 64, 64, 2, None) == gla.GLA_ERR_UNSUPPORTED
+    assert f(p(A + 4), p(2 * A), None, 1, 1, 10, 1, 64, 64, 0, None) == gla.GLA_ERR_ALIGNMENT
+    assert f(p(A), p(A + 256), None, 1, 1, 10, 1, 64, 64, 0, None) == gla.GLA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """The product path has no fallback: importing the binding with no built library raises."""
+    import importlib
+    import sys
+    from chunkwise_gated_linear_chunked_gb300 import build
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
+    sys.modules.pop("chunkwise_gated_linear_chunked_gb300.binding", None)
+    try:
+        with pytest.raises(ImportError):
+            importlib.import_module("chunkwise_gated_linear_chunked_gb300.binding")
+    finally:
+        sys.modules.pop("chunkwise_gated_linear_chunked_gb300.binding", None)

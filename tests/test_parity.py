@@ -1,0 +1,154 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
+
+Small cases compare every element and span several chunks, segments and ragged tails; the full-size
+benchmark workloads run in the benchmark's launch configuration and compare every output of sampled heads
+(all sequences of those heads), which the oracle computes one (sequence, head) at a time.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from chunkwise_gated_linear_chunked_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
+from parity_util import TOL, TOL_OBF16, as_f64, assert_close, errors, run_gpu, run_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from chunkwise_gated_linear_chunked_gb300 import build
+    build.build()
+
+
+SMALL = [
+    # (dtype, B, T, H, K, V, h0, lengths)
+    ("f32", 1, 256, 2, 64, 64, False, None),          # the fp32 workload itself
+    ("f32", 2, 200, 3, 128, 128, True, None),         # ragged last chunk (200 = 3*64 + 8)
+    ("bf16", 2, 200, 3, 128, 128, True, None),
+    ("bf16", 3, 130, 2, 64, 256, True, None),
+    ("bf16", 1, 1, 2, 128, 64, True, None),           # a single row
+    ("bf16", 1, 64, 1, 128, 128, False, None),        # exactly one chunk
+    ("bf16", 1, 3000, 1, 128, 128, True, None),       # one head, long: split into segments + scan
+    ("f32", 1, 5000, 1, 64, 128, True, None),
+    ("bf16", 1, 0, 2, 64, 64, True, [1, 63, 64, 65, 0, 130, 300, 2]),   # varlen incl. an empty sequence
+    ("bf16", 1, 0, 1, 128, 128, True, [3000, 7, 1500]),                  # varlen with segments
+    ("f32", 1, 0, 2, 64, 64, False, [0, 0, 5]),
+]
+
+
+def _case_id(c):
+    d, B, T, H, K, V, h0, L = c
+    return f"{d}-B{B}T{T if L is None else 'var' + str(len(L))}H{H}K{K}V{V}{'-h0' if h0 else ''}"
+
+
+@pytest.mark.parametrize("case", SMALL, ids=_case_id)
+def test_small_cases_elementwise(case):
+    d, B, T, H, K, V, h0, lengths = case
+    inp = make_inputs(d, B=B, T=T, H=H, K=K, V=V, h0=h0, lengths=lengths, seed=zlib.crc32(_case_id(case).encode()) % 1000)
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(as_f64(o), o_ref, TOL[d], "o")
+    assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
+
+
+def test_bf16_output_variant():
+    inp = make_inputs("bf16", B=2, T=300, H=2, K=128, V=128, h0=True, seed=3)
+    o, ht = run_gpu(inp, out_dtype=torch.bfloat16)
+    assert o.dtype == torch.bfloat16
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(as_f64(o), o_ref, TOL_OBF16, "o(bf16)")
+    assert_close(as_f64(ht), ht_ref, TOL["bf16"], "ht")
+
+
+def test_empty_batch_rows_give_initial_state():
+    inp = make_inputs("bf16", B=2, T=0, H=2, K=64, V=128, h0=True, seed=4)
+    o, ht = run_gpu(inp)
+    assert o.numel() == 0
+    assert torch.equal(ht.cpu(), inp.h0)
+
+
+def test_deterministic_bitwise():
+    inp = make_inputs("bf16", B=1, T=2500, H=2, K=128, V=128, h0=True, seed=5)
+    o1, h1 = run_gpu(inp)
+    o2, h2 = run_gpu(inp)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_in_place_state_streaming():
+    """h0 == ht (same buffer): two halves fed through one state buffer equal the full run."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = make_inputs("bf16", B=2, T=1000, H=2, K=128, V=128, h0=True, seed=6)
+    q, k, v, g, h0, _ = to_device(inp)
+    state = h0.clone()
+    outs = []
+    for a, b in ((0, 437), (437, 1000)):
+        sl = lambda x: x[:, a:b].contiguous()
+        o = torch.empty(2, b - a, 2, 128, device="cuda")
+        ws = binding.get_workspace(binding.workspace_size(2, b - a, 2, 128, 128, 2), "cuda")
+        rc = binding.fwd_into(sl(q), sl(k), sl(v), sl(g), o, inp.scale, state, state, None, 2, 2, b - a, 2,
+                              128, 128, 64, binding.GLA_BF16, ws)
+        assert rc == 0
+        outs.append(o)
+    torch.cuda.synchronize()
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(as_f64(torch.cat(outs, 1)), o_ref, TOL["bf16"], "o")
+    assert_close(as_f64(state), ht_ref, TOL["bf16"], "ht")
+
+
+def test_device_side_cu_seqlens_validation():
+    """Offsets that do not end at T are caught on the device: status INVALID_ARG, o left untouched."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = make_inputs("bf16", B=1, T=0, H=1, K=64, V=64, lengths=[10, 20], seed=7)
+    q, k, v, g, _, _ = to_device(inp)
+    bad = torch.tensor([0, 10, 25], dtype=torch.int32, device="cuda")   # T is 30
+    o = torch.full((1, 30, 1, 64), 7.0, device="cuda")
+    ws = torch.zeros(binding.workspace_size(1, 30, 1, 64, 64, 2), dtype=torch.uint8, device="cuda")
+    rc = binding.fwd_into(q, k, v, g, o, inp.scale, None, None, bad, 2, 1, 30, 1, 64, 64, 64,
+                          binding.GLA_BF16, ws)
+    assert rc == 0
+    assert binding.get_status(ws) == binding.GLA_ERR_INVALID_ARG
+    assert binding.get_status(ws) == binding.GLA_OK          # the status word is sticky until read
+    assert torch.all(o == 7.0)
+    good = inp.cu_seqlens.cuda()
+    rc = binding.fwd_into(q, k, v, g, o, inp.scale, None, None, good, 2, 1, 30, 1, 64, 64, 64,
+                          binding.GLA_BF16, ws)
+    assert rc == 0 and binding.get_status(ws) == binding.GLA_OK
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk", [16, 64, 128])
+def test_chunk_local_cumsum_kernel(dtype, chunk):
+    import oracle
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    from chunkwise_gated_linear_chunked_gb300.inputs import stored_numpy
+    for lengths, B, T in ((None, 2, 333), ([5, 0, 64, 200, 1], 1, 0)):
+        inp = make_inputs(dtype, B=B, T=T, H=3, K=64, V=64, lengths=lengths, seed=8)
+        cu = None if inp.cu_seqlens is None else inp.cu_seqlens.cuda()
+        G = binding.chunk_local_cumsum(inp.g.cuda(), chunk=chunk, cu_seqlens=cu)
+        ref = oracle.chunk_local_cumsum(stored_numpy(inp.g), chunk,
+                                        None if cu is None else inp.cu_seqlens.numpy())
+        # fp32 running sums of at most `chunk` terms of magnitude <= ~0.5
+        np.testing.assert_allclose(as_f64(G), ref, rtol=0, atol=2e-6 * chunk)
+
+
+# --------------------------------------------------------------------------------------------------
+# Full-size benchmark workloads (the configuration bench.py times), sampled heads
+# --------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_full_size_workload_sampled_heads(name):
+    w = WORKLOADS[name]
+    inp = workload_inputs(name)
+    o, ht = run_gpu(inp)
+    heads = [0, w.H - 1] if w.H > 1 else [0]
+    o_ref, ht_ref = run_oracle(inp, heads=heads)
+    o_s = as_f64(o[:, :, heads])
+    ht_s = as_f64(ht[:, heads])
+    assert_close(o_s, o_ref, TOL[w.dtype], f"{name} o")
+    assert_close(ht_s, ht_ref, TOL[w.dtype], f"{name} ht")
+    # every output is finite, not only the sampled heads
+    assert torch.isfinite(o).all() and torch.isfinite(ht).all()
