@@ -159,7 +159,13 @@ class KernelTimer:
 
     def __init__(self, max_launches=16):
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_launches)]
-        self._handles = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        for e in self.events:   # torch creates the CUDA event on first record: materialise the handles
+            e.record()
+        torch.cuda.synchronize()
+        handles = [e.cuda_event for e in self.events]
+        if not all(handles):
+            raise RuntimeError("KernelTimer: could not create CUDA events")
+        self._handles = (ctypes.c_void_p * len(self.events))(*handles)
         self._ids = (ctypes.c_int * max_launches)()
 
     def __enter__(self):

@@ -152,3 +152,20 @@ def test_full_size_workload_sampled_heads(name):
     assert_close(ht_s, ht_ref, TOL[w.dtype], f"{name} ht")
     # every output is finite, not only the sampled heads
     assert torch.isfinite(o).all() and torch.isfinite(ht).all()
+
+
+def test_kernel_timer_brackets_every_launch():
+    """The measurement hook records events around each launch of gla_fwd on the call's stream."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = make_inputs("bf16", B=1, T=3000, H=1, K=128, V=128, h0=True, seed=9)   # segments: 3 kernels
+    q, k, v, g, h0, _ = to_device(inp)
+    timer = binding.KernelTimer()
+    with timer:
+        o, ht = binding.gla_fwd(q, k, v, g, scale=inp.scale, initial_state=h0)
+    torch.cuda.synchronize()
+    res = timer.results()
+    assert len(res) >= 1 and all(ms > 0 for _, ms in res), res
+    assert res[-1][0].startswith("out"), res
+    o2, _ = binding.gla_fwd(q, k, v, g, scale=inp.scale, initial_state=h0)   # disarmed: no events
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
