@@ -33,7 +33,8 @@ DEFAULT_WORKLOAD = "b4_t2k_h8"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # kernel name -> source file that defines it (a traffic figure is only reused while that file is unchanged)
 KERNEL_SOURCES = {"out_ffma": "csrc/ffma_kernels.cu", "state_ffma": "csrc/ffma_kernels.cu",
-                  "scan_segments": "csrc/ffma_kernels.cu", "plan_varlen": "csrc/ffma_kernels.cu"}
+                  "scan_segments": "csrc/ffma_kernels.cu", "plan_varlen": "csrc/ffma_kernels.cu",
+                  "out_tc": "csrc/tc_kernels.cu", "state_tc": "csrc/tc_kernels.cu"}
 
 
 def parse_args(argv=None):
@@ -312,7 +313,7 @@ def main(argv=None):
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": compute_dtype(inp), "data": "synthetic",
             "config": {"workload": args.workload, "desc": w.note, "B": B, "T": T, "H": H, "K": K, "V": V,
                        "N": N, "chunk": inp.chunk, "input_dtype": inp.dtype, "h0": inp.h0 is not None,
                        "tokens_per_step": wu["tokens"], "algorithmic_bytes_per_step": wu["bytes"],
@@ -328,10 +329,16 @@ def main(argv=None):
         dist.destroy_process_group()
 
 
+def compute_dtype(inp):
+    """Arithmetic type of the path: fp16 tensor-core operands (fp32 accumulation) for bf16 inputs with
+    K == 128 and V a multiple of 128, fp32 CUDA-core arithmetic otherwise."""
+    return "f16" if inp.dtype == "bf16" and inp.K == 128 and inp.V % 128 == 0 else "f32"
+
+
 def kernel_algorithmic_bytes(name, wu):
-    if name == "out_ffma":
+    if name in ("out_ffma", "out_tc"):
         return wu["bytes"]
-    if name == "state_ffma":
+    if name in ("state_ffma", "state_tc"):
         return wu["in_bytes"]   # upper bound: k, g, v of the non-final segments are a subset
     return wu["state_bytes"]
 

@@ -15,7 +15,7 @@ import torch
 from .build import LIB
 
 GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_ALIGNMENT, GLA_ERR_WORKSPACE, GLA_ERR_CUDA, \
-    GLA_ERR_TIMEOUT = range(7)
+    GLA_ERR_TIMEOUT, GLA_ERR_RANGE = range(8)
 GLA_F32, GLA_BF16, GLA_BF16_OBF16 = 0, 1, 2
 
 EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",

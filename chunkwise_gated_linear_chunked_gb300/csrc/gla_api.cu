@@ -58,7 +58,8 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
     std::memset(&pl, 0, sizeof pl);
     pl.B = B; pl.T = T; pl.H = H; pl.K = K; pl.V = V; pl.N = N; pl.chunk = chunk; pl.dtype = dtype;
     pl.varlen = varlen;
-    pl.BV = 64;
+    pl.tc = tc_supported(dtype, K, V);
+    pl.BV = pl.tc ? 128 : 64;
     pl.NV = V / pl.BV;
     const long long rows = varlen ? (long long)T : (long long)B * T;
     const int nseq = varlen ? N : B;
@@ -116,7 +117,7 @@ struct Profile {
 };
 thread_local Profile g_prof;
 
-enum KernelId { K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4 };
+enum KernelId { K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_STATE_TC = 5, K_OUT_TC = 6 };
 
 // Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
 template <typename Fn>
@@ -245,13 +246,21 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     if (varlen && profiled(K_PLAN, s, [&] { return launch_plan_varlen(pl, a, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;
     if (pl.multi) {
-        if (profiled(K_STATE_FFMA, s, [&] { return launch_state_ffma(pl, a, s); }) != cudaSuccess)
+        if (pl.tc) {
+            if (profiled(K_STATE_TC, s, [&] { return launch_state_tc(pl, a, s); }) != cudaSuccess)
+                return GLA_ERR_CUDA;
+        } else if (profiled(K_STATE_FFMA, s, [&] { return launch_state_ffma(pl, a, s); }) != cudaSuccess) {
             return GLA_ERR_CUDA;
+        }
         if (profiled(K_SCAN, s, [&] { return launch_scan(pl, a, s); }) != cudaSuccess)
             return GLA_ERR_CUDA;
     }
-    if (profiled(K_OUT_FFMA, s, [&] { return launch_out_ffma(pl, a, s); }) != cudaSuccess)
+    if (pl.tc) {
+        if (profiled(K_OUT_TC, s, [&] { return launch_out_tc(pl, a, s); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+    } else if (profiled(K_OUT_FFMA, s, [&] { return launch_out_ffma(pl, a, s); }) != cudaSuccess) {
         return GLA_ERR_CUDA;
+    }
     return GLA_OK;
 }
 
@@ -283,6 +292,7 @@ extern "C" const char *gla_strerror(int code)
     case GLA_ERR_WORKSPACE: return "workspace missing or too small";
     case GLA_ERR_CUDA: return "CUDA runtime or launch failure";
     case GLA_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case GLA_ERR_RANGE: return "a value left the fp16 operand range of the tensor-core path";
     default: return "unknown status code";
     }
 }
@@ -332,6 +342,8 @@ extern "C" const char *gla_kernel_name(int kernel_id)
     case K_STATE_FFMA: return "state_ffma";
     case K_SCAN: return "scan_segments";
     case K_OUT_FFMA: return "out_ffma";
+    case K_STATE_TC: return "state_tc";
+    case K_OUT_TC: return "out_tc";
     default: return "unknown";
     }
 }

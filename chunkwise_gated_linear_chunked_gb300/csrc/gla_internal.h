@@ -21,7 +21,8 @@ struct Plan {
     int P;        // dense: segments per sequence (>= 1); varlen: 0 (per sequence, from the plan kernel)
     int J;        // slots: exact (dense) or an upper bound (varlen)
     bool multi;   // some sequence may span more than one segment: state + scan passes are needed
-    int BV, NV;   // value-tile width and count for the CUDA-core kernels
+    bool tc;      // tensor-core path (bf16 inputs, K == 128, V multiple of 128)
+    int BV, NV;   // value-tile width and count (64 on CUDA cores, 128 on tensor cores)
     // workspace layout (byte offsets)
     size_t off_status, off_table, off_seq, off_ss, off_gtot, total;
 };
@@ -77,6 +78,9 @@ cudaError_t launch_plan_varlen(const Plan &pl, const Args &a, cudaStream_t s);
 cudaError_t launch_state_ffma(const Plan &pl, const Args &a, cudaStream_t s);
 cudaError_t launch_scan(const Plan &pl, const Args &a, cudaStream_t s);
 cudaError_t launch_out_ffma(const Plan &pl, const Args &a, cudaStream_t s);
+bool tc_supported(int dtype, int K, int V);
+cudaError_t launch_state_tc(const Plan &pl, const Args &a, cudaStream_t s);
+cudaError_t launch_out_tc(const Plan &pl, const Args &a, cudaStream_t s);
 cudaError_t launch_chunk_cumsum(const void *g, float *G, const int32_t *cu, int N, int B, int T, int H,
                                 int K, int chunk, int dtype, cudaStream_t s);
 

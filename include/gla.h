@@ -49,7 +49,9 @@ typedef enum gla_status {
     GLA_ERR_ALIGNMENT = 3,     /* a device pointer is not 16-byte aligned                           */
     GLA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than gla_fwd_workspace_size()           */
     GLA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed                       */
-    GLA_ERR_TIMEOUT = 6        /* (device) a bounded wait inside a kernel ran out; outputs invalid  */
+    GLA_ERR_TIMEOUT = 6,       /* (device) a bounded wait inside a kernel ran out; outputs invalid  */
+    GLA_ERR_RANGE = 7          /* (device) a value left the fp16 operand range of the tensor-core
+                                  path (see gla_fwd); outputs invalid, use GLA_F32 inputs instead  */
 } gla_status;
 
 typedef enum gla_dtype {
@@ -78,8 +80,13 @@ typedef enum gla_dtype {
  *               BEFORE ITS FIRST USE (it carries the sticky status word between calls).  One workspace
  *               must not be used by two calls that may run concurrently.
  *
- * Valid domain of the fast intra-chunk factorisation: for every chunk and key dimension the gate sum
- * over half a chunk (32 steps) must stay above about -80; outside it results may overflow to inf/NaN.
+ * Paths: bf16 inputs with K == 128 and V in {128, 256} run on the tcgen05 tensor cores with fp16 operands
+ * and fp32 accumulation; everything else runs on fp32 CUDA cores.  Valid domain of the tensor-core path
+ * (its intra-chunk scores are factorised around an anchor row in the middle of each chunk): every
+ * operand it forms must stay inside the fp16 range, i.e. |q|, |k| * exp(gate sum over up to half a chunk)
+ * below 65000, |v| < 65000, |state| < 65000 and intra-chunk scores below 65000 in magnitude; the kernels
+ * check this and report GLA_ERR_RANGE through gla_get_status() otherwise.  The fp32 path's domain is the
+ * fp32 range of the same factorisation (gate sums over half a chunk above about -80).
  * Returns GLA_OK once enqueued, else a synchronous gla_status.
  */
 int gla_fwd(const void *q, const void *k, const void *v, const void *g, void *o, float scale,

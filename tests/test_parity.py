@@ -169,3 +169,22 @@ def test_kernel_timer_brackets_every_launch():
     o2, _ = binding.gla_fwd(q, k, v, g, scale=inp.scale, initial_state=h0)   # disarmed: no events
     torch.cuda.synchronize()
     assert torch.equal(o, o2)
+
+
+def test_tensor_core_range_check_reports_status():
+    """Values outside the fp16 operand range of the tensor-core path are reported, not silently wrong."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = make_inputs("bf16", B=1, T=130, H=1, K=128, V=128, seed=10)
+    q, k, v, g, _, _ = to_device(inp)
+    v = (v.float() * 1e5).to(torch.bfloat16)
+    ws = torch.zeros(binding.workspace_size(1, 130, 1, 128, 128, 1), dtype=torch.uint8, device="cuda")
+    o = torch.empty(1, 130, 1, 128, device="cuda")
+    rc = binding.fwd_into(q, k, v, g, o, inp.scale, None, None, None, 1, 1, 130, 1, 128, 128, 64,
+                          binding.GLA_BF16, ws)
+    assert rc == 0
+    assert binding.get_status(ws) == binding.GLA_ERR_RANGE
+    # in range again: clean status
+    q, k, v, g, _, _ = to_device(inp)
+    rc = binding.fwd_into(q, k, v, g, o, inp.scale, None, None, None, 1, 1, 130, 1, 128, 128, 64,
+                          binding.GLA_BF16, ws)
+    assert rc == 0 and binding.get_status(ws) == binding.GLA_OK
