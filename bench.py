@@ -273,16 +273,12 @@ def main(argv=None):
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     status = binding.get_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {binding.strerror(status)} in the timed region")
 
-    value = wu["tokens"] * args.steps * world / (total_ms / 1e3)
+    value = whole_job_value(wu["tokens"], args.steps, world, total_ms)
     ms_per_step = total_ms / args.steps
 
     # dominant kernel and its roofline
@@ -333,6 +329,21 @@ def compute_dtype(inp):
     """Arithmetic type of the path: fp16 tensor-core operands (fp32 accumulation) for bf16 inputs with
     K == 128 and V a multiple of 128, fp32 CUDA-core arithmetic otherwise."""
     return "f16" if inp.dtype == "bf16" and inp.K == 128 and inp.V % 128 == 0 else "f32"
+
+
+def max_over_ranks(total_ms, dist=None, device=None):
+    """The timed region's length: the maximum over ranks of each rank's timed total (ms)."""
+    if dist is None:
+        return total_ms
+    import torch
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_step, steps, world, total_ms):
+    """Tokens per second over all ranks: every rank processes `tokens_per_step` each step (weak scaling)."""
+    return tokens_per_step * steps * world / (total_ms / 1e3)
 
 
 def kernel_algorithmic_bytes(name, wu):
