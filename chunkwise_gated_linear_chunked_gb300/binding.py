@@ -19,7 +19,7 @@ GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_ALIGNMENT, GLA_ERR_WOR
 GLA_F32, GLA_BF16, GLA_BF16_OBF16 = 0, 1, 2
 
 EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",
-           "gla_profile_events", "gla_profile_launches", "gla_kernel_name")
+           "gla_profile_events", "gla_profile_launches", "gla_kernel_name", "gla_fwd_noalloc")
 
 if not os.path.exists(LIB):
     raise ImportError(f"libgla.so not built ({LIB}); call chunkwise_gated_linear_chunked_gb300.build.build()")

@@ -123,6 +123,27 @@ int gla_chunk_local_cumsum(const void *g, float *G, const int32_t *cu_seqlens, i
                            int H, int K, int chunk, int dtype, void *stream);
 
 /*
+ * gla_fwd_noalloc — gla_fwd without a caller-provided workspace, for callers that cannot allocate device
+ * memory: host runtimes that own every device byte through their own pool and forbid other allocations
+ * once running, or call paths that must not risk an allocation failure or the device-wide
+ * synchronisation a cudaMalloc can cause.  It has no counterpart on the pages.
+ *
+ * Arguments, layouts, results and synchronous errors are those of gla_fwd.  The scratch comes from one
+ * 32 MiB device array inside the library (held by every device that loads it, until exit); problems whose
+ * gla_fwd_workspace_size() exceeds 32 MiB are rejected with GLA_ERR_WORKSPACE before anything is enqueued.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Nothing is allocated: no cudaMalloc,
+ * cudaFree or allocating library routine is called (each call enqueues a 256-byte cudaMemsetAsync that
+ * clears the status word, then the gla_fwd kernels).  All calls share the one array, so calls that may
+ * overlap on the GPU (different streams without ordering) race and must not be made.  Device-side
+ * conditions (bad cu_seqlens, GLA_ERR_RANGE, GLA_ERR_TIMEOUT) are recorded in the array and cleared by
+ * the next call; they cannot be read back — callers that need them use gla_fwd with a workspace.
+ */
+int gla_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, void *o, float scale,
+                    const float *h0, float *ht, const int32_t *cu_seqlens, int N, int B, int T, int H,
+                    int K, int V, int chunk, int dtype, void *stream);
+
+/*
  * Measurement hook (no counterpart on the pages; it exists so a benchmark can time each kernel of the
  * path with CUDA events on the stream the kernels run on).  While `events` is non-NULL, every later
  * gla_fwd call made from this host thread records events[2i] right before and events[2i+1] right after
