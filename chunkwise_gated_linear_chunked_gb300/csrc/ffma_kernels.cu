@@ -397,10 +397,15 @@ __global__ void __launch_bounds__(1024) plan_varlen(Args a)
     int base = 0;
     for (int n0 = 0; n0 < N; n0 += blockDim.x) {
         const int n = n0 + tid;
-        int cnt = 0;
+        int cnt = 0, seg = a.L;
         if (n < N) {
             const int len = a.cu[n + 1] - a.cu[n];
             cnt = len > 0 ? (len + a.L - 1) / a.L : 1;
+            if (a.seg_cap > 0 && cnt > a.seg_cap) {
+                // longer segments for this sequence (a multiple of the chunk), at most seg_cap of them
+                seg = ((len + a.seg_cap - 1) / a.seg_cap + kChunk - 1) / kChunk * kChunk;
+                cnt = (len + seg - 1) / seg;
+            }
         }
         // block-wide inclusive scan of cnt
         int x = cnt;
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(1024) plan_varlen(Args a)
             seqinfo[n] = make_int2(first, cnt);
             const int bos = a.cu[n], eos = a.cu[n + 1];
             for (int q = 0; q < cnt; ++q)
-                table[first + q] = make_int4(n, q, min(bos + q * a.L, eos), min(bos + (q + 1) * a.L, eos));
+                table[first + q] = make_int4(n, q, min(bos + q * seg, eos), min(bos + (q + 1) * seg, eos));
         }
         base += warp_sums[(blockDim.x >> 5) - 1];
         __syncthreads();

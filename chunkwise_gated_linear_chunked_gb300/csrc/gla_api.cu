@@ -1,5 +1,6 @@
 // libgla C ABI: argument validation, the segment planner, the workspace layout and the launch sequence
 // of the chunkwise GLA forward.  Declarations and contracts: include/gla.h.
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstring>
@@ -71,7 +72,44 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
     if (whole < C)
         whole = C;
     long long L = whole;
-    if (base < target && rows > 0) {
+    if (pl.tc && rows > 0) {
+        // Tensor path, one CTA per SM: pick the segment length with the lowest modelled time, counted in
+        // chunk-times of one CTA: whole waves of the output pass, plus (with more than one segment) the
+        // state pass at ~0.6 of a chunk-time per chunk, the output prologue's scan over earlier segments
+        // and a fixed launch/tail cost.
+        const long long sms = sm_count();
+        const long long nv = pl.NV;
+        double best = 1e300;
+        for (long long m = 2; m <= whole / C; m = (m < 8 ? m + 1 : m + (m >> 2))) {
+            const long long Lc = std::min<long long>(m * C, whole);
+            if (!varlen && (T + Lc - 1) / Lc > kMaxSegments)
+                continue;   // the output prologue reads every earlier segment: keep that quadratic cost small
+            if (varlen && Lc < 8 * C && Lc < whole)
+                continue;   // lengths are unknown here: no segments shorter than 8 chunks
+            long long units, state_units;
+            if (varlen) {
+                const long long J = std::min<long long>((long long)N * kMaxSegments, (long long)N + (T + Lc - 1) / Lc);
+                units = J * H * nv;
+                state_units = Lc < T ? (J - N) * H * nv : 0;
+            } else {
+                const long long P = (T + Lc - 1) / Lc;
+                units = (long long)B * P * H * nv;
+                state_units = (long long)B * (P - 1) * H * nv;
+            }
+            const double chunks = (double)(Lc / C);
+            double cost = (double)((units + sms - 1) / sms) * chunks;
+            if (state_units > 0) {
+                const double segs = (double)(state_units / ((long long)std::max(1, varlen ? N : B) * H * nv) + 1);
+                cost += 0.6 * (double)((state_units + sms - 1) / sms) * chunks + 2.0 + 0.3 * segs;
+            }
+            if (cost < best - 1e-9) {
+                best = cost;
+                L = Lc;
+            }
+            if (Lc == whole)
+                break;
+        }
+    } else if (base < target && rows > 0) {
         long long per = (rows * H * pl.NV + target - 1) / target;   // rows per CTA
         per = (per + C - 1) / C;
         if (per < 4)
@@ -83,7 +121,7 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
     pl.L = (int)L;
     if (varlen) {
         pl.P = 0;
-        pl.J = N + (int)((T + L - 1) / L);
+        pl.J = (int)std::min<long long>((long long)N * kMaxSegments, (long long)N + (T + L - 1) / L);
         pl.multi = L < T;
     } else {
         pl.P = T > 0 ? (int)((T + L - 1) / L) : 1;
@@ -105,6 +143,9 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
     pl.off_gtot = off;
     if (pl.multi)
         off += align_up(sizeof(float) * (size_t)pl.J * H * K);
+    pl.off_h0c = off;
+    if (pl.multi && pl.tc)
+        off += align_up(sizeof(float) * (size_t)N * H * K * V);
     pl.total = off;
 }
 
@@ -231,6 +272,7 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     std::memset(&a, 0, sizeof a);
     a.q = q; a.k = k; a.v = v; a.g = g; a.o = o; a.h0 = h0; a.ht = ht; a.cu = cu_seqlens;
     a.scale = scale;
+    a.seg_cap = kMaxSegments;
     a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.N = N; a.L = pl.L; a.P = pl.P; a.J = pl.J;
     a.status = reinterpret_cast<int *>(ws + pl.off_status);
     if (varlen) {
@@ -240,6 +282,8 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     if (pl.multi) {
         a.ss = reinterpret_cast<float *>(ws + pl.off_ss);
         a.gtot = reinterpret_cast<float *>(ws + pl.off_gtot);
+        if (pl.tc)
+            a.h0c = reinterpret_cast<float *>(ws + pl.off_h0c);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     g_prof.launches = 0;
@@ -247,13 +291,15 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
         return GLA_ERR_CUDA;
     if (pl.multi) {
         if (pl.tc) {
+            // the output kernel evaluates the segment scan in its prologue
             if (profiled(K_STATE_TC, s, [&] { return launch_state_tc(pl, a, s); }) != cudaSuccess)
                 return GLA_ERR_CUDA;
-        } else if (profiled(K_STATE_FFMA, s, [&] { return launch_state_ffma(pl, a, s); }) != cudaSuccess) {
-            return GLA_ERR_CUDA;
+        } else {
+            if (profiled(K_STATE_FFMA, s, [&] { return launch_state_ffma(pl, a, s); }) != cudaSuccess)
+                return GLA_ERR_CUDA;
+            if (profiled(K_SCAN, s, [&] { return launch_scan(pl, a, s); }) != cudaSuccess)
+                return GLA_ERR_CUDA;
         }
-        if (profiled(K_SCAN, s, [&] { return launch_scan(pl, a, s); }) != cudaSuccess)
-            return GLA_ERR_CUDA;
     }
     if (pl.tc) {
         if (profiled(K_OUT_TC, s, [&] { return launch_out_tc(pl, a, s); }) != cudaSuccess)

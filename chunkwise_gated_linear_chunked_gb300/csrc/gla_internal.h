@@ -9,7 +9,8 @@
 
 namespace gla {
 
-constexpr int kChunk = 64;   // chunk length C (rows per intra-chunk tile)
+constexpr int kChunk = 64;          // chunk length C (rows per intra-chunk tile)
+constexpr int kMaxSegments = 24;    // most segments one sequence is split into
 
 // One forward call's launch plan.  Segments of L rows (L a multiple of the chunk) split each sequence
 // so that long sequences with few heads still fill the GPU; a "slot" is one (sequence, segment) pair and
@@ -24,7 +25,7 @@ struct Plan {
     bool tc;      // tensor-core path (bf16 inputs, K == 128, V multiple of 128)
     int BV, NV;   // value-tile width and count (64 on CUDA cores, 128 on tensor cores)
     // workspace layout (byte offsets)
-    size_t off_status, off_table, off_seq, off_ss, off_gtot, total;
+    size_t off_status, off_table, off_seq, off_ss, off_gtot, off_h0c, total;
 };
 
 // Kernel arguments (passed by value).
@@ -36,10 +37,12 @@ struct Args {
     const int32_t *cu;     // device offsets or nullptr
     float scale;
     int B, T, H, K, V, N, L, P, J;
+    int seg_cap;           // varlen: most segments per sequence (the segment length grows to respect it)
     const int4 *table;     // varlen: per slot {n, p, bos, eos}; n < 0 marks an unused slot
     const int2 *seqinfo;   // varlen: per sequence {first slot, slot count}
     float *ss;             // [J][H][K][V]: segment contributions, then segment start states
     float *gtot;           // [J][H][K]: total log-decay of each segment
+    float *h0c;            // [N][H][K][V]: copy of h0 for sequences split into segments (tensor path)
     int *status;           // sticky device status word
 };
 

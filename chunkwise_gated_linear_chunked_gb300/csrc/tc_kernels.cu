@@ -4,7 +4,9 @@
 // gates (FusedChunkGLAFunction.forward, kernel a), the state contribution (k*exp(G_last-G))^T V
 // (prepare_qg_kg, fused_chunk_gla_fwd_kernel: kernel b), and the output = inter-chunk term (q*exp(G)) S plus
 // the causally masked intra-chunk term with the inclusive diagonal (fwd_inner_chunk, the A @ v product of
-// FusedChunkGLAFunction.forward: kernel d), with scale applied to the sum.
+// FusedChunkGLAFunction.forward: kernel d), with scale applied to the sum.  Segments of a long sequence are
+// combined by the decayed scan S_in(p+1) = diag(exp(Gtot(p))) S_in(p) + dS(p) (kernel c), which the output
+// kernel evaluates in its prologue from the state pass's per-segment dS and Gtot.
 //
 // One CTA owns one (segment, head, 128-wide value tile).  The K x V state lives in TMEM transposed
 // (lane = value column v, column = key dimension), so every MMA has M = 128:
@@ -12,14 +14,20 @@
 //   (b) P    = q~    k~^T      A = q~ (rows 64..127 unused),   B = k~  [s][key]   (K-major, smem)
 //   (c) S^T += V^T   k^^T     A = V^T [v][t]  (K-major, smem), B = k^^T [key][t] (K-major, smem)
 //   (d) O^T += V^T   P^T      A = V^T [v][s],                  B = P   [t][s]     (K-major, smem)
-// with q~ = q*exp(G-G_a), k~ = k*exp(G_a-G), k^ = k*exp(G_last-G), S' = diag(exp(G_a)) S, the anchor a in
-// the middle of the chunk.  Operands are fp16 (bf16 inputs widen exactly; 11-bit significands keep the
-// result within the parity bounds where single-rounded bf16 operands do not), accumulation is fp32 in TMEM.
+// with q~ = q*exp(G-G_a), k~ = k*exp(G_a-G), k^ = k*exp(G_last-G), S' = diag(exp(G_a)) S, and the anchor a
+// the middle row of the chunk.  Operands are fp16 (bf16 inputs widen exactly; 11-bit significands keep the
+// result within the parity bounds where single-rounded bf16 operands do not); accumulation is fp32 in TMEM.
 //
-// Roles: warps 0-3 (128 threads) form the compute group — in the gating pass thread i owns key column i
-// (and value column i), elsewhere thread i owns TMEM lane i; warp 4 lane 0 issues the TMA loads (two raw
-// stages of q, k, g, v tiles) and the MMAs.  Every mbarrier wait is bounded; on timeout the kernel records
-// GLA_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+// Pipeline (one CTA per SM): three 64 KB stages hold a chunk's raw tiles and, converted in place, its
+// operands — TMA loads q and k already in the 128-byte-swizzled K-major layout the MMA reads, so q~ and k~
+// overwrite q and k element by element; k^^T and V^T are written over the g and v tiles once those have been
+// read into registers.  Warp roles:
+//   warps 0-3  gating group: cumsum and gating of chunk c+1.. while the tensor cores work on chunk c;
+//   warps 4-7  TMEM group: state conversion, masked scores -> P, output epilogue (warp w owns TMEM lanes
+//              32*(w%4)..+31);
+//   warp 8     lane 0 issues the TMA loads and the MMAs.
+// Every mbarrier wait is bounded; on timeout the kernel records GLA_ERR_TIMEOUT, drains its own copies and
+// MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -35,20 +43,20 @@ using namespace tc;
 constexpr int C = 64;            // chunk rows
 constexpr int KD = 128;          // key dimension handled by this path
 constexpr int VT = 128;          // value tile = TMEM lanes
-constexpr int NCOMP = 128;       // compute threads
-constexpr int NTHREADS = NCOMP + 32;
+constexpr int NA = 128;          // gating group
+constexpr int NB = 128;          // TMEM group
+constexpr int NTHREADS = NA + NB + 32;
 constexpr float L2E = 1.4426950408889634f;
 
-// shared memory (byte offsets from a 1024-aligned base)
-constexpr int RAW_TILE = C * 128 * 2;          // one [64][128] bf16 tile
-constexpr int RAW_STAGE = 4 * RAW_TILE;        // q, k, g, v
-constexpr int OFF_RAW = 0;                     // two stages
-constexpr int OFF_QK = 2 * RAW_STAGE;          // [q~ kb0 | k~ kb0 | q~ kb1 | k~ kb1], 8 KB each
-constexpr int OFF_KH = OFF_QK + 32768;         // k^^T [key][t]
-constexpr int OFF_VT = OFF_KH + 16384;         // V^T  [v][t]
-constexpr int OFF_P = OFF_VT + 16384;          // P    [t][s]
-constexpr int OFF_EG = OFF_P + 8192;           // exp(G_a)[128], exp(G_last)[128]
-constexpr int OFF_BAR = OFF_EG + 1024;         // mbarriers + TMEM address slot
+// one stage (64 KB): [q kb0 | k kb0 | q kb1 | k kb1] (8 KB each, SW128 K-major, 64 rows), g (16 KB),
+// v (16 KB).  g and v are loaded unswizzled as [t][128] and later hold k^^T and V^T ([128][t], SW128).
+constexpr int NSTAGE = 3;
+constexpr int STAGE = 65536;
+constexpr int ST_Q0 = 0, ST_K0 = 8192, ST_Q1 = 16384, ST_K1 = 24576, ST_G = 32768, ST_V = 49152;
+constexpr int OFF_P = NSTAGE * STAGE;          // P [t][s] fp16, 8 KB
+constexpr int OFF_EG = OFF_P + 8192;           // per stage: exp(G_a)[128], exp(G_last)[128]
+constexpr int OFF_PS = OFF_EG + NSTAGE * 1024; // gating-group partial sums: [2 parity][2 halves][128]
+constexpr int OFF_BAR = OFF_PS + 2048;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
 
 // TMEM columns (fp32 unless noted)
@@ -61,12 +69,20 @@ constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t ID_N64 = idesc_f16_f32(128, 64);
 constexpr uint32_t ID_N128 = idesc_f16_f32(128, 128);
 
-__device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
-
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t habs_max(uint32_t m, uint32_t h2)
+{
+    __half2 a = *reinterpret_cast<const __half2 *>(&m), b = *reinterpret_cast<const __half2 *>(&h2);
+    const __half2 r = __hmax2(a, __habs2(b));
+    return *reinterpret_cast<const uint32_t *>(&r);
 }
 
 template <typename T>
@@ -76,7 +92,7 @@ __device__ __forceinline__ float to_out<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
-__device__ __forceinline__ void named_sync_compute() { asm volatile("bar.sync 1, %0;" ::"n"(NCOMP) : "memory"); }
+__device__ __forceinline__ void sync_gating() { asm volatile("bar.sync 1, %0;" ::"n"(NA) : "memory"); }
 
 template <bool OUT, typename Tout>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -87,11 +103,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *raw_full = bars + 0, *raw_empty = bars + 2, *ops_ready = bars + 4, *p_ready = bars + 5;
-    uint64_t *mma1 = bars + 6, *mma2 = bars + 7, *fin = bars + 8;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
-    float *eGa = reinterpret_cast<float *>(sm + OFF_EG), *eGl = eGa + 128;
+    uint64_t *full = bars + 0, *prep = bars + 3, *ops_ready = bars + 6, *p_ready = bars + 7;
+    uint64_t *mma1 = bars + 8, *mma2 = bars + 9, *fin = bars + 10;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
 
+    // the varlen slot table comes from the preceding plan kernel
+    if (a.table || !OUT)
+        grid_dep_wait();
     const int vt = blockIdx.x, h = blockIdx.y, j = blockIdx.z;
     int n, p, bos, eos, send;
     if (!resolve_slot(a, j, n, p, bos, eos, send))
@@ -104,13 +122,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp == 0)
         tmem_alloc(tmem_slot, TM_COLS);
-    if (tid == NCOMP) {
-        bar_init(&raw_full[0], 1);
-        bar_init(&raw_full[1], 1);
-        bar_init(&raw_empty[0], NCOMP);
-        bar_init(&raw_empty[1], NCOMP);
-        bar_init(ops_ready, NCOMP);
-        bar_init(p_ready, NCOMP);
+    if (tid == NA + NB) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            bar_init(&full[s], 1);
+            bar_init(&prep[s], NA);
+        }
+        bar_init(ops_ready, NB);
+        bar_init(p_ready, NB);
         bar_init(mma1, 1);
         bar_init(mma2, 1);
         bar_init(fin, 1);
@@ -124,34 +142,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_before();
     __syncthreads();
     fence_after();
+    if (!OUT)
+        grid_dep_launch();   // every CTA of this grid is running: the output pass may start launching
     const uint32_t tmem = *tmem_slot;
+    bool ok = true;
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ control: TMA + MMA issue
+    if (warp == 8) {
+        // ---------------------------------------------------------------------- control: TMA + MMA
         if (lane == 0) {
-            bool ok = true;
-            constexpr uint32_t tx = (OUT ? 4 : 3) * RAW_TILE;
-            int last_issued[2] = {-1, -1};
+            constexpr uint32_t tx = (OUT ? 4 : 3) * 16384;
+            int last_issued[NSTAGE] = {-1, -1, -1};
             auto issue = [&](int c) {
-                const int s = c & 1;
-                uint8_t *st = sm + OFF_RAW + s * RAW_STAGE;
+                const int s = c % NSTAGE;
+                uint8_t *st = sm + s * STAGE;
                 const int row0 = bos + c * C;
-                bar_expect_tx(&raw_full[s], tx);
-                if (OUT)
-                    tma_load_3d(st, &tm_q, 0, h, row0, &raw_full[s]);
-                tma_load_3d(st + RAW_TILE, &tm_k, 0, h, row0, &raw_full[s]);
-                tma_load_3d(st + 2 * RAW_TILE, &tm_g, 0, h, row0, &raw_full[s]);
-                tma_load_3d(st + 3 * RAW_TILE, &tm_v, v0, h, row0, &raw_full[s]);
+                bar_expect_tx(&full[s], tx);
+                if (OUT) {
+                    tma_load_3d(st + ST_Q0, &tm_q, 0, h, row0, &full[s]);
+                    tma_load_3d(st + ST_Q1, &tm_q, 64, h, row0, &full[s]);
+                }
+                tma_load_3d(st + ST_K0, &tm_k, 0, h, row0, &full[s]);
+                tma_load_3d(st + ST_K1, &tm_k, 64, h, row0, &full[s]);
+                tma_load_3d(st + ST_G, &tm_g, 0, h, row0, &full[s]);
+                tma_load_3d(st + ST_V, &tm_v, v0, h, row0, &full[s]);
                 last_issued[s] = c;
             };
-            if (nchunks > 0)
-                issue(0);
-            if (nchunks > 1)
-                issue(1);
-            const uint32_t qk = smem_u32(sm + OFF_QK), kh = smem_u32(sm + OFF_KH);
-            const uint32_t vtile = smem_u32(sm + OFF_VT), pt = smem_u32(sm + OFF_P);
+            for (int c = 0; c < NSTAGE && c < nchunks; ++c)
+                issue(c);
+            const uint32_t pt = smem_u32(sm + OFF_P);
             for (int c = 0; c < nchunks; ++c) {
                 const uint32_t ph = c & 1;
+                const uint32_t st = smem_u32(sm + (c % NSTAGE) * STAGE);
+                // refill the stage of chunk c-1 (once its MMAs are complete) with chunk c+2
+                if (c >= 1 && c + 2 < nchunks) {
+                    if (!(ok = bar_wait(mma2, (c - 1) & 1)))
+                        break;
+                    issue(c + 2);
+                }
                 if (!(ok = bar_wait(ops_ready, ph)))
                     break;
                 fence_after();
@@ -159,139 +186,204 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // (a) O^T = S'^T q~^T : A = S' (TMEM), B = q~ rows t, K = key
                     for (int k = 0; k < KD / 16; ++k)
                         mma_ts(tmem + TM_O, tmem + TM_SOP + k * 8,
-                               sdesc_sw128(qk + (k >> 2) * 16384 + (k & 3) * 32), ID_N64, k > 0);
+                               sdesc_sw128(st + (k >> 2) * 16384 + (k & 3) * 32), ID_N64, k > 0);
                     // (b) P = q~ k~^T : A = q~ (128-row view), B = k~ rows s
                     for (int k = 0; k < KD / 16; ++k)
-                        mma_ss(tmem + TM_P, sdesc_sw128(qk + (k >> 2) * 16384 + (k & 3) * 32),
-                               sdesc_sw128(qk + (k >> 2) * 16384 + 8192 + (k & 3) * 32), ID_N64, k > 0);
+                        mma_ss(tmem + TM_P, sdesc_sw128(st + (k >> 2) * 16384 + (k & 3) * 32),
+                               sdesc_sw128(st + (k >> 2) * 16384 + ST_K0 + (k & 3) * 32), ID_N64, k > 0);
                 }
                 // (c) S^T += V^T k^^T : K = t
                 for (int k = 0; k < C / 16; ++k)
-                    mma_ss(tmem + TM_S, sdesc_sw128(vtile + k * 32), sdesc_sw128(kh + k * 32), ID_N128, 1);
+                    mma_ss(tmem + TM_S, sdesc_sw128(st + ST_V + k * 32), sdesc_sw128(st + ST_G + k * 32),
+                           ID_N128, 1);
                 mma_commit(mma1);
-                if (c + 2 < nchunks) {
-                    if (!(ok = bar_wait(&raw_empty[c & 1], (c >> 1) & 1)))
-                        break;
-                    issue(c + 2);
-                }
                 if (OUT) {
                     if (!(ok = bar_wait(p_ready, ph)))
                         break;
                     fence_after();
                     // (d) O^T += V^T P^T : K = s
                     for (int k = 0; k < C / 16; ++k)
-                        mma_ss(tmem + TM_O, sdesc_sw128(vtile + k * 32), sdesc_sw128(pt + k * 32), ID_N64, 1);
+                        mma_ss(tmem + TM_O, sdesc_sw128(st + ST_V + k * 32), sdesc_sw128(pt + k * 32), ID_N64, 1);
                 }
                 mma_commit(mma2);
             }
-            // drain: every MMA issued by this thread, and the last copy into each raw stage
             mma_commit(fin);
             bool drained = bar_wait(fin, 0);
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < NSTAGE; ++s)
                 if (last_issued[s] >= 0)
-                    drained &= bar_wait(&raw_full[s], (last_issued[s] >> 1) & 1);
+                    drained &= bar_wait(&full[s], (last_issued[s] / NSTAGE) & 1);
             if (!ok || !drained)
                 report(a.status, GLA_ERR_TIMEOUT);
         }
+    } else if (warp < 4) {
+        // ---------------------------------------------------------------------- gating group
+        // thread: key pair kp (keys 2kp, 2kp+1; value columns likewise), row half rh (rows 32rh..32rh+31)
+        const int kp = tid & 63, rh = tid >> 6;
+        const int key = 2 * kp;
+        const int kb = key >> 6, kc = key & 63;   // K-block and column inside the 128-byte row
+        float *psum = reinterpret_cast<float *>(sm + OFF_PS);
+        uint32_t hmax = 0;                         // |fp16 operand| maximum (half2)
+        float gsum0 = 0.f, gsum1 = 0.f;            // segment log-decay totals (state pass)
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c % NSTAGE;
+            uint8_t *st = sm + s * STAGE;
+            const int len = min(C, eos - (bos + c * C));
+            if (!(ok = bar_wait(&full[s], (c / NSTAGE) & 1)))
+                break;
+            // pass 1: this thread's g and v rows into registers (rows >= len are zero)
+            uint32_t gr[32], vr[32];
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int t = 32 * rh + u;
+                const bool in = t < len;
+                gr[u] = in ? *reinterpret_cast<const uint32_t *>(st + ST_G + t * 256 + kp * 4) : 0u;
+                vr[u] = in ? *reinterpret_cast<const uint32_t *>(st + ST_V + t * 256 + kp * 4) : 0u;
+                s0 += bf_lo(gr[u]);
+                s1 += bf_hi(gr[u]);
+            }
+            float *ps = psum + (c & 1) * 256;
+            ps[rh * 128 + key] = s0;
+            ps[rh * 128 + key + 1] = s1;
+            sync_gating();   // partial sums visible; every g / v tile read is done
+            const float ga0 = ps[key], ga1 = ps[key + 1];                        // G at the anchor row
+            const float gl0 = ga0 + ps[128 + key], gl1 = ga1 + ps[128 + key + 1];  // G at the last row
+            float G0 = rh ? ga0 : 0.f, G1 = rh ? ga1 : 0.f;
+            if (rh == 0) {
+                float *eg = reinterpret_cast<float *>(sm + OFF_EG + s * 1024);
+                eg[key] = ex2(ga0 * L2E);
+                eg[key + 1] = ex2(ga1 * L2E);
+                eg[128 + key] = ex2(gl0 * L2E);
+                eg[128 + key + 1] = ex2(gl1 * L2E);
+                gsum0 += gl0;
+                gsum1 += gl1;
+            }
+            const float gaL0 = ga0 * L2E, gaL1 = ga1 * L2E, glL0 = gl0 * L2E, glL1 = gl1 * L2E;
+            const float cl0 = ex2(glL0 - gaL0), cl1 = ex2(glL1 - gaL1);
+            uint32_t kh[32];
+            uint8_t *qk = st + kb * 16384;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int t = 32 * rh + u;
+                G0 += bf_lo(gr[u]);
+                G1 += bf_hi(gr[u]);
+                const float x0 = G0 * L2E, x1 = G1 * L2E;
+                const uint32_t off = sw128(t, kc);
+                if (OUT) {
+                    const uint32_t qw = *reinterpret_cast<const uint32_t *>(qk + ST_Q0 + off);
+                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
+                    const bool in = t < len;
+                    const float e0 = ex2(x0 - gaL0), e1 = ex2(x1 - gaL1);
+                    const float f0 = ex2(gaL0 - x0), f1 = ex2(gaL1 - x1);
+                    const float q0 = in ? bf_lo(qw) * e0 : 0.f, q1 = in ? bf_hi(qw) * e1 : 0.f;
+                    const float k0 = in ? bf_lo(kw) * f0 : 0.f, k1 = in ? bf_hi(kw) * f1 : 0.f;
+                    const uint32_t qh = pack_h2(q0, q1), kth = pack_h2(k0, k1);
+                    *reinterpret_cast<uint32_t *>(qk + ST_Q0 + off) = qh;
+                    *reinterpret_cast<uint32_t *>(qk + ST_K0 + off) = kth;
+                    hmax = habs_max(habs_max(hmax, qh), kth);
+                    kh[u] = pack_h2(k0 * cl0, k1 * cl1);
+                } else {
+                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
+                    const bool in = t < len;
+                    const float k0 = in ? bf_lo(kw) * ex2(glL0 - x0) : 0.f;
+                    const float k1 = in ? bf_hi(kw) * ex2(glL1 - x1) : 0.f;
+                    kh[u] = pack_h2(k0, k1);
+                }
+                // v: bf16 -> fp16 (exact within the fp16 range)
+                vr[u] = pack_h2(bf_lo(vr[u]), bf_hi(vr[u]));
+                hmax = habs_max(hmax, vr[u]);
+                hmax = habs_max(hmax, kh[u]);
+            }
+            // k^^T and V^T rows (key / value column 2kp and 2kp+1), columns t = 32rh.., over the g / v tiles
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int t0 = 32 * rh + 8 * jj;
+                uint32_t k_lo[4], k_hi[4], v_lo[4], v_hi[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t a0 = kh[8 * jj + 2 * w], a1 = kh[8 * jj + 2 * w + 1];
+                    const uint32_t b0 = vr[8 * jj + 2 * w], b1 = vr[8 * jj + 2 * w + 1];
+                    k_lo[w] = __byte_perm(a0, a1, 0x5410);
+                    k_hi[w] = __byte_perm(a0, a1, 0x7632);
+                    v_lo[w] = __byte_perm(b0, b1, 0x5410);
+                    v_hi[w] = __byte_perm(b0, b1, 0x7632);
+                }
+                *reinterpret_cast<uint4 *>(st + ST_G + sw128(key, t0)) = make_uint4(k_lo[0], k_lo[1], k_lo[2], k_lo[3]);
+                *reinterpret_cast<uint4 *>(st + ST_G + sw128(key + 1, t0)) = make_uint4(k_hi[0], k_hi[1], k_hi[2], k_hi[3]);
+                *reinterpret_cast<uint4 *>(st + ST_V + sw128(key, t0)) = make_uint4(v_lo[0], v_lo[1], v_lo[2], v_lo[3]);
+                *reinterpret_cast<uint4 *>(st + ST_V + sw128(key + 1, t0)) = make_uint4(v_hi[0], v_hi[1], v_hi[2], v_hi[3]);
+            }
+            fence_proxy_async();
+            bar_arrive(&prep[s]);
+        }
+        if (ok && !OUT && vt == 0 && rh == 0) {
+            float *gt = a.gtot + ((size_t)j * H + h) * KD;
+            gt[key] = gsum0;
+            gt[key + 1] = gsum1;
+        }
+        const __half2 hm = *reinterpret_cast<const __half2 *>(&hmax);
+        if (!(fmaxf(__low2float(hm), __high2float(hm)) <= 65000.f))
+            report(a.status, GLA_ERR_RANGE);
+        if (!ok)
+            report(a.status, GLA_ERR_TIMEOUT);
     } else {
-        // ------------------------------------------------------------ compute group (128 threads)
-        const int i = tid;
-        const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;   // this warp's TMEM lane quarter
-        bool ok = true;
-        float amax = 0.f;   // largest magnitude converted to an fp16 operand
-        float gsum = 0.f;   // total log-decay of the segment for key i (state pass)
-
-        // initial state -> TMEM (thread = lane v); S^T[v][key] = S[key][v]
+        // ---------------------------------------------------------------------- TMEM group
+        const int b = tid - NA;                                   // TMEM lane = value column (or row t)
+        const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        float amax = 0.f;
+        // initial state of the segment -> TMEM (S^T[v][key] = S[key][v])
         {
-            const float *src = nullptr;
-            if (OUT)
-                src = multi ? a.ss + ((size_t)j * H + h) * KD * V
-                            : (a.h0 ? a.h0 + ((size_t)n * H + h) * KD * V : nullptr);
+            const size_t hoff = ((size_t)n * H + h) * KD * V;
+            if (!OUT && p == 0 && a.h0 && a.h0c) {
+                // keep a copy of this sequence's h0: the output pass reads it after ht (which may be the
+                // same buffer) has been written by the sequence's last segment
+                for (int k = 0; k < KD; ++k)
+                    a.h0c[hoff + (size_t)k * V + v0 + b] = __ldg(a.h0 + hoff + (size_t)k * V + v0 + b);
+            }
+            const bool several = OUT && multi && !(p == 0 && eos == send);   // sequence has > 1 segment
+            const float *h0p = nullptr;
+            if (OUT && a.h0)
+                h0p = several ? a.h0c + hoff : a.h0 + hoff;
+            const bool scan = several && p > 0;
+            if (several)
+                grid_dep_wait();   // h0 copy and per-segment contributions come from the state pass
+            const int j0 = j - p;
             for (int kc = 0; kc < KD / 32; ++kc) {
                 uint32_t r[32];
+                float acc[32];
 #pragma unroll
                 for (int u = 0; u < 32; ++u)
-                    r[u] = __float_as_uint(src ? __ldg(src + (size_t)(kc * 32 + u) * V + v0 + i) : 0.f);
+                    acc[u] = h0p ? __ldg(h0p + (size_t)(kc * 32 + u) * V + v0 + b) : 0.f;
+                if (scan) {
+                    for (int m = 0; m < p; ++m) {
+                        const size_t jm = (size_t)(j0 + m) * H + h;
+                        const float *dS = a.ss + jm * KD * V + (size_t)(kc * 32) * V + v0 + b;
+                        const float *gt = a.gtot + jm * KD + kc * 32;
+#pragma unroll
+                        for (int u = 0; u < 32; ++u)
+                            acc[u] = fmaf(ex2(__ldg(gt + u) * L2E), acc[u], __ldg(dS + (size_t)u * V));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    r[u] = __float_as_uint(acc[u]);
                 tmem_st32(tmem + lrow + TM_S + kc * 32, r);
             }
             tmem_wait_st();
         }
-
+        Tout *go = static_cast<Tout *>(a.o);
         for (int c = 0; c < nchunks; ++c) {
-            const int s = c & 1;
+            const int s = c % NSTAGE;
             const uint32_t ph = c & 1;
             const int row0 = bos + c * C;
             const int len = min(C, eos - row0);
-            const uint8_t *st = sm + OFF_RAW + s * RAW_STAGE;
-            const __nv_bfloat16 *rq = reinterpret_cast<const __nv_bfloat16 *>(st);
-            const __nv_bfloat16 *rk = rq + C * 128, *rg = rk + C * 128, *rv = rg + C * 128;
-            if (!(ok = bar_wait(&raw_full[s], (c >> 1) & 1)))
+            if (!OUT && c > 0 && !(ok = bar_wait(mma1, (c - 1) & 1)))
                 break;
-
-            // pass 1: chunk-local cumsum of column i -> G at the anchor and at the last valid row
-            const int ra = min(C / 2 - 1, len - 1);
-            float G = 0.f, Ga = 0.f;
-            for (int t = 0; t < len; ++t) {
-                G += bf(rg + t * 128 + i);
-                if (t == ra)
-                    Ga = G;
-            }
-            const float Gl = G;
-            gsum += Gl;
-            // the previous chunk's MMAs must be done before its operand buffers are overwritten
-            if (c > 0 && !(ok = bar_wait(mma2, (c - 1) & 1)))
+            if (!(ok = bar_wait(&prep[s], (c / NSTAGE) & 1)))
                 break;
-
-            // pass 2: gated operands (thread i = key column i; value column i for V^T)
-            const float cl = exp2f((Gl - Ga) * L2E);
-            G = 0.f;
-            uint8_t *qk = sm + OFF_QK + (i >> 6) * 16384;
-            const int ic = i & 63;
-#pragma unroll 1
-            for (int t0 = 0; t0 < C; t0 += 8) {
-                uint32_t khp[4], vp[4];
-#pragma unroll
-                for (int u = 0; u < 8; u += 2) {
-                    float kh2[2], vv2[2];
-#pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        const int t = t0 + u + w;
-                        float qt = 0.f, kt = 0.f, kk = 0.f, vv = 0.f;
-                        if (t < len) {
-                            G += bf(rg + t * 128 + i);
-                            const float kv = bf(rk + t * 128 + i);
-                            vv = bf(rv + t * 128 + i);
-                            if (OUT) {
-                                const float qv = bf(rq + t * 128 + i);
-                                qt = qv * exp2f((G - Ga) * L2E);
-                                kt = kv * exp2f((Ga - G) * L2E);
-                                kk = kt * cl;
-                            } else {
-                                kk = kv * exp2f((Gl - G) * L2E);
-                            }
-                        }
-                        if (OUT) {
-                            *reinterpret_cast<__half *>(qk + sw128(t, ic)) = __float2half_rn(qt);
-                            *reinterpret_cast<__half *>(qk + 8192 + sw128(t, ic)) = __float2half_rn(kt);
-                            amax = fmaxf(amax, fmaxf(fabsf(qt), fabsf(kt)));
-                        }
-                        amax = fmaxf(amax, fmaxf(fabsf(kk), fabsf(vv)));
-                        kh2[w] = kk;
-                        vv2[w] = vv;
-                    }
-                    khp[u / 2] = pack_h2(kh2[0], kh2[1]);
-                    vp[u / 2] = pack_h2(vv2[0], vv2[1]);
-                }
-                *reinterpret_cast<uint4 *>(sm + OFF_KH + sw128(i, t0)) = make_uint4(khp[0], khp[1], khp[2], khp[3]);
-                *reinterpret_cast<uint4 *>(sm + OFF_VT + sw128(i, t0)) = make_uint4(vp[0], vp[1], vp[2], vp[3]);
-            }
-            eGa[i] = exp2f(Ga * L2E);
-            eGl[i] = exp2f(Gl * L2E);
-            fence_proxy_async();
-            bar_arrive(&raw_empty[s]);
-            named_sync_compute();   // eGa / eGl complete
-
-            // state: S' = diag(exp(G_a)) S (fp16 operand), S <- diag(exp(G_last)) S (thread = lane v)
+            fence_after();
+            const float *eg = reinterpret_cast<const float *>(sm + OFF_EG + s * 1024);
+            // S' = diag(exp(G_a)) S (fp16 operand); S <- diag(exp(G_last)) S
             for (int kc = 0; kc < KD / 32; ++kc) {
                 uint32_t r[32];
                 tmem_ld32(tmem + lrow + TM_S + kc * 32, r);
@@ -300,78 +392,83 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     uint32_t op[16];
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
-                        const float s0 = __uint_as_float(r[2 * u]) * eGa[kc * 32 + 2 * u];
-                        const float s1 = __uint_as_float(r[2 * u + 1]) * eGa[kc * 32 + 2 * u + 1];
+                        const float2 e = *reinterpret_cast<const float2 *>(eg + kc * 32 + 2 * u);
+                        const float s0 = __uint_as_float(r[2 * u]) * e.x;
+                        const float s1 = __uint_as_float(r[2 * u + 1]) * e.y;
                         amax = fmaxf(amax, fmaxf(fabsf(s0), fabsf(s1)));
                         op[u] = pack_h2(s0, s1);
                     }
                     tmem_st16(tmem + lrow + TM_SOP + kc * 16, op);
                 }
 #pragma unroll
-                for (int u = 0; u < 32; ++u)
-                    r[u] = __float_as_uint(__uint_as_float(r[u]) * eGl[kc * 32 + u]);
+                for (int u = 0; u < 32; u += 4) {
+                    const float4 e = *reinterpret_cast<const float4 *>(eg + 128 + kc * 32 + u);
+                    r[u] = __float_as_uint(__uint_as_float(r[u]) * e.x);
+                    r[u + 1] = __float_as_uint(__uint_as_float(r[u + 1]) * e.y);
+                    r[u + 2] = __float_as_uint(__uint_as_float(r[u + 2]) * e.z);
+                    r[u + 3] = __float_as_uint(__uint_as_float(r[u + 3]) * e.w);
+                }
                 tmem_st32(tmem + lrow + TM_S + kc * 32, r);
             }
             tmem_wait_st();
             fence_before();
             bar_arrive(ops_ready);
+            if (!OUT)
+                continue;
 
-            if (OUT) {
-                // masked scores -> fp16 P[t][s] (thread = lane t, t < 64)
-                if (!(ok = bar_wait(mma1, ph)))
-                    break;
-                fence_after();
-                if (warp < 2) {
-                    const int t = i;
-                    for (int sc = 0; sc < 2; ++sc) {
-                        uint32_t r[32];
-                        tmem_ld32(tmem + lrow + TM_P + sc * 32, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int u0 = 0; u0 < 32; u0 += 8) {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int u = 0; u < 8; u += 2) {
-                                const int sa = sc * 32 + u0 + u;
-                                const float p0 = sa <= t ? __uint_as_float(r[u0 + u]) : 0.f;
-                                const float p1 = sa + 1 <= t ? __uint_as_float(r[u0 + u + 1]) : 0.f;
-                                amax = fmaxf(amax, fmaxf(fabsf(p0), fabsf(p1)));
-                                pk[u / 2] = pack_h2(p0, p1);
-                            }
-                            *reinterpret_cast<uint4 *>(sm + OFF_P + sw128(t, sc * 32 + u0)) =
-                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        }
-                    }
-                }
-                fence_proxy_async();
-                fence_before();
-                bar_arrive(p_ready);
-
-                // output (thread = lane v): o[t, v] = scale * O^T[v][t]
-                if (!(ok = bar_wait(mma2, ph)))
-                    break;
-                fence_after();
-                Tout *go = static_cast<Tout *>(a.o);
-                for (int oc = 0; oc < 2; ++oc) {
+            // masked scores -> fp16 P[t][s] (lanes t < 64: warps 4 and 5)
+            if (!(ok = bar_wait(mma1, ph)))
+                break;
+            fence_after();
+            if ((warp & 3) < 2) {
+                const int t = b;
+                for (int sc = 0; sc < 2; ++sc) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + lrow + TM_O + oc * 32, r);
+                    tmem_ld32(tmem + lrow + TM_P + sc * 32, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const int t = oc * 32 + u;
-                        if (t < len) {
-                            const float val = a.scale * __uint_as_float(r[u]);
-                            go[((size_t)(row0 + t) * H + h) * V + v0 + i] = to_out<Tout>(val);
+                    for (int u0 = 0; u0 < 32; u0 += 8) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int u = 0; u < 8; u += 2) {
+                            const int sa = sc * 32 + u0 + u;
+                            const float p0 = sa <= t ? __uint_as_float(r[u0 + u]) : 0.f;
+                            const float p1 = sa + 1 <= t ? __uint_as_float(r[u0 + u + 1]) : 0.f;
+                            amax = fmaxf(amax, fmaxf(fabsf(p0), fabsf(p1)));
+                            pk[u / 2] = pack_h2(p0, p1);
                         }
+                        *reinterpret_cast<uint4 *>(sm + OFF_P + sw128(t, sc * 32 + u0)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }
                 }
-                fence_before();
             }
+            fence_proxy_async();
+            fence_before();
+            bar_arrive(p_ready);
+
+            // output (thread = lane v): o[t, v] = scale * O^T[v][t]
+            if (!(ok = bar_wait(mma2, ph)))
+                break;
+            fence_after();
+            Tout *orow = go + ((size_t)row0 * H + h) * V + v0 + b;
+            const size_t rstride = (size_t)H * V;
+            for (int oc = 0; oc < 2; ++oc) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lrow + TM_O + oc * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int t = oc * 32 + u;
+                    if (t < len)
+                        orow[(size_t)t * rstride] = to_out<Tout>(a.scale * __uint_as_float(r[u]));
+                }
+            }
+            fence_before();
         }
 
-        // final state of the segment: ht (output pass, last segment) or the contribution (state pass)
+        // final state of the segment: ht (output pass, last segment) or dS (state pass)
         if (ok && nchunks > 0)
-            ok = bar_wait(mma2, (nchunks - 1) & 1);
+            ok = bar_wait(mma1, (nchunks - 1) & 1);
         if (ok) {
             fence_after();
             float *dst = nullptr;
@@ -386,11 +483,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tmem_wait_ld();
 #pragma unroll
                     for (int u = 0; u < 32; ++u)
-                        dst[(size_t)(kc * 32 + u) * V + v0 + i] = __uint_as_float(r[u]);
+                        dst[(size_t)(kc * 32 + u) * V + v0 + b] = __uint_as_float(r[u]);
                 }
             }
-            if (!OUT && vt == 0)
-                a.gtot[((size_t)j * H + h) * KD + i] = gsum;
         }
         if (!ok)
             report(a.status, GLA_ERR_TIMEOUT);
@@ -420,28 +515,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// [rows][H][D] bf16 tensor, box = 128 (inner) x 1 head x 64 rows.
-bool encode_rows(CUtensorMap *m, const void *ptr, int D, int H, long long rows)
+// [rows][H][D] bf16 tensor; box = `inner` elements x 1 head x 64 rows.
+bool encode_rows(CUtensorMap *m, const void *ptr, int D, int H, long long rows, int inner, bool swizzle)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-    cuuint32_t box[3] = {128, 1, (cuuint32_t)C};
+    cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)C};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool OUT, typename Tout>
-cudaError_t launch_one(const Plan &pl, const Args &a, cudaStream_t s)
+cudaError_t launch_one(const Plan &pl, const Args &a, cudaStream_t s, bool pdl)
 {
     const long long rows = pl.varlen ? (long long)pl.T : (long long)pl.B * pl.T;
     CUtensorMap mq, mk, mg, mv;
-    if (!encode_rows(&mq, a.q, pl.K, pl.H, rows) || !encode_rows(&mk, a.k, pl.K, pl.H, rows) ||
-        !encode_rows(&mg, a.g, pl.K, pl.H, rows) || !encode_rows(&mv, a.v, pl.V, pl.H, rows))
+    if (!encode_rows(&mq, a.q, pl.K, pl.H, rows, 64, true) || !encode_rows(&mk, a.k, pl.K, pl.H, rows, 64, true) ||
+        !encode_rows(&mg, a.g, pl.K, pl.H, rows, 128, false) ||
+        !encode_rows(&mv, a.v, pl.V, pl.H, rows, 128, false))
         return cudaErrorInvalidValue;
     auto f = gla_tc<OUT, Tout>;
     static bool attr = false;
@@ -451,8 +547,21 @@ cudaError_t launch_one(const Plan &pl, const Args &a, cudaStream_t s)
             return e;
         attr = true;
     }
-    dim3 grid(pl.V / VT, pl.H, pl.J);
-    f<<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mg, mv, a, pl.multi ? 1 : 0);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.V / VT, pl.H, pl.J);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = pdl ? 1 : 0;
+    int multi = pl.multi ? 1 : 0;
+    void *args[] = {&mq, &mk, &mg, &mv, const_cast<Args *>(&a), &multi};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(f), args);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
@@ -465,14 +574,15 @@ bool tc_supported(int dtype, int K, int V)
 
 cudaError_t launch_state_tc(const Plan &pl, const Args &a, cudaStream_t s)
 {
-    return launch_one<false, float>(pl, a, s);
+    return launch_one<false, float>(pl, a, s, pl.varlen);
 }
 
 cudaError_t launch_out_tc(const Plan &pl, const Args &a, cudaStream_t s)
 {
+    const bool pdl = pl.multi || pl.varlen;   // a kernel of this call precedes it in the stream
     if (pl.dtype == GLA_BF16_OBF16)
-        return launch_one<true, __nv_bfloat16>(pl, a, s);
-    return launch_one<true, float>(pl, a, s);
+        return launch_one<true, __nv_bfloat16>(pl, a, s, pdl);
+    return launch_one<true, float>(pl, a, s, pdl);
 }
 
 }  // namespace gla

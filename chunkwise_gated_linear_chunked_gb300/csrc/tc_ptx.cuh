@@ -215,5 +215,24 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------------------------------------------
+// Programmatic dependent launch and the hardware base-2 exponential
+// ---------------------------------------------------------------------------------------------------
+
+// Block until the preceding grid in the stream has completed and its writes are visible (a no-op when
+// this grid was not launched as a programmatic dependent).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream (launched as a programmatic dependent) to start launching.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// 2^x with the SFU's approximate exponential (relative error far below the fp16 operand rounding).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 }  // namespace tc
 }  // namespace gla
