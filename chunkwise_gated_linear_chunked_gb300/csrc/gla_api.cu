@@ -80,8 +80,8 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
         const long long sms = sm_count();
         const long long nv = pl.NV;
         double best = 1e300;
-        for (long long m = 2; m <= whole / C; m = (m < 8 ? m + 1 : m + (m >> 2))) {
-            const long long Lc = std::min<long long>(m * C, whole);
+        for (long long m = 2;; m = (m < 8 ? m + 1 : m + (m >> 2))) {
+            const long long Lc = std::min<long long>(m * C, whole);   // the last candidate is `whole`
             if (!varlen && (T + Lc - 1) / Lc > kMaxSegments)
                 continue;   // the output prologue reads every earlier segment: keep that quadratic cost small
             if (varlen && Lc < 8 * C && Lc < whole)

@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/gla.h"
+#include "gla.h"
 
 namespace gla {
 

@@ -10,9 +10,9 @@
 //
 // One CTA owns one (segment, head, 128-wide value tile).  The K x V state lives in TMEM transposed
 // (lane = value column v, column = key dimension), so every MMA has M = 128:
+//   (c) S^T += V^T   k^^T     A = V^T [v][t]  (K-major, smem), B = k^^T [key][t] (K-major, smem)
 //   (a) O^T  = S'^T  q~^T      A = S' from TMEM (fp16),        B = q~  [t][key]   (K-major, smem)
 //   (b) P    = q~    k~^T      A = q~ (rows 64..127 unused),   B = k~  [s][key]   (K-major, smem)
-//   (c) S^T += V^T   k^^T     A = V^T [v][t]  (K-major, smem), B = k^^T [key][t] (K-major, smem)
 //   (d) O^T += V^T   P^T      A = V^T [v][s],                  B = P   [t][s]     (K-major, smem)
 // with q~ = q*exp(G-G_a), k~ = k*exp(G_a-G), k^ = k*exp(G_last-G), S' = diag(exp(G_a)) S, and the anchor a
 // the middle row of the chunk.  Operands are fp16 (bf16 inputs widen exactly; 11-bit significands keep the
@@ -21,13 +21,13 @@
 // Pipeline (one CTA per SM): three 64 KB stages hold a chunk's raw tiles and, converted in place, its
 // operands — TMA loads q and k already in the 128-byte-swizzled K-major layout the MMA reads, so q~ and k~
 // overwrite q and k element by element; k^^T and V^T are written over the g and v tiles once those have been
-// read into registers.  Warp roles:
-//   warps 0-3  gating group: cumsum and gating of chunk c+1.. while the tensor cores work on chunk c;
-//   warps 4-7  TMEM group: state conversion, masked scores -> P, output epilogue (warp w owns TMEM lanes
-//              32*(w%4)..+31);
-//   warp 8     lane 0 issues the TMA loads and the MMAs.
-// Every mbarrier wait is bounded; on timeout the kernel records GLA_ERR_TIMEOUT, drains its own copies and
-// MMAs, frees TMEM and returns.
+// read into registers.  S' and O^T are double-buffered in TMEM so consecutive chunks overlap.  Warp roles:
+//   warps 0-7    gating group: cumsum and gating, running ahead of the tensor cores;
+//   warps 8-11   state group: state conversion (S', decay), masked scores -> P;
+//   warps 12-15  output group: O^T -> shared memory -> TMA tensor store (scalar stores for a ragged chunk);
+//   warp 16      lane 0 issues the TMA loads and the MMAs.
+// (Warps w of the state and output groups own TMEM lanes 32*(w%4)..+31.)  Every mbarrier wait is bounded; on
+// timeout the kernel records GLA_ERR_TIMEOUT, drains its own copies, stores and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
@@ -43,27 +43,30 @@ using namespace tc;
 constexpr int C = 64;            // chunk rows
 constexpr int KD = 128;          // key dimension handled by this path
 constexpr int VT = 128;          // value tile = TMEM lanes
-constexpr int NA = 128;          // gating group
-constexpr int NB = 128;          // TMEM group
-constexpr int NTHREADS = NA + NB + 32;
+constexpr int NA = 256;          // gating group: 8 warps
+constexpr int NB = 128;          // state group
+constexpr int NC = 128;          // output group
+constexpr int WB = NA / 32, WC = (NA + NB) / 32, WCTL = (NA + NB + NC) / 32;   // first warp of each group
+constexpr int NTHREADS = NA + NB + NC + 32;
 constexpr float L2E = 1.4426950408889634f;
 
 // one stage (64 KB): [q kb0 | k kb0 | q kb1 | k kb1] (8 KB each, SW128 K-major, 64 rows), g (16 KB),
 // v (16 KB).  g and v are loaded unswizzled as [t][128] and later hold k^^T and V^T ([128][t], SW128).
 constexpr int NSTAGE = 3;
 constexpr int STAGE = 65536;
-constexpr int ST_Q0 = 0, ST_K0 = 8192, ST_Q1 = 16384, ST_K1 = 24576, ST_G = 32768, ST_V = 49152;
+constexpr int ST_Q0 = 0, ST_K0 = 8192, ST_G = 32768, ST_V = 49152;
 constexpr int OFF_P = NSTAGE * STAGE;          // P [t][s] fp16, 8 KB
 constexpr int OFF_EG = OFF_P + 8192;           // per stage: exp(G_a)[128], exp(G_last)[128]
-constexpr int OFF_PS = OFF_EG + NSTAGE * 1024; // gating-group partial sums: [2 parity][2 halves][128]
-constexpr int OFF_BAR = OFF_PS + 2048;
+constexpr int OFF_PS = OFF_EG + NSTAGE * 1024; // gating-group partial sums: [2 parity][4 quarters][128]
+constexpr int OFF_OST = OFF_PS + 4096;         // output staging: 32 rows x 128 fp32 (16 KB)
+constexpr int OFF_BAR = OFF_OST + 16384;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
 
 // TMEM columns (fp32 unless noted)
 constexpr uint32_t TM_S = 0;      // S^T accumulator: 128 columns (key)
-constexpr uint32_t TM_SOP = 128;  // S'^T fp16 operand: 64 columns (key pairs)
-constexpr uint32_t TM_O = 192;    // O^T: 64 columns (t)
-constexpr uint32_t TM_P = 256;    // P: 64 columns (s), lanes t
+constexpr uint32_t TM_SOP = 128;  // S'^T fp16 operand, two buffers of 64 columns (key pairs)
+constexpr uint32_t TM_O = 256;    // O^T, two buffers of 64 columns (t)
+constexpr uint32_t TM_P = 384;    // P: 64 columns (s), lanes t
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t ID_N64 = idesc_f16_f32(128, 64);
@@ -93,19 +96,21 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 __device__ __forceinline__ void sync_gating() { asm volatile("bar.sync 1, %0;" ::"n"(NA) : "memory"); }
+__device__ __forceinline__ void sync_output() { asm volatile("bar.sync 2, %0;" ::"n"(NC) : "memory"); }
 
 template <bool OUT, typename Tout>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-           const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v, Args a,
-           int multi)
+           const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
+           const __grid_constant__ CUtensorMap tm_o, Args a, int multi)
 {
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *full = bars + 0, *prep = bars + 3, *ops_ready = bars + 6, *p_ready = bars + 7;
-    uint64_t *mma1 = bars + 8, *mma2 = bars + 9, *fin = bars + 10;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+    uint64_t *mma_st = bars + 8, *mma1 = bars + 9, *mma2 = bars + 10, *o_free = bars + 11;   // o_free[2]
+    uint64_t *fin = bars + 13;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
 
     // the varlen slot table comes from the preceding plan kernel
     if (a.table || !OUT)
@@ -122,19 +127,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp == 0)
         tmem_alloc(tmem_slot, TM_COLS);
-    if (tid == NA + NB) {
+    if (tid == NA + NB + NC) {
         for (int s = 0; s < NSTAGE; ++s) {
             bar_init(&full[s], 1);
             bar_init(&prep[s], NA);
         }
         bar_init(ops_ready, NB);
         bar_init(p_ready, NB);
+        bar_init(mma_st, 1);
         bar_init(mma1, 1);
         bar_init(mma2, 1);
+        bar_init(&o_free[0], NC);
+        bar_init(&o_free[1], NC);
         bar_init(fin, 1);
         bar_fence_init();
-        if (OUT)
+        if (OUT) {
             tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_o);
+        }
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_g);
         tma_prefetch_desc(&tm_v);
@@ -147,7 +157,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
 
-    if (warp == 8) {
+    if (warp == WCTL) {
         // ---------------------------------------------------------------------- control: TMA + MMA
         if (lane == 0) {
             constexpr uint32_t tx = (OUT ? 4 : 3) * 16384;
@@ -159,10 +169,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 bar_expect_tx(&full[s], tx);
                 if (OUT) {
                     tma_load_3d(st + ST_Q0, &tm_q, 0, h, row0, &full[s]);
-                    tma_load_3d(st + ST_Q1, &tm_q, 64, h, row0, &full[s]);
+                    tma_load_3d(st + 16384 + ST_Q0, &tm_q, 64, h, row0, &full[s]);
                 }
                 tma_load_3d(st + ST_K0, &tm_k, 0, h, row0, &full[s]);
-                tma_load_3d(st + ST_K1, &tm_k, 64, h, row0, &full[s]);
+                tma_load_3d(st + 16384 + ST_K0, &tm_k, 64, h, row0, &full[s]);
                 tma_load_3d(st + ST_G, &tm_g, 0, h, row0, &full[s]);
                 tma_load_3d(st + ST_V, &tm_v, v0, h, row0, &full[s]);
                 last_issued[s] = c;
@@ -182,28 +192,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!(ok = bar_wait(ops_ready, ph)))
                     break;
                 fence_after();
-                if (OUT) {
-                    // (a) O^T = S'^T q~^T : A = S' (TMEM), B = q~ rows t, K = key
-                    for (int k = 0; k < KD / 16; ++k)
-                        mma_ts(tmem + TM_O, tmem + TM_SOP + k * 8,
-                               sdesc_sw128(st + (k >> 2) * 16384 + (k & 3) * 32), ID_N64, k > 0);
-                    // (b) P = q~ k~^T : A = q~ (128-row view), B = k~ rows s
-                    for (int k = 0; k < KD / 16; ++k)
-                        mma_ss(tmem + TM_P, sdesc_sw128(st + (k >> 2) * 16384 + (k & 3) * 32),
-                               sdesc_sw128(st + (k >> 2) * 16384 + ST_K0 + (k & 3) * 32), ID_N64, k > 0);
-                }
-                // (c) S^T += V^T k^^T : K = t
+                // (c) S^T += V^T k^^T : K = t (first, so the next chunk's state conversion can start early)
                 for (int k = 0; k < C / 16; ++k)
                     mma_ss(tmem + TM_S, sdesc_sw128(st + ST_V + k * 32), sdesc_sw128(st + ST_G + k * 32),
                            ID_N128, 1);
-                mma_commit(mma1);
+                mma_commit(mma_st);
                 if (OUT) {
+                    const uint32_t ob = tmem + TM_O + (c & 1) * 64;
+                    if (c >= 2 && !(ok = bar_wait(&o_free[c & 1], ((c - 2) >> 1) & 1)))
+                        break;
+                    fence_after();
+                    // (a) O^T = S'^T q~^T : A = S' (TMEM), B = q~ rows t, K = key
+                    for (int k = 0; k < KD / 16; ++k)
+                        mma_ts(ob, tmem + TM_SOP + (c & 1) * 64 + k * 8,
+                               sdesc_sw128(st + (k >> 2) * 16384 + ST_Q0 + (k & 3) * 32), ID_N64, k > 0);
+                    // (b) P = q~ k~^T : A = q~ (128-row view), B = k~ rows s
+                    for (int k = 0; k < KD / 16; ++k)
+                        mma_ss(tmem + TM_P, sdesc_sw128(st + (k >> 2) * 16384 + ST_Q0 + (k & 3) * 32),
+                               sdesc_sw128(st + (k >> 2) * 16384 + ST_K0 + (k & 3) * 32), ID_N64, k > 0);
+                    mma_commit(mma1);
                     if (!(ok = bar_wait(p_ready, ph)))
                         break;
                     fence_after();
                     // (d) O^T += V^T P^T : K = s
                     for (int k = 0; k < C / 16; ++k)
-                        mma_ss(tmem + TM_O, sdesc_sw128(st + ST_V + k * 32), sdesc_sw128(pt + k * 32), ID_N64, 1);
+                        mma_ss(ob, sdesc_sw128(st + ST_V + k * 32), sdesc_sw128(pt + k * 32), ID_N64, 1);
                 }
                 mma_commit(mma2);
             }
@@ -215,10 +228,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!ok || !drained)
                 report(a.status, GLA_ERR_TIMEOUT);
         }
-    } else if (warp < 4) {
-        // ---------------------------------------------------------------------- gating group
-        // thread: key pair kp (keys 2kp, 2kp+1; value columns likewise), row half rh (rows 32rh..32rh+31)
-        const int kp = tid & 63, rh = tid >> 6;
+    } else if (warp < WB) {
+        // ---------------------------------------------------------------------- gating group (8 warps)
+        // thread: key pair kp (keys 2kp, 2kp+1; value columns likewise), row quarter rq (rows 16rq..+15)
+        const int kp = tid & 63, rq = tid >> 6;
         const int key = 2 * kp;
         const int kb = key >> 6, kc = key & 63;   // K-block and column inside the 128-byte row
         float *psum = reinterpret_cast<float *>(sm + OFF_PS);
@@ -231,25 +244,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!(ok = bar_wait(&full[s], (c / NSTAGE) & 1)))
                 break;
             // pass 1: this thread's g and v rows into registers (rows >= len are zero)
-            uint32_t gr[32], vr[32];
+            uint32_t gr[16], vr[16];
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int t = 32 * rh + u;
+            for (int u = 0; u < 16; ++u) {
+                const int t = 16 * rq + u;
                 const bool in = t < len;
                 gr[u] = in ? *reinterpret_cast<const uint32_t *>(st + ST_G + t * 256 + kp * 4) : 0u;
                 vr[u] = in ? *reinterpret_cast<const uint32_t *>(st + ST_V + t * 256 + kp * 4) : 0u;
                 s0 += bf_lo(gr[u]);
                 s1 += bf_hi(gr[u]);
             }
-            float *ps = psum + (c & 1) * 256;
-            ps[rh * 128 + key] = s0;
-            ps[rh * 128 + key + 1] = s1;
+            float *ps = psum + (c & 1) * 512;
+            ps[rq * 128 + key] = s0;
+            ps[rq * 128 + key + 1] = s1;
             sync_gating();   // partial sums visible; every g / v tile read is done
-            const float ga0 = ps[key], ga1 = ps[key + 1];                        // G at the anchor row
-            const float gl0 = ga0 + ps[128 + key], gl1 = ga1 + ps[128 + key + 1];  // G at the last row
-            float G0 = rh ? ga0 : 0.f, G1 = rh ? ga1 : 0.f;
-            if (rh == 0) {
+            float p0[4], p1[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                p0[r] = ps[r * 128 + key];
+                p1[r] = ps[r * 128 + key + 1];
+            }
+            const float ga0 = p0[0] + p0[1], ga1 = p1[0] + p1[1];      // G at the anchor row (31)
+            const float gl0 = ga0 + (p0[2] + p0[3]), gl1 = ga1 + (p1[2] + p1[3]);   // G at the last row
+            float G0 = rq == 0 ? 0.f : rq == 1 ? p0[0] : rq == 2 ? ga0 : ga0 + p0[2];
+            float G1 = rq == 0 ? 0.f : rq == 1 ? p1[0] : rq == 2 ? ga1 : ga1 + p1[2];
+            if (rq == 0) {
                 float *eg = reinterpret_cast<float *>(sm + OFF_EG + s * 1024);
                 eg[key] = ex2(ga0 * L2E);
                 eg[key + 1] = ex2(ga1 * L2E);
@@ -260,19 +280,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             const float gaL0 = ga0 * L2E, gaL1 = ga1 * L2E, glL0 = gl0 * L2E, glL1 = gl1 * L2E;
             const float cl0 = ex2(glL0 - gaL0), cl1 = ex2(glL1 - gaL1);
-            uint32_t kh[32];
+            uint32_t kh[16];
             uint8_t *qk = st + kb * 16384;
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int t = 32 * rh + u;
+            for (int u = 0; u < 16; ++u) {
+                const int t = 16 * rq + u;
                 G0 += bf_lo(gr[u]);
                 G1 += bf_hi(gr[u]);
                 const float x0 = G0 * L2E, x1 = G1 * L2E;
                 const uint32_t off = sw128(t, kc);
+                const bool in = t < len;
                 if (OUT) {
                     const uint32_t qw = *reinterpret_cast<const uint32_t *>(qk + ST_Q0 + off);
                     const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
-                    const bool in = t < len;
                     const float e0 = ex2(x0 - gaL0), e1 = ex2(x1 - gaL1);
                     const float f0 = ex2(gaL0 - x0), f1 = ex2(gaL1 - x1);
                     const float q0 = in ? bf_lo(qw) * e0 : 0.f, q1 = in ? bf_hi(qw) * e1 : 0.f;
@@ -284,7 +304,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     kh[u] = pack_h2(k0 * cl0, k1 * cl1);
                 } else {
                     const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
-                    const bool in = t < len;
                     const float k0 = in ? bf_lo(kw) * ex2(glL0 - x0) : 0.f;
                     const float k1 = in ? bf_hi(kw) * ex2(glL1 - x1) : 0.f;
                     kh[u] = pack_h2(k0, k1);
@@ -294,10 +313,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 hmax = habs_max(hmax, vr[u]);
                 hmax = habs_max(hmax, kh[u]);
             }
-            // k^^T and V^T rows (key / value column 2kp and 2kp+1), columns t = 32rh.., over the g / v tiles
+            // k^^T and V^T rows (key / value column 2kp and 2kp+1), columns t = 16rq.., over the g / v tiles
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int t0 = 32 * rh + 8 * jj;
+            for (int jj = 0; jj < 2; ++jj) {
+                const int t0 = 16 * rq + 8 * jj;
                 uint32_t k_lo[4], k_hi[4], v_lo[4], v_hi[4];
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
@@ -316,7 +335,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             fence_proxy_async();
             bar_arrive(&prep[s]);
         }
-        if (ok && !OUT && vt == 0 && rh == 0) {
+        if (ok && !OUT && vt == 0 && rq == 0) {
             float *gt = a.gtot + ((size_t)j * H + h) * KD;
             gt[key] = gsum0;
             gt[key + 1] = gsum1;
@@ -326,8 +345,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             report(a.status, GLA_ERR_RANGE);
         if (!ok)
             report(a.status, GLA_ERR_TIMEOUT);
-    } else {
-        // ---------------------------------------------------------------------- TMEM group
+    } else if (warp < WC) {
+        // ---------------------------------------------------------------------- state group
         const int b = tid - NA;                                   // TMEM lane = value column (or row t)
         const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;
         float amax = 0.f;
@@ -371,13 +390,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             tmem_wait_st();
         }
-        Tout *go = static_cast<Tout *>(a.o);
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % NSTAGE;
             const uint32_t ph = c & 1;
-            const int row0 = bos + c * C;
-            const int len = min(C, eos - row0);
-            if (!OUT && c > 0 && !(ok = bar_wait(mma1, (c - 1) & 1)))
+            if (c > 0 && !(ok = bar_wait(mma_st, (c - 1) & 1)))   // the previous chunk's state update
                 break;
             if (!(ok = bar_wait(&prep[s], (c / NSTAGE) & 1)))
                 break;
@@ -398,7 +414,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         amax = fmaxf(amax, fmaxf(fabsf(s0), fabsf(s1)));
                         op[u] = pack_h2(s0, s1);
                     }
-                    tmem_st16(tmem + lrow + TM_SOP + kc * 16, op);
+                    tmem_st16(tmem + lrow + TM_SOP + (c & 1) * 64 + kc * 16, op);
                 }
 #pragma unroll
                 for (int u = 0; u < 32; u += 4) {
@@ -416,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!OUT)
                 continue;
 
-            // masked scores -> fp16 P[t][s] (lanes t < 64: warps 4 and 5)
+            // masked scores -> fp16 P[t][s] (lanes t < 64: the first two warps of the group)
             if (!(ok = bar_wait(mma1, ph)))
                 break;
             fence_after();
@@ -445,30 +461,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             fence_proxy_async();
             fence_before();
             bar_arrive(p_ready);
-
-            // output (thread = lane v): o[t, v] = scale * O^T[v][t]
-            if (!(ok = bar_wait(mma2, ph)))
-                break;
-            fence_after();
-            Tout *orow = go + ((size_t)row0 * H + h) * V + v0 + b;
-            const size_t rstride = (size_t)H * V;
-            for (int oc = 0; oc < 2; ++oc) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lrow + TM_O + oc * 32, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int t = oc * 32 + u;
-                    if (t < len)
-                        orow[(size_t)t * rstride] = to_out<Tout>(a.scale * __uint_as_float(r[u]));
-                }
-            }
-            fence_before();
         }
 
         // final state of the segment: ht (output pass, last segment) or dS (state pass)
         if (ok && nchunks > 0)
-            ok = bar_wait(mma1, (nchunks - 1) & 1);
+            ok = bar_wait(mma_st, (nchunks - 1) & 1);
         if (ok) {
             fence_after();
             float *dst = nullptr;
@@ -491,6 +488,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             report(a.status, GLA_ERR_TIMEOUT);
         if (!(amax <= 65000.f))
             report(a.status, GLA_ERR_RANGE);
+    } else if (OUT) {
+        // ---------------------------------------------------------------------- output group
+        const int b = tid - NA - NB;   // TMEM lane = value column
+        const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const bool leader = b == 0;
+        float *ost = reinterpret_cast<float *>(sm + OFF_OST);
+        Tout *go = static_cast<Tout *>(a.o);
+        const size_t rstride = (size_t)H * V;
+        for (int c = 0; c < nchunks; ++c) {
+            const int row0 = bos + c * C;
+            const int len = min(C, eos - row0);
+            if (!(ok = bar_wait(mma2, c & 1)))
+                break;
+            fence_after();
+            const uint32_t ob = tmem + lrow + TM_O + (c & 1) * 64;
+            const bool tma = sizeof(Tout) == 4 && len == C;
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                tmem_ld32(ob + half * 32, r);
+                tmem_wait_ld();
+                if (tma) {
+                    if (leader)
+                        bulk_wait_read();   // the previous store has read the staging buffer
+                    sync_output();
+#pragma unroll
+                    for (int u = 0; u < 32; ++u)
+                        ost[u * 128 + b] = a.scale * __uint_as_float(r[u]);
+                    fence_proxy_async();
+                    sync_output();
+                    if (leader) {
+                        tma_store_3d(&tm_o, ost, v0, h, row0 + half * 32);
+                        bulk_commit();
+                    }
+                } else {
+                    Tout *orow = go + ((size_t)row0 * H + h) * V + v0 + b;
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const int t = half * 32 + u;
+                        if (t < len)
+                            orow[(size_t)t * rstride] = to_out<Tout>(a.scale * __uint_as_float(r[u]));
+                    }
+                }
+            }
+            fence_before();
+            bar_arrive(&o_free[c & 1]);
+        }
+        if (leader)
+            bulk_wait_all();
+        if (!ok)
+            report(a.status, GLA_ERR_TIMEOUT);
     }
 
     fence_before();
@@ -515,29 +562,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// [rows][H][D] bf16 tensor; box = `inner` elements x 1 head x 64 rows.
-bool encode_rows(CUtensorMap *m, const void *ptr, int D, int H, long long rows, int inner, bool swizzle)
+// [rows][H][D] tensor of bf16 or fp32; box = `inner` elements x 1 head x `brows` rows.
+bool encode_rows(CUtensorMap *m, const void *ptr, int D, int H, long long rows, int inner, int brows, bool swizzle,
+                 bool f32 = false)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
+    const cuuint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-    cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)C};
-    cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es};
+    cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)brows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool OUT, typename Tout>
 cudaError_t launch_one(const Plan &pl, const Args &a, cudaStream_t s, bool pdl)
 {
     const long long rows = pl.varlen ? (long long)pl.T : (long long)pl.B * pl.T;
-    CUtensorMap mq, mk, mg, mv;
-    if (!encode_rows(&mq, a.q, pl.K, pl.H, rows, 64, true) || !encode_rows(&mk, a.k, pl.K, pl.H, rows, 64, true) ||
-        !encode_rows(&mg, a.g, pl.K, pl.H, rows, 128, false) ||
-        !encode_rows(&mv, a.v, pl.V, pl.H, rows, 128, false))
+    CUtensorMap mq, mk, mg, mv, mo;
+    if (!encode_rows(&mq, a.q, pl.K, pl.H, rows, 64, C, true) || !encode_rows(&mk, a.k, pl.K, pl.H, rows, 64, C, true) ||
+        !encode_rows(&mg, a.g, pl.K, pl.H, rows, 128, C, false) ||
+        !encode_rows(&mv, a.v, pl.V, pl.H, rows, 128, C, false))
+        return cudaErrorInvalidValue;
+    // o: fp32 rows, box 128 x 1 x 32 (the output group's 16 KB staging buffer); unused for bf16 o
+    if (!encode_rows(&mo, OUT && sizeof(Tout) == 4 ? a.o : a.v, pl.V, pl.H, rows, 128, 32, false,
+                     OUT && sizeof(Tout) == 4))
         return cudaErrorInvalidValue;
     auto f = gla_tc<OUT, Tout>;
     static bool attr = false;
@@ -558,7 +612,7 @@ cudaError_t launch_one(const Plan &pl, const Args &a, cudaStream_t s, bool pdl)
     cfg.attrs = attrs;
     cfg.numAttrs = pdl ? 1 : 0;
     int multi = pl.multi ? 1 : 0;
-    void *args[] = {&mq, &mk, &mg, &mv, const_cast<Args *>(&a), &multi};
+    void *args[] = {&mq, &mk, &mg, &mv, &mo, const_cast<Args *>(&a), &multi};
     cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(f), args);
     if (e != cudaSuccess)
         return e;
