@@ -6,7 +6,8 @@
 // the causally masked intra-chunk term with the inclusive diagonal (fwd_inner_chunk, the A @ v product of
 // FusedChunkGLAFunction.forward: kernel d), with scale applied to the sum.  Segments of a long sequence are
 // combined by the decayed scan S_in(p+1) = diag(exp(Gtot(p))) S_in(p) + dS(p) (kernel c), which the output
-// kernel evaluates in its prologue from the state pass's per-segment dS and Gtot.
+// kernel evaluates in its prologue from the state pass's per-segment dS and Gtot.  Gates are summed in log2
+// units (g * log2(e)) so every decay factor is one hardware exp2.
 //
 // One CTA owns one (segment, head, 128-wide value tile).  The K x V state lives in TMEM transposed
 // (lane = value column v, column = key dimension), so every MMA has M = 128:
@@ -17,20 +18,27 @@
 // with q~ = q*exp(G-G_a), k~ = k*exp(G_a-G), k^ = k*exp(G_last-G), S' = diag(exp(G_a)) S, and the anchor a
 // the middle row of the chunk.  Operands are fp16 (bf16 inputs widen exactly; 11-bit significands keep the
 // result within the parity bounds where single-rounded bf16 operands do not); accumulation is fp32 in TMEM.
+// The state pass walks its segment's chunks last to first and folds the decay of the later chunks into k^
+// (k * exp(G_last - G + later decay) <= |k|), so its state accumulates with no rescaling at all.
 //
 // Pipeline (one CTA per SM): three 64 KB stages hold a chunk's raw tiles and, converted in place, its
 // operands — TMA loads q and k already in the 128-byte-swizzled K-major layout the MMA reads, so q~ and k~
 // overwrite q and k element by element; k^^T and V^T are written over the g and v tiles once those have been
 // read into registers.  S' and O^T are double-buffered in TMEM so consecutive chunks overlap.  Warp roles:
 //   warps 0-7    gating group: cumsum and gating, running ahead of the tensor cores;
-//   warps 8-11   state group: state conversion (S', decay), masked scores -> P;
-//   warps 12-15  output group: O^T -> shared memory -> TMA tensor store (scalar stores for a ragged chunk);
+//   warps 8-11   state group: state conversion (S', decay) of the output pass;
+//   warps 12-15  output group: masked scores -> P, then O^T -> shared memory -> TMA tensor store (scalar
+//                stores for a ragged chunk);
 //   warp 16      lane 0 issues the TMA loads and the MMAs.
-// (Warps w of the state and output groups own TMEM lanes 32*(w%4)..+31.)  Every mbarrier wait is bounded; on
-// timeout the kernel records GLA_ERR_TIMEOUT, drains its own copies, stores and MMAs, frees TMEM and returns.
+// (Warps w of the state and output groups own TMEM lanes 32*(w%4)..+31.)  An operand that leaves the fp16
+// range makes the outputs non-finite; the kernels check o, ht and dS and report GLA_ERR_RANGE.  Every mbarrier
+// wait is bounded; on timeout the kernel records GLA_ERR_TIMEOUT, drains its own copies, stores and MMAs,
+// frees TMEM and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
+
+#include <type_traits>
 
 #include "gla_internal.h"
 #include "tc_ptx.cuh"
@@ -80,13 +88,7 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ uint32_t habs_max(uint32_t m, uint32_t h2)
-{
-    __half2 a = *reinterpret_cast<const __half2 *>(&m), b = *reinterpret_cast<const __half2 *>(&h2);
-    const __half2 r = __hmax2(a, __habs2(b));
-    return *reinterpret_cast<const uint32_t *>(&r);
-}
+__device__ __forceinline__ bool finite(float x) { return fabsf(x) <= 3.402823466e38f; }
 
 template <typename T>
 __device__ __forceinline__ T to_out(float x);
@@ -124,6 +126,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, V = a.V, v0 = vt * VT;
     const int nchunks = (eos - bos + C - 1) / C;
+    // chunk handled at step i: in order for the output pass, last to first for the state pass
+    auto chunk_of = [&](int i) { return OUT ? i : nchunks - 1 - i; };
 
     if (warp == 0)
         tmem_alloc(tmem_slot, TM_COLS);
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bar_init(&prep[s], NA);
         }
         bar_init(ops_ready, NB);
-        bar_init(p_ready, NB);
+        bar_init(p_ready, NC);
         bar_init(mma_st, 1);
         bar_init(mma1, 1);
         bar_init(mma2, 1);
@@ -162,10 +166,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             constexpr uint32_t tx = (OUT ? 4 : 3) * 16384;
             int last_issued[NSTAGE] = {-1, -1, -1};
-            auto issue = [&](int c) {
-                const int s = c % NSTAGE;
+            auto issue = [&](int i) {
+                const int s = i % NSTAGE;
                 uint8_t *st = sm + s * STAGE;
-                const int row0 = bos + c * C;
+                const int row0 = bos + chunk_of(i) * C;
                 bar_expect_tx(&full[s], tx);
                 if (OUT) {
                     tma_load_3d(st + ST_Q0, &tm_q, 0, h, row0, &full[s]);
@@ -175,36 +179,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tma_load_3d(st + 16384 + ST_K0, &tm_k, 64, h, row0, &full[s]);
                 tma_load_3d(st + ST_G, &tm_g, 0, h, row0, &full[s]);
                 tma_load_3d(st + ST_V, &tm_v, v0, h, row0, &full[s]);
-                last_issued[s] = c;
+                last_issued[s] = i;
             };
-            for (int c = 0; c < NSTAGE && c < nchunks; ++c)
-                issue(c);
+            for (int i = 0; i < NSTAGE && i < nchunks; ++i)
+                issue(i);
             const uint32_t pt = smem_u32(sm + OFF_P);
-            for (int c = 0; c < nchunks; ++c) {
-                const uint32_t ph = c & 1;
-                const uint32_t st = smem_u32(sm + (c % NSTAGE) * STAGE);
-                // refill the stage of chunk c-1 (once its MMAs are complete) with chunk c+2
-                if (c >= 1 && c + 2 < nchunks) {
-                    if (!(ok = bar_wait(mma2, (c - 1) & 1)))
+            for (int i = 0; i < nchunks; ++i) {
+                const uint32_t ph = i & 1;
+                const int s = i % NSTAGE;
+                const uint32_t st = smem_u32(sm + s * STAGE);
+                // refill the stage of step i-1 (once its MMAs are complete) with step i+2
+                if (i >= 1 && i + 2 < nchunks) {
+                    if (!(ok = bar_wait(mma2, (i - 1) & 1)))
                         break;
-                    issue(c + 2);
+                    issue(i + 2);
                 }
-                if (!(ok = bar_wait(ops_ready, ph)))
+                // output pass: the state group's conversion (which follows the gating); state pass: gating
+                if (!(ok = OUT ? bar_wait(ops_ready, ph) : bar_wait(&prep[s], (i / NSTAGE) & 1)))
                     break;
                 fence_after();
                 // (c) S^T += V^T k^^T : K = t (first, so the next chunk's state conversion can start early)
                 for (int k = 0; k < C / 16; ++k)
                     mma_ss(tmem + TM_S, sdesc_sw128(st + ST_V + k * 32), sdesc_sw128(st + ST_G + k * 32),
-                           ID_N128, 1);
+                           ID_N128, (OUT || i > 0 || k > 0) ? 1u : 0u);
                 mma_commit(mma_st);
                 if (OUT) {
-                    const uint32_t ob = tmem + TM_O + (c & 1) * 64;
-                    if (c >= 2 && !(ok = bar_wait(&o_free[c & 1], ((c - 2) >> 1) & 1)))
+                    const uint32_t ob = tmem + TM_O + (i & 1) * 64;
+                    if (i >= 2 && !(ok = bar_wait(&o_free[i & 1], ((i - 2) >> 1) & 1)))
                         break;
                     fence_after();
                     // (a) O^T = S'^T q~^T : A = S' (TMEM), B = q~ rows t, K = key
                     for (int k = 0; k < KD / 16; ++k)
-                        mma_ts(ob, tmem + TM_SOP + (c & 1) * 64 + k * 8,
+                        mma_ts(ob, tmem + TM_SOP + (i & 1) * 64 + k * 8,
                                sdesc_sw128(st + (k >> 2) * 16384 + ST_Q0 + (k & 3) * 32), ID_N64, k > 0);
                     // (b) P = q~ k~^T : A = q~ (128-row view), B = k~ rows s
                     for (int k = 0; k < KD / 16; ++k)
@@ -235,15 +241,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int key = 2 * kp;
         const int kb = key >> 6, kc = key & 63;   // K-block and column inside the 128-byte row
         float *psum = reinterpret_cast<float *>(sm + OFF_PS);
-        uint32_t hmax = 0;                         // |fp16 operand| maximum (half2)
-        float gsum0 = 0.f, gsum1 = 0.f;            // segment log-decay totals (state pass)
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c % NSTAGE;
+        float D0 = 0.f, D1 = 0.f;                  // state pass: decay (log2) of the chunks already done
+        for (int i = 0; i < nchunks; ++i) {
+            const int s = i % NSTAGE;
             uint8_t *st = sm + s * STAGE;
-            const int len = min(C, eos - (bos + c * C));
-            if (!(ok = bar_wait(&full[s], (c / NSTAGE) & 1)))
+            const int len = min(C, eos - (bos + chunk_of(i) * C));
+            if (!(ok = bar_wait(&full[s], (i / NSTAGE) & 1)))
                 break;
-            // pass 1: this thread's g and v rows into registers (rows >= len are zero)
+            // pass 1: this thread's g and v rows into registers (rows >= len are zero); log2 partial sums
             uint32_t gr[16], vr[16];
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -252,10 +257,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const bool in = t < len;
                 gr[u] = in ? *reinterpret_cast<const uint32_t *>(st + ST_G + t * 256 + kp * 4) : 0u;
                 vr[u] = in ? *reinterpret_cast<const uint32_t *>(st + ST_V + t * 256 + kp * 4) : 0u;
-                s0 += bf_lo(gr[u]);
-                s1 += bf_hi(gr[u]);
+                s0 = fmaf(bf_lo(gr[u]), L2E, s0);
+                s1 = fmaf(bf_hi(gr[u]), L2E, s1);
             }
-            float *ps = psum + (c & 1) * 512;
+            float *ps = psum + (i & 1) * 512;
             ps[rq * 128 + key] = s0;
             ps[rq * 128 + key + 1] = s1;
             sync_gating();   // partial sums visible; every g / v tile read is done
@@ -265,53 +270,62 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 p0[r] = ps[r * 128 + key];
                 p1[r] = ps[r * 128 + key + 1];
             }
-            const float ga0 = p0[0] + p0[1], ga1 = p1[0] + p1[1];      // G at the anchor row (31)
-            const float gl0 = ga0 + (p0[2] + p0[3]), gl1 = ga1 + (p1[2] + p1[3]);   // G at the last row
-            float G0 = rq == 0 ? 0.f : rq == 1 ? p0[0] : rq == 2 ? ga0 : ga0 + p0[2];
-            float G1 = rq == 0 ? 0.f : rq == 1 ? p1[0] : rq == 2 ? ga1 : ga1 + p1[2];
-            if (rq == 0) {
-                float *eg = reinterpret_cast<float *>(sm + OFF_EG + s * 1024);
-                eg[key] = ex2(ga0 * L2E);
-                eg[key + 1] = ex2(ga1 * L2E);
-                eg[128 + key] = ex2(gl0 * L2E);
-                eg[128 + key + 1] = ex2(gl1 * L2E);
-                gsum0 += gl0;
-                gsum1 += gl1;
-            }
-            const float gaL0 = ga0 * L2E, gaL1 = ga1 * L2E, glL0 = gl0 * L2E, glL1 = gl1 * L2E;
-            const float cl0 = ex2(glL0 - gaL0), cl1 = ex2(glL1 - gaL1);
+            const float ga0 = p0[0] + p0[1], ga1 = p1[0] + p1[1];                 // G(anchor = row 31)
+            const float gl0 = ga0 + (p0[2] + p0[3]), gl1 = ga1 + (p1[2] + p1[3]);   // G(last row)
+            float X0 = rq == 0 ? 0.f : rq == 1 ? p0[0] : rq == 2 ? ga0 : ga0 + p0[2];
+            float X1 = rq == 0 ? 0.f : rq == 1 ? p1[0] : rq == 2 ? ga1 : ga1 + p1[2];
             uint32_t kh[16];
             uint8_t *qk = st + kb * 16384;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int t = 16 * rq + u;
-                G0 += bf_lo(gr[u]);
-                G1 += bf_hi(gr[u]);
-                const float x0 = G0 * L2E, x1 = G1 * L2E;
-                const uint32_t off = sw128(t, kc);
-                const bool in = t < len;
-                if (OUT) {
-                    const uint32_t qw = *reinterpret_cast<const uint32_t *>(qk + ST_Q0 + off);
-                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
-                    const float e0 = ex2(x0 - gaL0), e1 = ex2(x1 - gaL1);
-                    const float f0 = ex2(gaL0 - x0), f1 = ex2(gaL1 - x1);
-                    const float q0 = in ? bf_lo(qw) * e0 : 0.f, q1 = in ? bf_hi(qw) * e1 : 0.f;
-                    const float k0 = in ? bf_lo(kw) * f0 : 0.f, k1 = in ? bf_hi(kw) * f1 : 0.f;
-                    const uint32_t qh = pack_h2(q0, q1), kth = pack_h2(k0, k1);
-                    *reinterpret_cast<uint32_t *>(qk + ST_Q0 + off) = qh;
-                    *reinterpret_cast<uint32_t *>(qk + ST_K0 + off) = kth;
-                    hmax = habs_max(habs_max(hmax, qh), kth);
-                    kh[u] = pack_h2(k0 * cl0, k1 * cl1);
-                } else {
-                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
-                    const float k0 = in ? bf_lo(kw) * ex2(glL0 - x0) : 0.f;
-                    const float k1 = in ? bf_hi(kw) * ex2(glL1 - x1) : 0.f;
-                    kh[u] = pack_h2(k0, k1);
+            if (OUT) {
+                if (rq == 0) {
+                    float *eg = reinterpret_cast<float *>(sm + OFF_EG + s * 1024);
+                    eg[key] = ex2(ga0);
+                    eg[key + 1] = ex2(ga1);
+                    eg[128 + key] = ex2(gl0);
+                    eg[128 + key + 1] = ex2(gl1);
                 }
-                // v: bf16 -> fp16 (exact within the fp16 range)
-                vr[u] = pack_h2(bf_lo(vr[u]), bf_hi(vr[u]));
-                hmax = habs_max(hmax, vr[u]);
-                hmax = habs_max(hmax, kh[u]);
+                const float cl0 = ex2(gl0 - ga0), cl1 = ex2(gl1 - ga1);
+                auto gate = [&](auto full_tag) {
+                    constexpr bool FULL = decltype(full_tag)::value;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int t = 16 * rq + u;
+                        X0 = fmaf(bf_lo(gr[u]), L2E, X0);
+                        X1 = fmaf(bf_hi(gr[u]), L2E, X1);
+                        const uint32_t off = sw128(t, kc);
+                        const uint32_t qw = *reinterpret_cast<const uint32_t *>(qk + ST_Q0 + off);
+                        const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
+                        float q0 = bf_lo(qw) * ex2(X0 - ga0), q1 = bf_hi(qw) * ex2(X1 - ga1);
+                        float k0 = bf_lo(kw) * ex2(ga0 - X0), k1 = bf_hi(kw) * ex2(ga1 - X1);
+                        if (!FULL && t >= len)
+                            q0 = q1 = k0 = k1 = 0.f;
+                        *reinterpret_cast<uint32_t *>(qk + ST_Q0 + off) = pack_h2(q0, q1);
+                        *reinterpret_cast<uint32_t *>(qk + ST_K0 + off) = pack_h2(k0, k1);
+                        kh[u] = pack_h2(k0 * cl0, k1 * cl1);
+                        vr[u] = pack_h2(bf_lo(vr[u]), bf_hi(vr[u]));   // bf16 -> fp16
+                    }
+                };
+                if (len == C)
+                    gate(std::true_type{});
+                else
+                    gate(std::false_type{});
+            } else {
+                // k^ = k * 2^(G_last - G + D): this chunk's decay to its end, then the later chunks' decay
+                const float e0 = gl0 + D0, e1 = gl1 + D1;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int t = 16 * rq + u;
+                    X0 = fmaf(bf_lo(gr[u]), L2E, X0);
+                    X1 = fmaf(bf_hi(gr[u]), L2E, X1);
+                    const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + sw128(t, kc));
+                    const bool in = t < len;
+                    const float k0 = in ? bf_lo(kw) * ex2(e0 - X0) : 0.f;
+                    const float k1 = in ? bf_hi(kw) * ex2(e1 - X1) : 0.f;
+                    kh[u] = pack_h2(k0, k1);
+                    vr[u] = pack_h2(bf_lo(vr[u]), bf_hi(vr[u]));
+                }
+                D0 = e0;
+                D1 = e1;
             }
             // k^^T and V^T rows (key / value column 2kp and 2kp+1), columns t = 16rq.., over the g / v tiles
 #pragma unroll
@@ -336,20 +350,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             bar_arrive(&prep[s]);
         }
         if (ok && !OUT && vt == 0 && rq == 0) {
-            float *gt = a.gtot + ((size_t)j * H + h) * KD;
-            gt[key] = gsum0;
-            gt[key + 1] = gsum1;
+            float *gt = a.gtot + ((size_t)j * H + h) * KD;   // total decay of the segment, log2 units
+            gt[key] = D0;
+            gt[key + 1] = D1;
         }
-        const __half2 hm = *reinterpret_cast<const __half2 *>(&hmax);
-        if (!(fmaxf(__low2float(hm), __high2float(hm)) <= 65000.f))
-            report(a.status, GLA_ERR_RANGE);
         if (!ok)
             report(a.status, GLA_ERR_TIMEOUT);
     } else if (warp < WC) {
         // ---------------------------------------------------------------------- state group
-        const int b = tid - NA;                                   // TMEM lane = value column (or row t)
+        const int b = tid - NA;                                   // TMEM lane = value column
         const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        float amax = 0.f;
         // initial state of the segment -> TMEM (S^T[v][key] = S[key][v])
         {
             const size_t hoff = ((size_t)n * H + h) * KD * V;
@@ -367,7 +377,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (several)
                 grid_dep_wait();   // h0 copy and per-segment contributions come from the state pass
             const int j0 = j - p;
-            for (int kc = 0; kc < KD / 32; ++kc) {
+            // (the state pass starts its accumulator with the first MMA instead)
+            for (int kc = 0; OUT && kc < KD / 32; ++kc) {
                 uint32_t r[32];
                 float acc[32];
 #pragma unroll
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const float *gt = a.gtot + jm * KD + kc * 32;
 #pragma unroll
                         for (int u = 0; u < 32; ++u)
-                            acc[u] = fmaf(ex2(__ldg(gt + u) * L2E), acc[u], __ldg(dS + (size_t)u * V));
+                            acc[u] = fmaf(ex2(__ldg(gt + u)), acc[u], __ldg(dS + (size_t)u * V));
                     }
                 }
 #pragma unroll
@@ -388,52 +399,101 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     r[u] = __float_as_uint(acc[u]);
                 tmem_st32(tmem + lrow + TM_S + kc * 32, r);
             }
-            tmem_wait_st();
+            if (OUT)
+                tmem_wait_st();
         }
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c % NSTAGE;
-            const uint32_t ph = c & 1;
-            if (c > 0 && !(ok = bar_wait(mma_st, (c - 1) & 1)))   // the previous chunk's state update
-                break;
-            if (!(ok = bar_wait(&prep[s], (c / NSTAGE) & 1)))
-                break;
-            fence_after();
-            const float *eg = reinterpret_cast<const float *>(sm + OFF_EG + s * 1024);
-            // S' = diag(exp(G_a)) S (fp16 operand); S <- diag(exp(G_last)) S
-            for (int kc = 0; kc < KD / 32; ++kc) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lrow + TM_S + kc * 32, r);
-                tmem_wait_ld();
-                if (OUT) {
-                    uint32_t op[16];
+        if (OUT) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % NSTAGE;
+                if (c > 0 && !(ok = bar_wait(mma_st, (c - 1) & 1)))   // the previous chunk's state update
+                    break;
+                if (!(ok = bar_wait(&prep[s], (c / NSTAGE) & 1)))
+                    break;
+                fence_after();
+                const float *eg = reinterpret_cast<const float *>(sm + OFF_EG + s * 1024);
+                // S' = diag(exp(G_a)) S (fp16 operand); S <- diag(exp(G_last)) S; 16 columns at a time with
+                // the next load in flight
+                uint32_t r[16], rn[16];
+                tmem_ld16(tmem + lrow + TM_S, r);
+                tmem_wait_ld(r);
+                for (int q = 0; q < KD / 16; ++q) {
+                    if (q + 1 < KD / 16)
+                        tmem_ld16(tmem + lrow + TM_S + (q + 1) * 16, rn);
+                    uint32_t op[8];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const float2 e = *reinterpret_cast<const float2 *>(eg + kc * 32 + 2 * u);
-                        const float s0 = __uint_as_float(r[2 * u]) * e.x;
-                        const float s1 = __uint_as_float(r[2 * u + 1]) * e.y;
-                        amax = fmaxf(amax, fmaxf(fabsf(s0), fabsf(s1)));
-                        op[u] = pack_h2(s0, s1);
+                    for (int u = 0; u < 8; ++u) {
+                        const float2 e = *reinterpret_cast<const float2 *>(eg + q * 16 + 2 * u);
+                        op[u] = pack_h2(__uint_as_float(r[2 * u]) * e.x, __uint_as_float(r[2 * u + 1]) * e.y);
                     }
-                    tmem_st16(tmem + lrow + TM_SOP + (c & 1) * 64 + kc * 16, op);
-                }
 #pragma unroll
-                for (int u = 0; u < 32; u += 4) {
-                    const float4 e = *reinterpret_cast<const float4 *>(eg + 128 + kc * 32 + u);
-                    r[u] = __float_as_uint(__uint_as_float(r[u]) * e.x);
-                    r[u + 1] = __float_as_uint(__uint_as_float(r[u + 1]) * e.y);
-                    r[u + 2] = __float_as_uint(__uint_as_float(r[u + 2]) * e.z);
-                    r[u + 3] = __float_as_uint(__uint_as_float(r[u + 3]) * e.w);
+                    for (int u = 0; u < 16; u += 4) {
+                        const float4 e = *reinterpret_cast<const float4 *>(eg + 128 + q * 16 + u);
+                        r[u] = __float_as_uint(__uint_as_float(r[u]) * e.x);
+                        r[u + 1] = __float_as_uint(__uint_as_float(r[u + 1]) * e.y);
+                        r[u + 2] = __float_as_uint(__uint_as_float(r[u + 2]) * e.z);
+                        r[u + 3] = __float_as_uint(__uint_as_float(r[u + 3]) * e.w);
+                    }
+                    tmem_st8(tmem + lrow + TM_SOP + (c & 1) * 64 + q * 8, op);
+                    tmem_st16(tmem + lrow + TM_S + q * 16, r);
+                    if (q + 1 < KD / 16) {
+                        tmem_wait_ld(rn);
+#pragma unroll
+                        for (int u = 0; u < 16; ++u)
+                            r[u] = rn[u];
+                    }
                 }
-                tmem_st32(tmem + lrow + TM_S + kc * 32, r);
+                tmem_wait_st();
+                fence_before();
+                bar_arrive(ops_ready);
             }
-            tmem_wait_st();
-            fence_before();
-            bar_arrive(ops_ready);
-            if (!OUT)
-                continue;
+        }
 
+        // final state of the segment: ht (output pass, last segment) or dS (state pass), once every MMA
+        // is complete.  (`fin` completes a single phase; the per-chunk barriers cannot be used here because
+        // a parity wait only tells the current phase from the one before it, and the state pass's MMAs may
+        // run any number of phases ahead of this group.)
+        if (ok)
+            ok = bar_wait(fin, 0);
+        if (ok) {
+            fence_after();
+            float *dst = nullptr;
+            if (OUT)
+                dst = (eos == send && a.ht) ? a.ht + ((size_t)n * H + h) * KD * V : nullptr;
+            else
+                dst = a.ss + ((size_t)j * H + h) * KD * V;
+            if (dst) {
+                bool fin_ok = true;
+                for (int kc = 0; kc < KD / 32; ++kc) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lrow + TM_S + kc * 32, r);
+                    tmem_wait_ld(r);
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const float x = __uint_as_float(r[u]);
+                        fin_ok &= finite(x);
+                        dst[(size_t)(kc * 32 + u) * V + v0 + b] = x;
+                    }
+                }
+                if (!fin_ok)
+                    report(a.status, GLA_ERR_RANGE);
+            }
+        }
+        if (!ok)
+            report(a.status, GLA_ERR_TIMEOUT);
+    } else if (OUT) {
+        // ---------------------------------------------------------------------- output group
+        const int b = tid - NA - NB;   // TMEM lane: row t of P, value column of O^T
+        const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const bool leader = b == 0;
+        float *ost = reinterpret_cast<float *>(sm + OFF_OST);
+        Tout *go = static_cast<Tout *>(a.o);
+        const size_t rstride = (size_t)H * V;
+        bool fin_ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const int row0 = bos + c * C;
+            const int len = min(C, eos - row0);
             // masked scores -> fp16 P[t][s] (lanes t < 64: the first two warps of the group)
-            if (!(ok = bar_wait(mma1, ph)))
+            if (!(ok = bar_wait(mma1, c & 1)))
                 break;
             fence_after();
             if ((warp & 3) < 2) {
@@ -441,7 +501,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int sc = 0; sc < 2; ++sc) {
                     uint32_t r[32];
                     tmem_ld32(tmem + lrow + TM_P + sc * 32, r);
-                    tmem_wait_ld();
+                    tmem_wait_ld(r);
 #pragma unroll
                     for (int u0 = 0; u0 < 32; u0 += 8) {
                         uint32_t pk[4];
@@ -450,7 +510,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             const int sa = sc * 32 + u0 + u;
                             const float p0 = sa <= t ? __uint_as_float(r[u0 + u]) : 0.f;
                             const float p1 = sa + 1 <= t ? __uint_as_float(r[u0 + u + 1]) : 0.f;
-                            amax = fmaxf(amax, fmaxf(fabsf(p0), fabsf(p1)));
                             pk[u / 2] = pack_h2(p0, p1);
                         }
                         *reinterpret_cast<uint4 *>(sm + OFF_P + sw128(t, sc * 32 + u0)) =
@@ -461,44 +520,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             fence_proxy_async();
             fence_before();
             bar_arrive(p_ready);
-        }
 
-        // final state of the segment: ht (output pass, last segment) or dS (state pass)
-        if (ok && nchunks > 0)
-            ok = bar_wait(mma_st, (nchunks - 1) & 1);
-        if (ok) {
-            fence_after();
-            float *dst = nullptr;
-            if (OUT)
-                dst = (eos == send && a.ht) ? a.ht + ((size_t)n * H + h) * KD * V : nullptr;
-            else
-                dst = a.ss + ((size_t)j * H + h) * KD * V;
-            if (dst) {
-                for (int kc = 0; kc < KD / 32; ++kc) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lrow + TM_S + kc * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int u = 0; u < 32; ++u)
-                        dst[(size_t)(kc * 32 + u) * V + v0 + b] = __uint_as_float(r[u]);
-                }
-            }
-        }
-        if (!ok)
-            report(a.status, GLA_ERR_TIMEOUT);
-        if (!(amax <= 65000.f))
-            report(a.status, GLA_ERR_RANGE);
-    } else if (OUT) {
-        // ---------------------------------------------------------------------- output group
-        const int b = tid - NA - NB;   // TMEM lane = value column
-        const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const bool leader = b == 0;
-        float *ost = reinterpret_cast<float *>(sm + OFF_OST);
-        Tout *go = static_cast<Tout *>(a.o);
-        const size_t rstride = (size_t)H * V;
-        for (int c = 0; c < nchunks; ++c) {
-            const int row0 = bos + c * C;
-            const int len = min(C, eos - row0);
+            // output: o[t, v] = scale * O^T[v][t]
             if (!(ok = bar_wait(mma2, c & 1)))
                 break;
             fence_after();
@@ -507,14 +530,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int half = 0; half < 2; ++half) {
                 uint32_t r[32];
                 tmem_ld32(ob + half * 32, r);
-                tmem_wait_ld();
+                tmem_wait_ld(r);
                 if (tma) {
                     if (leader)
                         bulk_wait_read();   // the previous store has read the staging buffer
                     sync_output();
 #pragma unroll
-                    for (int u = 0; u < 32; ++u)
-                        ost[u * 128 + b] = a.scale * __uint_as_float(r[u]);
+                    for (int u = 0; u < 32; ++u) {
+                        const float x = a.scale * __uint_as_float(r[u]);
+                        fin_ok &= finite(x);
+                        ost[u * 128 + b] = x;
+                    }
                     fence_proxy_async();
                     sync_output();
                     if (leader) {
@@ -526,8 +552,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const int t = half * 32 + u;
-                        if (t < len)
-                            orow[(size_t)t * rstride] = to_out<Tout>(a.scale * __uint_as_float(r[u]));
+                        const float x = a.scale * __uint_as_float(r[u]);
+                        if (t < len) {
+                            fin_ok &= finite(x);
+                            orow[(size_t)t * rstride] = to_out<Tout>(x);
+                        }
                     }
                 }
             }
@@ -536,6 +565,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (leader)
             bulk_wait_all();
+        if (!fin_ok)
+            report(a.status, GLA_ERR_RANGE);
         if (!ok)
             report(a.status, GLA_ERR_TIMEOUT);
     }
