@@ -89,6 +89,13 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ bool finite(float x) { return fabsf(x) <= 3.402823466e38f; }
+// running max of |x| that keeps NaN (a single max.NaN per element)
+__device__ __forceinline__ float amax_nan(float m, float x)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(fabsf(x)));
+    return r;
+}
 
 template <typename T>
 __device__ __forceinline__ T to_out(float x);
@@ -285,6 +292,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     eg[128 + key + 1] = ex2(gl1);
                 }
                 const float cl0 = ex2(gl0 - ga0), cl1 = ex2(gl1 - ga1);
+                // X relative to the anchor; swizzled offsets of this thread's column in rows 16rq + u
+                X0 -= ga0;
+                X1 -= ga1;
+                uint32_t xo[8];
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    xo[w] = sw128(16 * rq + w, kc);
                 auto gate = [&](auto full_tag) {
                     constexpr bool FULL = decltype(full_tag)::value;
 #pragma unroll
@@ -292,11 +306,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const int t = 16 * rq + u;
                         X0 = fmaf(bf_lo(gr[u]), L2E, X0);
                         X1 = fmaf(bf_hi(gr[u]), L2E, X1);
-                        const uint32_t off = sw128(t, kc);
+                        const uint32_t off = xo[u & 7] + (u >> 3) * 1024;
                         const uint32_t qw = *reinterpret_cast<const uint32_t *>(qk + ST_Q0 + off);
                         const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
-                        float q0 = bf_lo(qw) * ex2(X0 - ga0), q1 = bf_hi(qw) * ex2(X1 - ga1);
-                        float k0 = bf_lo(kw) * ex2(ga0 - X0), k1 = bf_hi(kw) * ex2(ga1 - X1);
+                        float q0 = bf_lo(qw) * ex2(X0), q1 = bf_hi(qw) * ex2(X1);
+                        float k0 = bf_lo(kw) * ex2(-X0), k1 = bf_hi(kw) * ex2(-X1);
                         if (!FULL && t >= len)
                             q0 = q1 = k0 = k1 = 0.f;
                         *reinterpret_cast<uint32_t *>(qk + ST_Q0 + off) = pack_h2(q0, q1);
@@ -413,12 +427,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const float *eg = reinterpret_cast<const float *>(sm + OFF_EG + s * 1024);
                 // S' = diag(exp(G_a)) S (fp16 operand); S <- diag(exp(G_last)) S; 16 columns at a time with
                 // the next load in flight
-                uint32_t r[16], rn[16];
-                tmem_ld16(tmem + lrow + TM_S, r);
-                tmem_wait_ld(r);
-                for (int q = 0; q < KD / 16; ++q) {
-                    if (q + 1 < KD / 16)
-                        tmem_ld16(tmem + lrow + TM_S + (q + 1) * 16, rn);
+                uint32_t ra[16], rb[16];
+                auto convert = [&](uint32_t(&r)[16], int q) {
                     uint32_t op[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
@@ -435,12 +445,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                     tmem_st8(tmem + lrow + TM_SOP + (c & 1) * 64 + q * 8, op);
                     tmem_st16(tmem + lrow + TM_S + q * 16, r);
-                    if (q + 1 < KD / 16) {
-                        tmem_wait_ld(rn);
-#pragma unroll
-                        for (int u = 0; u < 16; ++u)
-                            r[u] = rn[u];
-                    }
+                };
+                // two 16-column blocks per step, the next block's load in flight while one is converted
+                tmem_ld16(tmem + lrow + TM_S, ra);
+                tmem_wait_ld(ra);
+#pragma unroll 1
+                for (int q = 0; q < KD / 16; q += 2) {
+                    tmem_ld16(tmem + lrow + TM_S + (q + 1) * 16, rb);
+                    convert(ra, q);
+                    tmem_wait_ld(rb);
+                    if (q + 2 < KD / 16)
+                        tmem_ld16(tmem + lrow + TM_S + (q + 2) * 16, ra);
+                    convert(rb, q + 1);
+                    if (q + 2 < KD / 16)
+                        tmem_wait_ld(ra);
                 }
                 tmem_wait_st();
                 fence_before();
@@ -488,7 +506,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float *ost = reinterpret_cast<float *>(sm + OFF_OST);
         Tout *go = static_cast<Tout *>(a.o);
         const size_t rstride = (size_t)H * V;
-        bool fin_ok = true;
+        float omax = 0.f;
         for (int c = 0; c < nchunks; ++c) {
             const int row0 = bos + c * C;
             const int len = min(C, eos - row0);
@@ -538,7 +556,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int u = 0; u < 32; ++u) {
                         const float x = a.scale * __uint_as_float(r[u]);
-                        fin_ok &= finite(x);
+                        omax = amax_nan(omax, x);
                         ost[u * 128 + b] = x;
                     }
                     fence_proxy_async();
@@ -554,7 +572,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const int t = half * 32 + u;
                         const float x = a.scale * __uint_as_float(r[u]);
                         if (t < len) {
-                            fin_ok &= finite(x);
+                            omax = amax_nan(omax, x);
                             orow[(size_t)t * rstride] = to_out<Tout>(x);
                         }
                     }
@@ -565,7 +583,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (leader)
             bulk_wait_all();
-        if (!fin_ok)
+        if (!finite(omax))
             report(a.status, GLA_ERR_RANGE);
         if (!ok)
             report(a.status, GLA_ERR_TIMEOUT);

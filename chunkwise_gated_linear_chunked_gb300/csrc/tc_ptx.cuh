@@ -209,10 +209,12 @@ __device__ __forceinline__ void bar_expect_tx(uint64_t *bar, uint32_t bytes)
 __device__ __forceinline__ bool bar_try(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+    // the suspend-time hint (ns) lets a waiting warp sleep instead of competing for issue slots; the thread
+    // resumes as soon as the phase completes
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}\n"
                  : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
                  : "memory");
     return ok != 0;
 }
