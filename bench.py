@@ -34,7 +34,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel name -> source file that defines it (a traffic figure is only reused while that file is unchanged)
 KERNEL_SOURCES = {"out_ffma": "csrc/ffma_kernels.cu", "state_ffma": "csrc/ffma_kernels.cu",
                   "scan_segments": "csrc/ffma_kernels.cu", "plan_varlen": "csrc/ffma_kernels.cu",
-                  "out_tc": "csrc/tc_kernels.cu", "state_tc": "csrc/tc_kernels.cu"}
+                  "fused_tc": "csrc/tc_fused.cu"}
 
 
 def parse_args(argv=None):
@@ -347,9 +347,9 @@ def whole_job_value(tokens_per_step, steps, world, total_ms):
 
 
 def kernel_algorithmic_bytes(name, wu):
-    if name in ("out_ffma", "out_tc"):
+    if name in ("out_ffma", "fused_tc"):
         return wu["bytes"]
-    if name in ("state_ffma", "state_tc"):
+    if name == "state_ffma":
         return wu["in_bytes"]   # upper bound: k, g, v of the non-final segments are a subset
     return wu["state_bytes"]
 

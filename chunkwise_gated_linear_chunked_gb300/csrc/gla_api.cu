@@ -15,6 +15,23 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+long long l2_bytes()
+{
+    static std::mutex mu;
+    static long long cache[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
+        return 126LL << 20;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0)
+            n = 126 << 20;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 int sm_count()
 {
     static std::mutex mu;
@@ -73,41 +90,27 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
         whole = C;
     long long L = whole;
     if (pl.tc && rows > 0) {
-        // Tensor path, one CTA per SM: pick the segment length with the lowest modelled time, counted in
-        // chunk-times of one CTA: whole waves of the output pass, plus (with more than one segment) the
-        // state pass at ~0.6 of a chunk-time per chunk, the output prologue's scan over earlier segments
-        // and a fixed launch/tail cost.
+        // Fused tensor-core kernel (one persistent CTA per SM).  A segment that is not the last of its
+        // sequence is read twice (state pass, then output pass): keep its k, g and v (768 bytes per row of
+        // one 128-wide value tile) in about half of L2 across all SMs.  Dense batches are split only when
+        // the (sequence, head, value tile) items alone leave SMs idle; then into the fewest segments that
+        // fill the GPU in one wave, or the L2-sized segments if those are more.
         const long long sms = sm_count();
         const long long nv = pl.NV;
-        double best = 1e300;
-        for (long long m = 2;; m = (m < 8 ? m + 1 : m + (m >> 2))) {
-            const long long Lc = std::min<long long>(m * C, whole);   // the last candidate is `whole`
-            if (!varlen && (T + Lc - 1) / Lc > kMaxSegments)
-                continue;   // the output prologue reads every earlier segment: keep that quadratic cost small
-            if (varlen && Lc < 8 * C && Lc < whole)
-                continue;   // lengths are unknown here: no segments shorter than 8 chunks
-            long long units, state_units;
-            if (varlen) {
-                const long long J = std::min<long long>((long long)N * kMaxSegments, (long long)N + (T + Lc - 1) / Lc);
-                units = J * H * nv;
-                state_units = Lc < T ? (J - N) * H * nv : 0;
-            } else {
-                const long long P = (T + Lc - 1) / Lc;
-                units = (long long)B * P * H * nv;
-                state_units = (long long)B * (P - 1) * H * nv;
-            }
-            const double chunks = (double)(Lc / C);
-            double cost = (double)((units + sms - 1) / sms) * chunks;
-            if (state_units > 0) {
-                const double segs = (double)(state_units / ((long long)std::max(1, varlen ? N : B) * H * nv) + 1);
-                cost += 0.6 * (double)((state_units + sms - 1) / sms) * chunks + 2.0 + 0.3 * segs;
-            }
-            if (cost < best - 1e-9) {
-                best = cost;
-                L = Lc;
-            }
-            if (Lc == whole)
-                break;
+        long long Ll2 = (l2_bytes() / 2) / (sms * 768) / C * C;
+        if (Ll2 < 4 * C)
+            Ll2 = 4 * C;
+        if (varlen) {
+            L = std::min(Ll2, whole);
+        } else {
+            const long long units1 = (long long)B * H * nv;
+            const long long pmin = (T + Ll2 - 1) / Ll2;
+            long long P = 1;
+            if (units1 < sms)
+                P = units1 * pmin >= sms ? pmin : std::max(pmin, sms / units1);
+            L = ((T + P - 1) / P + C - 1) / C * C;
+            if (L > whole)
+                L = whole;
         }
     } else if (base < target && rows > 0) {
         long long per = (rows * H * pl.NV + target - 1) / target;   // rows per CTA
@@ -121,7 +124,7 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
     pl.L = (int)L;
     if (varlen) {
         pl.P = 0;
-        pl.J = (int)std::min<long long>((long long)N * kMaxSegments, (long long)N + (T + L - 1) / L);
+        pl.J = N + (int)((T + L - 1) / L);
         pl.multi = L < T;
     } else {
         pl.P = T > 0 ? (int)((T + L - 1) / L) : 1;
@@ -141,11 +144,14 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
     if (pl.multi)
         off += align_up(sizeof(float) * (size_t)pl.J * H * K * V);
     pl.off_gtot = off;
-    if (pl.multi)
+    if (pl.multi && !pl.tc)
         off += align_up(sizeof(float) * (size_t)pl.J * H * K);
-    pl.off_h0c = off;
-    if (pl.multi && pl.tc)
-        off += align_up(sizeof(float) * (size_t)N * H * K * V);
+    // the fused kernel's work counters live in the fixed header (status word at byte 0, counters at 16),
+    // so they mean the same thing whatever the layout of the previous call that used this workspace
+    pl.off_ctr = 16;
+    pl.off_flags = off;
+    if (pl.tc && pl.multi)
+        off += align_up(sizeof(int) * (size_t)pl.J * H * pl.NV);
     pl.total = off;
 }
 
@@ -158,7 +164,7 @@ struct Profile {
 };
 thread_local Profile g_prof;
 
-enum KernelId { K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_STATE_TC = 5, K_OUT_TC = 6 };
+enum KernelId { K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_FUSED_TC = 7 };
 
 // Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
 template <typename Fn>
@@ -272,7 +278,7 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     std::memset(&a, 0, sizeof a);
     a.q = q; a.k = k; a.v = v; a.g = g; a.o = o; a.h0 = h0; a.ht = ht; a.cu = cu_seqlens;
     a.scale = scale;
-    a.seg_cap = kMaxSegments;
+    a.seg_cap = 0;
     a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.N = N; a.L = pl.L; a.P = pl.P; a.J = pl.J;
     a.status = reinterpret_cast<int *>(ws + pl.off_status);
     if (varlen) {
@@ -281,32 +287,36 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     }
     if (pl.multi) {
         a.ss = reinterpret_cast<float *>(ws + pl.off_ss);
-        a.gtot = reinterpret_cast<float *>(ws + pl.off_gtot);
-        if (pl.tc)
-            a.h0c = reinterpret_cast<float *>(ws + pl.off_h0c);
+        if (!pl.tc)
+            a.gtot = reinterpret_cast<float *>(ws + pl.off_gtot);
+    }
+    if (pl.tc) {
+        a.ctr = reinterpret_cast<int *>(ws + pl.off_ctr);
+        if (pl.multi)
+            a.flags = reinterpret_cast<int *>(ws + pl.off_flags);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     g_prof.launches = 0;
     if (varlen && profiled(K_PLAN, s, [&] { return launch_plan_varlen(pl, a, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;
-    if (pl.multi) {
-        if (pl.tc) {
-            // the output kernel evaluates the segment scan in its prologue
-            if (profiled(K_STATE_TC, s, [&] { return launch_state_tc(pl, a, s); }) != cudaSuccess)
-                return GLA_ERR_CUDA;
-        } else {
-            if (profiled(K_STATE_FFMA, s, [&] { return launch_state_ffma(pl, a, s); }) != cudaSuccess)
-                return GLA_ERR_CUDA;
-            if (profiled(K_SCAN, s, [&] { return launch_scan(pl, a, s); }) != cudaSuccess)
-                return GLA_ERR_CUDA;
-        }
-    }
     if (pl.tc) {
-        if (profiled(K_OUT_TC, s, [&] { return launch_out_tc(pl, a, s); }) != cudaSuccess)
+        // one persistent kernel: state pass, chained segment scan and output pass per work item; the
+        // chain's publication flags start cleared
+        const int sms = sm_count();
+        if (pl.multi && cudaMemsetAsync(a.flags, 0, sizeof(int) * (size_t)pl.J * H * pl.NV, s) != cudaSuccess)
             return GLA_ERR_CUDA;
-    } else if (profiled(K_OUT_FFMA, s, [&] { return launch_out_ffma(pl, a, s); }) != cudaSuccess) {
-        return GLA_ERR_CUDA;
+        if (profiled(K_FUSED_TC, s, [&] { return launch_fused_tc(pl, a, s, sms); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+        return GLA_OK;
     }
+    if (pl.multi) {
+        if (profiled(K_STATE_FFMA, s, [&] { return launch_state_ffma(pl, a, s); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+        if (profiled(K_SCAN, s, [&] { return launch_scan(pl, a, s); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+    }
+    if (profiled(K_OUT_FFMA, s, [&] { return launch_out_ffma(pl, a, s); }) != cudaSuccess)
+        return GLA_ERR_CUDA;
     return GLA_OK;
 }
 
@@ -388,8 +398,7 @@ extern "C" const char *gla_kernel_name(int kernel_id)
     case K_STATE_FFMA: return "state_ffma";
     case K_SCAN: return "scan_segments";
     case K_OUT_FFMA: return "out_ffma";
-    case K_STATE_TC: return "state_tc";
-    case K_OUT_TC: return "out_tc";
+    case K_FUSED_TC: return "fused_tc";
     default: return "unknown";
     }
 }

@@ -25,7 +25,7 @@ struct Plan {
     bool tc;      // tensor-core path (bf16 inputs, K == 128, V multiple of 128)
     int BV, NV;   // value-tile width and count (64 on CUDA cores, 128 on tensor cores)
     // workspace layout (byte offsets)
-    size_t off_status, off_table, off_seq, off_ss, off_gtot, off_h0c, total;
+    size_t off_status, off_table, off_seq, off_ss, off_gtot, off_ctr, off_flags, total;
 };
 
 // Kernel arguments (passed by value).
@@ -42,7 +42,8 @@ struct Args {
     const int2 *seqinfo;   // varlen: per sequence {first slot, slot count}
     float *ss;             // [J][H][K][V]: segment contributions, then segment start states
     float *gtot;           // [J][H][K]: total log-decay of each segment
-    float *h0c;            // [N][H][K][V]: copy of h0 for sequences split into segments (tensor path)
+    int *ctr;              // fused tensor kernel: [0] next work item, [1] finished CTAs (zero between calls)
+    int *flags;            // fused tensor kernel: per work item, 1 once its segment end state is published
     int *status;           // sticky device status word
 };
 
@@ -82,8 +83,7 @@ cudaError_t launch_state_ffma(const Plan &pl, const Args &a, cudaStream_t s);
 cudaError_t launch_scan(const Plan &pl, const Args &a, cudaStream_t s);
 cudaError_t launch_out_ffma(const Plan &pl, const Args &a, cudaStream_t s);
 bool tc_supported(int dtype, int K, int V);
-cudaError_t launch_state_tc(const Plan &pl, const Args &a, cudaStream_t s);
-cudaError_t launch_out_tc(const Plan &pl, const Args &a, cudaStream_t s);
+cudaError_t launch_fused_tc(const Plan &pl, const Args &a, cudaStream_t s, int sms);
 cudaError_t launch_chunk_cumsum(const void *g, float *G, const int32_t *cu, int N, int B, int T, int H,
                                 int K, int chunk, int dtype, cudaStream_t s);
 

@@ -239,6 +239,48 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity)
     return true;
 }
 
+// As bar_wait, but also gives up at once when the CTA-wide abort word is set, and sets it on a timeout,
+// so that one failed wait ends every role of the CTA quickly instead of each running out its own limit.
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
+{
+    if (bar_try(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    while (!bar_try(bar, parity)) {
+        if (*abort)
+            return false;
+        if (global_ns() - t0 > kWaitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// Spin (with short sleeps) until the global word `flag` equals `want` (acquire), or the limit / abort hits.
+__device__ __forceinline__ bool flag_wait(const int *flag, int want, volatile int *abort)
+{
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v == want)
+            return true;
+        if (*abort)
+            return false;
+        if (global_ns() - t0 > kWaitNs) {
+            *abort = 1;
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
+__device__ __forceinline__ void flag_set(int *flag, int value)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(value) : "memory");
+}
+
 // ---------------------------------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------------------------------
