@@ -143,9 +143,12 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
     pl.off_ss = off;
     if (pl.multi)
         off += align_up(sizeof(float) * (size_t)pl.J * H * K * V);
+    pl.off_agg = off;
+    if (pl.multi && pl.tc)
+        off += align_up(sizeof(float) * (size_t)pl.J * H * K * V);
     pl.off_gtot = off;
-    if (pl.multi && !pl.tc)
-        off += align_up(sizeof(float) * (size_t)pl.J * H * K);
+    if (pl.multi)
+        off += align_up(sizeof(float) * (size_t)pl.J * H * K * (pl.tc ? pl.NV : 1));
     // the fused kernel's work counters live in the fixed header (status word at byte 0, counters at 16),
     // so they mean the same thing whatever the layout of the previous call that used this workspace
     pl.off_ctr = 16;
@@ -287,8 +290,9 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     }
     if (pl.multi) {
         a.ss = reinterpret_cast<float *>(ws + pl.off_ss);
-        if (!pl.tc)
-            a.gtot = reinterpret_cast<float *>(ws + pl.off_gtot);
+        a.gtot = reinterpret_cast<float *>(ws + pl.off_gtot);
+        if (pl.tc)
+            a.agg = reinterpret_cast<float *>(ws + pl.off_agg);
     }
     if (pl.tc) {
         a.ctr = reinterpret_cast<int *>(ws + pl.off_ctr);

@@ -25,7 +25,7 @@ struct Plan {
     bool tc;      // tensor-core path (bf16 inputs, K == 128, V multiple of 128)
     int BV, NV;   // value-tile width and count (64 on CUDA cores, 128 on tensor cores)
     // workspace layout (byte offsets)
-    size_t off_status, off_table, off_seq, off_ss, off_gtot, off_ctr, off_flags, total;
+    size_t off_status, off_table, off_seq, off_ss, off_agg, off_gtot, off_ctr, off_flags, total;
 };
 
 // Kernel arguments (passed by value).
@@ -38,12 +38,16 @@ struct Args {
     float scale;
     int B, T, H, K, V, N, L, P, J;
     int seg_cap;           // varlen: most segments per sequence (the segment length grows to respect it)
+    int lb;                // fused tensor kernel: segments per block of the start-state scan
     const int4 *table;     // varlen: per slot {n, p, bos, eos}; n < 0 marks an unused slot
     const int2 *seqinfo;   // varlen: per sequence {first slot, slot count}
-    float *ss;             // [J][H][K][V]: segment contributions, then segment start states
-    float *gtot;           // [J][H][K]: total log-decay of each segment
+    float *ss;             // CUDA cores: [J][H][K][V] segment contributions, then segment start states;
+                           // tensor cores: [J][H][NV] tiles of the segment end states (key-interleaved)
+    float *agg;            // tensor cores: [J][H][NV] tiles of the segment contributions (key-interleaved)
+    float *gtot;           // CUDA cores: [J][H][K]; tensor cores: [J][H][NV][K]: total log-decay of a segment
     int *ctr;              // fused tensor kernel: [0] next work item, [1] finished CTAs (zero between calls)
-    int *flags;            // fused tensor kernel: per work item, 1 once its segment end state is published
+    int *flags;            // fused tensor kernel: per work item, 1 once its segment contribution and decay
+                           // are published, 2 once its segment end state is
     int *status;           // sticky device status word
 };
 

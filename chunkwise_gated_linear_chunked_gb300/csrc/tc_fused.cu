@@ -13,8 +13,9 @@
 // not the last of its sequence the CTA
 //   1. walks the segment's chunks last to first and accumulates dS = sum_t k_t^T v_t exp(G_end - G_t) in
 //      TMEM with no rescaling (the later chunks' decay is folded into k^ <= |k|),
-//   2. waits for its predecessor's published S_out (a workspace flag, cleared before each call; item p = 0
-//      reads h0), publishes its own S_out, and
+//   2. finds its start state S_in from the predecessors' published contributions and end states by a
+//      fixed two-level scan (blocks of lb segments; workspace flags, cleared before each call; segment 0
+//      reads h0) and publishes its own contribution or end state, and
 //   3. runs the output pass over the same chunks, first to last, while they are still in L2.
 // The last segment of a sequence skips 1. and 2.'s publication and writes ht at the end.  One segment per
 // sequence is the plain single pass.
@@ -29,7 +30,8 @@
 // where single-rounded bf16 operands do not); accumulation is fp32 in TMEM; gates are summed in log2 units.
 //
 // Roles: warps 0-7 gating (cumsum, gating, operand conversion in place in the TMA stage); warps 8-11 state
-// (chain step, S' and decay per chunk, final state); warps 12-15 output (P, O^T -> smem -> TMA store);
+// (S' and decay per chunk, final state); warps 12-15 output (P, O^T -> smem -> TMA store); warps 8-15
+// together run the look-back at the start of an item;
 // warp 16 lane 0 TMA + MMA issue.  Three 64 KB stages.  Every wait is bounded and a CTA-wide abort word ends
 // all roles quickly after the first failure (GLA_ERR_TIMEOUT); non-finite outputs report GLA_ERR_RANGE.
 #include <cuda_bf16.h>
@@ -65,7 +67,8 @@ constexpr int OFF_EG = OFF_P + 8192;              // per stage: exp(G_a)[128], e
 constexpr int OFF_PS = OFF_EG + NSTAGE * 1024;    // gating partial sums [2][4][128]
 constexpr int OFF_OST = OFF_PS + 4096;            // output staging, 32 rows x 128 fp32
 constexpr int OFF_GT = OFF_OST + 16384;           // segment decay (log2) per key, [128]
-constexpr int OFF_MISC = OFF_GT + 512;            // item slot, abort word
+constexpr int OFF_WL = OFF_GT + 512;             // look-back: running log2 weight per key, [128]
+constexpr int OFF_MISC = OFF_WL + 512;            // item slot, abort word, look-back flag value
 constexpr int OFF_BAR = OFF_MISC + 64;
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
 
@@ -97,6 +100,22 @@ __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return
 __device__ __forceinline__ void sync_gating() { asm volatile("bar.sync 1, %0;" ::"n"(NA) : "memory"); }
 __device__ __forceinline__ void sync_output() { asm volatile("bar.sync 2, %0;" ::"n"(NC) : "memory"); }
 __device__ __forceinline__ void sync_state() { asm volatile("bar.sync 3, %0;" ::"n"(NB) : "memory"); }
+// the chain team: state and output groups together
+__device__ __forceinline__ void sync_team() { asm volatile("bar.sync 4, %0;" ::"n"(NB + NC) : "memory"); }
+__device__ __forceinline__ bool team_all(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 4, %2, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "n"(NB + NC)
+                 : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ float4 f4(const uint32_t *r)
+{
+    return make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]), __uint_as_float(r[3]));
+}
 
 template <typename Tout>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -113,9 +132,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t *mma_a = bars + 13, *a_done = bars + 14, *g_done = bars + 15, *tmem_free = bars + 16;
     uint64_t *item_done = bars + 17;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
-    volatile int *misc = reinterpret_cast<volatile int *>(sm + OFF_MISC);   // [0] item, [1] abort
+    volatile int *misc = reinterpret_cast<volatile int *>(sm + OFF_MISC);   // [0] item, [1] abort, [2] flag
     volatile int *abort_w = misc + 1;
     float *gts = reinterpret_cast<float *>(sm + OFF_GT);
+    float *wl = reinterpret_cast<float *>(sm + OFF_WL);
 
     if (a.table)
         grid_dep_wait();   // the varlen slot table comes from the preceding plan kernel
@@ -153,7 +173,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr int ready = 1;   // flag value that marks a published S_out (the flags are cleared per call)
 
     // CTA-wide running counts (identical in every role): chunks through the stage ring, output-pass chunks,
     // state-pass chunks, items with a state pass, items completed
@@ -180,6 +199,166 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int nA = last ? 0 : nchunks;   // state-pass chunks (reverse order)
         const int nQ = nA + nchunks;         // chunks through the ring: state pass, then output pass
         auto chunk_of = [&](int q) { return q < nA ? nA - 1 - q : q - nA; };
+
+        // ---------------------------------------------------------------------- chain team
+        // Start state of the item's segment into TMEM S.  Segments are grouped in blocks of lb; the first
+        // segment of a block (a boundary, p % lb == 0) publishes its end state S_out = 2^Gtot S_in + dS
+        // (flag 2), every other segment with a state pass publishes its contribution dS and decay Gtot
+        // (flag 1) as soon as the pass is done.  With p0 the last boundary before p,
+        //   S_in(p) = sum_{i = p-1 .. p0+1} 2^(Gtot(p-1) + ... + Gtot(i+1)) dS(i) + 2^(Gtot(p-1) + ... + Gtot(p0+1)) S_out(p0),
+        // summed newest first, and S_in(0) = h0.  The grouping is fixed, so the result does not depend on
+        // timing; lb = 1 is the plain serial chain (one tile read and one written per segment), a larger lb
+        // shortens the chain of dependent publications when all items run at once.
+        // 256 threads, lane = value column; the state group takes keys 0..63, the output group 64..127.
+        // TMEM S' (free until the output pass) accumulates the sum.  Published tiles are key-interleaved
+        // (float4 of 4 keys per value column) so a warp reads 512 contiguous bytes per load.
+        auto chain = [&]() -> bool {
+            const int half = warp >= WC ? 1 : 0;
+            const int b = tid - NA - half * NB;
+            const int kb0 = 64 * half;
+            const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            const bool leader = tid == NA;
+            const size_t tile = (size_t)KD * VT;
+            const size_t mine = ((size_t)j * H + h) * NV + vt;
+            const int HN = H * NV;
+            const bool boundary = p % a.lb == 0;
+            bool ok = true;
+            if (nA > 0)
+                ok = bar_wait(g_done, naitems & 1, abort_w) && bar_wait(a_done, naitems & 1, abort_w);
+            if (!team_all(ok))
+                return false;
+            fence_after();
+            if (nA > 0 && !boundary) {
+                float4 *dst = reinterpret_cast<float4 *>(a.agg + mine * tile);
+                for (int sub = 0; sub < 2; ++sub) {
+                    const int k0 = kb0 + 32 * sub;
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lrow + TM_S + k0, r);
+                    tmem_wait_ld(r);
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        __stcg(dst + (size_t)(k0 / 4 + w) * VT + b, f4(r + 4 * w));
+                }
+                if (b < 64)
+                    __stcg(a.gtot + mine * KD + kb0 + b, gts[kb0 + b]);
+                __threadfence();
+                sync_team();
+                if (leader)
+                    flag_set(a.flags + u, 1);
+            }
+            const int p0 = p > 0 ? (p - 1) / a.lb * a.lb : 0;
+            if (p > 0) {
+                if (b < 64)
+                    wl[kb0 + b] = 0.f;
+                for (int i = p - 1; i > p0; --i) {
+                    const int back = p - i;
+                    if (leader)
+                        misc[2] = flag_wait_ge(a.flags + (u - back * HN), 1, abort_w);
+                    sync_team();
+                    if (misc[2] == 0)
+                        return false;   // uniform: every thread read the same value
+                    const size_t ti = mine - (size_t)back * HN;
+                    const float4 *src = reinterpret_cast<const float4 *>(a.agg + ti * tile);
+                    const float gi = b < 64 ? __ldcg(a.gtot + ti * KD + kb0 + b) : 0.f;
+                    for (int sub = 0; sub < 2; ++sub) {
+                        const int k0 = kb0 + 32 * sub;
+                        float4 x[8];
+#pragma unroll
+                        for (int w = 0; w < 8; ++w)
+                            x[w] = __ldcg(src + (size_t)(k0 / 4 + w) * VT + b);
+                        uint32_t r[32];
+                        if (back > 1) {
+                            tmem_ld32(tmem + lrow + TM_SOP + k0, r);
+                            tmem_wait_ld(r);
+                        } else {
+#pragma unroll
+                            for (int uu = 0; uu < 32; ++uu)
+                                r[uu] = 0u;
+                        }
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            const float4 e = *reinterpret_cast<const float4 *>(wl + k0 + 4 * w);
+                            r[4 * w] = __float_as_uint(fmaf(ex2(e.x), x[w].x, __uint_as_float(r[4 * w])));
+                            r[4 * w + 1] = __float_as_uint(fmaf(ex2(e.y), x[w].y, __uint_as_float(r[4 * w + 1])));
+                            r[4 * w + 2] = __float_as_uint(fmaf(ex2(e.z), x[w].z, __uint_as_float(r[4 * w + 2])));
+                            r[4 * w + 3] = __float_as_uint(fmaf(ex2(e.w), x[w].w, __uint_as_float(r[4 * w + 3])));
+                        }
+                        tmem_st32(tmem + lrow + TM_SOP + k0, r);
+                    }
+                    tmem_wait_st();
+                    sync_team();   // every thread has used this step's weights
+                    if (b < 64)
+                        wl[kb0 + b] += gi;
+                }
+                // the end state of the block's boundary segment
+                if (leader)
+                    misc[2] = flag_wait_ge(a.flags + (u - (p - p0) * HN), 2, abort_w);
+                sync_team();
+                if (misc[2] == 0)
+                    return false;
+            }
+            // S_in -> TMEM S; a boundary segment with a state pass publishes S_out = 2^Gtot * S_in + dS
+            const bool acc = p - 1 > p0;   // contributions were summed into TMEM S'
+            const bool pub = nA > 0 && boundary;
+            const size_t soff = ((size_t)n * H + h) * KD * V + v0 + b;
+            const float4 *bsrc = reinterpret_cast<const float4 *>(a.ss + (mine - (size_t)(p - p0) * HN) * tile);
+            float4 *bdst = reinterpret_cast<float4 *>(a.ss + mine * tile);
+            for (int sub = 0; sub < 2; ++sub) {
+                const int k0 = kb0 + 32 * sub;
+                uint32_t sn[32];
+                if (p > 0) {
+                    float4 x[8];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        x[w] = __ldcg(bsrc + (size_t)(k0 / 4 + w) * VT + b);
+                    if (acc) {
+                        tmem_ld32(tmem + lrow + TM_SOP + k0, sn);
+                        tmem_wait_ld(sn);
+                    } else {
+#pragma unroll
+                        for (int uu = 0; uu < 32; ++uu)
+                            sn[uu] = 0u;
+                    }
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const float4 e = *reinterpret_cast<const float4 *>(wl + k0 + 4 * w);
+                        sn[4 * w] = __float_as_uint(fmaf(ex2(e.x), x[w].x, __uint_as_float(sn[4 * w])));
+                        sn[4 * w + 1] = __float_as_uint(fmaf(ex2(e.y), x[w].y, __uint_as_float(sn[4 * w + 1])));
+                        sn[4 * w + 2] = __float_as_uint(fmaf(ex2(e.z), x[w].z, __uint_as_float(sn[4 * w + 2])));
+                        sn[4 * w + 3] = __float_as_uint(fmaf(ex2(e.w), x[w].w, __uint_as_float(sn[4 * w + 3])));
+                    }
+                } else if (a.h0) {
+#pragma unroll
+                    for (int uu = 0; uu < 32; ++uu)
+                        sn[uu] = __float_as_uint(__ldcg(a.h0 + soff + (size_t)(k0 + uu) * V));
+                } else {
+#pragma unroll
+                    for (int uu = 0; uu < 32; ++uu)
+                        sn[uu] = 0u;
+                }
+                if (pub) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lrow + TM_S + k0, r);
+                    tmem_wait_ld(r);
+#pragma unroll
+                    for (int uu = 0; uu < 32; ++uu)
+                        r[uu] = __float_as_uint(fmaf(ex2(gts[k0 + uu]), __uint_as_float(sn[uu]), __uint_as_float(r[uu])));
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        __stcg(bdst + (size_t)(k0 / 4 + w) * VT + b, f4(r + 4 * w));
+                }
+                tmem_st32(tmem + lrow + TM_S + k0, sn);
+            }
+            tmem_wait_st();
+            if (pub)
+                __threadfence();
+            fence_before();
+            sync_team();
+            fence_after();
+            if (pub && leader)
+                flag_set(a.flags + u, 2);
+            return true;
+        };
 
         if (warp == WCTL) {
             // ------------------------------------------------------------------ control: TMA + MMA
@@ -393,59 +572,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // ------------------------------------------------------------------ state group
             const int b = tid - NA;
             const uint32_t lrow = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            const size_t soff = ((size_t)n * H + h) * KD * V + v0 + b;   // h0 / ht column of this lane
-            bool ok = true;
-            // S_in: h0 for the first segment, else the predecessor's published S_out
-            const float *src = nullptr;
-            if (p == 0) {
-                src = a.h0 ? a.h0 + soff : nullptr;
-            } else {
-                if (b == 0)
-                    ok = flag_wait(a.flags + (u - H * NV), ready, abort_w);
-                sync_state();
-                ok = ok && !*abort_w;
-                src = a.ss + ((size_t)(j - 1) * H + h) * KD * V + v0 + b;
-            }
-            if (nA > 0) {
-                // chain step: S_out = 2^Gtot * S_in + dS (dS is in TMEM once the state pass is done)
-                ok = ok && bar_wait(g_done, naitems & 1, abort_w) && bar_wait(a_done, naitems & 1, abort_w);
-                if (ok) {
-                    fence_after();
-                    float *dst = a.ss + ((size_t)j * H + h) * KD * V + v0 + b;
-                    for (int kc = 0; kc < KD / 32; ++kc) {
-                        uint32_t r[32];
-                        float sin[32];
-                        tmem_ld32(tmem + lrow + TM_S + kc * 32, r);
-                        // all 32 loads first: interleaved with the stores below they could not be hoisted
-                        // (src and dst may alias as far as the compiler knows) and would run one by one
-#pragma unroll
-                        for (int uu = 0; uu < 32; ++uu)
-                            sin[uu] = src ? __ldcg(src + (size_t)(kc * 32 + uu) * V) : 0.f;
-                        tmem_wait_ld(r);
-#pragma unroll
-                        for (int uu = 0; uu < 32; ++uu) {
-                            const int k = kc * 32 + uu;
-                            __stcg(dst + (size_t)k * V, fmaf(ex2(gts[k]), sin[uu], __uint_as_float(r[uu])));
-                            r[uu] = __float_as_uint(sin[uu]);
-                        }
-                        tmem_st32(tmem + lrow + TM_S + kc * 32, r);
-                    }
-                    tmem_wait_st();
-                    __threadfence();
-                    sync_state();
-                    if (b == 0)
-                        flag_set(a.flags + u, ready);
-                }
-            } else if (ok) {
-                for (int kc = 0; kc < KD / 32; ++kc) {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int uu = 0; uu < 32; ++uu)
-                        r[uu] = __float_as_uint(src ? __ldcg(src + (size_t)(kc * 32 + uu) * V) : 0.f);
-                    tmem_st32(tmem + lrow + TM_S + kc * 32, r);
-                }
-                tmem_wait_st();
-            }
+            const size_t soff = ((size_t)n * H + h) * KD * V + v0 + b;   // ht column of this lane
+            bool ok = chain();
             // output pass: per chunk S' = diag(exp(G_a)) S (fp16), S <- diag(exp(G_last)) S
             for (int c = 0; ok && c < nchunks; ++c) {
                 const int gq = qbase + nA + c, gb = nbbase + c;
@@ -525,8 +653,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float *ost = reinterpret_cast<float *>(sm + OFF_OST);
             Tout *go = static_cast<Tout *>(a.o);
             const size_t rstride = (size_t)H * V;
-            bool ok = true;
-            for (int c = 0; c < nchunks; ++c) {
+            bool ok = chain();
+            for (int c = 0; ok && c < nchunks; ++c) {
                 const int gb = nbbase + c;
                 const int row0 = bos + c * C;
                 const int len = min(C, eos - row0);
@@ -686,6 +814,11 @@ cudaError_t launch_fused_t(const Plan &pl, const Args &a, cudaStream_t s, int sm
         attr = true;
     }
     int nitems = pl.J * pl.H * (pl.V / VT);
+    // scan block length: when every item runs at once the chain of end-state publications is the critical
+    // path, so only every 8th segment publishes one; with several waves the predecessors finished earlier
+    // and the plain chain (one tile read per item) costs least
+    Args ka = a;
+    ka.lb = nitems <= sms ? 8 : 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)std::min(nitems, sms));
     cfg.blockDim = dim3(NTHREADS);
@@ -696,7 +829,7 @@ cudaError_t launch_fused_t(const Plan &pl, const Args &a, cudaStream_t s, int sm
     attrs[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = pl.varlen ? 1 : 0;
-    void *args[] = {&mq, &mk, &mg, &mv, &mo, const_cast<Args *>(&a), &nitems};
+    void *args[] = {&mq, &mk, &mg, &mv, &mo, &ka, &nitems};
     cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(f), args);
     if (e != cudaSuccess)
         return e;

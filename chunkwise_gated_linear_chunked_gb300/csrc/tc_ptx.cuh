@@ -276,6 +276,25 @@ __device__ __forceinline__ bool flag_wait(const int *flag, int want, volatile in
     }
 }
 
+// Waits until *flag >= want and returns the value seen (0 after an abort or the time limit).
+__device__ __forceinline__ int flag_wait_ge(const int *flag, int want, volatile int *abort)
+{
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v >= want)
+            return v;
+        if (*abort)
+            return 0;
+        if (global_ns() - t0 > kWaitNs) {
+            *abort = 1;
+            return 0;
+        }
+        __nanosleep(32);
+    }
+}
+
 __device__ __forceinline__ void flag_set(int *flag, int value)
 {
     asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(value) : "memory");
