@@ -31,8 +31,8 @@
 //
 // Roles: warps 0-7 gating (cumsum, gating, operand conversion in place in the TMA stage); warps 8-11 state
 // (S' and decay per chunk, final state); warps 12-15 output (P, O^T -> smem -> TMA store); warps 8-15
-// together run the look-back at the start of an item;
-// warp 16 lane 0 TMA + MMA issue.  Three 64 KB stages.  Every wait is bounded and a CTA-wide abort word ends
+// together run the start-state scan of an item; warp 16 lane 0 issues the MMAs, warp 17 lane 0 the TMA
+// loads (three 64 KB stages, freed by MMA commits).  Every wait is bounded and a CTA-wide abort word ends
 // all roles quickly after the first failure (GLA_ERR_TIMEOUT); non-finite outputs report GLA_ERR_RANGE.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -54,9 +54,9 @@ constexpr int VT = 128;
 constexpr int NA = 256;          // gating group
 constexpr int NB = 128;          // state group
 constexpr int NC = 128;          // output group
-constexpr int WB = NA / 32, WC = (NA + NB) / 32, WCTL = (NA + NB + NC) / 32;
-constexpr int CTL = NA + NB + NC;   // control thread
-constexpr int NTHREADS = NA + NB + NC + 32;
+constexpr int WB = NA / 32, WC = (NA + NB) / 32, WCTL = (NA + NB + NC) / 32, WPRD = WCTL + 1;
+constexpr int CTL = NA + NB + NC;   // MMA issue thread
+constexpr int NTHREADS = NA + NB + NC + 64;
 constexpr float L2E = 1.4426950408889634f;
 
 constexpr int NSTAGE = 3;
@@ -99,7 +99,6 @@ __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float x) { return
 
 __device__ __forceinline__ void sync_gating() { asm volatile("bar.sync 1, %0;" ::"n"(NA) : "memory"); }
 __device__ __forceinline__ void sync_output() { asm volatile("bar.sync 2, %0;" ::"n"(NC) : "memory"); }
-__device__ __forceinline__ void sync_state() { asm volatile("bar.sync 3, %0;" ::"n"(NB) : "memory"); }
 // the chain team: state and output groups together
 __device__ __forceinline__ void sync_team() { asm volatile("bar.sync 4, %0;" ::"n"(NB + NC) : "memory"); }
 __device__ __forceinline__ bool team_all(bool v)
@@ -131,7 +130,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t *o_free = bars + 11;                                   // [2]
     uint64_t *mma_a = bars + 13, *a_done = bars + 14, *g_done = bars + 15, *tmem_free = bars + 16;
     uint64_t *item_done = bars + 17;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
+    uint64_t *empty = bars + 18;                                    // [3]: stage free again
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 21);
     volatile int *misc = reinterpret_cast<volatile int *>(sm + OFF_MISC);   // [0] item, [1] abort, [2] flag
     volatile int *abort_w = misc + 1;
     float *gts = reinterpret_cast<float *>(sm + OFF_GT);
@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bar_init(g_done, NA);
         bar_init(tmem_free, NB);
         bar_init(item_done, 1);
+        for (int s = 0; s < NSTAGE; ++s)
+            bar_init(&empty[s], 1);
         bar_fence_init();
         misc[1] = 0;
         tma_prefetch_desc(&tm_q);
@@ -360,11 +362,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             return true;
         };
 
-        if (warp == WCTL) {
-            // ------------------------------------------------------------------ control: TMA + MMA
+        if (warp == WPRD) {
+            // ------------------------------------------------------------------ TMA producer
             if (lane == 0) {
-                auto issue = [&](int q) {
-                    const int s = (qbase + q) % NSTAGE;
+                bool ok = true;
+                for (int q = 0; q < nQ; ++q) {
+                    const int gq = qbase + q, s = gq % NSTAGE;
+                    // the stage is free once the MMAs of the chunk three places earlier are complete
+                    if (gq >= NSTAGE && !(ok = bar_wait(&empty[s], (gq / NSTAGE - 1) & 1, abort_w)))
+                        break;
                     uint8_t *st = sm + s * STAGE;
                     const int row0 = bos + chunk_of(q) * C;
                     const bool out = q >= nA;
@@ -377,26 +383,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tma_load_3d(st + 16384 + ST_K0, &tm_k, 64, h, row0, &full[s]);
                     tma_load_3d(st + ST_G, &tm_g, 0, h, row0, &full[s]);
                     tma_load_3d(st + ST_V, &tm_v, v0, h, row0, &full[s]);
-                };
+                }
+                if (!ok) {
+                    *abort_w = 1;
+                    report(a.status, GLA_ERR_TIMEOUT);
+                }
+            }
+        } else if (warp == WCTL) {
+            // ------------------------------------------------------------------ MMA issue
+            if (lane == 0) {
                 bool ok = true;
-                // the previous item's MMAs are complete and its final state has been read (its stages and
-                // TMEM S are free) once the state group releases it
+                // the previous item's MMAs are complete and its final state has been read once the state
+                // group releases TMEM S
                 if (items > 0)
                     ok = bar_wait(tmem_free, (items - 1) & 1, abort_w);
-                for (int q = 0; ok && q < NSTAGE && q < nQ; ++q)
-                    issue(q);
                 const uint32_t pt = smem_u32(sm + OFF_P);
                 for (int q = 0; ok && q < nQ; ++q) {
                     const int s = (qbase + q) % NSTAGE;
                     const uint32_t st = smem_u32(sm + s * STAGE);
-                    if (q >= 1 && q + 2 < nQ) {
-                        // refill the stage of chunk q-1 once its MMAs are complete
-                        ok = q - 1 < nA ? bar_wait(mma_a, (nabase + q - 1) & 1, abort_w)
-                                        : bar_wait(mma2, (nbbase + q - 1 - nA) & 1, abort_w);
-                        if (!ok)
-                            break;
-                        issue(q + 2);
-                    }
                     if (q < nA) {
                         if (!(ok = bar_wait(&prep[s], ((qbase + q) / NSTAGE) & 1, abort_w)))
                             break;
@@ -405,6 +409,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             mma_ss(tmem + TM_S, sdesc_sw128(st + ST_V + k * 32), sdesc_sw128(st + ST_G + k * 32),
                                    ID_N128, (q > 0 || k > 0) ? 1u : 0u);
                         mma_commit(mma_a);
+                        mma_commit(&empty[s]);
                         if (q == nA - 1)
                             mma_commit(a_done);
                     } else {
@@ -433,6 +438,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         for (int k = 0; k < C / 16; ++k)
                             mma_ss(ob, sdesc_sw128(st + ST_V + k * 32), sdesc_sw128(pt + k * 32), ID_N64, 1);
                         mma_commit(mma2);
+                        mma_commit(&empty[s]);
                     }
                 }
                 mma_commit(item_done);

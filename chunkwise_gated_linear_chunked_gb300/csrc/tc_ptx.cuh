@@ -352,5 +352,6 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+
 }  // namespace tc
 }  // namespace gla
