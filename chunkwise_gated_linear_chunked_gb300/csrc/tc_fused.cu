@@ -232,13 +232,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             fence_after();
             if (nA > 0 && !boundary) {
                 float4 *dst = reinterpret_cast<float4 *>(a.agg + mine * tile);
-                for (int sub = 0; sub < 2; ++sub) {
-                    const int k0 = kb0 + 32 * sub;
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lrow + TM_S + k0, r);
+                for (int sub = 0; sub < 4; ++sub) {
+                    const int k0 = kb0 + 16 * sub;
+                    uint32_t r[16];
+                    tmem_ld16(tmem + lrow + TM_S + k0, r);
                     tmem_wait_ld(r);
 #pragma unroll
-                    for (int w = 0; w < 8; ++w)
+                    for (int w = 0; w < 4; ++w)
                         __stcg(dst + (size_t)(k0 / 4 + w) * VT + b, f4(r + 4 * w));
                 }
                 if (b < 64)
@@ -263,29 +263,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const float4 *src = reinterpret_cast<const float4 *>(a.agg + ti * tile);
                     const float gi = b < 64 ? __ldcg(a.gtot + ti * KD + kb0 + b) : 0.f;
                     for (int sub = 0; sub < 2; ++sub) {
+                        // 32 keys of loads in flight, consumed 16 TMEM columns at a time
                         const int k0 = kb0 + 32 * sub;
                         float4 x[8];
 #pragma unroll
                         for (int w = 0; w < 8; ++w)
                             x[w] = __ldcg(src + (size_t)(k0 / 4 + w) * VT + b);
-                        uint32_t r[32];
-                        if (back > 1) {
-                            tmem_ld32(tmem + lrow + TM_SOP + k0, r);
-                            tmem_wait_ld(r);
-                        } else {
 #pragma unroll
-                            for (int uu = 0; uu < 32; ++uu)
-                                r[uu] = 0u;
-                        }
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int k1 = k0 + 16 * hh;
+                            uint32_t r[16];
+                            if (back > 1) {
+                                tmem_ld16(tmem + lrow + TM_SOP + k1, r);
+                                tmem_wait_ld(r);
+                            } else {
 #pragma unroll
-                        for (int w = 0; w < 8; ++w) {
-                            const float4 e = *reinterpret_cast<const float4 *>(wl + k0 + 4 * w);
-                            r[4 * w] = __float_as_uint(fmaf(ex2(e.x), x[w].x, __uint_as_float(r[4 * w])));
-                            r[4 * w + 1] = __float_as_uint(fmaf(ex2(e.y), x[w].y, __uint_as_float(r[4 * w + 1])));
-                            r[4 * w + 2] = __float_as_uint(fmaf(ex2(e.z), x[w].z, __uint_as_float(r[4 * w + 2])));
-                            r[4 * w + 3] = __float_as_uint(fmaf(ex2(e.w), x[w].w, __uint_as_float(r[4 * w + 3])));
+                                for (int uu = 0; uu < 16; ++uu)
+                                    r[uu] = 0u;
+                            }
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                const float4 e = *reinterpret_cast<const float4 *>(wl + k1 + 4 * w);
+                                const float4 xv = x[4 * hh + w];
+                                r[4 * w] = __float_as_uint(fmaf(ex2(e.x), xv.x, __uint_as_float(r[4 * w])));
+                                r[4 * w + 1] = __float_as_uint(fmaf(ex2(e.y), xv.y, __uint_as_float(r[4 * w + 1])));
+                                r[4 * w + 2] = __float_as_uint(fmaf(ex2(e.z), xv.z, __uint_as_float(r[4 * w + 2])));
+                                r[4 * w + 3] = __float_as_uint(fmaf(ex2(e.w), xv.w, __uint_as_float(r[4 * w + 3])));
+                            }
+                            tmem_st16(tmem + lrow + TM_SOP + k1, r);
                         }
-                        tmem_st32(tmem + lrow + TM_SOP + k0, r);
                     }
                     tmem_wait_st();
                     sync_team();   // every thread has used this step's weights
@@ -305,25 +311,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const size_t soff = ((size_t)n * H + h) * KD * V + v0 + b;
             const float4 *bsrc = reinterpret_cast<const float4 *>(a.ss + (mine - (size_t)(p - p0) * HN) * tile);
             float4 *bdst = reinterpret_cast<float4 *>(a.ss + mine * tile);
-            for (int sub = 0; sub < 2; ++sub) {
-                const int k0 = kb0 + 32 * sub;
-                uint32_t sn[32];
+#pragma unroll 1
+            for (int sub = 0; sub < 4; ++sub) {
+                const int k1 = kb0 + 16 * sub;
+                uint32_t sn[16];
                 if (p > 0) {
-                    float4 x[8];
+                    float4 x[4];
 #pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        x[w] = __ldcg(bsrc + (size_t)(k0 / 4 + w) * VT + b);
+                    for (int w = 0; w < 4; ++w)
+                        x[w] = __ldcg(bsrc + (size_t)(k1 / 4 + w) * VT + b);
                     if (acc) {
-                        tmem_ld32(tmem + lrow + TM_SOP + k0, sn);
+                        tmem_ld16(tmem + lrow + TM_SOP + k1, sn);
                         tmem_wait_ld(sn);
                     } else {
 #pragma unroll
-                        for (int uu = 0; uu < 32; ++uu)
+                        for (int uu = 0; uu < 16; ++uu)
                             sn[uu] = 0u;
                     }
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        const float4 e = *reinterpret_cast<const float4 *>(wl + k0 + 4 * w);
+                    for (int w = 0; w < 4; ++w) {
+                        const float4 e = *reinterpret_cast<const float4 *>(wl + k1 + 4 * w);
                         sn[4 * w] = __float_as_uint(fmaf(ex2(e.x), x[w].x, __uint_as_float(sn[4 * w])));
                         sn[4 * w + 1] = __float_as_uint(fmaf(ex2(e.y), x[w].y, __uint_as_float(sn[4 * w + 1])));
                         sn[4 * w + 2] = __float_as_uint(fmaf(ex2(e.z), x[w].z, __uint_as_float(sn[4 * w + 2])));
@@ -331,25 +338,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 } else if (a.h0) {
 #pragma unroll
-                    for (int uu = 0; uu < 32; ++uu)
-                        sn[uu] = __float_as_uint(__ldcg(a.h0 + soff + (size_t)(k0 + uu) * V));
+                    for (int uu = 0; uu < 16; ++uu)
+                        sn[uu] = __float_as_uint(__ldcg(a.h0 + soff + (size_t)(k1 + uu) * V));
                 } else {
 #pragma unroll
-                    for (int uu = 0; uu < 32; ++uu)
+                    for (int uu = 0; uu < 16; ++uu)
                         sn[uu] = 0u;
                 }
                 if (pub) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lrow + TM_S + k0, r);
+                    uint32_t r[16];
+                    tmem_ld16(tmem + lrow + TM_S + k1, r);
                     tmem_wait_ld(r);
 #pragma unroll
-                    for (int uu = 0; uu < 32; ++uu)
-                        r[uu] = __float_as_uint(fmaf(ex2(gts[k0 + uu]), __uint_as_float(sn[uu]), __uint_as_float(r[uu])));
+                    for (int uu = 0; uu < 16; ++uu)
+                        r[uu] = __float_as_uint(fmaf(ex2(gts[k1 + uu]), __uint_as_float(sn[uu]), __uint_as_float(r[uu])));
 #pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        __stcg(bdst + (size_t)(k0 / 4 + w) * VT + b, f4(r + 4 * w));
+                    for (int w = 0; w < 4; ++w)
+                        __stcg(bdst + (size_t)(k1 / 4 + w) * VT + b, f4(r + 4 * w));
                 }
-                tmem_st32(tmem + lrow + TM_S + k0, sn);
+                tmem_st16(tmem + lrow + TM_S + k1, sn);
             }
             tmem_wait_st();
             if (pub)

@@ -352,6 +352,5 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-
 }  // namespace tc
 }  // namespace gla
