@@ -55,6 +55,27 @@ def test_small_cases_elementwise(case):
     assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
 
 
+# Start-state scan of the tensor-core path.  On a 152-SM GB300 with 126 MB of L2 the planner cuts these into
+# 512-row segments: 9 segments x 16 heads = 144 items fit in one wave, so segments are grouped in blocks of 8
+# and segment 9 starts from the end state published by segment 8; 8 segments x 40 heads = 320 items take
+# several waves and use the plain serial chain.  Every head is compared with the oracle.
+SCAN_CASES = [
+    ("bf16", 1, 4608, 16, 128, 128, True, None),
+    ("bf16", 1, 4096, 40, 128, 128, True, None),
+    ("bf16", 2, 2560, 12, 128, 128, False, None),
+]
+
+
+@pytest.mark.parametrize("case", SCAN_CASES, ids=_case_id)
+def test_segment_scan_all_heads(case):
+    d, B, T, H, K, V, h0, lengths = case
+    inp = make_inputs(d, B=B, T=T, H=H, K=K, V=V, h0=h0, lengths=lengths, seed=zlib.crc32(_case_id(case).encode()) % 1000)
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(as_f64(o), o_ref, TOL[d], "o")
+    assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
+
+
 def test_bf16_output_variant():
     inp = make_inputs("bf16", B=2, T=300, H=2, K=128, V=128, h0=True, seed=3)
     o, ht = run_gpu(inp, out_dtype=torch.bfloat16)
