@@ -149,8 +149,9 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
     pl.off_gtot = off;
     if (pl.multi)
         off += align_up(sizeof(float) * (size_t)pl.J * H * K * (pl.tc ? pl.NV : 1));
-    // the fused kernel's work counters live in the fixed header (status word at byte 0, counters at 16),
-    // so they mean the same thing whatever the layout of the previous call that used this workspace
+    // the fused kernel's work counters and launch epoch live in the fixed header (status word at byte 0,
+    // counters at 16, epoch at 24), so they mean the same thing whatever the layout of the previous call
+    // that used this workspace
     pl.off_ctr = 16;
     pl.off_flags = off;
     if (pl.tc && pl.multi)
@@ -304,11 +305,9 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     if (varlen && profiled(K_PLAN, s, [&] { return launch_plan_varlen(pl, a, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;
     if (pl.tc) {
-        // one persistent kernel: state pass, chained segment scan and output pass per work item; the
-        // chain's publication flags start cleared
+        // one persistent kernel: state pass, segment scan and output pass per work item (its publication
+        // flags are tagged with a launch epoch kept in the workspace header, so they need no clearing)
         const int sms = sm_count();
-        if (pl.multi && cudaMemsetAsync(a.flags, 0, sizeof(int) * (size_t)pl.J * H * pl.NV, s) != cudaSuccess)
-            return GLA_ERR_CUDA;
         if (profiled(K_FUSED_TC, s, [&] { return launch_fused_tc(pl, a, s, sms); }) != cudaSuccess)
             return GLA_ERR_CUDA;
         return GLA_OK;

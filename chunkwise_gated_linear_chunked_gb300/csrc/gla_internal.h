@@ -45,9 +45,10 @@ struct Args {
                            // tensor cores: [J][H][NV] tiles of the segment end states (key-interleaved)
     float *agg;            // tensor cores: [J][H][NV] tiles of the segment contributions (key-interleaved)
     float *gtot;           // CUDA cores: [J][H][K]; tensor cores: [J][H][NV][K]: total log-decay of a segment
-    int *ctr;              // fused tensor kernel: [0] next work item, [1] finished CTAs (zero between calls)
-    int *flags;            // fused tensor kernel: per work item, 1 once its segment contribution and decay
-                           // are published, 2 once its segment end state is
+    int *ctr;              // fused tensor kernel: [0] next work item, [1] finished CTAs (both zero between
+                           // calls), [2] launch epoch (advanced by every launch)
+    int *flags;            // fused tensor kernel: per work item (epoch << 2) | 1 once its segment contribution
+                           // and decay are published, (epoch << 2) | 2 once its segment end state is
     int *status;           // sticky device status word
 };
 

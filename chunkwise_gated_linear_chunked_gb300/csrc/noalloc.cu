@@ -38,8 +38,9 @@ extern "C" int gla_fwd_noalloc(const void *q, const void *k, const void *v, cons
     const size_t need = gla_fwd_workspace_size(B, T, H, K, V, N, chunk, dtype);
     if (need > kScratchBytes)
         return GLA_ERR_WORKSPACE;
-    // The array keeps the previous call's contents; only the status word must start at zero.
-    if (need > 0 && cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The array keeps the previous call's contents; only the status word (the header's first 16 bytes) must
+    // start at zero.  The work counters and the launch epoch behind it carry over between calls.
+    if (need > 0 && cudaMemsetAsync(scratch, 0, 16, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return GLA_ERR_CUDA;
     return gla_fwd(q, k, v, g, o, scale, h0, ht, cu_seqlens, N, B, T, H, K, V, chunk, dtype, scratch,
                    kScratchBytes, stream);

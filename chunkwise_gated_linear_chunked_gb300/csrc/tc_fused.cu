@@ -58,6 +58,7 @@ constexpr int WB = NA / 32, WC = (NA + NB) / 32, WCTL = (NA + NB + NC) / 32, WPR
 constexpr int CTL = NA + NB + NC;   // MMA issue thread
 constexpr int NTHREADS = NA + NB + NC + 64;
 constexpr float L2E = 1.4426950408889634f;
+constexpr uint32_t kEpochMask = 0x3FFFFFFFu;   // a flag holds (epoch << 2) | kind
 
 constexpr int NSTAGE = 3;
 constexpr int STAGE = 65536;
@@ -140,6 +141,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (a.table)
         grid_dep_wait();   // the varlen slot table comes from the preceding plan kernel
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // launch epoch: publication flags of this launch carry it, so flags left by earlier launches need no
+    // clearing; the last CTA out advances it (no CTA can still be starting by then)
+    const uint32_t tag = static_cast<uint32_t>(*reinterpret_cast<volatile int *>(a.ctr + 2)) & kEpochMask;
     const int H = a.H, V = a.V, NV = V / VT;
 
     if (warp == 0)
@@ -224,6 +228,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const size_t mine = ((size_t)j * H + h) * NV + vt;
             const int HN = H * NV;
             const bool boundary = p % a.lb == 0;
+            const size_t soff = ((size_t)n * H + h) * KD * V + v0 + b;
+            // the first segment of a sequence with a state pass stages h0 in TMEM S' while the pass runs
+            const bool h0pre = p == 0 && nA > 0 && a.h0 != nullptr;
+            if (h0pre) {
+                for (int sub = 0; sub < 4; ++sub) {
+                    const int k1 = kb0 + 16 * sub;
+                    uint32_t x[16];
+#pragma unroll
+                    for (int uu = 0; uu < 16; ++uu)
+                        x[uu] = __float_as_uint(__ldcg(a.h0 + soff + (size_t)(k1 + uu) * V));
+                    tmem_st16(tmem + lrow + TM_SOP + k1, x);
+                }
+                tmem_wait_st();
+            }
             bool ok = true;
             if (nA > 0)
                 ok = bar_wait(g_done, naitems & 1, abort_w) && bar_wait(a_done, naitems & 1, abort_w);
@@ -246,7 +264,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __threadfence();
                 sync_team();
                 if (leader)
-                    flag_set(a.flags + u, 1);
+                    flag_set(a.flags + u, static_cast<int>(tag << 2 | 1u));
             }
             const int p0 = p > 0 ? (p - 1) / a.lb * a.lb : 0;
             if (p > 0) {
@@ -255,7 +273,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int i = p - 1; i > p0; --i) {
                     const int back = p - i;
                     if (leader)
-                        misc[2] = flag_wait_ge(a.flags + (u - back * HN), 1, abort_w);
+                        misc[2] = flag_wait_tag(a.flags + (u - back * HN), tag, 1, abort_w);
                     sync_team();
                     if (misc[2] == 0)
                         return false;   // uniform: every thread read the same value
@@ -300,7 +318,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 // the end state of the block's boundary segment
                 if (leader)
-                    misc[2] = flag_wait_ge(a.flags + (u - (p - p0) * HN), 2, abort_w);
+                    misc[2] = flag_wait_tag(a.flags + (u - (p - p0) * HN), tag, 2, abort_w);
                 sync_team();
                 if (misc[2] == 0)
                     return false;
@@ -308,7 +326,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // S_in -> TMEM S; a boundary segment with a state pass publishes S_out = 2^Gtot * S_in + dS
             const bool acc = p - 1 > p0;   // contributions were summed into TMEM S'
             const bool pub = nA > 0 && boundary;
-            const size_t soff = ((size_t)n * H + h) * KD * V + v0 + b;
             const float4 *bsrc = reinterpret_cast<const float4 *>(a.ss + (mine - (size_t)(p - p0) * HN) * tile);
             float4 *bdst = reinterpret_cast<float4 *>(a.ss + mine * tile);
 #pragma unroll 1
@@ -336,6 +353,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         sn[4 * w + 2] = __float_as_uint(fmaf(ex2(e.z), x[w].z, __uint_as_float(sn[4 * w + 2])));
                         sn[4 * w + 3] = __float_as_uint(fmaf(ex2(e.w), x[w].w, __uint_as_float(sn[4 * w + 3])));
                     }
+                } else if (h0pre) {
+                    tmem_ld16(tmem + lrow + TM_SOP + k1, sn);
+                    tmem_wait_ld(sn);
                 } else if (a.h0) {
 #pragma unroll
                     for (int uu = 0; uu < 16; ++uu)
@@ -365,7 +385,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             sync_team();
             fence_after();
             if (pub && leader)
-                flag_set(a.flags + u, 2);
+                flag_set(a.flags + u, static_cast<int>(tag << 2 | 2u));
             return true;
         };
 
@@ -766,6 +786,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (atomicAdd(a.ctr + 1, 1) == (int)gridDim.x - 1) {
             a.ctr[0] = 0;   // the last CTA out leaves the counters zeroed for the next call
             a.ctr[1] = 0;
+            a.ctr[2] = static_cast<int>((tag + 1) & kEpochMask);
             __threadfence();
         }
     }

@@ -257,33 +257,16 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, volatil
     return true;
 }
 
-// Spin (with short sleeps) until the global word `flag` equals `want` (acquire), or the limit / abort hits.
-__device__ __forceinline__ bool flag_wait(const int *flag, int want, volatile int *abort)
+// Publication flags tagged with the launch epoch: a flag holds (epoch << 2) | kind.  Waits until *flag
+// carries `tag` with a kind of at least `kind` and returns the value seen (0 after an abort or the time
+// limit).  Values left by earlier launches carry another epoch and count as unset.
+__device__ __forceinline__ int flag_wait_tag(const int *flag, uint32_t tag, int kind, volatile int *abort)
 {
     const unsigned long long t0 = global_ns();
     for (;;) {
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (v == want)
-            return true;
-        if (*abort)
-            return false;
-        if (global_ns() - t0 > kWaitNs) {
-            *abort = 1;
-            return false;
-        }
-        __nanosleep(64);
-    }
-}
-
-// Waits until *flag >= want and returns the value seen (0 after an abort or the time limit).
-__device__ __forceinline__ int flag_wait_ge(const int *flag, int want, volatile int *abort)
-{
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (v >= want)
+        if ((uint32_t)v >> 2 == tag && (v & 3) >= kind)
             return v;
         if (*abort)
             return 0;

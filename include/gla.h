@@ -77,7 +77,9 @@ typedef enum gla_dtype {
  *   chunk       chunk length; 64 is supported.  The result does not depend on it in exact arithmetic.
  *   K           64 or 128.          V  64, 128 or 256.          B, T, H, N >= 0 (T*H*max(K,V) < 2^31).
  *   workspace   device scratch of at least gla_fwd_workspace_size() bytes, 256-byte aligned, ZEROED
- *               BEFORE ITS FIRST USE (it carries the sticky status word between calls).  One workspace
+ *               BEFORE ITS FIRST USE and not written by the caller afterwards: its 256-byte header carries
+ *               the sticky status word, work counters and a launch epoch between calls (the epoch tags
+ *               the segment scan's publication flags, so they need no clearing per call).  One workspace
  *               must not be used by two calls that may run concurrently.
  *
  * Paths: bf16 inputs with K == 128 and V in {128, 256} run on the tcgen05 tensor cores with fp16 operands
