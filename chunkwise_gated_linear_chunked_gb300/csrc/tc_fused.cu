@@ -38,6 +38,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "gla_internal.h"
@@ -840,12 +841,17 @@ cudaError_t launch_fused_t(const Plan &pl, const Args &a, cudaStream_t s, int sm
     if (!encode_rows(&mo, f32o ? a.o : a.v, pl.V, pl.H, rows, 128, 32, false, f32o))
         return cudaErrorInvalidValue;
     auto f = gla_fused<Tout>;
-    static bool attr = false;
-    if (!attr) {
+    // the shared-memory opt-in is per device: remember it per device ordinal (set every time beyond 64)
+    static std::atomic<unsigned long long> attr_set{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return cudaErrorInvalidDevice;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
-        attr = true;
+        attr_set.fetch_or(bit, std::memory_order_release);
     }
     int nitems = pl.J * pl.H * (pl.V / VT);
     // scan block length: when every item runs at once the chain of end-state publications is the critical

@@ -59,10 +59,15 @@ def test_small_cases_elementwise(case):
 # 512-row segments: 9 segments x 16 heads = 144 items fit in one wave, so segments are grouped in blocks of 8
 # and segment 9 starts from the end state published by segment 8; 8 segments x 40 heads = 320 items take
 # several waves and use the plain serial chain.  Every head is compared with the oracle.
+# A varlen pack of 40 sequences (lengths 0 .. 2099, including empty and single-row ones).
+MANY_LENGTHS = [(i * 677) % 2100 if i % 9 else (i // 9) % 3 for i in range(40)]
 SCAN_CASES = [
     ("bf16", 1, 4608, 16, 128, 128, True, None),
     ("bf16", 1, 4096, 40, 128, 128, True, None),
     ("bf16", 2, 2560, 12, 128, 128, False, None),
+    ("bf16", 1, 40000, 1, 128, 128, True, None),     # one head: ~125 segments in one wave, 15 block hops
+    ("bf16", 1, 0, 2, 128, 128, True, MANY_LENGTHS),
+    ("bf16", 1, 0, 1, 128, 256, False, MANY_LENGTHS),
 ]
 
 
