@@ -1,7 +1,7 @@
-"""Oracle for the GLA forward pass — TEST INFRASTRUCTURE ONLY.
+"""Oracle for the GLA forward and backward passes — TEST INFRASTRUCTURE ONLY.
 
-A plain fp64 CPU implementation (``gla_oracle.c``) of the gated linear attention recurrence and of the
-chunk-local gate cumsum, wrapped with ctypes over numpy arrays.  Only ``tests/``, the smoke check in
+A plain fp64 CPU implementation (``gla_oracle.c``) of the gated linear attention recurrence, of its
+reverse-mode gradients and of the chunk-local gate cumsum, wrapped with ctypes over numpy arrays.  Only ``tests/``, the smoke check in
 ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
 neither imports nor links it; the two share no code.
 
@@ -14,9 +14,15 @@ Method citations (page "fla/ops/gla/fused_chunk.py"):
 Varlen convention (offsets, per-sequence states): page "fla/ops/ttt/fused_chunk.py",
 ``fused_chunk_ttt_linear_fwd_kernel`` and ``fused_chunk_ttt_linear``.
 
-Pins: every function here is checked in ``tests/test_oracle.py`` against quantities that do not come from
-the oracle itself (brute-force quadratic form, the g == 0 closed form, scalar closed forms, state-split
-invariance, varlen == separate runs, symmetry invariances, and hand-derived golden fixtures).
+Backward (``gla_bwd``): page "fla/ops/gla/fused_chunk.py", ``fused_chunk_gla_bwd_kernel`` and
+``bwd_inner_chunk`` (chunked gradients of the same recurrence) and ``FusedChunkGLAFunction.backward`` (dg from
+the reverse cumsum of ``q*dq - k*dk``); the oracle differentiates the plain recurrence step by step instead.
+
+Pins: every function here is checked in ``tests/test_oracle.py`` / ``tests/test_oracle_bwd.py`` against
+quantities that do not come from the oracle itself (brute-force quadratic form, the g == 0 closed form,
+scalar closed forms, state-split invariance, varlen == separate runs, symmetry invariances, hand-derived
+golden fixtures; for the backward: central finite differences of the forward oracle in fp64 and the
+gate-gradient identity).
 """
 from __future__ import annotations
 
@@ -34,7 +40,7 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -62,18 +68,29 @@ def _load():
             lib.oracle_gla_fwd.restype = i
             lib.oracle_chunk_local_cumsum.argtypes = [p, i, p, p, i, i, i, i, i, i]
             lib.oracle_chunk_local_cumsum.restype = i
+            _declare_bwd(lib)
             _lib = lib
     return _lib
 
 
+def _declare_bwd(lib):
+    p, i = ctypes.c_void_p, ctypes.c_int
+    lib.oracle_gla_bwd.argtypes = [p, p, p, p, p, i, p, p, p, p, p, p, p, p, i, i, i, i, i, i,
+                                   ctypes.c_double, i]
+    lib.oracle_gla_bwd.restype = i
+
+
 def _as_stored(x: np.ndarray):
-    """Return (contiguous array, dtype code).  bf16 tensors are passed as their raw uint16 words."""
+    """Return (contiguous array, dtype code).  bf16 tensors are passed as their raw uint16 words; float64
+    inputs (finite-difference checks) are read as they are."""
     x = np.ascontiguousarray(x)
     if x.dtype == np.float32:
         return x, F32
     if x.dtype == np.uint16:
         return x, BF16
-    raise TypeError(f"oracle inputs must be float32 or bf16 words (uint16), got {x.dtype}")
+    if x.dtype == np.float64:
+        return x, F64
+    raise TypeError(f"oracle inputs must be float32, float64 or bf16 words (uint16), got {x.dtype}")
 
 
 def _ptr(a):
@@ -87,6 +104,8 @@ def load_variant(path: str):
     p, i = ctypes.c_void_p, ctypes.c_int
     lib.oracle_gla_fwd.argtypes = [p, p, p, p, i, p, p, p, p, i, i, i, i, i, i, ctypes.c_double, i]
     lib.oracle_gla_fwd.restype = i
+    if hasattr(lib, "oracle_gla_bwd"):
+        _declare_bwd(lib)
     return lib
 
 
@@ -125,6 +144,50 @@ def gla_fwd(q, k, v, g, scale, h0=None, cu_seqlens=None, want_ht=True, nthreads=
     if rc < 0:
         raise RuntimeError(f"oracle_gla_fwd failed ({rc})")
     return o, ht, rc
+
+
+def gla_bwd(q, k, v, g, do, scale, h0=None, dht=None, cu_seqlens=None, nthreads=0, lib=None):
+    """fp64 reverse-mode gradients of the GLA recurrence for L = sum(o * do) + sum(ht * dht).
+
+    q, k, g: [B, T, H, K]; v, do: [B, T, H, V]; all one stored type (float32, bf16 words or float64).
+    h0, dht: optional [N, H, K, V] (widened to float64).  Returns float64 (dq, dk, dv, dg, dh0) shaped like
+    q, k, v, g and [N, H, K, V].
+    """
+    arrs = list(map(_as_stored, (q, k, v, g, do)))
+    if len({a[1] for a in arrs}) != 1:
+        raise TypeError("q, k, v, g, do must share one stored type")
+    (q, dt), (k, _), (v, _), (g, _), (do, _) = arrs
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:3] != q.shape[:3] or do.shape != v.shape:
+        raise ValueError("shape mismatch between q, k, v, g, do")
+    cu = None
+    N = B
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        N = cu.size - 1
+        if cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+            raise ValueError("cu_seqlens must be non-decreasing from 0 to T")
+    st = []
+    for x in (h0, dht):
+        if x is not None:
+            x = np.ascontiguousarray(x, dtype=np.float64)
+            if x.shape != (N, H, K, V):
+                raise ValueError(f"states must be [N, H, K, V] = {(N, H, K, V)}, got {x.shape}")
+        st.append(x)
+    dq = np.zeros(q.shape, np.float64)
+    dk = np.zeros(q.shape, np.float64)
+    dv = np.zeros(v.shape, np.float64)
+    dg = np.zeros(q.shape, np.float64)
+    dh0 = np.zeros((N, H, K, V), np.float64)
+    rc = (lib or _load()).oracle_gla_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(do), dt, _ptr(st[0]),
+                                         _ptr(st[1]), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dh0),
+                                         _ptr(cu), N, B, T, H, K, V, float(scale), int(nthreads))
+    if rc < 0:
+        raise RuntimeError(f"oracle_gla_bwd failed ({rc})")
+    return dq, dk, dv, dg, dh0
 
 
 def chunk_local_cumsum(g, chunk, cu_seqlens=None):

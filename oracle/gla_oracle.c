@@ -1,5 +1,5 @@
 /*
- * Oracle for the gated linear attention (GLA) forward pass — TEST INFRASTRUCTURE ONLY.
+ * Oracle for the gated linear attention (GLA) forward and backward passes — TEST INFRASTRUCTURE ONLY.
  *
  * Plain, slow, step-by-step fp64 CPU implementation.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg may load this library; the CUDA library never links or calls it and
@@ -29,7 +29,8 @@
  * The chunk size does not enter: the result is the same for every chunking in exact arithmetic.
  *
  * Also here: the chunk-local inclusive cumsum of g (chunk_local_cumsum as called by
- * FusedChunkGLAFunction.forward), with chunks aligned to each sequence's first token.
+ * FusedChunkGLAFunction.forward), with chunks aligned to each sequence's first token, and the backward
+ * pass of the same recurrence by plain reverse-mode differentiation (oracle_gla_bwd, below).
  */
 #include <math.h>
 #include <pthread.h>
@@ -38,13 +39,16 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F64 = 2 };
 
-/* Exact widening of one stored element to double. bf16 is the high half of an IEEE binary32. */
+/* Exact widening of one stored element to double. bf16 is the high half of an IEEE binary32; fp64 inputs
+ * (used by the finite-difference checks of the backward) are read as they are. */
 static double widen(const void *base, size_t idx, int dtype)
 {
     if (dtype == ORACLE_F32)
         return (double)((const float *)base)[idx];
+    if (dtype == ORACLE_F64)
+        return ((const double *)base)[idx];
     uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
     float f;
     memcpy(&f, &bits, sizeof f);
@@ -134,7 +138,7 @@ int oracle_gla_fwd(const void *q, const void *k, const void *v, const void *g, i
 {
     if (!q || !k || !v || !g || !o || H <= 0 || K <= 0 || V <= 0 || B < 0 || T < 0)
         return -1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16)
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64)
         return -1;
     int32_t *dense = NULL;
     const int32_t *cu = cu_seqlens;
@@ -202,4 +206,193 @@ int oracle_chunk_local_cumsum(const void *g, int dtype, double *G, const int32_t
             }
     }
     return 0;
+}
+
+/*
+ * Backward pass of the recurrence above, by reverse-mode differentiation of its steps (the pages' chunked
+ * backward, fused_chunk_gla_bwd_kernel and bwd_inner_chunk of "fla/ops/gla/fused_chunk.py", is a
+ * re-association of the same gradients).  For the loss L = sum(o * do) + sum(ht * dht):
+ *
+ *     A_t      = dL/dS_t (everything after S_t included):   A_last = dht + scale q_last^T do_last,
+ *                A_t = diag(exp(g_{t+1})) A_{t+1} + scale q_t^T do_t
+ *     dq_t     = scale * S_t do_t^T              (contract over V)
+ *     dk_t     = A_t v_t^T                       (contract over V)
+ *     dv_t     = k_t A_t                         (contract over K)
+ *     dg_t[k]  = exp(g_t[k]) * sum_v A_t[k,v] S_{t-1}[k,v]
+ *     dh0      = diag(exp(g_first)) A_first
+ *
+ * S_{t-1} is needed on the way back: the forward sweep keeps the state at every 64th step and each block
+ * of 64 steps is recomputed from its checkpoint before it is walked backwards.  do has the stored type of
+ * q, k, v, g; h0 and dht are double [N,H,K,V] or NULL (zeros).  Outputs are double in the layouts of
+ * q / v / h0; dh0 may be NULL.  Returns the threads used, or a negative value on bad arguments.
+ */
+enum { BWD_BLOCK = 64 };
+
+typedef struct {
+    const void *q, *k, *v, *g, *dout;
+    int dtype;
+    const double *h0, *dht;
+    double *dq, *dk, *dv, *dg, *dh0;
+    const int32_t *cu;
+    int N, H, K, V;
+    double scale;
+    int next;
+    pthread_mutex_t mu;
+} bwd_job;
+
+/* one step of the forward recurrence on a K x V state */
+static void fwd_step(const bwd_job *J, long t, int h, double *S)
+{
+    const int H = J->H, K = J->K, V = J->V;
+    const size_t kb = ((size_t)t * H + h) * K, vb = ((size_t)t * H + h) * V;
+    for (int i = 0; i < K; ++i) {
+        const double e = exp(widen(J->g, kb + i, J->dtype));
+        const double kt = widen(J->k, kb + i, J->dtype);
+        double *srow = S + (size_t)i * V;
+        for (int j = 0; j < V; ++j)
+            srow[j] = e * srow[j] + kt * widen(J->v, vb + j, J->dtype);
+    }
+}
+
+static int bwd_one(bwd_job *J, int item)
+{
+    const int n = item / J->H, h = item % J->H;
+    const int H = J->H, K = J->K, V = J->V;
+    const long bos = J->cu[n], eos = J->cu[n + 1], len = eos - bos;
+    const size_t KV = (size_t)K * V;
+    const long nb = (len + BWD_BLOCK - 1) / BWD_BLOCK;
+    /* ck[m] = state before block m (ck[0] = h0); blk[i] = state after the i-th step of the current block */
+    double *ck = (double *)malloc(sizeof(double) * KV * (size_t)(nb > 0 ? nb : 1));
+    double *blk = (double *)malloc(sizeof(double) * KV * BWD_BLOCK);
+    double *S = (double *)malloc(sizeof(double) * KV);
+    double *A = (double *)malloc(sizeof(double) * KV);
+    if (!ck || !blk || !S || !A) {
+        free(ck); free(blk); free(S); free(A);
+        return -2;
+    }
+    const size_t st = ((size_t)n * H + h) * KV;
+    for (size_t e = 0; e < KV; ++e) {
+        S[e] = J->h0 ? J->h0[st + e] : 0.0;
+        A[e] = J->dht ? J->dht[st + e] : 0.0;
+    }
+    for (long t = bos; t < eos; ++t) {
+        if ((t - bos) % BWD_BLOCK == 0)
+            memcpy(ck + (size_t)((t - bos) / BWD_BLOCK) * KV, S, sizeof(double) * KV);
+        fwd_step(J, t, h, S);
+    }
+    for (long m = nb - 1; m >= 0; --m) {
+        const long b0 = bos + m * BWD_BLOCK, b1 = b0 + BWD_BLOCK < eos ? b0 + BWD_BLOCK : eos;
+        memcpy(S, ck + (size_t)m * KV, sizeof(double) * KV);
+        for (long t = b0; t < b1; ++t) {
+            fwd_step(J, t, h, S);
+            memcpy(blk + (size_t)(t - b0) * KV, S, sizeof(double) * KV);
+        }
+        for (long t = b1 - 1; t >= b0; --t) {
+            const size_t kb = ((size_t)t * H + h) * K, vb = ((size_t)t * H + h) * V;
+            const double *St = blk + (size_t)(t - b0) * KV;                             /* S_t */
+            const double *Sp = t > b0 ? blk + (size_t)(t - b0 - 1) * KV : ck + (size_t)m * KV;  /* S_{t-1} */
+            /* A <- A + scale q_t^T do_t: now dL/dS_t */
+            for (int i = 0; i < K; ++i) {
+                const double qi = J->scale * widen(J->q, kb + i, J->dtype);
+                for (int j = 0; j < V; ++j)
+                    A[(size_t)i * V + j] += qi * widen(J->dout, vb + j, J->dtype);
+            }
+            for (int i = 0; i < K; ++i) {
+                double aq = 0.0, ak = 0.0, ag = 0.0;
+                for (int j = 0; j < V; ++j) {
+                    const double dj = widen(J->dout, vb + j, J->dtype);
+                    aq += St[(size_t)i * V + j] * dj;
+                    ak += A[(size_t)i * V + j] * widen(J->v, vb + j, J->dtype);
+                    ag += A[(size_t)i * V + j] * Sp[(size_t)i * V + j];
+                }
+                J->dq[kb + i] = J->scale * aq;
+                J->dk[kb + i] = ak;
+                J->dg[kb + i] = exp(widen(J->g, kb + i, J->dtype)) * ag;
+            }
+            for (int j = 0; j < V; ++j) {
+                double av = 0.0;
+                for (int i = 0; i < K; ++i)
+                    av += widen(J->k, kb + i, J->dtype) * A[(size_t)i * V + j];
+                J->dv[vb + j] = av;
+            }
+            /* A <- diag(exp(g_t)) A: dL/dS_{t-1} before the o_{t-1} term */
+            for (int i = 0; i < K; ++i) {
+                const double e = exp(widen(J->g, kb + i, J->dtype));
+                for (int j = 0; j < V; ++j)
+                    A[(size_t)i * V + j] *= e;
+            }
+        }
+    }
+    if (J->dh0)
+        memcpy(J->dh0 + st, A, sizeof(double) * KV);
+    free(ck); free(blk); free(S); free(A);
+    return 0;
+}
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *J = (bwd_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int item = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (item >= J->N * J->H)
+            break;
+        if (bwd_one(J, item) != 0)
+            return (void *)1;
+    }
+    return NULL;
+}
+
+int oracle_gla_bwd(const void *q, const void *k, const void *v, const void *g, const void *dout, int dtype,
+                   const double *h0, const double *dht, double *dq, double *dk, double *dv, double *dg,
+                   double *dh0, const int32_t *cu_seqlens, int N, int B, int T, int H, int K, int V,
+                   double scale, int nthreads)
+{
+    if (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg || H <= 0 || K <= 0 || V <= 0 || B < 0 ||
+        T < 0)
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64)
+        return -1;
+    int32_t *dense = NULL;
+    const int32_t *cu = cu_seqlens;
+    if (!cu) {
+        N = B;
+        dense = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N + 1));
+        if (!dense)
+            return -2;
+        for (int n = 0; n <= N; ++n)
+            dense[n] = n * T;
+        cu = dense;
+    }
+    if (N == 0) {
+        free(dense);
+        return 0;
+    }
+    if (dh0)
+        memset(dh0, 0, sizeof(double) * (size_t)N * H * K * V);
+    bwd_job J = {q, k, v, g, dout, dtype, h0, dht, dq, dk, dv, dg, dh0, cu, N, H, K, V, scale, 0,
+                 PTHREAD_MUTEX_INITIALIZER};
+    const int nt = resolve_threads(nthreads, N * H);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    int rc = nt;
+    if (!tid) {
+        free(dense);
+        return -2;
+    }
+    int started = 0;
+    for (; started < nt; ++started)
+        if (pthread_create(&tid[started], NULL, bwd_worker, &J) != 0)
+            break;
+    if (started == 0 && bwd_worker(&J))
+        rc = -2;
+    for (int i = 0; i < started; ++i) {
+        void *res = NULL;
+        pthread_join(tid[i], &res);
+        if (res)
+            rc = -2;
+    }
+    free(tid);
+    free(dense);
+    return started ? rc : (rc < 0 ? rc : 1);
 }
