@@ -8,7 +8,8 @@ stream (gla_profile_events).  ``e2e`` repeats the measurement through the same p
 copied host->device from pinned memory and o/ht copied back inside the timed region.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this method has) on a bounded sample of
-the same workload instead.
+the same workload instead.  ``--pass bwd`` measures the backward (gla_bwd: dq, dk, dv, dg, dh0 for a random
+upstream gradient of o and of the final state) on the same workload instead of the forward.
 
 Multi-GPU (torchrun): the workload's sequences are independent problems, so each rank runs its own copy
 (weak scaling, no collective on the data path); the step time is the max over ranks.
@@ -47,6 +48,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd")
     return ap.parse_args(argv)
 
 
@@ -223,6 +225,8 @@ def main(argv=None):
     from chunkwise_gated_linear_chunked_gb300 import binding
 
     inp = workload_inputs(args.workload)
+    if args.pass_ == "bwd":
+        return run_backward(args, w, inp, dev, dist, world, rank)
     wu = work_units(inp)
     q, k, v, g = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.g))
     h0 = None if inp.h0 is None else inp.h0.to(dev)
@@ -319,6 +323,156 @@ def main(argv=None):
             "kernels_ms": {n: round(statistics.mean(v), 5) for n, v in per_kernel.items()},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+FP32_LANES_PER_SM = 128   # fp32 FMA lanes per SM (4 sub-partitions x 32)
+
+
+def bwd_chunks(inp):
+    if inp.cu_seqlens is None:
+        return inp.q.shape[0] * -(-inp.q.shape[1] // inp.chunk)
+    lens = (inp.cu_seqlens[1:] - inp.cu_seqlens[:-1]).tolist()
+    return sum(max(1, -(-L // inp.chunk)) for L in lens)
+
+
+def bwd_kernel_flops(name, inp):
+    """Algorithmic flops of one launch of a backward kernel (2 per multiply-add, masked tiles counted)."""
+    C, K, V, H = inp.chunk, inp.K, inp.V, inp.H
+    nc = bwd_chunks(inp) * H
+    if name == "bwd_grads":
+        return 2 * nc * (C * C * (3 * K + 2 * V) + 3 * C * K * V)
+    if name == "bwd_chunk_sums":
+        return 2 * nc * 2 * C * K * V
+    if name == "bwd_scan":
+        return 2 * 2 * nc * K * V
+    return 0
+
+
+def oracle_bwd_sample(inp, do, dht, seconds):
+    """The fp64 backward oracle over groups of heads for about `seconds`; tokens/s, threads, description."""
+    import oracle
+    from chunkwise_gated_linear_chunked_gb300.inputs import stored_numpy
+    cores = os.cpu_count() or 1
+    H = inp.H
+    per_group = max(1, min(H, -(-cores // max(inp.N, 1))))
+    t0 = time.perf_counter()
+    token_heads, threads, groups, h = 0, 1, 0, 0
+    while True:
+        heads = [(h + i) % H for i in range(per_group)]
+        sel = lambda x: x[:, :, heads].contiguous()
+        arrs = [stored_numpy(sel(x)) for x in (inp.q, inp.k, inp.v, inp.g, do)]
+        st = lambda x: None if x is None else x[:, heads].contiguous().numpy()
+        cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
+        oracle.gla_bwd(*arrs, inp.scale, h0=st(inp.h0), dht=st(dht), cu_seqlens=cu, nthreads=cores)
+        threads = min(cores, inp.N * len(heads))
+        token_heads += inp.q.shape[0] * inp.q.shape[1] * len(heads)
+        groups += 1
+        h = (h + per_group) % H
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    desc = (f"fp64 backward oracle over {groups} group(s) of {per_group} head(s) x all {inp.N} sequence(s) "
+            f"({token_heads} token-heads, {el:.1f} s wall)")
+    return token_heads / H / el, threads, desc
+
+
+def run_backward(args, w, inp, dev, dist, world, rank):
+    """The backward step: one gla_bwd over the workload with a seeded random upstream gradient of o (input
+    dtype) and of the final state (fp32); inputs resident in HBM, L2 flushed before each step."""
+    import torch
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    B, T, H, K, V, N = inp.q.shape[0], inp.q.shape[1], inp.H, inp.K, inp.V, inp.N
+    code = binding.GLA_F32 if inp.dtype == "f32" else binding.GLA_BF16
+    gen = torch.Generator().manual_seed(w.seed + 7)
+    do_cpu = torch.randn(tuple(inp.v.shape), generator=gen).to(inp.v.dtype)
+    dht_cpu = torch.randn(N, H, K, V, generator=gen) * 0.5
+    q, k, v, g, do = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.g, do_cpu))
+    dht = dht_cpu.to(dev)
+    h0 = None if inp.h0 is None else inp.h0.to(dev)
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dg = (torch.empty(B, T, H, K, **f32) for _ in range(3))
+    dv = torch.empty(B, T, H, V, **f32)
+    dh0 = torch.empty(N, H, K, V, **f32)
+    ws = torch.zeros(max(256, binding.bwd_workspace_size(B, T, H, K, V, N, inp.chunk, code)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        rc = binding.bwd_into(q, k, v, g, do, inp.scale, h0, dht, dq, dk, dv, dg, dh0, cu, N, B, T, H, K, V,
+                              inp.chunk, code, ws, stream)
+        if rc != 0:
+            raise binding.GlaError(rc, "gla_bwd")
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if binding.get_status(ws) != 0:
+        raise RuntimeError("device status error during warm-up")
+    timer = binding.KernelTimer()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms, per_kernel, launches = [], {}, 0
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        for _ in range(args.steps):
+            flush.zero_()
+            with timer:
+                start.record(stream)
+                step()
+                end.record(stream)
+            torch.cuda.synchronize()
+            step_ms.append(start.elapsed_time(end))
+            res = timer.results()
+            launches += len(res)
+            for name, ms in res:
+                per_kernel.setdefault(name, []).append(ms)
+    if dist is not None:
+        dist.barrier()
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
+    if binding.get_status(ws) != 0:
+        raise RuntimeError("device status error in the timed region")
+    tokens = B * T
+    value = whole_job_value(tokens, args.steps, world, total_ms)
+    ms_per_step = total_ms / args.steps
+    kern_tot = {n: sum(x) for n, x in per_kernel.items()}
+    dom = max(kern_tot, key=kern_tot.get)
+    dom_ms = statistics.mean(per_kernel[dom])
+    props = torch.cuda.get_device_properties(dev)
+    csum = clocks.summary()
+    mhz = csum.get("sm_max_mhz") or 2070.0
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    flops = bwd_kernel_flops(dom, inp)
+    achieved = flops / (dom_ms / 1e3) / 1e12
+    roofline = {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                               f"{mhz:.0f} MHz", "traffic": None, "algorithmic_flops_per_launch": flops}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, threads, desc = oracle_bwd_sample(inp, do_cpu, dht_cpu, args.cpu_seconds)
+        cpu = {"value": round(val, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        line = {
+            "metric": "GLA bwd tokens/s on 1 GB300 (dq, dk, dv, dg, dh0); % of fp32 CUDA-core peak",
+            "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "pass": "bwd", "desc": w.note, "B": B, "T": T, "H": H,
+                       "K": K, "V": V, "N": N, "chunk": inp.chunk, "input_dtype": inp.dtype,
+                       "h0": inp.h0 is not None, "dht": True,
+                       "l2": "flushed before every timed step (zero-fill of a 2x L2 buffer, outside the events)",
+                       "parallelism": "replicas" if world == 1 else f"weak x{world} (independent sequences)"},
+            "roofline": roofline,
+            "kernels_ms": {n: round(statistics.mean(x), 5) for n, x in per_kernel.items()},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": csum,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

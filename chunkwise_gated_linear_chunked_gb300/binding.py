@@ -19,7 +19,8 @@ GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_ALIGNMENT, GLA_ERR_WOR
 GLA_F32, GLA_BF16, GLA_BF16_OBF16 = 0, 1, 2
 
 EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",
-           "gla_profile_events", "gla_profile_launches", "gla_kernel_name", "gla_fwd_noalloc")
+           "gla_profile_events", "gla_profile_launches", "gla_kernel_name", "gla_fwd_noalloc", "gla_bwd",
+           "gla_bwd_workspace_size")
 
 if not os.path.exists(LIB):
     raise ImportError(f"libgla.so not built ({LIB}); call chunkwise_gated_linear_chunked_gb300.build.build()")
@@ -42,6 +43,11 @@ _lib.gla_profile_launches.argtypes = []
 _lib.gla_profile_launches.restype = _i
 _lib.gla_kernel_name.argtypes = [_i]
 _lib.gla_kernel_name.restype = ctypes.c_char_p
+_lib.gla_bwd.argtypes = [_p, _p, _p, _p, _p, _f, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i,
+                         _i, _p, _sz, _p]
+_lib.gla_bwd.restype = _i
+_lib.gla_bwd_workspace_size.argtypes = [_i] * 8
+_lib.gla_bwd_workspace_size.restype = _sz
 
 
 class GlaError(RuntimeError):
@@ -134,6 +140,54 @@ def gla_fwd(q, k, v, g, scale=None, initial_state=None, output_final_state=True,
     if rc != GLA_OK:
         raise GlaError(rc)
     return o, ht
+
+
+def bwd_workspace_size(B, T, H, K, V, N, chunk=64, dtype=GLA_BF16) -> int:
+    return int(_lib.gla_bwd_workspace_size(B, T, H, K, V, N, chunk, dtype))
+
+
+def bwd_into(q, k, v, g, do, scale, h0, dht, dq, dk, dv, dg, dh0, cu_seqlens, N, B, T, H, K, V, chunk, dtype,
+             workspace, stream=None) -> int:
+    """Raw backward call: tensors (or None) are passed as device pointers.  Returns the code."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return int(_lib.gla_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(do), float(scale), _ptr(h0), _ptr(dht),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dh0), _ptr(cu_seqlens), int(N), int(B),
+                            int(T), int(H), int(K), int(V), int(chunk), int(dtype), _ptr(workspace), nbytes,
+                            _stream_handle(stream)))
+
+
+def gla_bwd(q, k, v, g, do, scale=None, initial_state=None, dht=None, cu_seqlens=None, chunk=64, stream=None,
+            workspace=None, want_dh0=True):
+    """GLA backward on the GPU for L = sum(o * do) + sum(ht * dht).
+
+    q, k, g: [B, T, H, K]; v, do: [B, T, H, V] (cuda, contiguous, all fp32 or all bf16).  initial_state and
+    dht: optional fp32 [N, H, K, V].  Returns fp32 (dq, dk, dv, dg, dh0 or None).
+    """
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    code = {torch.float32: GLA_F32, torch.bfloat16: GLA_BF16}.get(q.dtype)
+    if code is None:
+        raise GlaError(GLA_ERR_UNSUPPORTED, f"gla_bwd dtype {q.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("do", do)):
+        if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+            raise GlaError(GLA_ERR_INVALID_ARG, f"gla_bwd: {name} must be a contiguous cuda {q.dtype} tensor")
+    for name, t in (("initial_state", initial_state), ("dht", dht)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise GlaError(GLA_ERR_INVALID_ARG, f"gla_bwd: {name} must be a contiguous fp32 tensor")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dk, dg = (torch.empty(B, T, H, K, **f32) for _ in range(3))
+    dv = torch.empty(B, T, H, V, **f32)
+    dh0 = torch.empty(N, H, K, V, **f32) if want_dh0 else None
+    if workspace is None:
+        workspace = get_workspace(bwd_workspace_size(B, T, H, K, V, N, chunk, code), q.device)
+    rc = bwd_into(q, k, v, g, do, scale, initial_state, dht, dq, dk, dv, dg, dh0, cu_seqlens, N, B, T, H, K, V,
+                  chunk, code, workspace, stream)
+    if rc != GLA_OK:
+        raise GlaError(rc, "gla_bwd")
+    return dq, dk, dv, dg, dh0
 
 
 def get_status(workspace, stream=None) -> int:

@@ -168,7 +168,10 @@ struct Profile {
 };
 thread_local Profile g_prof;
 
-enum KernelId { K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_FUSED_TC = 7 };
+enum KernelId {
+    K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_FUSED_TC = 7,
+    K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11
+};
 
 // Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
 template <typename Fn>
@@ -402,6 +405,175 @@ extern "C" const char *gla_kernel_name(int kernel_id)
     case K_SCAN: return "scan_segments";
     case K_OUT_FFMA: return "out_ffma";
     case K_FUSED_TC: return "fused_tc";
+    case K_BWD_SUMS: return "bwd_chunk_sums";
+    case K_BWD_SCAN: return "bwd_scan";
+    case K_BWD_GRADS: return "bwd_grads";
+    case K_BWD_DG: return "bwd_dg";
     default: return "unknown";
     }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// Backward pass
+// ---------------------------------------------------------------------------------------------------
+namespace gla {
+namespace {
+
+struct BwdPlan {
+    int J, NC;
+    size_t off_table, off_seq, off_dS, off_dR, off_gl, off_ht, off_dgt, total;
+};
+
+void make_bwd_plan(BwdPlan &bp, int B, int T, int H, int K, int V, int N, bool varlen)
+{
+    std::memset(&bp, 0, sizeof bp);
+    const int C = kChunk;
+    bp.NC = varlen ? 0 : (T + C - 1) / C;
+    bp.J = varlen ? N + (T + C - 1) / C : B * bp.NC;
+    const int nseq = varlen ? N : B;
+    size_t off = kAlign;   // status header
+    bp.off_table = off;
+    if (varlen)
+        off += align_up(sizeof(int4) * (size_t)bp.J);
+    bp.off_seq = off;
+    if (varlen)
+        off += align_up(sizeof(int2) * (size_t)N);
+    const size_t tile = sizeof(float) * (size_t)bp.J * H * K * V;
+    bp.off_dS = off;
+    off += align_up(tile);
+    bp.off_dR = off;
+    off += align_up(tile);
+    bp.off_gl = off;
+    off += align_up(sizeof(float) * (size_t)bp.J * H * K);
+    bp.off_ht = off;
+    off += align_up(sizeof(float) * (size_t)nseq * H * K * V);
+    bp.off_dgt = off;
+    off += align_up(sizeof(float) * (size_t)bp.J * H * K);
+    bp.total = off;
+}
+
+int check_bwd_shape(int B, int T, int H, int K, int V, int N, int chunk, int dtype, bool varlen)
+{
+    if (dtype != GLA_F32 && dtype != GLA_BF16)
+        return GLA_ERR_UNSUPPORTED;
+    if (B < 0 || T < 0 || H <= 0 || N < 0)
+        return GLA_ERR_INVALID_ARG;
+    if (varlen ? B != 1 : N != B)
+        return GLA_ERR_INVALID_ARG;
+    if (chunk != kChunk || !bwd_supported(dtype, K, V))
+        return GLA_ERR_UNSUPPORTED;
+    const long long rows = varlen ? (long long)T : (long long)B * T;
+    if (rows * H * (K > V ? K : V) >= (1LL << 31) || (long long)(N + T / kChunk + 1) * H * K * V >= (1LL << 31))
+        return GLA_ERR_UNSUPPORTED;
+    return GLA_OK;
+}
+
+}  // namespace
+}  // namespace gla
+
+using namespace gla;
+
+extern "C" size_t gla_bwd_workspace_size(int B, int T, int H, int K, int V, int N, int chunk, int dtype)
+{
+    if (check_bwd_shape(B, T, H, K, V, N, chunk, dtype, false) != GLA_OK &&
+        check_bwd_shape(1, T, H, K, V, N, chunk, dtype, true) != GLA_OK)
+        return 0;
+    BwdPlan a, b;
+    make_bwd_plan(a, B, T, H, K, V, B, false);
+    make_bwd_plan(b, 1, T, H, K, V, N, true);
+    return a.total > b.total ? a.total : b.total;
+}
+
+extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *g, const void *dout, float scale,
+                       const float *h0, const float *dht, float *dq, float *dk, float *dv, float *dg, float *dh0,
+                       const int32_t *cu_seqlens, int N, int B, int T, int H, int K, int V, int chunk, int dtype,
+                       void *workspace, size_t workspace_bytes, void *stream)
+{
+    const bool varlen = cu_seqlens != nullptr;
+    int rc = check_bwd_shape(B, T, H, K, V, N, chunk, dtype, varlen);
+    if (rc != GLA_OK)
+        return rc;
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return GLA_ERR_INVALID_ARG;
+    const size_t rows = varlen ? (size_t)T : (size_t)B * T;
+    const size_t esz = dtype == GLA_F32 ? 4 : 2;
+    if (rows > 0 && (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg))
+        return GLA_ERR_INVALID_ARG;
+    for (const void *p : {q, k, v, g, dout, (const void *)h0, (const void *)dht, (const void *)dq,
+                          (const void *)dk, (const void *)dv, (const void *)dg, (const void *)dh0,
+                          (const void *)cu_seqlens})
+        if (misaligned(p))
+            return GLA_ERR_ALIGNMENT;
+    BwdPlan bp;
+    make_bwd_plan(bp, B, T, H, K, V, N, varlen);
+    if (!workspace || workspace_bytes < bp.total)
+        return GLA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
+        return GLA_ERR_ALIGNMENT;
+    // aliasing: every output overlaps no input, no workspace and no other output
+    const size_t sbytes = (size_t)(varlen ? N : B) * H * K * V * 4;
+    const Range in[] = {range_of(q, rows * H * K * esz), range_of(k, rows * H * K * esz),
+                        range_of(g, rows * H * K * esz), range_of(v, rows * H * V * esz),
+                        range_of(dout, rows * H * V * esz), range_of(h0, h0 ? sbytes : 0),
+                        range_of(dht, dht ? sbytes : 0),
+                        range_of(cu_seqlens, varlen ? sizeof(int32_t) * (size_t)(N + 1) : 0),
+                        range_of(workspace, bp.total)};
+    const Range out[] = {range_of(dq, rows * H * K * 4), range_of(dk, rows * H * K * 4),
+                         range_of(dg, rows * H * K * 4), range_of(dv, rows * H * V * 4),
+                         range_of(dh0, dh0 ? sbytes : 0)};
+    for (size_t i = 0; i < sizeof out / sizeof out[0]; ++i) {
+        for (const Range &r : in)
+            if (overlap(out[i], r))
+                return GLA_ERR_INVALID_ARG;
+        for (size_t j2 = i + 1; j2 < sizeof out / sizeof out[0]; ++j2)
+            if (overlap(out[i], out[j2]))
+                return GLA_ERR_INVALID_ARG;
+    }
+    for (size_t i = 0; i + 1 < sizeof in / sizeof in[0]; ++i)
+        if (overlap(in[i], in[8]))
+            return GLA_ERR_INVALID_ARG;
+    const int nseq = varlen ? N : B;
+    g_prof.launches = 0;
+    if (nseq == 0)
+        return GLA_OK;
+
+    char *ws = static_cast<char *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    BwdArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.g = g; a.dout = dout; a.h0 = h0; a.dht = dht;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dh0 = dh0;
+    a.scale = scale;
+    a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.N = nseq; a.NC = bp.NC;
+    a.status = reinterpret_cast<int *>(ws);
+    a.dS = reinterpret_cast<float *>(ws + bp.off_dS);
+    a.dR = reinterpret_cast<float *>(ws + bp.off_dR);
+    a.gl = reinterpret_cast<float *>(ws + bp.off_gl);
+    a.ht = reinterpret_cast<float *>(ws + bp.off_ht);
+    a.dgt = reinterpret_cast<float *>(ws + bp.off_dgt);
+    if (varlen) {
+        // the forward's slot planner with 64-row segments gives the chunk table
+        Args pa;
+        std::memset(&pa, 0, sizeof pa);
+        pa.cu = cu_seqlens; pa.N = N; pa.T = T; pa.L = kChunk; pa.J = bp.J; pa.seg_cap = 0;
+        pa.status = a.status;
+        pa.table = reinterpret_cast<const int4 *>(ws + bp.off_table);
+        pa.seqinfo = reinterpret_cast<const int2 *>(ws + bp.off_seq);
+        a.table = pa.table;
+        a.seqinfo = pa.seqinfo;
+        Plan pl;
+        std::memset(&pl, 0, sizeof pl);
+        if (profiled(K_PLAN, s, [&] { return launch_plan_varlen(pl, pa, s); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+    }
+    const int J = bp.J;
+    if (J > 0 && profiled(K_BWD_SUMS, s, [&] { return launch_bwd_sums(a, J, dtype, s); }) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    if (profiled(K_BWD_SCAN, s, [&] { return launch_bwd_scan(a, s); }) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    if (J > 0 && profiled(K_BWD_GRADS, s, [&] { return launch_bwd_grads(a, J, dtype, s); }) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    if (profiled(K_BWD_DG, s, [&] { return launch_bwd_dg(a, J, s); }) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    return GLA_OK;
 }

@@ -52,6 +52,24 @@ struct Args {
     int *status;           // sticky device status word
 };
 
+// Backward kernel arguments (passed by value).  Chunk slots: dense j = n * NC + c; varlen from the slot
+// table (plan_varlen with 64-row segments).
+struct BwdArgs {
+    const void *q, *k, *v, *g, *dout;
+    const float *h0, *dht;
+    float *dq, *dk, *dv, *dg, *dh0;   // fp32 outputs; dh0 may be nullptr
+    float scale;
+    int B, T, H, K, V, N, NC;
+    const int4 *table;                // varlen: per chunk slot {n, p, bos, eos}; n < 0 marks an unused slot
+    const int2 *seqinfo;              // varlen: per sequence {first slot, slot count}
+    float *dS;                        // [J][H][K][V]: chunk contributions, then chunk-start states
+    float *dR;                        // [J][H][K][V]: adjoint contributions, then chunk-end adjoints
+    float *gl;                        // [J][H][K]: chunk total log-decay (natural log)
+    float *ht;                        // [N][H][K][V]: final states
+    float *dgt;                       // [J][H][K]: chunk sums of q dq - k dk, then their carries
+    int *status;
+};
+
 // Map slot j to (sequence n, segment p, rows [bos, eos), sequence end).  False for an unused slot.
 __device__ __forceinline__ bool resolve_slot(const Args &a, int j, int &n, int &p, int &bos, int &eos,
                                              int &send)
@@ -89,6 +107,11 @@ cudaError_t launch_scan(const Plan &pl, const Args &a, cudaStream_t s);
 cudaError_t launch_out_ffma(const Plan &pl, const Args &a, cudaStream_t s);
 bool tc_supported(int dtype, int K, int V);
 cudaError_t launch_fused_tc(const Plan &pl, const Args &a, cudaStream_t s, int sms);
+bool bwd_supported(int dtype, int K, int V);
+cudaError_t launch_bwd_sums(const BwdArgs &a, int J, int dtype, cudaStream_t s);
+cudaError_t launch_bwd_scan(const BwdArgs &a, cudaStream_t s);
+cudaError_t launch_bwd_grads(const BwdArgs &a, int J, int dtype, cudaStream_t s);
+cudaError_t launch_bwd_dg(const BwdArgs &a, int J, cudaStream_t s);
 cudaError_t launch_chunk_cumsum(const void *g, float *G, const int32_t *cu, int N, int B, int T, int H,
                                 int K, int chunk, int dtype, cudaStream_t s);
 

@@ -135,7 +135,7 @@ int gla_chunk_local_cumsum(const void *g, float *G, const int32_t *cu_seqlens, i
  * gla_fwd_workspace_size() exceeds 32 MiB are rejected with GLA_ERR_WORKSPACE before anything is enqueued.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture.  Nothing is allocated: no cudaMalloc,
- * cudaFree or allocating library routine is called (each call enqueues a 256-byte cudaMemsetAsync that
+ * cudaFree or allocating library routine is called (each call enqueues a 16-byte cudaMemsetAsync that
  * clears the status word, then the gla_fwd kernels).  All calls share the one array, so calls that may
  * overlap on the GPU (different streams without ordering) race and must not be made.  Device-side
  * conditions (bad cu_seqlens, GLA_ERR_RANGE, GLA_ERR_TIMEOUT) are recorded in the array and cleared by
@@ -146,14 +146,41 @@ int gla_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, 
                     int K, int V, int chunk, int dtype, void *stream);
 
 /*
+ * gla_bwd — gradients of the forward above (page "fla/ops/gla/fused_chunk.py": fused_chunk_gla_bwd_kernel,
+ * bwd_inner_chunk, FusedChunkGLAFunction.backward) for the loss L = sum(o * dout) + sum(ht * dht):
+ *
+ *   dq = dL/dq, dk = dL/dk, dg = dL/dg   [rows, H, K] fp32 (device, written)
+ *   dv = dL/dv                           [rows, H, V] fp32 (device, written)
+ *   dh0 = dL/dh0                         [N, H, K, V] fp32 (device) or NULL to skip it
+ *
+ * q, k, v, g, scale, h0, cu_seqlens, N, B, T, H, chunk: as for gla_fwd (the forward is recomputed; pass the
+ * same h0 the forward used, or NULL for a zero initial state).  dout [rows, H, V] in the input dtype (the
+ * gradient of o); dht [N, H, K, V] fp32 or NULL (no loss on the final state).  dtype GLA_F32 (every input
+ * fp32) or GLA_BF16 (q, k, v, g, dout bf16); all arithmetic is fp32 on CUDA cores.  K and V in {64, 128};
+ * chunk 64.  workspace: at least gla_bwd_workspace_size() bytes, 256-byte aligned, zeroed before its first
+ * use (status word in its first bytes); it holds the chunk-start states and chunk-end adjoints
+ * (2 * chunks * H * K * V fp32).  Outputs must not overlap any input, the workspace or one another.  The
+ * library allocates nothing and is stream-ordered.  Errors as for gla_fwd (GLA_ERR_UNSUPPORTED for other
+ * dtypes or head sizes); valid domain: the fp32 range of the same mid-chunk factorisation as the fp32
+ * forward path.  Returns GLA_OK once enqueued.
+ */
+int gla_bwd(const void *q, const void *k, const void *v, const void *g, const void *dout, float scale,
+            const float *h0, const float *dht, float *dq, float *dk, float *dv, float *dg, float *dh0,
+            const int32_t *cu_seqlens, int N, int B, int T, int H, int K, int V, int chunk, int dtype,
+            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace gla_bwd needs for this problem (0 for an unsupported shape). */
+size_t gla_bwd_workspace_size(int B, int T, int H, int K, int V, int N, int chunk, int dtype);
+
+/*
  * Measurement hook (no counterpart on the pages; it exists so a benchmark can time each kernel of the
  * path with CUDA events on the stream the kernels run on).  While `events` is non-NULL, every later
- * gla_fwd call made from this host thread records events[2i] right before and events[2i+1] right after
+ * gla_fwd / gla_bwd call made from this host thread records events[2i] right before and events[2i+1] right after
  * its i-th kernel launch (for i < n_events / 2), on the call's stream, and stores that launch's kernel id
  * in kernel_ids[i] (host array of n_events / 2 ints, may be NULL).  `events` are cudaEvent_t handles
  * created by the caller.  Pass events == NULL to stop.  Returns GLA_OK, or GLA_ERR_INVALID_ARG for
- * n_events < 0.  gla_profile_launches() returns how many kernels the last gla_fwd call on this thread
- * launched, and gla_kernel_name() names a kernel id.
+ * n_events < 0.  gla_profile_launches() returns how many kernels the last gla_fwd / gla_bwd call on this
+ * thread launched, and gla_kernel_name() names a kernel id.
  */
 int gla_profile_events(void **events, int n_events, int *kernel_ids);
 int gla_profile_launches(void);
