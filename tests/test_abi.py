@@ -120,3 +120,31 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
             importlib.import_module("chunkwise_gated_linear_chunked_gb300.binding")
     finally:
         sys.modules.pop("chunkwise_gated_linear_chunked_gb300.binding", None)
+
+
+def bwd(gla, q=A, k=2 * A, v=3 * A, g=4 * A, do=5 * A, scale=0.125, h0=None, dht=None, dq=8 * A, dk=9 * A,
+        dv=10 * A, dg=11 * A, dh0=None, cu=None, N=2, B=2, T=100, H=2, K=64, V=64, chunk=64, dtype=1, ws=64 * A,
+        wsb=1 << 40):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return gla.lib().gla_bwd(p(q), p(k), p(v), p(g), p(do), scale, p(h0), p(dht), p(dq), p(dk), p(dv), p(dg),
+                             p(dh0), p(cu), N, B, T, H, K, V, chunk, dtype, p(ws), wsb, None)
+
+
+def test_bwd_rejects_before_any_cuda_work(gla):
+    assert bwd(gla, V=256) == gla.GLA_ERR_UNSUPPORTED                 # value width 256 is forward-only
+    assert bwd(gla, K=96) == gla.GLA_ERR_UNSUPPORTED
+    assert bwd(gla, chunk=32) == gla.GLA_ERR_UNSUPPORTED
+    assert bwd(gla, dtype=gla.GLA_BF16_OBF16) == gla.GLA_ERR_UNSUPPORTED
+    assert bwd(gla, scale=0.0) == gla.GLA_ERR_INVALID_ARG
+    assert bwd(gla, N=3) == gla.GLA_ERR_INVALID_ARG
+    assert bwd(gla, dq=None) == gla.GLA_ERR_INVALID_ARG
+    assert bwd(gla, do=5 * A + 8) == gla.GLA_ERR_ALIGNMENT
+    assert bwd(gla, dh0=20 * A + 4) == gla.GLA_ERR_ALIGNMENT
+    assert bwd(gla, ws=None) == gla.GLA_ERR_WORKSPACE
+    assert gla.bwd_workspace_size(2, 100, 2, 64, 64, 2, 64, 1) > 4096   # chunk states and adjoints
+    assert bwd(gla, wsb=4096) == gla.GLA_ERR_WORKSPACE
+    assert bwd(gla, dq=A + 256) == gla.GLA_ERR_INVALID_ARG            # dq overlaps q
+    assert bwd(gla, dk=8 * A + 256) == gla.GLA_ERR_INVALID_ARG        # dk overlaps dq
+    assert bwd(gla, dh0=64 * A) == gla.GLA_ERR_INVALID_ARG            # dh0 overlaps the workspace
+    assert bwd(gla, ws=A) == gla.GLA_ERR_INVALID_ARG                  # workspace overlaps inputs
+    assert gla.bwd_workspace_size(1, 100, 2, 64, 256, 1, 64, 1) == 0
