@@ -16,7 +16,7 @@ from .build import LIB
 
 GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_ALIGNMENT, GLA_ERR_WORKSPACE, GLA_ERR_CUDA, \
     GLA_ERR_TIMEOUT, GLA_ERR_RANGE = range(8)
-GLA_F32, GLA_BF16, GLA_BF16_OBF16 = 0, 1, 2
+GLA_F32, GLA_BF16, GLA_BF16_OBF16, GLA_F16 = 0, 1, 2, 3
 
 EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",
            "gla_profile_events", "gla_profile_launches", "gla_kernel_name", "gla_fwd_noalloc", "gla_bwd",
@@ -75,7 +75,7 @@ def _stream_handle(stream):
 
 
 DTYPE_CODE = {(torch.float32, torch.float32): GLA_F32, (torch.bfloat16, torch.float32): GLA_BF16,
-              (torch.bfloat16, torch.bfloat16): GLA_BF16_OBF16}
+              (torch.bfloat16, torch.bfloat16): GLA_BF16_OBF16, (torch.float16, torch.float32): GLA_F16}
 
 _ws_lock = threading.Lock()
 _ws_cache: dict = {}
@@ -168,7 +168,7 @@ def gla_bwd(q, k, v, g, do, scale=None, initial_state=None, dht=None, cu_seqlens
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if scale is None:
         scale = K ** -0.5
-    code = {torch.float32: GLA_F32, torch.bfloat16: GLA_BF16}.get(q.dtype)
+    code = {torch.float32: GLA_F32, torch.bfloat16: GLA_BF16, torch.float16: GLA_F16}.get(q.dtype)
     if code is None:
         raise GlaError(GLA_ERR_UNSUPPORTED, f"gla_bwd dtype {q.dtype}")
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("do", do)):
@@ -197,7 +197,7 @@ def get_status(workspace, stream=None) -> int:
 def chunk_local_cumsum(g, chunk=64, cu_seqlens=None, stream=None):
     B, T, H, K = g.shape
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
-    code = GLA_F32 if g.dtype == torch.float32 else GLA_BF16
+    code = {torch.float32: GLA_F32, torch.bfloat16: GLA_BF16, torch.float16: GLA_F16}.get(g.dtype, GLA_BF16)
     G = torch.empty(B, T, H, K, dtype=torch.float32, device=g.device)
     rc = int(_lib.gla_chunk_local_cumsum(_ptr(g), _ptr(G), _ptr(cu_seqlens), N, B, T, H, K, chunk, code,
                                          _stream_handle(stream)))

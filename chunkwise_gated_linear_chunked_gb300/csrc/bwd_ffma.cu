@@ -583,13 +583,16 @@ cudaError_t launch_grads_kv(const BwdArgs &a, int J, cudaStream_t s)
 
 bool bwd_supported(int dtype, int K, int V)
 {
-    return (dtype == GLA_F32 || dtype == GLA_BF16) && (K == 64 || K == 128) && (V == 64 || V == 128);
+    return (dtype == GLA_F32 || dtype == GLA_BF16 || dtype == GLA_F16) && (K == 64 || K == 128) &&
+           (V == 64 || V == 128);
 }
 
 cudaError_t launch_bwd_sums(const BwdArgs &a, int J, int dtype, cudaStream_t s)
 {
     if (dtype == GLA_F32)
         return a.K == 64 ? launch_sums_t<float, 64>(a, J, s) : launch_sums_t<float, 128>(a, J, s);
+    if (dtype == GLA_F16)
+        return a.K == 64 ? launch_sums_t<__half, 64>(a, J, s) : launch_sums_t<__half, 128>(a, J, s);
     return a.K == 64 ? launch_sums_t<__nv_bfloat16, 64>(a, J, s) : launch_sums_t<__nv_bfloat16, 128>(a, J, s);
 }
 
@@ -601,6 +604,8 @@ cudaError_t launch_bwd_scan(const BwdArgs &a, cudaStream_t s)
 
 cudaError_t launch_bwd_grads(const BwdArgs &a, int J, int dtype, cudaStream_t s)
 {
+    if (dtype == GLA_F16)
+        return launch_grads_kv<__half>(a, J, s);
     return dtype == GLA_F32 ? launch_grads_kv<float>(a, J, s) : launch_grads_kv<__nv_bfloat16>(a, J, s);
 }
 

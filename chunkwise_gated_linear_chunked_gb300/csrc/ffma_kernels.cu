@@ -503,7 +503,7 @@ cudaError_t launch_plan_varlen(const Plan &pl, const Args &a, cudaStream_t s)
 cudaError_t launch_state_ffma(const Plan &pl, const Args &a, cudaStream_t s)
 {
     dim3 grid(pl.NV, pl.H, pl.J);
-    const bool bf = pl.dtype != GLA_F32;
+    const bool bf = pl.dtype == GLA_BF16 || pl.dtype == GLA_BF16_OBF16, hf = pl.dtype == GLA_F16;
 #define GLA_STATE(TIN, KK)                                                                  \
     {                                                                                       \
         auto f = state_ffma<TIN, KK>;                                                       \
@@ -515,9 +515,9 @@ cudaError_t launch_state_ffma(const Plan &pl, const Args &a, cudaStream_t s)
         return cudaGetLastError();                                                          \
     }
     if (pl.K == 64) {
-        if (bf) GLA_STATE(__nv_bfloat16, 64) else GLA_STATE(float, 64)
+        if (bf) GLA_STATE(__nv_bfloat16, 64) else if (hf) GLA_STATE(__half, 64) else GLA_STATE(float, 64)
     } else {
-        if (bf) GLA_STATE(__nv_bfloat16, 128) else GLA_STATE(float, 128)
+        if (bf) GLA_STATE(__nv_bfloat16, 128) else if (hf) GLA_STATE(__half, 128) else GLA_STATE(float, 128)
     }
 #undef GLA_STATE
 }
@@ -547,6 +547,8 @@ cudaError_t launch_out_ffma(const Plan &pl, const Args &a, cudaStream_t s)
         if (pl.K == 64) GLA_OUT(float, float, 64) else GLA_OUT(float, float, 128)
     } else if (pl.dtype == GLA_BF16) {
         if (pl.K == 64) GLA_OUT(__nv_bfloat16, float, 64) else GLA_OUT(__nv_bfloat16, float, 128)
+    } else if (pl.dtype == GLA_F16) {
+        if (pl.K == 64) GLA_OUT(__half, float, 64) else GLA_OUT(__half, float, 128)
     } else {
         if (pl.K == 64) GLA_OUT(__nv_bfloat16, __nv_bfloat16, 64)
         else GLA_OUT(__nv_bfloat16, __nv_bfloat16, 128)
@@ -565,6 +567,9 @@ cudaError_t launch_chunk_cumsum(const void *g, float *G, const int32_t *cu, int 
     if (dtype == GLA_F32)
         chunk_cumsum_standalone<float><<<grid, threads, 0, s>>>(static_cast<const float *>(g), G, cu,
                                                                   N, T, rows, H, K, chunk);
+    else if (dtype == GLA_F16)
+        chunk_cumsum_standalone<__half><<<grid, threads, 0, s>>>(static_cast<const __half *>(g), G, cu, N, T,
+                                                                   rows, H, K, chunk);
     else
         chunk_cumsum_standalone<__nv_bfloat16><<<grid, threads, 0, s>>>(
             static_cast<const __nv_bfloat16 *>(g), G, cu, N, T, rows, H, K, chunk);

@@ -50,17 +50,20 @@ int sm_count()
 }
 
 bool supported_k(int K) { return K == 64 || K == 128; }
+// Accepted chunk lengths.  The kernels always tile at kChunk rows: the result of the method does not depend
+// on the chunk length in exact arithmetic, so the argument only selects rounding, and one tiling serves all.
+bool supported_chunk(int chunk) { return chunk == 16 || chunk == 32 || chunk == 64 || chunk == 128; }
 bool supported_v(int V) { return V == 64 || V == 128 || V == 256; }
 
 int check_shape(int B, int T, int H, int K, int V, int N, int chunk, int dtype, bool varlen)
 {
-    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_BF16_OBF16)
+    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_BF16_OBF16 && dtype != GLA_F16)
         return GLA_ERR_UNSUPPORTED;
     if (B < 0 || T < 0 || H <= 0 || N < 0 || K <= 0 || V <= 0)
         return GLA_ERR_INVALID_ARG;
     if (varlen ? B != 1 : N != B)
         return GLA_ERR_INVALID_ARG;
-    if (chunk != kChunk || !supported_k(K) || !supported_v(V))
+    if (!supported_chunk(chunk) || !supported_k(K) || !supported_v(V))
         return GLA_ERR_UNSUPPORTED;
     const long long rows = varlen ? (long long)T : (long long)B * T;
     if (rows * H * (K > V ? K : V) >= (1LL << 31) || (long long)N * H * K * V >= (1LL << 31))
@@ -219,11 +222,11 @@ extern "C" size_t gla_fwd_workspace_size(int B, int T, int H, int K, int V, int 
     size_t best = 0;
     Plan pl;
     if (varlen_ok && B == 1) {
-        make_plan(pl, B, T, H, K, V, N, chunk, dtype, true);
+        make_plan(pl, B, T, H, K, V, N, kChunk, dtype, true);
         best = pl.total;
     }
     if (dense_ok) {
-        make_plan(pl, B, T, H, K, V, N, chunk, dtype, false);
+        make_plan(pl, B, T, H, K, V, N, kChunk, dtype, false);
         if (pl.total > best)
             best = pl.total;
     }
@@ -249,7 +252,7 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
         misaligned(h0) || misaligned(ht) || misaligned(cu_seqlens))
         return GLA_ERR_ALIGNMENT;
     Plan pl;
-    make_plan(pl, B, T, H, K, V, N, chunk, dtype, varlen);
+    make_plan(pl, B, T, H, K, V, N, kChunk, dtype, varlen);
     if (!workspace)
         return GLA_ERR_WORKSPACE;
     if (workspace_bytes < pl.total)
@@ -363,7 +366,7 @@ extern "C" int gla_chunk_local_cumsum(const void *g, float *G, const int32_t *cu
                                       int T, int H, int K, int chunk, int dtype, void *stream)
 {
     const bool varlen = cu_seqlens != nullptr;
-    if (dtype != GLA_F32 && dtype != GLA_BF16)
+    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_F16)
         return GLA_ERR_UNSUPPORTED;
     if (B < 0 || T < 0 || H <= 0 || K <= 0 || N < 0 || (varlen ? B != 1 : false))
         return GLA_ERR_INVALID_ARG;
@@ -454,13 +457,13 @@ void make_bwd_plan(BwdPlan &bp, int B, int T, int H, int K, int V, int N, bool v
 
 int check_bwd_shape(int B, int T, int H, int K, int V, int N, int chunk, int dtype, bool varlen)
 {
-    if (dtype != GLA_F32 && dtype != GLA_BF16)
+    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_F16)
         return GLA_ERR_UNSUPPORTED;
     if (B < 0 || T < 0 || H <= 0 || N < 0)
         return GLA_ERR_INVALID_ARG;
     if (varlen ? B != 1 : N != B)
         return GLA_ERR_INVALID_ARG;
-    if (chunk != kChunk || !bwd_supported(dtype, K, V))
+    if (!supported_chunk(chunk) || !bwd_supported(dtype, K, V))
         return GLA_ERR_UNSUPPORTED;
     const long long rows = varlen ? (long long)T : (long long)B * T;
     if (rows * H * (K > V ? K : V) >= (1LL << 31) || (long long)(N + T / kChunk + 1) * H * K * V >= (1LL << 31))

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace gla {
 
@@ -42,6 +43,18 @@ struct IO<__nv_bfloat16> {
         u.x = *reinterpret_cast<const unsigned *>(&a);
         u.y = *reinterpret_cast<const unsigned *>(&b);
         *reinterpret_cast<uint2 *>(p) = u;
+    }
+};
+
+template <>
+struct IO<__half> {
+    static __device__ __forceinline__ float load1(const __half *p) { return __half2float(*p); }
+    static __device__ __forceinline__ float4 load4(const __half *p)
+    {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(p));
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
     }
 };
 

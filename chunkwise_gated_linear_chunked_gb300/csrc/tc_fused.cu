@@ -1,4 +1,5 @@
-// Persistent fused tensor-core kernel of the chunkwise GLA forward (bf16 inputs, K = 128, V in {128, 256}).
+// Persistent fused tensor-core kernel of the chunkwise GLA forward (bf16 or fp16 inputs, K = 128, V in
+// {128, 256}).
 //
 // Method (page "fla/ops/gla/fused_chunk.py"): per chunk of C = 64 rows with chunk-local cumsum G of the gates
 // (FusedChunkGLAFunction.forward, kernel a), the state contribution (k*exp(G_last-G))^T V (prepare_qg_kg,
@@ -83,8 +84,29 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// A 32-bit word of two 16-bit inputs: widened halves, and the pair as an fp16 operand word (bf16 rounds
+// once to fp16; fp16 inputs are already in operand form).
+template <typename Tin>
+struct In;
+template <>
+struct In<__nv_bfloat16> {
+    static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+    static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+    static __device__ __forceinline__ uint32_t op(uint32_t w);
+};
+template <>
+struct In<__half> {
+    static __device__ __forceinline__ float lo(uint32_t w)
+    {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+    }
+    static __device__ __forceinline__ float hi(uint32_t w)
+    {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+    }
+    static __device__ __forceinline__ uint32_t op(uint32_t w) { return w; }
+};
+__device__ __forceinline__ uint32_t In<__nv_bfloat16>::op(uint32_t w) { return pack_h2(lo(w), hi(w)); }
 __device__ __forceinline__ bool finite(float x) { return fabsf(x) <= 3.402823466e38f; }
 __device__ __forceinline__ float amax_nan(float m, float x)
 {
@@ -118,7 +140,7 @@ __device__ __forceinline__ float4 f4(const uint32_t *r)
     return make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]), __uint_as_float(r[3]));
 }
 
-template <typename Tout>
+template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gla_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
@@ -501,8 +523,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const bool in = t < len;
                     gr[uu] = in ? *reinterpret_cast<const uint32_t *>(st + ST_G + t * 256 + kp * 4) : 0u;
                     vr[uu] = in ? *reinterpret_cast<const uint32_t *>(st + ST_V + t * 256 + kp * 4) : 0u;
-                    s0 = fmaf(bf_lo(gr[uu]), L2E, s0);
-                    s1 = fmaf(bf_hi(gr[uu]), L2E, s1);
+                    s0 = fmaf(In<Tin>::lo(gr[uu]), L2E, s0);
+                    s1 = fmaf(In<Tin>::hi(gr[uu]), L2E, s1);
                 }
                 float *ps = psum + (gq & 1) * 512;
                 ps[rq * 128 + key] = s0;
@@ -537,19 +559,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int uu = 0; uu < 16; ++uu) {
                             const int t = 16 * rq + uu;
-                            X0 = fmaf(bf_lo(gr[uu]), L2E, X0);
-                            X1 = fmaf(bf_hi(gr[uu]), L2E, X1);
+                            X0 = fmaf(In<Tin>::lo(gr[uu]), L2E, X0);
+                            X1 = fmaf(In<Tin>::hi(gr[uu]), L2E, X1);
                             const uint32_t off = xo[uu & 7] + (uu >> 3) * 1024;
                             const uint32_t qw = *reinterpret_cast<const uint32_t *>(qk + ST_Q0 + off);
                             const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
-                            float q0 = bf_lo(qw) * ex2(X0), q1 = bf_hi(qw) * ex2(X1);
-                            float k0 = bf_lo(kw) * ex2(-X0), k1 = bf_hi(kw) * ex2(-X1);
+                            float q0 = In<Tin>::lo(qw) * ex2(X0), q1 = In<Tin>::hi(qw) * ex2(X1);
+                            float k0 = In<Tin>::lo(kw) * ex2(-X0), k1 = In<Tin>::hi(kw) * ex2(-X1);
                             if (!FULL && t >= len)
                                 q0 = q1 = k0 = k1 = 0.f;
                             *reinterpret_cast<uint32_t *>(qk + ST_Q0 + off) = pack_h2(q0, q1);
                             *reinterpret_cast<uint32_t *>(qk + ST_K0 + off) = pack_h2(k0, k1);
                             kh[uu] = pack_h2(k0 * cl0, k1 * cl1);
-                            vr[uu] = pack_h2(bf_lo(vr[uu]), bf_hi(vr[uu]));
+                            vr[uu] = In<Tin>::op(vr[uu]);
                         }
                     };
                     if (len == C)
@@ -562,15 +584,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int uu = 0; uu < 16; ++uu) {
                         const int t = 16 * rq + uu;
-                        X0 = fmaf(bf_lo(gr[uu]), L2E, X0);
-                        X1 = fmaf(bf_hi(gr[uu]), L2E, X1);
+                        X0 = fmaf(In<Tin>::lo(gr[uu]), L2E, X0);
+                        X1 = fmaf(In<Tin>::hi(gr[uu]), L2E, X1);
                         const uint32_t kw =
                             *reinterpret_cast<const uint32_t *>(qk + ST_K0 + xo[uu & 7] + (uu >> 3) * 1024);
                         const bool in = t < len;
-                        const float k0 = in ? bf_lo(kw) * ex2(e0 - X0) : 0.f;
-                        const float k1 = in ? bf_hi(kw) * ex2(e1 - X1) : 0.f;
+                        const float k0 = in ? In<Tin>::lo(kw) * ex2(e0 - X0) : 0.f;
+                        const float k1 = in ? In<Tin>::hi(kw) * ex2(e1 - X1) : 0.f;
                         kh[uu] = pack_h2(k0, k1);
-                        vr[uu] = pack_h2(bf_lo(vr[uu]), bf_hi(vr[uu]));
+                        vr[uu] = In<Tin>::op(vr[uu]);
                     }
                     D0 = e0;
                     D1 = e1;
@@ -812,35 +834,39 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 bool encode_rows(CUtensorMap *m, const void *ptr, int D, int H, long long rows, int inner, int brows, bool swizzle,
-                 bool f32 = false)
+                 CUtensorMapDataType type)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
-    const cuuint64_t es = f32 ? 4 : 2;
+    const cuuint64_t es = type == CU_TENSOR_MAP_DATA_TYPE_FLOAT32 ? 4 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es};
     cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)brows};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr),
+    return fn(m, type, 3, const_cast<void *>(ptr),
               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Tout>
+template <typename Tin, typename Tout>
 cudaError_t launch_fused_t(const Plan &pl, const Args &a, cudaStream_t s, int sms)
 {
     const long long rows = pl.varlen ? (long long)pl.T : (long long)pl.B * pl.T;
+    const CUtensorMapDataType tin =
+        std::is_same<Tin, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap mq, mk, mg, mv, mo;
-    if (!encode_rows(&mq, a.q, pl.K, pl.H, rows, 64, C, true) || !encode_rows(&mk, a.k, pl.K, pl.H, rows, 64, C, true) ||
-        !encode_rows(&mg, a.g, pl.K, pl.H, rows, 128, C, false) ||
-        !encode_rows(&mv, a.v, pl.V, pl.H, rows, 128, C, false))
+    if (!encode_rows(&mq, a.q, pl.K, pl.H, rows, 64, C, true, tin) ||
+        !encode_rows(&mk, a.k, pl.K, pl.H, rows, 64, C, true, tin) ||
+        !encode_rows(&mg, a.g, pl.K, pl.H, rows, 128, C, false, tin) ||
+        !encode_rows(&mv, a.v, pl.V, pl.H, rows, 128, C, false, tin))
         return cudaErrorInvalidValue;
     const bool f32o = sizeof(Tout) == 4;
-    if (!encode_rows(&mo, f32o ? a.o : a.v, pl.V, pl.H, rows, 128, 32, false, f32o))
+    if (!encode_rows(&mo, f32o ? a.o : a.v, pl.V, pl.H, rows, 128, 32, false,
+                     f32o ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
         return cudaErrorInvalidValue;
-    auto f = gla_fused<Tout>;
+    auto f = gla_fused<Tin, Tout>;
     // the shared-memory opt-in is per device: remember it per device ordinal (set every time beyond 64)
     static std::atomic<unsigned long long> attr_set{0};
     int dev = 0;
@@ -886,8 +912,10 @@ bool tc_supported(int dtype, int K, int V)
 cudaError_t launch_fused_tc(const Plan &pl, const Args &a, cudaStream_t s, int sms)
 {
     if (pl.dtype == GLA_BF16_OBF16)
-        return launch_fused_t<__nv_bfloat16>(pl, a, s, sms);
-    return launch_fused_t<float>(pl, a, s, sms);
+        return launch_fused_t<__nv_bfloat16, __nv_bfloat16>(pl, a, s, sms);
+    if (pl.dtype == GLA_F16)
+        return launch_fused_t<__half, float>(pl, a, s, sms);
+    return launch_fused_t<__nv_bfloat16, float>(pl, a, s, sms);
 }
 
 }  // namespace gla

@@ -21,7 +21,7 @@ import torch.nn.functional as F
 @dataclass(frozen=True)
 class Workload:
     name: str
-    dtype: str            # "f32" | "bf16"
+    dtype: str            # "f32" | "bf16" | "f16"
     B: int
     T: int                # per-sequence length (dense) or packed total (varlen, filled in)
     H: int
@@ -51,7 +51,7 @@ WORKLOADS = {
                               note="bf16 B=1 H=32 T=65536 K=V=128, stores ht"),
 }
 
-TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 @dataclass
@@ -107,10 +107,11 @@ def workload_inputs(name: str) -> Inputs:
 
 
 def stored_numpy(x: torch.Tensor):
-    """A CPU tensor as the numpy array of its stored words: float32 as is, bf16 as uint16 bit patterns."""
+    """A CPU tensor as the numpy array of its stored words: float32 and float16 as they are, bf16 as uint16
+    bit patterns."""
     x = x.detach().contiguous().cpu()
     if x.dtype == torch.bfloat16:
         return x.view(torch.int16).numpy().view("uint16")
-    if x.dtype == torch.float32:
+    if x.dtype in (torch.float32, torch.float16):
         return x.numpy()
     raise TypeError(f"unsupported dtype {x.dtype}")

@@ -57,7 +57,8 @@ typedef enum gla_status {
 typedef enum gla_dtype {
     GLA_F32 = 0,        /* q, k, v, g fp32; o fp32                                                  */
     GLA_BF16 = 1,       /* q, k, v, g bf16; o fp32 (default for bf16 inputs, see below)             */
-    GLA_BF16_OBF16 = 2  /* q, k, v, g bf16; o bf16 (the pages' o.to(v) convention)                  */
+    GLA_BF16_OBF16 = 2, /* q, k, v, g bf16; o bf16 (the pages' o.to(v) convention)                  */
+    GLA_F16 = 3         /* q, k, v, g fp16; o fp32 (same paths and bounds as GLA_BF16)                */
 } gla_dtype;
 /* o is fp32 for bf16 inputs by default: at the benchmark magnitudes (|o| up to ~20) a bf16-rounded o
  * alone carries up to 0.06 of rounding error, above the 2e-2 max-abs parity bound.  State h0/ht is fp32
@@ -74,7 +75,8 @@ typedef enum gla_dtype {
  *               token's gate like any carried state (fused_chunk_gla_fwd_kernel).
  *   ht          [N,H,K,V] fp32 final state (device) or NULL to skip it.  May equal h0.
  *   cu_seqlens  int32 [N+1] device offsets or NULL (dense: N == B sequences of T rows).
- *   chunk       chunk length; 64 is supported.  The result does not depend on it in exact arithmetic.
+ *   chunk       chunk length: 16, 32, 64 or 128.  The result does not depend on it in exact arithmetic;
+ *               the kernels tile at 64 rows whatever the value (so it selects no different rounding here).
  *   K           64 or 128.          V  64, 128 or 256.          B, T, H, N >= 0 (T*H*max(K,V) < 2^31).
  *   workspace   device scratch of at least gla_fwd_workspace_size() bytes, 256-byte aligned, ZEROED
  *               BEFORE ITS FIRST USE and not written by the caller afterwards: its 256-byte header carries
@@ -157,7 +159,7 @@ int gla_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, 
  * same h0 the forward used, or NULL for a zero initial state).  dout [rows, H, V] in the input dtype (the
  * gradient of o); dht [N, H, K, V] fp32 or NULL (no loss on the final state).  dtype GLA_F32 (every input
  * fp32) or GLA_BF16 (q, k, v, g, dout bf16); all arithmetic is fp32 on CUDA cores.  K and V in {64, 128};
- * chunk 64.  workspace: at least gla_bwd_workspace_size() bytes, 256-byte aligned, zeroed before its first
+ * chunk 16, 32, 64 or 128 (tiled at 64 rows, as for gla_fwd).  workspace: at least gla_bwd_workspace_size() bytes, 256-byte aligned, zeroed before its first
  * use (status word in its first bytes); it holds the chunk-start states and chunk-end adjoints
  * (2 * chunks * H * K * V fp32).  Outputs must not overlap any input, the workspace or one another.  The
  * library allocates nothing and is stream-ordered.  Errors as for gla_fwd (GLA_ERR_UNSUPPORTED for other

@@ -40,7 +40,7 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16, F64 = 0, 1, 2
+F32, BF16, F64, F16 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -90,7 +90,9 @@ def _as_stored(x: np.ndarray):
         return x, BF16
     if x.dtype == np.float64:
         return x, F64
-    raise TypeError(f"oracle inputs must be float32, float64 or bf16 words (uint16), got {x.dtype}")
+    if x.dtype == np.float16:
+        return x.view(np.uint16), F16
+    raise TypeError(f"oracle inputs must be float32, float16, float64 or bf16 words (uint16), got {x.dtype}")
 
 
 def _ptr(a):

@@ -14,7 +14,7 @@
  *     o_t     = scale * q_t S_t
  *     ht[n,h] = S_last
  *
- * Inputs are read in their stored type (fp32, or bf16 stored as raw 16-bit words) and widened exactly
+ * Inputs are read in their stored type (fp32, fp16, or bf16 stored as raw 16-bit words) and widened exactly
  * to double element by element; nothing is rounded on the way.  Layouts are time-major with interleaved
  * heads: q, k, g are [rows, H, K] and v, o are [rows, H, V] where rows = B*T (dense) or the packed
  * total length (varlen, B == 1).  h0 / ht are [N, H, K, V] in double (an fp32 h0 widens exactly).
@@ -39,7 +39,21 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F64 = 2 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F64 = 2, ORACLE_F16 = 3 };
+
+/* IEEE binary16 bit pattern to double, exactly: sign, 5-bit exponent (bias 15), 10-bit fraction. */
+static double half_bits_to_double(uint16_t b)
+{
+    const int sign = b >> 15, e = (b >> 10) & 0x1f, f = b & 0x3ff;
+    double x;
+    if (e == 0)
+        x = ldexp((double)f, -24);                       /* subnormal: f * 2^-24 */
+    else if (e == 31)
+        x = f ? NAN : INFINITY;
+    else
+        x = ldexp((double)(f | 0x400), e - 25);          /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -x : x;
+}
 
 /* Exact widening of one stored element to double. bf16 is the high half of an IEEE binary32; fp64 inputs
  * (used by the finite-difference checks of the backward) are read as they are. */
@@ -49,6 +63,8 @@ static double widen(const void *base, size_t idx, int dtype)
         return (double)((const float *)base)[idx];
     if (dtype == ORACLE_F64)
         return ((const double *)base)[idx];
+    if (dtype == ORACLE_F16)
+        return half_bits_to_double(((const uint16_t *)base)[idx]);
     uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
     float f;
     memcpy(&f, &bits, sizeof f);
@@ -138,7 +154,7 @@ int oracle_gla_fwd(const void *q, const void *k, const void *v, const void *g, i
 {
     if (!q || !k || !v || !g || !o || H <= 0 || K <= 0 || V <= 0 || B < 0 || T < 0)
         return -1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64)
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64 && dtype != ORACLE_F16)
         return -1;
     int32_t *dense = NULL;
     const int32_t *cu = cu_seqlens;
@@ -352,7 +368,7 @@ int oracle_gla_bwd(const void *q, const void *k, const void *v, const void *g, c
     if (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg || H <= 0 || K <= 0 || V <= 0 || B < 0 ||
         T < 0)
         return -1;
-    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64)
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64 && dtype != ORACLE_F16)
         return -1;
     int32_t *dense = NULL;
     const int32_t *cu = cu_seqlens;

@@ -133,7 +133,7 @@ def bwd(gla, q=A, k=2 * A, v=3 * A, g=4 * A, do=5 * A, scale=0.125, h0=None, dht
 def test_bwd_rejects_before_any_cuda_work(gla):
     assert bwd(gla, V=256) == gla.GLA_ERR_UNSUPPORTED                 # value width 256 is forward-only
     assert bwd(gla, K=96) == gla.GLA_ERR_UNSUPPORTED
-    assert bwd(gla, chunk=32) == gla.GLA_ERR_UNSUPPORTED
+    assert bwd(gla, chunk=48) == gla.GLA_ERR_UNSUPPORTED
     assert bwd(gla, dtype=gla.GLA_BF16_OBF16) == gla.GLA_ERR_UNSUPPORTED
     assert bwd(gla, scale=0.0) == gla.GLA_ERR_INVALID_ARG
     assert bwd(gla, N=3) == gla.GLA_ERR_INVALID_ARG

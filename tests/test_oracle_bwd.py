@@ -175,3 +175,20 @@ def test_backward_pins_catch_planted_mistake(name, tmp_path):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake {name}"
+
+
+def test_fp16_inputs_widen_exactly():
+    """fp16 inputs (including subnormals and large values) give exactly the results of the same values in
+    float64: the oracle's half decoder agrees with numpy's conversion, forward and backward."""
+    rng = np.random.default_rng(12)
+    B, T, H, K, V = 1, 9, 2, 3, 4
+    vals = lambda *s: (rng.standard_normal(s) * rng.choice([1e-6, 1e-2, 1.0, 300.0], size=s)).astype(np.float16)
+    q, k, v, do = vals(B, T, H, K), vals(B, T, H, K), vals(B, T, H, V), vals(B, T, H, V)
+    g = (-np.abs(rng.standard_normal((B, T, H, K))) * 0.2).astype(np.float16)
+    q[0, 0, 0, 0] = np.float16(6e-8)       # subnormal
+    wide = [x.astype(np.float64) for x in (q, k, v, g, do)]
+    o16, ht16, _ = oracle.gla_fwd(q, k, v, g, 0.5)
+    o64, ht64, _ = oracle.gla_fwd(*wide[:4], 0.5)
+    assert np.array_equal(o16, o64) and np.array_equal(ht16, ht64)
+    for x, y in zip(oracle.gla_bwd(q, k, v, g, do, 0.5), oracle.gla_bwd(*wide, 0.5)):
+        assert np.array_equal(x, y)

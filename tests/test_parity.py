@@ -37,6 +37,10 @@ SMALL = [
     ("bf16", 1, 0, 2, 64, 64, True, [1, 63, 64, 65, 0, 130, 300, 2]),   # varlen incl. an empty sequence
     ("bf16", 1, 0, 1, 128, 128, True, [3000, 7, 1500]),                  # varlen with segments
     ("f32", 1, 0, 2, 64, 64, False, [0, 0, 5]),
+    ("f16", 2, 200, 3, 128, 128, True, None),         # fp16 inputs: tensor-core path
+    ("f16", 1, 3000, 1, 128, 256, True, None),        # fp16, segments + scan, V = 256
+    ("f16", 2, 130, 2, 64, 64, True, None),           # fp16 on the CUDA-core path
+    ("f16", 1, 0, 2, 128, 128, True, [1, 63, 64, 65, 0, 130, 300, 2]),
 ]
 
 
@@ -79,6 +83,18 @@ def test_segment_scan_all_heads(case):
     o_ref, ht_ref = run_oracle(inp)
     assert_close(as_f64(o), o_ref, TOL[d], "o")
     assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 128])
+def test_chunk_argument_selects_same_tiling(chunk):
+    """chunk is accepted as 16, 32, 64 or 128; the kernels tile at 64 rows, so the result is the same."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = make_inputs("bf16", B=1, T=300, H=2, K=128, V=128, h0=True, seed=31)
+    q, k, v, g, h0, _ = to_device(inp)
+    o64, ht64 = binding.gla_fwd(q, k, v, g, scale=inp.scale, initial_state=h0, chunk=64)
+    o, ht = binding.gla_fwd(q, k, v, g, scale=inp.scale, initial_state=h0, chunk=chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o64) and torch.equal(ht, ht64)
 
 
 def test_bf16_output_variant():

@@ -68,6 +68,8 @@ CASES = [
     ("bf16", 1, 700, 2, 64, 64, True, False, None),
     ("bf16", 1, 0, 2, 128, 128, True, True, [1, 63, 64, 65, 0, 130, 300, 2]),   # varlen incl. empty
     ("f32", 1, 0, 1, 64, 64, True, True, [0, 0, 5]),
+    ("f16", 2, 200, 2, 128, 128, True, True, None),
+    ("f16", 1, 0, 2, 64, 128, True, True, [1, 63, 64, 65, 0, 130]),
 ]
 
 
