@@ -17,6 +17,7 @@ from .build import LIB
 GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_ALIGNMENT, GLA_ERR_WORKSPACE, GLA_ERR_CUDA, \
     GLA_ERR_TIMEOUT, GLA_ERR_RANGE = range(8)
 GLA_F32, GLA_BF16, GLA_BF16_OBF16, GLA_F16 = 0, 1, 2, 3
+GLA_HEAD_FIRST = 0x100   # OR-ed into the dtype code: [B, H, T, *] tensors
 
 EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",
            "gla_profile_events", "gla_profile_launches", "gla_kernel_name", "gla_fwd_noalloc", "gla_bwd",
@@ -107,14 +108,18 @@ def fwd_into(q, k, v, g, o, scale, h0, ht, cu_seqlens, N, B, T, H, K, V, chunk, 
 
 
 def gla_fwd(q, k, v, g, scale=None, initial_state=None, output_final_state=True, cu_seqlens=None,
-            chunk=64, out_dtype=None, stream=None, workspace=None):
+            chunk=64, out_dtype=None, stream=None, workspace=None, head_first=False):
     """GLA forward on the GPU.
 
-    q, k, g: [B, T, H, K]; v: [B, T, H, V] (cuda, contiguous, all fp32 or all bf16).
-    initial_state: optional fp32 [N, H, K, V].  cu_seqlens: optional int32 [N+1] cuda offsets (B == 1).
-    out_dtype: fp32 (default) or, for bf16 inputs, bf16.  Returns (o, final_state or None).
+    q, k, g: [B, T, H, K]; v: [B, T, H, V] (cuda, contiguous, all fp32, all bf16 or all fp16), or
+    [B, H, T, *] with head_first=True (dense batches).  initial_state: optional fp32 [N, H, K, V].
+    cu_seqlens: optional int32 [N+1] cuda offsets (B == 1).  out_dtype: fp32 (default) or, for bf16 inputs,
+    bf16.  Returns (o in the layout of the inputs, final_state or None).
     """
-    B, T, H, K = q.shape
+    if head_first:
+        B, H, T, K = q.shape
+    else:
+        B, T, H, K = q.shape
     V = v.shape[-1]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if scale is None:
@@ -126,7 +131,7 @@ def gla_fwd(q, k, v, g, scale=None, initial_state=None, output_final_state=True,
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
         if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
             raise GlaError(GLA_ERR_INVALID_ARG, f"gla_fwd: {name} must be a contiguous cuda {q.dtype} tensor")
-    o = torch.empty(B, T, H, V, dtype=out_dtype, device=q.device)
+    o = torch.empty(*((B, H, T, V) if head_first else (B, T, H, V)), dtype=out_dtype, device=q.device)
     ht = torch.empty(N, H, K, V, dtype=torch.float32, device=q.device) if output_final_state else None
     h0 = initial_state
     if h0 is not None and (h0.dtype != torch.float32 or not h0.is_contiguous()):
@@ -135,6 +140,8 @@ def gla_fwd(q, k, v, g, scale=None, initial_state=None, output_final_state=True,
         raise GlaError(GLA_ERR_INVALID_ARG, "gla_fwd: cu_seqlens must be int32")
     if workspace is None:
         workspace = get_workspace(workspace_size(B, T, H, K, V, N, chunk, code), q.device)
+    if head_first:
+        code |= GLA_HEAD_FIRST
     rc = fwd_into(q, k, v, g, o, scale, h0, ht, cu_seqlens, N, B, T, H, K, V, chunk, code, workspace,
                   stream)
     if rc != GLA_OK:
@@ -157,13 +164,17 @@ def bwd_into(q, k, v, g, do, scale, h0, dht, dq, dk, dv, dg, dh0, cu_seqlens, N,
 
 
 def gla_bwd(q, k, v, g, do, scale=None, initial_state=None, dht=None, cu_seqlens=None, chunk=64, stream=None,
-            workspace=None, want_dh0=True):
+            workspace=None, want_dh0=True, head_first=False):
     """GLA backward on the GPU for L = sum(o * do) + sum(ht * dht).
 
-    q, k, g: [B, T, H, K]; v, do: [B, T, H, V] (cuda, contiguous, all fp32 or all bf16).  initial_state and
-    dht: optional fp32 [N, H, K, V].  Returns fp32 (dq, dk, dv, dg, dh0 or None).
+    q, k, g: [B, T, H, K]; v, do: [B, T, H, V] (cuda, contiguous, all fp32, bf16 or fp16), or [B, H, T, *]
+    with head_first=True.  initial_state and dht: optional fp32 [N, H, K, V].  Returns fp32 (dq, dk, dv, dg,
+    dh0 or None), in the layout of the inputs.
     """
-    B, T, H, K = q.shape
+    if head_first:
+        B, H, T, K = q.shape
+    else:
+        B, T, H, K = q.shape
     V = v.shape[-1]
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if scale is None:
@@ -178,11 +189,14 @@ def gla_bwd(q, k, v, g, do, scale=None, initial_state=None, dht=None, cu_seqlens
         if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
             raise GlaError(GLA_ERR_INVALID_ARG, f"gla_bwd: {name} must be a contiguous fp32 tensor")
     f32 = dict(dtype=torch.float32, device=q.device)
-    dq, dk, dg = (torch.empty(B, T, H, K, **f32) for _ in range(3))
-    dv = torch.empty(B, T, H, V, **f32)
+    shk, shv = ((B, H, T, K), (B, H, T, V)) if head_first else ((B, T, H, K), (B, T, H, V))
+    dq, dk, dg = (torch.empty(*shk, **f32) for _ in range(3))
+    dv = torch.empty(*shv, **f32)
     dh0 = torch.empty(N, H, K, V, **f32) if want_dh0 else None
     if workspace is None:
         workspace = get_workspace(bwd_workspace_size(B, T, H, K, V, N, chunk, code), q.device)
+    if head_first:
+        code |= GLA_HEAD_FIRST
     rc = bwd_into(q, k, v, g, do, scale, initial_state, dht, dq, dk, dv, dg, dh0, cu_seqlens, N, B, T, H, K, V,
                   chunk, code, workspace, stream)
     if rc != GLA_OK:

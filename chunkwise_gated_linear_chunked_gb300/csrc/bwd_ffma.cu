@@ -64,20 +64,22 @@ __global__ void __launch_bounds__(NTB) bwd_chunk_sums(BwdArgs a)
     if (!bwd_slot(a, j, n, bos, eos))
         return;
     const int len = eos - bos, H = a.H, V = a.V;
+    const size_t rb = row_head(bos, h, H, a.T, a.hf);   // row t of the chunk: row-head index rb + t * rs
+    const int rs = a.hf ? 1 : H;
     const Tin *q = static_cast<const Tin *>(a.q), *k = static_cast<const Tin *>(a.k);
     const Tin *g = static_cast<const Tin *>(a.g), *v = static_cast<const Tin *>(a.v);
     const Tin *dout = static_cast<const Tin *>(a.dout);
     if (tid < K) {
         float run = 0.f;
         for (int i = 0; i < C; ++i) {
-            run += i < len ? IO<Tin>::load1(g + ((size_t)(bos + i) * H + h) * K + tid) : 0.f;
+            run += i < len ? IO<Tin>::load1(g + (rb + (size_t)i * rs) * K + tid) : 0.f;
             QE[i * K + tid] = run;
         }
         GL[tid] = run;
     }
     for (int e = tid; e < C * 16; e += NTB) {
         const int i = e >> 4, c4 = (e & 15) * 4;
-        const size_t o = ((size_t)(bos + i) * H + h) * V + v0 + c4;
+        const size_t o = (rb + (size_t)i * rs) * V + v0 + c4;
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         *reinterpret_cast<float4 *>(VS + i * 64 + c4) = i < len ? IO<Tin>::load4(v + o) : z;
         *reinterpret_cast<float4 *>(DS + i * 64 + c4) = i < len ? IO<Tin>::load4(dout + o) : z;
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(NTB) bwd_chunk_sums(BwdArgs a)
     __syncthreads();
     for (int e = tid; e < C * K; e += NTB) {
         const int i = e / K, kk = e - i * K;
-        const size_t o = ((size_t)(bos + i) * H + h) * K + kk;
+        const size_t o = (rb + (size_t)i * rs) * K + kk;
         const float G = QE[e];
         const float qv = i < len ? IO<Tin>::load1(q + o) : 0.f;
         const float kv = i < len ? IO<Tin>::load1(k + o) : 0.f;
@@ -291,6 +293,8 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
     if (!bwd_slot(a, j, n, bos, eos))
         return;
     const int len = eos - bos, H = a.H;
+    const size_t rb = row_head(bos, h, H, a.T, a.hf);   // row t of the chunk: row-head index rb + t * rs
+    const int rs = a.hf ? 1 : H;
     const Tin *q = static_cast<const Tin *>(a.q), *k = static_cast<const Tin *>(a.k);
     const Tin *g = static_cast<const Tin *>(a.g), *v = static_cast<const Tin *>(a.v);
     const Tin *dout = static_cast<const Tin *>(a.dout);
@@ -299,7 +303,7 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
     // ---- load the chunk (rows >= len are zero; their gate is 0, so G stays at G_l there)
     for (int e = tid; e < C * K / 4; e += NTB) {
         const int i = e / (K / 4), c4 = (e - i * (K / 4)) * 4;
-        const size_t o = ((size_t)(bos + i) * H + h) * K + c4;
+        const size_t o = (rb + (size_t)i * rs) * K + c4;
         const bool in = i < len;
         *reinterpret_cast<float4 *>(Q + i * K + c4) = in ? IO<Tin>::load4(q + o) : z4;
         *reinterpret_cast<float4 *>(KA + i * K + c4) = in ? IO<Tin>::load4(k + o) : z4;
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
     }
     for (int e = tid; e < C * V / 4; e += NTB) {
         const int i = e / (V / 4), c4 = (e - i * (V / 4)) * 4;
-        const size_t o = ((size_t)(bos + i) * H + h) * V + c4;
+        const size_t o = (rb + (size_t)i * rs) * V + c4;
         const bool in = i < len;
         *reinterpret_cast<float4 *>(VV + i * V + c4) = in ? IO<Tin>::load4(v + o) : z4;
         *reinterpret_cast<float4 *>(DO + i * V + c4) = in ? IO<Tin>::load4(dout + o) : z4;
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
         for (int r = 0; r < 4; ++r) {
             const int jj = 4 * ty + r;
             if (jj < len) {
-                float *row = a.dv + ((size_t)(bos + jj) * H + h) * V;
+                float *row = a.dv + (rb + (size_t)jj * rs) * V;
 #pragma unroll
                 for (int c = 0; c < V / 16; c += 4)
                     *reinterpret_cast<float4 *>(row + col_of(c, tx)) =
@@ -443,7 +447,7 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
             accq[r][c] = x * expf(G[i * K + kk] - GA[kk]);
         }
         if (i < len) {
-            float *row = a.dq + ((size_t)(bos + i) * H + h) * K;
+            float *row = a.dq + (rb + (size_t)i * rs) * K;
 #pragma unroll
             for (int c = 0; c < K / 16; c += 4)
                 *reinterpret_cast<float4 *>(row + col_of(c, tx)) =
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
             acck[r][c] = x * expf(GA[kk] - G[i * K + kk]);
         }
         if (i < len) {
-            float *row = a.dk + ((size_t)(bos + i) * H + h) * K;
+            float *row = a.dk + (rb + (size_t)i * rs) * K;
 #pragma unroll
             for (int c = 0; c < K / 16; c += 4)
                 *reinterpret_cast<float4 *>(row + col_of(c, tx)) =
@@ -490,7 +494,7 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
         float run = 0.f;
         for (int i = len - 1; i >= 0; --i) {
             run += PD[i * K + tid];
-            a.dg[((size_t)(bos + i) * H + h) * K + tid] = run;
+            a.dg[(rb + (size_t)i * rs) * K + tid] = run;
         }
         a.dgt[((size_t)j * H + h) * K + tid] = run;
     }
@@ -533,8 +537,10 @@ __global__ void __launch_bounds__(128) bwd_dg_add(BwdArgs a)
     if (kk >= a.K || !bwd_slot(a, j, n, bos, eos))
         return;
     const float carry = a.dgt[((size_t)j * a.H + h) * a.K + kk];
-    for (int t = bos; t < eos; ++t)
-        a.dg[((size_t)t * a.H + h) * a.K + kk] += carry;
+    const size_t rb = row_head(bos, h, a.H, a.T, a.hf);
+    const int rs = a.hf ? 1 : a.H;
+    for (int t = 0; t < eos - bos; ++t)
+        a.dg[(rb + (size_t)t * rs) * a.K + kk] += carry;
 }
 
 template <typename F>

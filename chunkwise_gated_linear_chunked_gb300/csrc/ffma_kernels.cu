@@ -43,10 +43,11 @@ struct Smem {
     static constexpr int STATE_FLOATS = S_TOT + NT;
 };
 
-// Chunk-local inclusive cumsum of g for rows [c0, c0+len) of head h into Gs[C][K] (rows >= len get the
-// running total, i.e. g = 0 there).  NT/K threads share a column; each scans C/(NT/K) rows in registers.
+// Chunk-local inclusive cumsum of g for the chunk's rows t < len into Gs[C][K] (rows >= len get the
+// running total, i.e. g = 0 there); row t of the chunk is row-head index rb + t * rs (layout-dependent).
+// NT/K threads share a column; each scans C/(NT/K) rows in registers.
 template <typename Tin, int K>
-__device__ __forceinline__ void chunk_cumsum(const Tin *__restrict__ g, int H, int h, int c0, int len,
+__device__ __forceinline__ void chunk_cumsum(const Tin *__restrict__ g, size_t rb, int rs, int len,
                                              float *Gs, float *Tot)
 {
     constexpr int PARTS = NT / K, RPP = C / PARTS;
@@ -56,7 +57,7 @@ __device__ __forceinline__ void chunk_cumsum(const Tin *__restrict__ g, int H, i
 #pragma unroll
     for (int r = 0; r < RPP; ++r) {
         const int t = part * RPP + r;
-        const float x = t < len ? IO<Tin>::load1(g + ((size_t)(c0 + t) * H + h) * K + col) : 0.f;
+        const float x = t < len ? IO<Tin>::load1(g + (rb + (size_t)t * rs) * K + col) : 0.f;
         run += x;
         vals[r] = run;
     }
@@ -72,14 +73,14 @@ __device__ __forceinline__ void chunk_cumsum(const Tin *__restrict__ g, int H, i
 
 // Load the [C][BV] value tile (rows >= len zero) into Vs.
 template <typename Tin>
-__device__ __forceinline__ void load_v(const Tin *__restrict__ v, int H, int V, int h, int v0, int c0,
-                                       int len, float *Vs)
+__device__ __forceinline__ void load_v(const Tin *__restrict__ v, size_t rb, int rs, int V, int v0, int len,
+                                       float *Vs)
 {
     for (int e = threadIdx.x; e < C * BV / 4; e += NT) {
         const int t = (e * 4) / BV, c = (e * 4) % BV;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < len)
-            x = IO<Tin>::load4(v + ((size_t)(c0 + t) * H + h) * V + v0 + c);
+            x = IO<Tin>::load4(v + (rb + (size_t)t * rs) * V + v0 + c);
         *reinterpret_cast<float4 *>(Vs + t * BV + c) = x;
     }
 }
@@ -141,8 +142,10 @@ __global__ void __launch_bounds__(NT) state_ffma(Args a)
     float gsum = 0.f;
     for (int c0 = bos; c0 < eos; c0 += C) {
         const int len = min(C, eos - c0);
-        chunk_cumsum<Tin, K>(gg, H, h, c0, len, Gs, Tot);
-        load_v<Tin>(gv, H, V, h, v0, c0, len, Vs);
+        const size_t rb = row_head(c0, h, H, a.T, a.hf);
+        const int rs = a.hf ? 1 : H;
+        chunk_cumsum<Tin, K>(gg, rb, rs, len, Gs, Tot);
+        load_v<Tin>(gv, rb, rs, V, v0, len, Vs);
         __syncthreads();
         if (threadIdx.x < K) {
             Gl[threadIdx.x] = Gs[(len - 1) * K + threadIdx.x];
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(NT) state_ffma(Args a)
             const int t = (e * 4) / K, kk = (e * 4) % K;
             float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t < len)
-                kv = IO<Tin>::load4(gk + ((size_t)(c0 + t) * H + h) * K + kk);
+                kv = IO<Tin>::load4(gk + (rb + (size_t)t * rs) * K + kk);
             float4 G4 = *reinterpret_cast<float4 *>(Gs + t * K + kk);
             G4.x = kv.x * expf(Gl[kk] - G4.x);
             G4.y = kv.y * expf(Gl[kk + 1] - G4.y);
@@ -217,8 +220,10 @@ __global__ void __launch_bounds__(NT, 1) out_ffma(Args a, int multi)
 
     for (int c0 = bos; c0 < eos; c0 += C) {
         const int len = min(C, eos - c0);
-        chunk_cumsum<Tin, K>(gg, H, h, c0, len, Gs, Tot);
-        load_v<Tin>(gv, H, V, h, v0, c0, len, Vs);
+        const size_t rb = row_head(c0, h, H, a.T, a.hf);
+        const int rs = a.hf ? 1 : H;
+        chunk_cumsum<Tin, K>(gg, rb, rs, len, Gs, Tot);
+        load_v<Tin>(gv, rb, rs, V, v0, len, Vs);
         __syncthreads();
         const int ra = min(C / 2 - 1, len - 1);
         if (tid < K) {
@@ -231,8 +236,8 @@ __global__ void __launch_bounds__(NT, 1) out_ffma(Args a, int multi)
             const int t = (e * 4) / K, kk = (e * 4) % K;
             float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), kv = qv;
             if (t < len) {
-                qv = IO<Tin>::load4(gq + ((size_t)(c0 + t) * H + h) * K + kk);
-                kv = IO<Tin>::load4(gk + ((size_t)(c0 + t) * H + h) * K + kk);
+                qv = IO<Tin>::load4(gq + (rb + (size_t)t * rs) * K + kk);
+                kv = IO<Tin>::load4(gk + (rb + (size_t)t * rs) * K + kk);
             }
             float4 G4 = *reinterpret_cast<float4 *>(Gs + t * K + kk);
             float kh[4];
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(NT, 1) out_ffma(Args a, int multi)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 if (t0 + i < len)
-                    IO<Tout>::store4(go + ((size_t)(c0 + t0 + i) * H + h) * V + v0 + cv,
+                    IO<Tout>::store4(go + (rb + (size_t)(t0 + i) * rs) * V + v0 + cv,
                                      make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
         }
 

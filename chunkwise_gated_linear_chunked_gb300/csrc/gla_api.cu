@@ -215,6 +215,7 @@ using namespace gla;
 
 extern "C" size_t gla_fwd_workspace_size(int B, int T, int H, int K, int V, int N, int chunk, int dtype)
 {
+    dtype &= ~GLA_HEAD_FIRST;   // the layout does not change the workspace
     // The workspace size does not depend on whether cu_seqlens is given except through N; size for the
     // larger of the two layouts so one query serves both.
     const bool varlen_ok = check_shape(B, T, H, K, V, N, chunk, dtype, B == 1) == GLA_OK;
@@ -239,6 +240,10 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
                        void *stream)
 {
     const bool varlen = cu_seqlens != nullptr;
+    const bool hf = (dtype & GLA_HEAD_FIRST) != 0;
+    dtype &= ~GLA_HEAD_FIRST;
+    if (hf && varlen)
+        return GLA_ERR_UNSUPPORTED;
     int rc = check_shape(B, T, H, K, V, N, chunk, dtype, varlen);
     if (rc != GLA_OK)
         return rc;
@@ -289,6 +294,7 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     a.q = q; a.k = k; a.v = v; a.g = g; a.o = o; a.h0 = h0; a.ht = ht; a.cu = cu_seqlens;
     a.scale = scale;
     a.seg_cap = 0;
+    a.hf = hf ? 1 : 0;
     a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.N = N; a.L = pl.L; a.P = pl.P; a.J = pl.J;
     a.status = reinterpret_cast<int *>(ws + pl.off_status);
     if (varlen) {
@@ -478,6 +484,7 @@ using namespace gla;
 
 extern "C" size_t gla_bwd_workspace_size(int B, int T, int H, int K, int V, int N, int chunk, int dtype)
 {
+    dtype &= ~GLA_HEAD_FIRST;
     if (check_bwd_shape(B, T, H, K, V, N, chunk, dtype, false) != GLA_OK &&
         check_bwd_shape(1, T, H, K, V, N, chunk, dtype, true) != GLA_OK)
         return 0;
@@ -493,6 +500,10 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
                        void *workspace, size_t workspace_bytes, void *stream)
 {
     const bool varlen = cu_seqlens != nullptr;
+    const bool hf = (dtype & GLA_HEAD_FIRST) != 0;
+    dtype &= ~GLA_HEAD_FIRST;
+    if (hf && varlen)
+        return GLA_ERR_UNSUPPORTED;
     int rc = check_bwd_shape(B, T, H, K, V, N, chunk, dtype, varlen);
     if (rc != GLA_OK)
         return rc;
@@ -548,6 +559,7 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
     a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dh0 = dh0;
     a.scale = scale;
     a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.N = nseq; a.NC = bp.NC;
+    a.hf = hf ? 1 : 0;
     a.status = reinterpret_cast<int *>(ws);
     a.dS = reinterpret_cast<float *>(ws + bp.off_dS);
     a.dR = reinterpret_cast<float *>(ws + bp.off_dR);

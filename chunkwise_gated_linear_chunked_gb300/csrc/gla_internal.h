@@ -38,6 +38,7 @@ struct Args {
     float scale;
     int B, T, H, K, V, N, L, P, J;
     int seg_cap;           // varlen: most segments per sequence (the segment length grows to respect it)
+    int hf;                // head-first layout [B, H, T, *] of q, k, v, g, o (dense batches only)
     int lb;                // fused tensor kernel: segments per block of the start-state scan
     const int4 *table;     // varlen: per slot {n, p, bos, eos}; n < 0 marks an unused slot
     const int2 *seqinfo;   // varlen: per sequence {first slot, slot count}
@@ -52,6 +53,16 @@ struct Args {
     int *status;           // sticky device status word
 };
 
+// Row-head index of packed row `row` (b*T + t for a dense batch) and head h: time-major [rows, H, *] or
+// head-first [B, H, T, *] (dense batches only).  Multiply by the row width and add the column.
+__device__ __forceinline__ size_t row_head(int row, int h, int H, int T, int hf)
+{
+    if (!hf)
+        return (size_t)row * H + h;
+    const int b = row / T;
+    return ((size_t)b * H + h) * T + (row - b * T);
+}
+
 // Backward kernel arguments (passed by value).  Chunk slots: dense j = n * NC + c; varlen from the slot
 // table (plan_varlen with 64-row segments).
 struct BwdArgs {
@@ -60,6 +71,7 @@ struct BwdArgs {
     float *dq, *dk, *dv, *dg, *dh0;   // fp32 outputs; dh0 may be nullptr
     float scale;
     int B, T, H, K, V, N, NC;
+    int hf;                           // head-first layout [B, H, T, *] of inputs and gradients (dense only)
     const int4 *table;                // varlen: per chunk slot {n, p, bos, eos}; n < 0 marks an unused slot
     const int2 *seqinfo;              // varlen: per sequence {first slot, slot count}
     float *dS;                        // [J][H][K][V]: chunk contributions, then chunk-start states

@@ -140,7 +140,7 @@ __device__ __forceinline__ float4 f4(const uint32_t *r)
     return make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]), __uint_as_float(r[3]));
 }
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool HF>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gla_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
@@ -423,16 +423,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         break;
                     uint8_t *st = sm + s * STAGE;
                     const int row0 = bos + chunk_of(q) * C;
+                    // tensor-map coordinates of the chunk: (head, row) time-major, (row in sequence,
+                    // sequence * H + head) head-first
+                    const int tc1 = HF ? row0 - n * a.T : h, tc2 = HF ? n * H + h : row0;
                     const bool out = q >= nA;
                     bar_expect_tx(&full[s], (out ? 4 : 3) * 16384);
                     if (out) {
-                        tma_load_3d(st + ST_Q0, &tm_q, 0, h, row0, &full[s]);
-                        tma_load_3d(st + 16384 + ST_Q0, &tm_q, 64, h, row0, &full[s]);
+                        tma_load_3d(st + ST_Q0, &tm_q, 0, tc1, tc2, &full[s]);
+                        tma_load_3d(st + 16384 + ST_Q0, &tm_q, 64, tc1, tc2, &full[s]);
                     }
-                    tma_load_3d(st + ST_K0, &tm_k, 0, h, row0, &full[s]);
-                    tma_load_3d(st + 16384 + ST_K0, &tm_k, 64, h, row0, &full[s]);
-                    tma_load_3d(st + ST_G, &tm_g, 0, h, row0, &full[s]);
-                    tma_load_3d(st + ST_V, &tm_v, v0, h, row0, &full[s]);
+                    tma_load_3d(st + ST_K0, &tm_k, 0, tc1, tc2, &full[s]);
+                    tma_load_3d(st + 16384 + ST_K0, &tm_k, 64, tc1, tc2, &full[s]);
+                    tma_load_3d(st + ST_G, &tm_g, 0, tc1, tc2, &full[s]);
+                    tma_load_3d(st + ST_V, &tm_v, v0, tc1, tc2, &full[s]);
                 }
                 if (!ok) {
                     *abort_w = 1;
@@ -708,7 +711,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const bool leader = b == 0;
             float *ost = reinterpret_cast<float *>(sm + OFF_OST);
             Tout *go = static_cast<Tout *>(a.o);
-            const size_t rstride = (size_t)H * V;
+            const size_t rstride = HF ? (size_t)V : (size_t)H * V;   // between consecutive rows of o
             bool ok = chain();
             for (int c = 0; ok && c < nchunks; ++c) {
                 const int gb = nbbase + c;
@@ -763,11 +766,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         fence_proxy_async();
                         sync_output();
                         if (leader) {
-                            tma_store_3d(&tm_o, ost, v0, h, row0 + half * 32);
+                            if (HF)
+                                tma_store_3d(&tm_o, ost, v0, row0 - n * a.T + half * 32, n * H + h);
+                            else
+                                tma_store_3d(&tm_o, ost, v0, h, row0 + half * 32);
                             bulk_commit();
                         }
                     } else {
-                        Tout *orow = go + ((size_t)row0 * H + h) * V + v0 + b;
+                        Tout *orow = go + row_head(row0, h, H, a.T, HF ? 1 : 0) * V + v0 + b;
 #pragma unroll
                         for (int uu = 0; uu < 32; ++uu) {
                             const int t = half * 32 + uu;
@@ -833,8 +839,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+// 3-D map of a [rows, H, D] tensor (time-major), or of a [B, H, T, D] one as {D, T, B*H} (head-first, T > 0);
+// boxes of `inner` x `brows` rows of one head.
 bool encode_rows(CUtensorMap *m, const void *ptr, int D, int H, long long rows, int inner, int brows, bool swizzle,
-                 CUtensorMapDataType type)
+                 CUtensorMapDataType type, bool hf, int T)
 {
     auto fn = encode_fn();
     if (!fn)
@@ -843,6 +851,14 @@ bool encode_rows(CUtensorMap *m, const void *ptr, int D, int H, long long rows, 
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)D * es, (cuuint64_t)H * D * es};
     cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)brows};
+    if (hf && T > 0) {
+        dims[1] = (cuuint64_t)T;
+        dims[2] = (cuuint64_t)(rows / T) * H;
+        strides[0] = (cuuint64_t)D * es;
+        strides[1] = (cuuint64_t)T * D * es;
+        box[1] = (cuuint32_t)brows;
+        box[2] = 1;
+    }
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, type, 3, const_cast<void *>(ptr),
               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -850,23 +866,24 @@ bool encode_rows(CUtensorMap *m, const void *ptr, int D, int H, long long rows, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool HF>
 cudaError_t launch_fused_t(const Plan &pl, const Args &a, cudaStream_t s, int sms)
 {
     const long long rows = pl.varlen ? (long long)pl.T : (long long)pl.B * pl.T;
     const CUtensorMapDataType tin =
         std::is_same<Tin, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap mq, mk, mg, mv, mo;
-    if (!encode_rows(&mq, a.q, pl.K, pl.H, rows, 64, C, true, tin) ||
-        !encode_rows(&mk, a.k, pl.K, pl.H, rows, 64, C, true, tin) ||
-        !encode_rows(&mg, a.g, pl.K, pl.H, rows, 128, C, false, tin) ||
-        !encode_rows(&mv, a.v, pl.V, pl.H, rows, 128, C, false, tin))
+    const bool hf = HF;
+    if (!encode_rows(&mq, a.q, pl.K, pl.H, rows, 64, C, true, tin, hf, pl.T) ||
+        !encode_rows(&mk, a.k, pl.K, pl.H, rows, 64, C, true, tin, hf, pl.T) ||
+        !encode_rows(&mg, a.g, pl.K, pl.H, rows, 128, C, false, tin, hf, pl.T) ||
+        !encode_rows(&mv, a.v, pl.V, pl.H, rows, 128, C, false, tin, hf, pl.T))
         return cudaErrorInvalidValue;
     const bool f32o = sizeof(Tout) == 4;
     if (!encode_rows(&mo, f32o ? a.o : a.v, pl.V, pl.H, rows, 128, 32, false,
-                     f32o ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+                     f32o ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, hf, pl.T))
         return cudaErrorInvalidValue;
-    auto f = gla_fused<Tin, Tout>;
+    auto f = gla_fused<Tin, Tout, HF>;
     // the shared-memory opt-in is per device: remember it per device ordinal (set every time beyond 64)
     static std::atomic<unsigned long long> attr_set{0};
     int dev = 0;
@@ -911,11 +928,15 @@ bool tc_supported(int dtype, int K, int V)
 
 cudaError_t launch_fused_tc(const Plan &pl, const Args &a, cudaStream_t s, int sms)
 {
+    // the layout is a template parameter, so the time-major kernel carries no layout branches
     if (pl.dtype == GLA_BF16_OBF16)
-        return launch_fused_t<__nv_bfloat16, __nv_bfloat16>(pl, a, s, sms);
+        return a.hf ? launch_fused_t<__nv_bfloat16, __nv_bfloat16, true>(pl, a, s, sms)
+                    : launch_fused_t<__nv_bfloat16, __nv_bfloat16, false>(pl, a, s, sms);
     if (pl.dtype == GLA_F16)
-        return launch_fused_t<__half, float>(pl, a, s, sms);
-    return launch_fused_t<__nv_bfloat16, float>(pl, a, s, sms);
+        return a.hf ? launch_fused_t<__half, float, true>(pl, a, s, sms)
+                    : launch_fused_t<__half, float, false>(pl, a, s, sms);
+    return a.hf ? launch_fused_t<__nv_bfloat16, float, true>(pl, a, s, sms)
+                : launch_fused_t<__nv_bfloat16, float, false>(pl, a, s, sms);
 }
 
 }  // namespace gla

@@ -60,6 +60,11 @@ typedef enum gla_dtype {
     GLA_BF16_OBF16 = 2, /* q, k, v, g bf16; o bf16 (the pages' o.to(v) convention)                  */
     GLA_F16 = 3         /* q, k, v, g fp16; o fp32 (same paths and bounds as GLA_BF16)                */
 } gla_dtype;
+
+/* OR-ed into the dtype argument of gla_fwd / gla_bwd (and their workspace queries): q, k, v, g, o (and the
+ * gradients) are head-first [B, H, T, *] instead of [B, T, H, *].  Dense batches only (GLA_ERR_UNSUPPORTED
+ * with cu_seqlens); h0 / ht keep [N, H, K, V].  Same paths, kernels and results otherwise. */
+#define GLA_HEAD_FIRST 0x100
 /* o is fp32 for bf16 inputs by default: at the benchmark magnitudes (|o| up to ~20) a bf16-rounded o
  * alone carries up to 0.06 of rounding error, above the 2e-2 max-abs parity bound.  State h0/ht is fp32
  * for every dtype (fused_chunk_gla_fwd_kernel keeps the state in fp32 and stores ht as fp32). */

@@ -230,3 +230,38 @@ def test_tensor_core_range_check_reports_status():
     rc = binding.fwd_into(q, k, v, g, o, inp.scale, None, None, None, 1, 1, 130, 1, 128, 128, 64,
                           binding.GLA_BF16, ws)
     assert rc == 0 and binding.get_status(ws) == binding.GLA_OK
+
+
+HEAD_FIRST_CASES = [
+    ("bf16", 2, 200, 3, 128, 128, True, None),    # tensor-core path, ragged chunk
+    ("bf16", 1, 3000, 2, 128, 256, True, None),   # segments + scan, V = 256
+    ("f16", 2, 130, 2, 128, 128, False, None),
+    ("f32", 2, 200, 2, 64, 64, True, None),       # CUDA-core path
+]
+
+
+@pytest.mark.parametrize("case", HEAD_FIRST_CASES, ids=_case_id)
+def test_head_first_layout(case):
+    """[B, H, T, *] inputs give the head-first permutation of the time-major result (elementwise parity)."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    d, B, T, H, K, V, h0, _ = case
+    inp = make_inputs(d, B=B, T=T, H=H, K=K, V=V, h0=h0, seed=zlib.crc32(_case_id(case).encode()) % 1000)
+    hf = lambda x: x.transpose(1, 2).contiguous().cuda()
+    o, ht = binding.gla_fwd(hf(inp.q), hf(inp.k), hf(inp.v), hf(inp.g), scale=inp.scale,
+                            initial_state=None if inp.h0 is None else inp.h0.cuda(), head_first=True)
+    torch.cuda.synchronize()
+    o_ref, ht_ref = run_oracle(inp)
+    assert o.shape == (B, H, T, V)
+    assert_close(as_f64(o.transpose(1, 2)), o_ref, TOL[d], "o")
+    assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
+
+
+def test_head_first_rejected_with_cu_seqlens():
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = make_inputs("bf16", B=1, T=0, H=1, K=128, V=128, lengths=[3, 5], seed=32)
+    q, k, v, g, _, cu = to_device(inp)
+    with pytest.raises(binding.GlaError) as e:
+        binding.gla_fwd(q.transpose(1, 2).contiguous(), k.transpose(1, 2).contiguous(),
+                        v.transpose(1, 2).contiguous(), g.transpose(1, 2).contiguous(), scale=inp.scale,
+                        cu_seqlens=cu, head_first=True)
+    assert e.value.code == binding.GLA_ERR_UNSUPPORTED

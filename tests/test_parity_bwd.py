@@ -114,3 +114,17 @@ def test_backward_rejects_unsupported_value_width():
     with pytest.raises(binding.GlaError) as e:
         _run(inp, do, None)
     assert e.value.code == binding.GLA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("d,K,V", [("bf16", 128, 128), ("f32", 64, 128)])
+def test_backward_head_first(d, K, V):
+    """[B, H, T, *] tensors: gradients are the head-first permutation of the time-major ones."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = make_inputs(d, B=2, T=200, H=2, K=K, V=V, h0=True, seed=27)
+    do, dh = _grad_inputs(inp, 28)
+    hf = lambda x: x.transpose(1, 2).contiguous().cuda()
+    got = binding.gla_bwd(hf(inp.q), hf(inp.k), hf(inp.v), hf(inp.g), hf(do), scale=inp.scale,
+                          initial_state=inp.h0.cuda(), dht=dh.cuda(), head_first=True)
+    torch.cuda.synchronize()
+    got = [x.transpose(1, 2) for x in got[:4]] + [got[4]]
+    _check(got, _oracle(inp, do, dh))
