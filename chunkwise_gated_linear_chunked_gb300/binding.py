@@ -16,7 +16,7 @@ from .build import LIB
 
 GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_ALIGNMENT, GLA_ERR_WORKSPACE, GLA_ERR_CUDA, \
     GLA_ERR_TIMEOUT, GLA_ERR_RANGE = range(8)
-GLA_F32, GLA_BF16, GLA_BF16_OBF16, GLA_F16 = 0, 1, 2, 3
+GLA_F32, GLA_BF16, GLA_BF16_OBF16, GLA_F16, GLA_BF16_GF32, GLA_F16_GF32 = 0, 1, 2, 3, 4, 5
 GLA_HEAD_FIRST = 0x100   # OR-ed into the dtype code: [B, H, T, *] tensors
 
 EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",
@@ -78,6 +78,24 @@ def _stream_handle(stream):
 DTYPE_CODE = {(torch.float32, torch.float32): GLA_F32, (torch.bfloat16, torch.float32): GLA_BF16,
               (torch.bfloat16, torch.bfloat16): GLA_BF16_OBF16, (torch.float16, torch.float32): GLA_F16}
 
+# 16-bit q, k, v with an fp32 g (o fp32)
+GF32_CODE = {torch.bfloat16: GLA_BF16_GF32, torch.float16: GLA_F16_GF32}
+
+
+def _dtype_code(q, g, out_dtype, what):
+    """The dtype code of a call: q, k, v share one dtype; g has it too, or is fp32 beside 16-bit q, k, v."""
+    if g.dtype == q.dtype:
+        code = DTYPE_CODE.get((q.dtype, out_dtype)) if out_dtype is not None else \
+            {torch.float32: GLA_F32, torch.bfloat16: GLA_BF16, torch.float16: GLA_F16}.get(q.dtype)
+    elif g.dtype == torch.float32 and out_dtype in (None, torch.float32):
+        code = GF32_CODE.get(q.dtype)
+    else:
+        code = None
+    if code is None:
+        raise GlaError(GLA_ERR_UNSUPPORTED, f"{what} dtypes q {q.dtype}, g {g.dtype} -> {out_dtype}")
+    return code
+
+
 _ws_lock = threading.Lock()
 _ws_cache: dict = {}
 
@@ -125,11 +143,9 @@ def gla_fwd(q, k, v, g, scale=None, initial_state=None, output_final_state=True,
     if scale is None:
         scale = K ** -0.5
     out_dtype = out_dtype or torch.float32
-    code = DTYPE_CODE.get((q.dtype, out_dtype))
-    if code is None:
-        raise GlaError(GLA_ERR_UNSUPPORTED, f"gla_fwd dtype {q.dtype} -> {out_dtype}")
+    code = _dtype_code(q, g, out_dtype, "gla_fwd")
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g)):
-        if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+        if (t.dtype != q.dtype and t is not g) or not t.is_cuda or not t.is_contiguous():
             raise GlaError(GLA_ERR_INVALID_ARG, f"gla_fwd: {name} must be a contiguous cuda {q.dtype} tensor")
     o = torch.empty(*((B, H, T, V) if head_first else (B, T, H, V)), dtype=out_dtype, device=q.device)
     ht = torch.empty(N, H, K, V, dtype=torch.float32, device=q.device) if output_final_state else None
@@ -179,11 +195,9 @@ def gla_bwd(q, k, v, g, do, scale=None, initial_state=None, dht=None, cu_seqlens
     N = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if scale is None:
         scale = K ** -0.5
-    code = {torch.float32: GLA_F32, torch.bfloat16: GLA_BF16, torch.float16: GLA_F16}.get(q.dtype)
-    if code is None:
-        raise GlaError(GLA_ERR_UNSUPPORTED, f"gla_bwd dtype {q.dtype}")
+    code = _dtype_code(q, g, None, "gla_bwd")
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("do", do)):
-        if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous():
+        if (t.dtype != q.dtype and t is not g) or not t.is_cuda or not t.is_contiguous():
             raise GlaError(GLA_ERR_INVALID_ARG, f"gla_bwd: {name} must be a contiguous cuda {q.dtype} tensor")
     for name, t in (("initial_state", initial_state), ("dht", dht)):
         if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):

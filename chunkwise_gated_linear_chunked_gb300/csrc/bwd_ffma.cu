@@ -50,7 +50,7 @@ __device__ __forceinline__ bool bwd_slot(const BwdArgs &a, int j, int &n, int &b
 // ------------------------------------------------------------------------------------------------
 // per chunk and 64-wide value tile: dS = sum_j (k_j e^{G_l - G_j})^T v_j, dR = scale sum_i (q_i e^{G_i})^T do_i
 // ------------------------------------------------------------------------------------------------
-template <typename Tin, int K>
+template <typename Tin, int K, typename Tg>
 __global__ void __launch_bounds__(NTB) bwd_chunk_sums(BwdArgs a)
 {
     extern __shared__ float sm[];
@@ -67,12 +67,13 @@ __global__ void __launch_bounds__(NTB) bwd_chunk_sums(BwdArgs a)
     const size_t rb = row_head(bos, h, H, a.T, a.hf);   // row t of the chunk: row-head index rb + t * rs
     const int rs = a.hf ? 1 : H;
     const Tin *q = static_cast<const Tin *>(a.q), *k = static_cast<const Tin *>(a.k);
-    const Tin *g = static_cast<const Tin *>(a.g), *v = static_cast<const Tin *>(a.v);
+    const Tg *g = static_cast<const Tg *>(a.g);
+    const Tin *v = static_cast<const Tin *>(a.v);
     const Tin *dout = static_cast<const Tin *>(a.dout);
     if (tid < K) {
         float run = 0.f;
         for (int i = 0; i < C; ++i) {
-            run += i < len ? IO<Tin>::load1(g + (rb + (size_t)i * rs) * K + tid) : 0.f;
+            run += i < len ? IO<Tg>::load1(g + (rb + (size_t)i * rs) * K + tid) : 0.f;
             QE[i * K + tid] = run;
         }
         GL[tid] = run;
@@ -280,7 +281,7 @@ struct BwdSmem {
     static constexpr int FLOATS = PART + NTB;
 };
 
-template <typename Tin, int K, int V>
+template <typename Tin, int K, int V, typename Tg>
 __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
 {
     using L = BwdSmem<K, V>;
@@ -296,7 +297,8 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
     const size_t rb = row_head(bos, h, H, a.T, a.hf);   // row t of the chunk: row-head index rb + t * rs
     const int rs = a.hf ? 1 : H;
     const Tin *q = static_cast<const Tin *>(a.q), *k = static_cast<const Tin *>(a.k);
-    const Tin *g = static_cast<const Tin *>(a.g), *v = static_cast<const Tin *>(a.v);
+    const Tg *g = static_cast<const Tg *>(a.g);
+    const Tin *v = static_cast<const Tin *>(a.v);
     const Tin *dout = static_cast<const Tin *>(a.dout);
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
 
@@ -307,7 +309,7 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
         const bool in = i < len;
         *reinterpret_cast<float4 *>(Q + i * K + c4) = in ? IO<Tin>::load4(q + o) : z4;
         *reinterpret_cast<float4 *>(KA + i * K + c4) = in ? IO<Tin>::load4(k + o) : z4;
-        *reinterpret_cast<float4 *>(G + i * K + c4) = in ? IO<Tin>::load4(g + o) : z4;
+        *reinterpret_cast<float4 *>(G + i * K + c4) = in ? IO<Tg>::load4(g + o) : z4;
     }
     for (int e = tid; e < C * V / 4; e += NTB) {
         const int i = e / (V / 4), c4 = (e - i * (V / 4)) * 4;
@@ -549,11 +551,11 @@ cudaError_t smem_optin(F *f, size_t bytes)
     return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-template <typename Tin, int K>
+template <typename Tin, int K, typename Tg = Tin>
 cudaError_t launch_sums_t(const BwdArgs &a, int J, cudaStream_t s)
 {
     const size_t bytes = sizeof(float) * ((size_t)2 * C * K + 2 * C * 64 + K);
-    auto f = bwd_chunk_sums<Tin, K>;
+    auto f = bwd_chunk_sums<Tin, K, Tg>;
     cudaError_t e = smem_optin(f, bytes);
     if (e != cudaSuccess)
         return e;
@@ -561,11 +563,11 @@ cudaError_t launch_sums_t(const BwdArgs &a, int J, cudaStream_t s)
     return cudaGetLastError();
 }
 
-template <typename Tin, int K, int V>
+template <typename Tin, int K, int V, typename Tg>
 cudaError_t launch_grads_t(const BwdArgs &a, int J, cudaStream_t s)
 {
     const size_t bytes = sizeof(float) * BwdSmem<K, V>::FLOATS;
-    auto f = bwd_grads<Tin, K, V>;
+    auto f = bwd_grads<Tin, K, V, Tg>;
     cudaError_t e = smem_optin(f, bytes);
     if (e != cudaSuccess)
         return e;
@@ -573,24 +575,25 @@ cudaError_t launch_grads_t(const BwdArgs &a, int J, cudaStream_t s)
     return cudaGetLastError();
 }
 
-template <typename Tin>
+template <typename Tin, typename Tg = Tin>
 cudaError_t launch_grads_kv(const BwdArgs &a, int J, cudaStream_t s)
 {
     if (a.K == 64 && a.V == 64)
-        return launch_grads_t<Tin, 64, 64>(a, J, s);
+        return launch_grads_t<Tin, 64, 64, Tg>(a, J, s);
     if (a.K == 64 && a.V == 128)
-        return launch_grads_t<Tin, 64, 128>(a, J, s);
+        return launch_grads_t<Tin, 64, 128, Tg>(a, J, s);
     if (a.K == 128 && a.V == 64)
-        return launch_grads_t<Tin, 128, 64>(a, J, s);
-    return launch_grads_t<Tin, 128, 128>(a, J, s);
+        return launch_grads_t<Tin, 128, 64, Tg>(a, J, s);
+    return launch_grads_t<Tin, 128, 128, Tg>(a, J, s);
 }
 
 }  // namespace
 
 bool bwd_supported(int dtype, int K, int V)
 {
-    return (dtype == GLA_F32 || dtype == GLA_BF16 || dtype == GLA_F16) && (K == 64 || K == 128) &&
-           (V == 64 || V == 128);
+    return (dtype == GLA_F32 || dtype == GLA_BF16 || dtype == GLA_F16 || dtype == GLA_BF16_GF32 ||
+            dtype == GLA_F16_GF32) &&
+           (K == 64 || K == 128) && (V == 64 || V == 128);
 }
 
 cudaError_t launch_bwd_sums(const BwdArgs &a, int J, int dtype, cudaStream_t s)
@@ -599,6 +602,11 @@ cudaError_t launch_bwd_sums(const BwdArgs &a, int J, int dtype, cudaStream_t s)
         return a.K == 64 ? launch_sums_t<float, 64>(a, J, s) : launch_sums_t<float, 128>(a, J, s);
     if (dtype == GLA_F16)
         return a.K == 64 ? launch_sums_t<__half, 64>(a, J, s) : launch_sums_t<__half, 128>(a, J, s);
+    if (dtype == GLA_BF16_GF32)
+        return a.K == 64 ? launch_sums_t<__nv_bfloat16, 64, float>(a, J, s)
+                         : launch_sums_t<__nv_bfloat16, 128, float>(a, J, s);
+    if (dtype == GLA_F16_GF32)
+        return a.K == 64 ? launch_sums_t<__half, 64, float>(a, J, s) : launch_sums_t<__half, 128, float>(a, J, s);
     return a.K == 64 ? launch_sums_t<__nv_bfloat16, 64>(a, J, s) : launch_sums_t<__nv_bfloat16, 128>(a, J, s);
 }
 
@@ -612,6 +620,10 @@ cudaError_t launch_bwd_grads(const BwdArgs &a, int J, int dtype, cudaStream_t s)
 {
     if (dtype == GLA_F16)
         return launch_grads_kv<__half>(a, J, s);
+    if (dtype == GLA_BF16_GF32)
+        return launch_grads_kv<__nv_bfloat16, float>(a, J, s);
+    if (dtype == GLA_F16_GF32)
+        return launch_grads_kv<__half, float>(a, J, s);
     return dtype == GLA_F32 ? launch_grads_kv<float>(a, J, s) : launch_grads_kv<__nv_bfloat16>(a, J, s);
 }
 

@@ -46,8 +46,8 @@ struct Smem {
 // Chunk-local inclusive cumsum of g for the chunk's rows t < len into Gs[C][K] (rows >= len get the
 // running total, i.e. g = 0 there); row t of the chunk is row-head index rb + t * rs (layout-dependent).
 // NT/K threads share a column; each scans C/(NT/K) rows in registers.
-template <typename Tin, int K>
-__device__ __forceinline__ void chunk_cumsum(const Tin *__restrict__ g, size_t rb, int rs, int len,
+template <typename Tg, int K>
+__device__ __forceinline__ void chunk_cumsum(const Tg *__restrict__ g, size_t rb, int rs, int len,
                                              float *Gs, float *Tot)
 {
     constexpr int PARTS = NT / K, RPP = C / PARTS;
@@ -57,7 +57,7 @@ __device__ __forceinline__ void chunk_cumsum(const Tin *__restrict__ g, size_t r
 #pragma unroll
     for (int r = 0; r < RPP; ++r) {
         const int t = part * RPP + r;
-        const float x = t < len ? IO<Tin>::load1(g + (rb + (size_t)t * rs) * K + col) : 0.f;
+        const float x = t < len ? IO<Tg>::load1(g + (rb + (size_t)t * rs) * K + col) : 0.f;
         run += x;
         vals[r] = run;
     }
@@ -121,7 +121,7 @@ __device__ __forceinline__ void advance_state(float (&S)[K / 16][4], const float
 
 // Segment state contribution (kernel b) for every non-final segment: dS = sum over the segment's chunks
 // of the decayed k^T v, starting from zero, plus the segment's total log-decay (kernel a fused in).
-template <typename Tin, int K>
+template <typename Tin, int K, typename Tg = Tin>
 __global__ void __launch_bounds__(NT) state_ffma(Args a)
 {
     extern __shared__ float4 smem4[];
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(NT) state_ffma(Args a)
     if (!resolve_slot(a, j, n, p, bos, eos, send) || eos == send)
         return;
     const Tin *__restrict__ gk = static_cast<const Tin *>(a.k);
-    const Tin *__restrict__ gg = static_cast<const Tin *>(a.g);
+    const Tg *__restrict__ gg = static_cast<const Tg *>(a.g);
     const Tin *__restrict__ gv = static_cast<const Tin *>(a.v);
     const int H = a.H, V = a.V, v0 = vt * BV;
     const int sk0 = (threadIdx.x / 16) * KPT, sv0 = (threadIdx.x % 16) * 4;
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(NT) state_ffma(Args a)
         const int len = min(C, eos - c0);
         const size_t rb = row_head(c0, h, H, a.T, a.hf);
         const int rs = a.hf ? 1 : H;
-        chunk_cumsum<Tin, K>(gg, rb, rs, len, Gs, Tot);
+        chunk_cumsum<Tg, K>(gg, rb, rs, len, Gs, Tot);
         load_v<Tin>(gv, rb, rs, V, v0, len, Vs);
         __syncthreads();
         if (threadIdx.x < K) {
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(NT) state_ffma(Args a)
 
 // Fused output (kernel d): per (value tile, head, slot) run the chunk loop of the segment with the state
 // in registers.  o_t = q~_t S' + sum_{s<=t} (q~_t . k~_s) v_s;  S <- diag(exp(G_last)) S + k^^T V.
-template <typename Tin, typename Tout, int K>
+template <typename Tin, typename Tout, int K, typename Tg = Tin>
 __global__ void __launch_bounds__(NT, 1) out_ffma(Args a, int multi)
 {
     extern __shared__ float4 smem4[];
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(NT, 1) out_ffma(Args a, int multi)
         return;
     const Tin *__restrict__ gq = static_cast<const Tin *>(a.q);
     const Tin *__restrict__ gk = static_cast<const Tin *>(a.k);
-    const Tin *__restrict__ gg = static_cast<const Tin *>(a.g);
+    const Tg *__restrict__ gg = static_cast<const Tg *>(a.g);
     const Tin *__restrict__ gv = static_cast<const Tin *>(a.v);
     Tout *__restrict__ go = static_cast<Tout *>(a.o);
     const int H = a.H, V = a.V, v0 = vt * BV;
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(NT, 1) out_ffma(Args a, int multi)
         const int len = min(C, eos - c0);
         const size_t rb = row_head(c0, h, H, a.T, a.hf);
         const int rs = a.hf ? 1 : H;
-        chunk_cumsum<Tin, K>(gg, rb, rs, len, Gs, Tot);
+        chunk_cumsum<Tg, K>(gg, rb, rs, len, Gs, Tot);
         load_v<Tin>(gv, rb, rs, V, v0, len, Vs);
         __syncthreads();
         const int ra = min(C / 2 - 1, len - 1);
@@ -509,15 +509,21 @@ cudaError_t launch_state_ffma(const Plan &pl, const Args &a, cudaStream_t s)
 {
     dim3 grid(pl.NV, pl.H, pl.J);
     const bool bf = pl.dtype == GLA_BF16 || pl.dtype == GLA_BF16_OBF16, hf = pl.dtype == GLA_F16;
-#define GLA_STATE(TIN, KK)                                                                  \
+#define GLA_STATE(TIN, KK, ...)                                                             \
     {                                                                                       \
-        auto f = state_ffma<TIN, KK>;                                                       \
+        auto f = state_ffma<TIN, KK, ##__VA_ARGS__>;                                        \
         const size_t sm = Smem<KK>::STATE_FLOATS * sizeof(float);                           \
         cudaError_t e = set_smem(f, sm);                                                    \
         if (e != cudaSuccess)                                                               \
             return e;                                                                       \
         f<<<grid, NT, sm, s>>>(a);                                                          \
         return cudaGetLastError();                                                          \
+    }
+    if (pl.dtype == GLA_BF16_GF32) {
+        if (pl.K == 64) GLA_STATE(__nv_bfloat16, 64, float) else GLA_STATE(__nv_bfloat16, 128, float)
+    }
+    if (pl.dtype == GLA_F16_GF32) {
+        if (pl.K == 64) GLA_STATE(__half, 64, float) else GLA_STATE(__half, 128, float)
     }
     if (pl.K == 64) {
         if (bf) GLA_STATE(__nv_bfloat16, 64) else if (hf) GLA_STATE(__half, 64) else GLA_STATE(float, 64)
@@ -538,9 +544,9 @@ cudaError_t launch_out_ffma(const Plan &pl, const Args &a, cudaStream_t s)
 {
     dim3 grid(pl.NV, pl.H, pl.J);
     const int multi = pl.multi ? 1 : 0;
-#define GLA_OUT(TIN, TOUT, KK)                                                              \
+#define GLA_OUT(TIN, TOUT, KK, ...)                                                         \
     {                                                                                       \
-        auto f = out_ffma<TIN, TOUT, KK>;                                                   \
+        auto f = out_ffma<TIN, TOUT, KK, ##__VA_ARGS__>;                                    \
         const size_t sm = Smem<KK>::OUT_FLOATS * sizeof(float);                             \
         cudaError_t e = set_smem(f, sm);                                                    \
         if (e != cudaSuccess)                                                               \
@@ -554,6 +560,10 @@ cudaError_t launch_out_ffma(const Plan &pl, const Args &a, cudaStream_t s)
         if (pl.K == 64) GLA_OUT(__nv_bfloat16, float, 64) else GLA_OUT(__nv_bfloat16, float, 128)
     } else if (pl.dtype == GLA_F16) {
         if (pl.K == 64) GLA_OUT(__half, float, 64) else GLA_OUT(__half, float, 128)
+    } else if (pl.dtype == GLA_BF16_GF32) {
+        if (pl.K == 64) GLA_OUT(__nv_bfloat16, float, 64, float) else GLA_OUT(__nv_bfloat16, float, 128, float)
+    } else if (pl.dtype == GLA_F16_GF32) {
+        if (pl.K == 64) GLA_OUT(__half, float, 64, float) else GLA_OUT(__half, float, 128, float)
     } else {
         if (pl.K == 64) GLA_OUT(__nv_bfloat16, __nv_bfloat16, 64)
         else GLA_OUT(__nv_bfloat16, __nv_bfloat16, 128)

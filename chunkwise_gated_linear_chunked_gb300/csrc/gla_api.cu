@@ -57,7 +57,8 @@ bool supported_v(int V) { return V == 64 || V == 128 || V == 256; }
 
 int check_shape(int B, int T, int H, int K, int V, int N, int chunk, int dtype, bool varlen)
 {
-    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_BF16_OBF16 && dtype != GLA_F16)
+    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_BF16_OBF16 && dtype != GLA_F16 &&
+        dtype != GLA_BF16_GF32 && dtype != GLA_F16_GF32)
         return GLA_ERR_UNSUPPORTED;
     if (B < 0 || T < 0 || H <= 0 || N < 0 || K <= 0 || V <= 0)
         return GLA_ERR_INVALID_ARG;
@@ -251,6 +252,7 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
         return GLA_ERR_INVALID_ARG;
     const size_t rows = varlen ? (size_t)T : (size_t)B * T;
     const size_t esz = dtype == GLA_F32 ? 4 : 2, osz = dtype == GLA_BF16_OBF16 ? 2 : 4;
+    const size_t gsz = (dtype == GLA_F32 || dtype == GLA_BF16_GF32 || dtype == GLA_F16_GF32) ? 4 : 2;
     if (rows > 0 && (!q || !k || !v || !g || !o))
         return GLA_ERR_INVALID_ARG;
     if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(g) || misaligned(o) ||
@@ -266,7 +268,7 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
         return GLA_ERR_ALIGNMENT;
     // aliasing: outputs overlap no input and no other output (h0 == ht exactly is allowed)
     const Range rq = range_of(q, rows * H * K * esz), rk = range_of(k, rows * H * K * esz);
-    const Range rg = range_of(g, rows * H * K * esz), rv = range_of(v, rows * H * V * esz);
+    const Range rg = range_of(g, rows * H * K * gsz), rv = range_of(v, rows * H * V * esz);
     const Range ro = range_of(o, rows * H * V * osz);
     const size_t sbytes = (size_t)N * H * K * V * 4;
     const Range rh0 = range_of(h0, h0 ? sbytes : 0), rht = range_of(ht, ht ? sbytes : 0);
@@ -463,7 +465,8 @@ void make_bwd_plan(BwdPlan &bp, int B, int T, int H, int K, int V, int N, bool v
 
 int check_bwd_shape(int B, int T, int H, int K, int V, int N, int chunk, int dtype, bool varlen)
 {
-    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_F16)
+    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_F16 && dtype != GLA_BF16_GF32 &&
+        dtype != GLA_F16_GF32)
         return GLA_ERR_UNSUPPORTED;
     if (B < 0 || T < 0 || H <= 0 || N < 0)
         return GLA_ERR_INVALID_ARG;
@@ -511,6 +514,7 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
         return GLA_ERR_INVALID_ARG;
     const size_t rows = varlen ? (size_t)T : (size_t)B * T;
     const size_t esz = dtype == GLA_F32 ? 4 : 2;
+    const size_t gsz = (dtype == GLA_F32 || dtype == GLA_BF16_GF32 || dtype == GLA_F16_GF32) ? 4 : 2;
     if (rows > 0 && (!q || !k || !v || !g || !dout || !dq || !dk || !dv || !dg))
         return GLA_ERR_INVALID_ARG;
     for (const void *p : {q, k, v, g, dout, (const void *)h0, (const void *)dht, (const void *)dq,
@@ -527,7 +531,7 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
     // aliasing: every output overlaps no input, no workspace and no other output
     const size_t sbytes = (size_t)(varlen ? N : B) * H * K * V * 4;
     const Range in[] = {range_of(q, rows * H * K * esz), range_of(k, rows * H * K * esz),
-                        range_of(g, rows * H * K * esz), range_of(v, rows * H * V * esz),
+                        range_of(g, rows * H * K * gsz), range_of(v, rows * H * V * esz),
                         range_of(dout, rows * H * V * esz), range_of(h0, h0 ? sbytes : 0),
                         range_of(dht, dht ? sbytes : 0),
                         range_of(cu_seqlens, varlen ? sizeof(int32_t) * (size_t)(N + 1) : 0),

@@ -923,7 +923,9 @@ cudaError_t launch_fused_t(const Plan &pl, const Args &a, cudaStream_t s, int sm
 
 bool tc_supported(int dtype, int K, int V)
 {
-    return dtype != GLA_F32 && K == KD && V % VT == 0 && V <= 256;
+    // 16-bit q, k, v and g (an fp32 g tile does not fit the stage ring: those shapes run on CUDA cores)
+    return (dtype == GLA_BF16 || dtype == GLA_BF16_OBF16 || dtype == GLA_F16) && K == KD && V % VT == 0 &&
+           V <= 256;
 }
 
 cudaError_t launch_fused_tc(const Plan &pl, const Args &a, cudaStream_t s, int sms)

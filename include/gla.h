@@ -58,7 +58,9 @@ typedef enum gla_dtype {
     GLA_F32 = 0,        /* q, k, v, g fp32; o fp32                                                  */
     GLA_BF16 = 1,       /* q, k, v, g bf16; o fp32 (default for bf16 inputs, see below)             */
     GLA_BF16_OBF16 = 2, /* q, k, v, g bf16; o bf16 (the pages' o.to(v) convention)                  */
-    GLA_F16 = 3         /* q, k, v, g fp16; o fp32 (same paths and bounds as GLA_BF16)                */
+    GLA_F16 = 3,        /* q, k, v, g fp16; o fp32 (same paths and bounds as GLA_BF16)                */
+    GLA_BF16_GF32 = 4,  /* q, k, v bf16, g fp32; o fp32 (fp32 CUDA-core path)                         */
+    GLA_F16_GF32 = 5    /* q, k, v fp16, g fp32; o fp32 (fp32 CUDA-core path)                         */
 } gla_dtype;
 
 /* OR-ed into the dtype argument of gla_fwd / gla_bwd (and their workspace queries): q, k, v, g, o (and the

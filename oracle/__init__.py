@@ -95,6 +95,19 @@ def _as_stored(x: np.ndarray):
     raise TypeError(f"oracle inputs must be float32, float16, float64 or bf16 words (uint16), got {x.dtype}")
 
 
+def _widen(x):
+    x = np.ascontiguousarray(x)
+    return bf16_words_to_f64(x) if x.dtype == np.uint16 else x.astype(np.float64)
+
+
+def _common_type(*xs):
+    """Inputs of one stored type pass through; mixed types (e.g. 16-bit q, k, v with an fp32 g) are all
+    widened exactly to float64."""
+    if len({np.asarray(x).dtype for x in xs}) == 1:
+        return xs
+    return tuple(_widen(x) for x in xs)
+
+
 def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
@@ -118,6 +131,7 @@ def gla_fwd(q, k, v, g, scale, h0=None, cu_seqlens=None, want_ht=True, nthreads=
     h0: optional [N, H, K, V] (float32 or float64; widened to float64).  cu_seqlens: optional int32 [N+1] (host), requires B == 1.
     Returns (o float64 [B, T, H, V], ht float64 [N, H, K, V] or None, threads used).
     """
+    q, k, v, g = _common_type(q, k, v, g)
     (q, dt), (k, dk), (v, dv), (g, dg) = map(_as_stored, (q, k, v, g))
     if len({dt, dk, dv, dg}) != 1:
         raise TypeError("q, k, v, g must share one stored type")
@@ -155,6 +169,7 @@ def gla_bwd(q, k, v, g, do, scale, h0=None, dht=None, cu_seqlens=None, nthreads=
     h0, dht: optional [N, H, K, V] (widened to float64).  Returns float64 (dq, dk, dv, dg, dh0) shaped like
     q, k, v, g and [N, H, K, V].
     """
+    q, k, v, g, do = _common_type(q, k, v, g, do)
     arrs = list(map(_as_stored, (q, k, v, g, do)))
     if len({a[1] for a in arrs}) != 1:
         raise TypeError("q, k, v, g, do must share one stored type")

@@ -245,7 +245,11 @@ def test_oracle_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.gla_fwd(q[:1], k[:1], v[:1], g[:1], 1.0, cu_seqlens=np.array([0, 9], np.int32))
     with pytest.raises(TypeError):
-        oracle.gla_fwd(q.astype(np.float64), k, v, g, 1.0)
+        oracle.gla_fwd(q.astype(np.int32), k.astype(np.int32), v.astype(np.int32), g.astype(np.int32), 1.0)
+    # mixed stored types (the method keeps g's type separate) are widened exactly: same as all-fp64
+    mixed = oracle.gla_fwd(q, k, v, g.astype(np.float64), 1.0)[0]
+    wide = oracle.gla_fwd(*(x.astype(np.float64) for x in (q, k, v, g)), 1.0)[0]
+    assert np.array_equal(mixed, wide)
 
 
 # ----------------------------------------------------------------------------------------------------

@@ -265,3 +265,30 @@ def test_head_first_rejected_with_cu_seqlens():
                         v.transpose(1, 2).contiguous(), g.transpose(1, 2).contiguous(), scale=inp.scale,
                         cu_seqlens=cu, head_first=True)
     assert e.value.code == binding.GLA_ERR_UNSUPPORTED
+
+
+GF32_CASES = [
+    ("bf16", 2, 200, 2, 128, 128, True, None),
+    ("f16", 1, 3000, 1, 64, 128, True, None),      # segments + scan
+    ("bf16", 1, 0, 2, 128, 64, True, [1, 63, 64, 65, 0, 130, 300, 2]),
+]
+
+
+def _with_fp32_gate(inp, seed):
+    """Replace g by an fp32 gate of the same recipe (16-bit q, k, v with fp32 g, as the method allows)."""
+    import dataclasses
+    gen = torch.Generator().manual_seed(seed)
+    g32 = torch.nn.functional.logsigmoid(torch.randn(tuple(inp.g.shape), generator=gen)) / 16
+    return dataclasses.replace(inp, g=g32)
+
+
+@pytest.mark.parametrize("case", GF32_CASES, ids=_case_id)
+def test_fp32_gate_with_16bit_inputs(case):
+    """16-bit q, k, v with an fp32 g run on the fp32 CUDA-core path: the fp32 bound applies."""
+    d, B, T, H, K, V, h0, lengths = case
+    seed = zlib.crc32(_case_id(case).encode()) % 1000
+    inp = _with_fp32_gate(make_inputs(d, B=B, T=T, H=H, K=K, V=V, h0=h0, lengths=lengths, seed=seed), seed + 1)
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(as_f64(o), o_ref, TOL["f32"], "o")
+    assert_close(as_f64(ht), ht_ref, TOL["f32"], "ht")

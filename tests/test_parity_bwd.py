@@ -128,3 +128,13 @@ def test_backward_head_first(d, K, V):
     torch.cuda.synchronize()
     got = [x.transpose(1, 2) for x in got[:4]] + [got[4]]
     _check(got, _oracle(inp, do, dh))
+
+
+@pytest.mark.parametrize("d", ["bf16", "f16"])
+def test_backward_fp32_gate(d):
+    import dataclasses
+    inp = make_inputs(d, B=2, T=200, H=2, K=128, V=128, h0=True, seed=29)
+    gen = torch.Generator().manual_seed(30)
+    inp = dataclasses.replace(inp, g=torch.nn.functional.logsigmoid(torch.randn(tuple(inp.g.shape), generator=gen)) / 16)
+    do, dh = _grad_inputs(inp, 31)
+    _check(_run(inp, do, dh), _oracle(inp, do, dh))
