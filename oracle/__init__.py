@@ -14,6 +14,9 @@ Method citations (page "fla/ops/gla/fused_chunk.py"):
 Varlen convention (offsets, per-sequence states): page "fla/ops/ttt/fused_chunk.py",
 ``fused_chunk_ttt_linear_fwd_kernel`` and ``fused_chunk_ttt_linear``.
 
+TTT-linear forward (``ttt_linear_fwd``): page "fla/ops/ttt/fused_chunk.py", ``fused_chunk_ttt_linear_fwd_kernel``
+and the ``norm_residual`` step of ``fused_chunk_ttt_linear`` (pins in ``tests/test_oracle_ttt.py``).
+
 Backward (``gla_bwd``): page "fla/ops/gla/fused_chunk.py", ``fused_chunk_gla_bwd_kernel`` and
 ``bwd_inner_chunk`` (chunked gradients of the same recurrence) and ``FusedChunkGLAFunction.backward`` (dg from
 the reverse cumsum of ``q*dq - k*dk``); the oracle differentiates the plain recurrence step by step instead.
@@ -205,6 +208,45 @@ def gla_bwd(q, k, v, g, do, scale, h0=None, dht=None, cu_seqlens=None, nthreads=
     if rc < 0:
         raise RuntimeError(f"oracle_gla_bwd failed ({rc})")
     return dq, dk, dv, dg, dh0
+
+
+def ttt_linear_fwd(q, k, v, w, b, eta, scale, eps, chunk, h0=None, hb0=None, cu_seqlens=None, nthreads=0,
+                   lib=None):
+    """fp64 TTT-linear forward (mini-batch gradient descent in chunks of ``chunk`` rows, then the residual
+    norm).  q, k, v: [B, T, H, D] (one stored type, or mixed: widened exactly); w, b: [H, D]; eta: [B, T, H]
+    (or [..., 1]); h0: [N, H, D, D]; hb0: [N, H, D] (or [N, H, 1, D]).  Returns float64 (o [B, T, H, D],
+    ht [N, H, D, D], hbt [N, H, D])."""
+    q, k, v = _common_type(q, k, v)
+    (q, dt), (k, _), (v, _) = map(_as_stored, (q, k, v))
+    B, T, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one shape [B, T, H, D] (TTT-linear needs K == V)")
+    cu = None
+    N = B
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        N = cu.size - 1
+    f64 = lambda x: None if x is None else np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    w, b = f64(w).reshape(H, D), f64(b).reshape(H, D)
+    eta = f64(eta).reshape(B * T, H)
+    h0 = None if h0 is None else f64(h0).reshape(N, H, D, D)
+    hb0 = None if hb0 is None else f64(hb0).reshape(N, H, D)
+    o = np.zeros((B, T, H, D), np.float64)
+    ht = np.zeros((N, H, D, D), np.float64)
+    hbt = np.zeros((N, H, D), np.float64)
+    lib = lib or _load()
+    if not getattr(lib, "_ttt_declared", False):
+        p_, i_ = ctypes.c_void_p, ctypes.c_int
+        lib.oracle_ttt_linear_fwd.argtypes = [p_, p_, p_, i_, p_, p_, p_, ctypes.c_double, ctypes.c_double, p_, p_,
+                                              p_, p_, p_, p_, i_, i_, i_, i_, i_, i_, i_]
+        lib.oracle_ttt_linear_fwd.restype = i_
+        lib._ttt_declared = True
+    rc = lib.oracle_ttt_linear_fwd(_ptr(q), _ptr(k), _ptr(v), dt, _ptr(w), _ptr(b), _ptr(eta), float(scale),
+                                   float(eps), _ptr(h0), _ptr(hb0), _ptr(o), _ptr(ht), _ptr(hbt), _ptr(cu), N, B, T,
+                                   H, D, int(chunk), int(nthreads))
+    if rc < 0:
+        raise RuntimeError(f"oracle_ttt_linear_fwd failed ({rc})")
+    return o, ht, hbt
 
 
 def chunk_local_cumsum(g, chunk, cu_seqlens=None):

@@ -412,3 +412,198 @@ int oracle_gla_bwd(const void *q, const void *k, const void *v, const void *g, c
     free(dense);
     return started ? rc : (rc < 0 ? rc : 1);
 }
+
+/*
+ * TTT-linear forward by mini-batch gradient descent (page "fla/ops/ttt/fused_chunk.py":
+ * fused_chunk_ttt_linear_fwd_kernel, then the norm_residual step of fused_chunk_ttt_linear), written in
+ * the kernel's dual form, fp64.  Per (sequence, head), with state h [D][D] and bias hb [D] and chunks of
+ * `chunk` rows (the mini-batch: the result depends on it):
+ *
+ *     kh_i  = k_i h + hb;  xhat_i = (kh_i - mean) / sqrt(var + eps) over D;  r_i = 1 / sqrt(var + eps)
+ *     g_i   = (xhat_i * w + b + k_i - v_i) * w                     gradient of the inner loss wrt xhat
+ *     v2_i  = r_i / D * (D g_i - sum(g_i) - xhat_i * sum(g_i * xhat_i))      ... and wrt kh_i
+ *     o_i   = scale q_i h + hb - eta_i * sum_{j <= i} (scale q_i . k_j + 1) v2_j
+ *     o_i  += LN(o_i) * w + b                                       (the residual norm of the wrapper)
+ *     h    -= eta_last * sum_j k_j^T v2_j;   hb -= eta_last * sum_j v2_j
+ *
+ * Rows past the end of a sequence do not exist (a partial last chunk has only its valid rows).  q, k, v
+ * are [rows, H, D] in the stored type `dtype`; w, b [H][D]; eta [rows][H]; h0 [N,H,D,D], hb0 [N,H,D] or
+ * NULL; outputs o [rows, H, D], ht, hbt (or NULL) in double.  Returns threads used or a negative value.
+ */
+typedef struct {
+    const void *q, *k, *v;
+    int dtype;
+    const double *w, *b, *eta, *h0, *hb0;
+    double *o, *ht, *hbt;
+    const int32_t *cu;
+    int N, H, D, BT;
+    double scale, eps;
+    int next;
+    pthread_mutex_t mu;
+} ttt_job;
+
+static void layer_norm(const double *x, int D, double eps, double *xhat, double *rstd)
+{
+    double mean = 0.0, var = 0.0;
+    for (int d = 0; d < D; ++d)
+        mean += x[d];
+    mean /= D;
+    for (int d = 0; d < D; ++d)
+        var += (x[d] - mean) * (x[d] - mean);
+    var /= D;
+    const double r = 1.0 / sqrt(var + eps);
+    for (int d = 0; d < D; ++d)
+        xhat[d] = (x[d] - mean) * r;
+    if (rstd)
+        *rstd = r;
+}
+
+static int ttt_one(ttt_job *J, int item)
+{
+    const int n = item / J->H, h = item % J->H, H = J->H, D = J->D, BT = J->BT;
+    const long bos = J->cu[n], eos = J->cu[n + 1];
+    const double *w = J->w + (size_t)h * D, *b = J->b + (size_t)h * D;
+    double *S = (double *)malloc(sizeof(double) * (size_t)D * D);
+    double *hb = (double *)malloc(sizeof(double) * (size_t)D);
+    double *V2 = (double *)malloc(sizeof(double) * (size_t)BT * D);
+    double *kh = (double *)malloc(sizeof(double) * (size_t)D);
+    double *xh = (double *)malloc(sizeof(double) * (size_t)D);
+    double *gv = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!S || !hb || !V2 || !kh || !xh || !gv) {
+        free(S); free(hb); free(V2); free(kh); free(xh); free(gv);
+        return -2;
+    }
+    const size_t st = ((size_t)n * H + h);
+    for (size_t e = 0; e < (size_t)D * D; ++e)
+        S[e] = J->h0 ? J->h0[st * D * D + e] : 0.0;
+    for (int d = 0; d < D; ++d)
+        hb[d] = J->hb0 ? J->hb0[st * D + d] : 0.0;
+    for (long r0 = bos; r0 < eos; r0 += BT) {
+        const long r1 = r0 + BT < eos ? r0 + BT : eos;
+        /* gradients of the inner loss at the chunk-start state */
+        for (long t = r0; t < r1; ++t) {
+            const size_t rb = ((size_t)t * H + h) * D;
+            for (int c = 0; c < D; ++c) {
+                double acc = hb[c];
+                for (int kk = 0; kk < D; ++kk)
+                    acc += widen(J->k, rb + kk, J->dtype) * S[(size_t)kk * D + c];
+                kh[c] = acc;
+            }
+            double r;
+            layer_norm(kh, D, J->eps, xh, &r);
+            double sg = 0.0, sgx = 0.0;
+            for (int c = 0; c < D; ++c) {
+                gv[c] = (xh[c] * w[c] + b[c] + widen(J->k, rb + c, J->dtype) - widen(J->v, rb + c, J->dtype)) * w[c];
+                sg += gv[c];
+                sgx += gv[c] * xh[c];
+            }
+            for (int c = 0; c < D; ++c)
+                V2[(size_t)(t - r0) * D + c] = r / D * (D * gv[c] - sg - xh[c] * sgx);
+        }
+        /* outputs, dual form, then the residual norm */
+        for (long t = r0; t < r1; ++t) {
+            const size_t rb = ((size_t)t * H + h) * D;
+            const double et = J->eta[(size_t)t * H + h];
+            for (int c = 0; c < D; ++c) {
+                double acc = hb[c];
+                for (int kk = 0; kk < D; ++kk)
+                    acc += J->scale * widen(J->q, rb + kk, J->dtype) * S[(size_t)kk * D + c];
+                kh[c] = acc;
+            }
+            for (long s = r0; s <= t; ++s) {
+                const size_t sb = ((size_t)s * H + h) * D;
+                double a = 0.0;
+                for (int kk = 0; kk < D; ++kk)
+                    a += J->scale * widen(J->q, rb + kk, J->dtype) * widen(J->k, sb + kk, J->dtype);
+                for (int c = 0; c < D; ++c)
+                    kh[c] -= et * (a + 1.0) * V2[(size_t)(s - r0) * D + c];
+            }
+            layer_norm(kh, D, J->eps, xh, NULL);
+            for (int c = 0; c < D; ++c)
+                J->o[rb + c] = kh[c] + xh[c] * w[c] + b[c];
+        }
+        /* state update with the learning rate of the chunk's last row */
+        const double el = J->eta[(size_t)(r1 - 1) * H + h];
+        for (long s = r0; s < r1; ++s) {
+            const size_t sb = ((size_t)s * H + h) * D;
+            for (int kk = 0; kk < D; ++kk) {
+                const double kv = el * widen(J->k, sb + kk, J->dtype);
+                for (int c = 0; c < D; ++c)
+                    S[(size_t)kk * D + c] -= kv * V2[(size_t)(s - r0) * D + c];
+            }
+            for (int c = 0; c < D; ++c)
+                hb[c] -= el * V2[(size_t)(s - r0) * D + c];
+        }
+    }
+    if (J->ht)
+        memcpy(J->ht + st * D * D, S, sizeof(double) * (size_t)D * D);
+    if (J->hbt)
+        memcpy(J->hbt + st * D, hb, sizeof(double) * (size_t)D);
+    free(S); free(hb); free(V2); free(kh); free(xh); free(gv);
+    return 0;
+}
+
+static void *ttt_worker(void *arg)
+{
+    ttt_job *J = (ttt_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int item = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (item >= J->N * J->H)
+            break;
+        if (ttt_one(J, item) != 0)
+            return (void *)1;
+    }
+    return NULL;
+}
+
+int oracle_ttt_linear_fwd(const void *q, const void *k, const void *v, int dtype, const double *w,
+                          const double *b, const double *eta, double scale, double eps, const double *h0,
+                          const double *hb0, double *o, double *ht, double *hbt, const int32_t *cu_seqlens,
+                          int N, int B, int T, int H, int D, int chunk, int nthreads)
+{
+    if (!q || !k || !v || !w || !b || !eta || !o || H <= 0 || D <= 0 || B < 0 || T < 0 || chunk <= 0)
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64 && dtype != ORACLE_F16)
+        return -1;
+    int32_t *dense = NULL;
+    const int32_t *cu = cu_seqlens;
+    if (!cu) {
+        N = B;
+        dense = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N + 1));
+        if (!dense)
+            return -2;
+        for (int n = 0; n <= N; ++n)
+            dense[n] = n * T;
+        cu = dense;
+    }
+    if (N == 0) {
+        free(dense);
+        return 0;
+    }
+    ttt_job J = {q, k, v, dtype, w, b, eta, h0, hb0, o, ht, hbt, cu, N, H, D, chunk, scale, eps, 0,
+                 PTHREAD_MUTEX_INITIALIZER};
+    const int nt = resolve_threads(nthreads, N * H);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    int rc = nt;
+    if (!tid) {
+        free(dense);
+        return -2;
+    }
+    int started = 0;
+    for (; started < nt; ++started)
+        if (pthread_create(&tid[started], NULL, ttt_worker, &J) != 0)
+            break;
+    if (started == 0 && ttt_worker(&J))
+        rc = -2;
+    for (int i = 0; i < started; ++i) {
+        void *res = NULL;
+        pthread_join(tid[i], &res);
+        if (res)
+            rc = -2;
+    }
+    free(tid);
+    free(dense);
+    return started ? rc : (rc < 0 ? rc : 1);
+}
