@@ -48,7 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "ttt"], default="fwd")
+    ap.add_argument("--ttt-chunk", type=int, default=16, help="mini-batch size of --pass ttt")
     return ap.parse_args(argv)
 
 
@@ -227,6 +228,8 @@ def main(argv=None):
     inp = workload_inputs(args.workload)
     if args.pass_ == "bwd":
         return run_backward(args, w, inp, dev, dist, world, rank)
+    if args.pass_ == "ttt":
+        return run_ttt(args, w, inp, dev, dist, world, rank)
     wu = work_units(inp)
     q, k, v, g = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.g))
     h0 = None if inp.h0 is None else inp.h0.to(dev)
@@ -471,6 +474,133 @@ def run_backward(args, w, inp, dev, dist, world, rank):
                        "l2": "flushed before every timed step (zero-fill of a 2x L2 buffer, outside the events)",
                        "parallelism": "replicas" if world == 1 else f"weak x{world} (independent sequences)"},
             "roofline": roofline,
+            "kernels_ms": {n: round(statistics.mean(x), 5) for n, x in per_kernel.items()},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": csum,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def ttt_inputs(w, inp):
+    """TTT-linear inputs on the workload's q, k, v (K == V): seeded LayerNorm weight/bias and learning rate."""
+    import torch
+    gen = torch.Generator().manual_seed(w.seed + 11)
+    H, D = inp.H, inp.K
+    lw = 1.0 + 0.2 * torch.randn(H, D, generator=gen)
+    lb = 0.1 * torch.randn(H, D, generator=gen)
+    eta = 0.02 + 0.05 * torch.rand(tuple(inp.q.shape[:3]), generator=gen)
+    return lw, lb, eta
+
+
+def ttt_flops(inp, chunk):
+    """Algorithmic flops of one TTT-linear launch (2 per multiply-add): per mini-batch of BT rows the
+    k h and q h products (2 BT D^2), the masked scores and their use (~BT^2 D) and the state update (BT D^2)."""
+    D, H = inp.K, inp.H
+    if inp.cu_seqlens is None:
+        lens = [inp.q.shape[1]] * inp.q.shape[0]
+    else:
+        lens = (inp.cu_seqlens[1:] - inp.cu_seqlens[:-1]).tolist()
+    total = 0
+    for L in lens:
+        for r0 in range(0, L, chunk):
+            bt = min(chunk, L - r0)
+            total += 3 * bt * D * D + bt * bt * D
+    return 2 * total * H
+
+
+def run_ttt(args, w, inp, dev, dist, world, rank):
+    """The TTT-linear forward step over the workload (one gla_ttt_linear_fwd), L2 flushed before each step."""
+    import torch
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    if inp.K != inp.V:
+        raise SystemExit("--pass ttt needs a workload with K == V")
+    lw, lb, eta = ttt_inputs(w, inp)
+    q, k, v = (x.to(dev) for x in (inp.q, inp.k, inp.v))
+    lwd, lbd, etad = lw.to(dev), lb.to(dev), eta.to(dev)
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.to(dev)
+    scale = inp.K ** -0.5
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.ttt_linear_fwd(q, k, v, lwd, lbd, etad, scale=scale, eps=1e-6, chunk=args.ttt_chunk,
+                               cu_seqlens=cu, workspace=ws, stream=stream)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    timer = binding.KernelTimer()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms, per_kernel, launches = [], {}, 0
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        for _ in range(args.steps):
+            flush.zero_()
+            with timer:
+                start.record(stream)
+                step()
+                end.record(stream)
+            torch.cuda.synchronize()
+            step_ms.append(start.elapsed_time(end))
+            res = timer.results()
+            launches += len(res)
+            for name, ms in res:
+                per_kernel.setdefault(name, []).append(ms)
+    if dist is not None:
+        dist.barrier()
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
+    if binding.get_status(ws) != 0:
+        raise RuntimeError("device status error in the timed region")
+    B, T = inp.q.shape[0], inp.q.shape[1]
+    value = whole_job_value(B * T, args.steps, world, total_ms)
+    dom = "ttt_linear_fwd"
+    dom_ms = statistics.mean(per_kernel[dom])
+    props = torch.cuda.get_device_properties(dev)
+    csum = clocks.summary()
+    mhz = csum.get("sm_max_mhz") or 2070.0
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    flops = ttt_flops(inp, args.ttt_chunk)
+    achieved = flops / (dom_ms / 1e3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        from chunkwise_gated_linear_chunked_gb300.inputs import stored_numpy
+        cores = os.cpu_count() or 1
+        t0 = time.perf_counter()
+        token_heads, h = 0, 0
+        while True:
+            heads = [(h + i) % inp.H for i in range(min(inp.H, cores))]
+            sel = lambda x: x[:, :, heads].contiguous()
+            oracle.ttt_linear_fwd(*(stored_numpy(sel(x)) for x in (inp.q, inp.k, inp.v)), lw[heads].numpy(),
+                                  lb[heads].numpy(), sel(eta).numpy(), scale, 1e-6, args.ttt_chunk,
+                                  cu_seqlens=None if inp.cu_seqlens is None else inp.cu_seqlens.numpy(),
+                                  nthreads=cores)
+            token_heads += B * T * len(heads)
+            h = (h + len(heads)) % inp.H
+            if time.perf_counter() - t0 >= args.cpu_seconds:
+                break
+        el = time.perf_counter() - t0
+        cpu = {"value": round(token_heads / inp.H / el, 1), "unit": "tokens/s", "cores": min(cores, inp.N * inp.H),
+               "kind": "oracle", "sample": f"fp64 TTT-linear oracle, {token_heads} token-heads, {el:.1f} s wall"}
+    if rank == 0:
+        line = {
+            "metric": "TTT-linear fwd tokens/s on 1 GB300; % of fp32 CUDA-core peak",
+            "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "pass": "ttt", "chunk": args.ttt_chunk, "B": B, "T": T,
+                       "H": inp.H, "D": inp.K, "input_dtype": inp.dtype,
+                       "l2": "flushed before every timed step (zero-fill of a 2x L2 buffer, outside the events)",
+                       "parallelism": "replicas" if world == 1 else f"weak x{world} (independent sequences)"},
+            "roofline": {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2), "peak": round(peak, 1),
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                                        f"{mhz:.0f} MHz", "traffic": None, "algorithmic_flops_per_launch": flops},
             "kernels_ms": {n: round(statistics.mean(x), 5) for n, x in per_kernel.items()},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": csum,
         }

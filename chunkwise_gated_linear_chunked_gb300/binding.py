@@ -21,7 +21,7 @@ GLA_HEAD_FIRST = 0x100   # OR-ed into the dtype code: [B, H, T, *] tensors
 
 EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",
            "gla_profile_events", "gla_profile_launches", "gla_kernel_name", "gla_fwd_noalloc", "gla_bwd",
-           "gla_bwd_workspace_size")
+           "gla_bwd_workspace_size", "gla_ttt_linear_fwd", "gla_ttt_workspace_size")
 
 if not os.path.exists(LIB):
     raise ImportError(f"libgla.so not built ({LIB}); call chunkwise_gated_linear_chunked_gb300.build.build()")
@@ -49,6 +49,11 @@ _lib.gla_bwd.argtypes = [_p, _p, _p, _p, _p, _f, _p, _p, _p, _p, _p, _p, _p, _p,
 _lib.gla_bwd.restype = _i
 _lib.gla_bwd_workspace_size.argtypes = [_i] * 8
 _lib.gla_bwd_workspace_size.restype = _sz
+_lib.gla_ttt_linear_fwd.argtypes = [_p, _p, _p, _p, _p, _p, _f, _f, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
+                                    _i, _p, _sz, _p]
+_lib.gla_ttt_linear_fwd.restype = _i
+_lib.gla_ttt_workspace_size.argtypes = []
+_lib.gla_ttt_workspace_size.restype = _sz
 
 
 class GlaError(RuntimeError):
@@ -216,6 +221,39 @@ def gla_bwd(q, k, v, g, do, scale=None, initial_state=None, dht=None, cu_seqlens
     if rc != GLA_OK:
         raise GlaError(rc, "gla_bwd")
     return dq, dk, dv, dg, dh0
+
+
+def ttt_linear_fwd(q, k, v, w, b, eta, scale=None, eps=1e-6, chunk=16, initial_state=None,
+                   initial_state_bias=None, output_final_state=True, cu_seqlens=None, stream=None, workspace=None):
+    """TTT-linear forward on the GPU.  q, k, v: [B, T, H, D] (cuda, contiguous, fp32 / bf16 / fp16); w, b:
+    fp32 [H, D]; eta: fp32 [B, T, H] (or [..., 1]).  Returns fp32 (o [B, T, H, D], ht [N, H, D, D] or None,
+    hbt [N, H, D] or None)."""
+    B, T, H, D = q.shape
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if scale is None:
+        scale = D ** -0.5
+    code = {torch.float32: GLA_F32, torch.bfloat16: GLA_BF16, torch.float16: GLA_F16}.get(q.dtype)
+    if code is None:
+        raise GlaError(GLA_ERR_UNSUPPORTED, f"gla_ttt_linear_fwd dtype {q.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != q.dtype or not t.is_cuda or not t.is_contiguous() or t.shape != q.shape:
+            raise GlaError(GLA_ERR_INVALID_ARG, f"gla_ttt_linear_fwd: {name} must be a contiguous cuda tensor like q")
+    f32 = lambda x: None if x is None else x.contiguous().float()
+    w, b, eta = f32(w), f32(b), f32(eta)
+    h0, hb0 = f32(initial_state), f32(initial_state_bias)
+    o = torch.empty(B, T, H, D, dtype=torch.float32, device=q.device)
+    ht = torch.empty(N, H, D, D, dtype=torch.float32, device=q.device) if output_final_state else None
+    hbt = torch.empty(N, H, D, dtype=torch.float32, device=q.device) if output_final_state else None
+    if workspace is None:
+        workspace = get_workspace(int(_lib.gla_ttt_workspace_size()), q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = int(_lib.gla_ttt_linear_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(b), _ptr(eta), float(scale),
+                                     float(eps), _ptr(h0), _ptr(hb0), _ptr(o), _ptr(ht), _ptr(hbt), _ptr(cu_seqlens),
+                                     N, B, T, H, D, int(chunk), code, _ptr(workspace), nbytes,
+                                     _stream_handle(stream)))
+    if rc != GLA_OK:
+        raise GlaError(rc, "gla_ttt_linear_fwd")
+    return o, ht, hbt
 
 
 def get_status(workspace, stream=None) -> int:

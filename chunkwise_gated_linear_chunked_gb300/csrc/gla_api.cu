@@ -174,7 +174,7 @@ thread_local Profile g_prof;
 
 enum KernelId {
     K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_FUSED_TC = 7,
-    K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11
+    K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11, K_TTT = 12
 };
 
 // Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
@@ -420,6 +420,7 @@ extern "C" const char *gla_kernel_name(int kernel_id)
     case K_BWD_SCAN: return "bwd_scan";
     case K_BWD_GRADS: return "bwd_grads";
     case K_BWD_DG: return "bwd_dg";
+    case K_TTT: return "ttt_linear_fwd";
     default: return "unknown";
     }
 }
@@ -593,6 +594,75 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
     if (J > 0 && profiled(K_BWD_GRADS, s, [&] { return launch_bwd_grads(a, J, dtype, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;
     if (profiled(K_BWD_DG, s, [&] { return launch_bwd_dg(a, J, s); }) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    return GLA_OK;
+}
+
+// ---------------------------------------------------------------------------------------------------
+// TTT-linear forward
+// ---------------------------------------------------------------------------------------------------
+extern "C" size_t gla_ttt_workspace_size(void) { return 256; }
+
+extern "C" int gla_ttt_linear_fwd(const void *q, const void *k, const void *v, const float *w, const float *b,
+                                  const float *eta, float scale, float eps, const float *h0, const float *hb0,
+                                  float *o, float *ht, float *hbt, const int32_t *cu_seqlens, int N, int B, int T,
+                                  int H, int D, int chunk, int dtype, void *workspace, size_t workspace_bytes,
+                                  void *stream)
+{
+    const bool varlen = cu_seqlens != nullptr;
+    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_F16)
+        return GLA_ERR_UNSUPPORTED;
+    if ((D != 64 && D != 128) || (chunk != 16 && chunk != 32))
+        return GLA_ERR_UNSUPPORTED;
+    if (B < 0 || T < 0 || H <= 0 || N < 0 || (varlen ? B != 1 : N != B))
+        return GLA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale) || !(eps > 0.f) || !std::isfinite(eps))
+        return GLA_ERR_INVALID_ARG;
+    const size_t rows = varlen ? (size_t)T : (size_t)B * T;
+    if (rows * H * D >= (1ull << 31))
+        return GLA_ERR_UNSUPPORTED;
+    if (rows > 0 && (!q || !k || !v || !eta || !o))
+        return GLA_ERR_INVALID_ARG;
+    if (!w || !b)
+        return GLA_ERR_INVALID_ARG;
+    for (const void *p : {q, k, v, (const void *)w, (const void *)b, (const void *)eta, (const void *)h0,
+                          (const void *)hb0, (const void *)o, (const void *)ht, (const void *)hbt,
+                          (const void *)cu_seqlens})
+        if (misaligned(p))
+            return GLA_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < gla_ttt_workspace_size())
+        return GLA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
+        return GLA_ERR_ALIGNMENT;
+    const size_t esz = dtype == GLA_F32 ? 4 : 2;
+    const size_t sq = (size_t)N * H * D * D * 4, sb = (size_t)N * H * D * 4;
+    const Range in[] = {range_of(q, rows * H * D * esz), range_of(k, rows * H * D * esz),
+                        range_of(v, rows * H * D * esz), range_of(w, (size_t)H * D * 4),
+                        range_of(b, (size_t)H * D * 4), range_of(eta, rows * H * 4),
+                        range_of(h0, h0 ? sq : 0), range_of(hb0, hb0 ? sb : 0),
+                        range_of(cu_seqlens, varlen ? sizeof(int32_t) * (size_t)(N + 1) : 0),
+                        range_of(workspace, 256)};
+    const Range out[] = {range_of(o, rows * H * D * 4), range_of(ht, ht ? sq : 0), range_of(hbt, hbt ? sb : 0)};
+    for (size_t i = 0; i < 3; ++i) {
+        for (const Range &r : in)
+            if (overlap(out[i], r))
+                return GLA_ERR_INVALID_ARG;
+        for (size_t j2 = i + 1; j2 < 3; ++j2)
+            if (overlap(out[i], out[j2]))
+                return GLA_ERR_INVALID_ARG;
+    }
+    g_prof.launches = 0;
+    const int nseq = varlen ? N : B;
+    if (nseq == 0)
+        return GLA_OK;
+    TttArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.w = w; a.b = b; a.eta = eta; a.scale = scale; a.eps = eps;
+    a.h0 = h0; a.hb0 = hb0; a.o = o; a.ht = ht; a.hbt = hbt; a.cu = cu_seqlens;
+    a.N = nseq; a.T = T; a.H = H; a.D = D; a.BT = chunk;
+    a.status = static_cast<int *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (profiled(K_TTT, s, [&] { return launch_ttt_linear_fwd(a, dtype, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;
     return GLA_OK;
 }

@@ -119,6 +119,20 @@ cudaError_t launch_scan(const Plan &pl, const Args &a, cudaStream_t s);
 cudaError_t launch_out_ffma(const Plan &pl, const Args &a, cudaStream_t s);
 bool tc_supported(int dtype, int K, int V);
 cudaError_t launch_fused_tc(const Plan &pl, const Args &a, cudaStream_t s, int sms);
+// TTT-linear forward arguments (passed by value).
+struct TttArgs {
+    const void *q, *k, *v;            // [rows, H, D]
+    const float *w, *b;               // [H, D] LayerNorm weight and bias
+    const float *eta;                 // [rows, H] per-token learning rate
+    float scale, eps;
+    const float *h0, *hb0;            // [N, H, D, D], [N, H, D] or nullptr
+    float *o, *ht, *hbt;              // [rows, H, D] fp32; final states or nullptr
+    const int32_t *cu;                // varlen offsets or nullptr
+    int N, T, H, D, BT;
+    int *status;
+};
+cudaError_t launch_ttt_linear_fwd(const TttArgs &a, int dtype, cudaStream_t s);
+
 bool bwd_supported(int dtype, int K, int V);
 cudaError_t launch_bwd_sums(const BwdArgs &a, int J, int dtype, cudaStream_t s);
 cudaError_t launch_bwd_scan(const BwdArgs &a, cudaStream_t s);

@@ -182,6 +182,30 @@ int gla_bwd(const void *q, const void *k, const void *v, const void *g, const vo
 size_t gla_bwd_workspace_size(int B, int T, int H, int K, int V, int N, int chunk, int dtype);
 
 /*
+ * gla_ttt_linear_fwd — TTT-linear forward, the second workload of the same chunked-state machinery (page
+ * "fla/ops/ttt/fused_chunk.py": fused_chunk_ttt_linear_fwd_kernel, then the norm_residual step of
+ * fused_chunk_ttt_linear).  Per (sequence, head) an inner model h [D][D], hb [D] takes one gradient step of
+ * 1/2 |LN(k h + hb) * w + b + k - v|^2 per mini-batch of `chunk` rows (the result depends on `chunk`), and
+ * o_i = scale q_i h_i + hb_i (dual form, rows up to i of the mini-batch), followed by o += LN(o) * w + b.
+ *
+ *   q, k, v     [rows, H, D] device, fp32 / bf16 / fp16 by dtype (GLA_F32, GLA_BF16, GLA_F16); K == V == D
+ *   w, b        [H, D] fp32 LayerNorm weight and bias;  eta [rows, H] fp32 per-token learning rate
+ *   scale > 0, eps > 0;  h0 [N, H, D, D], hb0 [N, H, D] fp32 or NULL (zeros)
+ *   o           [rows, H, D] fp32 (written);  ht [N, H, D, D], hbt [N, H, D] fp32 or NULL
+ *   cu_seqlens  int32 [N+1] device offsets or NULL (as gla_fwd);  D in {64, 128};  chunk in {16, 32}
+ *   workspace   gla_ttt_workspace_size() bytes, 256-byte aligned, zeroed before first use (status word:
+ *               bad cu_seqlens are reported there, read it with gla_get_status; those sequences are skipped)
+ *
+ * Rows past the end of a sequence take no part in the last mini-batch (the page's kernel adds its zero-padded
+ * rows to the hb update).  fp32 CUDA cores, one CTA per (sequence, head).  Errors as for gla_fwd.
+ */
+int gla_ttt_linear_fwd(const void *q, const void *k, const void *v, const float *w, const float *b,
+                       const float *eta, float scale, float eps, const float *h0, const float *hb0, float *o,
+                       float *ht, float *hbt, const int32_t *cu_seqlens, int N, int B, int T, int H, int D,
+                       int chunk, int dtype, void *workspace, size_t workspace_bytes, void *stream);
+size_t gla_ttt_workspace_size(void);
+
+/*
  * Measurement hook (no counterpart on the pages; it exists so a benchmark can time each kernel of the
  * path with CUDA events on the stream the kernels run on).  While `events` is non-NULL, every later
  * gla_fwd / gla_bwd call made from this host thread records events[2i] right before and events[2i+1] right after

@@ -1,0 +1,79 @@
+"""GPU parity of the TTT-linear forward (gla_ttt_linear_fwd through the C ABI) against its fp64 oracle.
+
+Tolerance: relative L2 <= 1e-4 for o, ht and hbt.  The inner model is updated by a serial fp32 recurrence over
+T / chunk mini-batches, each accumulating over D terms and one LayerNorm, so rounding grows with the number of
+steps; the test lengths (<= 520 rows, <= 33 steps) stay well inside that bound.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunkwise_gated_linear_chunked_gb300.inputs import stored_numpy
+from parity_util import as_f64, errors
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def make_ttt(dtype, B, T, H, D, h0, lengths, seed):
+    g = torch.Generator().manual_seed(seed)
+    cu = None
+    if lengths is not None:
+        B, T = 1, sum(lengths)
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    N = B if cu is None else len(lengths)
+    q, k, v = (torch.randn(B, T, H, D, generator=g).to(TORCH[dtype]) for _ in range(3))
+    w = 1.0 + 0.2 * torch.randn(H, D, generator=g)
+    b = 0.1 * torch.randn(H, D, generator=g)
+    eta = 0.02 + 0.05 * torch.rand(B, T, H, generator=g)
+    s0 = 0.1 * torch.randn(N, H, D, D, generator=g) if h0 else None
+    sb0 = 0.1 * torch.randn(N, H, D, generator=g) if h0 else None
+    return q, k, v, w, b, eta, s0, sb0, cu
+
+
+CASES = [
+    ("f32", 1, 64, 1, 64, True, None, 16),
+    ("f32", 2, 200, 2, 128, True, None, 16),      # ragged last mini-batch
+    ("bf16", 2, 130, 2, 128, False, None, 32),
+    ("f16", 1, 97, 3, 64, True, None, 16),
+    ("bf16", 1, 0, 2, 64, True, [1, 15, 16, 17, 0, 130, 300], 16),   # varlen incl. empty
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-B{c[1]}T{c[2]}H{c[3]}D{c[4]}-bt{c[7]}")
+def test_ttt_linear_forward(case):
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    d, B, T, H, D, h0, lengths, chunk = case
+    q, k, v, w, b, eta, s0, sb0, cu = make_ttt(d, B, T, H, D, h0, lengths, zlib.crc32(repr(case).encode()) % 1000)
+    scale = D ** -0.5
+    dev = lambda x: None if x is None else x.cuda()
+    o, ht, hbt = binding.ttt_linear_fwd(dev(q), dev(k), dev(v), dev(w), dev(b), dev(eta), scale=scale, eps=1e-6,
+                                        chunk=chunk, initial_state=dev(s0), initial_state_bias=dev(sb0),
+                                        cu_seqlens=dev(cu))
+    torch.cuda.synchronize()
+    ref = oracle.ttt_linear_fwd(*(stored_numpy(x) for x in (q, k, v)), w.numpy(), b.numpy(), eta.numpy(), scale,
+                                1e-6, chunk, h0=None if s0 is None else s0.numpy(),
+                                hb0=None if sb0 is None else sb0.numpy(),
+                                cu_seqlens=None if cu is None else cu.numpy())
+    for name, x, y in zip(("o", "ht", "hbt"), (o, ht, hbt), ref):
+        rel, mabs = errors(as_f64(x), y)
+        assert rel <= TOL, f"{name}: rel-L2 {rel:.3e} (max-abs {mabs:.3e})"
+
+
+def test_ttt_bad_offsets_are_reported_not_faulted():
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    q, k, v, w, b, eta, *_ = make_ttt("f32", 1, 40, 1, 64, False, None, 1)
+    cu = torch.tensor([0, 30, 20, 40], dtype=torch.int32).cuda()   # decreasing: invalid
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    binding.ttt_linear_fwd(q.cuda(), k.cuda(), v.cuda(), w.cuda(), b.cuda(), eta.cuda(), cu_seqlens=cu, workspace=ws)
+    assert binding.get_status(ws) == binding.GLA_ERR_INVALID_ARG
