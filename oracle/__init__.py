@@ -17,6 +17,10 @@ Varlen convention (offsets, per-sequence states): page "fla/ops/ttt/fused_chunk.
 TTT-linear forward (``ttt_linear_fwd``): page "fla/ops/ttt/fused_chunk.py", ``fused_chunk_ttt_linear_fwd_kernel``
 and the ``norm_residual`` step of ``fused_chunk_ttt_linear`` (pins in ``tests/test_oracle_ttt.py``).
 
+WY representation forward of the gated delta rule (``wy_fwd``): page
+"fla/ops/gated_delta_rule/backends/triton_ascend/wy_fast.py", ``recompute_w_u_fwd_kernel_npu`` and
+``recompute_w_u_fwd_npu`` (pins in ``tests/test_oracle_wy.py``).
+
 Backward (``gla_bwd``): page "fla/ops/gla/fused_chunk.py", ``fused_chunk_gla_bwd_kernel`` and
 ``bwd_inner_chunk`` (chunked gradients of the same recurrence) and ``FusedChunkGLAFunction.backward`` (dg from
 the reverse cumsum of ``q*dq - k*dk``); the oracle differentiates the plain recurrence step by step instead.
@@ -247,6 +251,38 @@ def ttt_linear_fwd(q, k, v, w, b, eta, scale, eps, chunk, h0=None, hb0=None, cu_
     if rc < 0:
         raise RuntimeError(f"oracle_ttt_linear_fwd failed ({rc})")
     return o, ht, hbt
+
+
+def wy_fwd(k, v, beta, A, g=None, cu_seqlens=None, nthreads=0, lib=None):
+    """fp64 WY representation forward of the gated delta rule: per chunk of BT = A.shape[-1] rows from each
+    sequence start, u = A (v * beta) and w = A (k * beta * 2^g).  k: [B, T, H, K]; v: [B, T, HV, V];
+    beta: [B, T, HV]; A: [B, T, HV, BT]; g: [B, T, HV] (log2 units) or None.  k, v, beta, A share one stored
+    type (mixed types are widened exactly).  Returns float64 (w [B, T, HV, K], u [B, T, HV, V])."""
+    k, v, beta, A = _common_type(k, v, beta, A)
+    (k, dt), (v, _), (beta, _), (A, _) = map(_as_stored, (k, v, beta, A))
+    B, T, H, K = k.shape
+    HV, V, BT = v.shape[2], v.shape[3], A.shape[-1]
+    if v.shape[:2] != (B, T) or A.shape[:3] != (B, T, HV) or beta.reshape(B, T, -1).shape[2] != HV:
+        raise ValueError("wy_fwd: k [B,T,H,K], v [B,T,HV,V], beta [B,T,HV], A [B,T,HV,BT]")
+    cu = None
+    N = B
+    if cu_seqlens is not None:
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        N = cu.size - 1
+    g = None if g is None else np.ascontiguousarray(np.asarray(g, dtype=np.float64).reshape(B * T, HV))
+    w = np.zeros((B, T, HV, K), np.float64)
+    u = np.zeros((B, T, HV, V), np.float64)
+    lib = lib or _load()
+    if not getattr(lib, "_wy_declared", False):
+        p_, i_ = ctypes.c_void_p, ctypes.c_int
+        lib.oracle_wy_fwd.argtypes = [p_, p_, p_, p_, i_, p_, p_, p_, p_, i_, i_, i_, i_, i_, i_, i_, i_, i_]
+        lib.oracle_wy_fwd.restype = i_
+        lib._wy_declared = True
+    rc = lib.oracle_wy_fwd(_ptr(k), _ptr(v), _ptr(A), _ptr(beta), dt, _ptr(g), _ptr(w), _ptr(u), _ptr(cu), N, B, T,
+                           H, HV, K, V, BT, int(nthreads))
+    if rc < 0:
+        raise RuntimeError(f"oracle_wy_fwd failed ({rc})")
+    return w, u
 
 
 def chunk_local_cumsum(g, chunk, cu_seqlens=None):

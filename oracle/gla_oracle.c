@@ -607,3 +607,109 @@ int oracle_ttt_linear_fwd(const void *q, const void *k, const void *v, int dtype
     free(dense);
     return started ? rc : (rc < 0 ? rc : 1);
 }
+
+/*
+ * WY representation forward of the gated delta rule (page
+ * "fla/ops/gated_delta_rule/backends/triton_ascend/wy_fast.py": recompute_w_u_fwd_kernel_npu and its host
+ * launcher recompute_w_u_fwd_npu), fp64.  Each sequence is cut into chunks of BT rows from its first row
+ * (the last chunk may be partial).  For value head hv, whose key head is hv / (HV / H), and a row t of the
+ * chunk [c0, c1):
+ *
+ *     u_t = sum_{s = c0}^{c1 - 1} A_t[s - c0] * beta_s * v_s
+ *     w_t = sum_{s = c0}^{c1 - 1} A_t[s - c0] * beta_s * 2^{g_s} * k_s        (the factor 2^{g_s} is 1 without g)
+ *
+ * A_t is row t of A [rows, HV, BT]: the chunk's BT x BT matrix stored row by row, used as a full square.
+ * Rows past the end of a sequence do not exist, and the columns of A that would refer to them are not read.
+ * k [rows, H, K], v [rows, HV, V], A and beta [rows, HV] are in the stored type `dtype`; g [rows, HV] is in
+ * double or NULL; the outputs w [rows, HV, K] and u [rows, HV, V] are double and start at zero.
+ */
+typedef struct {
+    const void *k, *v, *A, *beta;
+    int dtype;
+    const double *g;
+    double *w, *u;
+    const int32_t *cu;
+    int N, H, HV, K, V, BT;
+    int next;
+    pthread_mutex_t mu;
+} wy_job;
+
+static void wy_one(wy_job *J, int item)
+{
+    const int HV = J->HV, K = J->K, V = J->V, BT = J->BT;
+    const int n = item / HV, hv = item % HV, hk = hv / (HV / J->H);
+    const long first = J->cu[n], end = J->cu[n + 1];
+    for (long c0 = first; c0 < end; c0 += BT) {
+        const long c1 = c0 + BT < end ? c0 + BT : end;
+        for (long t = c0; t < c1; ++t) {
+            double *wrow = J->w + ((size_t)t * HV + hv) * K, *urow = J->u + ((size_t)t * HV + hv) * V;
+            for (long s = c0; s < c1; ++s) {
+                const double coef = widen(J->A, ((size_t)t * HV + hv) * BT + (size_t)(s - c0), J->dtype) *
+                                    widen(J->beta, (size_t)s * HV + hv, J->dtype);
+                const double decay = J->g ? exp2(J->g[(size_t)s * HV + hv]) : 1.0;
+                for (int c = 0; c < V; ++c)
+                    urow[c] += coef * widen(J->v, ((size_t)s * HV + hv) * V + c, J->dtype);
+                for (int c = 0; c < K; ++c)
+                    wrow[c] += coef * decay * widen(J->k, ((size_t)s * J->H + hk) * K + c, J->dtype);
+            }
+        }
+    }
+}
+
+static void *wy_worker(void *arg)
+{
+    wy_job *J = (wy_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int item = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (item >= J->N * J->HV)
+            break;
+        wy_one(J, item);
+    }
+    return NULL;
+}
+
+int oracle_wy_fwd(const void *k, const void *v, const void *A, const void *beta, int dtype, const double *g,
+                  double *w, double *u, const int32_t *cu_seqlens, int N, int B, int T, int H, int HV, int K,
+                  int V, int BT, int nthreads)
+{
+    if (!k || !v || !A || !beta || !w || !u || H <= 0 || HV <= 0 || HV % H || K <= 0 || V <= 0 || BT <= 0 ||
+        B < 0 || T < 0)
+        return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64 && dtype != ORACLE_F16)
+        return -1;
+    int32_t *dense = NULL;
+    const int32_t *cu = cu_seqlens;
+    if (!cu) {
+        N = B;
+        dense = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N + 1));
+        if (!dense)
+            return -2;
+        for (int n = 0; n <= N; ++n)
+            dense[n] = n * T;
+        cu = dense;
+    }
+    if (N == 0) {
+        free(dense);
+        return 0;
+    }
+    wy_job J = {k, v, A, beta, dtype, g, w, u, cu, N, H, HV, K, V, BT, 0, PTHREAD_MUTEX_INITIALIZER};
+    const int nt = resolve_threads(nthreads, N * HV);
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+    if (!tid) {
+        free(dense);
+        return -2;
+    }
+    int started = 0;
+    for (; started < nt; ++started)
+        if (pthread_create(&tid[started], NULL, wy_worker, &J) != 0)
+            break;
+    if (started == 0)
+        wy_worker(&J);
+    for (int i = 0; i < started; ++i)
+        pthread_join(tid[i], NULL);
+    free(tid);
+    free(dense);
+    return started ? nt : 1;
+}
