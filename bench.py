@@ -26,6 +26,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -48,7 +50,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "ttt"], default="fwd")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "ttt", "wy"], default="fwd")
     ap.add_argument("--ttt-chunk", type=int, default=16, help="mini-batch size of --pass ttt")
     return ap.parse_args(argv)
 
@@ -230,6 +232,8 @@ def main(argv=None):
         return run_backward(args, w, inp, dev, dist, world, rank)
     if args.pass_ == "ttt":
         return run_ttt(args, w, inp, dev, dist, world, rank)
+    if args.pass_ == "wy":
+        return run_wy(args, w, dev, dist, world, rank)
     wu = work_units(inp)
     q, k, v, g = (x.to(dev) for x in (inp.q, inp.k, inp.v, inp.g))
     h0 = None if inp.h0 is None else inp.h0.to(dev)
@@ -602,6 +606,131 @@ def run_ttt(args, w, inp, dev, dist, world, rank):
                          "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
                                         f"{mhz:.0f} MHz", "traffic": None, "algorithmic_flops_per_launch": flops},
             "kernels_ms": {n: round(statistics.mean(x), 5) for n, x in per_kernel.items()},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": csum,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def wy_bytes_flops(x):
+    """Algorithmic bytes and flops of one WY launch: k read once per key head, v, beta, A, g read once,
+    w and u written once; 2 flops per multiply-add of the chunk products (BT x BT by BT x (K + V))."""
+    esz = 4 if x.dtype == "f32" else 2
+    rows = x.B * x.T
+    nbytes = rows * (x.H * x.K + x.HV * (x.V + 1 + x.BT)) * esz + rows * x.HV * 4 * (x.g is not None)
+    nbytes += rows * x.HV * (x.K + x.V) * 4
+    if x.cu_seqlens is None:
+        lens = [x.T] * x.B
+    else:
+        lens = (x.cu_seqlens[1:] - x.cu_seqlens[:-1]).tolist()
+    flops = 0
+    for L in lens:
+        for r0 in range(0, L, x.BT):
+            m = min(x.BT, L - r0)
+            flops += 2 * m * m * (x.K + x.V)
+    return nbytes, flops * x.HV
+
+
+def run_wy(args, w, dev, dist, world, rank):
+    """The WY-representation forward of the gated delta rule (one gla_wy_fwd) on the workload's shapes."""
+    import torch
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    from chunkwise_gated_linear_chunked_gb300.inputs import stored_numpy, wy_workload_inputs
+    x = wy_workload_inputs(args.workload)
+    k, v, beta, A, g = (t.to(dev) for t in (x.k, x.v, x.beta, x.A, x.g))
+    cu = None if x.cu_seqlens is None else x.cu_seqlens.to(dev)
+    N = x.B if cu is None else cu.numel() - 1
+    ws = torch.zeros(max(int(binding.lib().gla_wy_workspace_size(x.T, N, x.BT, int(cu is not None))), 256),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        return binding.wy_fwd(k, v, beta, A, g, cu_seqlens=cu, workspace=ws, stream=stream)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 64 << 20), dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    timer = binding.KernelTimer()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms, per_kernel, launches = [], {}, 0
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        for _ in range(args.steps):
+            flush.zero_()
+            with timer:
+                start.record(stream)
+                step()
+                end.record(stream)
+            torch.cuda.synchronize()
+            step_ms.append(start.elapsed_time(end))
+            res = timer.results()
+            launches += len(res)
+            for name, ms in res:
+                per_kernel.setdefault(name, []).append(ms)
+    if dist is not None:
+        dist.barrier()
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
+    if binding.get_status(ws) != 0:
+        raise RuntimeError("device status error in the timed region")
+    value = whole_job_value(x.B * x.T, args.steps, world, total_ms)
+    dom = "wy_fwd_ffma"
+    dom_ms = statistics.mean(per_kernel[dom])
+    props = torch.cuda.get_device_properties(dev)
+    csum = clocks.summary()
+    mhz = csum.get("sm_max_mhz") or 2070.0
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    nbytes, flops = wy_bytes_flops(x)
+    achieved = flops / (dom_ms / 1e3) / 1e12
+    peaks, hbm_src = load_peaks()
+    hbm_peak = peak_hbm(peaks)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        cores = os.cpu_count() or 1
+        t0 = time.perf_counter()
+        rows_done, n = 0, 0
+        while True:   # whole sequences of the workload, in turn, until the time budget is used
+            if x.cu_seqlens is None:
+                sl = slice(n, n + 1)
+                sub = [t[sl] for t in (x.k, x.v, x.beta, x.A, x.g)]
+                cus = None
+            else:
+                a0, a1 = int(x.cu_seqlens[n]), int(x.cu_seqlens[n + 1])
+                sub = [t[:, a0:a1] for t in (x.k, x.v, x.beta, x.A, x.g)]
+                cus = np.array([0, a1 - a0], dtype=np.int32)
+            oracle.wy_fwd(*(stored_numpy(t.contiguous()) for t in sub[:4]), sub[4].double().numpy(),
+                          cu_seqlens=cus, nthreads=cores)
+            rows_done += sub[0].shape[0] * sub[0].shape[1]
+            n = (n + 1) % (x.B if x.cu_seqlens is None else x.cu_seqlens.numel() - 1)
+            if time.perf_counter() - t0 >= args.cpu_seconds:
+                break
+        el = time.perf_counter() - t0
+        cpu = {"value": round(rows_done / el, 1), "unit": "tokens/s", "cores": min(cores, x.HV),
+               "kind": "oracle", "sample": f"fp64 WY oracle on whole sequences of the workload, {rows_done} rows, "
+                                           f"{el:.1f} s wall"}
+    if rank == 0:
+        line = {
+            "metric": "gated-delta WY forward tokens/s on 1 GB300; % of fp32 CUDA-core peak",
+            "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "pass": "wy", "chunk": x.BT, "B": x.B, "T": x.T, "H": x.H,
+                       "HV": x.HV, "K": x.K, "V": x.V, "input_dtype": x.dtype, "outputs": "fp32",
+                       "l2": "flushed before every timed step (zero-fill of a 2x L2 buffer, outside the events)",
+                       "parallelism": "replicas" if world == 1 else f"weak x{world} (independent sequences)"},
+            "roofline": {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2), "peak": round(peak, 1),
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                                        f"{mhz:.0f} MHz", "traffic": None, "algorithmic_flops_per_launch": flops,
+                         "hbm": {"algorithmic_bytes_per_launch": nbytes,
+                                 "achieved_gbs": round(nbytes / (dom_ms / 1e3) / 1e9, 1),
+                                 "peak_gbs": hbm_peak, "peak_source": hbm_src}},
+            "kernels_ms": {n_: round(statistics.mean(t), 5) for n_, t in per_kernel.items()},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": csum,
         }
         print(json.dumps(line), flush=True)

@@ -21,7 +21,8 @@ GLA_HEAD_FIRST = 0x100   # OR-ed into the dtype code: [B, H, T, *] tensors
 
 EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",
            "gla_profile_events", "gla_profile_launches", "gla_kernel_name", "gla_fwd_noalloc", "gla_bwd",
-           "gla_bwd_workspace_size", "gla_ttt_linear_fwd", "gla_ttt_workspace_size")
+           "gla_bwd_workspace_size", "gla_ttt_linear_fwd", "gla_ttt_workspace_size", "gla_wy_fwd",
+           "gla_wy_workspace_size")
 
 if not os.path.exists(LIB):
     raise ImportError(f"libgla.so not built ({LIB}); call chunkwise_gated_linear_chunked_gb300.build.build()")
@@ -52,6 +53,10 @@ _lib.gla_bwd_workspace_size.restype = _sz
 _lib.gla_ttt_linear_fwd.argtypes = [_p, _p, _p, _p, _p, _p, _f, _f, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
                                     _i, _p, _sz, _p]
 _lib.gla_ttt_linear_fwd.restype = _i
+_lib.gla_wy_fwd.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p] + [_i] * 9 + [_p, _sz, _p]
+_lib.gla_wy_fwd.restype = _i
+_lib.gla_wy_workspace_size.argtypes = [_i, _i, _i, _i]
+_lib.gla_wy_workspace_size.restype = _sz
 _lib.gla_ttt_workspace_size.argtypes = []
 _lib.gla_ttt_workspace_size.restype = _sz
 
@@ -254,6 +259,41 @@ def ttt_linear_fwd(q, k, v, w, b, eta, scale=None, eps=1e-6, chunk=16, initial_s
     if rc != GLA_OK:
         raise GlaError(rc, "gla_ttt_linear_fwd")
     return o, ht, hbt
+
+
+def wy_fwd(k, v, beta, A, g=None, cu_seqlens=None, out_dtype=None, stream=None, workspace=None):
+    """WY representation forward of the gated delta rule on the GPU: per chunk of BT = A.shape[-1] rows,
+    u = A (v * beta) and w = A (k * beta * 2^g).  k: [B, T, H, K]; v: [B, T, HV, V]; beta: [B, T, HV];
+    A: [B, T, HV, BT] (k, v, beta, A: one dtype, fp32 / bf16 / fp16, cuda, contiguous); g: fp32 [B, T, HV]
+    (log2 units) or None.  Returns (w [B, T, HV, K], u [B, T, HV, V]) in fp32, or in bf16 when
+    ``out_dtype=torch.bfloat16`` with bf16 inputs."""
+    B, T, H, K = k.shape
+    HV, V, BT = v.shape[2], v.shape[3], A.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    code = {torch.float32: GLA_F32, torch.bfloat16: GLA_BF16, torch.float16: GLA_F16}.get(k.dtype)
+    if code is None:
+        raise GlaError(GLA_ERR_UNSUPPORTED, f"gla_wy_fwd dtype {k.dtype}")
+    odt = torch.float32
+    if out_dtype == torch.bfloat16:
+        if code != GLA_BF16:
+            raise GlaError(GLA_ERR_UNSUPPORTED, "gla_wy_fwd: bf16 outputs need bf16 inputs")
+        code, odt = GLA_BF16_OBF16, torch.bfloat16
+    for name, t in (("k", k), ("v", v), ("beta", beta), ("A", A)):
+        if t.dtype != k.dtype or not t.is_cuda or not t.is_contiguous():
+            raise GlaError(GLA_ERR_INVALID_ARG, f"gla_wy_fwd: {name} must be a contiguous cuda tensor of k's dtype")
+    if g is not None:
+        g = g.contiguous().float()
+    w = torch.empty(B, T, HV, K, dtype=odt, device=k.device)
+    u = torch.empty(B, T, HV, V, dtype=odt, device=k.device)
+    if workspace is None:
+        need = int(_lib.gla_wy_workspace_size(T, N, BT, int(cu_seqlens is not None)))
+        workspace = get_workspace(max(need, 256), k.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = int(_lib.gla_wy_fwd(_ptr(k), _ptr(v), _ptr(beta), _ptr(A), _ptr(g), _ptr(w), _ptr(u), _ptr(cu_seqlens), N, B,
+                             T, H, HV, K, V, int(BT), code, _ptr(workspace), nbytes, _stream_handle(stream)))
+    if rc != GLA_OK:
+        raise GlaError(rc, "gla_wy_fwd")
+    return w, u
 
 
 def get_status(workspace, stream=None) -> int:

@@ -174,7 +174,7 @@ thread_local Profile g_prof;
 
 enum KernelId {
     K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_FUSED_TC = 7,
-    K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11, K_TTT = 12
+    K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11, K_TTT = 12, K_WY = 13
 };
 
 // Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
@@ -421,6 +421,7 @@ extern "C" const char *gla_kernel_name(int kernel_id)
     case K_BWD_GRADS: return "bwd_grads";
     case K_BWD_DG: return "bwd_dg";
     case K_TTT: return "ttt_linear_fwd";
+    case K_WY: return "wy_fwd_ffma";
     default: return "unknown";
     }
 }
@@ -663,6 +664,114 @@ extern "C" int gla_ttt_linear_fwd(const void *q, const void *k, const void *v, c
     a.status = static_cast<int *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (profiled(K_TTT, s, [&] { return launch_ttt_linear_fwd(a, dtype, s); }) != cudaSuccess)
+        return GLA_ERR_CUDA;
+    return GLA_OK;
+}
+
+// ---------------------------------------------------------------------------------------------------
+// WY representation forward (gated delta rule)
+// ---------------------------------------------------------------------------------------------------
+
+namespace {
+
+struct WyPlan {
+    int J, NT;
+    size_t off_table, off_seq, total;
+};
+
+WyPlan make_wy_plan(int B, int T, int N, int chunk, bool varlen)
+{
+    WyPlan wp;
+    std::memset(&wp, 0, sizeof wp);
+    wp.NT = varlen ? 0 : (T + chunk - 1) / chunk;
+    wp.J = varlen ? N + (T + chunk - 1) / chunk : B * wp.NT;
+    size_t off = kAlign;   // status header
+    wp.off_table = off;
+    if (varlen)
+        off += align_up(sizeof(int4) * (size_t)wp.J);
+    wp.off_seq = off;
+    if (varlen)
+        off += align_up(sizeof(int2) * (size_t)N);
+    wp.total = off;
+    return wp;
+}
+
+}  // namespace
+
+extern "C" size_t gla_wy_workspace_size(int T, int N, int chunk, int varlen)
+{
+    if (T < 0 || N < 0 || (chunk != 16 && chunk != 32 && chunk != 64))
+        return 0;
+    return make_wy_plan(1, T, N, chunk, varlen != 0).total;
+}
+
+extern "C" int gla_wy_fwd(const void *k, const void *v, const void *beta, const void *A, const float *g, void *w,
+                          void *u, const int32_t *cu_seqlens, int N, int B, int T, int H, int HV, int K, int V,
+                          int chunk, int dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    const bool varlen = cu_seqlens != nullptr;
+    if (dtype != GLA_F32 && dtype != GLA_BF16 && dtype != GLA_BF16_OBF16 && dtype != GLA_F16)
+        return GLA_ERR_UNSUPPORTED;
+    if (B < 0 || T < 0 || H <= 0 || HV <= 0 || N < 0 || K <= 0 || V <= 0 || (varlen ? B != 1 : N != B))
+        return GLA_ERR_INVALID_ARG;
+    if (HV % H)
+        return GLA_ERR_INVALID_ARG;
+    if (!wy_supported(dtype, K, V, chunk))
+        return GLA_ERR_UNSUPPORTED;
+    const size_t rows = varlen ? (size_t)T : (size_t)B * T;
+    if (rows * HV * (size_t)(K > V ? (K > chunk ? K : chunk) : (V > chunk ? V : chunk)) >= (1ull << 31) ||
+        rows * H * K >= (1ull << 31))
+        return GLA_ERR_UNSUPPORTED;
+    if (rows > 0 && (!k || !v || !beta || !A || !w || !u))
+        return GLA_ERR_INVALID_ARG;
+    for (const void *p : {k, v, beta, A, (const void *)g, (const void *)w, (const void *)u, (const void *)cu_seqlens})
+        if (misaligned(p))
+            return GLA_ERR_ALIGNMENT;
+    const WyPlan wp = make_wy_plan(B, T, N, chunk, varlen);
+    if (!workspace || workspace_bytes < wp.total)
+        return GLA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
+        return GLA_ERR_ALIGNMENT;
+    const size_t esz = dtype == GLA_F32 ? 4 : 2, osz = dtype == GLA_BF16_OBF16 ? 2 : 4;
+    const Range in[] = {range_of(k, rows * H * K * esz), range_of(v, rows * HV * V * esz),
+                        range_of(beta, rows * HV * esz), range_of(A, rows * HV * chunk * esz),
+                        range_of(g, g ? rows * HV * 4 : 0),
+                        range_of(cu_seqlens, varlen ? sizeof(int32_t) * (size_t)(N + 1) : 0),
+                        range_of(workspace, wp.total)};
+    const Range out[] = {range_of(w, rows * HV * K * osz), range_of(u, rows * HV * V * osz)};
+    for (const Range &o : out)
+        for (const Range &r : in)
+            if (overlap(o, r))
+                return GLA_ERR_INVALID_ARG;
+    if (overlap(out[0], out[1]))
+        return GLA_ERR_INVALID_ARG;
+    for (size_t i = 0; i + 1 < sizeof in / sizeof in[0]; ++i)   // the workspace is written (chunk table)
+        if (overlap(in[i], in[6]))
+            return GLA_ERR_INVALID_ARG;
+    g_prof.launches = 0;
+    if ((varlen ? N : B) == 0 || rows == 0)
+        return GLA_OK;
+    char *ws = static_cast<char *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WyArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.k = k; a.v = v; a.beta = beta; a.A = A; a.g = g; a.w = w; a.u = u;
+    a.B = B; a.T = T; a.H = H; a.HV = HV; a.K = K; a.V = V; a.BT = chunk; a.NT = wp.NT;
+    if (varlen) {
+        // the forward's slot planner with segments of one chunk gives the chunk table
+        Args pa;
+        std::memset(&pa, 0, sizeof pa);
+        pa.cu = cu_seqlens; pa.N = N; pa.T = T; pa.L = chunk; pa.J = wp.J; pa.seg_cap = 0;
+        pa.status = reinterpret_cast<int *>(ws);
+        pa.table = reinterpret_cast<const int4 *>(ws + wp.off_table);
+        pa.seqinfo = reinterpret_cast<const int2 *>(ws + wp.off_seq);
+        a.table = pa.table;
+        Plan pl;
+        std::memset(&pl, 0, sizeof pl);
+        if (profiled(K_PLAN, s, [&] { return launch_plan_varlen(pl, pa, s); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+    }
+    if (wp.J > 0 && profiled(K_WY, s, [&] { return launch_wy_fwd(a, wp.J, dtype, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;
     return GLA_OK;
 }

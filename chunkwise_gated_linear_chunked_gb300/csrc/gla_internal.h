@@ -133,6 +133,18 @@ struct TttArgs {
 };
 cudaError_t launch_ttt_linear_fwd(const TttArgs &a, int dtype, cudaStream_t s);
 
+// WY representation forward arguments (passed by value).  Chunk slots: dense j = n * NT + p; varlen from
+// the slot table (plan_varlen with segments of BT rows).
+struct WyArgs {
+    const void *k, *v, *beta, *A;     // [rows, H, K], [rows, HV, V], [rows, HV], [rows, HV, BT]
+    const float *g;                   // [rows, HV] log2-domain gate or nullptr
+    void *w, *u;                      // [rows, HV, K], [rows, HV, V]
+    int B, T, H, HV, K, V, BT, NT;
+    const int4 *table;                // varlen: per chunk slot {n, p, bos, eos}; n < 0 marks an unused slot
+};
+bool wy_supported(int dtype, int K, int V, int BT);
+cudaError_t launch_wy_fwd(const WyArgs &a, int J, int dtype, cudaStream_t s);
+
 bool bwd_supported(int dtype, int K, int V);
 cudaError_t launch_bwd_sums(const BwdArgs &a, int J, int dtype, cudaStream_t s);
 cudaError_t launch_bwd_scan(const BwdArgs &a, cudaStream_t s);

@@ -9,6 +9,13 @@ lengths are drawn first (uniform integers in [lo, hi]); then q, k ~ N(0,1) [B,T,
 [B,T,H,V], g = logsigmoid(N(0,1)) / 16 [B,T,H,K] (drawn and transformed in fp32, then cast), and, when the
 workload has an initial state, h0 = 0.1 * N(0,1) fp32 [N,H,K,V].  q, k, v, g are cast to the input dtype.
 scale = K ** -0.5.
+
+WY-representation workload (gated delta rule, ``make_wy_inputs``): the same generator and length draw,
+then k = N(0,1) / sqrt(K) [B,T,H,K] (rows of about unit norm, as the rule's normalised keys),
+v ~ N(0,1) [B,T,HV,V], beta = sigmoid(N(0,1)) [B,T,HV], A [B,T,HV,BT] unit lower-triangular per chunk (1 on
+the chunk's diagonal, 0.1 * N(0,1) below it, 0 above; chunks start at each sequence's first row), and the
+log2-domain gate g = -4 * U(0,1) fp32 [B,T,HV] (a factor 2^g in [1/16, 1]).  k, v, beta, A are cast to the
+input dtype.
 """
 from __future__ import annotations
 
@@ -98,6 +105,64 @@ def make_inputs(dtype="bf16", B=1, T=64, H=1, K=64, V=64, h0=False, lengths=None
     g = (F.logsigmoid(torch.randn(B, T, H, K, generator=gen)) / 16).to(tdt)
     h = (0.1 * torch.randn(N, H, K, V, generator=gen)) if h0 else None
     return Inputs(q, k, v, g, h, cu, K ** -0.5, B, T, H, K, V, N, chunk, dtype)
+
+
+@dataclass
+class WyInputs:
+    k: torch.Tensor
+    v: torch.Tensor
+    beta: torch.Tensor
+    A: torch.Tensor
+    g: torch.Tensor | None
+    cu_seqlens: torch.Tensor | None   # int32 [N+1] (CPU)
+    B: int
+    T: int
+    H: int
+    HV: int
+    K: int
+    V: int
+    BT: int
+    N: int
+    dtype: str
+
+
+def make_wy_inputs(dtype="bf16", B=1, T=64, H=1, HV=1, K=64, V=64, BT=64, gate=True, lengths=None, varlen=None,
+                   seed=0) -> WyInputs:
+    """Draw one WY-representation input set on the CPU (dense, or varlen as in ``make_inputs``)."""
+    gen = torch.Generator().manual_seed(int(seed))
+    cu = None
+    if varlen:
+        n, lo, hi = varlen
+        lengths = torch.randint(lo, hi + 1, (n,), generator=gen).tolist()
+    if lengths is not None:
+        lengths = [int(x) for x in lengths]
+        B, T = 1, sum(lengths)
+        cu = torch.tensor([0] + lengths, dtype=torch.int64).cumsum(0).to(torch.int32)
+    N = B if cu is None else cu.numel() - 1
+    tdt = TORCH_DTYPE[dtype]
+    k = (torch.randn(B, T, H, K, generator=gen) / K ** 0.5).to(tdt)
+    v = torch.randn(B, T, HV, V, generator=gen).to(tdt)
+    beta = torch.sigmoid(torch.randn(B, T, HV, generator=gen)).to(tdt)
+    # position of every row inside its chunk (chunks start at each sequence's first row)
+    if cu is None:
+        pos = (torch.arange(T) % BT).repeat(B)
+    else:
+        starts = torch.repeat_interleave(cu[:-1].long(), torch.tensor(lengths))
+        pos = (torch.arange(T) - starts) % BT
+    col = torch.arange(BT)
+    A = 0.1 * torch.randn(B * T, HV, BT, generator=gen)
+    A = torch.where(col[None, None, :] < pos[:, None, None], A, torch.zeros(()))
+    A = torch.where(col[None, None, :] == pos[:, None, None], torch.ones(()), A)
+    A = A.reshape(B, T, HV, BT).to(tdt)
+    g = (-4.0 * torch.rand(B, T, HV, generator=gen)) if gate else None
+    return WyInputs(k, v, beta, A, g, cu, B, T, H, HV, K, V, BT, N, dtype)
+
+
+def wy_workload_inputs(name: str, BT: int = 64) -> WyInputs:
+    """The WY workload with the shapes of forward workload ``name`` (HV = H key and value heads)."""
+    w = WORKLOADS[name]
+    return make_wy_inputs(w.dtype, B=w.B, T=w.T, H=w.H, HV=w.H, K=w.K, V=w.V, BT=BT, varlen=w.varlen or None,
+                          seed=w.seed + 50)
 
 
 def workload_inputs(name: str) -> Inputs:

@@ -197,7 +197,9 @@ size_t gla_bwd_workspace_size(int B, int T, int H, int K, int V, int N, int chun
  *               bad cu_seqlens are reported there, read it with gla_get_status; those sequences are skipped)
  *
  * Rows past the end of a sequence take no part in the last mini-batch (the page's kernel adds its zero-padded
- * rows to the hb update).  fp32 CUDA cores, one CTA per (sequence, head).  Errors as for gla_fwd.
+ * rows to the hb update).  fp32 CUDA cores, one thread-block cluster of D / 16 CTAs per (sequence, head).
+ * Errors as for gla_fwd; a bounded wait inside the kernel that ran out is reported as GLA_ERR_TIMEOUT in
+ * the status word (the outputs of that call are then void).
  */
 int gla_ttt_linear_fwd(const void *q, const void *k, const void *v, const float *w, const float *b,
                        const float *eta, float scale, float eps, const float *h0, const float *hb0, float *o,
@@ -218,6 +220,37 @@ size_t gla_ttt_workspace_size(void);
 int gla_profile_events(void **events, int n_events, int *kernel_ids);
 int gla_profile_launches(void);
 const char *gla_kernel_name(int kernel_id);
+
+/*
+ * gla_wy_fwd — WY representation forward of the gated delta rule, a third chunked workload (page
+ * "fla/ops/gated_delta_rule/backends/triton_ascend/wy_fast.py": recompute_w_u_fwd_kernel_npu and its launcher
+ * recompute_w_u_fwd_npu).  Each sequence is cut into chunks of `chunk` rows from its first row (the last one
+ * may be partial).  For value head hv, whose key head is hv / (HV / H), and row t of chunk [c0, c1):
+ *
+ *   u_t = sum_{s in [c0, c1)} A_t[s - c0] beta_s v_s,   w_t = sum_{s in [c0, c1)} A_t[s - c0] beta_s 2^{g_s} k_s
+ *
+ *   k      [rows, H, K] device, input dtype          v     [rows, HV, V] device, input dtype
+ *   beta   [rows, HV]   device, input dtype          A     [rows, HV, chunk] device, input dtype: row t holds
+ *                                                           row t - c0 of its chunk's matrix (full square)
+ *   g      [rows, HV] fp32 log2-domain gate (the factor is 2^g) or NULL (factor 1)
+ *   w      [rows, HV, K], u [rows, HV, V] device, written: fp32, or bf16 for GLA_BF16_OBF16
+ *   rows = B * T (dense) or the packed length T (varlen: cu_seqlens int32 [N+1] on the device, B == 1,
+ *   cu_seqlens[N] == T; bad offsets are reported in the status word and no row is written)
+ *   dtype  GLA_F32, GLA_BF16 (fp32 outputs), GLA_BF16_OBF16 or GLA_F16 (fp32 outputs);  K, V in {64, 128};
+ *   HV a multiple of H;  chunk in {16, 32, 64}
+ *   workspace  at least gla_wy_workspace_size(T, N, chunk) bytes, 256-byte aligned, zeroed before its first
+ *              use (status word, then the varlen chunk table)
+ *
+ * Rows past the end of a sequence do not exist: the columns of A that would refer to them are not read.
+ * fp32 CUDA cores, one CTA per (chunk, value head).  Outputs must not overlap any input, the workspace or
+ * each other.  Errors as for gla_fwd; returns GLA_OK once enqueued.
+ */
+int gla_wy_fwd(const void *k, const void *v, const void *beta, const void *A, const float *g, void *w, void *u,
+               const int32_t *cu_seqlens, int N, int B, int T, int H, int HV, int K, int V, int chunk, int dtype,
+               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace gla_wy_fwd needs (dense batches: N is ignored). */
+size_t gla_wy_workspace_size(int T, int N, int chunk, int varlen);
 
 #ifdef __cplusplus
 }

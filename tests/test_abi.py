@@ -148,3 +148,29 @@ def test_bwd_rejects_before_any_cuda_work(gla):
     assert bwd(gla, dh0=64 * A) == gla.GLA_ERR_INVALID_ARG            # dh0 overlaps the workspace
     assert bwd(gla, ws=A) == gla.GLA_ERR_INVALID_ARG                  # workspace overlaps inputs
     assert gla.bwd_workspace_size(1, 100, 2, 64, 256, 1, 64, 1) == 0
+
+
+def wy(gla, k=A, v=2 * A, beta=3 * A, Am=4 * A, g=5 * A, w=8 * A, u=9 * A, cu=None, N=2, B=2, T=100, H=2, HV=4,
+       K=64, V=64, chunk=64, dtype=1, ws=64 * A, wsb=1 << 40):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return gla.lib().gla_wy_fwd(p(k), p(v), p(beta), p(Am), p(g), p(w), p(u), p(cu), N, B, T, H, HV, K, V, chunk,
+                                dtype, p(ws), wsb, None)
+
+
+def test_wy_rejects_before_any_cuda_work(gla):
+    assert wy(gla, K=96) == gla.GLA_ERR_UNSUPPORTED
+    assert wy(gla, V=256) == gla.GLA_ERR_UNSUPPORTED
+    assert wy(gla, chunk=128) == gla.GLA_ERR_UNSUPPORTED
+    assert wy(gla, dtype=gla.GLA_BF16_GF32) == gla.GLA_ERR_UNSUPPORTED
+    assert wy(gla, HV=3) == gla.GLA_ERR_INVALID_ARG                    # value heads not a multiple of key heads
+    assert wy(gla, N=3) == gla.GLA_ERR_INVALID_ARG
+    assert wy(gla, w=None) == gla.GLA_ERR_INVALID_ARG
+    assert wy(gla, beta=3 * A + 2) == gla.GLA_ERR_ALIGNMENT
+    assert wy(gla, ws=None) == gla.GLA_ERR_WORKSPACE
+    assert wy(gla, w=2 * A + 64) == gla.GLA_ERR_INVALID_ARG            # w overlaps v
+    assert wy(gla, u=8 * A + 64) == gla.GLA_ERR_INVALID_ARG            # u overlaps w
+    assert wy(gla, ws=A) == gla.GLA_ERR_INVALID_ARG                    # workspace overlaps k
+    lib = gla.lib()
+    assert lib.gla_wy_workspace_size(100, 2, 48, 0) == 0
+    assert lib.gla_wy_workspace_size(1000, 5, 64, 1) > lib.gla_wy_workspace_size(1000, 5, 64, 0)
+    assert wy(gla, cu=80 * A, N=3, B=1, wsb=256) == gla.GLA_ERR_WORKSPACE   # varlen needs the chunk table
