@@ -37,7 +37,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel name -> source file that defines it (a traffic figure is only reused while that file is unchanged)
 KERNEL_SOURCES = {"out_ffma": "csrc/ffma_kernels.cu", "state_ffma": "csrc/ffma_kernels.cu",
                   "scan_segments": "csrc/ffma_kernels.cu", "plan_varlen": "csrc/ffma_kernels.cu",
-                  "fused_tc": "csrc/tc_fused.cu"}
+                  "fused_tc": "csrc/tc_fused.cu", "ttt_linear_fwd": "csrc/ttt_ffma.cu",
+                  "wy_fwd_ffma": "csrc/wy_ffma.cu"}
 
 
 def parse_args(argv=None):
@@ -604,7 +605,8 @@ def run_ttt(args, w, inp, dev, dist, world, rank):
             "roofline": {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2), "peak": round(peak, 1),
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                          "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
-                                        f"{mhz:.0f} MHz", "traffic": None, "algorithmic_flops_per_launch": flops},
+                                        f"{mhz:.0f} MHz", "traffic": traffic_for(dom, args.workload),
+                         "algorithmic_flops_per_launch": flops},
             "kernels_ms": {n: round(statistics.mean(x), 5) for n, x in per_kernel.items()},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": csum,
         }
@@ -726,7 +728,8 @@ def run_wy(args, w, dev, dist, world, rank):
             "roofline": {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2), "peak": round(peak, 1),
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                          "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
-                                        f"{mhz:.0f} MHz", "traffic": None, "algorithmic_flops_per_launch": flops,
+                                        f"{mhz:.0f} MHz", "traffic": traffic_for(dom, args.workload),
+                         "algorithmic_flops_per_launch": flops,
                          "hbm": {"algorithmic_bytes_per_launch": nbytes,
                                  "achieved_gbs": round(nbytes / (dom_ms / 1e3) / 1e9, 1),
                                  "peak_gbs": hbm_peak, "peak_source": hbm_src}},
