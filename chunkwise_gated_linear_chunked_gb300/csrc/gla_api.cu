@@ -174,7 +174,8 @@ thread_local Profile g_prof;
 
 enum KernelId {
     K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_FUSED_TC = 7,
-    K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11, K_TTT = 12, K_WY = 13
+    K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11, K_TTT = 12, K_WY = 13,
+    K_WY_TC = 14
 };
 
 // Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
@@ -422,6 +423,7 @@ extern "C" const char *gla_kernel_name(int kernel_id)
     case K_BWD_DG: return "bwd_dg";
     case K_TTT: return "ttt_linear_fwd";
     case K_WY: return "wy_fwd_ffma";
+    case K_WY_TC: return "wy_fwd_tc";
     default: return "unknown";
     }
 }
@@ -757,6 +759,7 @@ extern "C" int gla_wy_fwd(const void *k, const void *v, const void *beta, const 
     std::memset(&a, 0, sizeof a);
     a.k = k; a.v = v; a.beta = beta; a.A = A; a.g = g; a.w = w; a.u = u;
     a.B = B; a.T = T; a.H = H; a.HV = HV; a.K = K; a.V = V; a.BT = chunk; a.NT = wp.NT;
+    a.status = reinterpret_cast<int *>(ws);
     if (varlen) {
         // the forward's slot planner with segments of one chunk gives the chunk table
         Args pa;
@@ -771,7 +774,11 @@ extern "C" int gla_wy_fwd(const void *k, const void *v, const void *beta, const 
         if (profiled(K_PLAN, s, [&] { return launch_plan_varlen(pl, pa, s); }) != cudaSuccess)
             return GLA_ERR_CUDA;
     }
-    if (wp.J > 0 && profiled(K_WY, s, [&] { return launch_wy_fwd(a, wp.J, dtype, s); }) != cudaSuccess)
+    // bf16 inputs with K == V in {64, 128}: tensor cores; every other case: fp32 CUDA cores
+    const bool tc = wy_tc_supported(dtype, K, V);
+    if (wp.J > 0 && profiled(tc ? K_WY_TC : K_WY, s, [&] {
+            return tc ? launch_wy_fwd_tc(a, wp.J, dtype, s) : launch_wy_fwd(a, wp.J, dtype, s);
+        }) != cudaSuccess)
         return GLA_ERR_CUDA;
     return GLA_OK;
 }

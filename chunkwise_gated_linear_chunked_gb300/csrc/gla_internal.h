@@ -141,9 +141,12 @@ struct WyArgs {
     void *w, *u;                      // [rows, HV, K], [rows, HV, V]
     int B, T, H, HV, K, V, BT, NT;
     const int4 *table;                // varlen: per chunk slot {n, p, bos, eos}; n < 0 marks an unused slot
+    int *status;                      // sticky device status word
 };
 bool wy_supported(int dtype, int K, int V, int BT);
 cudaError_t launch_wy_fwd(const WyArgs &a, int J, int dtype, cudaStream_t s);
+bool wy_tc_supported(int dtype, int K, int V);
+cudaError_t launch_wy_fwd_tc(const WyArgs &a, int J, int dtype, cudaStream_t s);
 
 bool bwd_supported(int dtype, int K, int V);
 cudaError_t launch_bwd_sums(const BwdArgs &a, int J, int dtype, cudaStream_t s);

@@ -13,6 +13,8 @@
 // columns over the BT columns of A with packed two-wide fmas (two rows at a time) and stores straight from
 // registers (a warp writes contiguous row segments of w and u).  Rows past the end of a sequence are
 // zero in X and in A^T, so they add nothing, and they are not stored.
+#include <atomic>
+
 #include "gla_internal.h"
 #include "io.cuh"
 
@@ -254,9 +256,16 @@ cudaError_t launch_wy_t(const WyArgs &a, int J, cudaStream_t s)
 {
     const size_t bytes = sizeof(float) * WySmem<Tin, BT, K + V>::FLOATS;
     auto f = wy_fwd_ffma<Tin, Tout, BT, K, V>;
-    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    static std::atomic<uint64_t> ready{0};   // per-device shared-memory opt-in, done once
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    if (!(ready.load(std::memory_order_acquire) & (1ull << (dev & 63)))) {
+        if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes)) != cudaSuccess)
+            return e;
+        ready.fetch_or(1ull << (dev & 63), std::memory_order_release);
+    }
     f<<<dim3(a.HV, J), NTW, bytes, s>>>(a);
     return cudaGetLastError();
 }

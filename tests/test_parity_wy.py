@@ -2,7 +2,8 @@
 against its fp64 oracle.
 
 Tolerance: fp32 outputs rel-L2 <= 1e-5 (inputs are exact in both; each output is one fp32 sum of at most
-64 products); bf16 outputs rel-L2 <= 5e-3 and max-abs <= 2e-2 (one bf16 rounding of values of order 1).
+64 products; the tensor-core kernel splits each fp32 operand into three bf16 terms, exact to fp32 rounding);
+bf16 outputs rel-L2 <= 5e-3 and max-abs <= 2e-2 (one bf16 rounding of values of order 1).
 """
 import zlib
 
@@ -55,6 +56,10 @@ CASES = [
     ("bf16", 1, 0, 1, 2, 128, 64, 32, True, [1, 31, 32, 33, 0, 130, 7], False),    # varlen incl. empty
     ("bf16", 1, 96, 1, 1, 128, 128, 64, True, None, True),                         # bf16 outputs
     ("f32", 1, 1, 1, 1, 128, 128, 64, True, None, False),                          # a single row
+    # bf16 with K == V: the tensor-core kernel (the cases above with bf16 and K == V also take it)
+    ("bf16", 2, 77, 1, 1, 64, 64, 16, True, None, False),                          # chunk 16, one block
+    ("bf16", 1, 0, 2, 2, 128, 128, 32, True, [5, 32, 0, 70, 1], False),            # chunk 32, varlen
+    ("bf16", 3, 100, 1, 3, 128, 128, 64, False, None, True),                       # no gate, bf16 outputs
 ]
 
 
