@@ -10,11 +10,13 @@
 // its raw bf16 rows are copied straight into a 128-byte-swizzled tile.  The A operand X^T (M x K, K-major)
 // is formed on chip: X is scaled in fp32 and split into three bf16 terms x = x1 + x2 + x3 (8 significand
 // bits each, exact to fp32 rounding), each written transposed into its own swizzled tile; the three MMA
-// groups accumulate into the same TMEM columns.  A and the raw k | v rows of the next item arrive by 16-byte
-// asynchronous copies while the current item is converted, multiplied and stored; the epilogue reads D^T from
-// TMEM (lane = column of w or u) and stores rows of w and u with coalesced 128-byte segments.
+// groups accumulate into the same TMEM columns.  A work item is one 128-column block of one (chunk, value
+// head), so that two CTAs fit on an SM and one's conversion overlaps the other's MMAs and stores.  A and the
+// raw k | v columns of the next item arrive by 16-byte asynchronous copies while the current item is
+// converted, multiplied and stored; the epilogue reads D^T from TMEM (lane = column of w or u) and each warp
+// stores 32 consecutive columns of a row per instruction.
 //
-// Persistent: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...  Rows past the end of a
+// Persistent: two CTAs per SM walk the items blockIdx.x, blockIdx.x + gridDim.x, ...  Rows past the end of a
 // sequence: X^T is zero there (so A's columns for them contribute nothing) and their outputs are not stored.
 #include <atomic>
 
@@ -30,17 +32,18 @@ constexpr int NTC = 256;   // threads per CTA (8 warps)
 
 template <int BT, int KV>
 struct WyTcSmem {
-    static constexpr int NBLK = KV / 128;                      // 128-column blocks of X
+    static constexpr int NBLK = KV / 128;                      // 128-column blocks of X (one per work item)
     static constexpr int XT_TILE = 128 * 128;                  // bytes: 128 rows (columns of X) x 64 s slots
-    static constexpr int A_TILE = (BT < 8 ? 8 : BT) * 128;     // bytes: BT rows (t) x 64 s slots
-    static constexpr int XT = 0;                               // [3 terms][NBLK] X^T tiles (1024-aligned)
-    static constexpr int AB = XT + 3 * NBLK * XT_TILE;         // [2] A tiles (B operand)
-    static constexpr int RAW = AB + 2 * ((A_TILE + 1023) / 1024) * 1024;   // [2][BT][KV] raw k | v (bf16)
-    static constexpr int F = RAW + 2 * BT * KV * 2;            // [2][2][BT] row factors (k part, v part)
+    static constexpr int A_TILE = BT * 128;                    // bytes: BT rows (t) x 64 s slots
+    static constexpr int A_STRIDE = (A_TILE + 1023) / 1024 * 1024;
+    static constexpr int XT = 0;                               // [3 terms] X^T tiles of the block (1024-aligned)
+    static constexpr int AB = XT + 3 * XT_TILE;                // [2] A tiles (B operand)
+    static constexpr int RAW = AB + 2 * A_STRIDE;              // [2][BT][128] raw columns of the block (bf16)
+    static constexpr int F = RAW + 2 * BT * 128 * 2;           // [2][2][BT] row factors (k part, v part)
     static constexpr int BAR = F + 2 * 2 * BT * 4;             // mbarrier (MMA done)
     static constexpr int TSLOT = BAR + 8;                      // TMEM base address
     static constexpr int BYTES = TSLOT + 8;
-    static constexpr int TCOLS = NBLK * BT <= 32 ? 32 : (NBLK * BT <= 64 ? 64 : 128);
+    static constexpr int TCOLS = BT <= 32 ? 32 : 64;
 };
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation, both operands K-major.
@@ -61,11 +64,6 @@ __device__ __forceinline__ void cp_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(__nv_bfloat16 h)
-{
-    return static_cast<uint32_t>(*reinterpret_cast<const unsigned short *>(&h));
-}
-
 template <typename T>
 __device__ __forceinline__ T to_out_tc(float x);
 template <>
@@ -79,11 +77,15 @@ __device__ __forceinline__ __nv_bfloat16 to_out_tc<__nv_bfloat16>(float x)
     return __float2bfloat16_rn(x);
 }
 
-// Resolve work item `it` to (value head, first row, valid rows); false if it has no rows.
-__device__ __forceinline__ bool wy_item(const WyArgs &a, int it, int BT, int &hv, int &bos, int &m)
+// Resolve work item `it` = ((chunk slot j, value head hv), column block cb) to (cb, hv, first row, valid
+// rows); false if it has no rows.
+__device__ __forceinline__ bool wy_item(const WyArgs &a, int it, int BT, int nblk, int &cb, int &hv, int &bos,
+                                        int &m)
 {
-    const int j = it / a.HV;
-    hv = it - j * a.HV;
+    const int jh = it / nblk;
+    cb = it - jh * nblk;
+    const int j = jh / a.HV;
+    hv = jh - j * a.HV;
     int eos;
     if (a.table) {
         const int4 e = a.table[j];
@@ -101,7 +103,7 @@ __device__ __forceinline__ bool wy_item(const WyArgs &a, int it, int BT, int &hv
 }
 
 template <typename Tout, int BT, int K, int V>
-__global__ void __launch_bounds__(NTC, 1) wy_fwd_tc(WyArgs a, int items)
+__global__ void __launch_bounds__(NTC, 2) wy_fwd_tc(WyArgs a, int items)
 {
     constexpr int KV = K + V;
     using L = WyTcSmem<BT, KV>;
@@ -132,23 +134,22 @@ __global__ void __launch_bounds__(NTC, 1) wy_fwd_tc(WyArgs a, int items)
     // ---- asynchronous copies of item `it` into buffer `b`: A's valid rows into the swizzled B tile, the
     //      k | v rows into the raw buffer (one commit group per item, even when it has no rows)
     auto copy_item = [&](int it, int b) {
-        int hv, bos, m;
-        if (it < items && wy_item(a, it, BT, hv, bos, m)) {
+        int cb, hv, bos, m;
+        if (it < items && wy_item(a, it, BT, NBLK, cb, hv, bos, m)) {
             const int hk = hv / (HV / a.H);
-            unsigned char *at = sm + L::AB + b * ((L::A_TILE + 1023) / 1024) * 1024;
+            unsigned char *at = sm + L::AB + b * L::A_STRIDE;
             for (int e = tid; e < BT * CPR; e += NTC) {
                 const int t = e / CPR, c = e - t * CPR;
                 if (t < m)
                     cp_async16(at + tc::sw128(t, 8 * c), A + ((size_t)(bos + t) * HV + hv) * BT + 8 * c);
             }
-            __nv_bfloat16 *raw = reinterpret_cast<__nv_bfloat16 *>(sm + L::RAW) + b * BT * KV;
-            constexpr int UK = K / 8, UR = KV / 8;
-            for (int e = tid; e < BT * UR; e += NTC) {
-                const int s = e / UR, u = e - s * UR;
+            __nv_bfloat16 *raw = reinterpret_cast<__nv_bfloat16 *>(sm + L::RAW) + b * BT * 128;
+            for (int e = tid; e < BT * 16; e += NTC) {   // 16 copies of 8 columns per row of the block
+                const int s = e >> 4, cg = cb * 128 + 8 * (e & 15);
                 if (s < m) {
                     const size_t row = (size_t)(bos + s);
-                    cp_async16(raw + s * KV + 8 * u, u < UK ? k + (row * a.H + hk) * K + 8 * u
-                                                            : v + (row * HV + hv) * V + 8 * (u - UK));
+                    cp_async16(raw + s * 128 + 8 * (e & 15),
+                               cg < K ? k + (row * a.H + hk) * K + cg : v + (row * HV + hv) * V + (cg - K));
                 }
             }
         }
@@ -157,8 +158,8 @@ __global__ void __launch_bounds__(NTC, 1) wy_fwd_tc(WyArgs a, int items)
     // row factors of item `it` (plain loads; threads < BT)
     auto load_factors = [&](int it, float &fk, float &fv) {
         fk = fv = 0.f;
-        int hv, bos, m;
-        if (tid < BT && it < items && wy_item(a, it, BT, hv, bos, m) && tid < m) {
+        int cb, hv, bos, m;
+        if (tid < BT && it < items && wy_item(a, it, BT, NBLK, cb, hv, bos, m) && tid < m) {
             const size_t row = (size_t)(bos + tid);
             fv = __bfloat162float(beta[row * HV + hv]);
             fk = a.g ? fv * exp2f(a.g[row * HV + hv]) : fv;
@@ -182,43 +183,35 @@ __global__ void __launch_bounds__(NTC, 1) wy_fwd_tc(WyArgs a, int items)
         load_factors(it + step, nfk, nfv);   // the next item's factors, used after this item
         cp_wait<1>();                        // this item's copies (the next item's may still fly)
         __syncthreads();
-        int hv, bos, m;
-        const bool live = wy_item(a, it, BT, hv, bos, m);
+        int cb, hv, bos, m;
+        const bool live = wy_item(a, it, BT, NBLK, cb, hv, bos, m);
         if (live) {
             // ---- X^T terms: task (column c, s-group j of 8 rows); lanes take consecutive columns
-            const __nv_bfloat16 *raw = reinterpret_cast<const __nv_bfloat16 *>(sm + L::RAW) + b * BT * KV;
+            const __nv_bfloat16 *raw = reinterpret_cast<const __nv_bfloat16 *>(sm + L::RAW) + b * BT * 128;
             const float *Fb = F + b * 2 * BT;
-            for (int e = tid; e < KV * CPR; e += NTC) {
-                const int j = e / KV, c = e - j * KV;
-                const float *fr = Fb + (c < K ? 0 : BT);
+            for (int e = tid; e < 128 * CPR; e += NTC) {
+                const int j = e >> 7, c = e & 127;
+                const float *fr = Fb + (cb * 128 + c < K ? 0 : BT);
                 uint32_t p1[4], p2[4], p3[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t h1[2], h2[2], h3[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int s = 8 * j + 2 * q + h;
-                        const float x = s < m ? __bfloat162float(raw[s * KV + c]) * fr[s] : 0.f;
-                        const __nv_bfloat16 x1 = __float2bfloat16_rn(x);
-                        const float r1 = x - __bfloat162float(x1);
-                        const __nv_bfloat16 x2 = __float2bfloat16_rn(r1);
-                        const float r2 = r1 - __bfloat162float(x2);
-                        h1[h] = bf16_bits(x1);
-                        h2[h] = bf16_bits(x2);
-                        h3[h] = bf16_bits(__float2bfloat16_rn(r2));
-                    }
-                    p1[q] = h1[0] | (h1[1] << 16);
-                    p2[q] = h2[0] | (h2[1] << 16);
-                    p3[q] = h3[0] | (h3[1] << 16);
+                for (int q = 0; q < 4; ++q) {   // rows s0, s0 + 1 of the group, two at a time
+                    const int s0 = 8 * j + 2 * q;
+                    const float2 x = make_float2(s0 < m ? __bfloat162float(raw[s0 * 128 + c]) * fr[s0] : 0.f,
+                                                 s0 + 1 < m ? __bfloat162float(raw[(s0 + 1) * 128 + c]) * fr[s0 + 1] : 0.f);
+                    const __nv_bfloat162 x1 = __float22bfloat162_rn(x);
+                    const float2 y1 = __bfloat1622float2(x1);
+                    const float2 r1 = make_float2(x.x - y1.x, x.y - y1.y);
+                    const __nv_bfloat162 x2 = __float22bfloat162_rn(r1);
+                    const float2 y2 = __bfloat1622float2(x2);
+                    const __nv_bfloat162 x3 = __float22bfloat162_rn(make_float2(r1.x - y2.x, r1.y - y2.y));
+                    p1[q] = *reinterpret_cast<const uint32_t *>(&x1);
+                    p2[q] = *reinterpret_cast<const uint32_t *>(&x2);
+                    p3[q] = *reinterpret_cast<const uint32_t *>(&x3);
                 }
-                const int cb = c >> 7, cr = c & 127;
-                const uint32_t off = tc::sw128(cr, 8 * j);
-                *reinterpret_cast<uint4 *>(sm + L::XT + (0 * NBLK + cb) * L::XT_TILE + off) =
-                    make_uint4(p1[0], p1[1], p1[2], p1[3]);
-                *reinterpret_cast<uint4 *>(sm + L::XT + (1 * NBLK + cb) * L::XT_TILE + off) =
-                    make_uint4(p2[0], p2[1], p2[2], p2[3]);
-                *reinterpret_cast<uint4 *>(sm + L::XT + (2 * NBLK + cb) * L::XT_TILE + off) =
-                    make_uint4(p3[0], p3[1], p3[2], p3[3]);
+                const uint32_t off = tc::sw128(c, 8 * j);
+                *reinterpret_cast<uint4 *>(sm + L::XT + 0 * L::XT_TILE + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+                *reinterpret_cast<uint4 *>(sm + L::XT + 1 * L::XT_TILE + off) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+                *reinterpret_cast<uint4 *>(sm + L::XT + 2 * L::XT_TILE + off) = make_uint4(p3[0], p3[1], p3[2], p3[3]);
             }
             tc::fence_proxy_async();   // generic-proxy writes of the tiles -> visible to the MMAs
         }
@@ -226,18 +219,15 @@ __global__ void __launch_bounds__(NTC, 1) wy_fwd_tc(WyArgs a, int items)
         __syncthreads();
         tc::fence_after();
         if (live && tid == 0) {
-            const uint32_t at = tc::smem_u32(sm + L::AB + b * ((L::A_TILE + 1023) / 1024) * 1024);
+            const uint32_t at = tc::smem_u32(sm + L::AB + b * L::A_STRIDE);
             constexpr uint32_t idesc = idesc_bf16_f32(128, BT);
 #pragma unroll
-            for (int cb = 0; cb < NBLK; ++cb)
+            for (int term = 0; term < 3; ++term)
 #pragma unroll
-                for (int term = 0; term < 3; ++term)
-#pragma unroll
-                    for (int ks = 0; ks < BT / 16; ++ks) {
-                        const uint32_t xa = tc::smem_u32(sm + L::XT + (term * NBLK + cb) * L::XT_TILE) + 32 * ks;
-                        tc::mma_ss(tmem + cb * BT, tc::sdesc_sw128(xa), tc::sdesc_sw128(at + 32 * ks), idesc,
-                                   (term | ks) ? 1u : 0u);
-                    }
+                for (int ks = 0; ks < BT / 16; ++ks) {
+                    const uint32_t xa = tc::smem_u32(sm + L::XT + term * L::XT_TILE) + 32 * ks;
+                    tc::mma_ss(tmem, tc::sdesc_sw128(xa), tc::sdesc_sw128(at + 32 * ks), idesc, (term | ks) ? 1u : 0u);
+                }
             tc::mma_commit(bar);
         }
         if (live && !tc::bar_wait(bar, n & 1)) {   // bounded: 1 s
@@ -257,14 +247,17 @@ __global__ void __launch_bounds__(NTC, 1) wy_fwd_tc(WyArgs a, int items)
             F[(b ^ 1) * 2 * BT + tid] = nfk;
             F[(b ^ 1) * 2 * BT + BT + tid] = nfv;
         }
-        // ---- epilogue: warp group g = warp / 4 takes 32-column chunks (block, t range) g, g + 2, ...
+        // ---- epilogue: lane = column of the block; warp group g = warp / 4 takes the 32-row chunks g, g + 2,
+        //      ...; a warp stores 32 consecutive columns of one row per instruction
         if (live && !abort_flag) {
-            constexpr int TL = BT < 32 ? BT : 32, NT = BT / TL, TASKS = NBLK * NT;
+            constexpr int TL = BT < 32 ? BT : 32, NT = BT / TL;
             Tout *w = static_cast<Tout *>(a.w), *u = static_cast<Tout *>(a.u);
-            for (int task = warp >> 2; task < TASKS; task += 2) {
-                const int cb = task / NT, t0 = (task - cb * NT) * TL;
-                const int c = cb * 128 + 32 * (warp & 3) + lane;
-                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(cb * BT + t0);
+            const int c = cb * 128 + 32 * (warp & 3) + lane;
+            Tout *dst = c < K ? w + (size_t)hv * K + c : u + (size_t)hv * V + (c - K);
+            const size_t rstride = (size_t)HV * (c < K ? K : V);
+            for (int task = warp >> 2; task < NT; task += 2) {
+                const int t0 = task * TL;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)t0;
                 uint32_t r[32];
                 if constexpr (TL == 32) {
                     tc::tmem_ld32(taddr, r);
@@ -278,17 +271,9 @@ __global__ void __launch_bounds__(NTC, 1) wy_fwd_tc(WyArgs a, int items)
                         r[i] = r16[i];
                 }
 #pragma unroll
-                for (int i = 0; i < TL; ++i) {
-                    const int t = t0 + i;
-                    if (t < m) {
-                        const size_t row = (size_t)(bos + t);
-                        const float x = __uint_as_float(r[i]);
-                        if (c < K)
-                            w[(row * HV + hv) * K + c] = to_out_tc<Tout>(x);
-                        else
-                            u[(row * HV + hv) * V + (c - K)] = to_out_tc<Tout>(x);
-                    }
-                }
+                for (int i = 0; i < TL; ++i)
+                    if (t0 + i < m)
+                        dst[(size_t)(bos + t0 + i) * rstride] = to_out_tc<Tout>(__uint_as_float(r[i]));
             }
         }
         tc::fence_before();
@@ -321,8 +306,8 @@ cudaError_t launch_tc_t(const WyArgs &a, int J, cudaStream_t s)
         ready.fetch_or(bit, std::memory_order_release);
     }
     const int sms = sm_count[dev & 63];
-    const int items = J * a.HV;
-    const int grid = items < sms ? items : sms;
+    const int items = J * a.HV * L::NBLK;
+    const int grid = items < 2 * sms ? items : 2 * sms;   // two CTAs per SM
     f<<<grid, NTC, bytes, s>>>(a, items);
     return cudaGetLastError();
 }
