@@ -261,6 +261,15 @@ def ttt_linear_fwd(q, k, v, w, b, eta, scale=None, eps=1e-6, chunk=16, initial_s
     return o, ht, hbt
 
 
+def wy_into(k, v, beta, A, g, w, u, cu_seqlens, N, B, T, H, HV, K, V, chunk, dtype, workspace, stream=None) -> int:
+    """Raw call of gla_wy_fwd: tensors (or None) are passed as device pointers, sizes as given.  Returns the
+    code."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return int(_lib.gla_wy_fwd(_ptr(k), _ptr(v), _ptr(beta), _ptr(A), _ptr(g), _ptr(w), _ptr(u), _ptr(cu_seqlens),
+                               int(N), int(B), int(T), int(H), int(HV), int(K), int(V), int(chunk), int(dtype),
+                               _ptr(workspace), nbytes, _stream_handle(stream)))
+
+
 def wy_fwd(k, v, beta, A, g=None, cu_seqlens=None, out_dtype=None, stream=None, workspace=None):
     """WY representation forward of the gated delta rule on the GPU: per chunk of BT = A.shape[-1] rows,
     u = A (v * beta) and w = A (k * beta * 2^g).  k: [B, T, H, K]; v: [B, T, HV, V]; beta: [B, T, HV];
