@@ -11,12 +11,12 @@
 // is formed on chip: X is scaled in fp32 and split into three bf16 terms x = x1 + x2 + x3 (8 significand
 // bits each, exact to fp32 rounding), each written transposed into its own swizzled tile; the three MMA
 // groups accumulate into the same TMEM columns.  A work item is one 128-column block of one (chunk, value
-// head), so that two CTAs fit on an SM and one's conversion overlaps the other's MMAs and stores.  A and the
-// raw k | v columns of the next item arrive by 16-byte asynchronous copies while the current item is
-// converted, multiplied and stored; the epilogue reads D^T from TMEM (lane = column of w or u) and each warp
+// head), so that three CTAs (74 KB each) fit on an SM and one's conversion overlaps the others' MMAs and
+// stores.  A and the raw k | v columns of the next item arrive by 16-byte asynchronous copies while the
+// current item is stored; the epilogue reads D^T from TMEM (lane = column of w or u) and each warp
 // stores 32 consecutive columns of a row per instruction.
 //
-// Persistent: two CTAs per SM walk the items blockIdx.x, blockIdx.x + gridDim.x, ...  Rows past the end of a
+// Persistent: three CTAs per SM walk the items blockIdx.x, blockIdx.x + gridDim.x, ...  Rows past the end of a
 // sequence: X^T is zero there (so A's columns for them contribute nothing) and their outputs are not stored.
 #include <atomic>
 
@@ -37,10 +37,10 @@ struct WyTcSmem {
     static constexpr int A_TILE = BT * 128;                    // bytes: BT rows (t) x 64 s slots
     static constexpr int A_STRIDE = (A_TILE + 1023) / 1024 * 1024;
     static constexpr int XT = 0;                               // [3 terms] X^T tiles of the block (1024-aligned)
-    static constexpr int AB = XT + 3 * XT_TILE;                // [2] A tiles (B operand)
-    static constexpr int RAW = AB + 2 * A_STRIDE;              // [2][BT][128] raw columns of the block (bf16)
-    static constexpr int F = RAW + 2 * BT * 128 * 2;           // [2][2][BT] row factors (k part, v part)
-    static constexpr int BAR = F + 2 * 2 * BT * 4;             // mbarrier (MMA done)
+    static constexpr int AB = XT + 3 * XT_TILE;                // A tile (B operand)
+    static constexpr int RAW = AB + A_STRIDE;                  // [BT][128] raw columns of the block (bf16)
+    static constexpr int F = RAW + BT * 128 * 2;               // [2][BT] row factors (k part, v part)
+    static constexpr int BAR = F + 2 * BT * 4;                 // mbarrier (MMA done)
     static constexpr int TSLOT = BAR + 8;                      // TMEM base address
     static constexpr int BYTES = TSLOT + 8;
     static constexpr int TCOLS = BT <= 32 ? 32 : 64;
@@ -103,7 +103,7 @@ __device__ __forceinline__ bool wy_item(const WyArgs &a, int it, int BT, int nbl
 }
 
 template <typename Tout, int BT, int K, int V>
-__global__ void __launch_bounds__(NTC, 2) wy_fwd_tc(WyArgs a, int items)
+__global__ void __launch_bounds__(NTC, 3) wy_fwd_tc(WyArgs a, int items)
 {
     constexpr int KV = K + V;
     using L = WyTcSmem<BT, KV>;
@@ -133,17 +133,17 @@ __global__ void __launch_bounds__(NTC, 2) wy_fwd_tc(WyArgs a, int items)
 
     // ---- asynchronous copies of item `it` into buffer `b`: A's valid rows into the swizzled B tile, the
     //      k | v rows into the raw buffer (one commit group per item, even when it has no rows)
-    auto copy_item = [&](int it, int b) {
+    auto copy_item = [&](int it) {
         int cb, hv, bos, m;
         if (it < items && wy_item(a, it, BT, NBLK, cb, hv, bos, m)) {
             const int hk = hv / (HV / a.H);
-            unsigned char *at = sm + L::AB + b * L::A_STRIDE;
+            unsigned char *at = sm + L::AB;
             for (int e = tid; e < BT * CPR; e += NTC) {
                 const int t = e / CPR, c = e - t * CPR;
                 if (t < m)
                     cp_async16(at + tc::sw128(t, 8 * c), A + ((size_t)(bos + t) * HV + hv) * BT + 8 * c);
             }
-            __nv_bfloat16 *raw = reinterpret_cast<__nv_bfloat16 *>(sm + L::RAW) + b * BT * 128;
+            __nv_bfloat16 *raw = reinterpret_cast<__nv_bfloat16 *>(sm + L::RAW);
             for (int e = tid; e < BT * 16; e += NTC) {   // 16 copies of 8 columns per row of the block
                 const int s = e >> 4, cg = cb * 128 + 8 * (e & 15);
                 if (s < m) {
@@ -167,8 +167,7 @@ __global__ void __launch_bounds__(NTC, 2) wy_fwd_tc(WyArgs a, int items)
     };
 
     const int first = blockIdx.x, step = gridDim.x;
-    copy_item(first, 0);
-    copy_item(first + step, 1);
+    copy_item(first);
     float fk, fv;
     load_factors(first, fk, fv);
     if (tid < BT) {
@@ -178,17 +177,16 @@ __global__ void __launch_bounds__(NTC, 2) wy_fwd_tc(WyArgs a, int items)
     volatile int abort_flag = 0;
     int n = 0;
     for (int it = first; it < items; it += step, ++n) {
-        const int b = n & 1;
         float nfk, nfv;
         load_factors(it + step, nfk, nfv);   // the next item's factors, used after this item
-        cp_wait<1>();                        // this item's copies (the next item's may still fly)
+        cp_wait<0>();                        // this item's copies
         __syncthreads();
         int cb, hv, bos, m;
         const bool live = wy_item(a, it, BT, NBLK, cb, hv, bos, m);
         if (live) {
             // ---- X^T terms: task (column c, s-group j of 8 rows); lanes take consecutive columns
-            const __nv_bfloat16 *raw = reinterpret_cast<const __nv_bfloat16 *>(sm + L::RAW) + b * BT * 128;
-            const float *Fb = F + b * 2 * BT;
+            const __nv_bfloat16 *raw = reinterpret_cast<const __nv_bfloat16 *>(sm + L::RAW);
+            const float *Fb = F;
             for (int e = tid; e < 128 * CPR; e += NTC) {
                 const int j = e >> 7, c = e & 127;
                 const float *fr = Fb + (cb * 128 + c < K ? 0 : BT);
@@ -219,7 +217,7 @@ __global__ void __launch_bounds__(NTC, 2) wy_fwd_tc(WyArgs a, int items)
         __syncthreads();
         tc::fence_after();
         if (live && tid == 0) {
-            const uint32_t at = tc::smem_u32(sm + L::AB + b * L::A_STRIDE);
+            const uint32_t at = tc::smem_u32(sm + L::AB);
             constexpr uint32_t idesc = idesc_bf16_f32(128, BT);
 #pragma unroll
             for (int term = 0; term < 3; ++term)
@@ -240,12 +238,13 @@ __global__ void __launch_bounds__(NTC, 2) wy_fwd_tc(WyArgs a, int items)
         if (!live && !tc::bar_wait(bar, n & 1))
             abort_flag = 1;
         tc::fence_after();
-        // the MMAs no longer read buffer b: refill it with the item after next
+        // the MMAs no longer read the A tile and the conversion is done with the raw rows: fetch the next
+        // item while this one is stored (and the SM's other CTAs work)
         __syncthreads();
-        copy_item(it + 2 * step, b);
-        if (tid < BT) {   // factors of the next item go to the other buffer
-            F[(b ^ 1) * 2 * BT + tid] = nfk;
-            F[(b ^ 1) * 2 * BT + BT + tid] = nfv;
+        copy_item(it + step);
+        if (tid < BT) {   // factors of the next item
+            F[tid] = nfk;
+            F[BT + tid] = nfv;
         }
         // ---- epilogue: lane = column of the block; warp group g = warp / 4 takes the 32-row chunks g, g + 2,
         //      ...; a warp stores 32 consecutive columns of one row per instruction
@@ -307,7 +306,7 @@ cudaError_t launch_tc_t(const WyArgs &a, int J, cudaStream_t s)
     }
     const int sms = sm_count[dev & 63];
     const int items = J * a.HV * L::NBLK;
-    const int grid = items < 2 * sms ? items : 2 * sms;   // two CTAs per SM
+    const int grid = items < 3 * sms ? items : 3 * sms;   // three CTAs per SM
     f<<<grid, NTC, bytes, s>>>(a, items);
     return cudaGetLastError();
 }
