@@ -152,45 +152,37 @@ __global__ void __launch_bounds__(NTB) bwd_scan(BwdArgs a)
     }
     const size_t st = ((size_t)n * H + h) * K * V + e;
     const size_t hs = (size_t)H * K * V;                               // slot stride of dS / dR
-    float *dS = a.dS + ((size_t)first * H + h) * K * V + e;
-    float *dR = a.dR + ((size_t)first * H + h) * K * V + e;
-    const float *gl = a.gl + ((size_t)first * H + h) * K + kk;
+    float *__restrict__ dS = a.dS + ((size_t)first * H + h) * K * V + e;
+    float *__restrict__ dR = a.dR + ((size_t)first * H + h) * K * V + e;
+    const float *__restrict__ gl = a.gl + ((size_t)first * H + h) * K + kk;
     const size_t gs = (size_t)H * K;
-    // batches of D chunks: the D loads are issued before the in-place stores of the batch, so they overlap
-    constexpr int D = 8;
+    // The forward scan (chunk-start states, in place of dS, oldest first) and the backward scan (chunk-end
+    // adjoints, in place of dR, newest first) run in the same loop, in batches of D chunks whose loads are
+    // all issued before the batch's in-place stores, so both directions' loads overlap.
+    constexpr int D = 16;
     float S = a.h0 ? a.h0[st] : 0.f;
+    float R = a.dht ? a.dht[st] : 0.f;
     for (int c0 = 0; c0 < cnt; c0 += D) {
-        float t[D], e2[D];
+        const int c1 = cnt - 1 - c0;   // the backward scan's first chunk of this batch
+        float ts[D], es[D], tr[D], er[D];
 #pragma unroll
         for (int u = 0; u < D; ++u)
             if (c0 + u < cnt) {
-                t[u] = dS[(size_t)(c0 + u) * hs];
-                e2[u] = gl[(size_t)(c0 + u) * gs];
+                ts[u] = dS[(size_t)(c0 + u) * hs];
+                es[u] = gl[(size_t)(c0 + u) * gs];
+                tr[u] = dR[(size_t)(c1 - u) * hs];
+                er[u] = gl[(size_t)(c1 - u) * gs];
             }
 #pragma unroll
         for (int u = 0; u < D; ++u)
             if (c0 + u < cnt) {
                 dS[(size_t)(c0 + u) * hs] = S;
-                S = fmaf(expf(e2[u]), S, t[u]);
+                S = fmaf(expf(es[u]), S, ts[u]);
+                dR[(size_t)(c1 - u) * hs] = R;
+                R = fmaf(expf(er[u]), R, tr[u]);
             }
     }
     a.ht[st] = S;
-    float R = a.dht ? a.dht[st] : 0.f;
-    for (int c1 = cnt - 1; c1 >= 0; c1 -= D) {
-        float t[D], e2[D];
-#pragma unroll
-        for (int u = 0; u < D; ++u)
-            if (c1 - u >= 0) {
-                t[u] = dR[(size_t)(c1 - u) * hs];
-                e2[u] = gl[(size_t)(c1 - u) * gs];
-            }
-#pragma unroll
-        for (int u = 0; u < D; ++u)
-            if (c1 - u >= 0) {
-                dR[(size_t)(c1 - u) * hs] = R;
-                R = fmaf(expf(e2[u]), R, t[u]);
-            }
-    }
     if (a.dh0)
         a.dh0[st] = R;
 }

@@ -41,7 +41,8 @@ struct TttLayout {
     static constexpr int KG = D / 16;               // rows of h per thread
     static constexpr int DP = D + 4;                // padded row of the q / k tiles
     static constexpr int RA = BT / CL;              // rows of A each CTA computes
-    static constexpr int KSTR = BT * NCOL + 16;     // reduction buffer: one kind (k h or q h) of one warp
+    static constexpr int KSTR = 16 * NCOL + 16;     // reduction buffer: one kind (k h or q h) of one warp,
+                                                    // one 16-row block at a time
     static constexpr int MB = 0;                    // 4 mbarriers (X1, X2, X3, AX), 8 floats
     static constexpr int QB = 8;                    // [2][BT][DP] q (scaled)
     static constexpr int KB = QB + 2 * BT * DP;     // [2][BT][DP] k
@@ -298,10 +299,14 @@ __global__ void __launch_bounds__(NTT, 2) ttt_linear_fwd(TttArgs a)
             for (int dst = sl; dst < CL; dst += SL)
                 push(AX + par * BT * BT + ia * BT + j, BA, dst, s);
         }
-        // ---- partial k h and q h over this thread's KG rows of h (the pair in one packed fma); the two
-        //      lanes of a column pair split the kinds, the 8 warps are summed in shared memory
+        // ---- per 16-row block: partial k h and q h over this thread's KG rows of h (the pair in one packed
+        //      fma); the two lanes of a column pair split the kinds, the 8 warps are summed in shared memory;
+        //      then rows (thread (i, c)): k h + hb, q h + hb and the local LayerNorm statistics of k h + hb
+        float kh[NR], ro[NR];
 #pragma unroll
         for (int rb = 0; rb < NR; ++rb) {
+            if (rb > 0)
+                __syncthreads();   // every thread has read the previous block's partial sums
             float2 acc[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -322,24 +327,18 @@ __global__ void __launch_bounds__(NTT, 2) ttt_linear_fwd(TttArgs a)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const float keep = lo ? acc[i].x : acc[i].y, send = lo ? acc[i].y : acc[i].x;
-                RED[(2 * warp + (lane >> 4)) * L::KSTR + (rb * 16 + i) * NCOL + c] =
-                    keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                RED[(2 * warp + (lane >> 4)) * L::KSTR + i * NCOL + c] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
             }
-        }
-        __syncthreads();
-        // ---- rows (thread (i, c)): k h + hb and q h + hb; local LayerNorm statistics of k h + hb
-        float kh[NR], ro[NR];
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            const int i = (tid >> 4) + 16 * r;
+            __syncthreads();
+            const int il = tid >> 4, i = il + 16 * rb;
             float sk = hb, sq = hb;
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
-                sk += RED[(2 * w) * L::KSTR + i * NCOL + c];
-                sq += RED[(2 * w + 1) * L::KSTR + i * NCOL + c];
+                sk += RED[(2 * w) * L::KSTR + il * NCOL + c];
+                sq += RED[(2 * w + 1) * L::KSTR + il * NCOL + c];
             }
-            kh[r] = sk;
-            ro[r] = sq;
+            kh[rb] = sk;
+            ro[rb] = sq;
             const float ml = hsum(sk) * (1.f / NCOL), d = sk - ml, m2 = hsum(d * d);
             if (c < CL)
                 push2(X1 + 2 * ((int)rank * BT + i), B1, c, ml, m2);
