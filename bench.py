@@ -353,7 +353,7 @@ def bwd_kernel_flops(name, inp):
     nc = bwd_chunks(inp) * H
     if name == "bwd_grads":
         return 2 * nc * (C * C * (3 * K + 2 * V) + 3 * C * K * V)
-    if name == "bwd_chunk_sums":
+    if name in ("bwd_chunk_sums", "bwd_chunk_sums_tc"):
         return 2 * nc * 2 * C * K * V
     if name == "bwd_scan":
         return 2 * 2 * nc * K * V

@@ -175,7 +175,7 @@ thread_local Profile g_prof;
 enum KernelId {
     K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_FUSED_TC = 7,
     K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11, K_TTT = 12, K_WY = 13,
-    K_WY_TC = 14
+    K_WY_TC = 14, K_BWD_SUMS_TC = 15
 };
 
 // Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
@@ -424,6 +424,7 @@ extern "C" const char *gla_kernel_name(int kernel_id)
     case K_TTT: return "ttt_linear_fwd";
     case K_WY: return "wy_fwd_ffma";
     case K_WY_TC: return "wy_fwd_tc";
+    case K_BWD_SUMS_TC: return "bwd_chunk_sums_tc";
     default: return "unknown";
     }
 }
@@ -590,7 +591,11 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
             return GLA_ERR_CUDA;
     }
     const int J = bp.J;
-    if (J > 0 && profiled(K_BWD_SUMS, s, [&] { return launch_bwd_sums(a, J, dtype, s); }) != cudaSuccess)
+    // bf16 q, k, v, dout with K = 128: chunk sums on the tensor cores; everything else on CUDA cores
+    const bool sums_tc = bwd_sums_tc_supported(dtype, K, V);
+    if (J > 0 && profiled(sums_tc ? K_BWD_SUMS_TC : K_BWD_SUMS, s, [&] {
+            return sums_tc ? launch_bwd_sums_tc(a, J, dtype, s) : launch_bwd_sums(a, J, dtype, s);
+        }) != cudaSuccess)
         return GLA_ERR_CUDA;
     if (profiled(K_BWD_SCAN, s, [&] { return launch_bwd_scan(a, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;

@@ -150,6 +150,8 @@ cudaError_t launch_wy_fwd_tc(const WyArgs &a, int J, int dtype, cudaStream_t s);
 
 bool bwd_supported(int dtype, int K, int V);
 cudaError_t launch_bwd_sums(const BwdArgs &a, int J, int dtype, cudaStream_t s);
+bool bwd_sums_tc_supported(int dtype, int K, int V);
+cudaError_t launch_bwd_sums_tc(const BwdArgs &a, int J, int dtype, cudaStream_t s);
 cudaError_t launch_bwd_scan(const BwdArgs &a, cudaStream_t s);
 cudaError_t launch_bwd_grads(const BwdArgs &a, int J, int dtype, cudaStream_t s);
 cudaError_t launch_bwd_dg(const BwdArgs &a, int J, cudaStream_t s);
