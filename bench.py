@@ -38,7 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {"out_ffma": "csrc/ffma_kernels.cu", "state_ffma": "csrc/ffma_kernels.cu",
                   "scan_segments": "csrc/ffma_kernels.cu", "plan_varlen": "csrc/ffma_kernels.cu",
                   "fused_tc": "csrc/tc_fused.cu", "ttt_linear_fwd": "csrc/ttt_ffma.cu",
-                  "wy_fwd_ffma": "csrc/wy_ffma.cu", "wy_fwd_tc": "csrc/wy_tc.cu"}
+                  "wy_fwd_ffma": "csrc/wy_ffma.cu", "wy_fwd_tc": "csrc/wy_tc.cu",
+                  "bwd_chunk_sums_tc": "csrc/bwd_tc.cu"}
 
 
 def parse_args(argv=None):
