@@ -165,8 +165,11 @@ int gla_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, 
  * q, k, v, g, scale, h0, cu_seqlens, N, B, T, H, chunk: as for gla_fwd (the forward is recomputed; pass the
  * same h0 the forward used, or NULL for a zero initial state).  dout [rows, H, V] in the input dtype (the
  * gradient of o); dht [N, H, K, V] fp32 or NULL (no loss on the final state).  dtype GLA_F32 (every input
- * fp32) or GLA_BF16 (q, k, v, g, dout bf16); all arithmetic is fp32 on CUDA cores.  K and V in {64, 128};
- * chunk 16, 32, 64 or 128 (tiled at 64 rows, as for gla_fwd).  workspace: at least gla_bwd_workspace_size() bytes, 256-byte aligned, zeroed before its first
+ * fp32), GLA_BF16 (q, k, v, g, dout bf16), GLA_F16, GLA_BF16_GF32 or GLA_F16_GF32 (fp32 g), optionally OR-ed
+ * with GLA_HEAD_FIRST for dense batches.  Arithmetic is fp32: the per-chunk sums run on the tcgen05 tensor
+ * cores for bf16 inputs with K == 128 (fp32 operands split into three bf16 terms, fp32 accumulation), every
+ * other step on CUDA cores.  K and V in {64, 128}; chunk 16, 32, 64 or 128 (tiled at 64 rows, as for
+ * gla_fwd).  workspace: at least gla_bwd_workspace_size() bytes, 256-byte aligned, zeroed before its first
  * use (status word in its first bytes); it holds the chunk-start states and chunk-end adjoints
  * (2 * chunks * H * K * V fp32).  Outputs must not overlap any input, the workspace or one another.  The
  * library allocates nothing and is stream-ordered.  Errors as for gla_fwd (GLA_ERR_UNSUPPORTED for other
@@ -242,8 +245,10 @@ const char *gla_kernel_name(int kernel_id);
  *              use (status word, then the varlen chunk table)
  *
  * Rows past the end of a sequence do not exist: the columns of A that would refer to them are not read.
- * fp32 CUDA cores, one CTA per (chunk, value head).  Outputs must not overlap any input, the workspace or
- * each other.  Errors as for gla_fwd; returns GLA_OK once enqueued.
+ * bf16 inputs with K == V in {64, 128} run on the tcgen05 tensor cores (the fp32 operand k * beta * 2^g |
+ * v * beta split into three bf16 terms, A as it is stored, fp32 accumulation; a bounded wait inside reports
+ * GLA_ERR_TIMEOUT in the status word); everything else on fp32 CUDA cores.  Outputs must not overlap any
+ * input, the workspace or each other.  Errors as for gla_fwd; returns GLA_OK once enqueued.
  */
 int gla_wy_fwd(const void *k, const void *v, const void *beta, const void *A, const float *g, void *w, void *u,
                const int32_t *cu_seqlens, int N, int B, int T, int H, int HV, int K, int V, int chunk, int dtype,
