@@ -7,11 +7,13 @@
 // (bf16 operands, fp32 accumulation in TMEM): M = 128 keys, N = V, K = the chunk's 64 rows in steps of 16.
 // The A operands (k e^{G_l - G} and q e^{G}, fp32 on chip) are split into three bf16 terms x = x1 + x2 + x3
 // (exact to fp32 rounding) and written transposed into 128-byte-swizzled K-major tiles; the B operands
-// (v and do, bf16 already) are written transposed into one tile each.  Every input row of the chunk arrives
-// first by 16-byte asynchronous copies (q, k, v, do, g: one memory latency per CTA); a thread owns one key,
-// takes its cumsum from the staged gates and forms both gated operands.  dS is formed first; its tiles are
-// reused for dR once the first MMA group has completed.  Rows past the end of a chunk are zero in every
-// tile.  The epilogue reads TMEM (lane = key) and stores rows of dS and dR (fp32, [slot][H][K][V]).
+// (v and do, bf16 already) are written transposed into one tile each.  The rows of g, k and v arrive first by
+// 16-byte asynchronous copies (g inside the A-tile region until its cumsum is taken); a thread owns one key
+// and keeps its cumsum in registers for both gated operands.  dS is formed first; q and do are fetched into
+// the places of k and v while its MMAs run, and the tiles are reused for dR.  Rows past the end of a chunk are
+// zero in every tile.  The epilogue stages each result from TMEM (lane = key) in shared memory and writes
+// whole rows of dS and dR (fp32, [slot][H][K][V]) with lanes on consecutive columns.  About 97 KB per CTA:
+// two CTAs share an SM.
 #include <atomic>
 
 #include "gla_internal.h"
@@ -28,16 +30,17 @@ constexpr int NTS = 256;     // threads per CTA
 
 template <typename Tg, int V>
 struct SumsSmem {
-    static constexpr int AT = 0;                   // [3 terms] A^T tiles, 128 rows x 128 bytes each
+    static constexpr int AT = 0;                   // [3 terms] A^T tiles, 128 rows x 128 bytes each; the raw
+                                                   // gates [64][128] (Tg) live here until the cumsum is taken
     static constexpr int BT = AT + 3 * 16384;      // B^T tile, V rows x 128 bytes
-    static constexpr int RQ = BT + V * 128;        // raw rows of the chunk: q [64][128] bf16
-    static constexpr int RK = RQ + CT * KT * 2;    // k [64][128] bf16
-    static constexpr int RV = RK + CT * KT * 2;    // v [64][V] bf16
-    static constexpr int RD = RV + CT * V * 2;     // do [64][V] bf16
-    static constexpr int RG = RD + CT * V * 2;     // g [64][128] (Tg)
-    static constexpr int BAR = RG + CT * KT * (int)sizeof(Tg);
+    static constexpr int RK = BT + V * 128;        // raw rows [64][128] bf16: k, then q
+    static constexpr int RV = RK + CT * KT * 2;    // raw rows [64][V] bf16: v, then do
+    static constexpr int BAR = RV + CT * V * 2;
     static constexpr int TSLOT = BAR + 8;
     static constexpr int BYTES = TSLOT + 8;
+    static constexpr int SROW = V + 1;             // epilogue staging [128][V + 1] fp32 over AT .. RK
+    static_assert(KT * SROW * 4 <= RV, "staging fits below the raw v rows");
+    static_assert(CT * KT * (int)sizeof(Tg) <= BT, "raw gates fit in the A tiles");
 };
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src)
@@ -88,16 +91,15 @@ __device__ __forceinline__ void split3_store(unsigned char *tiles, int key, int 
 }
 
 template <typename Tg, int V>
-__global__ void __launch_bounds__(NTS, 1) bwd_chunk_sums_tc(BwdArgs a)
+__global__ void __launch_bounds__(NTS, 2) bwd_chunk_sums_tc(BwdArgs a)
 {
     using L = SumsSmem<Tg, V>;
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char *sm = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::TSLOT);
-    const __nv_bfloat16 *Rq = reinterpret_cast<const __nv_bfloat16 *>(sm + L::RQ);
     const __nv_bfloat16 *Rk = reinterpret_cast<const __nv_bfloat16 *>(sm + L::RK);
-    const Tg *Rg = reinterpret_cast<const Tg *>(sm + L::RG);
+    const Tg *Rg = reinterpret_cast<const Tg *>(sm + L::AT);
     const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int n, bos, eos;
     if (a.table) {
@@ -116,24 +118,20 @@ __global__ void __launch_bounds__(NTS, 1) bwd_chunk_sums_tc(BwdArgs a)
     const int len = eos - bos, H = a.H;
     const size_t rb = row_head(bos, h, H, a.T, a.hf);   // row t of the chunk: row-head index rb + t * rs
     const int rs = a.hf ? 1 : H;
-    // ---- every valid row of q, k, v, do, g by 16-byte asynchronous copies (one latency for all of them)
-    {
-        const char *srcs[5] = {static_cast<const char *>(a.q), static_cast<const char *>(a.k),
-                               static_cast<const char *>(a.v), static_cast<const char *>(a.dout),
-                               static_cast<const char *>(a.g)};
-        const int rowb[5] = {KT * 2, KT * 2, V * 2, V * 2, KT * (int)sizeof(Tg)};   // bytes per row
-        const int dsto[5] = {L::RQ, L::RK, L::RV, L::RD, L::RG};
-#pragma unroll
-        for (int x = 0; x < 5; ++x) {
-            const int per = rowb[x] / 16;
-            for (int e = tid; e < CT * per; e += NTS) {
-                const int t = e / per, c = e - t * per;
-                if (t < len)
-                    cp_async16(sm + dsto[x] + t * rowb[x] + 16 * c, srcs[x] + (rb + (size_t)t * rs) * rowb[x] + 16 * c);
-            }
+    // 16-byte asynchronous copies of the valid rows of a [rows, H, width] tensor into shared rows of rowb bytes
+    auto stage = [&](const void *src, int rowb, int dst) {
+        const int per = rowb / 16;
+        const char *s8 = static_cast<const char *>(src);
+        for (int e = tid; e < CT * per; e += NTS) {
+            const int t = e / per, c = e - t * per;
+            if (t < len)
+                cp_async16(sm + dst + t * rowb + 16 * c, s8 + (rb + (size_t)t * rs) * rowb + 16 * c);
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    }
+    };
+    stage(a.g, KT * (int)sizeof(Tg), L::AT);
+    stage(a.k, KT * 2, L::RK);
+    stage(a.v, V * 2, L::RV);
+    asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid == 0) {
         tc::bar_init(bar, 1);
         tc::bar_fence_init();
@@ -145,33 +143,38 @@ __global__ void __launch_bounds__(NTS, 1) bwd_chunk_sums_tc(BwdArgs a)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tslot;
-    // ---- thread: key = tid % 128, row groups jj = tid / 128 + 2 i (i < 4).  Cumsum of its key from the raw
-    //      gates (twice: the total first), then k e^{G_l - G} (three terms, to the A tiles) and q e^{G} (kept)
+    // ---- thread: key = tid % 128, row groups jj = tid / 128 + 2 i (i < 4); its cumsum from the staged gates
+    //      (the total first), kept in registers for both gated operands
     const int key = tid & 127, j0 = tid >> 7;
     float gl = 0.f;
     for (int t = 0; t < len; ++t)
         gl += wide<Tg>(Rg[t * KT + key]);
-    float xq[4][8];
+    float gv[4][8];
     {
         float run = 0.f;
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            float xk[8];
+        for (int jj = 0; jj < 8; ++jj)
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int t = 8 * jj + u;
-                const bool in = t < len;
-                run += in ? wide<Tg>(Rg[t * KT + key]) : 0.f;
-                if ((jj & 1) == j0) {
-                    xk[u] = in ? __bfloat162float(Rk[t * KT + key]) * expf(gl - run) : 0.f;
-                    xq[jj >> 1][u] = in ? __bfloat162float(Rq[t * KT + key]) * expf(run) : 0.f;
-                }
+                run += t < len ? wide<Tg>(Rg[t * KT + key]) : 0.f;
+                if ((jj & 1) == j0)
+                    gv[jj >> 1][u] = run;
             }
-            if ((jj & 1) == j0)
-                split3_store(sm + L::AT, key, jj, xk);
-        }
     }
-    // v^T: task (value column c, row group jj), from the raw rows
+    __syncthreads();   // the raw gates are read: the A tiles may be written
+    // ---- (k e^{G_l - G})^T in three terms, v^T in one
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int jj = j0 + 2 * i;
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int t = 8 * jj + u;
+            x[u] = t < len ? __bfloat162float(Rk[t * KT + key]) * expf(gl - gv[i][u]) : 0.f;
+        }
+        split3_store(sm + L::AT, key, jj, x);
+    }
     auto write_bt = [&](int roff) {
         const unsigned short *R = reinterpret_cast<const unsigned short *>(sm + roff);
         for (int e = tid; e < V * 8; e += NTS) {
@@ -205,13 +208,28 @@ __global__ void __launch_bounds__(NTS, 1) bwd_chunk_sums_tc(BwdArgs a)
     };
     if (tid == 0)
         issue(tmem);   // dS -> columns [0, V)
+    // the raw k and v rows are consumed: fetch q and do into their places while the MMAs run
+    stage(a.q, KT * 2, L::RK);
+    stage(a.dout, V * 2, L::RV);
+    asm volatile("cp.async.commit_group;" ::: "memory");
     bool ok = tc::bar_wait(bar, 0);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    tc::fence_before();
+    __syncthreads();   // q, do visible; the first MMA group no longer reads the tiles
     tc::fence_after();
-    // ---- the tiles are free again: (q e^{G})^T in three terms and do^T
+    // ---- (q e^{G})^T in three terms, do^T in one
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        split3_store(sm + L::AT, key, j0 + 2 * i, xq[i]);
-    write_bt(L::RD);
+    for (int i = 0; i < 4; ++i) {
+        const int jj = j0 + 2 * i;
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int t = 8 * jj + u;
+            x[u] = t < len ? __bfloat162float(Rk[t * KT + key]) * expf(gv[i][u]) : 0.f;
+        }
+        split3_store(sm + L::AT, key, jj, x);
+    }
+    write_bt(L::RV);
     tc::fence_proxy_async();
     tc::fence_before();
     __syncthreads();
@@ -220,26 +238,36 @@ __global__ void __launch_bounds__(NTS, 1) bwd_chunk_sums_tc(BwdArgs a)
         issue(tmem + V);   // dR (unscaled) -> columns [V, 2V)
     ok = tc::bar_wait(bar, 1) && ok;
     tc::fence_after();
+    __syncthreads();   // every warp past the wait before the tiles become staging
     if (!ok) {
         if (tid == 0)
             report(a.status, GLA_ERR_TIMEOUT);
     } else {
-        // ---- epilogue: warps 0-3 dS, warps 4-7 dR; lane = key, a row of V values per thread
+        // ---- epilogue, dS then dR: TMEM (lane = key) -> staging [key][V + 1] (warps 0-3 the first half of
+        //      the columns, warps 4-7 the second) -> whole rows of the workspace tile, lanes on columns
+        float *stg = reinterpret_cast<float *>(sm + L::AT);
         const int rkey = 32 * (warp & 3) + lane;
-        const bool isR = warp >= 4;
-        float *dst = (isR ? a.dR : a.dS) + (((size_t)j * H + h) * KT + rkey) * a.V;
-        const float mul = isR ? a.scale : 1.f;
-        const uint32_t base = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (isR ? V : 0);
+        float *const dsts[2] = {a.dS, a.dR};
 #pragma unroll
-        for (int cc = 0; cc < V / 32; ++cc) {
-            uint32_t r[32];
-            tc::tmem_ld32(base + 32 * cc, r);
-            tc::tmem_wait_ld(r);
+        for (int which = 0; which < 2; ++which) {
+            const float mul = which ? a.scale : 1.f;
 #pragma unroll
-            for (int w4 = 0; w4 < 8; ++w4)
-                *reinterpret_cast<float4 *>(dst + 32 * cc + 4 * w4) =
-                    make_float4(mul * __uint_as_float(r[4 * w4]), mul * __uint_as_float(r[4 * w4 + 1]),
-                                mul * __uint_as_float(r[4 * w4 + 2]), mul * __uint_as_float(r[4 * w4 + 3]));
+            for (int cc = 0; cc < V / 64; ++cc) {
+                const int c0 = (warp >> 2) * (V / 2) + 32 * cc;
+                uint32_t r[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(which * V + c0), r);
+                tc::tmem_wait_ld(r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    stg[rkey * L::SROW + c0 + i] = mul * __uint_as_float(r[i]);
+            }
+            __syncthreads();
+            float *dst = dsts[which] + ((size_t)j * H + h) * KT * V;
+            for (int e = tid; e < KT * V; e += NTS) {
+                const int kr = e / V, c = e - kr * V;
+                dst[e] = stg[kr * L::SROW + c];
+            }
+            __syncthreads();
         }
         if (tid < KT)
             a.gl[((size_t)j * H + h) * KT + tid] = gl;
