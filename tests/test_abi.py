@@ -174,3 +174,28 @@ def test_wy_rejects_before_any_cuda_work(gla):
     assert lib.gla_wy_workspace_size(100, 2, 48, 0) == 0
     assert lib.gla_wy_workspace_size(1000, 5, 64, 1) > lib.gla_wy_workspace_size(1000, 5, 64, 0)
     assert wy(gla, cu=80 * A, N=3, B=1, wsb=256) == gla.GLA_ERR_WORKSPACE   # varlen needs the chunk table
+
+
+def ttt(gla, q=A, k=2 * A, v=3 * A, w=4 * A, b=5 * A, eta=6 * A, scale=0.09, eps=1e-6, h0=None, hb0=None, o=8 * A,
+        ht=None, hbt=None, cu=None, N=2, B=2, T=100, H=2, D=64, chunk=16, dtype=1, ws=64 * A, wsb=1 << 20):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return gla.lib().gla_ttt_linear_fwd(p(q), p(k), p(v), p(w), p(b), p(eta), ctypes.c_float(scale),
+                                        ctypes.c_float(eps), p(h0), p(hb0), p(o), p(ht), p(hbt), p(cu), N, B, T, H, D,
+                                        chunk, dtype, p(ws), wsb, None)
+
+
+def test_ttt_rejects_before_any_cuda_work(gla):
+    assert ttt(gla, D=96) == gla.GLA_ERR_UNSUPPORTED
+    assert ttt(gla, chunk=64) == gla.GLA_ERR_UNSUPPORTED
+    assert ttt(gla, dtype=gla.GLA_BF16_GF32) == gla.GLA_ERR_UNSUPPORTED
+    assert ttt(gla, scale=0.0) == gla.GLA_ERR_INVALID_ARG
+    assert ttt(gla, eps=0.0) == gla.GLA_ERR_INVALID_ARG
+    assert ttt(gla, N=3) == gla.GLA_ERR_INVALID_ARG
+    assert ttt(gla, o=None) == gla.GLA_ERR_INVALID_ARG
+    assert ttt(gla, w=None) == gla.GLA_ERR_INVALID_ARG
+    assert ttt(gla, eta=6 * A + 4) == gla.GLA_ERR_ALIGNMENT
+    assert ttt(gla, ws=None) == gla.GLA_ERR_WORKSPACE
+    assert ttt(gla, wsb=16) == gla.GLA_ERR_WORKSPACE
+    assert ttt(gla, o=A + 64) == gla.GLA_ERR_INVALID_ARG                 # o overlaps q
+    assert ttt(gla, ht=20 * A, hbt=20 * A + 64) == gla.GLA_ERR_INVALID_ARG   # the two final states overlap
+    assert gla.lib().gla_ttt_workspace_size() >= 16
