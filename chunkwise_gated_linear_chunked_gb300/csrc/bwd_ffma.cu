@@ -511,16 +511,35 @@ __global__ void __launch_bounds__(NTB) bwd_dg_scan(BwdArgs a)
         cnt = a.NC;
     }
     float carry = 0.f;
-    if (a.dht) {
+    if (a.dht) {   // sum over v of ht * dht for this key: one contiguous row of V floats per thread
         const size_t st = (((size_t)n * H + h) * K + kk) * V;
-        for (int vv = 0; vv < V; ++vv)
-            carry = fmaf(a.ht[st + vv], a.dht[st + vv], carry);
+        const float4 *x4 = reinterpret_cast<const float4 *>(a.ht + st);
+        const float4 *y4 = reinterpret_cast<const float4 *>(a.dht + st);
+#pragma unroll 8
+        for (int i = 0; i < V / 4; ++i) {
+            const float4 x = x4[i], y = y4[i];
+            carry = fmaf(x.x, y.x, carry);
+            carry = fmaf(x.y, y.y, carry);
+            carry = fmaf(x.z, y.z, carry);
+            carry = fmaf(x.w, y.w, carry);
+        }
     }
-    for (int c = cnt - 1; c >= 0; --c) {
-        const size_t idx = ((size_t)(first + c) * H + h) * K + kk;
-        const float t = a.dgt[idx];
-        a.dgt[idx] = carry;
-        carry += t;
+    // reverse carry over the chunks, loads batched D chunks ahead of the in-place stores
+    float *__restrict__ dgt = a.dgt + ((size_t)first * H + h) * K + kk;
+    const size_t cs = (size_t)H * K;
+    constexpr int D = 16;
+    for (int c1 = cnt - 1; c1 >= 0; c1 -= D) {
+        float t[D];
+#pragma unroll
+        for (int u = 0; u < D; ++u)
+            if (c1 - u >= 0)
+                t[u] = dgt[(size_t)(c1 - u) * cs];
+#pragma unroll
+        for (int u = 0; u < D; ++u)
+            if (c1 - u >= 0) {
+                dgt[(size_t)(c1 - u) * cs] = carry;
+                carry += t[u];
+            }
     }
 }
 
@@ -532,9 +551,21 @@ __global__ void __launch_bounds__(128) bwd_dg_add(BwdArgs a)
         return;
     const float carry = a.dgt[((size_t)j * a.H + h) * a.K + kk];
     const size_t rb = row_head(bos, h, a.H, a.T, a.hf);
-    const int rs = a.hf ? 1 : a.H;
-    for (int t = 0; t < eos - bos; ++t)
-        a.dg[(rb + (size_t)t * rs) * a.K + kk] += carry;
+    const int rs = a.hf ? 1 : a.H, len = eos - bos;
+    float *__restrict__ dg = a.dg + rb * a.K + kk;
+    const size_t st = (size_t)rs * a.K;
+    constexpr int D = 8;   // rows per batch: all loads of a batch before its stores
+    for (int t0 = 0; t0 < len; t0 += D) {
+        float x[D];
+#pragma unroll
+        for (int u = 0; u < D; ++u)
+            if (t0 + u < len)
+                x[u] = dg[(size_t)(t0 + u) * st];
+#pragma unroll
+        for (int u = 0; u < D; ++u)
+            if (t0 + u < len)
+                dg[(size_t)(t0 + u) * st] = x[u] + carry;
+    }
 }
 
 template <typename F>
