@@ -39,7 +39,7 @@ KERNEL_SOURCES = {"out_ffma": "csrc/ffma_kernels.cu", "state_ffma": "csrc/ffma_k
                   "scan_segments": "csrc/ffma_kernels.cu", "plan_varlen": "csrc/ffma_kernels.cu",
                   "fused_tc": "csrc/tc_fused.cu", "ttt_linear_fwd": "csrc/ttt_ffma.cu",
                   "wy_fwd_ffma": "csrc/wy_ffma.cu", "wy_fwd_tc": "csrc/wy_tc.cu",
-                  "bwd_chunk_sums_tc": "csrc/bwd_tc.cu"}
+                  "bwd_chunk_sums_tc": "csrc/bwd_tc.cu", "bwd_grads": "csrc/bwd_ffma.cu"}
 
 
 def parse_args(argv=None):
@@ -463,7 +463,8 @@ def run_backward(args, w, inp, dev, dist, world, rank):
     roofline = {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2), "peak": round(peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                 "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
-                               f"{mhz:.0f} MHz", "traffic": None, "algorithmic_flops_per_launch": flops}
+                               f"{mhz:.0f} MHz", "traffic": traffic_for(dom, args.workload),
+                "algorithmic_flops_per_launch": flops}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         val, threads, desc = oracle_bwd_sample(inp, do_cpu, dht_cpu, args.cpu_seconds)
