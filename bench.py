@@ -2,7 +2,9 @@
 """Benchmark of the GLA forward on GB300: one JSON line per run (rank 0).
 
 A step is one gla_fwd over one batch of the workload (every kernel of the path), inputs resident in HBM.
-L2 is flushed (a write of a buffer twice the L2 size) before each timed step, outside the timed events.
+L2 is flushed (a write of a buffer twice the L2 size) before each timed step, outside the timed events; the
+steps are enqueued back to back, each between its own pair of CUDA events, and the host synchronises once
+after the last, so host launch latency stays outside the events.
 Per-kernel times come from CUDA events that libgla records around each of its launches on the call's
 stream (gla_profile_events).  ``e2e`` repeats the measurement through the same public call with the inputs
 copied host->device from pinned memory and o/ht copied back inside the timed region.
@@ -263,26 +265,11 @@ def main(argv=None):
     if binding.get_status(ws) != 0:
         raise RuntimeError("device status error during warm-up")
 
-    timer = binding.KernelTimer()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ms, per_kernel = [], {}
-    launches = 0
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
-        for _ in range(args.steps):
-            flush.zero_()
-            with timer:
-                start.record(stream)
-                step()
-                end.record(stream)
-            torch.cuda.synchronize()
-            step_ms.append(start.elapsed_time(end))
-            res = timer.results()
-            launches += len(res)
-            for name, ms in res:
-                per_kernel.setdefault(name, []).append(ms)
+        step_ms, per_kernel, launches = timed_steps(step, flush, stream, args.steps)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -424,25 +411,11 @@ def run_backward(args, w, inp, dev, dist, world, rank):
     torch.cuda.synchronize()
     if binding.get_status(ws) != 0:
         raise RuntimeError("device status error during warm-up")
-    timer = binding.KernelTimer()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ms, per_kernel, launches = [], {}, 0
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
-        for _ in range(args.steps):
-            flush.zero_()
-            with timer:
-                start.record(stream)
-                step()
-                end.record(stream)
-            torch.cuda.synchronize()
-            step_ms.append(start.elapsed_time(end))
-            res = timer.results()
-            launches += len(res)
-            for name, ms in res:
-                per_kernel.setdefault(name, []).append(ms)
+        step_ms, per_kernel, launches = timed_steps(step, flush, stream, args.steps)
     if dist is not None:
         dist.barrier()
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
@@ -539,25 +512,11 @@ def run_ttt(args, w, inp, dev, dist, world, rank):
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize()
-    timer = binding.KernelTimer()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ms, per_kernel, launches = [], {}, 0
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
-        for _ in range(args.steps):
-            flush.zero_()
-            with timer:
-                start.record(stream)
-                step()
-                end.record(stream)
-            torch.cuda.synchronize()
-            step_ms.append(start.elapsed_time(end))
-            res = timer.results()
-            launches += len(res)
-            for name, ms in res:
-                per_kernel.setdefault(name, []).append(ms)
+        step_ms, per_kernel, launches = timed_steps(step, flush, stream, args.steps)
     if dist is not None:
         dist.barrier()
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
@@ -681,25 +640,11 @@ def run_wy(args, w, dev, dist, world, rank):
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize()
-    timer = binding.KernelTimer()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ms, per_kernel, launches = [], {}, 0
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
-        for _ in range(args.steps):
-            flush.zero_()
-            with timer:
-                start.record(stream)
-                step()
-                end.record(stream)
-            torch.cuda.synchronize()
-            step_ms.append(start.elapsed_time(end))
-            res = timer.results()
-            launches += len(res)
-            for name, ms in res:
-                per_kernel.setdefault(name, []).append(ms)
+        step_ms, per_kernel, launches = timed_steps(step, flush, stream, args.steps)
     if dist is not None:
         dist.barrier()
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
@@ -766,6 +711,32 @@ def compute_dtype(inp):
     """Arithmetic type of the path: fp16 tensor-core operands (fp32 accumulation) for bf16 inputs with
     K == 128 and V a multiple of 128, fp32 CUDA-core arithmetic otherwise."""
     return "f16" if inp.dtype == "bf16" and inp.K == 128 and inp.V % 128 == 0 else "f32"
+
+
+def timed_steps(step, flush, stream, steps):
+    """Time `steps` calls of step() on the device.  Every step is preceded by an L2 flush (outside its
+    events) and bracketed by its own pair of CUDA events and its own per-kernel event set on the launching
+    stream; the steps are enqueued back to back and the host synchronises once at the end, so host launch
+    latency does not sit inside a step's events.  Returns (per-step ms, {kernel: [ms per launch]}, launches)."""
+    import torch
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    timers = [binding.KernelTimer() for _ in range(steps)]
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for timer, (start, end) in zip(timers, events):
+        flush.zero_()
+        with timer:
+            start.record(stream)
+            step()
+            end.record(stream)
+    torch.cuda.synchronize()
+    step_ms, per_kernel, launches = [], {}, 0
+    for timer, (start, end) in zip(timers, events):
+        step_ms.append(start.elapsed_time(end))
+        res = timer.results()
+        launches += len(res)
+        for name, ms in res:
+            per_kernel.setdefault(name, []).append(ms)
+    return step_ms, per_kernel, launches
 
 
 def max_over_ranks(total_ms, dist=None, device=None):
