@@ -2,7 +2,8 @@
 
 Tolerance: relative L2 <= 1e-4 for o, ht and hbt.  The inner model is updated by a serial fp32 recurrence over
 T / chunk mini-batches, each accumulating over D terms and one LayerNorm, so rounding grows with the number of
-steps; the test lengths (<= 520 rows, <= 33 steps) stay well inside that bound.
+steps; the shape cases (<= 520 rows, <= 33 steps) and the benchmark's full workload (2048 rows, 128 steps per
+head) stay inside that bound.
 """
 import zlib
 
@@ -77,3 +78,24 @@ def test_ttt_bad_offsets_are_reported_not_faulted():
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     binding.ttt_linear_fwd(q.cuda(), k.cuda(), v.cuda(), w.cuda(), b.cuda(), eta.cuda(), cu_seqlens=cu, workspace=ws)
     assert binding.get_status(ws) == binding.GLA_ERR_INVALID_ARG
+
+
+def test_ttt_full_size_b4_t2k_h8():
+    """The benchmark's TTT-linear workload (bf16 q, k, v of B=4, T=2048, H=8, D=128; mini-batch 16: 128 serial
+    gradient steps per head) in the bench's launch, whole tensors against the oracle."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    from chunkwise_gated_linear_chunked_gb300.inputs import WORKLOADS, workload_inputs
+    inp = workload_inputs("b4_t2k_h8")
+    gen = torch.Generator().manual_seed(WORKLOADS["b4_t2k_h8"].seed + 11)   # the bench's draw
+    w = 1.0 + 0.2 * torch.randn(inp.H, inp.K, generator=gen)
+    b = 0.1 * torch.randn(inp.H, inp.K, generator=gen)
+    eta = 0.02 + 0.05 * torch.rand(tuple(inp.q.shape[:3]), generator=gen)
+    scale = inp.K ** -0.5
+    o, ht, hbt = binding.ttt_linear_fwd(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), w.cuda(), b.cuda(), eta.cuda(),
+                                        scale=scale, eps=1e-6, chunk=16)
+    torch.cuda.synchronize()
+    ref = oracle.ttt_linear_fwd(*(stored_numpy(x) for x in (inp.q, inp.k, inp.v)), w.numpy(), b.numpy(),
+                                eta.numpy(), scale, 1e-6, 16)
+    for name, x, y in zip(("o", "ht", "hbt"), (o, ht, hbt), ref):
+        rel, mabs = errors(as_f64(x), y)
+        assert rel <= TOL, f"{name}: rel-L2 {rel:.3e} (max-abs {mabs:.3e})"
