@@ -94,25 +94,26 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
         whole = C;
     long long L = whole;
     if (pl.tc && rows > 0) {
-        // Fused tensor-core kernel (one persistent CTA per SM).  A segment that is not the last of its
-        // sequence is read twice (state pass, then output pass): keep its k, g and v (768 bytes per row of
-        // one 128-wide value tile) in about half of L2 across all SMs.  Dense batches are split only when
-        // the (sequence, head, value tile) items alone leave SMs idle; then into the fewest segments that
-        // fill the GPU in one wave, or the L2-sized segments if those are more.
+        // Fused tensor-core kernel (one persistent CTA per SM; a segment that is not the last of its sequence
+        // runs a state pass first and publishes its contribution for the segment scan).  Measured on GB300:
+        //  * dense batches whose (sequence, head, value tile) items already fill the GPU are not split (a
+        //    state pass costs more than the wave it would balance);
+        //  * otherwise the fewest segments that fill one wave: every item runs at once, so the segment scan
+        //    waits only for the state passes, never for a claimed but unstarted predecessor;
+        //  * varlen packs are cut into segments of at most kSegRows rows, which keeps the longest sequences
+        //    from setting the kernel's length while the scan's serial chain stays short.
         const long long sms = sm_count();
         const long long nv = pl.NV;
-        long long Ll2 = (l2_bytes() / 2) / (sms * 768) / C * C;
-        if (Ll2 < 4 * C)
-            Ll2 = 4 * C;
         if (varlen) {
-            L = std::min(Ll2, whole);
+            L = std::min<long long>(kSegRows, whole);
         } else {
             const long long units1 = (long long)B * H * nv;
-            const long long pmin = (T + Ll2 - 1) / Ll2;
             long long P = 1;
             if (units1 < sms)
-                P = units1 * pmin >= sms ? pmin : std::max(pmin, sms / units1);
+                P = std::max(1LL, sms / units1);
             L = ((T + P - 1) / P + C - 1) / C * C;
+            if (L < 4 * C)
+                L = 4 * C;
             if (L > whole)
                 L = whole;
         }

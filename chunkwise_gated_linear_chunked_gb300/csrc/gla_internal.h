@@ -10,7 +10,7 @@
 namespace gla {
 
 constexpr int kChunk = 64;          // chunk length C (rows per intra-chunk tile)
-constexpr int kMaxSegments = 24;    // most segments one sequence is split into
+constexpr int kSegRows = 2048;      // varlen packs: most rows of one segment on the tensor-core path
 
 // One forward call's launch plan.  Segments of L rows (L a multiple of the chunk) split each sequence
 // so that long sequences with few heads still fill the GPU; a "slot" is one (sequence, segment) pair and

@@ -40,6 +40,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major SW128 operand: the MN index is contiguous inside 128-byte
+// rows (64 16-bit elements, one swizzle atom wide), consecutive K indices are consecutive rows, 8-row K groups
+// are 1024 bytes apart (stride byte offset) and 64-element MN blocks are `mn_stride` bytes apart (leading
+// byte offset).  This is the layout a 128-byte-swizzled TMA box of [rows][64 elements] lands in, so a tile
+// whose rows are the K index (time) can feed the MMA without a transpose.  Advancing K by 16 = adding 2048.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_stride)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+    d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFF) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::f16 with fp16 A/B and fp32 accumulation, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
 {
@@ -48,6 +64,9 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N)
            | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
+// Operand-major bits of the instruction descriptor: A (bit 15) or B (bit 16) given MN-major.
+constexpr uint32_t kIdescAMajorMN = 1u << 15;
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
 
 // ---------------------------------------------------------------------------------------------------
 // tcgen05

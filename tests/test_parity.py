@@ -59,10 +59,12 @@ def test_small_cases_elementwise(case):
     assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
 
 
-# Start-state scan of the tensor-core path.  On a 152-SM GB300 with 126 MB of L2 the planner cuts these into
-# 512-row segments: 9 segments x 16 heads = 144 items fit in one wave, so segments are grouped in blocks of 8
-# and segment 9 starts from the end state published by segment 8; 8 segments x 40 heads = 320 items take
-# several waves and use the plain serial chain.  Every head is compared with the oracle.
+# Start-state scan of the tensor-core path.  On a 152-SM GB300 the planner cuts dense batches whose
+# (sequence, head) items leave SMs idle into the fewest segments that fill one wave (16 heads of 4608 rows:
+# 9 segments of 512 rows; 40 heads of 4096 rows: 3 segments; one head of 40000 rows: 125 segments), so
+# segments are grouped in blocks of 8 and each block starts from the end state published by the block
+# before.  Varlen packs are cut into segments of at most 2048 rows; 20 sequences of 4000 rows with 8 heads
+# give 320 items, more than one wave, which use blocks of 2.  Every head is compared with the oracle.
 # A varlen pack of 40 sequences (lengths 0 .. 2099, including empty and single-row ones).
 MANY_LENGTHS = [(i * 677) % 2100 if i % 9 else (i // 9) % 3 for i in range(40)]
 SCAN_CASES = [
@@ -72,6 +74,7 @@ SCAN_CASES = [
     ("bf16", 1, 40000, 1, 128, 128, True, None),     # one head: ~125 segments in one wave, 15 block hops
     ("bf16", 1, 0, 2, 128, 128, True, MANY_LENGTHS),
     ("bf16", 1, 0, 1, 128, 256, False, MANY_LENGTHS),
+    ("bf16", 1, 0, 8, 128, 128, True, [4000] * 20),   # several waves of items: scan blocks of 2
 ]
 
 
