@@ -2,9 +2,12 @@
 """Benchmark of the GLA forward on GB300: one JSON line per run (rank 0).
 
 A step is one gla_fwd over one batch of the workload (every kernel of the path), inputs resident in HBM.
-L2 is flushed (a write of a buffer twice the L2 size) before each timed step, outside the timed events; the
-steps are enqueued back to back, each between its own pair of CUDA events, and the host synchronises once
-after the last, so host launch latency stays outside the events.
+The default workload is the long-context one (B=1, H=32, T=65536, K=V=128, bf16).  L2 is flushed (a write of
+a buffer twice the L2 size) before each timed step, outside the timed events; the steps are enqueued back to
+back, each between its own pair of CUDA events, and the host synchronises once after the last, so host launch
+latency stays outside the events.  ``value`` is the tokens of all timed steps over their summed time; the
+line also gives the median step and the median launch of each kernel (the roofline uses the latter), and a
+``warm`` figure from the same number of steps without the flush.
 Per-kernel times come from CUDA events that libgla records around each of its launches on the call's
 stream (gla_profile_events).  ``e2e`` repeats the measurement through the same public call with the inputs
 copied host->device from pinned memory and o/ht copied back inside the timed region.
@@ -34,7 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GLA fwd tokens/s on 1 GB300; % of BF16 tensor peak or HBM roofline"
-DEFAULT_WORKLOAD = "b4_t2k_h8"
+DEFAULT_WORKLOAD = "long_t64k_h32"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # kernel name -> source file that defines it (a traffic figure is only reused while that file is unchanged)
 KERNEL_SOURCES = {"out_ffma": "csrc/ffma_kernels.cu", "state_ffma": "csrc/ffma_kernels.cu",
@@ -47,11 +50,12 @@ KERNEL_SOURCES = {"out_ffma": "csrc/ffma_kernels.cu", "state_ffma": "csrc/ffma_k
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-warm", action="store_true", help="skip the warm-L2 figure")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "ttt", "wy"], default="fwd")
@@ -129,7 +133,7 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
@@ -200,6 +204,28 @@ def oracle_sample(inp, seconds, head_start=0):
     desc = (f"fp64 oracle over {groups} group(s) of {per_group} head(s) x all {inp.N} sequence(s) "
             f"({token_heads} token-heads, {el:.1f} s wall)")
     return token_heads / H / el, threads, desc
+
+
+def oracle_single_thread(inp, max_rows=16384):
+    """The fp64 oracle on one thread: the first sequence's first head, its first `max_rows` rows at most;
+    tokens/s in the workload's unit (a token is one row with all H heads, so one head-row counts 1/H)."""
+    import oracle
+    from chunkwise_gated_linear_chunked_gb300.inputs import stored_numpy
+    if inp.cu_seqlens is None:
+        rows = min(inp.q.shape[1], max_rows)
+        sel = lambda x: x[:1, :rows, :1].contiguous()
+        cu = None
+    else:
+        a0, a1 = int(inp.cu_seqlens[0]), int(inp.cu_seqlens[1])
+        rows = min(a1 - a0, max_rows)
+        sel = lambda x: x[:, a0:a0 + rows, :1].contiguous()
+        cu = None
+    args = [stored_numpy(sel(x)) for x in (inp.q, inp.k, inp.v, inp.g)]
+    h0 = None if inp.h0 is None else inp.h0[:1, :1].contiguous().numpy()
+    t0 = time.perf_counter()
+    oracle.gla_fwd(*args, inp.scale, h0=h0, cu_seqlens=cu, nthreads=1)
+    el = time.perf_counter() - t0
+    return rows / inp.H / el, f"fp64 oracle, 1 thread, one head of the first sequence ({rows} rows, {el:.2f} s)"
 
 
 # ------------------------------------------------------------------------------------------------
@@ -281,11 +307,23 @@ def main(argv=None):
     value = whole_job_value(wu["tokens"], args.steps, world, total_ms)
     ms_per_step = total_ms / args.steps
 
-    # dominant kernel and its roofline
+    # the same steps without the L2 flush (inputs of the small workloads then partly stay in L2)
+    warm = None
+    if not args.no_warm:
+        wstep_ms, wper_kernel, _ = timed_steps(step, None, stream, args.steps)
+        torch.cuda.synchronize()
+        if binding.get_status(ws) != 0:
+            raise RuntimeError("device status error in the warm-L2 steps")
+        warm = {"ms_per_step_median": round(statistics.median(wstep_ms), 5),
+                "value": round(wu["tokens"] / (statistics.median(wstep_ms) / 1e3), 1),
+                "kernels_ms": {n: round(statistics.median(v), 5) for n, v in wper_kernel.items()},
+                "l2": "not flushed between steps"}
+
+    # dominant kernel and its roofline (median launch time)
     peaks, peak_src = load_peaks()
     kern_tot = {n: sum(v) for n, v in per_kernel.items()}
     dom = max(kern_tot, key=kern_tot.get)
-    dom_ms = statistics.mean(per_kernel[dom])
+    dom_ms = statistics.median(per_kernel[dom])
     dom_bytes = kernel_algorithmic_bytes(dom, wu)
     hbm = peak_hbm(peaks)
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
@@ -302,12 +340,16 @@ def main(argv=None):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         val, threads, desc = oracle_sample(inp, args.cpu_seconds)
-        cpu = {"value": round(val, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc}
+        v1, desc1 = oracle_single_thread(inp)
+        cpu = {"value": round(val, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "hardware_concurrency": os.cpu_count(),
+               "single_thread": {"value": round(v1, 1), "unit": "tokens/s", "sample": desc1}}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "ms_per_step_median": round(statistics.median(step_ms), 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": compute_dtype(inp), "data": "synthetic",
             "config": {"workload": args.workload, "desc": w.note, "B": B, "T": T, "H": H, "K": K, "V": V,
@@ -316,8 +358,8 @@ def main(argv=None):
                        "l2": "flushed before every timed step (zero-fill of a 2x L2 buffer, outside the events)",
                        "parallelism": "replicas" if world == 1 else f"weak x{world} (independent sequences)"},
             "roofline": roofline,
-            "kernels_ms": {n: round(statistics.mean(v), 5) for n, v in per_kernel.items()},
-            "cpu_baseline": cpu, "e2e": e2e,
+            "kernels_ms": {n: round(statistics.median(v), 5) for n, v in per_kernel.items()},
+            "warm": warm, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -426,7 +468,7 @@ def run_backward(args, w, inp, dev, dist, world, rank):
     ms_per_step = total_ms / args.steps
     kern_tot = {n: sum(x) for n, x in per_kernel.items()}
     dom = max(kern_tot, key=kern_tot.get)
-    dom_ms = statistics.mean(per_kernel[dom])
+    dom_ms = statistics.median(per_kernel[dom])
     props = torch.cuda.get_device_properties(dev)
     csum = clocks.summary()
     mhz = csum.get("sm_max_mhz") or 2070.0
@@ -454,7 +496,7 @@ def run_backward(args, w, inp, dev, dist, world, rank):
                        "l2": "flushed before every timed step (zero-fill of a 2x L2 buffer, outside the events)",
                        "parallelism": "replicas" if world == 1 else f"weak x{world} (independent sequences)"},
             "roofline": roofline,
-            "kernels_ms": {n: round(statistics.mean(x), 5) for n, x in per_kernel.items()},
+            "kernels_ms": {n: round(statistics.median(x), 5) for n, x in per_kernel.items()},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": csum,
         }
         print(json.dumps(line), flush=True)
@@ -525,7 +567,7 @@ def run_ttt(args, w, inp, dev, dist, world, rank):
     B, T = inp.q.shape[0], inp.q.shape[1]
     value = whole_job_value(B * T, args.steps, world, total_ms)
     dom = "ttt_linear_fwd"
-    dom_ms = statistics.mean(per_kernel[dom])
+    dom_ms = statistics.median(per_kernel[dom])
     props = torch.cuda.get_device_properties(dev)
     csum = clocks.summary()
     mhz = csum.get("sm_max_mhz") or 2070.0
@@ -568,7 +610,7 @@ def run_ttt(args, w, inp, dev, dist, world, rank):
                          "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
                                         f"{mhz:.0f} MHz", "traffic": traffic_for(dom, args.workload),
                          "algorithmic_flops_per_launch": flops},
-            "kernels_ms": {n: round(statistics.mean(x), 5) for n, x in per_kernel.items()},
+            "kernels_ms": {n: round(statistics.median(x), 5) for n, x in per_kernel.items()},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": csum,
         }
         print(json.dumps(line), flush=True)
@@ -651,8 +693,8 @@ def run_wy(args, w, dev, dist, world, rank):
     if binding.get_status(ws) != 0:
         raise RuntimeError("device status error in the timed region")
     value = whole_job_value(x.B * x.T, args.steps, world, total_ms)
-    dom = max((n_ for n_ in per_kernel if n_ != "plan_varlen"), key=lambda n_: statistics.mean(per_kernel[n_]))
-    dom_ms = statistics.mean(per_kernel[dom])
+    dom = max((n_ for n_ in per_kernel if n_ != "plan_varlen"), key=lambda n_: statistics.median(per_kernel[n_]))
+    dom_ms = statistics.median(per_kernel[dom])
     props = torch.cuda.get_device_properties(dev)
     csum = clocks.summary()
     mhz = csum.get("sm_max_mhz") or 2070.0
@@ -699,7 +741,7 @@ def run_wy(args, w, dev, dist, world, rank):
                        "l2": "flushed before every timed step (zero-fill of a 2x L2 buffer, outside the events)",
                        "parallelism": "replicas" if world == 1 else f"weak x{world} (independent sequences)"},
             "roofline": wy_roofline(dom, dom_ms, nbytes, flops, peak, hbm_peak, hbm_src, props, mhz, args.workload),
-            "kernels_ms": {n_: round(statistics.mean(t), 5) for n_, t in per_kernel.items()},
+            "kernels_ms": {n_: round(statistics.median(t), 5) for n_, t in per_kernel.items()},
             "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": csum,
         }
         print(json.dumps(line), flush=True)
@@ -723,7 +765,8 @@ def timed_steps(step, flush, stream, steps):
     timers = [binding.KernelTimer() for _ in range(steps)]
     events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for timer, (start, end) in zip(timers, events):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         with timer:
             start.record(stream)
             step()

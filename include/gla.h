@@ -142,13 +142,14 @@ int gla_chunk_local_cumsum(const void *g, float *G, const int32_t *cu_seqlens, i
  * Arguments, layouts, results and synchronous errors are those of gla_fwd.  The scratch comes from one
  * 32 MiB device array inside the library (held by every device that loads it, until exit); problems whose
  * gla_fwd_workspace_size() exceeds 32 MiB are rejected with GLA_ERR_WORKSPACE before anything is enqueued.
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  Nothing is allocated: no cudaMalloc,
- * cudaFree or allocating library routine is called (each call enqueues a 16-byte cudaMemsetAsync that
- * clears the status word, then the gla_fwd kernels).  All calls share the one array, so calls that may
- * overlap on the GPU (different streams without ordering) race and must not be made.  Device-side
- * conditions (bad cu_seqlens, GLA_ERR_RANGE, GLA_ERR_TIMEOUT) are recorded in the array and cleared by
- * the next call; they cannot be read back — callers that need them use gla_fwd with a workspace.
+ * The array's device address is looked up (cudaGetSymbolAddress) with the device current on the first call
+ * in each context, i.e. on the first call on a device and again after a device reset; make such a call
+ * before any stream capture.  Nothing is allocated: no cudaMalloc, cudaFree or allocating library routine
+ * is called, and the call enqueues only the gla_fwd kernels.  All calls share the one array, which keeps
+ * the previous call's contents, so calls that may overlap on the GPU (different streams without ordering)
+ * race on it and must not be made.  Device-side conditions (bad cu_seqlens, GLA_ERR_RANGE,
+ * GLA_ERR_TIMEOUT) go to a status word inside the array that cannot be read back; callers that need them
+ * use gla_fwd with a workspace.
  */
 int gla_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, void *o, float scale,
                     const float *h0, float *ht, const int32_t *cu_seqlens, int N, int B, int T, int H,
