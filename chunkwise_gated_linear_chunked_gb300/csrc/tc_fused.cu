@@ -630,18 +630,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 *abort_w = 1;
                 report(a.status, GLA_ERR_TIMEOUT);
             };
-            // O^T += V^T P^T of output chunk gb (stage s) once the P group has written P, then release the stage
-            auto finish_d = [&](int gb, int s) -> bool {
-                if (!bar_wait(p_ready, gb & 1, abort_w))
-                    return false;
-                fence_after();
+            // O^T += V^T P^T of the chunk in stage s (its P is in shared memory), then release the stage
+            auto issue_d = [&](int s) {
                 const uint32_t st = smem_u32(sm + s * STAGE);
                 for (int kk = 0; kk < C / 16; ++kk)
                     mma_ss(tmem + TM_O, sdesc_mn_sw128(st + ST_V + kk * 2048, kHalf), sdesc_sw128(pt + kk * 32),
                            ID_D, 1u);
                 mma_commit(mma2);
                 mma_commit(&empty[s]);
-                return true;
             };
             // state pass: dS accumulated from zero into the item's state buffer
             auto run_s = [&](const Item &it) -> bool {
@@ -667,10 +663,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 qbase += it.nA;
                 return true;
             };
-            // Output chunk gb.  Issue order: (c) first, so that the state group (which waits for it alone)
-            // can move on; then (d) of the previous chunk, whose P the P group has formed by now; then (b),
-            // which overwrites P; then (a) once the output group has read the previous O^T out of TMEM.
-            // Commits complete in issue order, so each commit also covers every earlier MMA.
+            // Output chunk gb needs four MMAs: (c) S += V^T k~ (needs the gating group's operands and the
+            // state group's S'), (b) the scores (operands only), (a) the inter-chunk product (S', and O^T free
+            // again), and later (d) O^T += V^T P^T (the P group's P).  They are issued as their inputs become
+            // ready, within the order the shared buffers impose: (d) of the previous chunk before (b) of this
+            // one (P in TMEM and in shared memory) and before (a) (both write O^T); (c) at any time.  Commits
+            // complete in issue order, so each also covers every earlier MMA: mma_st (after (c)) tells the
+            // state group that U and the previous chunk's S' buffer are ready, mma1 (after (b)) tells the P
+            // group that P and the shared P tile are, mma2 (after (d)) tells the output group that O^T is.
             auto run_o = [&](const Item &it) -> bool {
                 const uint32_t sb = tmem + TM_S + (it.itn & 1) * 128;
                 // Item itn - 2 (same state buffer) is finished before this item's commits: without this wait,
@@ -679,33 +679,71 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // at once in the steady state (that item's output pass completed two items ago).
                 if (it.itn >= 2 && !bar_wait(&tmem_free[it.itn & 1], ((it.itn - 2) >> 1) & 1, abort_w))
                     return false;
+                int pend = -1, pend_s = 0;   // output chunk whose (d) is still to be issued, and its stage
                 for (int c = 0; c < it.nchunks; ++c) {
                     const int s = (qbase + c) % NSTAGE, gb = nb + c;
                     const uint32_t st = smem_u32(sm + s * STAGE);
-                    if (!bar_wait(&prep[s], ((qbase + c) / NSTAGE) & 1, abort_w) ||
-                        !bar_wait(ops_ready, gb & 1, abort_w))
-                        return false;
-                    fence_after();
-                    for (int kk = 0; kk < C / 16; ++kk)
-                        mma_ss(sb, sdesc_mn_sw128(st + ST_V + kk * 2048, kHalf),
-                               sdesc_mn_sw128(st + ST_K0 + kk * 2048, kQK), ID_C, 1u);
-                    mma_commit(mma_st);
-                    if (c > 0 && !finish_d(gb - 1, (qbase + c - 1) % NSTAGE))
-                        return false;
-                    for (int kk = 0; kk < KD / 16; ++kk)
-                        mma_ss(tmem + TM_P, sdesc_sw128(st + (kk >> 2) * 16384 + ST_Q0 + (kk & 3) * 32),
-                               sdesc_sw128(st + (kk >> 2) * 16384 + ST_K0 + (kk & 3) * 32), ID_N64, kk > 0);
-                    mma_commit(mma1);
-                    if (gb >= 1 && !bar_wait(o_free, (gb - 1) & 1, abort_w))
-                        return false;
-                    fence_after();
-                    for (int kk = 0; kk < KD / 16; ++kk)
-                        mma_ts(tmem + TM_O, tmem + TM_SOP + (gb & 1) * 64 + kk * 8,
-                               sdesc_sw128(st + (kk >> 2) * 16384 + ST_Q0 + (kk & 3) * 32), ID_N64, kk > 0);
+                    bool have_ops = false, did_b = false, did_c = false, did_a = false;
+                    const unsigned long long t0 = global_ns();
+                    while (!(did_a && did_b && did_c)) {
+                        bool progress = false;
+                        if (pend >= 0 && bar_test(p_ready, pend & 1)) {
+                            fence_after();
+                            issue_d(pend_s);
+                            pend = -1;
+                            progress = true;
+                        }
+                        if (!have_ops && bar_test(&prep[s], ((qbase + c) / NSTAGE) & 1)) {
+                            fence_after();
+                            have_ops = true;
+                            progress = true;
+                        }
+                        if (have_ops && !did_b && pend < 0) {
+                            for (int kk = 0; kk < KD / 16; ++kk)
+                                mma_ss(tmem + TM_P, sdesc_sw128(st + (kk >> 2) * 16384 + ST_Q0 + (kk & 3) * 32),
+                                       sdesc_sw128(st + (kk >> 2) * 16384 + ST_K0 + (kk & 3) * 32), ID_N64, kk > 0);
+                            mma_commit(mma1);
+                            did_b = true;
+                            progress = true;
+                        }
+                        if (have_ops && !did_c && bar_test(ops_ready, gb & 1)) {
+                            fence_after();
+                            for (int kk = 0; kk < C / 16; ++kk)
+                                mma_ss(sb, sdesc_mn_sw128(st + ST_V + kk * 2048, kHalf),
+                                       sdesc_mn_sw128(st + ST_K0 + kk * 2048, kQK), ID_C, 1u);
+                            mma_commit(mma_st);
+                            did_c = true;
+                            progress = true;
+                        }
+                        if (did_c && !did_a && pend < 0 && (gb == 0 || bar_test(o_free, (gb - 1) & 1))) {
+                            fence_after();
+                            for (int kk = 0; kk < KD / 16; ++kk)
+                                mma_ts(tmem + TM_O, tmem + TM_SOP + (gb & 1) * 64 + kk * 8,
+                                       sdesc_sw128(st + (kk >> 2) * 16384 + ST_Q0 + (kk & 3) * 32), ID_N64,
+                                       kk > 0);
+                            did_a = true;
+                            progress = true;
+                        }
+                        if (!progress) {
+                            if (*abort_w)
+                                return false;
+                            if (global_ns() - t0 > kWaitNs) {
+                                *abort_w = 1;
+                                return false;
+                            }
+                            __nanosleep(20);
+                        }
+                    }
+                    pend = gb;
+                    pend_s = s;
                 }
                 // (d) of the item's last chunk
-                if (it.nchunks > 0 && !finish_d(nb + it.nchunks - 1, (qbase + it.nchunks - 1) % NSTAGE))
-                    return false;
+                if (pend >= 0) {
+                    if (!bar_wait(p_ready, pend & 1, abort_w))
+                        return false;
+                    fence_after();
+                    issue_d(pend_s);
+                }
                 mma_commit(&item_done[it.itn & 1]);
                 qbase += it.nchunks;
                 nb += it.nchunks;

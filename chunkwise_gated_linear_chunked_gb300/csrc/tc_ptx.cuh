@@ -238,6 +238,18 @@ __device__ __forceinline__ bool bar_try(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of phase `parity` of `bar` (no suspension).
+__device__ __forceinline__ bool bar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}\n"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ unsigned long long global_ns()
 {
     unsigned long long t;
