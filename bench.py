@@ -44,7 +44,8 @@ KERNEL_SOURCES = {"out_ffma": "csrc/ffma_kernels.cu", "state_ffma": "csrc/ffma_k
                   "scan_segments": "csrc/ffma_kernels.cu", "plan_varlen": "csrc/ffma_kernels.cu",
                   "fused_tc": "csrc/tc_fused.cu", "ttt_linear_fwd": "csrc/ttt_ffma.cu",
                   "wy_fwd_ffma": "csrc/wy_ffma.cu", "wy_fwd_tc": "csrc/wy_tc.cu",
-                  "bwd_chunk_sums_tc": "csrc/bwd_tc.cu", "bwd_grads": "csrc/bwd_ffma.cu"}
+                  "bwd_chunk_sums_tc": "csrc/bwd_tc.cu", "bwd_grads": "csrc/bwd_ffma.cu",
+                  "bwd_grads_tc": "csrc/bwd_grads_tc.cu"}
 
 
 def parse_args(argv=None):
@@ -381,12 +382,26 @@ def bwd_kernel_flops(name, inp):
     """Algorithmic flops of one launch of a backward kernel (2 per multiply-add, masked tiles counted)."""
     C, K, V, H = inp.chunk, inp.K, inp.V, inp.H
     nc = bwd_chunks(inp) * H
-    if name == "bwd_grads":
+    if name in ("bwd_grads", "bwd_grads_tc"):
         return 2 * nc * (C * C * (3 * K + 2 * V) + 3 * C * K * V)
     if name in ("bwd_chunk_sums", "bwd_chunk_sums_tc"):
         return 2 * nc * 2 * C * K * V
     if name == "bwd_scan":
         return 2 * 2 * nc * K * V
+    return 0
+
+
+def bwd_kernel_bytes(name, inp):
+    """Algorithmic HBM bytes of one launch of a tensor-core backward kernel: every input row read once, every
+    fp32 output row written once, the per-chunk [K][V] fp32 tiles it reads or writes moved once."""
+    K, V, H = inp.K, inp.V, inp.H
+    rows = inp.q.shape[0] * inp.q.shape[1] * H
+    nc = bwd_chunks(inp) * H
+    isz = 2 if inp.dtype in ("bf16", "f16") else 4
+    if name == "bwd_grads_tc":   # q, k, g, v, do in; S_c, R_c in; dq, dk, dg, dv out; chunk sums of dg out
+        return rows * (isz * (3 * K + 2 * V) + 4 * (3 * K + V)) + nc * (2 * K * V * 4 + K * 4)
+    if name == "bwd_chunk_sums_tc":   # q, k, g, v, do in; the two [K][V] contributions and G_l out
+        return rows * isz * (3 * K + 2 * V) + nc * (2 * K * V * 4 + K * 4)
     return 0
 
 
@@ -474,12 +489,22 @@ def run_backward(args, w, inp, dev, dist, world, rank):
     mhz = csum.get("sm_max_mhz") or 2070.0
     peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
     flops = bwd_kernel_flops(dom, inp)
-    achieved = flops / (dom_ms / 1e3) / 1e12
-    roofline = {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2), "peak": round(peak, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
-                               f"{mhz:.0f} MHz", "traffic": traffic_for(dom, args.workload),
-                "algorithmic_flops_per_launch": flops}
+    nbytes = bwd_kernel_bytes(dom, inp)
+    if nbytes:   # a tensor-core kernel: its fp32-accurate products are far from the tensor peak; HBM bounds it
+        peaks, src = load_peaks()
+        hbm = peak_hbm(peaks)
+        achieved = nbytes / (dom_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
+                    "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_source": f"{src} HBM copy",
+                    "traffic": traffic_for(dom, args.workload), "algorithmic_bytes_per_launch": nbytes,
+                    "algorithmic_flops_per_launch": flops}
+    else:
+        achieved = flops / (dom_ms / 1e3) / 1e12
+        roofline = {"bound": "alu", "kernel": dom, "achieved": round(achieved, 2), "peak": round(peak, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "peak_source": f"fp32 FMA: {props.multi_processor_count} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                                   f"{mhz:.0f} MHz", "traffic": traffic_for(dom, args.workload),
+                    "algorithmic_flops_per_launch": flops}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         val, threads, desc = oracle_bwd_sample(inp, do_cpu, dht_cpu, args.cpu_seconds)

@@ -176,7 +176,7 @@ thread_local Profile g_prof;
 enum KernelId {
     K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_FUSED_TC = 7,
     K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11, K_TTT = 12, K_WY = 13,
-    K_WY_TC = 14, K_BWD_SUMS_TC = 15
+    K_WY_TC = 14, K_BWD_SUMS_TC = 15, K_BWD_GRADS_TC = 16
 };
 
 // Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
@@ -426,6 +426,7 @@ extern "C" const char *gla_kernel_name(int kernel_id)
     case K_WY: return "wy_fwd_ffma";
     case K_WY_TC: return "wy_fwd_tc";
     case K_BWD_SUMS_TC: return "bwd_chunk_sums_tc";
+    case K_BWD_GRADS_TC: return "bwd_grads_tc";
     default: return "unknown";
     }
 }
@@ -600,7 +601,10 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
         return GLA_ERR_CUDA;
     if (profiled(K_BWD_SCAN, s, [&] { return launch_bwd_scan(a, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;
-    if (J > 0 && profiled(K_BWD_GRADS, s, [&] { return launch_bwd_grads(a, J, dtype, s); }) != cudaSuccess)
+    const bool grads_tc = bwd_grads_tc_supported(dtype, K, V);
+    if (J > 0 && profiled(grads_tc ? K_BWD_GRADS_TC : K_BWD_GRADS, s, [&] {
+            return grads_tc ? launch_bwd_grads_tc(a, J, s) : launch_bwd_grads(a, J, dtype, s);
+        }) != cudaSuccess)
         return GLA_ERR_CUDA;
     if (profiled(K_BWD_DG, s, [&] { return launch_bwd_dg(a, J, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;

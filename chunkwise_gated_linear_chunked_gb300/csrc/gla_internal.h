@@ -154,6 +154,8 @@ bool bwd_sums_tc_supported(int dtype, int K, int V);
 cudaError_t launch_bwd_sums_tc(const BwdArgs &a, int J, int dtype, cudaStream_t s);
 cudaError_t launch_bwd_scan(const BwdArgs &a, cudaStream_t s);
 cudaError_t launch_bwd_grads(const BwdArgs &a, int J, int dtype, cudaStream_t s);
+bool bwd_grads_tc_supported(int dtype, int K, int V);
+cudaError_t launch_bwd_grads_tc(const BwdArgs &a, int J, cudaStream_t s);
 cudaError_t launch_bwd_dg(const BwdArgs &a, int J, cudaStream_t s);
 cudaError_t launch_chunk_cumsum(const void *g, float *G, const int32_t *cu, int N, int B, int T, int H,
                                 int K, int chunk, int dtype, cudaStream_t s);

@@ -64,6 +64,9 @@ CASES = [
     ("f32", 2, 200, 2, 128, 128, True, True, None),       # ragged last chunk
     ("bf16", 2, 200, 3, 128, 128, True, True, None),
     ("bf16", 1, 1, 2, 64, 128, True, True, None),         # a single row
+    ("bf16", 1, 1, 2, 128, 128, True, True, None),        # a single row on the tensor-core path
+    ("bf16", 2, 320, 2, 128, 128, False, False, None),    # whole chunks, no initial state or dht
+    ("bf16", 1, 33, 1, 128, 128, True, False, None),      # one partial chunk past the anchor row
     ("bf16", 3, 130, 2, 128, 64, False, True, None),
     ("bf16", 1, 700, 2, 64, 64, True, False, None),
     ("bf16", 1, 0, 2, 128, 128, True, True, [1, 63, 64, 65, 0, 130, 300, 2]),   # varlen incl. empty
