@@ -9,17 +9,25 @@
 //   dv = AM^T do + k~ R'
 //   dg (chunk-local) = suffix sums over rows of q dq - k dk,  and the chunk total for the carry scan.
 //
-// One CTA (8 warps) per (chunk, head).  Every product is a tcgen05 kind::f16 MMA with bf16 operands and fp32
-// accumulation in TMEM, M = 128.  The three results are accumulated transposed (dq^T, dk^T with lane = key,
-// dv^T with lane = value column), so every accumulator fills all 128 lanes and the epilogue thread that owns a
-// key recomputes that key's cumsum and takes the dg suffix sums on its own.  Every operand is used in the
-// layout it is stored in (K-major or MN-major descriptors, 128-byte swizzle): nothing is transposed.  q, k,
-// v and do are exact in bf16; the computed operands (q~, k~, AM, BM, S', R') are split into three bf16 terms
-// x = x1 + x2 + x3 (exact to fp32 rounding): a product of two split operands takes the six term products
-// above the third order (x1 y1, x1 y2, x2 y1, x1 y3, x2 y2, x3 y1), a split operand times an exact one three,
-// so the result carries fp32-level error.  The state tiles S' and R' (three 32 KB terms each) are formed in
-// turn in the space of q~, AM and BM once the products that read those are complete.  Rows past the end of a
-// chunk are zero in every operand.  About 226 KB of shared memory: one CTA per SM.
+// Every product is a tcgen05 kind::f16 MMA with bf16 operands and fp32 accumulation in TMEM, M = 128.  The
+// three results are accumulated transposed (dq^T, dk^T with lane = key, dv^T with lane = value column), so
+// every accumulator fills all 128 lanes and the epilogue thread that owns a key takes that key's cumsum and the
+// dg suffix sums on its own.  Every operand is used in the layout it is stored in (K-major or MN-major
+// descriptors, 128-byte swizzle): nothing is transposed.  q, k, v and do are exact in bf16; the computed
+// operands (q~, k~, AM, BM, S', R') are split into three bf16 terms x = x1 + x2 + x3 (exact to fp32 rounding):
+// a product of two split operands takes the six term products above the third order (x1 y1, x1 y2, x2 y1,
+// x1 y3, x2 y2, x3 y1), a split operand times an exact one three, so the result carries fp32-level error.
+// Rows past the end of a chunk are zero in every operand.
+//
+// Persistent CTAs (one per SM, about 226 KB of shared memory) walk the (chunk, head) items.  Warps 0-7 form
+// the operands and issue the products (thread 0 issues); warps 8-11 are the epilogue, one thread per TMEM
+// lane.  The gating thread of a key and row half also leaves, in TMEM, that key's G - G_a on its rows and
+// the raw q and k there (packed), so the epilogue reads TMEM only and writes the gradients while the operand
+// warps go on to the next item's gating and score products.  The next item's q, k and g rows are copied in as
+// soon as the current gating has read its own, its v and do rows as soon as the current products are
+// complete.  The state tiles are read into registers while the products before them run: R' first (its
+// products are the longer phase, under which S_c is read), then S'.
+#include <algorithm>
 #include <atomic>
 
 #include <cuda_bf16.h>
@@ -31,9 +39,11 @@ namespace gla {
 
 namespace {
 
-constexpr int CT = kChunk;   // 64 rows per chunk
-constexpr int KD = 128;      // keys = value columns
-constexpr int NT = 256;      // threads per CTA
+constexpr int CT = kChunk;    // 64 rows per chunk
+constexpr int KD = 128;       // keys = value columns
+constexpr int NMAIN = 256;    // warps 0-7: operands and products
+constexpr int NEPI = 128;     // warps 8-11: epilogue
+constexpr int NT = NMAIN + NEPI;
 constexpr float L2E = 1.4426950408889634f;
 
 // shared memory (offsets from a 1024-byte aligned base); a [64 rows][128] bf16 tile is two 64-column halves of
@@ -42,18 +52,20 @@ constexpr int Q3 = 0;          // q~, three terms of 16 KB
 constexpr int AM3 = 49152;     // AM, three terms of 8 KB ([64 rows i][64 columns j]); the gating's partial sums
                                // live here before AM is formed
 constexpr int BM3 = 73728;     // BM, three terms of 8 KB
-constexpr int ST3 = 0;         // S', then R': three terms of 32 KB ([128 keys][128 v]) over Q3 .. BM3
+constexpr int ST3 = 0;         // R', then S': three terms of 32 KB ([128 keys][128 v]) over Q3 .. BM3
 constexpr int K3 = 98304;      // k~, three terms of 16 KB
 constexpr int DO = 147456;     // do [64 rows][128 v]
 constexpr int VV = 163840;     // v
 constexpr int RQ = 180224;     // raw rows, 256 bytes each: q
 constexpr int RK = 196608;     // k
 constexpr int RG = 212992;     // g
-constexpr int MISC = 229376;   // FA[128] = scale 2^(G_a), FR[128] = 2^(G_l - G_a); the dg partial totals in FA's
-                               // place in the epilogue
-constexpr int BAR = MISC + 1536;
-constexpr int SMEM_BYTES = BAR + 16 + 1024;
-constexpr uint32_t TM_AM = 0, TM_BM = 64, TM_DQ = 128, TM_DK = 192, TM_DV = 256, TM_COLS = 512;
+constexpr int MISC = 229376;   // FA[128] = scale 2^(G_a), FR[128] = 2^(G_l - G_a)
+constexpr int BAR = MISC + 1024;   // mma, acc_full, acc_empty, xq_full, xq_free, TMEM address, abort word
+constexpr int SMEM_BYTES = BAR + 64 + 1024;
+// TMEM columns (lane = key or value column): the score tiles (lanes 0..63 = rows), G - G_a in log2 units and
+// the packed raw q | k per row for the epilogue, the accumulators dq^T, dk^T, dv^T (column = row)
+constexpr uint32_t TM_AM = 0, TM_BM = 64, TM_X = 128, TM_QK = 192, TM_DQ = 256, TM_DK = 320, TM_DV = 384;
+constexpr uint32_t TM_COLS = 512;
 
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
 {
@@ -72,6 +84,21 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
                  "r"(src_bytes)
                  : "memory");
 }
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_all_but_newest() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// barrier 1 over the 256 threads of warps 0-7; the second form also ANDs a predicate over them
+__device__ __forceinline__ void main_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool main_and(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, 256, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v)
+                 : "memory");
+    return r != 0;
+}
 
 // Two fp32 values -> three bf16x2 words (x = x1 + x2 + x3 for each, exact to fp32 rounding).
 __device__ __forceinline__ void split3(float a, float b, uint32_t &w1, uint32_t &w2, uint32_t &w3)
@@ -87,9 +114,40 @@ __device__ __forceinline__ void split3(float a, float b, uint32_t &w1, uint32_t 
     w3 = *reinterpret_cast<const uint32_t *>(&x3);
 }
 
+// One fp32 value -> three bf16 terms stored at p, p + step, p + 2 step.
+__device__ __forceinline__ void split3_store(float x, unsigned char *p, int step)
+{
+    const __nv_bfloat16 x1 = __float2bfloat16_rn(x);
+    const float r = x - __bfloat162float(x1);
+    const __nv_bfloat16 x2 = __float2bfloat16_rn(r);
+    const __nv_bfloat16 x3 = __float2bfloat16_rn(r - __bfloat162float(x2));
+    *reinterpret_cast<__nv_bfloat16 *>(p) = x1;
+    *reinterpret_cast<__nv_bfloat16 *>(p + step) = x2;
+    *reinterpret_cast<__nv_bfloat16 *>(p + 2 * step) = x3;
+}
+
 __device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ float bf(const unsigned short *p) { return __uint_as_float(static_cast<uint32_t>(*p) << 16); }
+// 4x4 transpose inside each quad of lanes: on entry lane p holds a[i] = element (key p, row i) of its quad's
+// block, on exit a[i] = element (key i, row p), so that a lane can store four consecutive keys of one row.
+__device__ __forceinline__ void quad_transpose(float (&a)[4], int p)
+{
+#pragma unroll
+    for (int b = 1; b <= 2; b <<= 1) {
+        const bool hi = (p & b) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (i & b)
+                continue;
+            const float send = hi ? a[i] : a[i | b];
+            const float got = __shfl_xor_sync(0xffffffffu, send, b);
+            if (hi)
+                a[i] = got;
+            else
+                a[i | b] = got;
+        }
+    }
+}
 
 // K-major operand whose K index runs over two 64-element halves `hs` bytes apart: K step kk (16 elements)
 __device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, uint32_t hs)
@@ -102,321 +160,404 @@ __device__ __forceinline__ uint64_t mdesc(uint32_t base, int kk, uint32_t lbo)
     return tc::sdesc_mn_sw128(base + kk * 2048, lbo);
 }
 
-__global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a)
+// One (chunk, head) item: rows [bos, bos + len) of head h; row t of the chunk is row-head index rb + t * rs.
+struct Item {
+    int j, h, len;
+    size_t rb;
+};
+
+// The first used item at or after u on this CTA's stride (items u = j * H + h), or -1.
+__device__ __forceinline__ int next_item(const BwdArgs &a, int u, int nitems, Item &it)
+{
+    for (; u < nitems; u += gridDim.x) {
+        const int j = u / a.H, h = u - j * a.H;
+        int bos, eos;
+        if (a.table) {
+            const int4 e = a.table[j];
+            if (e.x < 0)
+                continue;
+            bos = e.z;
+            eos = e.w;
+        } else {
+            const int n = j / a.NC, c = j - n * a.NC;
+            bos = n * a.T + c * CT;
+            eos = min(bos + CT, n * a.T + a.T);
+        }
+        it.j = j;
+        it.h = h;
+        it.len = eos - bos;
+        it.rb = row_head(bos, h, a.H, a.T, a.hf);
+        return u;
+    }
+    return -1;
+}
+
+__global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
 {
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char *sm = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + BAR + 8);
+    uint64_t *bar_mma = reinterpret_cast<uint64_t *>(sm + BAR);
+    uint64_t *acc_full = bar_mma + 1, *acc_empty = bar_mma + 2, *xq_full = bar_mma + 3, *xq_free = bar_mma + 4;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + BAR + 40);
+    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + BAR + 44);
     float *FA = reinterpret_cast<float *>(sm + MISC), *FR = FA + 128;
-    const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int n, bos, eos;
-    if (a.table) {
-        const int4 e = a.table[j];
-        if (e.x < 0)
-            return;
-        n = e.x;
-        bos = e.z;
-        eos = e.w;
-    } else {
-        n = j / a.NC;
-        const int c = j - n * a.NC;
-        bos = n * a.T + c * CT;
-        eos = min(bos + CT, n * a.T + a.T);
-    }
-    (void)n;
-    const int len = eos - bos, H = a.H;
-    const size_t rb = row_head(bos, h, H, a.T, a.hf);   // row t of the chunk: row-head index rb + t * rs
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
     const int rs = a.hf ? 1 : H;
 
-    // ---- rows of the chunk by 16-byte asynchronous copies (rows past the end are zero-filled): q, k, g as
-    //      plain 256-byte rows; v and do straight into their swizzled operand tiles
-    {
-#pragma unroll
-        for (int which = 0; which < 5; ++which) {
-            const void *src = which == 0 ? a.q : which == 1 ? a.k : which == 2 ? a.g : which == 3 ? a.v : a.dout;
-            const int dst = which == 0 ? RQ : which == 1 ? RK : which == 2 ? RG : which == 3 ? VV : DO;
-            for (int r = tid; r < CT * 16; r += NT) {
-                const int t = r >> 4, c = r & 15;
-                const bool in = t < len;
-                const unsigned char *s =
-                    static_cast<const unsigned char *>(src) + ((rb + (size_t)(in ? t : 0) * rs) * KD + 8 * c) * 2;
-                const uint32_t off = which < 3 ? (uint32_t)(t * 256 + 16 * c)
-                                               : (uint32_t)((c >> 3) * 8192) + tc::sw128(t, 8 * (c & 7));
-                cp_async16(sm + dst + off, s, in ? 16u : 0u);
-            }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    }
     if (tid == 0) {
-        tc::bar_init(bar, 1);
+        tc::bar_init(bar_mma, 1);
+        tc::bar_init(acc_full, 1);
+        tc::bar_init(acc_empty, NEPI);
+        tc::bar_init(xq_full, NMAIN);
+        tc::bar_init(xq_free, NEPI);
+        *abort_w = 0;
         tc::bar_fence_init();
     }
     if (warp == 0)
         tc::tmem_alloc(tslot, TM_COLS);
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t sb = tc::smem_u32(sm);
 
-    // ---- gating: thread (key pair kp, row quarter rq); cumsum in log2 units, partial sums exchanged
-    {
-        const int kp = tid & 63, rq = tid >> 6, key = 2 * kp, kb = key >> 6, kc = key & 63;
-        float *psum = reinterpret_cast<float *>(sm + AM3);
-        uint32_t gr[16];
-        float s0 = 0.f, s1 = 0.f;
+    if (warp < 8) {
+        // ================================ operands and products ================================
+        // copies of an item's rows (rows past its end are zero-filled): q, k, g as plain 256-byte rows;
+        // v and do straight into their swizzled operand tiles
+        auto copy_rows = [&](const Item &it, bool raw) {
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int t = 16 * rq + u;
-            gr[u] = t < len ? *reinterpret_cast<const uint32_t *>(sm + RG + t * 256 + kp * 4) : 0u;
-            s0 = fmaf(lo16(gr[u]), L2E, s0);
-            s1 = fmaf(hi16(gr[u]), L2E, s1);
-        }
-        psum[rq * 128 + key] = s0;
-        psum[rq * 128 + key + 1] = s1;
-        __syncthreads();
-        float p0[4], p1[4];
+            for (int w = 0; w < 3; ++w) {
+                if (!raw && w == 2)
+                    break;
+                const int which = raw ? w : 3 + w;
+                const void *src = which == 0 ? a.q : which == 1 ? a.k : which == 2 ? a.g : which == 3 ? a.v : a.dout;
+                const int dst = which == 0 ? RQ : which == 1 ? RK : which == 2 ? RG : which == 3 ? VV : DO;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            p0[r] = psum[r * 128 + key];
-            p1[r] = psum[r * 128 + key + 1];
-        }
-        const float ga0 = p0[0] + p0[1], ga1 = p1[0] + p1[1];
-        const float gl0 = ga0 + p0[2] + p0[3], gl1 = ga1 + p1[2] + p1[3];
-        if (rq == 0) {
-            FA[key] = a.scale * tc::ex2(ga0);
-            FA[key + 1] = a.scale * tc::ex2(ga1);
-            FR[key] = tc::ex2(gl0 - ga0);
-            FR[key + 1] = tc::ex2(gl1 - ga1);
-        }
-        float X0 = (rq >= 1 ? p0[0] : 0.f) + (rq >= 2 ? p0[1] : 0.f) + (rq >= 3 ? p0[2] : 0.f) - ga0;
-        float X1 = (rq >= 1 ? p1[0] : 0.f) + (rq >= 2 ? p1[1] : 0.f) + (rq >= 3 ? p1[2] : 0.f) - ga1;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int t = 16 * rq + u;
-            X0 = fmaf(lo16(gr[u]), L2E, X0);
-            X1 = fmaf(hi16(gr[u]), L2E, X1);
-            const uint32_t qw = *reinterpret_cast<const uint32_t *>(sm + RQ + t * 256 + kp * 4);
-            const uint32_t kw = *reinterpret_cast<const uint32_t *>(sm + RK + t * 256 + kp * 4);
-            const bool in = t < len;
-            const float eq0 = tc::ex2(X0), eq1 = tc::ex2(X1), ek0 = tc::ex2(-X0), ek1 = tc::ex2(-X1);
-            const float q0 = in ? lo16(qw) * eq0 : 0.f, q1 = in ? hi16(qw) * eq1 : 0.f;
-            const float k0 = in ? lo16(kw) * ek0 : 0.f, k1 = in ? hi16(kw) * ek1 : 0.f;
-            const uint32_t off = (uint32_t)(kb * 8192) + tc::sw128(t, kc);
-            uint32_t w1, w2, w3;
-            split3(q0, q1, w1, w2, w3);
-            *reinterpret_cast<uint32_t *>(sm + Q3 + off) = w1;
-            *reinterpret_cast<uint32_t *>(sm + Q3 + 16384 + off) = w2;
-            *reinterpret_cast<uint32_t *>(sm + Q3 + 32768 + off) = w3;
-            split3(k0, k1, w1, w2, w3);
-            *reinterpret_cast<uint32_t *>(sm + K3 + off) = w1;
-            *reinterpret_cast<uint32_t *>(sm + K3 + 16384 + off) = w2;
-            *reinterpret_cast<uint32_t *>(sm + K3 + 32768 + off) = w3;
-        }
-    }
-    tc::fence_proxy_async();
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-
-    bool ok = true;
-    uint32_t phase = 0;
-    auto wait_mma = [&]() {
-        const bool got = tc::bar_wait(bar, phase & 1);
-        ++phase;
-        ok = __syncthreads_and(got && ok) != 0;
-        tc::fence_after();
-    };
-
-    // ---- AM = q~ k~^T (six term products), BM = do v^T
-    if (tid == 0) {
-        for (int p = 0; p < 6; ++p)
-            for (int kk = 0; kk < 8; ++kk)
-                tc::mma_ss(tmem + TM_AM, kdesc(sb + Q3 + PA[p] * 16384, kk, 8192),
-                           kdesc(sb + K3 + PB[p] * 16384, kk, 8192), ID, (p | kk) ? 1u : 0u);
-        for (int kk = 0; kk < 8; ++kk)
-            tc::mma_ss(tmem + TM_BM, kdesc(sb + DO, kk, 8192), kdesc(sb + VV, kk, 8192), ID, kk ? 1u : 0u);
-        tc::mma_commit(bar);
-    }
-    wait_mma();
-
-    // ---- AM, BM (TMEM lanes 0..63 = rows i, columns j) -> scale, inclusive causal mask, three bf16 terms in
-    //      their [i][j] tiles: warps 0, 1 take AM, warps 4, 5 BM
-    if (ok && (warp & 3) < 2 && (warp & 2) == 0) {
-        const int i = 32 * (warp & 1) + lane;
-        const bool isb = warp >= 4;
-        const uint32_t col = isb ? TM_BM : TM_AM;
-        const int dst = isb ? BM3 : AM3;
-        uint32_t r0[32], r1[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col, r0);
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col + 32, r1);
-        tc::tmem_wait_ld(r0);
-        tc::tmem_wait_ld(r1);
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-            uint32_t w1[4], w2[4], w3[4];
-#pragma unroll
-            for (int pr = 0; pr < 4; ++pr) {
-                const int jj = 8 * c8 + 2 * pr;
-                const uint32_t xa = c8 < 4 ? r0[jj & 31] : r1[jj & 31];
-                const uint32_t xb = c8 < 4 ? r0[(jj + 1) & 31] : r1[(jj + 1) & 31];
-                const float va = jj <= i ? a.scale * __uint_as_float(xa) : 0.f;
-                const float vb = jj + 1 <= i ? a.scale * __uint_as_float(xb) : 0.f;
-                split3(va, vb, w1[pr], w2[pr], w3[pr]);
+                for (int r = tid; r < CT * 16; r += NMAIN) {
+                    const int t = r >> 4, c = r & 15;
+                    const bool in = t < it.len;
+                    const unsigned char *s = static_cast<const unsigned char *>(src) +
+                                             ((it.rb + (size_t)(in ? t : 0) * rs) * KD + 8 * c) * 2;
+                    const uint32_t off = which < 3 ? (uint32_t)(t * 256 + 16 * c)
+                                                   : (uint32_t)((c >> 3) * 8192) + tc::sw128(t, 8 * (c & 7));
+                    cp_async16(sm + dst + off, s, in ? 16u : 0u);
+                }
             }
-            const uint32_t off = tc::sw128(i, 8 * c8);
-            *reinterpret_cast<uint4 *>(sm + dst + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-            *reinterpret_cast<uint4 *>(sm + dst + 8192 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-            *reinterpret_cast<uint4 *>(sm + dst + 16384 + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
-        }
-    }
-    tc::fence_proxy_async();
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
+        };
 
-    // ---- the products with the score tiles: dq^T = k~^T BM^T, dk^T = q~^T BM, dv^T = do^T AM
-    if (ok && tid == 0) {
-        for (int p = 0; p < 6; ++p)
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma_ss(tmem + TM_DQ, mdesc(sb + K3 + PA[p] * 16384, kk, 8192),
-                           kdesc(sb + BM3 + PB[p] * 8192, kk, 0), ID | tc::kIdescAMajorMN, (p | kk) ? 1u : 0u);
-        for (int p = 0; p < 6; ++p)
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma_ss(tmem + TM_DK, mdesc(sb + Q3 + PA[p] * 16384, kk, 8192),
-                           mdesc(sb + BM3 + PB[p] * 8192, kk, 8192), ID | tc::kIdescAMajorMN | tc::kIdescBMajorMN,
-                           (p | kk) ? 1u : 0u);
-        for (int t = 0; t < 3; ++t)
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma_ss(tmem + TM_DV, mdesc(sb + DO, kk, 8192), mdesc(sb + AM3 + t * 8192, kk, 8192),
-                           ID | tc::kIdescAMajorMN | tc::kIdescBMajorMN, (t | kk) ? 1u : 0u);
-        tc::mma_commit(bar);
-    }
-    if (ok)
-        wait_mma();
+        bool ok = true;
+        uint32_t mph = 0;   // completed waits on bar_mma
+        auto wait_mma = [&]() {
+            const bool got = tc::bar_wait(bar_mma, mph & 1, abort_w);
+            ++mph;
+            ok = main_and(got && ok);
+            tc::fence_after();
+        };
+        auto publish = [&]() {   // generic-proxy stores of all main threads -> visible to the next MMAs
+            tc::fence_proxy_async();
+            tc::fence_before();
+            main_sync();
+            tc::fence_after();
+        };
 
-    // ---- a state tile [128 keys][128 v] fp32 (this chunk's slot in the workspace) -> key-scaled, three bf16
-    //      terms over the q~ / AM / BM space (free now)
-    const size_t tile = ((size_t)j * H + h) * KD * KD;
-    auto split_state = [&](const float *src, const float *f) {
-        for (int e = tid; e < KD * 16; e += NT) {
-            const int key = e >> 4, c = e & 15;
-            const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(src + tile + (size_t)key * KD + 8 * c));
-            const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(src + tile + (size_t)key * KD + 8 * c + 4));
-            const float fk = f[key];
-            uint32_t w1[4], w2[4], w3[4];
-            split3(fk * x0.x, fk * x0.y, w1[0], w2[0], w3[0]);
-            split3(fk * x0.z, fk * x0.w, w1[1], w2[1], w3[1]);
-            split3(fk * x1.x, fk * x1.y, w1[2], w2[2], w3[2]);
-            split3(fk * x1.z, fk * x1.w, w1[3], w2[3], w3[3]);
-            const uint32_t off = (uint32_t)((c >> 3) * 16384) + tc::sw128(key, 8 * (c & 7));
-            *reinterpret_cast<uint4 *>(sm + ST3 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-            *reinterpret_cast<uint4 *>(sm + ST3 + 32768 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-            *reinterpret_cast<uint4 *>(sm + ST3 + 65536 + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
-        }
-        tc::fence_proxy_async();
-        tc::fence_before();
-        __syncthreads();
-        tc::fence_after();
-    };
-    if (ok) {
-        split_state(a.dS, FA);   // S' = scale 2^(G_a) S_c
-        if (tid == 0) {
-            for (int t = 0; t < 3; ++t)
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_ss(tmem + TM_DQ, kdesc(sb + ST3 + t * 32768, kk, 16384), kdesc(sb + DO, kk, 8192), ID, 1u);
-            tc::mma_commit(bar);
-        }
-        wait_mma();
-    }
-    if (ok) {
-        split_state(a.dR, FR);   // R' = 2^(G_l - G_a) R_c
-        if (tid == 0) {
-            for (int t = 0; t < 3; ++t)
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_ss(tmem + TM_DK, kdesc(sb + ST3 + t * 32768, kk, 16384), kdesc(sb + VV, kk, 8192), ID, 1u);
-            for (int p = 0; p < 6; ++p)
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_ss(tmem + TM_DV, mdesc(sb + ST3 + PA[p] * 32768, kk, 16384),
-                               kdesc(sb + K3 + PB[p] * 16384, kk, 8192), ID | tc::kIdescAMajorMN, 1u);
-            tc::mma_commit(bar);
-        }
-        wait_mma();
-    }
+        // the state tiles [128 keys][128 v] fp32 of an item (its slot in the workspace): into registers,
+        // then key-scaled and split into three bf16 terms over the q~ / AM / BM space
+        float4 st[16];
+        auto fetch_state = [&](const float *src, const Item &it) {
+            const size_t tile = ((size_t)it.j * H + it.h) * KD * KD;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const int e = tid + v * NMAIN, key = e >> 4, c = e & 15;
+                const float4 *p = reinterpret_cast<const float4 *>(src + tile + (size_t)key * KD + 8 * c);
+                st[2 * v] = __ldcg(p);
+                st[2 * v + 1] = __ldcg(p + 1);
+            }
+        };
+        auto split_state = [&](const float *f) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const int e = tid + v * NMAIN, key = e >> 4, c = e & 15;
+                const float fk = f[key];
+                const float4 x0 = st[2 * v], x1 = st[2 * v + 1];
+                uint32_t w1[4], w2[4], w3[4];
+                split3(fk * x0.x, fk * x0.y, w1[0], w2[0], w3[0]);
+                split3(fk * x0.z, fk * x0.w, w1[1], w2[1], w3[1]);
+                split3(fk * x1.x, fk * x1.y, w1[2], w2[2], w3[2]);
+                split3(fk * x1.z, fk * x1.w, w1[3], w2[3], w3[3]);
+                const uint32_t off = (uint32_t)((c >> 3) * 16384) + tc::sw128(key, 8 * (c & 7));
+                *reinterpret_cast<uint4 *>(sm + ST3 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                *reinterpret_cast<uint4 *>(sm + ST3 + 32768 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                *reinterpret_cast<uint4 *>(sm + ST3 + 65536 + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+            }
+            publish();
+        };
 
-    // ---- epilogue.  Warp w owns TMEM lanes 32 (w % 4) .. + 31 (keys for dq^T, dk^T; value columns for dv^T)
-    //      and rows 32 (w / 4) .. + 31 of the chunk.
-    if (ok) {
-        const int k = 32 * (warp & 3) + lane, half = warp >> 2, r0 = 32 * half;
+        Item cur, nxt;
+        int u = next_item(a, blockIdx.x, nitems, cur);
+        if (u >= 0)
+            copy_rows(cur, true);
+        cp_commit();
+        if (u >= 0)
+            copy_rows(cur, false);
+        cp_commit();
+        for (int nit = 0; u >= 0; ++nit) {
+            const int un = next_item(a, u + gridDim.x, nitems, nxt);
+            const int len = cur.len;
+            cp_wait_all_but_newest();   // this item's q, k, g
+            main_sync();
+
+            // ---- gating: thread (key k, row half rh); cumsum in log2 units, the halves' sums exchanged
+            const int gk = 32 * (warp & 3) + lane, rh = warp >> 2, gr0 = 32 * rh;
+            const uint32_t glane = (uint32_t)(32 * (warp & 3)) << 16;
+            uint32_t xw[32], qk[32];   // G - G_a (fp32 bits) and raw q | k of this key on the half's rows
+            {
+                const unsigned short *rgp = reinterpret_cast<const unsigned short *>(sm + RG);
+                const unsigned short *rqp = reinterpret_cast<const unsigned short *>(sm + RQ);
+                const unsigned short *rkp = reinterpret_cast<const unsigned short *>(sm + RK);
+                float *psum = reinterpret_cast<float *>(sm + AM3);
+                float gv[32], sum = 0.f;
+#pragma unroll
+                for (int v = 0; v < 32; ++v) {
+                    const int t = gr0 + v;
+                    gv[v] = t < len ? __uint_as_float(static_cast<uint32_t>(rgp[t * KD + gk]) << 16) * L2E : 0.f;
+                    sum += gv[v];
+                }
+                psum[rh * KD + gk] = sum;
+                main_sync();
+                const float ga = psum[gk], gl = ga + psum[KD + gk];
+                if (rh == 0) {
+                    FA[gk] = a.scale * tc::ex2(ga);
+                    FR[gk] = tc::ex2(gl - ga);
+                }
+                float G = rh ? ga : 0.f;
+                const int kb = gk >> 6, kc = gk & 63;
+#pragma unroll
+                for (int v = 0; v < 32; ++v) {
+                    const int t = gr0 + v;
+                    G += gv[v];
+                    const float X = G - ga;
+                    xw[v] = __float_as_uint(X);
+                    const bool in = t < len;
+                    const uint32_t qr = rqp[t * KD + gk], kr = rkp[t * KD + gk];
+                    qk[v] = in ? (qr << 16) | kr : 0u;
+                    const float qt = in ? __uint_as_float(qr << 16) * tc::ex2(X) : 0.f;
+                    const float kt = in ? __uint_as_float(kr << 16) * tc::ex2(-X) : 0.f;
+                    const uint32_t off = (uint32_t)(kb * 8192) + tc::sw128(t, kc);
+                    split3_store(qt, sm + Q3 + off, 16384);
+                    split3_store(kt, sm + K3 + off, 16384);
+                }
+            }
+            main_sync();   // the raw rows are read: the next item's q, k, g may come in
+            if (un >= 0)
+                copy_rows(nxt, true);
+            cp_commit();
+            // G - G_a and q | k to TMEM for the epilogue, once it has read the previous item's
+            if (nit == 0 || tc::bar_wait(xq_free, (nit - 1) & 1, abort_w)) {
+                tc::fence_after();
+                tc::tmem_st32(tmem + glane + TM_X + gr0, xw);
+                tc::tmem_st32(tmem + glane + TM_QK + gr0, qk);
+                tc::tmem_wait_st();
+            }
+            tc::fence_before();
+            tc::bar_arrive(xq_full);
+            cp_wait_all_but_newest();   // this item's v, do
+            publish();
+
+            // ---- AM = q~ k~^T (six term products), BM = do v^T
+            if (tid == 0) {
+                for (int p = 0; p < 6; ++p)
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ss(tmem + TM_AM, kdesc(sb + Q3 + PA[p] * 16384, kk, 8192),
+                                   kdesc(sb + K3 + PB[p] * 16384, kk, 8192), ID, (p | kk) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk)
+                    tc::mma_ss(tmem + TM_BM, kdesc(sb + DO, kk, 8192), kdesc(sb + VV, kk, 8192), ID, kk ? 1u : 0u);
+                tc::mma_commit(bar_mma);
+            }
+            wait_mma();
+            if (!ok)
+                break;
+
+            // ---- AM, BM (TMEM lanes 0..63 = rows i, columns j) -> scale, inclusive causal mask, three bf16
+            //      terms in their [i][j] tiles: warps 0, 1 take AM, warps 4, 5 BM
+            if ((warp & 2) == 0) {
+                const int i = 32 * (warp & 1) + lane;
+                const bool isb = warp >= 4;
+                const uint32_t col = isb ? TM_BM : TM_AM;
+                const int dst = isb ? BM3 : AM3;
+                uint32_t r0[32], r1[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col, r0);
+                tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + col + 32, r1);
+                tc::tmem_wait_ld(r0);
+                tc::tmem_wait_ld(r1);
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint32_t w1[4], w2[4], w3[4];
+#pragma unroll
+                    for (int pr = 0; pr < 4; ++pr) {
+                        const int jj = 8 * c8 + 2 * pr;
+                        const uint32_t xa = c8 < 4 ? r0[jj & 31] : r1[jj & 31];
+                        const uint32_t xb = c8 < 4 ? r0[(jj + 1) & 31] : r1[(jj + 1) & 31];
+                        const float va = jj <= i ? a.scale * __uint_as_float(xa) : 0.f;
+                        const float vb = jj + 1 <= i ? a.scale * __uint_as_float(xb) : 0.f;
+                        split3(va, vb, w1[pr], w2[pr], w3[pr]);
+                    }
+                    const uint32_t off = tc::sw128(i, 8 * c8);
+                    *reinterpret_cast<uint4 *>(sm + dst + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                    *reinterpret_cast<uint4 *>(sm + dst + 8192 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                    *reinterpret_cast<uint4 *>(sm + dst + 16384 + off) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+                }
+            }
+            publish();
+
+            // ---- the products with the score tiles, into the accumulators once the epilogue has drained the
+            //      previous item's: dq^T = k~^T BM^T, dk^T = q~^T BM, dv^T = do^T AM
+            const uint32_t acc = tmem;
+            if (tid == 0 && (nit == 0 || tc::bar_wait(acc_empty, (nit - 1) & 1, abort_w))) {
+                tc::fence_after();
+                for (int p = 0; p < 6; ++p)
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ss(acc + TM_DQ, mdesc(sb + K3 + PA[p] * 16384, kk, 8192),
+                                   kdesc(sb + BM3 + PB[p] * 8192, kk, 0), ID | tc::kIdescAMajorMN,
+                                   (p | kk) ? 1u : 0u);
+                for (int p = 0; p < 6; ++p)
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ss(acc + TM_DK, mdesc(sb + Q3 + PA[p] * 16384, kk, 8192),
+                                   mdesc(sb + BM3 + PB[p] * 8192, kk, 8192),
+                                   ID | tc::kIdescAMajorMN | tc::kIdescBMajorMN, (p | kk) ? 1u : 0u);
+                for (int t = 0; t < 3; ++t)
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ss(acc + TM_DV, mdesc(sb + DO, kk, 8192), mdesc(sb + AM3 + t * 8192, kk, 8192),
+                                   ID | tc::kIdescAMajorMN | tc::kIdescBMajorMN, (t | kk) ? 1u : 0u);
+                tc::mma_commit(bar_mma);
+            }
+            fetch_state(a.dR, cur);
+            wait_mma();
+            if (!ok)
+                break;
+
+            // ---- R' = 2^(G_l - G_a) R_c: dk^T += R' v^T, dv^T += R'^T k~^T
+            split_state(FR);
+            if (tid == 0) {
+                for (int t = 0; t < 3; ++t)
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ss(acc + TM_DK, kdesc(sb + ST3 + t * 32768, kk, 16384), kdesc(sb + VV, kk, 8192),
+                                   ID, 1u);
+                for (int p = 0; p < 6; ++p)
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ss(acc + TM_DV, mdesc(sb + ST3 + PA[p] * 32768, kk, 16384),
+                                   kdesc(sb + K3 + PB[p] * 16384, kk, 8192), ID | tc::kIdescAMajorMN, 1u);
+                tc::mma_commit(bar_mma);
+            }
+            fetch_state(a.dS, cur);
+            wait_mma();
+            if (!ok)
+                break;
+
+            // ---- S' = scale 2^(G_a) S_c: dq^T += S' do^T; the accumulator set goes to the epilogue
+            split_state(FA);
+            if (tid == 0) {
+                for (int t = 0; t < 3; ++t)
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc::mma_ss(acc + TM_DQ, kdesc(sb + ST3 + t * 32768, kk, 16384), kdesc(sb + DO, kk, 8192),
+                                   ID, 1u);
+                tc::mma_commit(bar_mma);
+                tc::mma_commit(acc_full);
+            }
+            wait_mma();   // every operand tile is free again
+            if (!ok)
+                break;
+            if (un >= 0)
+                copy_rows(nxt, false);
+            cp_commit();
+            cur = nxt;
+            u = un;
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+    } else {
+        // ================================ epilogue ================================
+        // Thread = TMEM lane k: key k of dq^T and dk^T, value column k of dv^T.  Rows 32..63 first, then
+        // 0..31, so that the dg suffix sums run from the last row in one pass.  Results go out as 16-byte
+        // stores of four consecutive keys of one row, after a transpose inside each quad of lanes.
+        const int k = 32 * (warp & 3) + lane, p = lane & 3, kq = k - p;
         const uint32_t lrow = (uint32_t)(32 * (warp & 3)) << 16;
-        const unsigned short *rq = reinterpret_cast<const unsigned short *>(sm + RQ);
-        const unsigned short *rk = reinterpret_cast<const unsigned short *>(sm + RK);
-        const unsigned short *rg = reinterpret_cast<const unsigned short *>(sm + RG);
-        // this key's cumsum (log2) up to row 31 (the anchor) and up to the row before this warp's rows
-        float ga = 0.f, pre = 0.f;
-        for (int t = 0; t < CT / 2; ++t)
-            ga += t < len ? bf(rg + t * KD + k) * L2E : 0.f;
-        pre = half ? ga : 0.f;
-        uint32_t aq[32], ak[32];
-        tc::tmem_ld32(tmem + lrow + TM_DQ + r0, aq);
-        tc::tmem_ld32(tmem + lrow + TM_DK + r0, ak);
-        tc::tmem_wait_ld(aq);
-        tc::tmem_wait_ld(ak);
-        float pd[32];
-        float G = pre;
+        Item it;
+        for (int u = next_item(a, blockIdx.x, nitems, it), nit = 0; u >= 0;
+             u = next_item(a, u + gridDim.x, nitems, it), ++nit) {
+            const int len = it.len;
+            const size_t rb = it.rb;
+            // rows r0 + 4 g + p (g = 0..7) of v[]: four keys from kq on, one 16-byte store each
+            auto store_rows = [&](float *out, const uint32_t (&v)[32], int r0) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int t = r0 + u;
-            const bool in = t < len;
-            G += in ? bf(rg + t * KD + k) * L2E : 0.f;
-            const float dq = tc::ex2(G - ga) * __uint_as_float(aq[u]);
-            const float dk = tc::ex2(ga - G) * __uint_as_float(ak[u]);
-            pd[u] = in ? bf(rq + t * KD + k) * dq - bf(rk + t * KD + k) * dk : 0.f;
-            if (in) {
-                const size_t row = rb + (size_t)t * rs;
-                a.dq[row * KD + k] = dq;
-                a.dk[row * KD + k] = dk;
+                for (int g = 0; g < 8; ++g) {
+                    float q4[4] = {__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                   __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])};
+                    quad_transpose(q4, p);
+                    const int t = r0 + 4 * g + p;
+                    if (t < len)
+                        *reinterpret_cast<float4 *>(out + (rb + (size_t)t * rs) * KD + kq) =
+                            make_float4(q4[0], q4[1], q4[2], q4[3]);
+                }
+            };
+            if (!tc::bar_wait(acc_full, nit & 1, abort_w) || !tc::bar_wait(xq_full, nit & 1, abort_w))
+                break;
+            tc::fence_after();
+            const uint32_t tl = tmem + lrow;
+            float run = 0.f;
+#pragma unroll 1
+            for (int half = 1; half >= 0; --half) {
+                const int r0 = 32 * half;
+                float pd[32];
+                uint32_t X[32], qk[32], r[32];   // r: an accumulator, then the results in its place
+                tc::tmem_ld32(tl + TM_X + r0, X);
+                tc::tmem_ld32(tl + TM_QK + r0, qk);
+                tc::tmem_ld32(tl + TM_DK + r0, r);
+                tc::tmem_wait_ld(X);
+                tc::tmem_wait_ld(qk);
+                tc::tmem_wait_ld(r);
+                if (half == 0) {   // G - G_a and q | k are read: the next item's may come in
+                    tc::fence_before();
+                    tc::bar_arrive(xq_free);
+                }
+#pragma unroll
+                for (int v = 0; v < 32; ++v) {
+                    const float dk = tc::ex2(-__uint_as_float(X[v])) * __uint_as_float(r[v]);
+                    pd[v] = -lo16(qk[v]) * dk;
+                    r[v] = __float_as_uint(dk);
+                }
+                store_rows(a.dk, r, r0);
+                tc::tmem_ld32(tl + TM_DQ + r0, r);
+                tc::tmem_wait_ld(r);
+#pragma unroll
+                for (int v = 0; v < 32; ++v) {
+                    const float dq = tc::ex2(__uint_as_float(X[v])) * __uint_as_float(r[v]);
+                    pd[v] = fmaf(hi16(qk[v]), dq, pd[v]);
+                    r[v] = __float_as_uint(dq);
+                }
+                store_rows(a.dq, r, r0);
+#pragma unroll
+                for (int v = 31; v >= 0; --v) {
+                    run += r0 + v < len ? pd[v] : 0.f;
+                    r[v] = __float_as_uint(run);
+                }
+                store_rows(a.dg, r, r0);
+                tc::tmem_ld32(tl + TM_DV + r0, r);
+                tc::tmem_wait_ld(r);
+                if (half == 0) {   // the accumulators are read: the next item's products may start
+                    tc::fence_before();
+                    tc::bar_arrive(acc_empty);
+                }
+                store_rows(a.dv, r, r0);
             }
+            a.dgt[((size_t)it.j * H + it.h) * KD + k] = run;
         }
-        uint32_t av[32];
-        tc::tmem_ld32(tmem + lrow + TM_DV + r0, av);
-        tc::tmem_wait_ld(av);
-#pragma unroll
-        for (int u = 0; u < 32; ++u)
-            if (r0 + u < len)
-                a.dv[(rb + (size_t)(r0 + u) * rs) * KD + k] = __uint_as_float(av[u]);
-        // suffix sums of q dq - k dk over the rows: the later rows' warps first, their totals to FA's place
-        float run = 0.f;
-        if (half) {
-#pragma unroll
-            for (int u = 31; u >= 0; --u) {
-                run += pd[u];
-                if (r0 + u < len)
-                    a.dg[(rb + (size_t)(r0 + u) * rs) * KD + k] = run;
-            }
-        }
-        __syncthreads();   // every thread of the CTA reaches this barrier (ok is uniform)
-        if (half)
-            FA[k] = run;
-        __syncthreads();
-        if (!half) {
-            run = FA[k];
-#pragma unroll
-            for (int u = 31; u >= 0; --u) {
-                run += pd[u];
-                if (u < len)
-                    a.dg[(rb + (size_t)u * rs) * KD + k] = run;
-            }
-            a.dgt[((size_t)j * H + h) * KD + k] = run;
-        }
-    } else if (tid == 0) {
-        report(a.status, GLA_ERR_TIMEOUT);
     }
+
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    if (tid == 0 && *abort_w)
+        report(a.status, GLA_ERR_TIMEOUT);
     if (warp == 0)
         tc::tmem_dealloc(tmem, TM_COLS);
 }
@@ -430,18 +571,28 @@ bool bwd_grads_tc_supported(int dtype, int K, int V)
 
 cudaError_t launch_bwd_grads_tc(const BwdArgs &a, int J, cudaStream_t s)
 {
-    static std::atomic<uint64_t> ready{0};   // per-device shared-memory opt-in, done once
+    static std::atomic<uint64_t> ready{0};   // per-device shared-memory opt-in and SM count, done once
+    static std::atomic<int> sm_count[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (!(ready.load(std::memory_order_acquire) & (1ull << (dev & 63)))) {
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(ready.load(std::memory_order_acquire) & bit)) {
         if ((e = cudaFuncSetAttribute(bwd_grads_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
             cudaSuccess)
             return e;
-        ready.fetch_or(1ull << (dev & 63), std::memory_order_release);
+        int sms = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        sm_count[dev & 63].store(sms, std::memory_order_relaxed);
+        ready.fetch_or(bit, std::memory_order_release);
     }
-    bwd_grads_tc<<<dim3(J, a.H), NT, SMEM_BYTES, s>>>(a);
+    const int nitems = J * a.H;
+    const int grid = std::min(nitems, sm_count[dev & 63].load(std::memory_order_relaxed));
+    if (grid <= 0)
+        return cudaSuccess;
+    bwd_grads_tc<<<grid, NT, SMEM_BYTES, s>>>(a, nitems);
     return cudaGetLastError();
 }
 
