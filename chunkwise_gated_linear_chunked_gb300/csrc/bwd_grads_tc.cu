@@ -14,15 +14,16 @@
 // every accumulator fills all 128 lanes and the epilogue thread that owns a key takes that key's cumsum and the
 // dg suffix sums on its own.  Every operand is used in the layout it is stored in (K-major or MN-major
 // descriptors, 128-byte swizzle): nothing is transposed.  q, k, v and do are exact in bf16; the computed
-// operands (q~, k~, AM, BM, S', R') are split into three bf16 terms x = x1 + x2 + x3 (exact to fp32 rounding):
+// operands (q~, k~, AM, BM, S', R') are split exactly into three bf16 terms x = x1 + x2 + x3:
 // a product of two split operands takes the six term products above the third order (x1 y1, x1 y2, x2 y1,
 // x1 y3, x2 y2, x3 y1), a split operand times an exact one three, so the result carries fp32-level error.
 // Rows past the end of a chunk are zero in every operand.
 //
 // Persistent CTAs (one per SM, about 226 KB of shared memory) walk the (chunk, head) items.  Warps 0-7 form
 // the operands and issue the products (thread 0 issues); warps 8-11 are the epilogue, one thread per TMEM
-// lane.  The gating thread of a key and row half also leaves, in TMEM, that key's G - G_a on its rows and
-// the raw q and k there (packed), so the epilogue reads TMEM only and writes the gradients while the operand
+// lane.  The gating thread of a key and row half also leaves, in TMEM, that key's factors 2^(G - G_a) and
+// 2^(G_a - G) on its rows and the raw q and k there (packed), so the epilogue reads TMEM only (and needs no
+// exponentials) and writes the gradients while the operand
 // warps go on to the next item's gating and score products.  The next item's q, k and g rows are copied in as
 // soon as the current gating has read its own, its v and do rows as soon as the current products are
 // complete.  The state tiles are read into registers while the products before them run: R' first (its
@@ -62,9 +63,11 @@ constexpr int RG = 212992;     // g
 constexpr int MISC = 229376;   // FA[128] = scale 2^(G_a), FR[128] = 2^(G_l - G_a)
 constexpr int BAR = MISC + 1024;   // mma, acc_full, acc_empty, xq_full, xq_free, TMEM address, abort word
 constexpr int SMEM_BYTES = BAR + 64 + 1024;
-// TMEM columns (lane = key or value column): the score tiles (lanes 0..63 = rows), G - G_a in log2 units and
-// the packed raw q | k per row for the epilogue, the accumulators dq^T, dk^T, dv^T (column = row)
-constexpr uint32_t TM_AM = 0, TM_BM = 64, TM_X = 128, TM_QK = 192, TM_DQ = 256, TM_DK = 320, TM_DV = 384;
+// TMEM columns (lane = key or value column): the score tiles (lanes 0..63 = rows), for the epilogue the
+// factors 2^(G - G_a), 2^(G_a - G) and the packed raw q | k per row, the accumulators dq^T, dk^T, dv^T
+// (column = row)
+constexpr uint32_t TM_AM = 0, TM_BM = 64, TM_EP = 128, TM_QK = 192, TM_DQ = 256, TM_DK = 320, TM_DV = 384,
+                   TM_EM = 448;
 constexpr uint32_t TM_COLS = 512;
 
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
@@ -74,9 +77,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
 }
 constexpr uint32_t ID = idesc_bf16(128, 64);
 
-// term pairs of a product of two split operands (i + j <= 2)
-__device__ constexpr int PA[6] = {0, 0, 1, 0, 1, 2};
-__device__ constexpr int PB[6] = {0, 1, 0, 2, 1, 0};
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes)
 {
@@ -100,30 +100,21 @@ __device__ __forceinline__ bool main_and(bool v)
     return r != 0;
 }
 
-// Two fp32 values -> three bf16x2 words (x = x1 + x2 + x3 for each, exact to fp32 rounding).
+// Two fp32 values -> three bf16x2 words with x = x1 + x2 + x3 exactly for each: x1 is x rounded to 8
+// significant bits (half-way cases away from zero) by an integer carry into the bits it keeps, x2 the
+// remainder (exact, by Sterbenz's lemma) rounded the same way, and x3 the rest, which has at most 8
+// significant bits.  Every term is a bf16 value without a conversion instruction; |x2| <= 2^-8 |x| and
+// |x3| <= 2^-16 |x|.  The low halves of the words hold a's terms, the high halves b's.
+__device__ __forceinline__ uint32_t bf16_cut(uint32_t u) { return (u + 0x8000u) & 0xFFFF0000u; }
 __device__ __forceinline__ void split3(float a, float b, uint32_t &w1, uint32_t &w2, uint32_t &w3)
 {
-    const __nv_bfloat162 x1 = __floats2bfloat162_rn(a, b);
-    const float2 y1 = __bfloat1622float2(x1);
-    const float ra = a - y1.x, rb = b - y1.y;
-    const __nv_bfloat162 x2 = __floats2bfloat162_rn(ra, rb);
-    const float2 y2 = __bfloat1622float2(x2);
-    const __nv_bfloat162 x3 = __floats2bfloat162_rn(ra - y2.x, rb - y2.y);
-    w1 = *reinterpret_cast<const uint32_t *>(&x1);
-    w2 = *reinterpret_cast<const uint32_t *>(&x2);
-    w3 = *reinterpret_cast<const uint32_t *>(&x3);
-}
-
-// One fp32 value -> three bf16 terms stored at p, p + step, p + 2 step.
-__device__ __forceinline__ void split3_store(float x, unsigned char *p, int step)
-{
-    const __nv_bfloat16 x1 = __float2bfloat16_rn(x);
-    const float r = x - __bfloat162float(x1);
-    const __nv_bfloat16 x2 = __float2bfloat16_rn(r);
-    const __nv_bfloat16 x3 = __float2bfloat16_rn(r - __bfloat162float(x2));
-    *reinterpret_cast<__nv_bfloat16 *>(p) = x1;
-    *reinterpret_cast<__nv_bfloat16 *>(p + step) = x2;
-    *reinterpret_cast<__nv_bfloat16 *>(p + 2 * step) = x3;
+    const uint32_t a1 = bf16_cut(__float_as_uint(a)), b1 = bf16_cut(__float_as_uint(b));
+    const float ra = a - __uint_as_float(a1), rb = b - __uint_as_float(b1);
+    const uint32_t a2 = bf16_cut(__float_as_uint(ra)), b2 = bf16_cut(__float_as_uint(rb));
+    const float sa = ra - __uint_as_float(a2), sb = rb - __uint_as_float(b2);
+    w1 = __byte_perm(a1, b1, 0x7632);
+    w2 = __byte_perm(a2, b2, 0x7632);
+    w3 = __byte_perm(__float_as_uint(sa), __float_as_uint(sb), 0x7632);
 }
 
 __device__ __forceinline__ float lo16(uint32_t w) { return __uint_as_float(w << 16); }
@@ -310,7 +301,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
             // ---- gating: thread (key k, row half rh); cumsum in log2 units, the halves' sums exchanged
             const int gk = 32 * (warp & 3) + lane, rh = warp >> 2, gr0 = 32 * rh;
             const uint32_t glane = (uint32_t)(32 * (warp & 3)) << 16;
-            uint32_t xw[32], qk[32];   // G - G_a (fp32 bits) and raw q | k of this key on the half's rows
+            uint32_t ep[32], em[32], qk[32];   // 2^(G - G_a), 2^(G_a - G) and raw q | k on the half's rows
             {
                 const unsigned short *rgp = reinterpret_cast<const unsigned short *>(sm + RG);
                 const unsigned short *rqp = reinterpret_cast<const unsigned short *>(sm + RQ);
@@ -336,26 +327,33 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
                 for (int v = 0; v < 32; ++v) {
                     const int t = gr0 + v;
                     G += gv[v];
-                    const float X = G - ga;
-                    xw[v] = __float_as_uint(X);
+                    const float X = G - ga, fp = tc::ex2(X), fm = tc::ex2(-X);
+                    ep[v] = __float_as_uint(fp);
+                    em[v] = __float_as_uint(fm);
                     const bool in = t < len;
                     const uint32_t qr = rqp[t * KD + gk], kr = rkp[t * KD + gk];
                     qk[v] = in ? (qr << 16) | kr : 0u;
-                    const float qt = in ? __uint_as_float(qr << 16) * tc::ex2(X) : 0.f;
-                    const float kt = in ? __uint_as_float(kr << 16) * tc::ex2(-X) : 0.f;
+                    const float qt = in ? __uint_as_float(qr << 16) * fp : 0.f;
+                    const float kt = in ? __uint_as_float(kr << 16) * fm : 0.f;
                     const uint32_t off = (uint32_t)(kb * 8192) + tc::sw128(t, kc);
-                    split3_store(qt, sm + Q3 + off, 16384);
-                    split3_store(kt, sm + K3 + off, 16384);
+                    uint32_t w[3];   // (q~, k~) term pairs: q~ in the low halves, k~ in the high ones
+                    split3(qt, kt, w[0], w[1], w[2]);
+#pragma unroll
+                    for (int e = 0; e < 3; ++e) {
+                        *reinterpret_cast<unsigned short *>(sm + Q3 + e * 16384 + off) = (unsigned short)(w[e] & 0xFFFFu);
+                        *reinterpret_cast<unsigned short *>(sm + K3 + e * 16384 + off) = (unsigned short)(w[e] >> 16);
+                    }
                 }
             }
             main_sync();   // the raw rows are read: the next item's q, k, g may come in
             if (un >= 0)
                 copy_rows(nxt, true);
             cp_commit();
-            // G - G_a and q | k to TMEM for the epilogue, once it has read the previous item's
+            // the factors and q | k to TMEM for the epilogue, once it has read the previous item's
             if (nit == 0 || tc::bar_wait(xq_free, (nit - 1) & 1, abort_w)) {
                 tc::fence_after();
-                tc::tmem_st32(tmem + glane + TM_X + gr0, xw);
+                tc::tmem_st32(tmem + glane + TM_EP + gr0, ep);
+                tc::tmem_st32(tmem + glane + TM_EM + gr0, em);
                 tc::tmem_st32(tmem + glane + TM_QK + gr0, qk);
                 tc::tmem_wait_st();
             }
@@ -366,10 +364,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
 
             // ---- AM = q~ k~^T (six term products), BM = do v^T
             if (tid == 0) {
-                for (int p = 0; p < 6; ++p)
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ss(tmem + TM_AM, kdesc(sb + Q3 + PA[p] * 16384, kk, 8192),
-                                   kdesc(sb + K3 + PB[p] * 16384, kk, 8192), ID, (p | kk) ? 1u : 0u);
+#pragma unroll 1
+                for (int ta = 0; ta < 3; ++ta)
+                    for (int tb = 0; ta + tb < 3; ++tb)
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma_ss(tmem + TM_AM, kdesc(sb + Q3 + ta * 16384, kk, 8192),
+                                       kdesc(sb + K3 + tb * 16384, kk, 8192), ID, (ta | tb | kk) ? 1u : 0u);
                 for (int kk = 0; kk < 8; ++kk)
                     tc::mma_ss(tmem + TM_BM, kdesc(sb + DO, kk, 8192), kdesc(sb + VV, kk, 8192), ID, kk ? 1u : 0u);
                 tc::mma_commit(bar_mma);
@@ -415,16 +415,21 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
             const uint32_t acc = tmem;
             if (tid == 0 && (nit == 0 || tc::bar_wait(acc_empty, (nit - 1) & 1, abort_w))) {
                 tc::fence_after();
-                for (int p = 0; p < 6; ++p)
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ss(acc + TM_DQ, mdesc(sb + K3 + PA[p] * 16384, kk, 8192),
-                                   kdesc(sb + BM3 + PB[p] * 8192, kk, 0), ID | tc::kIdescAMajorMN,
-                                   (p | kk) ? 1u : 0u);
-                for (int p = 0; p < 6; ++p)
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ss(acc + TM_DK, mdesc(sb + Q3 + PA[p] * 16384, kk, 8192),
-                                   mdesc(sb + BM3 + PB[p] * 8192, kk, 8192),
-                                   ID | tc::kIdescAMajorMN | tc::kIdescBMajorMN, (p | kk) ? 1u : 0u);
+#pragma unroll 1
+                for (int ta = 0; ta < 3; ++ta)
+                    for (int tb = 0; ta + tb < 3; ++tb)
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_ss(acc + TM_DQ, mdesc(sb + K3 + ta * 16384, kk, 8192),
+                                       kdesc(sb + BM3 + tb * 8192, kk, 0), ID | tc::kIdescAMajorMN,
+                                       (ta | tb | kk) ? 1u : 0u);
+#pragma unroll 1
+                for (int ta = 0; ta < 3; ++ta)
+                    for (int tb = 0; ta + tb < 3; ++tb)
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_ss(acc + TM_DK, mdesc(sb + Q3 + ta * 16384, kk, 8192),
+                                       mdesc(sb + BM3 + tb * 8192, kk, 8192),
+                                       ID | tc::kIdescAMajorMN | tc::kIdescBMajorMN, (ta | tb | kk) ? 1u : 0u);
+#pragma unroll 1
                 for (int t = 0; t < 3; ++t)
                     for (int kk = 0; kk < 4; ++kk)
                         tc::mma_ss(acc + TM_DV, mdesc(sb + DO, kk, 8192), mdesc(sb + AM3 + t * 8192, kk, 8192),
@@ -439,14 +444,17 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
             // ---- R' = 2^(G_l - G_a) R_c: dk^T += R' v^T, dv^T += R'^T k~^T
             split_state(FR);
             if (tid == 0) {
+#pragma unroll 1
                 for (int t = 0; t < 3; ++t)
                     for (int kk = 0; kk < 8; ++kk)
                         tc::mma_ss(acc + TM_DK, kdesc(sb + ST3 + t * 32768, kk, 16384), kdesc(sb + VV, kk, 8192),
                                    ID, 1u);
-                for (int p = 0; p < 6; ++p)
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ss(acc + TM_DV, mdesc(sb + ST3 + PA[p] * 32768, kk, 16384),
-                                   kdesc(sb + K3 + PB[p] * 16384, kk, 8192), ID | tc::kIdescAMajorMN, 1u);
+#pragma unroll 1
+                for (int ta = 0; ta < 3; ++ta)
+                    for (int tb = 0; ta + tb < 3; ++tb)
+                        for (int kk = 0; kk < 8; ++kk)
+                            tc::mma_ss(acc + TM_DV, mdesc(sb + ST3 + ta * 32768, kk, 16384),
+                                       kdesc(sb + K3 + tb * 16384, kk, 8192), ID | tc::kIdescAMajorMN, 1u);
                 tc::mma_commit(bar_mma);
             }
             fetch_state(a.dS, cur);
@@ -457,6 +465,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
             // ---- S' = scale 2^(G_a) S_c: dq^T += S' do^T; the accumulator set goes to the epilogue
             split_state(FA);
             if (tid == 0) {
+#pragma unroll 1
                 for (int t = 0; t < 3; ++t)
                     for (int kk = 0; kk < 8; ++kk)
                         tc::mma_ss(acc + TM_DQ, kdesc(sb + ST3 + t * 32768, kk, 16384), kdesc(sb + DO, kk, 8192),
@@ -508,29 +517,31 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
             for (int half = 1; half >= 0; --half) {
                 const int r0 = 32 * half;
                 float pd[32];
-                uint32_t X[32], qk[32], r[32];   // r: an accumulator, then the results in its place
-                tc::tmem_ld32(tl + TM_X + r0, X);
+                uint32_t f[32], qk[32], r[32];   // f: a factor; r: an accumulator, then the results in its place
+                tc::tmem_ld32(tl + TM_EM + r0, f);
                 tc::tmem_ld32(tl + TM_QK + r0, qk);
                 tc::tmem_ld32(tl + TM_DK + r0, r);
-                tc::tmem_wait_ld(X);
+                tc::tmem_wait_ld(f);
                 tc::tmem_wait_ld(qk);
                 tc::tmem_wait_ld(r);
-                if (half == 0) {   // G - G_a and q | k are read: the next item's may come in
+#pragma unroll
+                for (int v = 0; v < 32; ++v) {
+                    const float dk = __uint_as_float(f[v]) * __uint_as_float(r[v]);
+                    pd[v] = -lo16(qk[v]) * dk;
+                    r[v] = __float_as_uint(dk);
+                }
+                store_rows(a.dk, r, r0);
+                tc::tmem_ld32(tl + TM_EP + r0, f);
+                tc::tmem_ld32(tl + TM_DQ + r0, r);
+                tc::tmem_wait_ld(f);
+                tc::tmem_wait_ld(r);
+                if (half == 0) {   // the factors and q | k are read: the next item's may come in
                     tc::fence_before();
                     tc::bar_arrive(xq_free);
                 }
 #pragma unroll
                 for (int v = 0; v < 32; ++v) {
-                    const float dk = tc::ex2(-__uint_as_float(X[v])) * __uint_as_float(r[v]);
-                    pd[v] = -lo16(qk[v]) * dk;
-                    r[v] = __float_as_uint(dk);
-                }
-                store_rows(a.dk, r, r0);
-                tc::tmem_ld32(tl + TM_DQ + r0, r);
-                tc::tmem_wait_ld(r);
-#pragma unroll
-                for (int v = 0; v < 32; ++v) {
-                    const float dq = tc::ex2(__uint_as_float(X[v])) * __uint_as_float(r[v]);
+                    const float dq = __uint_as_float(f[v]) * __uint_as_float(r[v]);
                     pd[v] = fmaf(hi16(qk[v]), dq, pd[v]);
                     r[v] = __float_as_uint(dq);
                 }
