@@ -759,7 +759,7 @@ def run_wy(args, w, dev, dist, world, rank):
             "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16x3 (fp32 operands split in three bf16 terms), f32 accumulate" if dom == "wy_fwd_tc" else "f32",
+            "dtype": "bf16x2 (fp32 operands split in two bf16 terms), f32 accumulate" if dom == "wy_fwd_tc" else "f32",
             "data": "synthetic",
             "config": {"workload": args.workload, "pass": "wy", "chunk": x.BT, "B": x.B, "T": x.T, "H": x.H,
                        "HV": x.HV, "K": x.K, "V": x.V, "input_dtype": x.dtype, "outputs": "fp32",

@@ -8,10 +8,11 @@
 //   * N = BT rows of the chunk;  K = BT (the chunk's columns s), in steps of 16.
 // The B operand (N x K, K-major) is A itself: row t of the chunk's matrix is stored contiguously over s, so
 // its raw bf16 rows are copied straight into a 128-byte-swizzled tile.  The A operand X^T (M x K, K-major)
-// is formed on chip: X is scaled in fp32 and split into three bf16 terms x = x1 + x2 + x3 (8 significand
-// bits each, exact to fp32 rounding), each written transposed into its own swizzled tile; the three MMA
-// groups accumulate into the same TMEM columns.  A work item is one 128-column block of one (chunk, value
-// head), so that three CTAs (74 KB each) fit on an SM and one's conversion overlaps the others' MMAs and
+// is formed on chip: X is scaled in fp32 and split into two bf16 terms x = x1 + x2 + e, x1 = RN(x),
+// x2 = RN(x - x1), |e| <= 2^-18 |x| (within the fp32 outputs' 1e-5 relative bound, since A is exact), each
+// written transposed into its own swizzled tile; the two MMA groups accumulate into the same TMEM columns.
+// A work item is one 128-column block of one (chunk, value
+// head), so that three CTAs (58 KB each) fit on an SM and one's conversion overlaps the others' MMAs and
 // stores.  A and the raw k | v columns of the next item arrive by 16-byte asynchronous copies while the
 // current item is stored; the epilogue reads D^T from TMEM (lane = column of w or u) and each warp
 // stores 32 consecutive columns of a row per instruction.
@@ -36,8 +37,8 @@ struct WyTcSmem {
     static constexpr int XT_TILE = 128 * 128;                  // bytes: 128 rows (columns of X) x 64 s slots
     static constexpr int A_TILE = BT * 128;                    // bytes: BT rows (t) x 64 s slots
     static constexpr int A_STRIDE = (A_TILE + 1023) / 1024 * 1024;
-    static constexpr int XT = 0;                               // [3 terms] X^T tiles of the block (1024-aligned)
-    static constexpr int AB = XT + 3 * XT_TILE;                // A tile (B operand)
+    static constexpr int XT = 0;                               // [2 terms] X^T tiles of the block (1024-aligned)
+    static constexpr int AB = XT + 2 * XT_TILE;                // A tile (B operand)
     static constexpr int RAW = AB + A_STRIDE;                  // [BT][128] raw columns of the block (bf16)
     static constexpr int F = RAW + BT * 128 * 2;               // [2][BT] row factors (k part, v part)
     static constexpr int BAR = F + 2 * BT * 4;                 // mbarrier (MMA done)
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(NTC, 3) wy_fwd_tc(WyArgs a, int items)
             for (int e = tid; e < 128 * CPR; e += NTC) {
                 const int j = e >> 7, c = e & 127;
                 const float *fr = Fb + (cb * 128 + c < K ? 0 : BT);
-                uint32_t p1[4], p2[4], p3[4];
+                uint32_t p1[4], p2[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {   // rows s0, s0 + 1 of the group, two at a time
                     const int s0 = 8 * j + 2 * q;
@@ -198,18 +199,13 @@ __global__ void __launch_bounds__(NTC, 3) wy_fwd_tc(WyArgs a, int items)
                                                  s0 + 1 < m ? __bfloat162float(raw[(s0 + 1) * 128 + c]) * fr[s0 + 1] : 0.f);
                     const __nv_bfloat162 x1 = __float22bfloat162_rn(x);
                     const float2 y1 = __bfloat1622float2(x1);
-                    const float2 r1 = make_float2(x.x - y1.x, x.y - y1.y);
-                    const __nv_bfloat162 x2 = __float22bfloat162_rn(r1);
-                    const float2 y2 = __bfloat1622float2(x2);
-                    const __nv_bfloat162 x3 = __float22bfloat162_rn(make_float2(r1.x - y2.x, r1.y - y2.y));
+                    const __nv_bfloat162 x2 = __float22bfloat162_rn(make_float2(x.x - y1.x, x.y - y1.y));
                     p1[q] = *reinterpret_cast<const uint32_t *>(&x1);
                     p2[q] = *reinterpret_cast<const uint32_t *>(&x2);
-                    p3[q] = *reinterpret_cast<const uint32_t *>(&x3);
                 }
                 const uint32_t off = tc::sw128(c, 8 * j);
                 *reinterpret_cast<uint4 *>(sm + L::XT + 0 * L::XT_TILE + off) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
                 *reinterpret_cast<uint4 *>(sm + L::XT + 1 * L::XT_TILE + off) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
-                *reinterpret_cast<uint4 *>(sm + L::XT + 2 * L::XT_TILE + off) = make_uint4(p3[0], p3[1], p3[2], p3[3]);
             }
             tc::fence_proxy_async();   // generic-proxy writes of the tiles -> visible to the MMAs
         }
@@ -220,7 +216,7 @@ __global__ void __launch_bounds__(NTC, 3) wy_fwd_tc(WyArgs a, int items)
             const uint32_t at = tc::smem_u32(sm + L::AB);
             constexpr uint32_t idesc = idesc_bf16_f32(128, BT);
 #pragma unroll
-            for (int term = 0; term < 3; ++term)
+            for (int term = 0; term < 2; ++term)
 #pragma unroll
                 for (int ks = 0; ks < BT / 16; ++ks) {
                     const uint32_t xa = tc::smem_u32(sm + L::XT + term * L::XT_TILE) + 32 * ks;
