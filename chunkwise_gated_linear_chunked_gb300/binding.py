@@ -140,7 +140,7 @@ def gla_fwd(q, k, v, g, scale=None, initial_state=None, output_final_state=True,
     """GLA forward on the GPU.
 
     q, k, g: [B, T, H, K]; v: [B, T, H, V] (cuda, contiguous, all fp32, all bf16 or all fp16), or
-    [B, H, T, *] with head_first=True (dense batches).  initial_state: optional fp32 [N, H, K, V].
+    [B, H, T, *] with head_first=True (with cu_seqlens: [1, H, T, *]).  initial_state: optional fp32 [N, H, K, V].
     cu_seqlens: optional int32 [N+1] cuda offsets (B == 1).  out_dtype: fp32 (default) or, for bf16 inputs,
     bf16.  Returns (o in the layout of the inputs, final_state or None).
     """

@@ -245,8 +245,6 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     const bool varlen = cu_seqlens != nullptr;
     const bool hf = (dtype & GLA_HEAD_FIRST) != 0;
     dtype &= ~GLA_HEAD_FIRST;
-    if (hf && varlen)
-        return GLA_ERR_UNSUPPORTED;
     int rc = check_shape(B, T, H, K, V, N, chunk, dtype, varlen);
     if (rc != GLA_OK)
         return rc;
@@ -512,8 +510,6 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
     const bool varlen = cu_seqlens != nullptr;
     const bool hf = (dtype & GLA_HEAD_FIRST) != 0;
     dtype &= ~GLA_HEAD_FIRST;
-    if (hf && varlen)
-        return GLA_ERR_UNSUPPORTED;
     int rc = check_bwd_shape(B, T, H, K, V, N, chunk, dtype, varlen);
     if (rc != GLA_OK)
         return rc;

@@ -76,21 +76,28 @@ constexpr uint32_t kEpochMask = 0x3FFFFFFFu;   // a flag holds (epoch << 2) | ki
 constexpr int IQ = 4;                          // item queue depth
 constexpr uint32_t kHalf = 8192;               // one 64-column half of a 64-row 16-bit tile
 
-// Stage (64 KB): q and k as two 64-key halves each (128-byte swizzle, K-major for (a) and (b)), the raw
-// gate rows (unswizzled; overwritten by k^ in two swizzled 64-key halves), V as two swizzled 64-column halves.
-constexpr int NSTAGE = 3;
-constexpr int STAGE = 65536;
-constexpr int ST_Q0 = 0, ST_K0 = 8192, ST_G = 32768, ST_V = 49152;
-constexpr int OFF_P = NSTAGE * STAGE;             // P [t][s] fp16, 8 KB
-constexpr int OFF_EG = OFF_P + 8192;              // per output chunk (index mod 4): e[128], cl[128] (state group)
-constexpr int OFF_PS = OFF_EG + 4 * 1024;         // gating partial sums [2][4][128]
-constexpr int OFF_GT = OFF_PS + 4096;             // segment decay (log2) per key, [4][128] by state-pass item
-constexpr int OFF_WL = OFF_GT + 2048;             // look-back: running log2 weight per key, [128]
-constexpr int OFF_CL = OFF_WL + 512;              // state group: exp(G_last - G_a) of an item's last chunk, [2][128]
-constexpr int OFF_MISC = OFF_CL + 1024;           // [0..3] item queue, [4] abort word, [5] look-back flag
-constexpr int OFF_BAR = OFF_MISC + 64;
+// Stage: q and k as two 64-key halves each (128-byte swizzle, K-major for (a) and (b)), the raw gate rows
+// (unswizzled, 16 or 32 KB by the gate's element size; overwritten by k^ in two swizzled 64-key halves), V as
+// two swizzled 64-column halves.  64 KB stages with a 16-bit gate (three in the ring), 80 KB with an fp32 gate
+// (two).
+constexpr int ST_Q0 = 0, ST_K0 = 8192, ST_G = 32768;
 constexpr int NBARS = 40;
-constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;
+template <int GB>   // bytes per gate element
+struct Ring {
+    static constexpr int NSTAGE = GB == 2 ? 3 : 2;
+    static constexpr int ST_V = ST_G + C * KD * GB;
+    static constexpr int STAGE = ST_V + 16384;
+    static constexpr int OFF_P = NSTAGE * STAGE;          // P [t][s] fp16, 8 KB
+    static constexpr int OFF_EG = OFF_P + 8192;           // per output chunk (index mod 4): e[128], cl[128]
+    static constexpr int OFF_PS = OFF_EG + 4 * 1024;      // gating partial sums [2][4][128]
+    static constexpr int OFF_GT = OFF_PS + 4096;          // segment decay (log2) per key, [4][128] by state-pass item
+    static constexpr int OFF_WL = OFF_GT + 2048;          // look-back: running log2 weight per key, [128]
+    static constexpr int OFF_CL = OFF_WL + 512;           // state group: exp(G_last - G_a) of an item's last chunk
+    static constexpr int OFF_MISC = OFF_CL + 1024;        // [0..3] item queue, [4] abort word, [5] look-back flag
+    static constexpr int OFF_BAR = OFF_MISC + 64;
+    static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;
+};
+static_assert(Ring<2>::SMEM_BYTES <= 232448 && Ring<4>::SMEM_BYTES <= 232448, "shared memory per CTA");
 
 // TMEM columns: two state buffers (by item parity), two S' buffers (fp16, 64 columns each, by output chunk
 // parity; together also the start-state scan's accumulator), O^T, P.
@@ -128,6 +135,30 @@ struct In<__half> {
     static __device__ __forceinline__ uint32_t op(uint32_t w) { return w; }
 };
 __device__ __forceinline__ uint32_t In<__nv_bfloat16>::op(uint32_t w) { return pack_h2(lo(w), hi(w)); }
+// One row's gate values of keys 2 kp and 2 kp + 1 as the stage holds them (a 32-bit pair of 16-bit values,
+// or two floats), widened.
+template <typename Tg>
+struct GateW {
+    using W = uint32_t;
+    static __device__ __forceinline__ W load(const uint8_t *g, int t, int kp)
+    {
+        return *reinterpret_cast<const uint32_t *>(g + t * 256 + kp * 4);
+    }
+    static __device__ __forceinline__ W zero() { return 0u; }
+    static __device__ __forceinline__ float lo(W w) { return In<Tg>::lo(w); }
+    static __device__ __forceinline__ float hi(W w) { return In<Tg>::hi(w); }
+};
+template <>
+struct GateW<float> {
+    using W = float2;
+    static __device__ __forceinline__ W load(const uint8_t *g, int t, int kp)
+    {
+        return *reinterpret_cast<const float2 *>(g + t * 512 + kp * 8);
+    }
+    static __device__ __forceinline__ W zero() { return make_float2(0.f, 0.f); }
+    static __device__ __forceinline__ float lo(W w) { return w.x; }
+    static __device__ __forceinline__ float hi(W w) { return w.y; }
+};
 __device__ __forceinline__ bool finite(float x) { return fabsf(x) <= 3.402823466e38f; }
 __device__ __forceinline__ float amax_nan(float m, float x)
 {
@@ -420,12 +451,17 @@ __device__ __noinline__ bool chain_scan(const ChainCtx &a, const Item &it, int u
     return true;
 }
 
-template <typename Tin, typename Tout, bool HF>
+template <typename Tin, typename Tg, typename Tout, bool HF>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gla_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v, Args a,
               int nitems)
 {
+    using RG = Ring<sizeof(Tg)>;
+    constexpr int NSTAGE = RG::NSTAGE, STAGE = RG::STAGE, ST_V = RG::ST_V, OFF_P = RG::OFF_P, OFF_EG = RG::OFF_EG,
+                  OFF_PS = RG::OFF_PS, OFF_GT = RG::OFF_GT, OFF_WL = RG::OFF_WL, OFF_CL = RG::OFF_CL,
+                  OFF_MISC = RG::OFF_MISC, OFF_BAR = RG::OFF_BAR;
+    using GW = GateW<Tg>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
@@ -579,8 +615,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int row0 = it.bos + (out ? q : it.nA - 1 - q) * C;
                     // tensor-map coordinates of the chunk: (head, row) time-major, (row in sequence,
                     // sequence * H + head) head-first
-                    const int c1 = HF ? row0 - it.n * a.T : it.h, c2 = HF ? it.n * H + it.h : row0;
-                    bar_expect_tx(&full[s], (out ? 4 : 3) * 16384);
+                    // (a varlen pack is one batch row: its rows are global rows of that batch)
+                    const int nb = a.table ? 0 : it.n;
+                    const int c1 = HF ? row0 - nb * a.T : it.h, c2 = HF ? nb * H + it.h : row0;
+                    bar_expect_tx(&full[s], (out ? 4 : 3) * 16384 + (int)(sizeof(Tg) - 2) * 8192);
                     if (out) {
                         tma_load_3d(st + ST_Q0, &tm_q, 0, c1, c2, &full[s]);
                         tma_load_3d(st + 16384 + ST_Q0, &tm_q, 64, c1, c2, &full[s]);
@@ -780,7 +818,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int cq = out ? q : it.nA - 1 - q;
                 const int len = min(C, it.eos - (it.bos + cq * C));
                 const bool got = bar_wait(&full[s], (gq / NSTAGE) & 1, abort_w);
-                uint32_t gr[16];
+                typename GW::W gr[16];
                 float *ps = psum + (gq & 1) * 512;
                 if (got) {
                     v_operand<Tin>(st + ST_V, len, tid);
@@ -788,9 +826,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int uu = 0; uu < 16; ++uu) {
                         const int t = 16 * rq + uu;
-                        gr[uu] = t < len ? *reinterpret_cast<const uint32_t *>(st + ST_G + t * 256 + kp * 4) : 0u;
-                        s0 = fmaf(In<Tin>::lo(gr[uu]), L2E, s0);
-                        s1 = fmaf(In<Tin>::hi(gr[uu]), L2E, s1);
+                        gr[uu] = t < len ? GW::load(st + ST_G, t, kp) : GW::zero();
+                        s0 = fmaf(GW::lo(gr[uu]), L2E, s0);
+                        s1 = fmaf(GW::hi(gr[uu]), L2E, s1);
                     }
                     ps[rq * 128 + key] = s0;
                     ps[rq * 128 + key + 1] = s1;
@@ -838,8 +876,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int uu = 0; uu < 16; ++uu) {
                             const int t = 16 * rq + uu;
-                            X0 = fmaf(In<Tin>::lo(gr[uu]), L2E, X0);
-                            X1 = fmaf(In<Tin>::hi(gr[uu]), L2E, X1);
+                            X0 = fmaf(GW::lo(gr[uu]), L2E, X0);
+                            X1 = fmaf(GW::hi(gr[uu]), L2E, X1);
                             const uint32_t off = xo[uu & 7] + (uu >> 3) * 1024;
                             const uint32_t qw = *reinterpret_cast<const uint32_t *>(qk + ST_Q0 + off);
                             const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
@@ -861,8 +899,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int uu = 0; uu < 16; ++uu) {
                         const int t = 16 * rq + uu;
-                        X0 = fmaf(In<Tin>::lo(gr[uu]), L2E, X0);
-                        X1 = fmaf(In<Tin>::hi(gr[uu]), L2E, X1);
+                        X0 = fmaf(GW::lo(gr[uu]), L2E, X0);
+                        X1 = fmaf(GW::hi(gr[uu]), L2E, X1);
                         const uint32_t off = xo[uu & 7] + (uu >> 3) * 1024;
                         const uint32_t kw = *reinterpret_cast<const uint32_t *>(qk + ST_K0 + off);
                         const bool in = t < len;
@@ -1155,20 +1193,22 @@ bool encode_rows(CUtensorMap *m, const void *ptr, int D, int H, long long rows, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Tin, typename Tout, bool HF>
+template <typename Tin, typename Tg, typename Tout, bool HF>
 cudaError_t launch_fused_t(const Plan &pl, const Args &a, cudaStream_t s, int sms)
 {
+    constexpr int SMEM_BYTES = Ring<sizeof(Tg)>::SMEM_BYTES;
     const long long rows = pl.varlen ? (long long)pl.T : (long long)pl.B * pl.T;
     const CUtensorMapDataType tin =
         std::is_same<Tin, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType tg = std::is_same<Tg, float>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : tin;
     CUtensorMap mq, mk, mg, mv;
     const bool hf = HF;
     if (!encode_rows(&mq, a.q, pl.K, pl.H, rows, 64, C, true, tin, hf, pl.T) ||
         !encode_rows(&mk, a.k, pl.K, pl.H, rows, 64, C, true, tin, hf, pl.T) ||
-        !encode_rows(&mg, a.g, pl.K, pl.H, rows, 128, C, false, tin, hf, pl.T) ||
+        !encode_rows(&mg, a.g, pl.K, pl.H, rows, 128, C, false, tg, hf, pl.T) ||
         !encode_rows(&mv, a.v, pl.V, pl.H, rows, 64, C, true, tin, hf, pl.T))
         return cudaErrorInvalidValue;
-    auto f = gla_fused<Tin, Tout, HF>;
+    auto f = gla_fused<Tin, Tg, Tout, HF>;
     // the shared-memory opt-in is per device: remember it per device ordinal (set every time beyond 64)
     static std::atomic<unsigned long long> attr_set{0};
     int dev = 0;
@@ -1208,22 +1248,32 @@ cudaError_t launch_fused_t(const Plan &pl, const Args &a, cudaStream_t s, int sm
 
 bool tc_supported(int dtype, int K, int V)
 {
-    // 16-bit q, k, v and g (an fp32 g tile does not fit the stage ring: those shapes run on CUDA cores)
-    return (dtype == GLA_BF16 || dtype == GLA_BF16_OBF16 || dtype == GLA_F16) && K == KD && V % VT == 0 &&
-           V <= 256;
+    // 16-bit q, k, v; g 16-bit or fp32
+    return (dtype == GLA_BF16 || dtype == GLA_BF16_OBF16 || dtype == GLA_F16 || dtype == GLA_BF16_GF32 ||
+            dtype == GLA_F16_GF32) &&
+           K == KD && V % VT == 0 && V <= 256;
 }
 
 cudaError_t launch_fused_tc(const Plan &pl, const Args &a, cudaStream_t s, int sms)
 {
     // the layout is a template parameter, so the time-major kernel carries no layout branches
-    if (pl.dtype == GLA_BF16_OBF16)
-        return a.hf ? launch_fused_t<__nv_bfloat16, __nv_bfloat16, true>(pl, a, s, sms)
-                    : launch_fused_t<__nv_bfloat16, __nv_bfloat16, false>(pl, a, s, sms);
-    if (pl.dtype == GLA_F16)
-        return a.hf ? launch_fused_t<__half, float, true>(pl, a, s, sms)
-                    : launch_fused_t<__half, float, false>(pl, a, s, sms);
-    return a.hf ? launch_fused_t<__nv_bfloat16, float, true>(pl, a, s, sms)
-                : launch_fused_t<__nv_bfloat16, float, false>(pl, a, s, sms);
+    switch (pl.dtype) {
+    case GLA_BF16_OBF16:
+        return a.hf ? launch_fused_t<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, true>(pl, a, s, sms)
+                    : launch_fused_t<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16, false>(pl, a, s, sms);
+    case GLA_F16:
+        return a.hf ? launch_fused_t<__half, __half, float, true>(pl, a, s, sms)
+                    : launch_fused_t<__half, __half, float, false>(pl, a, s, sms);
+    case GLA_BF16_GF32:
+        return a.hf ? launch_fused_t<__nv_bfloat16, float, float, true>(pl, a, s, sms)
+                    : launch_fused_t<__nv_bfloat16, float, float, false>(pl, a, s, sms);
+    case GLA_F16_GF32:
+        return a.hf ? launch_fused_t<__half, float, float, true>(pl, a, s, sms)
+                    : launch_fused_t<__half, float, float, false>(pl, a, s, sms);
+    default:
+        return a.hf ? launch_fused_t<__nv_bfloat16, __nv_bfloat16, float, true>(pl, a, s, sms)
+                    : launch_fused_t<__nv_bfloat16, __nv_bfloat16, float, false>(pl, a, s, sms);
+    }
 }
 
 }  // namespace gla

@@ -59,13 +59,13 @@ typedef enum gla_dtype {
     GLA_BF16 = 1,       /* q, k, v, g bf16; o fp32 (default for bf16 inputs, see below)             */
     GLA_BF16_OBF16 = 2, /* q, k, v, g bf16; o bf16 (the pages' o.to(v) convention)                  */
     GLA_F16 = 3,        /* q, k, v, g fp16; o fp32 (same paths and bounds as GLA_BF16)                */
-    GLA_BF16_GF32 = 4,  /* q, k, v bf16, g fp32; o fp32 (fp32 CUDA-core path)                         */
-    GLA_F16_GF32 = 5    /* q, k, v fp16, g fp32; o fp32 (fp32 CUDA-core path)                         */
+    GLA_BF16_GF32 = 4,  /* q, k, v bf16, g fp32; o fp32 (forward: the tensor-core path for K == 128)  */
+    GLA_F16_GF32 = 5    /* q, k, v fp16, g fp32; o fp32 (as GLA_BF16_GF32)                             */
 } gla_dtype;
 
 /* OR-ed into the dtype argument of gla_fwd / gla_bwd (and their workspace queries): q, k, v, g, o (and the
- * gradients) are head-first [B, H, T, *] instead of [B, T, H, *].  Dense batches only (GLA_ERR_UNSUPPORTED
- * with cu_seqlens); h0 / ht keep [N, H, K, V].  Same paths, kernels and results otherwise. */
+ * gradients) are head-first [B, H, T, *] instead of [B, T, H, *]; with cu_seqlens (B == 1) that is [1, H, T, *]
+ * over the packed rows.  h0 / ht keep [N, H, K, V].  Same paths, kernels and results otherwise. */
 #define GLA_HEAD_FIRST 0x100
 /* o is fp32 for bf16 inputs by default: at the benchmark magnitudes (|o| up to ~20) a bf16-rounded o
  * alone carries up to 0.06 of rounding error, above the 2e-2 max-abs parity bound.  State h0/ht is fp32
@@ -91,8 +91,8 @@ typedef enum gla_dtype {
  *               the segment scan's publication flags, so they need no clearing per call).  One workspace
  *               must not be used by two calls that may run concurrently.
  *
- * Paths: bf16 inputs with K == 128 and V in {128, 256} run on the tcgen05 tensor cores with fp16 operands
- * and fp32 accumulation; everything else runs on fp32 CUDA cores.  Valid domain of the tensor-core path
+ * Paths: 16-bit q, k, v (g 16-bit or fp32) with K == 128 and V in {128, 256} run on the tcgen05 tensor cores
+ * with fp16 operands and fp32 accumulation; everything else runs on fp32 CUDA cores.  Valid domain of the tensor-core path
  * (its intra-chunk scores are factorised around an anchor row in the middle of each chunk): every
  * operand it forms must stay inside the fp16 range, i.e. |q|, |k| * exp(gate sum over up to half a chunk)
  * below 65000, |v| < 65000, |state| < 65000 and intra-chunk scores below 65000 in magnitude; the kernels
@@ -167,7 +167,7 @@ int gla_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, 
  * same h0 the forward used, or NULL for a zero initial state).  dout [rows, H, V] in the input dtype (the
  * gradient of o); dht [N, H, K, V] fp32 or NULL (no loss on the final state).  dtype GLA_F32 (every input
  * fp32), GLA_BF16 (q, k, v, g, dout bf16), GLA_F16, GLA_BF16_GF32 or GLA_F16_GF32 (fp32 g), optionally OR-ed
- * with GLA_HEAD_FIRST for dense batches.  Arithmetic is fp32: the per-chunk sums run on the tcgen05 tensor
+ * with GLA_HEAD_FIRST.  Arithmetic is fp32: the per-chunk sums run on the tcgen05 tensor
  * cores for bf16 inputs with K == 128 (fp32 operands split into three bf16 terms, fp32 accumulation), every
  * other step on CUDA cores.  K and V in {64, 128}; chunk 16, 32, 64 or 128 (tiled at 64 rows, as for
  * gla_fwd).  workspace: at least gla_bwd_workspace_size() bytes, 256-byte aligned, zeroed before its first

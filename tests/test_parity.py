@@ -262,21 +262,37 @@ def test_head_first_layout(case):
     assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
 
 
-def test_head_first_rejected_with_cu_seqlens():
+HEAD_FIRST_VARLEN_CASES = [
+    ("bf16", 1, 0, 2, 128, 128, True, [1, 63, 64, 65, 0, 130, 300, 2]),   # tensor-core path
+    ("bf16", 1, 0, 1, 128, 256, True, [3000, 7, 1500]),                  # segments + scan, V = 256
+    ("f32", 1, 0, 2, 64, 64, True, [5, 0, 200, 64]),                     # CUDA-core path
+]
+
+
+@pytest.mark.parametrize("case", HEAD_FIRST_VARLEN_CASES, ids=_case_id)
+def test_head_first_varlen(case):
+    """A packed varlen batch in [1, H, T, *] gives the head-first permutation of the time-major result."""
     from chunkwise_gated_linear_chunked_gb300 import binding
-    inp = make_inputs("bf16", B=1, T=0, H=1, K=128, V=128, lengths=[3, 5], seed=32)
-    q, k, v, g, _, cu = to_device(inp)
-    with pytest.raises(binding.GlaError) as e:
-        binding.gla_fwd(q.transpose(1, 2).contiguous(), k.transpose(1, 2).contiguous(),
-                        v.transpose(1, 2).contiguous(), g.transpose(1, 2).contiguous(), scale=inp.scale,
-                        cu_seqlens=cu, head_first=True)
-    assert e.value.code == binding.GLA_ERR_UNSUPPORTED
+    d, B, T, H, K, V, h0, lengths = case
+    inp = make_inputs(d, B=B, T=T, H=H, K=K, V=V, h0=h0, lengths=lengths,
+                      seed=zlib.crc32(_case_id(case).encode()) % 1000)
+    hf = lambda x: x.transpose(1, 2).contiguous().cuda()
+    o, ht = binding.gla_fwd(hf(inp.q), hf(inp.k), hf(inp.v), hf(inp.g), scale=inp.scale,
+                            initial_state=None if inp.h0 is None else inp.h0.cuda(),
+                            cu_seqlens=inp.cu_seqlens.cuda(), head_first=True)
+    torch.cuda.synchronize()
+    o_ref, ht_ref = run_oracle(inp)
+    assert o.shape == (1, H, inp.q.shape[1], V)
+    assert_close(as_f64(o.transpose(1, 2)), o_ref, TOL[d], "o")
+    assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
 
 
 GF32_CASES = [
-    ("bf16", 2, 200, 2, 128, 128, True, None),
-    ("f16", 1, 3000, 1, 64, 128, True, None),      # segments + scan
-    ("bf16", 1, 0, 2, 128, 64, True, [1, 63, 64, 65, 0, 130, 300, 2]),
+    ("bf16", 2, 200, 2, 128, 128, True, None),      # tensor-core path (two 80 KB stages)
+    ("f16", 1, 3000, 1, 128, 256, True, None),      # tensor-core path, segments + scan, V = 256
+    ("bf16", 1, 0, 2, 128, 128, True, [1, 63, 64, 65, 0, 130, 300, 2]),   # tensor-core path, varlen
+    ("f16", 1, 3000, 1, 64, 128, True, None),       # K = 64: CUDA-core path
+    ("bf16", 1, 0, 2, 64, 64, True, [1, 63, 64, 65, 0, 130, 300, 2]),
 ]
 
 
@@ -290,11 +306,31 @@ def _with_fp32_gate(inp, seed):
 
 @pytest.mark.parametrize("case", GF32_CASES, ids=_case_id)
 def test_fp32_gate_with_16bit_inputs(case):
-    """16-bit q, k, v with an fp32 g run on the fp32 CUDA-core path: the fp32 bound applies."""
+    """16-bit q, k, v with an fp32 g: K == 128 runs the tensor-core kernel (16-bit operands, so the 16-bit
+    bound applies, as with a 16-bit g); K == 64 runs the fp32 CUDA-core path (the fp32 bound)."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
     d, B, T, H, K, V, h0, lengths = case
     seed = zlib.crc32(_case_id(case).encode()) % 1000
     inp = _with_fp32_gate(make_inputs(d, B=B, T=T, H=H, K=K, V=V, h0=h0, lengths=lengths, seed=seed), seed + 1)
-    o, ht = run_gpu(inp)
+    timer = binding.KernelTimer()
+    with timer:
+        o, ht = run_gpu(inp)
+    names = [n for n, _ in timer.results()]
     o_ref, ht_ref = run_oracle(inp)
-    assert_close(as_f64(o), o_ref, TOL["f32"], "o")
-    assert_close(as_f64(ht), ht_ref, TOL["f32"], "ht")
+    tol = TOL[d] if K == 128 else TOL["f32"]
+    assert ("fused_tc" in names) == (K == 128), names
+    assert_close(as_f64(o), o_ref, tol, "o")
+    assert_close(as_f64(ht), ht_ref, tol, "ht")
+
+
+def test_fp32_gate_head_first_tensor_cores():
+    """fp32 g in the head-first layout on the tensor-core path."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = _with_fp32_gate(make_inputs("bf16", B=2, T=700, H=2, K=128, V=128, h0=True, seed=77), 78)
+    hf = lambda x: x.transpose(1, 2).contiguous().cuda()
+    o, ht = binding.gla_fwd(hf(inp.q), hf(inp.k), hf(inp.v), hf(inp.g), scale=inp.scale,
+                            initial_state=inp.h0.cuda(), head_first=True)
+    torch.cuda.synchronize()
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(as_f64(o.transpose(1, 2)), o_ref, TOL["bf16"], "o")
+    assert_close(as_f64(ht), ht_ref, TOL["bf16"], "ht")

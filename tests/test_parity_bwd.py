@@ -133,6 +133,21 @@ def test_backward_head_first(d, K, V):
     _check(got, _oracle(inp, do, dh))
 
 
+@pytest.mark.parametrize("d,K,V", [("bf16", 128, 128), ("f32", 64, 128)])
+def test_backward_head_first_varlen(d, K, V):
+    """A packed varlen batch in [1, H, T, *]: gradients are the head-first permutation of the time-major ones."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = make_inputs(d, B=1, T=0, H=2, K=K, V=V, h0=True, lengths=[1, 63, 64, 65, 0, 130, 300, 2], seed=33)
+    do, dh = _grad_inputs(inp, 34)
+    hf = lambda x: x.transpose(1, 2).contiguous().cuda()
+    got = binding.gla_bwd(hf(inp.q), hf(inp.k), hf(inp.v), hf(inp.g), hf(do), scale=inp.scale,
+                          initial_state=inp.h0.cuda(), dht=dh.cuda(), cu_seqlens=inp.cu_seqlens.cuda(),
+                          head_first=True)
+    torch.cuda.synchronize()
+    got = [x.transpose(1, 2) for x in got[:4]] + [got[4]]
+    _check(got, _oracle(inp, do, dh))
+
+
 @pytest.mark.parametrize("d", ["bf16", "f16"])
 def test_backward_fp32_gate(d):
     import dataclasses
