@@ -176,7 +176,7 @@ thread_local Profile g_prof;
 enum KernelId {
     K_PLAN = 1, K_STATE_FFMA = 2, K_SCAN = 3, K_OUT_FFMA = 4, K_FUSED_TC = 7,
     K_BWD_SUMS = 8, K_BWD_SCAN = 9, K_BWD_GRADS = 10, K_BWD_DG = 11, K_TTT = 12, K_WY = 13,
-    K_WY_TC = 14, K_BWD_SUMS_TC = 15, K_BWD_GRADS_TC = 16
+    K_WY_TC = 14, K_BWD_SUMS_TC = 15, K_BWD_GRADS_TC = 16, K_TTT_TC = 17
 };
 
 // Launch one kernel through `fn`, bracketed by the profiling events when they are armed.
@@ -425,6 +425,7 @@ extern "C" const char *gla_kernel_name(int kernel_id)
     case K_WY_TC: return "wy_fwd_tc";
     case K_BWD_SUMS_TC: return "bwd_chunk_sums_tc";
     case K_BWD_GRADS_TC: return "bwd_grads_tc";
+    case K_TTT_TC: return "ttt_linear_tc";
     default: return "unknown";
     }
 }
@@ -671,7 +672,10 @@ extern "C" int gla_ttt_linear_fwd(const void *q, const void *k, const void *v, c
     a.N = nseq; a.T = T; a.H = H; a.D = D; a.BT = chunk;
     a.status = static_cast<int *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (profiled(K_TTT, s, [&] { return launch_ttt_linear_fwd(a, dtype, s); }) != cudaSuccess)
+    // bf16 q, k, v with D == 128 on the tensor cores; other shapes on the CUDA-core cluster kernel
+    const bool tc = ttt_tc_supported(dtype, D, chunk);
+    if (profiled(tc ? K_TTT_TC : K_TTT, s,
+                 [&] { return tc ? launch_ttt_linear_tc(a, s) : launch_ttt_linear_fwd(a, dtype, s); }) != cudaSuccess)
         return GLA_ERR_CUDA;
     return GLA_OK;
 }

@@ -132,6 +132,8 @@ struct TttArgs {
     int *status;
 };
 cudaError_t launch_ttt_linear_fwd(const TttArgs &a, int dtype, cudaStream_t s);
+bool ttt_tc_supported(int dtype, int D, int BT);
+cudaError_t launch_ttt_linear_tc(const TttArgs &a, cudaStream_t s);
 
 // WY representation forward arguments (passed by value).  Chunk slots: dense j = n * NT + p; varlen from
 // the slot table (plan_varlen with segments of BT rows).

@@ -48,6 +48,10 @@ CASES = [
     ("bf16", 2, 130, 2, 128, False, None, 32),
     ("f16", 1, 97, 3, 64, True, None, 16),
     ("bf16", 1, 0, 2, 64, True, [1, 15, 16, 17, 0, 130, 300], 16),   # varlen incl. empty
+    # bf16 with D = 128: the tensor-core kernel
+    ("bf16", 2, 200, 2, 128, True, None, 16),     # ragged last mini-batch
+    ("bf16", 1, 0, 2, 128, True, [1, 15, 16, 17, 0, 130, 300], 16),
+    ("bf16", 1, 0, 1, 128, False, [33, 64, 7], 32),
 ]
 
 
@@ -69,6 +73,18 @@ def test_ttt_linear_forward(case):
     for name, x, y in zip(("o", "ht", "hbt"), (o, ht, hbt), ref):
         rel, mabs = errors(as_f64(x), y)
         assert rel <= TOL, f"{name}: rel-L2 {rel:.3e} (max-abs {mabs:.3e})"
+
+
+def test_ttt_tensor_core_kernel_runs_for_bf16_d128():
+    """bf16 q, k, v with D = 128 take the tensor-core kernel (the launch hook names the kernel that ran)."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    q, k, v, w, b, eta, s0, sb0, _ = make_ttt("bf16", 1, 64, 1, 128, True, None, 5)
+    timer = binding.KernelTimer()
+    with timer:
+        binding.ttt_linear_fwd(q.cuda(), k.cuda(), v.cuda(), w.cuda(), b.cuda(), eta.cuda(), chunk=16,
+                               initial_state=s0.cuda(), initial_state_bias=sb0.cuda())
+    torch.cuda.synchronize()
+    assert [n for n, _ in timer.results()] == ["ttt_linear_tc"]
 
 
 def test_ttt_bad_offsets_are_reported_not_faulted():
