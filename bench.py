@@ -632,7 +632,7 @@ def run_ttt(args, w, inp, dev, dist, world, rank):
             "metric": "TTT-linear fwd tokens/s on 1 GB300; % of fp32 CUDA-core peak",
             "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16x3 (fp32 state split in three bf16 terms), f32 accumulate" if dom == "ttt_linear_tc" else "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16x2 (fp32 state split in two bf16 terms for its products), f32 state and accumulate" if dom == "ttt_linear_tc" else "f32", "data": "synthetic",
             "config": {"workload": args.workload, "pass": "ttt", "chunk": args.ttt_chunk, "B": B, "T": T,
                        "H": inp.H, "D": inp.K, "input_dtype": inp.dtype,
                        "l2": "flushed before every timed step (zero-fill of a 2x L2 buffer, outside the events)",
