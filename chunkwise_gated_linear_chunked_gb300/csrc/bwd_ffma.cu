@@ -29,6 +29,19 @@ constexpr int C = kChunk;   // 64
 constexpr int NTB = 256;    // threads per CTA
 constexpr int AROW = 31;    // anchor row of the factorisation
 
+// Store four floats, or add them to what is there (a later value slice of the same gradient).
+__device__ __forceinline__ void put4(float *p, float4 x, int acc)
+{
+    if (acc) {
+        const float4 o = *reinterpret_cast<const float4 *>(p);
+        x.x += o.x;
+        x.y += o.y;
+        x.z += o.z;
+        x.w += o.w;
+    }
+    *reinterpret_cast<float4 *>(p) = x;
+}
+
 __device__ __forceinline__ bool bwd_slot(const BwdArgs &a, int j, int &n, int &bos, int &eos)
 {
     if (a.table) {
@@ -80,7 +93,7 @@ __global__ void __launch_bounds__(NTB) bwd_chunk_sums(BwdArgs a)
     }
     for (int e = tid; e < C * 16; e += NTB) {
         const int i = e >> 4, c4 = (e & 15) * 4;
-        const size_t o = (rb + (size_t)i * rs) * V + v0 + c4;
+        const size_t o = (rb + (size_t)i * rs) * a.ldv + v0 + c4;
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
         *reinterpret_cast<float4 *>(VS + i * 64 + c4) = i < len ? IO<Tin>::load4(v + o) : z;
         *reinterpret_cast<float4 *>(DS + i * 64 + c4) = i < len ? IO<Tin>::load4(dout + o) : z;
@@ -150,7 +163,8 @@ __global__ void __launch_bounds__(NTB) bwd_scan(BwdArgs a)
         first = n * a.NC;
         cnt = a.NC;
     }
-    const size_t st = ((size_t)n * H + h) * K * V + e;
+    const size_t st = ((size_t)n * H + h) * K * V + e;                 // ht in the workspace
+    const size_t su = (((size_t)n * H + h) * K + kk) * a.lds + (e - kk * V);   // h0, dht, dh0 of the caller
     const size_t hs = (size_t)H * K * V;                               // slot stride of dS / dR
     float *__restrict__ dS = a.dS + ((size_t)first * H + h) * K * V + e;
     float *__restrict__ dR = a.dR + ((size_t)first * H + h) * K * V + e;
@@ -160,8 +174,8 @@ __global__ void __launch_bounds__(NTB) bwd_scan(BwdArgs a)
     // adjoints, in place of dR, newest first) run in the same loop, in batches of D chunks whose loads are
     // all issued before the batch's in-place stores, so both directions' loads overlap.
     constexpr int D = 16;
-    float S = a.h0 ? a.h0[st] : 0.f;
-    float R = a.dht ? a.dht[st] : 0.f;
+    float S = a.h0 ? a.h0[su] : 0.f;
+    float R = a.dht ? a.dht[su] : 0.f;
     for (int c0 = 0; c0 < cnt; c0 += D) {
         const int c1 = cnt - 1 - c0;   // the backward scan's first chunk of this batch
         float ts[D], es[D], tr[D], er[D];
@@ -184,7 +198,7 @@ __global__ void __launch_bounds__(NTB) bwd_scan(BwdArgs a)
     }
     a.ht[st] = S;
     if (a.dh0)
-        a.dh0[st] = R;
+        a.dh0[su] = R;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -305,7 +319,7 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
     }
     for (int e = tid; e < C * V / 4; e += NTB) {
         const int i = e / (V / 4), c4 = (e - i * (V / 4)) * 4;
-        const size_t o = (rb + (size_t)i * rs) * V + c4;
+        const size_t o = (rb + (size_t)i * rs) * a.ldv + c4;
         const bool in = i < len;
         *reinterpret_cast<float4 *>(VV + i * V + c4) = in ? IO<Tin>::load4(v + o) : z4;
         *reinterpret_cast<float4 *>(DO + i * V + c4) = in ? IO<Tin>::load4(dout + o) : z4;
@@ -404,7 +418,7 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
         for (int r = 0; r < 4; ++r) {
             const int jj = 4 * ty + r;
             if (jj < len) {
-                float *row = a.dv + (rb + (size_t)jj * rs) * V;
+                float *row = a.dv + (rb + (size_t)jj * rs) * a.ldv;
 #pragma unroll
                 for (int c = 0; c < V / 16; c += 4)
                     *reinterpret_cast<float4 *>(row + col_of(c, tx)) =
@@ -444,8 +458,8 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
             float *row = a.dq + (rb + (size_t)i * rs) * K;
 #pragma unroll
             for (int c = 0; c < K / 16; c += 4)
-                *reinterpret_cast<float4 *>(row + col_of(c, tx)) =
-                    make_float4(accq[r][c], accq[r][c + 1], accq[r][c + 2], accq[r][c + 3]);
+                put4(row + col_of(c, tx), make_float4(accq[r][c], accq[r][c + 1], accq[r][c + 2], accq[r][c + 3]),
+                     a.acc);
         }
     }
     // ---- dk_j = e^{G_a - G_j} (sum_i BM_ij q~_i + e^{G_l - G_a} R_c v_j^T); k dk = k~ (that sum)
@@ -478,8 +492,8 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
             float *row = a.dk + (rb + (size_t)i * rs) * K;
 #pragma unroll
             for (int c = 0; c < K / 16; c += 4)
-                *reinterpret_cast<float4 *>(row + col_of(c, tx)) =
-                    make_float4(acck[r][c], acck[r][c + 1], acck[r][c + 2], acck[r][c + 3]);
+                put4(row + col_of(c, tx), make_float4(acck[r][c], acck[r][c + 1], acck[r][c + 2], acck[r][c + 3]),
+                     a.acc);
         }
     }
     __syncthreads();
@@ -488,7 +502,8 @@ __global__ void __launch_bounds__(NTB, 1) bwd_grads(BwdArgs a)
         float run = 0.f;
         for (int i = len - 1; i >= 0; --i) {
             run += PD[i * K + tid];
-            a.dg[(rb + (size_t)i * rs) * K + tid] = run;
+            float *d = a.dg + (rb + (size_t)i * rs) * K + tid;
+            *d = a.acc ? *d + run : run;
         }
         a.dgt[((size_t)j * H + h) * K + tid] = run;
     }
@@ -514,7 +529,7 @@ __global__ void __launch_bounds__(NTB) bwd_dg_scan(BwdArgs a)
     if (a.dht) {   // sum over v of ht * dht for this key: one contiguous row of V floats per thread
         const size_t st = (((size_t)n * H + h) * K + kk) * V;
         const float4 *x4 = reinterpret_cast<const float4 *>(a.ht + st);
-        const float4 *y4 = reinterpret_cast<const float4 *>(a.dht + st);
+        const float4 *y4 = reinterpret_cast<const float4 *>(a.dht + (((size_t)n * H + h) * K + kk) * a.lds);
 #pragma unroll 8
         for (int i = 0; i < V / 4; ++i) {
             const float4 x = x4[i], y = y4[i];

@@ -228,8 +228,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
                 for (int r = tid; r < CT * 16; r += NMAIN) {
                     const int t = r >> 4, c = r & 15;
                     const bool in = t < it.len;
+                    const size_t ld = which < 3 ? (size_t)KD : (size_t)a.ldv;   // v and do: the caller's stride
                     const unsigned char *s = static_cast<const unsigned char *>(src) +
-                                             ((it.rb + (size_t)(in ? t : 0) * rs) * KD + 8 * c) * 2;
+                                             ((it.rb + (size_t)(in ? t : 0) * rs) * ld + 8 * c) * 2;
                     const uint32_t off = which < 3 ? (uint32_t)(t * 256 + 16 * c)
                                                    : (uint32_t)((c >> 3) * 8192) + tc::sw128(t, 8 * (c & 7));
                     cp_async16(sm + dst + off, s, in ? 16u : 0u);
@@ -495,17 +496,27 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
              u = next_item(a, u + gridDim.x, nitems, it), ++nit) {
             const int len = it.len;
             const size_t rb = it.rb;
-            // rows r0 + 4 g + p (g = 0..7) of v[]: four keys from kq on, one 16-byte store each
-            auto store_rows = [&](float *out, const uint32_t (&v)[32], int r0) {
+            // rows r0 + 4 g + p (g = 0..7) of v[]: four keys from kq on, one 16-byte store each (rows ld apart;
+            // added to what is there when acc)
+            auto store_rows = [&](float *out, const uint32_t (&v)[32], int r0, size_t ld, int acc) {
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                     float q4[4] = {__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
                                    __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])};
                     quad_transpose(q4, p);
                     const int t = r0 + 4 * g + p;
-                    if (t < len)
-                        *reinterpret_cast<float4 *>(out + (rb + (size_t)t * rs) * KD + kq) =
-                            make_float4(q4[0], q4[1], q4[2], q4[3]);
+                    if (t < len) {
+                        float4 *dst = reinterpret_cast<float4 *>(out + (rb + (size_t)t * rs) * ld + kq);
+                        float4 x = make_float4(q4[0], q4[1], q4[2], q4[3]);
+                        if (acc) {
+                            const float4 o = *dst;
+                            x.x += o.x;
+                            x.y += o.y;
+                            x.z += o.z;
+                            x.w += o.w;
+                        }
+                        *dst = x;
+                    }
                 }
             };
             if (!tc::bar_wait(acc_full, nit & 1, abort_w) || !tc::bar_wait(xq_full, nit & 1, abort_w))
@@ -530,7 +541,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
                     pd[v] = -lo16(qk[v]) * dk;
                     r[v] = __float_as_uint(dk);
                 }
-                store_rows(a.dk, r, r0);
+                store_rows(a.dk, r, r0, KD, a.acc);
                 tc::tmem_ld32(tl + TM_EP + r0, f);
                 tc::tmem_ld32(tl + TM_DQ + r0, r);
                 tc::tmem_wait_ld(f);
@@ -545,20 +556,20 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
                     pd[v] = fmaf(hi16(qk[v]), dq, pd[v]);
                     r[v] = __float_as_uint(dq);
                 }
-                store_rows(a.dq, r, r0);
+                store_rows(a.dq, r, r0, KD, a.acc);
 #pragma unroll
                 for (int v = 31; v >= 0; --v) {
                     run += r0 + v < len ? pd[v] : 0.f;
                     r[v] = __float_as_uint(run);
                 }
-                store_rows(a.dg, r, r0);
+                store_rows(a.dg, r, r0, KD, a.acc);
                 tc::tmem_ld32(tl + TM_DV + r0, r);
                 tc::tmem_wait_ld(r);
                 if (half == 0) {   // the accumulators are read: the next item's products may start
                     tc::fence_before();
                     tc::bar_arrive(acc_empty);
                 }
-                store_rows(a.dv, r, r0);
+                store_rows(a.dv, r, r0, a.ldv, 0);
             }
             a.dgt[((size_t)it.j * H + it.h) * KD + k] = run;
         }

@@ -118,19 +118,20 @@ __global__ void __launch_bounds__(NTS, 2) bwd_chunk_sums_tc(BwdArgs a)
     const int len = eos - bos, H = a.H;
     const size_t rb = row_head(bos, h, H, a.T, a.hf);   // row t of the chunk: row-head index rb + t * rs
     const int rs = a.hf ? 1 : H;
-    // 16-byte asynchronous copies of the valid rows of a [rows, H, width] tensor into shared rows of rowb bytes
-    auto stage = [&](const void *src, int rowb, int dst) {
+    // 16-byte asynchronous copies of the valid rows of a [rows, H, width] tensor (global rows of strideb bytes)
+    // into shared rows of rowb bytes
+    auto stage = [&](const void *src, int rowb, int strideb, int dst) {
         const int per = rowb / 16;
         const char *s8 = static_cast<const char *>(src);
         for (int e = tid; e < CT * per; e += NTS) {
             const int t = e / per, c = e - t * per;
             if (t < len)
-                cp_async16(sm + dst + t * rowb + 16 * c, s8 + (rb + (size_t)t * rs) * rowb + 16 * c);
+                cp_async16(sm + dst + t * rowb + 16 * c, s8 + (rb + (size_t)t * rs) * strideb + 16 * c);
         }
     };
-    stage(a.g, KT * (int)sizeof(Tg), L::AT);
-    stage(a.k, KT * 2, L::RK);
-    stage(a.v, V * 2, L::RV);
+    stage(a.g, KT * (int)sizeof(Tg), KT * (int)sizeof(Tg), L::AT);
+    stage(a.k, KT * 2, KT * 2, L::RK);
+    stage(a.v, V * 2, a.ldv * 2, L::RV);
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (tid == 0) {
         tc::bar_init(bar, 1);
@@ -209,8 +210,8 @@ __global__ void __launch_bounds__(NTS, 2) bwd_chunk_sums_tc(BwdArgs a)
     if (tid == 0)
         issue(tmem);   // dS -> columns [0, V)
     // the raw k and v rows are consumed: fetch q and do into their places while the MMAs run
-    stage(a.q, KT * 2, L::RK);
-    stage(a.dout, V * 2, L::RV);
+    stage(a.q, KT * 2, KT * 2, L::RK);
+    stage(a.dout, V * 2, a.ldv * 2, L::RV);
     asm volatile("cp.async.commit_group;" ::: "memory");
     bool ok = tc::bar_wait(bar, 0);
     asm volatile("cp.async.wait_group 0;" ::: "memory");

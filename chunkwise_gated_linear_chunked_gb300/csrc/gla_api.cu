@@ -478,13 +478,17 @@ int check_bwd_shape(int B, int T, int H, int K, int V, int N, int chunk, int dty
         return GLA_ERR_INVALID_ARG;
     if (varlen ? B != 1 : N != B)
         return GLA_ERR_INVALID_ARG;
-    if (!supported_chunk(chunk) || !bwd_supported(dtype, K, V))
+    // V = 256 runs as two 128-wide value slices
+    if (!supported_chunk(chunk) || !bwd_supported(dtype, K, V == 256 ? 128 : V))
         return GLA_ERR_UNSUPPORTED;
     const long long rows = varlen ? (long long)T : (long long)B * T;
     if (rows * H * (K > V ? K : V) >= (1LL << 31) || (long long)(N + T / kChunk + 1) * H * K * V >= (1LL << 31))
         return GLA_ERR_UNSUPPORTED;
     return GLA_OK;
 }
+
+// The value width one pass of the backward handles: V, or 128-wide slices of a wider V.
+int bwd_slice(int V) { return V > 128 ? 128 : V; }
 
 }  // namespace
 }  // namespace gla
@@ -498,8 +502,8 @@ extern "C" size_t gla_bwd_workspace_size(int B, int T, int H, int K, int V, int 
         check_bwd_shape(1, T, H, K, V, N, chunk, dtype, true) != GLA_OK)
         return 0;
     BwdPlan a, b;
-    make_bwd_plan(a, B, T, H, K, V, B, false);
-    make_bwd_plan(b, 1, T, H, K, V, N, true);
+    make_bwd_plan(a, B, T, H, K, bwd_slice(V), B, false);
+    make_bwd_plan(b, 1, T, H, K, bwd_slice(V), N, true);
     return a.total > b.total ? a.total : b.total;
 }
 
@@ -526,8 +530,9 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
                           (const void *)cu_seqlens})
         if (misaligned(p))
             return GLA_ERR_ALIGNMENT;
+    const int VS = bwd_slice(V);   // value width of one pass
     BwdPlan bp;
-    make_bwd_plan(bp, B, T, H, K, V, N, varlen);
+    make_bwd_plan(bp, B, T, H, K, VS, N, varlen);
     if (!workspace || workspace_bytes < bp.total)
         return GLA_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign)
@@ -566,7 +571,8 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
     a.q = q; a.k = k; a.v = v; a.g = g; a.dout = dout; a.h0 = h0; a.dht = dht;
     a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dh0 = dh0;
     a.scale = scale;
-    a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.N = nseq; a.NC = bp.NC;
+    a.B = B; a.T = T; a.H = H; a.K = K; a.V = VS; a.N = nseq; a.NC = bp.NC;
+    a.ldv = V; a.lds = V; a.acc = 0;
     a.hf = hf ? 1 : 0;
     a.status = reinterpret_cast<int *>(ws);
     a.dS = reinterpret_cast<float *>(ws + bp.off_dS);
@@ -590,21 +596,33 @@ extern "C" int gla_bwd(const void *q, const void *k, const void *v, const void *
             return GLA_ERR_CUDA;
     }
     const int J = bp.J;
-    // bf16 q, k, v, dout with K = 128: chunk sums on the tensor cores; everything else on CUDA cores
-    const bool sums_tc = bwd_sums_tc_supported(dtype, K, V);
-    if (J > 0 && profiled(sums_tc ? K_BWD_SUMS_TC : K_BWD_SUMS, s, [&] {
-            return sums_tc ? launch_bwd_sums_tc(a, J, dtype, s) : launch_bwd_sums(a, J, dtype, s);
-        }) != cudaSuccess)
-        return GLA_ERR_CUDA;
-    if (profiled(K_BWD_SCAN, s, [&] { return launch_bwd_scan(a, s); }) != cudaSuccess)
-        return GLA_ERR_CUDA;
-    const bool grads_tc = bwd_grads_tc_supported(dtype, K, V);
-    if (J > 0 && profiled(grads_tc ? K_BWD_GRADS_TC : K_BWD_GRADS, s, [&] {
-            return grads_tc ? launch_bwd_grads_tc(a, J, s) : launch_bwd_grads(a, J, dtype, s);
-        }) != cudaSuccess)
-        return GLA_ERR_CUDA;
-    if (profiled(K_BWD_DG, s, [&] { return launch_bwd_dg(a, J, s); }) != cudaSuccess)
-        return GLA_ERR_CUDA;
+    // bf16 q, k, v, dout with K = 128: chunk sums on the tensor cores (and the gradients for 128-wide values);
+    // everything else on CUDA cores.  A V wider than one pass runs as value slices: dv, dh0 and the states are
+    // per slice, dq, dk and dg (linear in the slices) are accumulated by the later slices.
+    const bool sums_tc = bwd_sums_tc_supported(dtype, K, VS);
+    const bool grads_tc = bwd_grads_tc_supported(dtype, K, VS);
+    const size_t vbytes = dtype == GLA_F32 ? 4 : 2;
+    for (int v0 = 0; v0 < V; v0 += VS) {
+        a.v = static_cast<const char *>(v) + (size_t)v0 * vbytes;
+        a.dout = static_cast<const char *>(dout) + (size_t)v0 * vbytes;
+        a.dv = dv + v0;
+        a.h0 = h0 ? h0 + v0 : nullptr;
+        a.dht = dht ? dht + v0 : nullptr;
+        a.dh0 = dh0 ? dh0 + v0 : nullptr;
+        a.acc = v0 > 0;
+        if (J > 0 && profiled(sums_tc ? K_BWD_SUMS_TC : K_BWD_SUMS, s, [&] {
+                return sums_tc ? launch_bwd_sums_tc(a, J, dtype, s) : launch_bwd_sums(a, J, dtype, s);
+            }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+        if (profiled(K_BWD_SCAN, s, [&] { return launch_bwd_scan(a, s); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+        if (J > 0 && profiled(grads_tc ? K_BWD_GRADS_TC : K_BWD_GRADS, s, [&] {
+                return grads_tc ? launch_bwd_grads_tc(a, J, s) : launch_bwd_grads(a, J, dtype, s);
+            }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+        if (profiled(K_BWD_DG, s, [&] { return launch_bwd_dg(a, J, s); }) != cudaSuccess)
+            return GLA_ERR_CUDA;
+    }
     return GLA_OK;
 }
 

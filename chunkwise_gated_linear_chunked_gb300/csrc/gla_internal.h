@@ -79,6 +79,10 @@ struct BwdArgs {
     float *gl;                        // [J][H][K]: chunk total log-decay (natural log)
     float *ht;                        // [N][H][K][V]: final states
     float *dgt;                       // [J][H][K]: chunk sums of q dq - k dk, then their carries
+    int ldv;                          // row stride (elements) of v, dout and dv: V, or the full width when the
+                                      // call runs as 128-wide value slices (v, dout, dv then point at the slice)
+    int lds;                          // row stride of the rows of h0, dht and dh0 ([N][H][K][lds], likewise)
+    int acc;                          // add into dq, dk and dg (a second value slice) instead of writing
     int *status;
 };
 

@@ -167,12 +167,13 @@ int gla_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, 
  * same h0 the forward used, or NULL for a zero initial state).  dout [rows, H, V] in the input dtype (the
  * gradient of o); dht [N, H, K, V] fp32 or NULL (no loss on the final state).  dtype GLA_F32 (every input
  * fp32), GLA_BF16 (q, k, v, g, dout bf16), GLA_F16, GLA_BF16_GF32 or GLA_F16_GF32 (fp32 g), optionally OR-ed
- * with GLA_HEAD_FIRST.  Arithmetic is fp32: the per-chunk sums run on the tcgen05 tensor
- * cores for bf16 inputs with K == 128 (fp32 operands split into three bf16 terms, fp32 accumulation), every
- * other step on CUDA cores.  K and V in {64, 128}; chunk 16, 32, 64 or 128 (tiled at 64 rows, as for
- * gla_fwd).  workspace: at least gla_bwd_workspace_size() bytes, 256-byte aligned, zeroed before its first
- * use (status word in its first bytes); it holds the chunk-start states and chunk-end adjoints
- * (2 * chunks * H * K * V fp32).  Outputs must not overlap any input, the workspace or one another.  The
+ * with GLA_HEAD_FIRST.  Arithmetic is fp32: for bf16 inputs with K == 128 the per-chunk sums and the per-chunk
+ * gradients run on the tcgen05 tensor cores (fp32 operands split exactly into three bf16 terms, fp32
+ * accumulation), every other step on CUDA cores.  K in {64, 128}, V in {64, 128, 256} (V = 256 runs as two
+ * 128-wide value slices: dq, dk and dg are accumulated over them); chunk 16, 32, 64 or 128 (tiled at 64 rows,
+ * as for gla_fwd).  workspace: at least gla_bwd_workspace_size() bytes, 256-byte aligned, zeroed before its
+ * first use (status word in its first bytes); it holds the chunk-start states and chunk-end adjoints of one
+ * value slice (2 * chunks * H * K * min(V, 128) fp32).  Outputs must not overlap any input, the workspace or one another.  The
  * library allocates nothing and is stream-ordered.  Errors as for gla_fwd (GLA_ERR_UNSUPPORTED for other
  * dtypes or head sizes); valid domain: the fp32 range of the same mid-chunk factorisation as the fp32
  * forward path.  Returns GLA_OK once enqueued.

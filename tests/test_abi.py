@@ -131,7 +131,8 @@ def bwd(gla, q=A, k=2 * A, v=3 * A, g=4 * A, do=5 * A, scale=0.125, h0=None, dht
 
 
 def test_bwd_rejects_before_any_cuda_work(gla):
-    assert bwd(gla, V=256) == gla.GLA_ERR_UNSUPPORTED                 # value width 256 is forward-only
+    assert bwd(gla, V=512) == gla.GLA_ERR_UNSUPPORTED                 # value widths 64, 128 and 256 only
+    assert bwd(gla, V=192) == gla.GLA_ERR_UNSUPPORTED
     assert bwd(gla, K=96) == gla.GLA_ERR_UNSUPPORTED
     assert bwd(gla, chunk=48) == gla.GLA_ERR_UNSUPPORTED
     assert bwd(gla, dtype=gla.GLA_BF16_OBF16) == gla.GLA_ERR_UNSUPPORTED
@@ -147,7 +148,9 @@ def test_bwd_rejects_before_any_cuda_work(gla):
     assert bwd(gla, dk=8 * A + 256) == gla.GLA_ERR_INVALID_ARG        # dk overlaps dq
     assert bwd(gla, dh0=64 * A) == gla.GLA_ERR_INVALID_ARG            # dh0 overlaps the workspace
     assert bwd(gla, ws=A) == gla.GLA_ERR_INVALID_ARG                  # workspace overlaps inputs
-    assert gla.bwd_workspace_size(1, 100, 2, 64, 256, 1, 64, 1) == 0
+    assert gla.bwd_workspace_size(1, 100, 2, 64, 512, 1, 64, 1) == 0
+    # V = 256 runs as two 128-wide value slices that share one slice's workspace
+    assert gla.bwd_workspace_size(1, 100, 2, 64, 256, 1, 64, 1) == gla.bwd_workspace_size(1, 100, 2, 64, 128, 1, 64, 1)
 
 
 def wy(gla, k=A, v=2 * A, beta=3 * A, Am=4 * A, g=5 * A, w=8 * A, u=9 * A, cu=None, N=2, B=2, T=100, H=2, HV=4,

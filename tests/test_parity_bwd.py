@@ -110,13 +110,35 @@ def test_backward_large_sampled_heads():
     assert all(torch.isfinite(x).all() for x in got)
 
 
+V256_CASES = [
+    # dtype, B, T, H, K, V, h0, dht, varlen lengths: V = 256 runs as two 128-wide value slices
+    ("bf16", 2, 200, 2, 128, 256, True, True, None),                         # tensor-core slices
+    ("bf16", 1, 0, 2, 128, 256, True, True, [1, 63, 64, 65, 0, 130, 300, 2]),
+    ("f32", 1, 130, 2, 64, 256, False, True, None),                           # CUDA-core slices
+]
+
+
+@pytest.mark.parametrize("case", V256_CASES, ids=_id)
+def test_backward_value_width_256(case):
+    """dv, dh0 per 128-wide value slice, dq, dk, dg summed over the slices: every element against the oracle."""
+    d, B, T, H, K, V, h0, dht, lengths = case
+    inp = make_inputs(d, B=B, T=T, H=H, K=K, V=V, h0=h0, lengths=lengths, seed=zlib.crc32(_id(case).encode()) % 1000)
+    do, dh = _grad_inputs(inp, zlib.crc32(_id(case).encode()) % 1000 + 1, dht=dht)
+    _check(_run(inp, do, dh), _oracle(inp, do, dh))
+
+
 def test_backward_rejects_unsupported_value_width():
     from chunkwise_gated_linear_chunked_gb300 import binding
-    inp = make_inputs("bf16", B=1, T=64, H=1, K=128, V=256, h0=False, seed=25)
+    inp = make_inputs("bf16", B=1, T=64, H=1, K=128, V=64, h0=False, seed=25)
     do, _ = _grad_inputs(inp, 26, dht=False)
-    with pytest.raises(binding.GlaError) as e:
-        _run(inp, do, None)
-    assert e.value.code == binding.GLA_ERR_UNSUPPORTED
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    d = lambda x: x.cuda().contiguous()
+    f32 = dict(dtype=torch.float32, device="cuda")
+    out = [torch.empty(1, 64, 1, 512, **f32) for _ in range(4)]
+    rc = binding.bwd_into(d(inp.q), d(inp.k), d(torch.zeros(1, 64, 1, 512, dtype=torch.bfloat16)), d(inp.g),
+                          d(torch.zeros(1, 64, 1, 512, dtype=torch.bfloat16)), inp.scale, None, None, out[0], out[1],
+                          out[2], out[3], None, None, 1, 1, 64, 1, 128, 512, 64, binding.GLA_BF16, ws)
+    assert rc == binding.GLA_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("d,K,V", [("bf16", 128, 128), ("f32", 64, 128)])
