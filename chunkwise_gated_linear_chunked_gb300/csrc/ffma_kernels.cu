@@ -375,14 +375,19 @@ __global__ void __launch_bounds__(256) scan_segments(Args a)
 }
 
 // Varlen plan (one CTA): validate cu_seqlens, give each sequence max(1, ceil(len/L)) slots, fill the
-// slot table and per-sequence (first slot, count).  Invalid offsets: report and leave every slot unused.
+// slot table and per-sequence (first slot, count).  For the tensor-core kernel (a.sms > 0) the segment length
+// follows the pack (see below) and, for up to 1024 sequences, the slots are ordered longest sequence first.
+// Invalid offsets: report and leave every slot unused.
 __global__ void __launch_bounds__(1024) plan_varlen(Args a)
 {
     __shared__ int warp_sums[32];
-    __shared__ int bad;
+    __shared__ long long wsum[32];
+    __shared__ int wmax[32];
+    __shared__ int bad, seg_len;
+    __shared__ int lens[1024];   // ordered plan: the lengths, then the segment counts by rank
     int4 *table = const_cast<int4 *>(a.table);
     int2 *seqinfo = const_cast<int2 *>(a.seqinfo);
-    const int tid = threadIdx.x, N = a.N;
+    const int tid = threadIdx.x, N = a.N, lane = tid & 31, w = tid >> 5, nw = blockDim.x >> 5;
     if (tid == 0)
         bad = (a.cu[0] != 0 || a.cu[N] != a.T) ? 1 : 0;
     __syncthreads();
@@ -399,22 +404,9 @@ __global__ void __launch_bounds__(1024) plan_varlen(Args a)
             seqinfo[n] = make_int2(0, 0);
         return;
     }
-    int base = 0;
-    for (int n0 = 0; n0 < N; n0 += blockDim.x) {
-        const int n = n0 + tid;
-        int cnt = 0, seg = a.L;
-        if (n < N) {
-            const int len = a.cu[n + 1] - a.cu[n];
-            cnt = len > 0 ? (len + a.L - 1) / a.L : 1;
-            if (a.seg_cap > 0 && cnt > a.seg_cap) {
-                // longer segments for this sequence (a multiple of the chunk), at most seg_cap of them
-                seg = ((len + a.seg_cap - 1) / a.seg_cap + kChunk - 1) / kChunk * kChunk;
-                cnt = (len + seg - 1) / seg;
-            }
-        }
-        // block-wide inclusive scan of cnt
+    // exclusive block-wide scan of one int per thread (every thread calls it); returns the total in *total
+    auto block_scan = [&](int cnt, int &total) -> int {
         int x = cnt;
-        const int lane = tid & 31, w = tid >> 5;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -425,7 +417,7 @@ __global__ void __launch_bounds__(1024) plan_varlen(Args a)
             warp_sums[w] = x;
         __syncthreads();
         if (w == 0) {
-            int s = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+            int s = lane < nw ? warp_sums[lane] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, s, o);
@@ -436,15 +428,118 @@ __global__ void __launch_bounds__(1024) plan_varlen(Args a)
         }
         __syncthreads();
         const int incl = x + (w > 0 ? warp_sums[w - 1] : 0);
-        const int first = base + incl - cnt;
+        total = warp_sums[nw - 1];
+        __syncthreads();
+        return incl - cnt;
+    };
+    auto segments = [&](int len, int L, int &seg) {
+        seg = L;
+        int cnt = len > 0 ? (len + L - 1) / L : 1;
+        if (a.seg_cap > 0 && cnt > a.seg_cap) {
+            // longer segments for this sequence (a multiple of the chunk), at most seg_cap of them
+            seg = ((len + a.seg_cap - 1) / a.seg_cap + kChunk - 1) / kChunk * kChunk;
+            cnt = (len + seg - 1) / seg;
+        }
+        return cnt;
+    };
+
+    // Segment length.  Fixed (L rows) unless the tensor-core kernel's SM count is given: then, with the
+    // average load of a CTA in chunks A = (sum of the sequences' chunks) x H x value tiles / SMs, no sequence
+    // is cut when the longest is at most 1.25 A (its one item is then not much longer than an average CTA's
+    // work, and nothing runs a state pass); otherwise segments of about A / 1.7 chunks (a cut segment runs a
+    // state pass as well as its output pass), never shorter than L rows.
+    int L = a.L;
+    if (a.sms > 0) {
+        long long csum = 0;
+        int cmax = 0;
+        for (int n = tid; n < N; n += blockDim.x) {
+            const int len = a.cu[n + 1] - a.cu[n];
+            const int c = len > 0 ? (len + kChunk - 1) / kChunk : 1;
+            csum += c;
+            cmax = max(cmax, c);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            csum += __shfl_xor_sync(0xffffffffu, csum, o);
+            cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+        }
+        if (lane == 0) {
+            wsum[w] = csum;
+            wmax[w] = cmax;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            long long tot = 0;
+            int mx = 0;
+            for (int i = 0; i < nw; ++i) {
+                tot += wsum[i];
+                mx = max(mx, wmax[i]);
+            }
+            const double load = (double)tot * a.H * (a.V / 128) / a.sms;
+            long long lr;
+            if (mx <= 1.25 * load)
+                lr = (long long)mx * kChunk;
+            else
+                lr = max((long long)a.L, (long long)ceil(load / 1.7) * kChunk);
+            seg_len = (int)min(lr, (long long)(a.T > 0 ? (a.T + kChunk - 1) / kChunk * kChunk : kChunk));
+        }
+        __syncthreads();
+        L = max(seg_len, kChunk);
+    }
+
+    if (a.sms > 0 && N <= (int)blockDim.x) {
+        // sequences longest first (ties by index), so that the longest items are claimed in the first wave; the
+        // segments of a sequence stay consecutive and in order (the scan's predecessors are claimed earlier)
+        const int n = tid;
+        const int len = n < N ? a.cu[n + 1] - a.cu[n] : 0;
+        if (n < N)
+            lens[n] = len;
+        __syncthreads();
+        int rank = 0;
+        if (n < N)
+            for (int m = 0; m < N; ++m) {
+                const int lm = lens[m];
+                rank += lm > len || (lm == len && m < n);
+            }
+        int seg = L;
+        const int cnt = n < N ? segments(len, L, seg) : 0;
+        __syncthreads();
+        if (n < N)
+            lens[rank] = cnt;
+        __syncthreads();
+        int total = 0;
+        const int mine = tid < N ? lens[tid] : 0;
+        const int excl = block_scan(mine, total);
+        if (tid < N)
+            lens[tid] = excl;   // first slot of the sequence of rank tid
+        __syncthreads();
+        if (n < N) {
+            const int first = lens[rank];
+            seqinfo[n] = make_int2(first, cnt);
+            const int bos = a.cu[n], eos = a.cu[n + 1];
+            for (int q = 0; q < cnt; ++q)
+                table[first + q] = make_int4(n, q, min(bos + q * seg, eos), min(bos + (q + 1) * seg, eos));
+        }
+        for (int j = total + tid; j < a.J; j += blockDim.x)
+            table[j] = make_int4(-1, 0, 0, 0);
+        return;
+    }
+
+    int base = 0;
+    for (int n0 = 0; n0 < N; n0 += blockDim.x) {
+        const int n = n0 + tid;
+        int cnt = 0, seg = L;
+        if (n < N)
+            cnt = segments(a.cu[n + 1] - a.cu[n], L, seg);
+        int total = 0;
+        const int first = base + block_scan(cnt, total);
         if (n < N) {
             seqinfo[n] = make_int2(first, cnt);
             const int bos = a.cu[n], eos = a.cu[n + 1];
             for (int q = 0; q < cnt; ++q)
                 table[first + q] = make_int4(n, q, min(bos + q * seg, eos), min(bos + (q + 1) * seg, eos));
         }
-        base += warp_sums[(blockDim.x >> 5) - 1];
-        __syncthreads();
+        base += total;
     }
     for (int j = base + tid; j < a.J; j += blockDim.x)
         table[j] = make_int4(-1, 0, 0, 0);

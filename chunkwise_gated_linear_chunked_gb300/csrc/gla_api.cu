@@ -15,23 +15,6 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
-long long l2_bytes()
-{
-    static std::mutex mu;
-    static long long cache[128] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128)
-        return 126LL << 20;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cache[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0)
-            n = 126 << 20;
-        cache[dev] = n;
-    }
-    return cache[dev];
-}
-
 int sm_count()
 {
     static std::mutex mu;
@@ -100,8 +83,9 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
         //    state pass costs more than the wave it would balance);
         //  * otherwise the fewest segments that fill one wave: every item runs at once, so the segment scan
         //    waits only for the state passes, never for a claimed but unstarted predecessor;
-        //  * varlen packs are cut into segments of at most kSegRows rows, which keeps the longest sequences
-        //    from setting the kernel's length while the scan's serial chain stays short.
+        //  * varlen packs: the device plan cuts no sequence when the longest is not much longer than a CTA's
+        //    average load, else segments of about that load (never shorter than kSegRows rows, the bound the
+        //    slot count is sized for), longest sequences first.
         const long long sms = sm_count();
         const long long nv = pl.NV;
         if (varlen) {
@@ -298,6 +282,7 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     a.seg_cap = 0;
     a.hf = hf ? 1 : 0;
     a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.N = N; a.L = pl.L; a.P = pl.P; a.J = pl.J;
+    a.sms = pl.tc && varlen ? sm_count() : 0;   // the tensor-core kernel's varlen plan follows the pack
     a.status = reinterpret_cast<int *>(ws + pl.off_status);
     if (varlen) {
         a.table = reinterpret_cast<const int4 *>(ws + pl.off_table);

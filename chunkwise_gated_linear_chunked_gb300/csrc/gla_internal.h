@@ -40,6 +40,7 @@ struct Args {
     int seg_cap;           // varlen: most segments per sequence (the segment length grows to respect it)
     int hf;                // head-first layout [B, H, T, *] of q, k, v, g, o (dense batches only)
     int lb;                // fused tensor kernel: segments per block of the start-state scan
+    int sms;               // varlen plan for the tensor-core kernel: SM count (0: fixed segments of L rows)
     const int4 *table;     // varlen: per slot {n, p, bos, eos}; n < 0 marks an unused slot
     const int2 *seqinfo;   // varlen: per sequence {first slot, slot count}
     float *ss;             // CUDA cores: [J][H][K][V] segment contributions, then segment start states;
