@@ -100,6 +100,21 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
                 L = 4 * C;
             if (L > whole)
                 L = whole;
+            // Balanced pieces: when the units do not divide the CTAs evenly, equal segments per unit leave
+            // sms % units1 CTAs idle and every CTA waits as long as the longest segment.  Instead the B*H
+            // units' chunks, taken in order, are cut into sms / NV near-equal pieces (one CTA each, per value
+            // tile); a piece crossing from one unit into the next is two segments run by one CTA.  Worth it
+            // for long pieces only (every extra segment of a unit adds a tile to the segment scan), and only
+            // when the longest CTA's load drops by a tenth; a chunk of a state pass costs about 0.41 of an
+            // output chunk (it reads k, g, v at the HBM rate).
+            const long long units = (long long)B * H, nc = (T + C - 1) / C, np = sms / nv;
+            const double seg_load = (L < T ? 1.41 : 1.0) * (double)(L / C);
+            const double piece_load = 1.41 * (double)(units * nc) / (double)np;
+            if (units1 < sms && units < np && np % units != 0 && units * nc >= kPieceChunks * np &&
+                piece_load < 0.9 * seg_load) {
+                pl.np = (int)np;
+                pl.nc = (int)nc;
+            }
         }
     } else if (base < target && rows > 0) {
         long long per = (rows * H * pl.NV + target - 1) / target;   // rows per CTA
@@ -115,6 +130,16 @@ void make_plan(Plan &pl, int B, int T, int H, int K, int V, int N, int chunk, in
         pl.P = 0;
         pl.J = N + (int)((T + L - 1) / L);
         pl.multi = L < T;
+    } else if (pl.np) {
+        // most segments of one unit: the pieces it overlaps
+        const long long tot = (long long)B * H * pl.nc;
+        auto piece_of = [&](long long x) { return ((x + 1) * pl.np + tot - 1) / tot - 1; };
+        long long most = 1;
+        for (long long U = 0; U < (long long)B * H; ++U)
+            most = std::max(most, piece_of((U + 1) * pl.nc - 1) - piece_of(U * pl.nc) + 1);
+        pl.P = (int)most;
+        pl.J = B * pl.P;
+        pl.multi = pl.P > 1;
     } else {
         pl.P = T > 0 ? (int)((T + L - 1) / L) : 1;
         pl.J = B * pl.P;
@@ -283,6 +308,8 @@ extern "C" int gla_fwd(const void *q, const void *k, const void *v, const void *
     a.hf = hf ? 1 : 0;
     a.B = B; a.T = T; a.H = H; a.K = K; a.V = V; a.N = N; a.L = pl.L; a.P = pl.P; a.J = pl.J;
     a.sms = pl.tc && varlen ? sm_count() : 0;   // the tensor-core kernel's varlen plan follows the pack
+    a.np = pl.np;
+    a.nc = pl.nc;
     a.status = reinterpret_cast<int *>(ws + pl.off_status);
     if (varlen) {
         a.table = reinterpret_cast<const int4 *>(ws + pl.off_table);

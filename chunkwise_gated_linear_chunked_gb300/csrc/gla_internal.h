@@ -11,6 +11,7 @@ namespace gla {
 
 constexpr int kChunk = 64;          // chunk length C (rows per intra-chunk tile)
 constexpr int kSegRows = 2048;      // varlen packs: most rows of one segment on the tensor-core path
+constexpr int kPieceChunks = 16;    // dense balanced pieces: fewest chunks of a piece
 
 // One forward call's launch plan.  Segments of L rows (L a multiple of the chunk) split each sequence
 // so that long sequences with few heads still fill the GPU; a "slot" is one (sequence, segment) pair and
@@ -19,8 +20,11 @@ struct Plan {
     int B, T, H, K, V, N, chunk, dtype;
     bool varlen;
     int L;        // segment length in rows (multiple of chunk)
-    int P;        // dense: segments per sequence (>= 1); varlen: 0 (per sequence, from the plan kernel)
+    int P;        // dense: segments per sequence (>= 1), or per (sequence, head) unit with pieces;
+                  // varlen: 0 (per sequence, from the plan kernel)
     int J;        // slots: exact (dense) or an upper bound (varlen)
+    int np;       // dense, tensor cores: the units' chunks cut into np balanced pieces (0: segments of L)
+    int nc;       // chunks per sequence (pieces only)
     bool multi;   // some sequence may span more than one segment: state + scan passes are needed
     bool tc;      // tensor-core path (bf16 inputs, K == 128, V multiple of 128)
     int BV, NV;   // value-tile width and count (64 on CUDA cores, 128 on tensor cores)
@@ -41,6 +45,7 @@ struct Args {
     int hf;                // head-first layout [B, H, T, *] of q, k, v, g, o (dense batches only)
     int lb;                // fused tensor kernel: segments per block of the start-state scan
     int sms;               // varlen plan for the tensor-core kernel: SM count (0: fixed segments of L rows)
+    int np, nc;            // dense balanced pieces (tensor cores): piece count (0: off), chunks per sequence
     const int4 *table;     // varlen: per slot {n, p, bos, eos}; n < 0 marks an unused slot
     const int2 *seqinfo;   // varlen: per sequence {first slot, slot count}
     float *ss;             // CUDA cores: [J][H][K][V] segment contributions, then segment start states;

@@ -232,6 +232,40 @@ struct Item {
     bool last;
 };
 
+// Balanced pieces (dense batches): the chunks of the B*H (sequence, head) units, unit after unit, cut into np
+// pieces at chunk c * tot / np (rounded down), tot = B*H*nc.  A unit's segment p is its part of the p-th
+// piece that overlaps it; a piece is shorter than a unit, so it overlaps at most two.
+__device__ __forceinline__ long long piece_bnd(const Args &a, long long c, long long tot)
+{
+    return c * tot / a.np;
+}
+// the piece holding global chunk x
+__device__ __forceinline__ long long piece_of(const Args &a, long long x, long long tot)
+{
+    return ((x + 1) * a.np + tot - 1) / tot - 1;
+}
+
+// Slot j of head h: sequence n, segment p, rows [bos, eos) and the sequence end; false for an unused slot.
+__device__ __forceinline__ bool resolve_item(const Args &a, int j, int h, int &n, int &p, int &bos, int &eos,
+                                             int &send)
+{
+    if (!a.np)
+        return resolve_slot(a, j, n, p, bos, eos, send);
+    n = j / a.P;
+    p = j - n * a.P;
+    const long long tot = (long long)a.B * a.H * a.nc;
+    const long long u0 = ((long long)n * a.H + h) * a.nc, u1 = u0 + a.nc;
+    const long long c0 = piece_of(a, u0, tot);
+    const long long s0 = max(u0, piece_bnd(a, c0 + p, tot)), s1 = min(u1, piece_bnd(a, c0 + p + 1, tot));
+    if (s0 >= s1)
+        return false;
+    const int sb = n * a.T;
+    send = sb + a.T;
+    bos = sb + (int)(s0 - u0) * C;
+    eos = min(sb + (int)(s1 - u0) * C, send);
+    return true;
+}
+
 // What the start-state scan needs from the kernel (shared-memory words, barriers, the launch epoch).
 struct ChainCtx {
     const float *h0;
@@ -562,7 +596,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         it.vt = rem - it.h * NV;
         it.v0 = it.vt * VT;
         int send;
-        if (!resolve_slot(a, it.j, it.n, it.p, it.bos, it.eos, send))
+        if (!resolve_item(a, it.j, it.h, it.n, it.p, it.bos, it.eos, send))
             return false;   // unused varlen slot (every role sees the same)
         it.nchunks = (it.eos - it.bos + C - 1) / C;
         it.last = it.eos == send;
@@ -633,23 +667,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 qbase += n;
                 return true;
             };
-            int itn = 0, nac = 0;
+            // claim w: work item w, or with balanced pieces the one or two segments of piece w / NV (a
+            // piece crossing into the next unit runs that unit's first segment first: its end state is
+            // published early, and the previous unit's last segment then finds its start state ready)
+            const long long tot = (long long)a.B * H * a.nc;
+            auto claim = [&](int w, int (&us)[2]) -> int {
+                if (w < 0 || w >= nitems)
+                    return 0;
+                if (!a.np) {
+                    us[0] = w;
+                    return 1;
+                }
+                const int c = w / NV, vt = w - c * NV;
+                const long long ua = piece_bnd(a, c, tot) / a.nc, ub = (piece_bnd(a, c + 1, tot) - 1) / a.nc;
+                auto id = [&](long long unit, long long p) {
+                    const int n = (int)(unit / H), h = (int)(unit - (long long)n * H);
+                    return ((n * a.P + (int)p) * H + h) * NV + vt;
+                };
+                int m = 0;
+                if (ub != ua)
+                    us[m++] = id(ub, 0);
+                us[m++] = id(ua, c - piece_of(a, ua * a.nc, tot));
+                return m;
+            };
+            int itn = 0, nac = 0, k = 0;
             bool ok = true;
-            for (int k = 0;; ++k) {
-                if (k >= IQ && !(ok = bar_wait(&item_empty[k % IQ], ((k / IQ) - 1) & 1, abort_w)))
-                    break;
-                int u = *abort_w ? -1 : atomicAdd(a.ctr + 0, 1);
-                if (u >= nitems)
-                    u = -1;
-                iq[k % IQ] = u;
-                bar_arrive(&item_full[k % IQ]);
-                if (u < 0)
-                    break;
-                Item cur;
-                if (!decode(u, cur, itn, nac))
-                    continue;
-                if (!(ok = load(cur, false) && load(cur, true)))
-                    break;
+            for (bool more = true; more && ok;) {
+                int us[2];
+                const int m = claim(*abort_w ? -1 : atomicAdd(a.ctr + 0, 1), us);
+                more = m > 0;
+                for (int i = 0; i < (more ? m : 1) && ok; ++i, ++k) {
+                    if (k >= IQ && !(ok = bar_wait(&item_empty[k % IQ], ((k / IQ) - 1) & 1, abort_w)))
+                        break;
+                    const int u = more ? us[i] : -1;
+                    iq[k % IQ] = u;
+                    bar_arrive(&item_full[k % IQ]);
+                    Item cur;
+                    if (u >= 0 && decode(u, cur, itn, nac))
+                        ok = load(cur, false) && load(cur, true);
+                }
             }
             if (!ok)
                 fail();
@@ -1221,7 +1277,8 @@ cudaError_t launch_fused_t(const Plan &pl, const Args &a, cudaStream_t s, int sm
             return e;
         attr_set.fetch_or(bit, std::memory_order_release);
     }
-    int nitems = pl.J * pl.H * (pl.V / VT);
+    // work claims: items, or pieces per value tile
+    int nitems = pl.np ? pl.np * (pl.V / VT) : pl.J * pl.H * (pl.V / VT);
     // scan block length: when every item runs at once the chain of end-state publications is the critical
     // path, so only every 8th segment publishes one; with several waves a block of 2 halves the chain of
     // dependent publications for one extra tile read on every other segment

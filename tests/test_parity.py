@@ -89,6 +89,33 @@ def test_segment_scan_all_heads(case):
     assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
 
 
+# Balanced pieces of the tensor-core path: on a 152-SM GB300, dense batches whose (sequence, head) units do
+# not divide the CTAs evenly, with long enough pieces, are cut into 152 / NV near-equal pieces of the units'
+# chunks taken in order; a piece that crosses from one unit into the next runs the next unit's first
+# segment, then the previous unit's last.  40 heads of 4096 rows: 5 segments per head at most, 40 pieces
+# crossing a head boundary; 33 heads of 5000 rows (ragged last chunk); 3 sequences of 13 heads (pieces
+# crossing sequence boundaries); 20 heads with V = 256 (76 pieces per value tile).
+PIECE_CASES = [
+    ("bf16", 1, 4096, 40, 128, 128, False, None),
+    ("bf16", 1, 5000, 33, 128, 128, True, None),
+    ("bf16", 3, 4096, 13, 128, 128, True, None),
+    ("bf16", 1, 8192, 20, 128, 256, True, None),
+    ("f16", 1, 5000, 33, 128, 128, True, None),
+]
+
+
+@pytest.mark.parametrize("case", PIECE_CASES, ids=_case_id)
+def test_balanced_pieces_all_heads(case):
+    d, B, T, H, K, V, h0, lengths = case
+    inp = make_inputs(d, B=B, T=T, H=H, K=K, V=V, h0=h0, lengths=lengths, seed=zlib.crc32(_case_id(case).encode()) % 1000)
+    o, ht = run_gpu(inp)
+    o_ref, ht_ref = run_oracle(inp)
+    assert_close(as_f64(o), o_ref, TOL[d], "o")
+    assert_close(as_f64(ht), ht_ref, TOL[d], "ht")
+    o2, ht2 = run_gpu(inp)   # the result does not depend on which CTA took which piece
+    assert torch.equal(o, o2) and torch.equal(ht, ht2)
+
+
 @pytest.mark.parametrize("chunk", [16, 32, 128])
 def test_chunk_argument_selects_same_tiling(chunk):
     """chunk is accepted as 16, 32, 64 or 128; the kernels tile at 64 rows, so the result is the same."""
@@ -240,6 +267,7 @@ def test_tensor_core_range_check_reports_status():
 
 HEAD_FIRST_CASES = [
     ("bf16", 2, 200, 3, 128, 128, True, None),    # tensor-core path, ragged chunk
+    ("bf16", 3, 4096, 13, 128, 128, True, None),  # balanced pieces crossing heads and sequences
     ("bf16", 1, 3000, 2, 128, 256, True, None),   # segments + scan, V = 256
     ("f16", 2, 130, 2, 128, 128, False, None),
     ("f32", 2, 200, 2, 64, 64, True, None),       # CUDA-core path
@@ -290,6 +318,7 @@ def test_head_first_varlen(case):
 GF32_CASES = [
     ("bf16", 2, 200, 2, 128, 128, True, None),      # tensor-core path (two 80 KB stages)
     ("f16", 1, 3000, 1, 128, 256, True, None),      # tensor-core path, segments + scan, V = 256
+    ("bf16", 1, 5000, 33, 128, 128, True, None),    # tensor-core path, balanced pieces
     ("bf16", 1, 0, 2, 128, 128, True, [1, 63, 64, 65, 0, 130, 300, 2]),   # tensor-core path, varlen
     ("f16", 1, 3000, 1, 64, 128, True, None),       # K = 64: CUDA-core path
     ("bf16", 1, 0, 2, 64, 64, True, [1, 63, 64, 65, 0, 130, 300, 2]),
