@@ -91,8 +91,9 @@ struct Ring {
     static constexpr int OFF_EG = OFF_P + 8192;           // per output chunk (index mod 4): e[128], cl[128]
     static constexpr int OFF_PS = OFF_EG + 4 * 1024;      // gating partial sums [2][4][128]
     static constexpr int OFF_GT = OFF_PS + 4096;          // segment decay (log2) per key, [4][128] by state-pass item
-    static constexpr int OFF_WL = OFF_GT + 2048;          // look-back: running log2 weight per key, [128]
-    static constexpr int OFF_CL = OFF_WL + 512;           // state group: exp(G_last - G_a) of an item's last chunk
+    static constexpr int OFF_WL = OFF_GT + 2048;          // look-back: running log2 weight per key, [128], its
+                                                          // power of two [128], the segment decay factor [128]
+    static constexpr int OFF_CL = OFF_WL + 1536;          // state group: exp(G_last - G_a) of an item's last chunk
     static constexpr int OFF_MISC = OFF_CL + 1024;        // [0..3] item queue, [4] abort word, [5] look-back flag
     static constexpr int OFF_BAR = OFF_MISC + 64;
     static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16 + 1024;
@@ -298,7 +299,7 @@ __device__ __noinline__ bool chain_scan(const ChainCtx &a, const Item &it, int u
     const int tid = threadIdx.x, warp = tid >> 5;
     const uint32_t tmem = cx.tmem, tag = cx.tag;
     const int H = cx.H, NV = cx.NV, V = cx.V;
-    float *wl = cx.wl;
+    float *wl = cx.wl, *ew = cx.wl + 128, *eg = cx.wl + 256;
     volatile int *misc = cx.misc;
     volatile int *abort_w = misc + 4;
     uint64_t *g_done = cx.g_done, *a_done = cx.a_done;
@@ -355,20 +356,28 @@ __device__ __noinline__ bool chain_scan(const ChainCtx &a, const Item &it, int u
     }
     const int p0 = p > 0 ? (p - 1) / a.lb * a.lb : 0;
     if (p > 0) {
-        if (b < 64)
+        // the predecessors publish at about the same time: wait for all of them first, newest first, then
+        // read each tile with a thread's 64 keys in flight at once
+        if (leader) {
+            int okf = 1;
+            for (int i = p - 1; i > p0 && okf; --i)
+                okf = flag_wait_tag(a.flags + (u - (p - i) * HN), tag, 1, abort_w);
+            misc[5] = okf ? flag_wait_tag(a.flags + (u - (p - p0) * HN), tag, 2, abort_w) : 0;
+        }
+        if (b < 64) {
             wl[kb0 + b] = 0.f;
+            ew[kb0 + b] = 1.f;
+        }
+        sync_team();
+        if (misc[5] == 0)
+            return false;   // uniform: every thread read the same value
         for (int i = p - 1; i > p0; --i) {
             const int back = p - i;
-            if (leader)
-                misc[5] = flag_wait_tag(a.flags + (u - back * HN), tag, 1, abort_w);
-            sync_team();
-            if (misc[5] == 0)
-                return false;   // uniform: every thread read the same value
             const size_t ti = mine - (size_t)back * HN;
             const float4 *src = reinterpret_cast<const float4 *>(a.agg + ti * tile);
             const float gi = b < 64 ? __ldcg(a.gtot + ti * KD + kb0 + b) : 0.f;
+            sync_team();   // the weights of this step are in place
             for (int sub = 0; sub < 2; ++sub) {
-                // 32 keys of loads in flight, consumed 16 TMEM columns at a time
                 const int k0 = kb0 + 32 * sub;
                 float4 x[8];
 #pragma unroll
@@ -388,91 +397,87 @@ __device__ __noinline__ bool chain_scan(const ChainCtx &a, const Item &it, int u
                     }
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
-                        const float4 e = *reinterpret_cast<const float4 *>(wl + k1 + 4 * w);
+                        const float4 e = *reinterpret_cast<const float4 *>(ew + k1 + 4 * w);
                         const float4 xv = x[4 * hh + w];
-                        r[4 * w] = __float_as_uint(fmaf(ex2(e.x), xv.x, __uint_as_float(r[4 * w])));
-                        r[4 * w + 1] = __float_as_uint(fmaf(ex2(e.y), xv.y, __uint_as_float(r[4 * w + 1])));
-                        r[4 * w + 2] = __float_as_uint(fmaf(ex2(e.z), xv.z, __uint_as_float(r[4 * w + 2])));
-                        r[4 * w + 3] = __float_as_uint(fmaf(ex2(e.w), xv.w, __uint_as_float(r[4 * w + 3])));
+                        r[4 * w] = __float_as_uint(fmaf(e.x, xv.x, __uint_as_float(r[4 * w])));
+                        r[4 * w + 1] = __float_as_uint(fmaf(e.y, xv.y, __uint_as_float(r[4 * w + 1])));
+                        r[4 * w + 2] = __float_as_uint(fmaf(e.z, xv.z, __uint_as_float(r[4 * w + 2])));
+                        r[4 * w + 3] = __float_as_uint(fmaf(e.w, xv.w, __uint_as_float(r[4 * w + 3])));
                     }
                     tmem_st16(tmem + lrow + TM_SOP + k1, r);
                 }
             }
             tmem_wait_st();
             sync_team();   // every thread has used this step's weights
-            if (b < 64)
-                wl[kb0 + b] += gi;
+            if (b < 64) {
+                const float w1 = wl[kb0 + b] + gi;
+                wl[kb0 + b] = w1;
+                ew[kb0 + b] = ex2(w1);
+            }
         }
-        // the end state of the block's boundary segment
-        if (leader)
-            misc[5] = flag_wait_tag(a.flags + (u - (p - p0) * HN), tag, 2, abort_w);
-        sync_team();
-        if (misc[5] == 0)
-            return false;
     }
     // S_in -> TMEM state buffer; a boundary segment with a state pass publishes S_out = 2^Gtot * S_in + dS
     const bool acc = p - 1 > p0;   // contributions were summed into the S' columns
     const bool pub = it.nA > 0 && boundary;
     const float4 *bsrc = reinterpret_cast<const float4 *>(a.ss + (mine - (size_t)(p - p0) * HN) * tile);
     float4 *bdst = reinterpret_cast<float4 *>(a.ss + mine * tile);
-#pragma unroll 1
-    for (int sp = 0; sp < 2; ++sp) {
-        float4 xa[4], xc[4];
+    float4 xb[16];
+    if (p > 0) {
+        // the boundary's end state, 64 keys in flight
+#pragma unroll
+        for (int w = 0; w < 16; ++w)
+            xb[w] = __ldcg(bsrc + (size_t)(kb0 / 4 + w) * VT + b);
+    }
+    if (pub && b < 64)
+        eg[kb0 + b] = ex2(gts[kb0 + b]);
+    if (p > 0 || pub)
+        sync_team();   // the last step's weights (and the segment's decay factors) are in place
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {
+        const int k1 = kb0 + 16 * hh;
+        uint32_t sn[16];
         if (p > 0) {
-            // 32 keys of the boundary's end state in flight
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                xa[w] = __ldcg(bsrc + (size_t)((kb0 + 32 * sp) / 4 + w) * VT + b);
-                xc[w] = __ldcg(bsrc + (size_t)((kb0 + 32 * sp) / 4 + 4 + w) * VT + b);
-            }
-        }
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-            const int k1 = kb0 + 32 * sp + 16 * hh;
-            uint32_t sn[16];
-            if (p > 0) {
-                if (acc) {
-                    tmem_ld16(tmem + lrow + TM_SOP + k1, sn);
-                    tmem_wait_ld(sn);
-                } else {
-#pragma unroll
-                    for (int uu = 0; uu < 16; ++uu)
-                        sn[uu] = 0u;
-                }
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float4 e = *reinterpret_cast<const float4 *>(wl + k1 + 4 * w);
-                    const float4 xv = hh ? xc[w] : xa[w];
-                    sn[4 * w] = __float_as_uint(fmaf(ex2(e.x), xv.x, __uint_as_float(sn[4 * w])));
-                    sn[4 * w + 1] = __float_as_uint(fmaf(ex2(e.y), xv.y, __uint_as_float(sn[4 * w + 1])));
-                    sn[4 * w + 2] = __float_as_uint(fmaf(ex2(e.z), xv.z, __uint_as_float(sn[4 * w + 2])));
-                    sn[4 * w + 3] = __float_as_uint(fmaf(ex2(e.w), xv.w, __uint_as_float(sn[4 * w + 3])));
-                }
-            } else if (h0pre) {
+            if (acc) {
                 tmem_ld16(tmem + lrow + TM_SOP + k1, sn);
                 tmem_wait_ld(sn);
-            } else if (a.h0) {
-#pragma unroll
-                for (int uu = 0; uu < 16; ++uu)
-                    sn[uu] = __float_as_uint(__ldcg(a.h0 + soff + (size_t)(k1 + uu) * V));
             } else {
 #pragma unroll
                 for (int uu = 0; uu < 16; ++uu)
                     sn[uu] = 0u;
             }
-            if (pub) {
-                uint32_t r[16];
-                tmem_ld16(tmem + lrow + sb + k1, r);
-                tmem_wait_ld(r);
 #pragma unroll
-                for (int uu = 0; uu < 16; ++uu)
-                    r[uu] = __float_as_uint(fmaf(ex2(gts[k1 + uu]), __uint_as_float(sn[uu]), __uint_as_float(r[uu])));
-#pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    __stcg(bdst + (size_t)(k1 / 4 + w) * VT + b, f4(r + 4 * w));
+            for (int w = 0; w < 4; ++w) {
+                const float4 e = *reinterpret_cast<const float4 *>(ew + k1 + 4 * w);
+                const float4 xv = xb[4 * hh + w];
+                sn[4 * w] = __float_as_uint(fmaf(e.x, xv.x, __uint_as_float(sn[4 * w])));
+                sn[4 * w + 1] = __float_as_uint(fmaf(e.y, xv.y, __uint_as_float(sn[4 * w + 1])));
+                sn[4 * w + 2] = __float_as_uint(fmaf(e.z, xv.z, __uint_as_float(sn[4 * w + 2])));
+                sn[4 * w + 3] = __float_as_uint(fmaf(e.w, xv.w, __uint_as_float(sn[4 * w + 3])));
             }
-            tmem_st16(tmem + lrow + sb + k1, sn);
+        } else if (h0pre) {
+            tmem_ld16(tmem + lrow + TM_SOP + k1, sn);
+            tmem_wait_ld(sn);
+        } else if (a.h0) {
+#pragma unroll
+            for (int uu = 0; uu < 16; ++uu)
+                sn[uu] = __float_as_uint(__ldcg(a.h0 + soff + (size_t)(k1 + uu) * V));
+        } else {
+#pragma unroll
+            for (int uu = 0; uu < 16; ++uu)
+                sn[uu] = 0u;
         }
+        if (pub) {
+            uint32_t r[16];
+            tmem_ld16(tmem + lrow + sb + k1, r);
+            tmem_wait_ld(r);
+#pragma unroll
+            for (int uu = 0; uu < 16; ++uu)
+                r[uu] = __float_as_uint(fmaf(eg[k1 + uu], __uint_as_float(sn[uu]), __uint_as_float(r[uu])));
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                __stcg(bdst + (size_t)(k1 / 4 + w) * VT + b, f4(r + 4 * w));
+        }
+        tmem_st16(tmem + lrow + sb + k1, sn);
     }
     tmem_wait_st();
     fence_before();
