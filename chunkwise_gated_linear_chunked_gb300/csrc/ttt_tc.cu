@@ -7,23 +7,24 @@
 //   h   -= eta_last sum_j k_j^T v2_j,   hb -= eta_last sum_j v2_j
 //
 // One CTA per (sequence, head).  The state lives in TMEM, transposed and in fp32: lane m holds column m of
-// h (h^T[m][.]).  Per mini-batch:
-//   * h^T is split into two bf16 terms (h = h1 + h2 + e, |e| <= 2^-17 |h|, each term cut by integer
-//     rounding), written back to TMEM as the 16-bit A operand of the products [k h, q h]^T = h^T [k; q]^T
-//     (tcgen05 kind::f16, M = 128, N = 2 BT, K = D; k and q are exact in bf16); q k^T comes from one more
-//     product with the same shared-memory tile of [k; q] rows;
-//   * the rows' LayerNorm statistics and the two gradient sums are taken over the 128 lanes (four warps
-//     of 32, merged through shared memory);
-//   * the update h^T += (-eta_last v2)^T k is one more product accumulating into the fp32 state: -eta_last v2
-//     split exactly into three bf16 terms (MN-major A) times the k rows of the same tile (MN-major B),
-//     M = N = D, K = BT, so the state itself is never rewritten by the CUDA cores and carries no split error;
-//   * the outputs of a mini-batch (which the state chain does not need) are formed by a second group of warps
-//     one mini-batch behind: its q h columns, scores, v2 and learning rates are kept in buffers by parity,
-//     handed over and released through mbarriers, so the output LayerNorm runs beside the next mini-batch's
-//     state chain.
-// The next mini-batch's k, q, v rows and learning rates arrive by asynchronous copies while the current one
-// runs.  Rows past the end of a sequence are zero in k and q and take no part in the update (as the CUDA-core
-// path).
+// h (h^T[m][.]).  The serial chain of mini-batches never waits for a product of the state: with W_t =
+// -eta_last v2_t (the update h_{t+1} = h_t + k_t^T W_t),
+//   k_t h_t = k_t h_{t-1} + (k_t k_{t-1}^T) W_{t-1},
+// so k_t h_{t-1} is taken one mini-batch ahead, and the chain adds the correction on the CUDA cores (a
+// BT x BT by BT product per row) once W_{t-1} is known.  Per mini-batch t:
+//   * the split warps (which also form the outputs) cut h_t into two bf16 terms as soon as the update that
+//     made it is complete (h = h1 + h2 + e, |e| <= 2^-17 |h|, each term cut by integer rounding);
+//   * one issuing thread then takes h_t^T [q_t; k_{t+1}]^T (tcgen05 kind::f16, A the two terms from TMEM,
+//     M = 128, N = 2 BT, K = D: the outputs' q h and the next mini-batch's k h_t) and the row products of the
+//     tile [k_t; q_t; k_{t+1}] with k_t (q k^T for the outputs, k_{t+1} k_t^T for the next correction);
+//   * the chain warps take the rows' LayerNorm statistics and the two gradient sums over the 128 lanes (four
+//     warps of 32, merged through shared memory) and v2_t; -eta_last v2_t is split exactly into three bf16
+//     terms (MN-major A) and the update h^T += W^T k is one more product accumulating into the fp32 state
+//     (B: the k rows of the tile, MN-major), so the state itself is never rewritten by the CUDA cores;
+//   * the outputs of a mini-batch are formed one mini-batch behind from its q h columns, scores, v2 and
+//     learning rates, kept in buffers by parity and released through mbarriers.
+// Rows arrive by asynchronous copies two mini-batches ahead (three tiles in turn); rows past the end of a
+// sequence are zero in k and q and take no part in the update (as the CUDA-core path).
 #include <cuda_bf16.h>
 
 #include "gla_internal.h"
@@ -34,28 +35,32 @@ namespace gla {
 namespace {
 
 constexpr int D = 128;
-constexpr int NTH = 512;   // warps 0-7: the state chain; warps 8-15: the outputs (lane quadrant x row half)
+constexpr int NTH = 544;   // warps 0-7: the chain; 8-15: the state split and the outputs; 16: the MMA issue
 
 template <int BT>
 struct TtcLayout {
-    static constexpr int XH = 2 * BT * 128;          // one 64-feature half of the [k; q] tile (2 BT rows)
-    static constexpr int XB = 2 * XH;                // one [k; q] tile
-    static constexpr int X0 = 0;                     // [2] [k; q] tiles (K-major, 128-byte swizzle), by parity
-    static constexpr int VR = X0 + 2 * XB;           // [2][BT][D] raw v rows (bf16)
-    static constexpr int V2T = VR + 2 * BT * D * 2;  // [3] terms of -eta_last v2, MN-major: [BT rows][2 halves]
+    static constexpr int XH = 3 * BT * 128;          // one 64-feature half of a tile [k_t; q_t; k_{t+1}]
+    static constexpr int XB = 2 * XH;                // one tile
+    static constexpr int X0 = 0;                     // [3] tiles (K-major, 128-byte swizzle), by mini-batch mod 3
+    static constexpr int VR = X0 + 3 * XB;           // [3][BT][D] raw v rows (bf16), likewise
+    static constexpr int V2T = VR + 3 * BT * D * 2;  // [3] terms of -eta_last v2, MN-major: [BT rows][2 halves]
     static constexpr int V2H = BT * 128;             // one 64-column half of a term
     static constexpr int V2F = V2T + 3 * 2 * V2H;    // [2][BT][D] v2 fp32, by parity
     static constexpr int AS = V2F + 2 * BT * D * 4;  // [2][BT][BT] q k^T (unscaled), by parity
-    static constexpr int RED = AS + 2 * BT * BT * 4; // [4 quadrants][BT][2] per-row partial statistics
-    static constexpr int ET = RED + 4 * BT * 2 * 4;  // [2][BT] learning rates (0 past the end), by parity
-    static constexpr int E2 = ET + 2 * BT * 4;       // [2][BT + 1] the outputs' learning rates and eta_last
+    static constexpr int KK = AS + 2 * BT * BT * 4;  // [2][BT][BT] k_{t+1} k_t^T, by parity of t
+    static constexpr int RED = KK + 2 * BT * BT * 4; // [2 (statistics, gradient sums)][4 quadrants][BT][2]
+    static constexpr int ET = RED + 2 * 4 * BT * 2 * 4;  // [3][BT] learning rates (0 past the end)
+    static constexpr int E2 = ET + 3 * BT * 4;       // [2][BT + 1] the outputs' learning rates and eta_last
     static constexpr int RED2 = E2 + 2 * (BT + 4) * 4;   // [4][BT][2] the output warps' partial statistics
-    static constexpr int BAR = RED2 + 4 * BT * 2 * 4;    // mma, v2_full[2], out_free[2], TMEM address, abort
-    // the q k^T product reads rows 0..127 of the tile with K-halves XH apart: keep that span allocated
-    static constexpr int END = BAR + 64 > X0 + XB + XH + 128 * 128 ? BAR + 64 : X0 + XB + XH + 128 * 128;
+    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2]; TMEM address; abort word
+    static constexpr int BAR = RED2 + 4 * BT * 2 * 4;
+    // the row products read rows 0..127 of a tile with K-halves XH apart: keep that span allocated
+    static constexpr int END = BAR + 96 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 96 : X0 + 2 * XB + XH + 128 * 128;
     static constexpr int BYTES = END + 1024;
-    // TMEM columns: the state, its two bf16 terms (64 columns each), [k h, q h]^T and q k^T by parity
+    // TMEM columns: the state, its two bf16 terms (64 columns each), [q h_t, k_{t+1} h_t]^T by parity, the row
+    // products by parity
     static constexpr uint32_t HT = 0, HS = 128, DA = 256, DC = 384, COLS = 512;
+    static_assert(VR % 1024 == 0 && V2T % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 };
 
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
@@ -138,6 +143,105 @@ __device__ __forceinline__ void merge4(const float *red, int BT, int i, float ep
     rstd = rsqrtf(fmaf(s, 1.f / D, eps));
 }
 
+// Reduce-scatter over the warp: every lane brings V values (V = 16 or 32); lane l ends with the sum over the
+// 32 lanes of value q = l >> (V == 16 ? 1 : 0) (with V = 16, lanes 2q and 2q + 1 hold the same sum).  Halving
+// the values at each exchange takes V - 1 shuffles where V separate sums would take 5 V.
+template <int V>
+__device__ __forceinline__ float warp_rs(float (&v)[V], int lane)
+{
+    int o = 16;
+#pragma unroll
+    for (int n = V; n > 1; n >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < n / 2; ++k) {
+            const float keep = up ? v[n / 2 + k] : v[k], send = up ? v[k] : v[n / 2 + k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (; o > 0; o >>= 1)
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+// This warp's (mean, M2) over its 32 lanes of each of HB rows (x[u] belongs to row r0 + u) into
+// red[(qd BT + r0 + u) 2 + {0, 1}]: the sums of d = x - s (s the row's value in lane 0, so that the sum of
+// squares does not cancel) and of d^2, reduce-scattered; one lane per row writes.
+template <int HB>
+__device__ __forceinline__ void warp_row_stats(const float (&x)[HB], float *red, int qd, int BT, int r0, int lane)
+{
+    constexpr int V = 2 * HB, SH = V == 16 ? 1 : 0;
+    float v[V], s[HB];
+#pragma unroll
+    for (int u = 0; u < HB; ++u) {
+        s[u] = __shfl_sync(0xffffffffu, x[u], 0);
+        const float d = x[u] - s[u];
+        v[2 * u] = d;
+        v[2 * u + 1] = d * d;
+    }
+    const float tot = warp_rs<V>(v, lane);
+    const float sq = __shfl_xor_sync(0xffffffffu, tot, 1 << SH);   // the row's sum of squares (odd q)
+    const int q = lane >> SH, u = q >> 1;
+    float su = 0.f;
+#pragma unroll
+    for (int w = 0; w < HB; ++w)
+        su = w == u ? s[w] : su;
+    if ((q & 1) == 0 && (lane & ((1 << SH) - 1)) == 0) {
+        red[(qd * BT + r0 + u) * 2] = fmaf(tot, 1.f / 32, su);
+        red[(qd * BT + r0 + u) * 2 + 1] = fmaf(-tot, tot * (1.f / 32), sq);
+    }
+}
+// This warp's sums over its 32 lanes of a[u] and b[u] (row r0 + u) into red[(qd BT + r0 + u) 2 + {0, 1}].
+template <int HB>
+__device__ __forceinline__ void warp_row_sums(const float (&a)[HB], const float (&b)[HB], float *red, int qd, int BT,
+                                              int r0, int lane)
+{
+    constexpr int V = 2 * HB, SH = V == 16 ? 1 : 0;
+    float v[V];
+#pragma unroll
+    for (int u = 0; u < HB; ++u) {
+        v[2 * u] = a[u];
+        v[2 * u + 1] = b[u];
+    }
+    const float tot = warp_rs<V>(v, lane);
+    const int q = lane >> SH;
+    if ((lane & ((1 << SH) - 1)) == 0)
+        red[(qd * BT + r0 + (q >> 1)) * 2 + (q & 1)] = tot;
+}
+// mean and 1 / sqrt(var + eps) of rows r0 .. r0 + HB - 1 over the four quadrants: lane u merges row r0 + u,
+// then every lane takes all HB rows
+template <int HB>
+__device__ __forceinline__ void rows_merged(const float *red, int BT, int r0, float eps, int lane, float (&mean)[HB],
+                                            float (&rstd)[HB])
+{
+    float mm = 0.f, rr = 0.f;
+    if (lane < HB)
+        merge4(red, BT, r0 + lane, eps, mm, rr);
+#pragma unroll
+    for (int u = 0; u < HB; ++u) {
+        mean[u] = __shfl_sync(0xffffffffu, mm, u);
+        rstd[u] = __shfl_sync(0xffffffffu, rr, u);
+    }
+}
+// the four quadrants' sums of rows r0 .. r0 + HB - 1 (fixed order), every lane taking all HB rows
+template <int HB>
+__device__ __forceinline__ void rows_summed(const float *red, int BT, int r0, int lane, float (&a)[HB], float (&b)[HB])
+{
+    float x = 0.f, y = 0.f;
+    if (lane < HB)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            x += red[(q * BT + r0 + lane) * 2];
+            y += red[(q * BT + r0 + lane) * 2 + 1];
+        }
+#pragma unroll
+    for (int u = 0; u < HB; ++u) {
+        a[u] = __shfl_sync(0xffffffffu, x, u);
+        b[u] = __shfl_sync(0xffffffffu, y, u);
+    }
+}
+
 // x[0..N) = N consecutive 32-bit TMEM columns of this thread's lane (N = 4, 8, 16 or 32)
 template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&x)[N])
@@ -172,9 +276,10 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char *sm = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
-    uint64_t *v2_full = bar + 1, *out_free = bar + 3;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 40);
-    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 44);
+    uint64_t *prod = bar, *upd = bar + 1, *hs_ready = bar + 2, *v2t_ready = bar + 3;
+    uint64_t *v2_full = bar + 4, *out_free = bar + 6;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 64);
+    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 68);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, qd = warp & 3, rh = (warp >> 2) & 1;
     const int ctid = tid & 255;                          // index within the role
     const int m = 32 * qd + lane;                        // this thread's TMEM lane: output feature m
@@ -193,11 +298,15 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         bos = n * a.T;
         eos = bos + a.T;
     }
+    const int nmb = (eos - bos + BT - 1) / BT;   // mini-batches
     const __nv_bfloat16 *gq = static_cast<const __nv_bfloat16 *>(a.q), *gk = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(a.v);
 
     if (tid == 0) {
-        tc::bar_init(bar, 1);
+        tc::bar_init(prod, 1);
+        tc::bar_init(upd, 1);
+        tc::bar_init(hs_ready, 2);    // the split warps (h_t in two terms) and the chain (the tile's rows)
+        tc::bar_init(v2t_ready, 1);
         for (int b = 0; b < 2; ++b) {
             tc::bar_init(&v2_full[b], 256);
             tc::bar_init(&out_free[b], 256);
@@ -213,72 +322,276 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     const uint32_t tmem = *tslot, sb = tc::smem_u32(sm), tl = tmem + lrow;
     const size_t st = (size_t)n * H + h;
     const float scale = a.scale, eps = a.eps;
-    const float wm = a.w[(size_t)h * D + m], bm = a.b[(size_t)h * D + m];
-    float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;   // each role keeps its own copy, updated identically
+    const int r0h = HB * rh;   // first row of this thread's half
     bool ok = true;
 
-    if (warp < 8) {
-        // ================================ the state chain ================================
-        // initial state: h^T[m][c] = h0[c][m] for this thread's 64 columns c (row half rh)
+    if (warp == 16) {
+        // ================================ MMA issue ================================
+        if (lane == 0) {
+            constexpr uint32_t ID_Q = idesc_bf16(128, 2 * BT), ID_C = idesc_bf16(128, BT);
+            constexpr uint32_t ID_B = idesc_bf16(128, D) | tc::kIdescAMajorMN | tc::kIdescBMajorMN;
+            for (int t = 0; t < nmb && ok; ++t) {
+                const int p = t & 1;
+                const uint32_t xs = sb + L::X0 + (t % 3) * L::XB;
+                // h_t in two terms and the tile's rows are in place; the outputs of t - 2 are done with this
+                // parity's columns
+                ok = tc::bar_wait(hs_ready, t & 1, abort_w);
+                if (ok && t >= 2)
+                    ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w);
+                if (!ok)
+                    break;
+                tc::fence_after();
+                if (t == 0)   // k_0 h_0, the first mini-batch's rows (columns BT.. of the other parity)
+                    for (int tt = 0; tt < 2; ++tt)
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            tc::mma_ts(tmem + L::DA + 64 + BT, tmem + L::HS + 64 * tt + 8 * ks,
+                                       tc::sdesc_sw128(xs + (ks >> 2) * L::XH + (ks & 3) * 32), ID_C,
+                                       (tt | ks) ? 1u : 0u);
+                // [q_t h_t, k_{t+1} h_t]^T: tile rows BT .. 3 BT - 1
 #pragma unroll 1
-        for (int c32 = 0; c32 < 2; ++c32) {
-            uint32_t r[32];
-            const int c0 = 64 * rh + 32 * c32;
-#pragma unroll
-            for (int u = 0; u < 32; ++u)
-                r[u] = __float_as_uint(a.h0 ? a.h0[(st * D + c0 + u) * D + m] : 0.f);
-            tc::tmem_st32(tl + L::HT + c0, r);
+                for (int tt = 0; tt < 2; ++tt)
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        tc::mma_ts(tmem + L::DA + 64 * p, tmem + L::HS + 64 * tt + 8 * ks,
+                                   tc::sdesc_sw128(xs + BT * 128 + (ks >> 2) * L::XH + (ks & 3) * 32), ID_Q,
+                                   (tt | ks) ? 1u : 0u);
+                // the tile's rows times k_t: lanes BT.. q_t k_t^T, lanes 2 BT.. k_{t+1} k_t^T
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t dx = tc::sdesc_sw128(xs + (ks >> 2) * L::XH + (ks & 3) * 32);
+                    tc::mma_ss(tmem + L::DC + 32 * p, dx, dx, ID_C, ks ? 1u : 0u);
+                }
+                tc::mma_commit(prod);
+                // the update h^T += (-eta_last v2_t)^T k_t into the fp32 state
+                if (!(ok = tc::bar_wait(v2t_ready, t & 1, abort_w)))
+                    break;
+                tc::fence_after();
+                for (int tt = 0; tt < 3; ++tt)
+                    for (int ks = 0; ks < BT / 16; ++ks)
+                        tc::mma_ss(tmem + L::HT, tc::sdesc_mn_sw128(sb + L::V2T + tt * 2 * L::V2H + ks * 2048, L::V2H),
+                                   tc::sdesc_mn_sw128(xs + ks * 2048, L::XH), ID_B, 1u);
+                tc::mma_commit(upd);
+            }
         }
-        tc::tmem_wait_st();
-
-        // rows [r0, r0 + BT) of k, q (into the [k; q] tile of parity p, zero past the end), v, learning rates
-        auto copy_rows = [&](int r0, int p) {
-            const int len = min(BT, eos - r0);
-            unsigned char *xt = sm + L::X0 + p * L::XB;
-            for (int e = ctid; e < 3 * BT * 16; e += 256) {
+    } else if (warp < 8) {
+        // ================================ the chain ================================
+        float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;
+        const float wm = a.w[(size_t)h * D + m], bm = a.b[(size_t)h * D + m];
+        // mini-batch t's rows into tile t mod 3: k_t (rows 0..BT-1), q_t (BT..), k_{t+1} (2 BT..), zero past the
+        // end; its v rows and learning rates
+        auto copy_rows = [&](int t) {
+            const int r0 = bos + t * BT, slot = t % 3;
+            unsigned char *xt = sm + L::X0 + slot * L::XB;
+            for (int e = ctid; e < 4 * BT * 16; e += 256) {
                 const int which = e / (BT * 16), rem = e - which * (BT * 16), i = rem >> 4, c = rem & 15;
-                const bool in = i < len;
-                const size_t row = (size_t)(r0 + (in ? i : 0)) * H + h;
-                if (which < 2) {
-                    const __nv_bfloat16 *src = (which == 0 ? gk : gq) + row * D + 8 * c;
-                    const int rr = which * BT + i;   // tile row: k rows, then q rows
-                    cp_async16(xt + (c >> 3) * L::XH + tc::sw128(rr, 8 * (c & 7)), src, in ? 16u : 0u);
+                const int row = r0 + (which == 2 ? BT : 0) + i;
+                const bool in = row < eos;
+                const size_t gr = (size_t)(in ? row : r0) * H + h;
+                if (which < 3) {
+                    const __nv_bfloat16 *src = (which == 1 ? gq : gk) + gr * D + 8 * c;
+                    cp_async16(xt + (c >> 3) * L::XH + tc::sw128(which * BT + i, 8 * (c & 7)), src, in ? 16u : 0u);
                 } else {
-                    cp_async16(sm + L::VR + p * BT * D * 2 + i * D * 2 + 16 * c, gv + row * D + 8 * c,
-                               in ? 16u : 0u);
+                    cp_async16(sm + L::VR + slot * BT * D * 2 + i * D * 2 + 16 * c, gv + gr * D + 8 * c, in ? 16u : 0u);
                 }
             }
-            if (ctid < BT)
-                cp_async4(sm + L::ET + (p * BT + ctid) * 4, a.eta + (size_t)(r0 + (ctid < len ? ctid : 0)) * H + h,
-                          ctid < len ? 4u : 0u);
+            if (ctid < BT) {
+                const bool in = r0 + ctid < eos;
+                cp_async4(sm + L::ET + (slot * BT + ctid) * 4, a.eta + (size_t)(in ? r0 + ctid : r0) * H + h,
+                          in ? 4u : 0u);
+            }
             asm volatile("cp.async.commit_group;" ::: "memory");
         };
+        auto no_rows = []() { asm volatile("cp.async.commit_group;" ::: "memory"); };
 
-        float *RED = reinterpret_cast<float *>(sm + L::RED);
-        constexpr uint32_t ID_A = idesc_bf16(128, 2 * BT), ID_C = idesc_bf16(128, BT);
-        constexpr uint32_t ID_B = idesc_bf16(128, D) | tc::kIdescAMajorMN | tc::kIdescBMajorMN;
-        uint32_t phase = 0;
-        if (bos < eos)
-            copy_rows(bos, 0);
-        int p = 0, t = 0;
-        for (int r0 = bos; r0 < eos; r0 += BT, p ^= 1, ++t) {
-            const int len = min(BT, eos - r0);
-            // the previous update is complete (it read the k rows of the other tile): the next mini-batch's
-            // rows may come into that tile
-            if (t > 0) {
-                ok = tc::bar_wait(bar, phase & 1, abort_w) && ok;
-                ++phase;
-            }
-            tc::fence_after();
-            if (r0 + BT < eos)
-                copy_rows(r0 + BT, p ^ 1);
+        float *RED = reinterpret_cast<float *>(sm + L::RED), *RSG = RED + 4 * BT * 2;
+        if (nmb > 0) {
+            copy_rows(0);
+            if (nmb > 1)
+                copy_rows(1);
             else
-                asm volatile("cp.async.commit_group;" ::: "memory");
-            asm volatile("cp.async.wait_group 1;" ::: "memory");   // this mini-batch's rows
-            const unsigned char *xt = sm + L::X0 + p * L::XB;
-            const uint32_t xs = sb + L::X0 + p * L::XB;
-
-            // ---- split h^T into its two bf16 terms (TMEM -> TMEM): this thread's 64 columns
+                no_rows();
+            asm volatile("cp.async.wait_group 1;" ::: "memory");   // the first mini-batch's rows
+            tc::fence_proxy_async();
+            chain_sync();
+            if (ctid == 0)
+                tc::bar_arrive(hs_ready);
+        }
+        float elp = 0.f;   // eta_last of the previous mini-batch
+        for (int t = 0; t < nmb && ok; ++t) {
+            const int p = t & 1, r0 = bos + t * BT, len = min(BT, eos - r0);
+            const unsigned char *xt = sm + L::X0 + (t % 3) * L::XB;
+            // ---- k_t h_t + hb = (k_t h_{t-1}) + (k_t k_{t-1}^T) W_{t-1} + hb for this half's rows
+            if (t == 0) {
+                ok = tc::bar_wait(prod, 0, abort_w) && ok;   // k_0 h_0
+                tc::fence_after();
+            }
+            float kh[HB];
+            {
+                uint32_t r[HB];
+                tmem_ldn<HB>(tl + L::DA + 64 * (p ^ 1) + BT + r0h, r);
+#pragma unroll
+                for (int u = 0; u < HB; ++u)
+                    kh[u] = __uint_as_float(r[u]) + hb;
+            }
+            if (t > 0) {
+                const float *V2P = reinterpret_cast<const float *>(sm + L::V2F + (p ^ 1) * BT * D * 4);
+                const float *KKP = reinterpret_cast<const float *>(sm + L::KK + (p ^ 1) * BT * BT * 4);
+                float wj[BT];
+#pragma unroll
+                for (int j = 0; j < BT; ++j)
+                    wj[j] = -elp * V2P[j * D + m];
+#pragma unroll
+                for (int u = 0; u < HB; ++u) {
+                    const int i = r0h + u;
+                    float c = 0.f;
+#pragma unroll
+                    for (int j4 = 0; j4 < BT; j4 += 4) {
+                        const float4 k4 = *reinterpret_cast<const float4 *>(KKP + i * BT + j4);
+                        c = fmaf(k4.x, wj[j4], c);
+                        c = fmaf(k4.y, wj[j4 + 1], c);
+                        c = fmaf(k4.z, wj[j4 + 2], c);
+                        c = fmaf(k4.w, wj[j4 + 3], c);
+                    }
+                    kh[u] += c;
+                }
+            }
+            // ---- LayerNorm statistics of the rows
+            warp_row_stats<HB>(kh, RED, qd, BT, r0h, lane);
+            chain_sync();
+            if (ctid == 0 && t > 0)
+                tc::bar_arrive(hs_ready);   // the tile's rows have been in place since the last mini-batch
+            // ---- the update of the last mini-batch is complete: its tile takes the rows two ahead
+            if (t > 0) {
+                ok = tc::bar_wait(upd, (t - 1) & 1, abort_w) && ok;
+                tc::fence_after();
+            }
+            if (t + 2 < nmb)
+                copy_rows(t + 2);
+            else
+                no_rows();
+            // ---- gradient of the inner loss; its two row sums over the features
+            float xh[HB], gg[HB], rs[HB], gx[HB];
+            {
+                float mean[HB];
+                rows_merged<HB>(RED, BT, r0h, eps, lane, mean, rs);
+                const uint16_t *vr = reinterpret_cast<const uint16_t *>(sm + L::VR + (t % 3) * BT * D * 2);
+#pragma unroll
+                for (int u = 0; u < HB; ++u) {
+                    const int i = r0h + u;
+                    xh[u] = (kh[u] - mean[u]) * rs[u];
+                    const float ki =
+                        bf(*reinterpret_cast<const uint16_t *>(xt + (m >> 6) * L::XH + tc::sw128(i, m & 63)));
+                    gg[u] = i < len ? (fmaf(xh[u], wm, bm) + ki - bf(vr[i * D + m])) * wm : 0.f;
+                    gx[u] = gg[u] * xh[u];
+                }
+            }
+            warp_row_sums<HB>(gg, gx, RSG, qd, BT, r0h, lane);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");   // the next mini-batch's rows
+            tc::fence_proxy_async();   // the next mini-batch's copied rows -> the tensor cores
+            chain_sync();
+            // the outputs of two mini-batches ago are done with this parity's buffers
+            if (t >= 2) {
+                ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w) && ok;
+                tc::fence_after();
+            }
+            const float *ET = reinterpret_cast<const float *>(sm + L::ET + (t % 3) * BT * 4);
+            const float el = ET[len - 1];
+            float *V2F = reinterpret_cast<float *>(sm + L::V2F + p * BT * D * 4);
+            float v2[HB];
+            {
+                float sg[HB], sgx[HB];
+                rows_summed<HB>(RSG, BT, r0h, lane, sg, sgx);
+#pragma unroll
+                for (int u = 0; u < HB; ++u) {
+                    v2[u] = rs[u] * (1.f / D) * (D * gg[u] - sg[u] - xh[u] * sgx[u]);
+                    V2F[(r0h + u) * D + m] = v2[u];
+                }
+            }
+            if (ctid <= BT) {   // the learning rates and eta_last for the output warps
+                float *E2 = reinterpret_cast<float *>(sm + L::E2 + p * (BT + 4) * 4);
+                E2[ctid] = ctid < BT ? ET[ctid] : el;
+            }
+            // -eta_last v2 in three bf16 terms (exact), MN-major: row i, feature m (two rows per split)
+#pragma unroll
+            for (int u = 0; u < HB; u += 2) {
+                const int i = r0h + u;
+                uint32_t wv[3];
+                split3(-el * v2[u], -el * v2[u + 1], wv[0], wv[1], wv[2]);
+                const uint32_t off0 = (m >> 6) * L::V2H + tc::sw128(i, m & 63);
+                const uint32_t off1 = (m >> 6) * L::V2H + tc::sw128(i + 1, m & 63);
+#pragma unroll
+                for (int tt = 0; tt < 3; ++tt) {
+                    *reinterpret_cast<uint16_t *>(sm + L::V2T + tt * 2 * L::V2H + off0) = (uint16_t)(wv[tt] & 0xFFFFu);
+                    *reinterpret_cast<uint16_t *>(sm + L::V2T + tt * 2 * L::V2H + off1) = (uint16_t)(wv[tt] >> 16);
+                }
+            }
+            tc::fence_proxy_async();
+            chain_sync();
+            if (ctid == 0)
+                tc::bar_arrive(v2t_ready);
+            float sv = 0.f;
+#pragma unroll
+            for (int j = 0; j < BT; ++j)
+                sv += V2F[j * D + m];
+            hb = fmaf(-el, sv, hb);
+            elp = el;
+            // ---- this mini-batch's products are complete: the outputs' masked scores (scale q_i.k_j + 1 for
+            // j <= i) and k_{t+1} k_t^T for the next correction to shared memory (the warps of row half 0 that
+            // hold those TMEM lanes)
+            ok = tc::bar_wait(prod, t & 1, abort_w) && ok;
+            tc::fence_after();
+            if (rh == 0 && (qd == BT / 32 || qd == BT / 16)) {
+                uint32_t r[BT];
+                tmem_ldn<BT>(tl + L::DC + 32 * p, r);
+                const bool sc = qd == BT / 32;
+                const int row = m - (sc ? BT : 2 * BT);
+                float *dst = reinterpret_cast<float *>(sm + (sc ? L::AS : L::KK) + p * BT * BT * 4);
+                if (row >= 0 && row < BT)
+#pragma unroll
+                    for (int j = 0; j < BT; j += 4) {
+                        float4 x = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                                               __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                        if (sc) {
+                            x.x = j <= row ? fmaf(scale, x.x, 1.f) : 0.f;
+                            x.y = j + 1 <= row ? fmaf(scale, x.y, 1.f) : 0.f;
+                            x.z = j + 2 <= row ? fmaf(scale, x.z, 1.f) : 0.f;
+                            x.w = j + 3 <= row ? fmaf(scale, x.w, 1.f) : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(dst + row * BT + j) = x;
+                    }
+            }
+            tc::fence_before();
+            chain_sync();
+            tc::bar_arrive(&v2_full[p]);   // this mini-batch's q h columns, scores, v2 and rates: to the outputs
+        }
+        if (nmb > 0) {
+            ok = tc::bar_wait(upd, (nmb - 1) & 1, abort_w) && ok;   // the last update
+            tc::fence_after();
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (a.ht && nmb > 0) {
+#pragma unroll 1
+            for (int c32 = 0; c32 < 2; ++c32) {
+                uint32_t r[32];
+                const int c0 = 64 * rh + 32 * c32;
+                tc::tmem_ld32(tl + L::HT + c0, r);
+                tc::tmem_wait_ld(r);
+#pragma unroll
+                for (int u = 0; u < 32; ++u)
+                    a.ht[(st * D + c0 + u) * D + m] = __uint_as_float(r[u]);
+            }
+        } else if (a.ht) {   // an empty sequence: the initial state (the split warps fill the TMEM state unordered)
+            for (int u = 0; u < 64; ++u) {
+                const size_t e = (st * D + 64 * rh + u) * D + m;
+                a.ht[e] = a.h0 ? a.h0[e] : 0.f;
+            }
+        }
+        if (a.hbt && rh == 0)
+            a.hbt[st * D + m] = hb;
+    } else {
+        // ============ the state split, and the outputs one mini-batch behind ============
+        float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;   // kept here too, updated as the chain's
+        const float wm = a.w[(size_t)h * D + m], bm = a.b[(size_t)h * D + m];
+        // h^T (fp32, this thread's 64 columns) -> its two bf16 terms
+        auto split_state = [&]() {
 #pragma unroll 1
             for (int c32 = 0; c32 < 2; ++c32) {
                 uint32_t r[32], w1[16], w2[16];
@@ -292,172 +605,44 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 tc::tmem_st16(tl + L::HS + 1 * 64 + c0 / 2, w2);
             }
             tc::tmem_wait_st();
-            tc::fence_proxy_async();   // the copied rows of this mini-batch -> visible to the MMAs
-            tc::fence_before();
-            chain_sync();
-            tc::fence_after();
-            // the outputs of two mini-batches ago are done with this parity's TMEM columns and buffers
-            if (t >= 2)
-                ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w) && ok;
-            tc::fence_after();
-
-            // ---- [k h, q h]^T = h^T [k; q]^T (two terms of h) and q k^T, into this parity's columns
-            if (ctid == 0) {
+        };
+        // initial state: h^T[m][c] = h0[c][m] for this thread's 64 columns c (row half rh), and its two terms
 #pragma unroll 1
-                for (int tt = 0; tt < 2; ++tt)
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        tc::mma_ts(tmem + L::DA + 64 * p, tmem + L::HS + 64 * tt + 8 * ks,
-                                   tc::sdesc_sw128(xs + (ks >> 2) * L::XH + (ks & 3) * 32), ID_A, (tt | ks) ? 1u : 0u);
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t dx = tc::sdesc_sw128(xs + (ks >> 2) * L::XH + (ks & 3) * 32);
-                    tc::mma_ss(tmem + L::DC + 32 * p, dx, dx, ID_C, ks ? 1u : 0u);
-                }
-                tc::mma_commit(bar);
-            }
-            ok = tc::bar_wait(bar, phase & 1, abort_w) && ok;
-            ++phase;
-            tc::fence_after();
-
-            // ---- this half's rows of k h + hb; q k^T to shared memory; LayerNorm statistics
-            float kh[HB];
-            {
-                uint32_t r[HB];
-                tmem_ldn<HB>(tl + L::DA + 64 * p + HB * rh, r);
+        for (int c32 = 0; c32 < 2; ++c32) {
+            uint32_t r[32];
+            const int c0 = 64 * rh + 32 * c32;
 #pragma unroll
-                for (int u = 0; u < HB; ++u)
-                    kh[u] = __uint_as_float(r[u]) + hb;
-            }
-            // q k^T: TMEM lanes BT .. 2 BT - 1 (the q rows of the tile), columns j < BT; the whole warp of row half 0
-            // that holds those lanes loads (a warp-wide instruction), its lanes in range keep the values
-            if (warp == (BT == 16 ? 0 : 1)) {
-                uint32_t r[BT];
-                tmem_ldn<BT>(tl + L::DC + 32 * p, r);
-                float *AS = reinterpret_cast<float *>(sm + L::AS + p * BT * BT * 4);
-                if (m >= BT && m < 2 * BT)
-#pragma unroll
-                    for (int j = 0; j < BT; j += 4)
-                        *reinterpret_cast<float4 *>(AS + (m - BT) * BT + j) =
-                            make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
-                                        __uint_as_float(r[j + 3]));
-            }
-#pragma unroll
-            for (int u = 0; u < HB; ++u) {
-                float mean, m2;
-                warp_stats(kh[u], mean, m2);
-                if (lane == 0) {
-                    RED[(qd * BT + HB * rh + u) * 2] = mean;
-                    RED[(qd * BT + HB * rh + u) * 2 + 1] = m2;
-                }
-            }
-            chain_sync();
-            // ---- gradient of the inner loss; its two row sums over the features
-            float xh[HB], gg[HB], rs[HB];
-            const uint16_t *vr = reinterpret_cast<const uint16_t *>(sm + L::VR + p * BT * D * 2);
-#pragma unroll
-            for (int u = 0; u < HB; ++u) {
-                const int i = HB * rh + u;
-                float mean;
-                merge4(RED, BT, i, eps, mean, rs[u]);
-                xh[u] = (kh[u] - mean) * rs[u];
-                const float ki = bf(*reinterpret_cast<const uint16_t *>(xt + (m >> 6) * L::XH + tc::sw128(i, m & 63)));
-                gg[u] = i < len ? (fmaf(xh[u], wm, bm) + ki - bf(vr[i * D + m])) * wm : 0.f;
-            }
-            chain_sync();   // every thread has read the statistics: the buffer takes the gradient sums
-#pragma unroll
-            for (int u = 0; u < HB; ++u) {
-                const float sg = warp_sum(gg[u]), sgx = warp_sum(gg[u] * xh[u]);
-                if (lane == 0) {
-                    RED[(qd * BT + HB * rh + u) * 2] = sg;
-                    RED[(qd * BT + HB * rh + u) * 2 + 1] = sgx;
-                }
-            }
-            chain_sync();
-            const float *ET = reinterpret_cast<const float *>(sm + L::ET + p * BT * 4);
-            const float el = ET[len - 1];
-            float *V2F = reinterpret_cast<float *>(sm + L::V2F + p * BT * D * 4);
-            float v2[HB];
-#pragma unroll
-            for (int u = 0; u < HB; ++u) {
-                const int i = HB * rh + u;
-                float sg = 0.f, sgx = 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    sg += RED[(q * BT + i) * 2];
-                    sgx += RED[(q * BT + i) * 2 + 1];
-                }
-                v2[u] = rs[u] * (1.f / D) * (D * gg[u] - sg - xh[u] * sgx);
-                V2F[i * D + m] = v2[u];
-            }
-            if (ctid <= BT) {   // the learning rates and eta_last for the output warps
-                float *E2 = reinterpret_cast<float *>(sm + L::E2 + p * (BT + 4) * 4);
-                E2[ctid] = ctid < BT ? ET[ctid] : el;
-            }
-            // -eta_last v2 in three bf16 terms (exact), MN-major: row i, feature m (two rows per split)
-#pragma unroll
-            for (int u = 0; u < HB; u += 2) {
-                const int i = HB * rh + u;
-                uint32_t wv[3];
-                split3(-el * v2[u], -el * v2[u + 1], wv[0], wv[1], wv[2]);
-                const uint32_t off0 = (m >> 6) * L::V2H + tc::sw128(i, m & 63);
-                const uint32_t off1 = (m >> 6) * L::V2H + tc::sw128(i + 1, m & 63);
-#pragma unroll
-                for (int tt = 0; tt < 3; ++tt) {
-                    *reinterpret_cast<uint16_t *>(sm + L::V2T + tt * 2 * L::V2H + off0) = (uint16_t)(wv[tt] & 0xFFFFu);
-                    *reinterpret_cast<uint16_t *>(sm + L::V2T + tt * 2 * L::V2H + off1) = (uint16_t)(wv[tt] >> 16);
-                }
-            }
-            tc::fence_proxy_async();
+            for (int u = 0; u < 32; ++u)
+                r[u] = __float_as_uint(a.h0 ? a.h0[(st * D + c0 + u) * D + m] : 0.f);
+            tc::tmem_st32(tl + L::HT + c0, r);
+        }
+        tc::tmem_wait_st();
+        if (nmb > 0) {
+            split_state();
             tc::fence_before();
-            chain_sync();
-            tc::fence_after();
-            // ---- the update h^T += (-eta_last v2)^T k, accumulating into the fp32 state
-            if (ctid == 0) {
-                for (int tt = 0; tt < 3; ++tt)
-                    for (int ks = 0; ks < BT / 16; ++ks)
-                        tc::mma_ss(tmem + L::HT,
-                                   tc::sdesc_mn_sw128(sb + L::V2T + tt * 2 * L::V2H + ks * 2048, L::V2H),
-                                   tc::sdesc_mn_sw128(xs + ks * 2048, L::XH), ID_B, 1u);
-                tc::mma_commit(bar);
-            }
-            tc::bar_arrive(&v2_full[p]);   // this mini-batch's q h columns, scores, v2 and rates: to the outputs
-            float sv = 0.f;
-#pragma unroll
-            for (int j = 0; j < BT; ++j)
-                sv += V2F[j * D + m];
-            hb = fmaf(-el, sv, hb);
+            out_sync();
+            if (ctid == 0)
+                tc::bar_arrive(hs_ready);
         }
-        if (bos < eos) {
-            ok = tc::bar_wait(bar, phase & 1, abort_w) && ok;   // the last update
-            ++phase;
-        }
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        tc::fence_after();
-        if (a.ht) {
-#pragma unroll 1
-            for (int c32 = 0; c32 < 2; ++c32) {
-                uint32_t r[32];
-                const int c0 = 64 * rh + 32 * c32;
-                tc::tmem_ld32(tl + L::HT + c0, r);
-                tc::tmem_wait_ld(r);
-#pragma unroll
-                for (int u = 0; u < 32; ++u)
-                    a.ht[(st * D + c0 + u) * D + m] = __uint_as_float(r[u]);
-            }
-        }
-        if (a.hbt && rh == 0)
-            a.hbt[st * D + m] = hb;
-    } else {
-        // ================================ the outputs, one mini-batch behind ================================
-        // q h + hb - eta_i sum_{j<=i} (scale q_i.k_j + 1) v2_j from the mini-batch's q h columns, scores and
+        // q h + hb - eta_i sum_{j<=i} (scale q_i.k_j + 1) v2_j from the mini-batch's q h columns, masked scores and
         // v2, then o + LN(o) w + b
         float *RED2 = reinterpret_cast<float *>(sm + L::RED2);
-        int p = 0, t = 0;
-        for (int r0 = bos; r0 < eos; r0 += BT, p ^= 1, ++t) {
-            const int len = min(BT, eos - r0);
+        for (int t = 0; t < nmb && ok; ++t) {
+            const int p = t & 1, r0 = bos + t * BT, len = min(BT, eos - r0);
+            // h_{t+1} = h_t + k_t^T W_t is complete (and with it the products that read h_t's terms): its terms
+            if (t + 1 < nmb) {
+                ok = tc::bar_wait(upd, t & 1, abort_w) && ok;
+                tc::fence_after();
+                split_state();
+                tc::fence_before();
+                out_sync();
+                if (ctid == 0)
+                    tc::bar_arrive(hs_ready);
+            }
             ok = tc::bar_wait(&v2_full[p], (t >> 1) & 1, abort_w) && ok;
             tc::fence_after();
             uint32_t r[HB];
-            tmem_ldn<HB>(tl + L::DA + 64 * p + BT + HB * rh, r);
+            tmem_ldn<HB>(tl + L::DA + 64 * p + r0h, r);
             const float *V2F = reinterpret_cast<const float *>(sm + L::V2F + p * BT * D * 4);
             const float *AS = reinterpret_cast<const float *>(sm + L::AS + p * BT * BT * 4);
             const float *E2 = reinterpret_cast<const float *>(sm + L::E2 + p * (BT + 4) * 4);
@@ -468,37 +653,34 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             float ov[HB];
 #pragma unroll
             for (int u = 0; u < HB; ++u) {
-                const int i = HB * rh + u;
+                const int i = r0h + u;
                 float acc = 0.f;
 #pragma unroll
                 for (int j4 = 0; j4 < BT; j4 += 4) {
                     const float4 s4 = *reinterpret_cast<const float4 *>(AS + i * BT + j4);
-                    acc = fmaf(j4 <= i ? fmaf(scale, s4.x, 1.f) : 0.f, v2c[j4], acc);
-                    acc = fmaf(j4 + 1 <= i ? fmaf(scale, s4.y, 1.f) : 0.f, v2c[j4 + 1], acc);
-                    acc = fmaf(j4 + 2 <= i ? fmaf(scale, s4.z, 1.f) : 0.f, v2c[j4 + 2], acc);
-                    acc = fmaf(j4 + 3 <= i ? fmaf(scale, s4.w, 1.f) : 0.f, v2c[j4 + 3], acc);
+                    acc = fmaf(s4.x, v2c[j4], acc);
+                    acc = fmaf(s4.y, v2c[j4 + 1], acc);
+                    acc = fmaf(s4.z, v2c[j4 + 2], acc);
+                    acc = fmaf(s4.w, v2c[j4 + 3], acc);
                 }
                 ov[u] = fmaf(-E2[i], acc, fmaf(scale, __uint_as_float(r[u]), hb));
-                float mean, m2;
-                warp_stats(ov[u], mean, m2);
-                if (lane == 0) {
-                    RED2[(qd * BT + i) * 2] = mean;
-                    RED2[(qd * BT + i) * 2 + 1] = m2;
-                }
             }
+            warp_row_stats<HB>(ov, RED2, qd, BT, r0h, lane);
             const float el = E2[BT];
             float sv = 0.f;
 #pragma unroll
             for (int j = 0; j < BT; ++j)
                 sv += v2c[j];
             out_sync();
+            {
+                float mean[HB], rstd[HB];
+                rows_merged<HB>(RED2, BT, r0h, eps, lane, mean, rstd);
 #pragma unroll
-            for (int u = 0; u < HB; ++u) {
-                const int i = HB * rh + u;
-                float mean, rstd;
-                merge4(RED2, BT, i, eps, mean, rstd);
-                if (i < len)
-                    a.o[((size_t)(r0 + i) * H + h) * D + m] = ov[u] + fmaf((ov[u] - mean) * rstd, wm, bm);
+                for (int u = 0; u < HB; ++u) {
+                    const int i = r0h + u;
+                    if (i < len)
+                        a.o[((size_t)(r0 + i) * H + h) * D + m] = ov[u] + fmaf((ov[u] - mean[u]) * rstd[u], wm, bm);
+                }
             }
             hb = fmaf(-el, sv, hb);
             tc::fence_before();
