@@ -35,7 +35,7 @@ namespace gla {
 namespace {
 
 constexpr int D = 128;
-constexpr int NTH = 544;   // warps 0-7: the chain; 8-15: the state split and the outputs; 16: the MMA issue
+constexpr int NTH = 576;   // warps 0-7: the chain; 8-15: the state split and the outputs; 16: MMA issue; 17: row copies
 
 template <int BT>
 struct TtcLayout {
@@ -52,10 +52,10 @@ struct TtcLayout {
     static constexpr int ET = RED + 2 * 4 * BT * 2 * 4;  // [3][BT] learning rates (0 past the end)
     static constexpr int E2 = ET + 3 * BT * 4;       // [2][BT + 1] the outputs' learning rates and eta_last
     static constexpr int RED2 = E2 + 2 * (BT + 4) * 4;   // [4][BT][2] the output warps' partial statistics
-    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2]; TMEM address; abort word
+    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3]; TMEM address; abort word
     static constexpr int BAR = RED2 + 4 * BT * 2 * 4;
     // the row products read rows 0..127 of a tile with K-halves XH apart: keep that span allocated
-    static constexpr int END = BAR + 96 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 96 : X0 + 2 * XB + XH + 128 * 128;
+    static constexpr int END = BAR + 128 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 128 : X0 + 2 * XB + XH + 128 * 128;
     static constexpr int BYTES = END + 1024;
     // TMEM columns: the state, its two bf16 terms (64 columns each), [q h_t, k_{t+1} h_t]^T by parity, the row
     // products by parity
@@ -267,6 +267,18 @@ __device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&x)[N])
 
 __device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ void out_sync() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+// barrier of the 256 threads of a role (named barrier id) that also returns the AND of x over them, so that
+// a wait taken by one thread gives every thread the same outcome
+__device__ __forceinline__ bool role_all(bool x, int id)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, 256, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}\n"
+                 : "=r"(r)
+                 : "r"((uint32_t)x), "r"(id)
+                 : "memory");
+    return r != 0;
+}
 
 template <int BT>
 __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
@@ -278,8 +290,9 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
     uint64_t *prod = bar, *upd = bar + 1, *hs_ready = bar + 2, *v2t_ready = bar + 3;
     uint64_t *v2_full = bar + 4, *out_free = bar + 6;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 64);
-    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 68);
+    uint64_t *xfull = bar + 8, *slot_free = bar + 11;   // [3] by mini-batch mod 3: the tile's rows landed / free
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 112);
+    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 116);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, qd = warp & 3, rh = (warp >> 2) & 1;
     const int ctid = tid & 255;                          // index within the role
     const int m = 32 * qd + lane;                        // this thread's TMEM lane: output feature m
@@ -305,11 +318,15 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     if (tid == 0) {
         tc::bar_init(prod, 1);
         tc::bar_init(upd, 1);
-        tc::bar_init(hs_ready, 2);    // the split warps (h_t in two terms) and the chain (the tile's rows)
+        tc::bar_init(hs_ready, 1);
         tc::bar_init(v2t_ready, 1);
         for (int b = 0; b < 2; ++b) {
             tc::bar_init(&v2_full[b], 256);
             tc::bar_init(&out_free[b], 256);
+        }
+        for (int b = 0; b < 3; ++b) {
+            tc::bar_init(&xfull[b], 32);   // one completion-tracked arrival per lane of the copy warp
+            tc::bar_init(&slot_free[b], 1);
         }
         *abort_w = 0;
         tc::bar_fence_init();
@@ -335,12 +352,13 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 const uint32_t xs = sb + L::X0 + (t % 3) * L::XB;
                 // h_t in two terms and the tile's rows are in place; the outputs of t - 2 are done with this
                 // parity's columns
-                ok = tc::bar_wait(hs_ready, t & 1, abort_w);
+                ok = tc::bar_wait(hs_ready, t & 1, abort_w) && tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w);
                 if (ok && t >= 2)
                     ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w);
                 if (!ok)
                     break;
                 tc::fence_after();
+                tc::fence_proxy_async();   // the copied rows -> the tensor cores
                 if (t == 0)   // k_0 h_0, the first mini-batch's rows (columns BT.. of the other parity)
                     for (int tt = 0; tt < 2; ++tt)
                         for (int ks = 0; ks < D / 16; ++ks)
@@ -369,18 +387,19 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                         tc::mma_ss(tmem + L::HT, tc::sdesc_mn_sw128(sb + L::V2T + tt * 2 * L::V2H + ks * 2048, L::V2H),
                                    tc::sdesc_mn_sw128(xs + ks * 2048, L::XH), ID_B, 1u);
                 tc::mma_commit(upd);
+                tc::mma_commit(&slot_free[t % 3]);
             }
         }
-    } else if (warp < 8) {
-        // ================================ the chain ================================
-        float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;
-        const float wm = a.w[(size_t)h * D + m], bm = a.b[(size_t)h * D + m];
+    } else if (warp == 17) {
+        // ================================ row copies ================================
         // mini-batch t's rows into tile t mod 3: k_t (rows 0..BT-1), q_t (BT..), k_{t+1} (2 BT..), zero past the
-        // end; its v rows and learning rates
-        auto copy_rows = [&](int t) {
+        // end; its v rows and learning rates.  Each lane's copies arrive on the tile's barrier as they land.
+        for (int t = 0; t < nmb && ok; ++t) {
             const int r0 = bos + t * BT, slot = t % 3;
+            if (t >= 3 && !(ok = tc::bar_wait(&slot_free[slot], ((t / 3) - 1) & 1, abort_w)))
+                break;
             unsigned char *xt = sm + L::X0 + slot * L::XB;
-            for (int e = ctid; e < 4 * BT * 16; e += 256) {
+            for (int e = lane; e < 4 * BT * 16; e += 32) {
                 const int which = e / (BT * 16), rem = e - which * (BT * 16), i = rem >> 4, c = rem & 15;
                 const int row = r0 + (which == 2 ? BT : 0) + i;
                 const bool in = row < eos;
@@ -392,28 +411,20 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     cp_async16(sm + L::VR + slot * BT * D * 2 + i * D * 2 + 16 * c, gv + gr * D + 8 * c, in ? 16u : 0u);
                 }
             }
-            if (ctid < BT) {
-                const bool in = r0 + ctid < eos;
-                cp_async4(sm + L::ET + (slot * BT + ctid) * 4, a.eta + (size_t)(in ? r0 + ctid : r0) * H + h,
+            if (lane < BT) {
+                const bool in = r0 + lane < eos;
+                cp_async4(sm + L::ET + (slot * BT + lane) * 4, a.eta + (size_t)(in ? r0 + lane : r0) * H + h,
                           in ? 4u : 0u);
             }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        auto no_rows = []() { asm volatile("cp.async.commit_group;" ::: "memory"); };
-
-        float *RED = reinterpret_cast<float *>(sm + L::RED), *RSG = RED + 4 * BT * 2;
-        if (nmb > 0) {
-            copy_rows(0);
-            if (nmb > 1)
-                copy_rows(1);
-            else
-                no_rows();
-            asm volatile("cp.async.wait_group 1;" ::: "memory");   // the first mini-batch's rows
-            tc::fence_proxy_async();
-            chain_sync();
-            if (ctid == 0)
-                tc::bar_arrive(hs_ready);
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(&xfull[slot]))
+                         : "memory");
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");   // nothing lands after the CTA is gone
+    } else if (warp < 8) {
+        // ================================ the chain ================================
+        float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;
+        const float wm = a.w[(size_t)h * D + m], bm = a.b[(size_t)h * D + m];
+        float *RED = reinterpret_cast<float *>(sm + L::RED), *RSG = RED + 4 * BT * 2;
         float elp = 0.f;   // eta_last of the previous mini-batch
         for (int t = 0; t < nmb && ok; ++t) {
             const int p = t & 1, r0 = bos + t * BT, len = min(BT, eos - r0);
@@ -453,20 +464,12 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     kh[u] += c;
                 }
             }
-            // ---- LayerNorm statistics of the rows
+            // ---- LayerNorm statistics of the rows (one thread also sees this mini-batch's k and v rows landed;
+            // the barrier passes that on)
             warp_row_stats<HB>(kh, RED, qd, BT, r0h, lane);
-            chain_sync();
-            if (ctid == 0 && t > 0)
-                tc::bar_arrive(hs_ready);   // the tile's rows have been in place since the last mini-batch
-            // ---- the update of the last mini-batch is complete: its tile takes the rows two ahead
-            if (t > 0) {
-                ok = tc::bar_wait(upd, (t - 1) & 1, abort_w) && ok;
-                tc::fence_after();
-            }
-            if (t + 2 < nmb)
-                copy_rows(t + 2);
-            else
-                no_rows();
+            if (ctid == 0)
+                ok = tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w) && ok;
+            ok = role_all(ok, 1);
             // ---- gradient of the inner loss; its two row sums over the features
             float xh[HB], gg[HB], rs[HB], gx[HB];
             {
@@ -484,14 +487,15 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 }
             }
             warp_row_sums<HB>(gg, gx, RSG, qd, BT, r0h, lane);
-            asm volatile("cp.async.wait_group 1;" ::: "memory");   // the next mini-batch's rows
-            tc::fence_proxy_async();   // the next mini-batch's copied rows -> the tensor cores
-            chain_sync();
-            // the outputs of two mini-batches ago are done with this parity's buffers
-            if (t >= 2) {
-                ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w) && ok;
-                tc::fence_after();
+            // the last update is complete (its v2 terms may be overwritten) and the outputs of two mini-batches
+            // ago are done with this parity's buffers: one thread waits, the barrier passes it on
+            if (ctid == 0) {
+                if (t > 0)
+                    ok = tc::bar_wait(upd, (t - 1) & 1, abort_w) && ok;
+                if (t >= 2)
+                    ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w) && ok;
             }
+            ok = role_all(ok, 1);
             const float *ET = reinterpret_cast<const float *>(sm + L::ET + (t % 3) * BT * 4);
             const float el = ET[len - 1];
             float *V2F = reinterpret_cast<float *>(sm + L::V2F + p * BT * D * 4);
@@ -536,9 +540,9 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             // ---- this mini-batch's products are complete: the outputs' masked scores (scale q_i.k_j + 1 for
             // j <= i) and k_{t+1} k_t^T for the next correction to shared memory (the warps of row half 0 that
             // hold those TMEM lanes)
-            ok = tc::bar_wait(prod, t & 1, abort_w) && ok;
-            tc::fence_after();
             if (rh == 0 && (qd == BT / 32 || qd == BT / 16)) {
+                ok = tc::bar_wait(prod, t & 1, abort_w) && ok;
+                tc::fence_after();
                 uint32_t r[BT];
                 tmem_ldn<BT>(tl + L::DC + 32 * p, r);
                 const bool sc = qd == BT / 32;
@@ -559,14 +563,13 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     }
             }
             tc::fence_before();
-            chain_sync();
+            ok = role_all(ok, 1);   // (the staging warps' wait)
             tc::bar_arrive(&v2_full[p]);   // this mini-batch's q h columns, scores, v2 and rates: to the outputs
         }
         if (nmb > 0) {
             ok = tc::bar_wait(upd, (nmb - 1) & 1, abort_w) && ok;   // the last update
             tc::fence_after();
         }
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
         if (a.ht && nmb > 0) {
 #pragma unroll 1
             for (int c32 = 0; c32 < 2; ++c32) {
@@ -631,7 +634,9 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             const int p = t & 1, r0 = bos + t * BT, len = min(BT, eos - r0);
             // h_{t+1} = h_t + k_t^T W_t is complete (and with it the products that read h_t's terms): its terms
             if (t + 1 < nmb) {
-                ok = tc::bar_wait(upd, t & 1, abort_w) && ok;
+                if (ctid == 0)
+                    ok = tc::bar_wait(upd, t & 1, abort_w) && ok;
+                ok = role_all(ok, 2);
                 tc::fence_after();
                 split_state();
                 tc::fence_before();
