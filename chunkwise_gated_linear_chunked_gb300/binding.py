@@ -22,7 +22,7 @@ GLA_HEAD_FIRST = 0x100   # OR-ed into the dtype code: [B, H, T, *] tensors
 EXPORTS = ("gla_fwd", "gla_fwd_workspace_size", "gla_get_status", "gla_strerror", "gla_chunk_local_cumsum",
            "gla_profile_events", "gla_profile_launches", "gla_kernel_name", "gla_fwd_noalloc", "gla_bwd",
            "gla_bwd_workspace_size", "gla_ttt_linear_fwd", "gla_ttt_workspace_size", "gla_wy_fwd",
-           "gla_wy_workspace_size")
+           "gla_wy_workspace_size", "gla_fwd_host", "gla_fwd_host_workspace_size")
 
 if not os.path.exists(LIB):
     raise ImportError(f"libgla.so not built ({LIB}); call chunkwise_gated_linear_chunked_gb300.build.build()")
@@ -33,6 +33,10 @@ _lib.gla_fwd.argtypes = [_p, _p, _p, _p, _p, _f, _p, _p, _p, _i, _i, _i, _i, _i,
 _lib.gla_fwd.restype = _i
 _lib.gla_fwd_workspace_size.argtypes = [_i] * 8
 _lib.gla_fwd_workspace_size.restype = _sz
+_lib.gla_fwd_host.argtypes = [_p, _p, _p, _p, _p, _f, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _p, _sz, _p]
+_lib.gla_fwd_host.restype = _i
+_lib.gla_fwd_host_workspace_size.argtypes = [_i] * 9
+_lib.gla_fwd_host_workspace_size.restype = _sz
 _lib.gla_get_status.argtypes = [_p, _p]
 _lib.gla_get_status.restype = _i
 _lib.gla_strerror.argtypes = [_i]
@@ -133,6 +137,25 @@ def fwd_into(q, k, v, g, o, scale, h0, ht, cu_seqlens, N, B, T, H, K, V, chunk, 
     return int(_lib.gla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(o), float(scale), _ptr(h0), _ptr(ht),
                             _ptr(cu_seqlens), int(N), int(B), int(T), int(H), int(K), int(V), int(chunk),
                             int(dtype), _ptr(workspace), nbytes, _stream_handle(stream)))
+
+
+def host_workspace_size(B, T, H, K, V, N, chunk, dtype, head_groups) -> int:
+    return int(_lib.gla_fwd_host_workspace_size(int(B), int(T), int(H), int(K), int(V), int(N), int(chunk),
+                                                int(dtype), int(head_groups)))
+
+
+def fwd_host_into(q, k, v, g, o, scale, h0, ht, cu_seqlens, N, B, T, H, K, V, chunk, dtype, head_groups, workspace,
+                  stream=None) -> int:
+    """Raw call of gla_fwd_host: q, k, v, g, o, h0, ht, cu_seqlens are HOST tensors (or None), the workspace a
+    device tensor.  Returns the code."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("o", o), ("h0", h0), ("ht", ht),
+                    ("cu_seqlens", cu_seqlens)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise GlaError(GLA_ERR_INVALID_ARG, f"gla_fwd_host: {name} must be a contiguous host tensor")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return int(_lib.gla_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(o), float(scale), _ptr(h0), _ptr(ht),
+                                 _ptr(cu_seqlens), int(N), int(B), int(T), int(H), int(K), int(V), int(chunk),
+                                 int(dtype), int(head_groups), _ptr(workspace), nbytes, _stream_handle(stream)))
 
 
 def gla_fwd(q, k, v, g, scale=None, initial_state=None, output_final_state=True, cu_seqlens=None,

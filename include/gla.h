@@ -156,6 +156,38 @@ int gla_fwd_noalloc(const void *q, const void *k, const void *v, const void *g, 
                     int K, int V, int chunk, int dtype, void *stream);
 
 /*
+ * gla_fwd_host — gla_fwd on inputs and outputs in HOST memory (a serving path whose requests arrive in host
+ * memory).  It has no counterpart on the pages: the result is gla_fwd's, computed head group by head group.
+ *
+ * q, k, g [rows, H, K], v [rows, H, V], o [rows, H, V], h0 / ht [N, H, K, V] (fp32, each may be NULL) and
+ * cu_seqlens [N + 1] (int32 or NULL) are host pointers, time-major (GLA_HEAD_FIRST is rejected with
+ * GLA_ERR_UNSUPPORTED); page-locked host memory lets the copies run asynchronously and at full speed, other
+ * host memory works but is copied through staging.  The other arguments are gla_fwd's.  The H heads are
+ * processed in head_groups groups of H / head_groups heads (H must be a multiple of it, else
+ * GLA_ERR_INVALID_ARG): while one group's kernels run, the next group's inputs are copied to the device and
+ * the previous group's o (and ht) copied back, so a call takes about the time of its larger copy direction.
+ * Each group runs gla_fwd with H / head_groups heads; its segment plan can differ from that of one call with
+ * all H heads, so the two results agree within the arithmetic's rounding, not bit for bit.
+ *
+ * workspace: device memory of at least gla_fwd_host_workspace_size() bytes, 256-byte aligned, zeroed before
+ * its first use (it holds gla_fwd's workspace for one group, a copy of cu_seqlens and up to three groups'
+ * device buffers); gla_get_status() reads its status word.  Calls that share a workspace must be ordered on
+ * the GPU (for example on one stream).  The call enqueues everything on `stream` and on two side streams of
+ * its own (created on the first call from each host thread on each device, with their events, and kept until
+ * exit), joined back into `stream`: the host buffers may be read or reused once `stream` has reached that
+ * point.  Returns GLA_OK once enqueued, else a synchronous gla_status (GLA_ERR_WORKSPACE for a missing or
+ * small workspace, GLA_ERR_CUDA if an enqueue failed; work already enqueued then still runs).
+ */
+int gla_fwd_host(const void *q, const void *k, const void *v, const void *g, void *o, float scale,
+                 const float *h0, float *ht, const int32_t *cu_seqlens, int N, int B, int T, int H, int K,
+                 int V, int chunk, int dtype, int head_groups, void *workspace, size_t workspace_bytes,
+                 void *stream);
+
+/* Bytes of device workspace gla_fwd_host needs (0 for arguments it would reject). */
+size_t gla_fwd_host_workspace_size(int B, int T, int H, int K, int V, int N, int chunk, int dtype,
+                                   int head_groups);
+
+/*
  * gla_bwd — gradients of the forward above (page "fla/ops/gla/fused_chunk.py": fused_chunk_gla_bwd_kernel,
  * bwd_inner_chunk, FusedChunkGLAFunction.backward) for the loss L = sum(o * dout) + sum(ht * dht):
  *

@@ -202,3 +202,29 @@ def test_ttt_rejects_before_any_cuda_work(gla):
     assert ttt(gla, o=A + 64) == gla.GLA_ERR_INVALID_ARG                 # o overlaps q
     assert ttt(gla, ht=20 * A, hbt=20 * A + 64) == gla.GLA_ERR_INVALID_ARG   # the two final states overlap
     assert gla.lib().gla_ttt_workspace_size() >= 16
+
+
+def fwd_host(gla, q=A, k=2 * A, v=3 * A, g=4 * A, o=5 * A, scale=0.09, h0=None, ht=None, cu=None, N=2, B=2, T=100,
+             H=4, K=128, V=128, chunk=64, dtype=1, groups=2, ws=64 * A, wsb=1 << 34):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return gla.lib().gla_fwd_host(p(q), p(k), p(v), p(g), p(o), ctypes.c_float(scale), p(h0), p(ht), p(cu), N, B, T,
+                                  H, K, V, chunk, dtype, groups, p(ws), wsb, None)
+
+
+def test_host_entry_rejects_before_any_cuda_work(gla):
+    assert fwd_host(gla, groups=3) == gla.GLA_ERR_INVALID_ARG            # 4 heads in 3 groups
+    assert fwd_host(gla, groups=0) == gla.GLA_ERR_INVALID_ARG
+    assert fwd_host(gla, dtype=1 | gla.GLA_HEAD_FIRST) == gla.GLA_ERR_UNSUPPORTED
+    assert fwd_host(gla, K=96) == gla.GLA_ERR_UNSUPPORTED
+    assert fwd_host(gla, N=3) == gla.GLA_ERR_INVALID_ARG
+    assert fwd_host(gla, q=None) == gla.GLA_ERR_INVALID_ARG
+    assert fwd_host(gla, scale=0.0) == gla.GLA_ERR_INVALID_ARG
+    assert fwd_host(gla, ws=None) == gla.GLA_ERR_WORKSPACE
+    assert fwd_host(gla, wsb=1024) == gla.GLA_ERR_WORKSPACE
+    assert fwd_host(gla, ws=64 * A + 16) == gla.GLA_ERR_ALIGNMENT
+    lib = gla.lib()
+    lib.gla_fwd_host_workspace_size.restype = ctypes.c_size_t
+    assert lib.gla_fwd_host_workspace_size(2, 100, 4, 128, 128, 2, 64, 1, 3) == 0
+    two = lib.gla_fwd_host_workspace_size(2, 100, 4, 128, 128, 2, 64, 1, 2)
+    four = lib.gla_fwd_host_workspace_size(2, 100, 4, 128, 128, 2, 64, 1, 4)
+    assert 0 < four < two   # device buffers for at most three groups: 3 of 4 heads, against 2 slots of 2
