@@ -81,7 +81,7 @@ constexpr uint32_t kHalf = 8192;               // one 64-column half of a 64-row
 // two swizzled 64-column halves.  64 KB stages with a 16-bit gate (three in the ring), 80 KB with an fp32 gate
 // (two).
 constexpr int ST_Q0 = 0, ST_K0 = 8192, ST_G = 32768;
-constexpr int NBARS = 40;
+constexpr int NBARS = 42;
 template <int GB>   // bytes per gate element
 struct Ring {
     static constexpr int NSTAGE = GB == 2 ? 3 : 2;
@@ -512,6 +512,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t *item_full = bars + 27, *item_empty = bars + 31;              // [IQ]
     uint64_t *drain = bars + 35;
     uint64_t *eg_ready = bars + 36;                                        // [4]: by output chunk index
+    uint64_t *sop_free = bars + 40;                                        // [2]: MMA (a) of a chunk done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + NBARS);
     volatile int *misc = reinterpret_cast<volatile int *>(sm + OFF_MISC);   // [0..3] queue, [4] abort, [5] flag
     volatile int *iq = misc;
@@ -555,6 +556,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         bar_init(drain, 1);
         for (int i = 0; i < 4; ++i)
             bar_init(&eg_ready[i], 64);
+        for (int i = 0; i < 2; ++i)
+            bar_init(&sop_free[i], 1);
         bar_fence_init();
         misc[4] = 0;
         tma_prefetch_desc(&tm_q);
@@ -763,13 +766,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 return true;
             };
             // Output chunk gb needs four MMAs: (c) S += V^T k~ (needs the gating group's operands and the
-            // state group's S'), (b) the scores (operands only), (a) the inter-chunk product (S', and O^T free
-            // again), and later (d) O^T += V^T P^T (the P group's P).  They are issued as their inputs become
-            // ready, within the order the shared buffers impose: (d) of the previous chunk before (b) of this
-            // one (P in TMEM and in shared memory) and before (a) (both write O^T); (c) at any time.  Commits
-            // complete in issue order, so each also covers every earlier MMA: mma_st (after (c)) tells the
-            // state group that U and the previous chunk's S' buffer are ready, mma1 (after (b)) tells the P
-            // group that P and the shared P tile are, mma2 (after (d)) tells the output group that O^T is.
+            // state group's S'), (b) the scores (operands only), (a) the inter-chunk product (S' after (c), and
+            // O^T free again), and later (d) O^T += V^T P^T (the P group's P).  They are issued as their inputs
+            // become ready, within the order the shared buffers impose: (d) of the previous chunk before (b) of
+            // this one (P in TMEM and in shared memory) and before (a) (both write O^T); (c) of a chunk before
+            // its (a) and (d) (the stage is released after (d)).  Commits complete in issue order, so each also
+            // covers every earlier MMA: mma_st (after (c)) tells the state group that U is ready, sop_free
+            // (after (a)) that the chunk's S' buffer is free again, mma1 (after (b)) tells the P group that P
+            // and the shared P tile are, mma2 (after (d)) tells the output group that O^T is.
             auto run_o = [&](const Item &it) -> bool {
                 const uint32_t sb = tmem + TM_S + (it.itn & 1) * 128;
                 // Item itn - 2 (same state buffer) is finished before this item's commits: without this wait,
@@ -778,70 +782,70 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // at once in the steady state (that item's output pass completed two items ago).
                 if (it.itn >= 2 && !bar_wait(&tmem_free[it.itn & 1], ((it.itn - 2) >> 1) & 1, abort_w))
                     return false;
-                int pend = -1, pend_s = 0;   // output chunk whose (d) is still to be issued, and its stage
-                for (int c = 0; c < it.nchunks; ++c) {
-                    const int s = (qbase + c) % NSTAGE, gb = nb + c;
-                    const uint32_t st = smem_u32(sm + s * STAGE);
-                    bool have_ops = false, did_b = false, did_c = false, did_a = false;
-                    const unsigned long long t0 = global_ns();
-                    while (!(did_a && did_b && did_c)) {
-                        bool progress = false;
-                        if (pend >= 0 && bar_test(p_ready, pend & 1)) {
-                            fence_after();
-                            issue_d(pend_s);
-                            pend = -1;
-                            progress = true;
-                        }
-                        if (!have_ops && bar_test(&prep[s], ((qbase + c) / NSTAGE) & 1)) {
-                            fence_after();
-                            have_ops = true;
-                            progress = true;
-                        }
-                        if (have_ops && !did_b && pend < 0) {
-                            for (int kk = 0; kk < KD / 16; ++kk)
-                                mma_ss(tmem + TM_P, sdesc_sw128(st + (kk >> 2) * 16384 + ST_Q0 + (kk & 3) * 32),
-                                       sdesc_sw128(st + (kk >> 2) * 16384 + ST_K0 + (kk & 3) * 32), ID_N64, kk > 0);
-                            mma_commit(mma1);
-                            did_b = true;
-                            progress = true;
-                        }
-                        if (have_ops && !did_c && bar_test(ops_ready, gb & 1)) {
-                            fence_after();
-                            for (int kk = 0; kk < C / 16; ++kk)
-                                mma_ss(sb, sdesc_mn_sw128(st + ST_V + kk * 2048, kHalf),
-                                       sdesc_mn_sw128(st + ST_K0 + kk * 2048, kQK), ID_C, 1u);
-                            mma_commit(mma_st);
-                            did_c = true;
-                            progress = true;
-                        }
-                        if (did_c && !did_a && pend < 0 && (gb == 0 || bar_test(o_free, (gb - 1) & 1))) {
-                            fence_after();
-                            for (int kk = 0; kk < KD / 16; ++kk)
-                                mma_ts(tmem + TM_O, tmem + TM_SOP + (gb & 1) * 64 + kk * 8,
-                                       sdesc_sw128(st + (kk >> 2) * 16384 + ST_Q0 + (kk & 3) * 32), ID_N64,
-                                       kk > 0);
-                            did_a = true;
-                            progress = true;
-                        }
-                        if (!progress) {
-                            if (*abort_w)
-                                return false;
-                            if (global_ns() - t0 > kWaitNs) {
-                                *abort_w = 1;
-                                return false;
-                            }
-                            __nanosleep(20);
-                        }
+                // Cursors: the state chain ((c) of chunk jc as soon as its operands and S' are ready) runs ahead
+                // of the output chain ((b), (a), (d) of chunks jb, ja, jd), so the state recurrence does not wait
+                // for the epilogue that frees O^T.  (c) of a chunk precedes its (a) and (d) (the stage is
+                // released after (d)); (d) of a chunk precedes (b) and (a) of the next (P and O^T).
+                const int nch = it.nchunks;
+                int jb = 0, jc = 0, ja = 0, jd = 0;
+                auto stage_of = [&](int j) { return (qbase + j) % NSTAGE; };
+                auto ops_in = [&](int j) { return bar_test(&prep[stage_of(j)], ((qbase + j) / NSTAGE) & 1); };
+                unsigned long long t0 = global_ns();
+                while (jd < nch) {
+                    bool progress = false;
+                    if (jd < ja && bar_test(p_ready, (nb + jd) & 1)) {
+                        fence_after();
+                        issue_d(stage_of(jd));
+                        ++jd;
+                        progress = true;
                     }
-                    pend = gb;
-                    pend_s = s;
-                }
-                // (d) of the item's last chunk
-                if (pend >= 0) {
-                    if (!bar_wait(p_ready, pend & 1, abort_w))
-                        return false;
-                    fence_after();
-                    issue_d(pend_s);
+                    if (jc < nch && ops_in(jc) && bar_test(ops_ready, (nb + jc) & 1)) {
+                        fence_after();
+                        const uint32_t st = smem_u32(sm + stage_of(jc) * STAGE);
+                        for (int kk = 0; kk < C / 16; ++kk)
+                            mma_ss(sb, sdesc_mn_sw128(st + ST_V + kk * 2048, kHalf),
+                                   sdesc_mn_sw128(st + ST_K0 + kk * 2048, kQK), ID_C, 1u);
+                        mma_commit(mma_st);
+                        ++jc;
+                        progress = true;
+                    }
+                    if (jb < nch && jb <= jd && ops_in(jb)) {
+                        fence_after();
+                        const uint32_t st = smem_u32(sm + stage_of(jb) * STAGE);
+                        for (int kk = 0; kk < KD / 16; ++kk)
+                            mma_ss(tmem + TM_P, sdesc_sw128(st + (kk >> 2) * 16384 + ST_Q0 + (kk & 3) * 32),
+                                   sdesc_sw128(st + (kk >> 2) * 16384 + ST_K0 + (kk & 3) * 32), ID_N64, kk > 0);
+                        mma_commit(mma1);
+                        ++jb;
+                        progress = true;
+                    }
+                    if (ja < jc && ja <= jd && (nb + ja == 0 || bar_test(o_free, (nb + ja - 1) & 1))) {
+                        fence_after();
+                        const int gb = nb + ja;
+                        const uint32_t st = smem_u32(sm + stage_of(ja) * STAGE);
+                        for (int kk = 0; kk < KD / 16; ++kk)
+                            mma_ts(tmem + TM_O, tmem + TM_SOP + (gb & 1) * 64 + kk * 8,
+                                   sdesc_sw128(st + (kk >> 2) * 16384 + ST_Q0 + (kk & 3) * 32), ID_N64, kk > 0);
+                        mma_commit(&sop_free[gb & 1]);
+                        ++ja;
+                        progress = true;
+                    }
+                    if (progress) {
+                        t0 = global_ns();
+                    } else {
+                        if (*abort_w)
+                            return false;
+                        if (global_ns() - t0 > kWaitNs) {
+                            *abort_w = 1;
+                            return false;
+                        }
+                        // idle: wait on the state chain's next hand-over (the recurrence that sets the chunk
+                        // rate), waking when it completes or after a short while to look at the others
+                        if (jc < nch)
+                            bar_try_for(ops_ready, (nb + jc) & 1, 300);
+                        else
+                            bar_try_for(p_ready, (nb + jd) & 1, 300);
+                    }
                 }
                 mma_commit(&item_done[it.itn & 1]);
                 qbase += it.nchunks;
@@ -1011,10 +1015,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 return false;
             for (int c = 0; c < it.nchunks; ++c) {
                 const int gb = nb + c;
-                // U holds the previous chunk's contribution (its MMA (c) is complete, and with it the MMA (a)
-                // of the chunk before, the last reader of this chunk's S' buffer); the gating group has
-                // published this chunk's factors (it may still be forming the operands)
+                // U holds the previous chunk's contribution (its MMA (c) is complete); the MMA (a) two chunks
+                // back, the last reader of this chunk's S' buffer, is complete; the gating group has published
+                // this chunk's factors (it may still be forming the operands)
                 bool got = c == 0 || bar_wait(mma_st, (gb - 1) & 1, abort_w);
+                got = got && (gb < 2 || bar_wait(&sop_free[gb & 1], ((gb - 2) >> 1) & 1, abort_w));
                 got = got && bar_wait(&eg_ready[gb & 3], (gb >> 2) & 1, abort_w);
                 if (!__all_sync(0xffffffffu, got))
                     return false;

@@ -238,6 +238,18 @@ __device__ __forceinline__ bool bar_try(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// As bar_try with a suspend-time hint of `ns`: returns within about that time even if the phase is still open.
+__device__ __forceinline__ bool bar_try_for(uint64_t *bar, uint32_t parity, uint32_t ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}\n"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+                 : "memory");
+    return ok != 0;
+}
+
 // Non-blocking test of phase `parity` of `bar` (no suspension).
 __device__ __forceinline__ bool bar_test(uint64_t *bar, uint32_t parity)
 {
