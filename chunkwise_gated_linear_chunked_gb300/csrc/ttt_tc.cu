@@ -13,7 +13,7 @@
 // so k_t h_{t-1} is taken one mini-batch ahead, and the chain adds the correction on the CUDA cores (a
 // BT x BT by BT product per row) once W_{t-1} is known.  Per mini-batch t:
 //   * the split warps (which also form the outputs) cut h_t into two bf16 terms as soon as the update that
-//     made it is complete (h = h1 + h2 + e, |e| <= 2^-17 |h|, each term cut by integer rounding);
+//     made it is complete (h = h1 + h2 + e, |e| <= 2^-18 |h|, each term rounded to nearest by conversion);
 //   * one issuing thread then takes h_t^T [q_t; k_{t+1}]^T (tcgen05 kind::f16, A the two terms from TMEM,
 //     M = 128, N = 2 BT, K = D: the outputs' q h and the next mini-batch's k h_t) and the row products of the
 //     tile [k_t; q_t; k_{t+1}] with k_t (q k^T for the outputs, k_{t+1} k_t^T for the next correction);
@@ -94,37 +94,19 @@ __device__ __forceinline__ void split3(float a, float b, uint32_t &w1, uint32_t 
     w2 = __byte_perm(a2, b2, 0x7632);
     w3 = __byte_perm(__float_as_uint(sa), __float_as_uint(sb), 0x7632);
 }
-// Two fp32 values -> two bf16x2 words, x = x1 + x2 + e with |e| <= 2^-17 |x| (x1 rounded to 8 significant bits,
-// x2 the exact remainder rounded the same way).
-__device__ __forceinline__ void split2(float a, float b, uint32_t &w1, uint32_t &w2)
+// Two fp32 values -> two bf16x2 words by the conversion instruction (round to nearest): x = x1 + x2 + e with
+// |e| <= 2^-18 |x| (x1 = bf16(x), x2 = bf16(x - x1), the remainder exact by Sterbenz's lemma).  Six
+// instructions a pair against the integer cut's twelve.
+__device__ __forceinline__ void split2_rn(float a, float b, uint32_t &w1, uint32_t &w2)
 {
-    const uint32_t a1 = bf16_cut(__float_as_uint(a)), b1 = bf16_cut(__float_as_uint(b));
-    const float ra = a - __uint_as_float(a1), rb = b - __uint_as_float(b1);
-    w1 = __byte_perm(a1, b1, 0x7632);
-    w2 = __byte_perm(bf16_cut(__float_as_uint(ra)), bf16_cut(__float_as_uint(rb)), 0x7632);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);   // .x = a (low half), .y = b
+    w1 = *reinterpret_cast<const uint32_t *>(&h);
+    const float ra = a - __uint_as_float(w1 << 16), rb = b - __uint_as_float(w1 & 0xFFFF0000u);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(ra, rb);
+    w2 = *reinterpret_cast<const uint32_t *>(&l);
 }
 __device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
-// (mean, M2) of one value per lane over the warp (pairwise merges of equal counts)
-__device__ __forceinline__ void warp_stats(float x, float &mean, float &m2)
-{
-    mean = x;
-    m2 = 0.f;
-#pragma unroll
-    for (int o = 1, n = 1; o < 32; o <<= 1, n <<= 1) {
-        const float om = __shfl_xor_sync(0xffffffffu, mean, o), o2 = __shfl_xor_sync(0xffffffffu, m2, o);
-        const float d = om - mean;
-        m2 = m2 + o2 + d * d * (0.5f * n);   // two groups of n: n * n / (2 n)
-        mean = 0.5f * (mean + om);
-    }
-}
-__device__ __forceinline__ float warp_sum(float x)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
 // merge the four quadrants' (mean, M2) of 32 values each: mean and 1 / sqrt(var + eps)
 __device__ __forceinline__ void merge4(const float *red, int BT, int i, float eps, float &mean, float &rstd)
 {
@@ -603,7 +585,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 tc::tmem_wait_ld(r);
 #pragma unroll
                 for (int u = 0; u < 16; ++u)
-                    split2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]), w1[u], w2[u]);
+                    split2_rn(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]), w1[u], w2[u]);
                 tc::tmem_st16(tl + L::HS + 0 * 64 + c0 / 2, w1);
                 tc::tmem_st16(tl + L::HS + 1 * 64 + c0 / 2, w2);
             }
