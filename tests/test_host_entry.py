@@ -30,6 +30,31 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("variant", ["fp32_gate", "bf16_output"])
+def test_host_entry_dtype_variants(variant):
+    """fp32 g with bf16 q, k, v and bf16 o: the copies size each tensor by its own element type."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    inp = make_inputs("bf16", B=2, T=260, H=4, K=128, V=128, h0=True, seed=91)
+    g32 = torch.nn.functional.logsigmoid(torch.randn(inp.g.shape, generator=torch.Generator().manual_seed(5))) / 16
+    code = binding.GLA_BF16_GF32 if variant == "fp32_gate" else binding.GLA_BF16_OBF16
+    g_host = g32 if variant == "fp32_gate" else inp.g
+    B, T, H, K, V, N = 2, 260, 4, 128, 128, 2
+    pin = lambda x: x.contiguous().pin_memory()
+    out_dtype = torch.bfloat16 if variant == "bf16_output" else torch.float32
+    o = torch.empty(B, T, H, V, dtype=out_dtype).pin_memory()
+    ht = torch.empty(N, H, K, V).pin_memory()
+    ws = torch.zeros(binding.host_workspace_size(B, T, H, K, V, N, 64, code, 2), dtype=torch.uint8, device="cuda")
+    rc = binding.fwd_host_into(pin(inp.q), pin(inp.k), pin(inp.v), pin(g_host), o, inp.scale, pin(inp.h0), ht, None,
+                               N, B, T, H, K, V, 64, code, 2, ws)
+    assert rc == 0
+    torch.cuda.synchronize()
+    od, htd = binding.gla_fwd(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), g_host.cuda(), scale=inp.scale,
+                              initial_state=inp.h0.cuda(), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert_close(as_f64(o), as_f64(od), TOL["bf16"], "o vs gla_fwd")
+    assert_close(as_f64(ht), as_f64(htd), TOL["bf16"], "ht vs gla_fwd")
+
+
 def _id(c):
     return f"{c[0]}-B{c[1]}T{c[2]}H{c[3]}K{c[4]}V{c[5]}-G{c[8]}" + ("-var" if c[7] else "")
 
