@@ -46,20 +46,24 @@ struct TtcLayout {
     static constexpr int V2T = VR + 3 * BT * D * 2;  // [3] terms of -eta_last v2, MN-major: [BT rows][2 halves]
     static constexpr int V2H = BT * 128;             // one 64-column half of a term
     static constexpr int V2F = V2T + 3 * 2 * V2H;    // [2][BT][D] v2 fp32, by parity
-    static constexpr int AS = V2F + 2 * BT * D * 4;  // [2][BT][BT] q k^T (unscaled), by parity
-    static constexpr int KK = AS + 2 * BT * BT * 4;  // [2][BT][BT] k_{t+1} k_t^T, by parity of t
-    static constexpr int RED = KK + 2 * BT * BT * 4; // [2 (statistics, gradient sums)][4 quadrants][BT][2]
+    // the B operands of the small products with W = -eta_last v2 (K-major, 128-byte swizzle, BT rows of BT
+    // K values): two bf16 terms of k_{t+1} k_t^T (the next correction), two of the outputs' scaled scores
+    static constexpr int TB = BT * 128;
+    static constexpr int MT = (V2F + 2 * BT * D * 4 + 1023) / 1024 * 1024;
+    static constexpr int KKT = MT, MST = MT + 2 * TB;
+    static constexpr int RED = MT + 4 * TB;          // [2 (statistics, gradient sums)][4 quadrants][BT][2]
     static constexpr int ET = RED + 2 * 4 * BT * 2 * 4;  // [3][BT] learning rates (0 past the end)
     static constexpr int E2 = ET + 3 * BT * 4;       // [2][BT + 1] the outputs' learning rates and eta_last
     static constexpr int RED2 = E2 + 2 * (BT + 4) * 4;   // [4][BT][2] the output warps' partial statistics
-    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3]; TMEM address; abort word
-    static constexpr int BAR = RED2 + 4 * BT * 2 * 4;
+    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3], kk_ready, tail[2]; TMEM
+    // address; abort word
+    static constexpr int BAR = (RED2 + 4 * BT * 2 * 4 + 7) / 8 * 8;
     // the row products read rows 0..127 of a tile with K-halves XH apart: keep that span allocated
-    static constexpr int END = BAR + 128 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 128 : X0 + 2 * XB + XH + 128 * 128;
+    static constexpr int END = BAR + 160 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 160 : X0 + 2 * XB + XH + 128 * 128;
     static constexpr int BYTES = END + 1024;
     // TMEM columns: the state, its two bf16 terms (64 columns each), [q h_t, k_{t+1} h_t]^T by parity, the row
-    // products by parity
-    static constexpr uint32_t HT = 0, HS = 128, DA = 256, DC = 384, COLS = 512;
+    // products by parity, the outputs' score-weighted sums of v2 by parity
+    static constexpr uint32_t HT = 0, HS = 128, DA = 256, DC = 384, DO = 448, COLS = 512;
     static_assert(VR % 1024 == 0 && V2T % 1024 == 0, "swizzled tiles are 1024-byte aligned");
 };
 
@@ -273,8 +277,9 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     uint64_t *prod = bar, *upd = bar + 1, *hs_ready = bar + 2, *v2t_ready = bar + 3;
     uint64_t *v2_full = bar + 4, *out_free = bar + 6;
     uint64_t *xfull = bar + 8, *slot_free = bar + 11;   // [3] by mini-batch mod 3: the tile's rows landed / free
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 112);
-    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 116);
+    uint64_t *kk_ready = bar + 14, *tail = bar + 15;    // the small products' B operands staged / done [2]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 136);
+    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 140);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, qd = warp & 3, rh = (warp >> 2) & 1;
     const int ctid = tid & 255;                          // index within the role
     const int m = 32 * qd + lane;                        // this thread's TMEM lane: output feature m
@@ -310,6 +315,9 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             tc::bar_init(&xfull[b], 32);   // one completion-tracked arrival per lane of the copy warp
             tc::bar_init(&slot_free[b], 1);
         }
+        tc::bar_init(kk_ready, 1);
+        tc::bar_init(&tail[0], 1);
+        tc::bar_init(&tail[1], 1);
         *abort_w = 0;
         tc::bar_fence_init();
     }
@@ -370,6 +378,23 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                                    tc::sdesc_mn_sw128(xs + ks * 2048, L::XH), ID_B, 1u);
                 tc::mma_commit(upd);
                 tc::mma_commit(&slot_free[t % 3]);
+                // the small products with W_t (its three terms, MN-major A): the outputs' sums
+                // -eta_i sum_j (scale q_i.k_j + 1) v2_j, and the correction (k_{t+1} k_t^T) W_t onto k_{t+1} h_t
+                if (!(ok = tc::bar_wait(kk_ready, t & 1, abort_w)))
+                    break;
+                tc::fence_after();
+                constexpr uint32_t ID_W = idesc_bf16(128, BT) | tc::kIdescAMajorMN;
+                for (int tw = 0; tw < 3; ++tw)
+                    for (int tb = 0; tb < 2; ++tb)
+                        for (int ks = 0; ks < BT / 16; ++ks) {
+                            const uint64_t aw = tc::sdesc_mn_sw128(sb + L::V2T + tw * 2 * L::V2H + ks * 2048, L::V2H);
+                            tc::mma_ss(tmem + L::DO + 32 * p, aw, tc::sdesc_sw128(sb + L::MST + tb * L::TB + ks * 32),
+                                       ID_W, (tw | tb | ks) ? 1u : 0u);
+                            if (t + 1 < nmb)
+                                tc::mma_ss(tmem + L::DA + 64 * p + BT, aw,
+                                           tc::sdesc_sw128(sb + L::KKT + tb * L::TB + ks * 32), ID_W, 1u);
+                        }
+                tc::mma_commit(&tail[p]);
             }
         }
     } else if (warp == 17) {
@@ -407,13 +432,18 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;
         const float wm = a.w[(size_t)h * D + m], bm = a.b[(size_t)h * D + m];
         float *RED = reinterpret_cast<float *>(sm + L::RED), *RSG = RED + 4 * BT * 2;
-        float elp = 0.f;   // eta_last of the previous mini-batch
         for (int t = 0; t < nmb && ok; ++t) {
             const int p = t & 1, r0 = bos + t * BT, len = min(BT, eos - r0);
             const unsigned char *xt = sm + L::X0 + (t % 3) * L::XB;
-            // ---- k_t h_t + hb = (k_t h_{t-1}) + (k_t k_{t-1}^T) W_{t-1} + hb for this half's rows
+            // ---- k_t h_t + hb = (k_t h_{t-1} + (k_t k_{t-1}^T) W_{t-1}) + hb for this half's rows
             if (t == 0) {
                 ok = tc::bar_wait(prod, 0, abort_w) && ok;   // k_0 h_0
+                tc::fence_after();
+            } else {
+                // k_t h_{t-1} and its correction (k_t k_{t-1}^T) W_{t-1} are summed in TMEM
+                if (ctid == 0)
+                    ok = tc::bar_wait(&tail[p ^ 1], ((t - 1) >> 1) & 1, abort_w) && ok;
+                ok = role_all(ok, 1);
                 tc::fence_after();
             }
             float kh[HB];
@@ -423,28 +453,6 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
 #pragma unroll
                 for (int u = 0; u < HB; ++u)
                     kh[u] = __uint_as_float(r[u]) + hb;
-            }
-            if (t > 0) {
-                const float *V2P = reinterpret_cast<const float *>(sm + L::V2F + (p ^ 1) * BT * D * 4);
-                const float *KKP = reinterpret_cast<const float *>(sm + L::KK + (p ^ 1) * BT * BT * 4);
-                float wj[BT];
-#pragma unroll
-                for (int j = 0; j < BT; ++j)
-                    wj[j] = -elp * V2P[j * D + m];
-#pragma unroll
-                for (int u = 0; u < HB; ++u) {
-                    const int i = r0h + u;
-                    float c = 0.f;
-#pragma unroll
-                    for (int j4 = 0; j4 < BT; j4 += 4) {
-                        const float4 k4 = *reinterpret_cast<const float4 *>(KKP + i * BT + j4);
-                        c = fmaf(k4.x, wj[j4], c);
-                        c = fmaf(k4.y, wj[j4 + 1], c);
-                        c = fmaf(k4.z, wj[j4 + 2], c);
-                        c = fmaf(k4.w, wj[j4 + 3], c);
-                    }
-                    kh[u] += c;
-                }
             }
             // ---- LayerNorm statistics of the rows (one thread also sees this mini-batch's k and v rows landed;
             // the barrier passes that on)
@@ -518,10 +526,12 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             for (int j = 0; j < BT; ++j)
                 sv += V2F[j * D + m];
             hb = fmaf(-el, sv, hb);
-            elp = el;
             // ---- this mini-batch's products are complete: the outputs' masked scores (scale q_i.k_j + 1 for
             // j <= i) and k_{t+1} k_t^T for the next correction to shared memory (the warps of row half 0 that
             // hold those TMEM lanes)
+            // ---- this mini-batch's products are complete: the B operands of the small products to shared memory
+            // in two bf16 terms (the warps of row half 0 that hold those TMEM lanes): the outputs' scores
+            // (eta_i / eta_last)(scale q_i.k_j + 1) for j <= i (0 above the diagonal), and k_{t+1} k_t^T
             if (rh == 0 && (qd == BT / 32 || qd == BT / 16)) {
                 ok = tc::bar_wait(prod, t & 1, abort_w) && ok;
                 tc::fence_after();
@@ -529,24 +539,34 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 tmem_ldn<BT>(tl + L::DC + 32 * p, r);
                 const bool sc = qd == BT / 32;
                 const int row = m - (sc ? BT : 2 * BT);
-                float *dst = reinterpret_cast<float *>(sm + (sc ? L::AS : L::KK) + p * BT * BT * 4);
-                if (row >= 0 && row < BT)
+                if (row >= 0 && row < BT) {
+                    const float *E2 = reinterpret_cast<const float *>(sm + L::E2 + p * (BT + 4) * 4);
+                    const float f = sc ? E2[row] / E2[BT] : 1.f;
+                    unsigned char *t0 = sm + (sc ? L::MST : L::KKT), *t1 = t0 + L::TB;
 #pragma unroll
-                    for (int j = 0; j < BT; j += 4) {
-                        float4 x = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                               __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                        if (sc) {
-                            x.x = j <= row ? fmaf(scale, x.x, 1.f) : 0.f;
-                            x.y = j + 1 <= row ? fmaf(scale, x.y, 1.f) : 0.f;
-                            x.z = j + 2 <= row ? fmaf(scale, x.z, 1.f) : 0.f;
-                            x.w = j + 3 <= row ? fmaf(scale, x.w, 1.f) : 0.f;
+                    for (int j = 0; j < BT; j += 8) {
+                        uint32_t w1[4], w2[4];
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            float x0 = __uint_as_float(r[j + e]), x1 = __uint_as_float(r[j + e + 1]);
+                            if (sc) {
+                                x0 = j + e <= row ? f * fmaf(scale, x0, 1.f) : 0.f;
+                                x1 = j + e + 1 <= row ? f * fmaf(scale, x1, 1.f) : 0.f;
+                            }
+                            split2_rn(x0, x1, w1[e / 2], w2[e / 2]);
                         }
-                        *reinterpret_cast<float4 *>(dst + row * BT + j) = x;
+                        const uint32_t off = tc::sw128(row, j);
+                        *reinterpret_cast<uint4 *>(t0 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                        *reinterpret_cast<uint4 *>(t1 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
                     }
+                    tc::fence_proxy_async();
+                }
             }
             tc::fence_before();
             ok = role_all(ok, 1);   // (the staging warps' wait)
-            tc::bar_arrive(&v2_full[p]);   // this mini-batch's q h columns, scores, v2 and rates: to the outputs
+            if (ctid == 0)
+                tc::bar_arrive(kk_ready);
+            tc::bar_arrive(&v2_full[p]);   // this mini-batch's q h columns, v2 and rates: to the outputs
         }
         if (nmb > 0) {
             ok = tc::bar_wait(upd, (nmb - 1) & 1, abort_w) && ok;   // the last update
@@ -609,8 +629,8 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             if (ctid == 0)
                 tc::bar_arrive(hs_ready);
         }
-        // q h + hb - eta_i sum_{j<=i} (scale q_i.k_j + 1) v2_j from the mini-batch's q h columns, masked scores and
-        // v2, then o + LN(o) w + b
+        // q h + hb - eta_i sum_{j<=i} (scale q_i.k_j + 1) v2_j from the mini-batch's q h columns and the
+        // score-weighted sums of v2 (both in TMEM), then o + LN(o) w + b
         float *RED2 = reinterpret_cast<float *>(sm + L::RED2);
         for (int t = 0; t < nmb && ok; ++t) {
             const int p = t & 1, r0 = bos + t * BT, len = min(BT, eos - r0);
@@ -627,37 +647,25 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     tc::bar_arrive(hs_ready);
             }
             ok = tc::bar_wait(&v2_full[p], (t >> 1) & 1, abort_w) && ok;
+            if (ctid == 0)
+                ok = tc::bar_wait(&tail[p], (t >> 1) & 1, abort_w) && ok;   // the score-weighted sums of v2
+            ok = role_all(ok, 2);
             tc::fence_after();
-            uint32_t r[HB];
+            uint32_t r[HB], dz[HB];
             tmem_ldn<HB>(tl + L::DA + 64 * p + r0h, r);
+            tmem_ldn<HB>(tl + L::DO + 32 * p + r0h, dz);
             const float *V2F = reinterpret_cast<const float *>(sm + L::V2F + p * BT * D * 4);
-            const float *AS = reinterpret_cast<const float *>(sm + L::AS + p * BT * BT * 4);
             const float *E2 = reinterpret_cast<const float *>(sm + L::E2 + p * (BT + 4) * 4);
-            float v2c[BT];
-#pragma unroll
-            for (int j = 0; j < BT; ++j)
-                v2c[j] = V2F[j * D + m];
             float ov[HB];
 #pragma unroll
-            for (int u = 0; u < HB; ++u) {
-                const int i = r0h + u;
-                float acc = 0.f;
-#pragma unroll
-                for (int j4 = 0; j4 < BT; j4 += 4) {
-                    const float4 s4 = *reinterpret_cast<const float4 *>(AS + i * BT + j4);
-                    acc = fmaf(s4.x, v2c[j4], acc);
-                    acc = fmaf(s4.y, v2c[j4 + 1], acc);
-                    acc = fmaf(s4.z, v2c[j4 + 2], acc);
-                    acc = fmaf(s4.w, v2c[j4 + 3], acc);
-                }
-                ov[u] = fmaf(-E2[i], acc, fmaf(scale, __uint_as_float(r[u]), hb));
-            }
+            for (int u = 0; u < HB; ++u)   // q h + hb - eta_i sum_{j<=i} (scale q_i.k_j + 1) v2_j
+                ov[u] = fmaf(scale, __uint_as_float(r[u]), hb) + __uint_as_float(dz[u]);
             warp_row_stats<HB>(ov, RED2, qd, BT, r0h, lane);
             const float el = E2[BT];
             float sv = 0.f;
 #pragma unroll
             for (int j = 0; j < BT; ++j)
-                sv += v2c[j];
+                sv += V2F[j * D + m];
             out_sync();
             {
                 float mean[HB], rstd[HB];
