@@ -10,8 +10,9 @@
 // h (h^T[m][.]).  The serial chain of mini-batches never waits for a product of the state: with W_t =
 // -eta_last v2_t (the update h_{t+1} = h_t + k_t^T W_t),
 //   k_t h_t = k_t h_{t-1} + (k_t k_{t-1}^T) W_{t-1},
-// so k_t h_{t-1} is taken one mini-batch ahead, and the chain adds the correction on the CUDA cores (a
-// BT x BT by BT product per row) once W_{t-1} is known.  Per mini-batch t:
+// so k_t h_{t-1} is taken one mini-batch ahead and the correction, a product of k_t k_{t-1}^T (staged in
+// two bf16 terms one mini-batch ahead) with W_{t-1}'s three exact terms, is the first product issued once
+// W_{t-1} is known.  Per mini-batch t:
 //   * the split warps (which also form the outputs) cut h_t into two bf16 terms as soon as the update that
 //     made it is complete (h = h1 + h2 + e, |e| <= 2^-18 |h|, each term rounded to nearest by conversion);
 //   * one issuing thread then takes h_t^T [q_t; k_{t+1}]^T (tcgen05 kind::f16, A the two terms from TMEM,
@@ -21,8 +22,9 @@
 //     warps of 32, merged through shared memory) and v2_t; -eta_last v2_t is split exactly into three bf16
 //     terms (MN-major A) and the update h^T += W^T k is one more product accumulating into the fp32 state
 //     (B: the k rows of the tile, MN-major), so the state itself is never rewritten by the CUDA cores;
-//   * the outputs of a mini-batch are formed one mini-batch behind from its q h columns, scores, v2 and
-//     learning rates, kept in buffers by parity and released through mbarriers.
+//   * the outputs of a mini-batch are formed one mini-batch behind from its q h columns, v2, learning rates
+//     and the product of its masked scores (staged by two of the output warps) with W_t, kept in buffers by
+//     parity and released through mbarriers.
 // Rows arrive by asynchronous copies two mini-batches ahead (three tiles in turn); rows past the end of a
 // sequence are zero in k and q and take no part in the update (as the CUDA-core path).
 #include <cuda_bf16.h>
@@ -35,7 +37,8 @@ namespace gla {
 namespace {
 
 constexpr int D = 128;
-constexpr int NTH = 576;   // warps 0-7: the chain; 8-15: the state split and the outputs; 16: MMA issue; 17: row copies
+constexpr int NTH = 640;   // warps 0-7: the chain; 8-15: the state split and the outputs; 16-19: MMA issue, row
+                           // copies and the two warps that stage the small products' B operands
 
 template <int BT>
 struct TtcLayout {
@@ -55,8 +58,8 @@ struct TtcLayout {
     static constexpr int ET = RED + 2 * 4 * BT * 2 * 4;  // [3][BT] learning rates (0 past the end)
     static constexpr int E2 = ET + 3 * BT * 4;       // [2][BT + 1] the outputs' learning rates and eta_last
     static constexpr int RED2 = E2 + 2 * (BT + 4) * 4;   // [4][BT][2] the output warps' partial statistics
-    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3], kk_ready, tail[2]; TMEM
-    // address; abort word
+    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3], kk_ready, tail[2], corr;
+    // TMEM address; abort word
     static constexpr int BAR = (RED2 + 4 * BT * 2 * 4 + 7) / 8 * 8;
     // the row products read rows 0..127 of a tile with K-halves XH apart: keep that span allocated
     static constexpr int END = BAR + 160 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 160 : X0 + 2 * XB + XH + 128 * 128;
@@ -278,8 +281,9 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     uint64_t *v2_full = bar + 4, *out_free = bar + 6;
     uint64_t *xfull = bar + 8, *slot_free = bar + 11;   // [3] by mini-batch mod 3: the tile's rows landed / free
     uint64_t *kk_ready = bar + 14, *tail = bar + 15;    // the small products' B operands staged / done [2]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 136);
-    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 140);
+    uint64_t *corr = bar + 17;                           // the correction onto the next k h is done
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 144);
+    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 148);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, qd = warp & 3, rh = (warp >> 2) & 1;
     const int ctid = tid & 255;                          // index within the role
     const int m = 32 * qd + lane;                        // this thread's TMEM lane: output feature m
@@ -315,9 +319,10 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             tc::bar_init(&xfull[b], 32);   // one completion-tracked arrival per lane of the copy warp
             tc::bar_init(&slot_free[b], 1);
         }
-        tc::bar_init(kk_ready, 1);
+        tc::bar_init(kk_ready, 2);   // one arrival per staging warp
         tc::bar_init(&tail[0], 1);
         tc::bar_init(&tail[1], 1);
+        tc::bar_init(corr, 1);
         *abort_w = 0;
         tc::bar_fence_init();
     }
@@ -332,7 +337,10 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     const int r0h = HB * rh;   // first row of this thread's half
     bool ok = true;
 
-    if (warp == 16) {
+    // warps 16-19: the two staging warps are the ones whose TMEM lane quarter holds the row products' score rows
+    // (lanes BT..2 BT-1) and k_{t+1} k_t^T rows (lanes 2 BT..3 BT-1); the issue and copy warps take the others
+    constexpr int W_SC = 16 + BT / 32, W_KK = 16 + BT / 16, W_ISSUE = BT == 16 ? 18 : 16, W_COPY = 19;
+    if (warp == W_ISSUE) {
         // ================================ MMA issue ================================
         if (lane == 0) {
             constexpr uint32_t ID_Q = idesc_bf16(128, 2 * BT), ID_C = idesc_bf16(128, BT);
@@ -368,36 +376,83 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     tc::mma_ss(tmem + L::DC + 32 * p, dx, dx, ID_C, ks ? 1u : 0u);
                 }
                 tc::mma_commit(prod);
-                // the update h^T += (-eta_last v2_t)^T k_t into the fp32 state
-                if (!(ok = tc::bar_wait(v2t_ready, t & 1, abort_w)))
+                // W_t's terms (the chain) and the small products' B operands (two output warps) are in place
+                if (!(ok = tc::bar_wait(v2t_ready, t & 1, abort_w) && tc::bar_wait(kk_ready, t & 1, abort_w)))
                     break;
                 tc::fence_after();
+                // first the correction (k_{t+1} k_t^T) W_t onto k_{t+1} h_t, which the chain waits for; W_t in three
+                // terms (MN-major A), k_{t+1} k_t^T in two
+                constexpr uint32_t ID_W = idesc_bf16(128, BT) | tc::kIdescAMajorMN;
+                if (t + 1 < nmb)
+                    for (int tw = 0; tw < 3; ++tw)
+                        for (int tb = 0; tb < 2; ++tb)
+                            for (int ks = 0; ks < BT / 16; ++ks)
+                                tc::mma_ss(tmem + L::DA + 64 * p + BT,
+                                           tc::sdesc_mn_sw128(sb + L::V2T + tw * 2 * L::V2H + ks * 2048, L::V2H),
+                                           tc::sdesc_sw128(sb + L::KKT + tb * L::TB + ks * 32), ID_W, 1u);
+                tc::mma_commit(corr);
+                // the update h^T += W_t^T k_t into the fp32 state
                 for (int tt = 0; tt < 3; ++tt)
                     for (int ks = 0; ks < BT / 16; ++ks)
                         tc::mma_ss(tmem + L::HT, tc::sdesc_mn_sw128(sb + L::V2T + tt * 2 * L::V2H + ks * 2048, L::V2H),
                                    tc::sdesc_mn_sw128(xs + ks * 2048, L::XH), ID_B, 1u);
                 tc::mma_commit(upd);
                 tc::mma_commit(&slot_free[t % 3]);
-                // the small products with W_t (its three terms, MN-major A): the outputs' sums
-                // -eta_i sum_j (scale q_i.k_j + 1) v2_j, and the correction (k_{t+1} k_t^T) W_t onto k_{t+1} h_t
-                if (!(ok = tc::bar_wait(kk_ready, t & 1, abort_w)))
-                    break;
-                tc::fence_after();
-                constexpr uint32_t ID_W = idesc_bf16(128, BT) | tc::kIdescAMajorMN;
+                // the outputs' sums -eta_i sum_j (scale q_i.k_j + 1) v2_j
                 for (int tw = 0; tw < 3; ++tw)
                     for (int tb = 0; tb < 2; ++tb)
-                        for (int ks = 0; ks < BT / 16; ++ks) {
-                            const uint64_t aw = tc::sdesc_mn_sw128(sb + L::V2T + tw * 2 * L::V2H + ks * 2048, L::V2H);
-                            tc::mma_ss(tmem + L::DO + 32 * p, aw, tc::sdesc_sw128(sb + L::MST + tb * L::TB + ks * 32),
-                                       ID_W, (tw | tb | ks) ? 1u : 0u);
-                            if (t + 1 < nmb)
-                                tc::mma_ss(tmem + L::DA + 64 * p + BT, aw,
-                                           tc::sdesc_sw128(sb + L::KKT + tb * L::TB + ks * 32), ID_W, 1u);
-                        }
+                        for (int ks = 0; ks < BT / 16; ++ks)
+                            tc::mma_ss(tmem + L::DO + 32 * p,
+                                       tc::sdesc_mn_sw128(sb + L::V2T + tw * 2 * L::V2H + ks * 2048, L::V2H),
+                                       tc::sdesc_sw128(sb + L::MST + tb * L::TB + ks * 32), ID_W,
+                                       (tw | tb | ks) ? 1u : 0u);
                 tc::mma_commit(&tail[p]);
             }
         }
-    } else if (warp == 17) {
+    } else if (warp == W_SC || warp == W_KK) {
+        // ============ the B operands of the small products with W_t ============
+        // to shared memory in two bf16 terms: the outputs' scores (eta_i / eta_last)(scale q_i.k_j + 1) for
+        // j <= i (0 above the diagonal), and k_{t+1} k_t^T, once the mini-batch's row products are complete
+        // and the last mini-batch's small products (which read these buffers) are done
+        const bool sc = warp == W_SC;
+        for (int t = 0; t < nmb && ok; ++t) {
+            const int p = t & 1, len = min(BT, eos - (bos + t * BT));
+            ok = tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w) && tc::bar_wait(prod, t & 1, abort_w) &&
+                 (t == 0 || tc::bar_wait(&tail[p ^ 1], ((t - 1) >> 1) & 1, abort_w));
+            if (!ok)
+                break;
+            tc::fence_after();
+            uint32_t r[BT];
+            tmem_ldn<BT>(tl + L::DC + 32 * p, r);
+            const int row = m - (sc ? BT : 2 * BT);
+            if (row >= 0 && row < BT) {
+                const float *ET = reinterpret_cast<const float *>(sm + L::ET + (t % 3) * BT * 4);
+                const float f = sc ? ET[row] / ET[len - 1] : 1.f;
+                unsigned char *t0 = sm + (sc ? L::MST : L::KKT), *t1 = t0 + L::TB;
+#pragma unroll
+                for (int j = 0; j < BT; j += 8) {
+                    uint32_t w1[4], w2[4];
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        float x0 = __uint_as_float(r[j + e]), x1 = __uint_as_float(r[j + e + 1]);
+                        if (sc) {
+                            x0 = j + e <= row ? f * fmaf(scale, x0, 1.f) : 0.f;
+                            x1 = j + e + 1 <= row ? f * fmaf(scale, x1, 1.f) : 0.f;
+                        }
+                        split2_rn(x0, x1, w1[e / 2], w2[e / 2]);
+                    }
+                    const uint32_t off = tc::sw128(row, j);
+                    *reinterpret_cast<uint4 *>(t0 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+                    *reinterpret_cast<uint4 *>(t1 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+                }
+                tc::fence_proxy_async();
+            }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0)
+                tc::bar_arrive(kk_ready);
+        }
+    } else if (warp == W_COPY) {
         // ================================ row copies ================================
         // mini-batch t's rows into tile t mod 3: k_t (rows 0..BT-1), q_t (BT..), k_{t+1} (2 BT..), zero past the
         // end; its v rows and learning rates.  Each lane's copies arrive on the tile's barrier as they land.
@@ -442,7 +497,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             } else {
                 // k_t h_{t-1} and its correction (k_t k_{t-1}^T) W_{t-1} are summed in TMEM
                 if (ctid == 0)
-                    ok = tc::bar_wait(&tail[p ^ 1], ((t - 1) >> 1) & 1, abort_w) && ok;
+                    ok = tc::bar_wait(corr, (t - 1) & 1, abort_w) && ok;
                 ok = role_all(ok, 1);
                 tc::fence_after();
             }
@@ -477,11 +532,12 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 }
             }
             warp_row_sums<HB>(gg, gx, RSG, qd, BT, r0h, lane);
-            // the last update is complete (its v2 terms may be overwritten) and the outputs of two mini-batches
-            // ago are done with this parity's buffers: one thread waits, the barrier passes it on
+            // the last mini-batch's products with W are complete (its terms may be overwritten) and the outputs
+            // of two mini-batches ago are done with this parity's buffers: one thread waits, the barrier passes
+            // it on
             if (ctid == 0) {
                 if (t > 0)
-                    ok = tc::bar_wait(upd, (t - 1) & 1, abort_w) && ok;
+                    ok = tc::bar_wait(&tail[p ^ 1], ((t - 1) >> 1) & 1, abort_w) && ok;
                 if (t >= 2)
                     ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w) && ok;
             }
@@ -499,7 +555,8 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     V2F[(r0h + u) * D + m] = v2[u];
                 }
             }
-            if (ctid <= BT) {   // the learning rates and eta_last for the output warps
+            if (ctid <= BT) {   // the learning rates and eta_last for the output warps (the rates' slot is
+                                // refilled before the outputs run)
                 float *E2 = reinterpret_cast<float *>(sm + L::E2 + p * (BT + 4) * 4);
                 E2[ctid] = ctid < BT ? ET[ctid] : el;
             }
@@ -518,6 +575,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 }
             }
             tc::fence_proxy_async();
+            tc::fence_before();
             chain_sync();
             if (ctid == 0)
                 tc::bar_arrive(v2t_ready);
@@ -526,47 +584,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             for (int j = 0; j < BT; ++j)
                 sv += V2F[j * D + m];
             hb = fmaf(-el, sv, hb);
-            // ---- this mini-batch's products are complete: the outputs' masked scores (scale q_i.k_j + 1 for
-            // j <= i) and k_{t+1} k_t^T for the next correction to shared memory (the warps of row half 0 that
-            // hold those TMEM lanes)
-            // ---- this mini-batch's products are complete: the B operands of the small products to shared memory
-            // in two bf16 terms (the warps of row half 0 that hold those TMEM lanes): the outputs' scores
-            // (eta_i / eta_last)(scale q_i.k_j + 1) for j <= i (0 above the diagonal), and k_{t+1} k_t^T
-            if (rh == 0 && (qd == BT / 32 || qd == BT / 16)) {
-                ok = tc::bar_wait(prod, t & 1, abort_w) && ok;
-                tc::fence_after();
-                uint32_t r[BT];
-                tmem_ldn<BT>(tl + L::DC + 32 * p, r);
-                const bool sc = qd == BT / 32;
-                const int row = m - (sc ? BT : 2 * BT);
-                if (row >= 0 && row < BT) {
-                    const float *E2 = reinterpret_cast<const float *>(sm + L::E2 + p * (BT + 4) * 4);
-                    const float f = sc ? E2[row] / E2[BT] : 1.f;
-                    unsigned char *t0 = sm + (sc ? L::MST : L::KKT), *t1 = t0 + L::TB;
-#pragma unroll
-                    for (int j = 0; j < BT; j += 8) {
-                        uint32_t w1[4], w2[4];
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            float x0 = __uint_as_float(r[j + e]), x1 = __uint_as_float(r[j + e + 1]);
-                            if (sc) {
-                                x0 = j + e <= row ? f * fmaf(scale, x0, 1.f) : 0.f;
-                                x1 = j + e + 1 <= row ? f * fmaf(scale, x1, 1.f) : 0.f;
-                            }
-                            split2_rn(x0, x1, w1[e / 2], w2[e / 2]);
-                        }
-                        const uint32_t off = tc::sw128(row, j);
-                        *reinterpret_cast<uint4 *>(t0 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-                        *reinterpret_cast<uint4 *>(t1 + off) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-                    }
-                    tc::fence_proxy_async();
-                }
-            }
-            tc::fence_before();
-            ok = role_all(ok, 1);   // (the staging warps' wait)
-            if (ctid == 0)
-                tc::bar_arrive(kk_ready);
-            tc::bar_arrive(&v2_full[p]);   // this mini-batch's q h columns, v2 and rates: to the outputs
+            tc::bar_arrive(&v2_full[p]);   // this mini-batch's v2 and rates: to the outputs
         }
         if (nmb > 0) {
             ok = tc::bar_wait(upd, (nmb - 1) & 1, abort_w) && ok;   // the last update
@@ -591,8 +609,8 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         }
         if (a.hbt && rh == 0)
             a.hbt[st * D + m] = hb;
-    } else {
-        // ============ the state split, and the outputs one mini-batch behind ============
+    } else if (warp < 16) {
+        // ============ warps 8-15: the state split, and the outputs one mini-batch behind ============
         float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;   // kept here too, updated as the chain's
         const float wm = a.w[(size_t)h * D + m], bm = a.b[(size_t)h * D + m];
         // h^T (fp32, this thread's 64 columns) -> its two bf16 terms
