@@ -11,20 +11,24 @@
 // -eta_last v2_t (the update h_{t+1} = h_t + k_t^T W_t),
 //   k_t h_t = k_t h_{t-1} + (k_t k_{t-1}^T) W_{t-1},
 // so k_t h_{t-1} is taken one mini-batch ahead and the correction, a product of k_t k_{t-1}^T (staged in
-// two bf16 terms one mini-batch ahead) with W_{t-1}'s three exact terms, is the first product issued once
-// W_{t-1} is known.  Per mini-batch t:
+// two bf16 terms one mini-batch ahead) with W_{t-1}, is the first product issued once W_{t-1} is known.
+// Per mini-batch t:
 //   * the split warps (which also form the outputs) cut h_t into two bf16 terms as soon as the update that
 //     made it is complete (h = h1 + h2 + e, |e| <= 2^-18 |h|, each term rounded to nearest by conversion);
 //   * one issuing thread then takes h_t^T [q_t; k_{t+1}]^T (tcgen05 kind::f16, A the two terms from TMEM,
-//     M = 128, N = 2 BT, K = D: the outputs' q h and the next mini-batch's k h_t) and the row products of the
-//     tile [k_t; q_t; k_{t+1}] with k_t (q k^T for the outputs, k_{t+1} k_t^T for the next correction);
+//     M = 128, N = 2 BT, K = D: the outputs' q h and the next mini-batch's k h_t); the row products of the
+//     tile [k_t; q_t; k_{t+1}] with k_t (q k^T for the outputs, k_{t+1} k_t^T for the next correction) need
+//     no state and are issued a mini-batch ahead, and two staging warps turn them into the B operands of the
+//     small products with W_t (two bf16 terms each);
 //   * the chain warps take the rows' LayerNorm statistics and the two gradient sums over the 128 lanes (four
-//     warps of 32, merged through shared memory) and v2_t; -eta_last v2_t is split exactly into three bf16
-//     terms (MN-major A) and the update h^T += W^T k is one more product accumulating into the fp32 state
-//     (B: the k rows of the tile, MN-major), so the state itself is never rewritten by the CUDA cores;
+//     warps of 32, merged through shared memory) and v2_t; W_t = -eta_last v2_t is split exactly into three
+//     bf16 terms (MN-major A): the update h^T += W^T k is one more product accumulating into the fp32 state
+//     on all three (B: the k rows of the tile, MN-major), so the state itself is never rewritten by the CUDA
+//     cores, and the small products (the correction, the outputs' score-weighted sums) take the first two,
+//     which leave at most 2^-18 |W_t|;
 //   * the outputs of a mini-batch are formed one mini-batch behind from its q h columns, v2, learning rates
-//     and the product of its masked scores (staged by two of the output warps) with W_t, kept in buffers by
-//     parity and released through mbarriers.
+//     and the product of its masked scores with W_t, kept in buffers by parity and released through
+//     mbarriers.
 // Rows arrive by asynchronous copies two mini-batches ahead (three tiles in turn); rows past the end of a
 // sequence are zero in k and q and take no part in the update (as the CUDA-core path).
 #include <cuda_bf16.h>
@@ -58,8 +62,8 @@ struct TtcLayout {
     static constexpr int ET = RED + 2 * 4 * BT * 2 * 4;  // [3][BT] learning rates (0 past the end)
     static constexpr int E2 = ET + 3 * BT * 4;       // [2][BT + 1] the outputs' learning rates and eta_last
     static constexpr int RED2 = E2 + 2 * (BT + 4) * 4;   // [4][BT][2] the output warps' partial statistics
-    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3], kk_ready, tail[2], corr;
-    // TMEM address; abort word
+    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3], kk_ready, tail[2], corr,
+    // rows; TMEM address; abort word
     static constexpr int BAR = (RED2 + 4 * BT * 2 * 4 + 7) / 8 * 8;
     // the row products read rows 0..127 of a tile with K-halves XH apart: keep that span allocated
     static constexpr int END = BAR + 160 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 160 : X0 + 2 * XB + XH + 128 * 128;
@@ -282,8 +286,9 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     uint64_t *xfull = bar + 8, *slot_free = bar + 11;   // [3] by mini-batch mod 3: the tile's rows landed / free
     uint64_t *kk_ready = bar + 14, *tail = bar + 15;    // the small products' B operands staged / done [2]
     uint64_t *corr = bar + 17;                           // the correction onto the next k h is done
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 144);
-    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 148);
+    uint64_t *rows = bar + 18;                           // the row products of a tile are done
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 152);
+    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 156);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, qd = warp & 3, rh = (warp >> 2) & 1;
     const int ctid = tid & 255;                          // index within the role
     const int m = 32 * qd + lane;                        // this thread's TMEM lane: output feature m
@@ -323,6 +328,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         tc::bar_init(&tail[0], 1);
         tc::bar_init(&tail[1], 1);
         tc::bar_init(corr, 1);
+        tc::bar_init(rows, 1);
         *abort_w = 0;
         tc::bar_fence_init();
     }
@@ -345,18 +351,35 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         if (lane == 0) {
             constexpr uint32_t ID_Q = idesc_bf16(128, 2 * BT), ID_C = idesc_bf16(128, BT);
             constexpr uint32_t ID_B = idesc_bf16(128, D) | tc::kIdescAMajorMN | tc::kIdescBMajorMN;
+            constexpr uint32_t ID_W = idesc_bf16(128, BT) | tc::kIdescAMajorMN;
+            // the row products of tile tt (they need no state): its rows times k_tt, lanes BT.. q_tt k_tt^T, lanes
+            // 2 BT.. k_{tt+1} k_tt^T, for the staging warps.  Issued a mini-batch ahead.
+            auto row_products = [&](int tt) {
+                const uint32_t xr = sb + L::X0 + (tt % 3) * L::XB;
+                if (!tc::bar_wait(&xfull[tt % 3], (tt / 3) & 1, abort_w))
+                    return false;
+                tc::fence_after();
+                tc::fence_proxy_async();   // the copied rows -> the tensor cores
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t dx = tc::sdesc_sw128(xr + (ks >> 2) * L::XH + (ks & 3) * 32);
+                    tc::mma_ss(tmem + L::DC + 32 * (tt & 1), dx, dx, ID_C, ks ? 1u : 0u);
+                }
+                tc::mma_commit(rows);
+                return true;
+            };
+            if (nmb > 0)
+                ok = row_products(0);
             for (int t = 0; t < nmb && ok; ++t) {
                 const int p = t & 1;
                 const uint32_t xs = sb + L::X0 + (t % 3) * L::XB;
-                // h_t in two terms and the tile's rows are in place; the outputs of t - 2 are done with this
-                // parity's columns
-                ok = tc::bar_wait(hs_ready, t & 1, abort_w) && tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w);
+                // h_t in two terms is in place (the tile's rows were seen with its row products); the outputs
+                // of t - 2 are done with this parity's columns
+                ok = tc::bar_wait(hs_ready, t & 1, abort_w);
                 if (ok && t >= 2)
                     ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w);
                 if (!ok)
                     break;
                 tc::fence_after();
-                tc::fence_proxy_async();   // the copied rows -> the tensor cores
                 if (t == 0)   // k_0 h_0, the first mini-batch's rows (columns BT.. of the other parity)
                     for (int tt = 0; tt < 2; ++tt)
                         for (int ks = 0; ks < D / 16; ++ks)
@@ -370,36 +393,30 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                         tc::mma_ts(tmem + L::DA + 64 * p, tmem + L::HS + 64 * tt + 8 * ks,
                                    tc::sdesc_sw128(xs + BT * 128 + (ks >> 2) * L::XH + (ks & 3) * 32), ID_Q,
                                    (tt | ks) ? 1u : 0u);
-                // the tile's rows times k_t: lanes BT.. q_t k_t^T, lanes 2 BT.. k_{t+1} k_t^T
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t dx = tc::sdesc_sw128(xs + (ks >> 2) * L::XH + (ks & 3) * 32);
-                    tc::mma_ss(tmem + L::DC + 32 * p, dx, dx, ID_C, ks ? 1u : 0u);
-                }
                 tc::mma_commit(prod);
-                // W_t's terms (the chain) and the small products' B operands (two output warps) are in place
+                // W_t's terms (the chain) and the small products' B operands (the staging warps) are in place
                 if (!(ok = tc::bar_wait(v2t_ready, t & 1, abort_w) && tc::bar_wait(kk_ready, t & 1, abort_w)))
                     break;
                 tc::fence_after();
-                // first the correction (k_{t+1} k_t^T) W_t onto k_{t+1} h_t, which the chain waits for; W_t in three
-                // terms (MN-major A), k_{t+1} k_t^T in two
-                constexpr uint32_t ID_W = idesc_bf16(128, BT) | tc::kIdescAMajorMN;
+                // first the correction (k_{t+1} k_t^T) W_t onto k_{t+1} h_t, which the chain waits for: W_t's
+                // first two terms (MN-major A; they leave at most 2^-18 |W_t|), k_{t+1} k_t^T in two
                 if (t + 1 < nmb)
-                    for (int tw = 0; tw < 3; ++tw)
+                    for (int tw = 0; tw < 2; ++tw)
                         for (int tb = 0; tb < 2; ++tb)
                             for (int ks = 0; ks < BT / 16; ++ks)
                                 tc::mma_ss(tmem + L::DA + 64 * p + BT,
                                            tc::sdesc_mn_sw128(sb + L::V2T + tw * 2 * L::V2H + ks * 2048, L::V2H),
                                            tc::sdesc_sw128(sb + L::KKT + tb * L::TB + ks * 32), ID_W, 1u);
                 tc::mma_commit(corr);
-                // the update h^T += W_t^T k_t into the fp32 state
+                // the update h^T += W_t^T k_t into the fp32 state, on all three (exact) terms
                 for (int tt = 0; tt < 3; ++tt)
                     for (int ks = 0; ks < BT / 16; ++ks)
                         tc::mma_ss(tmem + L::HT, tc::sdesc_mn_sw128(sb + L::V2T + tt * 2 * L::V2H + ks * 2048, L::V2H),
                                    tc::sdesc_mn_sw128(xs + ks * 2048, L::XH), ID_B, 1u);
                 tc::mma_commit(upd);
                 tc::mma_commit(&slot_free[t % 3]);
-                // the outputs' sums -eta_i sum_j (scale q_i.k_j + 1) v2_j
-                for (int tw = 0; tw < 3; ++tw)
+                // the outputs' sums -eta_i sum_j (scale q_i.k_j + 1) v2_j (W_t's first two terms)
+                for (int tw = 0; tw < 2; ++tw)
                     for (int tb = 0; tb < 2; ++tb)
                         for (int ks = 0; ks < BT / 16; ++ks)
                             tc::mma_ss(tmem + L::DO + 32 * p,
@@ -407,6 +424,9 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                                        tc::sdesc_sw128(sb + L::MST + tb * L::TB + ks * 32), ID_W,
                                        (tw | tb | ks) ? 1u : 0u);
                 tc::mma_commit(&tail[p]);
+                // the next tile's row products (their buffer's last reader, staging t - 1, is done)
+                if (t + 1 < nmb)
+                    ok = row_products(t + 1);
             }
         }
     } else if (warp == W_SC || warp == W_KK) {
@@ -417,7 +437,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         const bool sc = warp == W_SC;
         for (int t = 0; t < nmb && ok; ++t) {
             const int p = t & 1, len = min(BT, eos - (bos + t * BT));
-            ok = tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w) && tc::bar_wait(prod, t & 1, abort_w) &&
+            ok = tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w) && tc::bar_wait(rows, t & 1, abort_w) &&
                  (t == 0 || tc::bar_wait(&tail[p ^ 1], ((t - 1) >> 1) & 1, abort_w));
             if (!ok)
                 break;
