@@ -50,16 +50,17 @@ struct TtcLayout {
     static constexpr int XB = 2 * XH;                // one tile
     static constexpr int X0 = 0;                     // [3] tiles (K-major, 128-byte swizzle), by mini-batch mod 3
     static constexpr int VR = X0 + 3 * XB;           // [3][BT][D] raw v rows (bf16), likewise
-    static constexpr int V2T = VR + 3 * BT * D * 2;  // [3] terms of -eta_last v2, MN-major: [BT rows][2 halves]
+    static constexpr int V2T = VR + 3 * BT * D * 2;  // [2][3] terms of -eta_last v2 by parity, MN-major: [BT rows][2 halves]
     static constexpr int V2H = BT * 128;             // one 64-column half of a term
-    static constexpr int V2F = V2T + 3 * 2 * V2H;    // [2][BT][D] v2 fp32, by parity
+    static constexpr int V2P = 3 * 2 * V2H;          // one parity's three terms
+    static constexpr int V2F = V2T + 2 * V2P;        // [2][BT][D] v2 fp32, by parity
     // the B operands of the small products with W = -eta_last v2 (K-major, 128-byte swizzle, BT rows of BT
     // K values): two bf16 terms of k_{t+1} k_t^T (the next correction), two of the outputs' scaled scores
     static constexpr int TB = BT * 128;
     static constexpr int MT = (V2F + 2 * BT * D * 4 + 1023) / 1024 * 1024;
     static constexpr int KKT = MT, MST = MT + 2 * TB;
-    static constexpr int RED = MT + 4 * TB;          // [2 (statistics, gradient sums)][4 quadrants][BT][2]
-    static constexpr int ET = RED + 2 * 4 * BT * 2 * 4;  // [3][BT] learning rates (0 past the end)
+    static constexpr int KH = MT + 4 * TB;           // [BT][D] k_t h_t + hb (fp32): the chain's rows
+    static constexpr int ET = KH + BT * D * 4;       // [3][BT] learning rates (0 past the end)
     static constexpr int E2 = ET + 3 * BT * 4;       // [2][BT + 1] the outputs' learning rates and eta_last
     static constexpr int RED2 = E2 + 2 * (BT + 4) * 4;   // [4][BT][2] the output warps' partial statistics
     // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3], kk_ready, tail[2], corr,
@@ -71,7 +72,8 @@ struct TtcLayout {
     // TMEM columns: the state, its two bf16 terms (64 columns each), [q h_t, k_{t+1} h_t]^T by parity, the row
     // products by parity, the outputs' score-weighted sums of v2 by parity
     static constexpr uint32_t HT = 0, HS = 128, DA = 256, DC = 384, DO = 448, COLS = 512;
-    static_assert(VR % 1024 == 0 && V2T % 1024 == 0, "swizzled tiles are 1024-byte aligned");
+    static_assert(VR % 1024 == 0 && V2T % 1024 == 0 && V2P % 1024 == 0, "swizzled tiles are 1024-byte aligned");
+    static_assert(BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
@@ -158,6 +160,16 @@ __device__ __forceinline__ float warp_rs(float (&v)[V], int lane)
         x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
 }
+// x[n] <- its sum over the warp's 32 lanes, the N sums interleaved
+template <int N>
+__device__ __forceinline__ void warp_sums(float (&x)[N])
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int n = 0; n < N; ++n)
+            x[n] += __shfl_xor_sync(0xffffffffu, x[n], o);
+}
 // This warp's (mean, M2) over its 32 lanes of each of HB rows (x[u] belongs to row r0 + u) into
 // red[(qd BT + r0 + u) 2 + {0, 1}]: the sums of d = x - s (s the row's value in lane 0, so that the sum of
 // squares does not cancel) and of d^2, reduce-scattered; one lane per row writes.
@@ -185,23 +197,6 @@ __device__ __forceinline__ void warp_row_stats(const float (&x)[HB], float *red,
         red[(qd * BT + r0 + u) * 2 + 1] = fmaf(-tot, tot * (1.f / 32), sq);
     }
 }
-// This warp's sums over its 32 lanes of a[u] and b[u] (row r0 + u) into red[(qd BT + r0 + u) 2 + {0, 1}].
-template <int HB>
-__device__ __forceinline__ void warp_row_sums(const float (&a)[HB], const float (&b)[HB], float *red, int qd, int BT,
-                                              int r0, int lane)
-{
-    constexpr int V = 2 * HB, SH = V == 16 ? 1 : 0;
-    float v[V];
-#pragma unroll
-    for (int u = 0; u < HB; ++u) {
-        v[2 * u] = a[u];
-        v[2 * u + 1] = b[u];
-    }
-    const float tot = warp_rs<V>(v, lane);
-    const int q = lane >> SH;
-    if ((lane & ((1 << SH) - 1)) == 0)
-        red[(qd * BT + r0 + (q >> 1)) * 2 + (q & 1)] = tot;
-}
 // mean and 1 / sqrt(var + eps) of rows r0 .. r0 + HB - 1 over the four quadrants: lane u merges row r0 + u,
 // then every lane takes all HB rows
 template <int HB>
@@ -217,24 +212,6 @@ __device__ __forceinline__ void rows_merged(const float *red, int BT, int r0, fl
         rstd[u] = __shfl_sync(0xffffffffu, rr, u);
     }
 }
-// the four quadrants' sums of rows r0 .. r0 + HB - 1 (fixed order), every lane taking all HB rows
-template <int HB>
-__device__ __forceinline__ void rows_summed(const float *red, int BT, int r0, int lane, float (&a)[HB], float (&b)[HB])
-{
-    float x = 0.f, y = 0.f;
-    if (lane < HB)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            x += red[(q * BT + r0 + lane) * 2];
-            y += red[(q * BT + r0 + lane) * 2 + 1];
-        }
-#pragma unroll
-    for (int u = 0; u < HB; ++u) {
-        a[u] = __shfl_sync(0xffffffffu, x, u);
-        b[u] = __shfl_sync(0xffffffffu, y, u);
-    }
-}
-
 // x[0..N) = N consecutive 32-bit TMEM columns of this thread's lane (N = 4, 8, 16 or 32)
 template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&x)[N])
@@ -405,13 +382,13 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                         for (int tb = 0; tb < 2; ++tb)
                             for (int ks = 0; ks < BT / 16; ++ks)
                                 tc::mma_ss(tmem + L::DA + 64 * p + BT,
-                                           tc::sdesc_mn_sw128(sb + L::V2T + tw * 2 * L::V2H + ks * 2048, L::V2H),
+                                           tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tw * 2 * L::V2H + ks * 2048, L::V2H),
                                            tc::sdesc_sw128(sb + L::KKT + tb * L::TB + ks * 32), ID_W, 1u);
                 tc::mma_commit(corr);
                 // the update h^T += W_t^T k_t into the fp32 state, on all three (exact) terms
                 for (int tt = 0; tt < 3; ++tt)
                     for (int ks = 0; ks < BT / 16; ++ks)
-                        tc::mma_ss(tmem + L::HT, tc::sdesc_mn_sw128(sb + L::V2T + tt * 2 * L::V2H + ks * 2048, L::V2H),
+                        tc::mma_ss(tmem + L::HT, tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tt * 2 * L::V2H + ks * 2048, L::V2H),
                                    tc::sdesc_mn_sw128(xs + ks * 2048, L::XH), ID_B, 1u);
                 tc::mma_commit(upd);
                 tc::mma_commit(&slot_free[t % 3]);
@@ -420,7 +397,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     for (int tb = 0; tb < 2; ++tb)
                         for (int ks = 0; ks < BT / 16; ++ks)
                             tc::mma_ss(tmem + L::DO + 32 * p,
-                                       tc::sdesc_mn_sw128(sb + L::V2T + tw * 2 * L::V2H + ks * 2048, L::V2H),
+                                       tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tw * 2 * L::V2H + ks * 2048, L::V2H),
                                        tc::sdesc_sw128(sb + L::MST + tb * L::TB + ks * 32), ID_W,
                                        (tw | tb | ks) ? 1u : 0u);
                 tc::mma_commit(&tail[p]);
@@ -504,9 +481,19 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         asm volatile("cp.async.wait_all;" ::: "memory");   // nothing lands after the CTA is gone
     } else if (warp < 8) {
         // ================================ the chain ================================
-        float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;
-        const float wm = a.w[(size_t)h * D + m], bm = a.b[(size_t)h * D + m];
-        float *RED = reinterpret_cast<float *>(sm + L::RED), *RSG = RED + 4 * BT * 2;
+        // k h arrives transposed (thread (qd, rh): feature m of rows r0h ..); it goes to shared memory once,
+        // and the rest of the step runs on rows: warp w takes rows RW w .. RW w + RW - 1 and lane l the
+        // features 4 l .. 4 l + 3, so every row statistic and gradient sum is a reduction within one warp
+        constexpr int RW = BT / 8;
+        const int i0 = RW * warp, f0 = 4 * lane;
+        float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;   // (feature m)
+        float wf[4], bv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            wf[e] = a.w[(size_t)h * D + f0 + e];
+            bv[e] = a.b[(size_t)h * D + f0 + e];
+        }
+        float *KH = reinterpret_cast<float *>(sm + L::KH);
         for (int t = 0; t < nmb && ok; ++t) {
             const int p = t & 1, r0 = bos + t * BT, len = min(BT, eos - r0);
             const unsigned char *xt = sm + L::X0 + (t % 3) * L::XB;
@@ -521,78 +508,97 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 ok = role_all(ok, 1);
                 tc::fence_after();
             }
-            float kh[HB];
             {
                 uint32_t r[HB];
                 tmem_ldn<HB>(tl + L::DA + 64 * (p ^ 1) + BT + r0h, r);
 #pragma unroll
                 for (int u = 0; u < HB; ++u)
-                    kh[u] = __uint_as_float(r[u]) + hb;
+                    KH[(r0h + u) * D + m] = __uint_as_float(r[u]) + hb;
             }
-            // ---- LayerNorm statistics of the rows (one thread also sees this mini-batch's k and v rows landed;
-            // the barrier passes that on)
-            warp_row_stats<HB>(kh, RED, qd, BT, r0h, lane);
-            if (ctid == 0)
-                ok = tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w) && ok;
-            ok = role_all(ok, 1);
-            // ---- gradient of the inner loss; its two row sums over the features
-            float xh[HB], gg[HB], rs[HB], gx[HB];
-            {
-                float mean[HB];
-                rows_merged<HB>(RED, BT, r0h, eps, lane, mean, rs);
-                const uint16_t *vr = reinterpret_cast<const uint16_t *>(sm + L::VR + (t % 3) * BT * D * 2);
-#pragma unroll
-                for (int u = 0; u < HB; ++u) {
-                    const int i = r0h + u;
-                    xh[u] = (kh[u] - mean[u]) * rs[u];
-                    const float ki =
-                        bf(*reinterpret_cast<const uint16_t *>(xt + (m >> 6) * L::XH + tc::sw128(i, m & 63)));
-                    gg[u] = i < len ? (fmaf(xh[u], wm, bm) + ki - bf(vr[i * D + m])) * wm : 0.f;
-                    gx[u] = gg[u] * xh[u];
-                }
-            }
-            warp_row_sums<HB>(gg, gx, RSG, qd, BT, r0h, lane);
-            // the last mini-batch's products with W are complete (its terms may be overwritten) and the outputs
-            // of two mini-batches ago are done with this parity's buffers: one thread waits, the barrier passes
-            // it on
+            // this mini-batch's rows have landed, and the outputs of two mini-batches ago are done with this
+            // parity's buffers (and so are the products that read this parity's W terms): one thread waits,
+            // the barrier passes it on
             if (ctid == 0) {
-                if (t > 0)
-                    ok = tc::bar_wait(&tail[p ^ 1], ((t - 1) >> 1) & 1, abort_w) && ok;
+                ok = tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w) && ok;
                 if (t >= 2)
                     ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w) && ok;
             }
             ok = role_all(ok, 1);
+            // ---- LayerNorm of the rows (two passes over registers)
             const float *ET = reinterpret_cast<const float *>(sm + L::ET + (t % 3) * BT * 4);
             const float el = ET[len - 1];
-            float *V2F = reinterpret_cast<float *>(sm + L::V2F + p * BT * D * 4);
-            float v2[HB];
-            {
-                float sg[HB], sgx[HB];
-                rows_summed<HB>(RSG, BT, r0h, lane, sg, sgx);
+            float x[RW][4], s1[RW], s2[RW], rs[RW];
 #pragma unroll
-                for (int u = 0; u < HB; ++u) {
-                    v2[u] = rs[u] * (1.f / D) * (D * gg[u] - sg[u] - xh[u] * sgx[u]);
-                    V2F[(r0h + u) * D + m] = v2[u];
+            for (int r = 0; r < RW; ++r) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(KH + (i0 + r) * D + f0);
+                x[r][0] = q4.x;
+                x[r][1] = q4.y;
+                x[r][2] = q4.z;
+                x[r][3] = q4.w;
+                s1[r] = (q4.x + q4.y) + (q4.z + q4.w);
+            }
+            warp_sums<RW>(s1);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const float mean = s1[r] * (1.f / D);
+                s2[r] = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x[r][e] -= mean;
+                    s2[r] = fmaf(x[r][e], x[r][e], s2[r]);
                 }
+            }
+            warp_sums<RW>(s2);
+            // ---- gradient of the inner loss; its two row sums over the features
+            float gg[RW][4], gs[2 * RW];
+            const unsigned char *vt = sm + L::VR + (t % 3) * BT * D * 2;
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int i = i0 + r;
+                rs[r] = rsqrtf(fmaf(s2[r], 1.f / D, eps));
+                const uint2 kw = *reinterpret_cast<const uint2 *>(xt + (f0 >> 6) * L::XH + tc::sw128(i, f0 & 63));
+                const uint2 vw = *reinterpret_cast<const uint2 *>(vt + (i * D + f0) * 2);
+                const float kv[4] = {__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
+                                     __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u)};
+                const float vv[4] = {__uint_as_float(vw.x << 16), __uint_as_float(vw.x & 0xFFFF0000u),
+                                     __uint_as_float(vw.y << 16), __uint_as_float(vw.y & 0xFFFF0000u)};
+                float sg = 0.f, sgx = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float xh = x[r][e] * rs[r];
+                    x[r][e] = xh;
+                    const float g = i < len ? (fmaf(xh, wf[e], bv[e]) + kv[e] - vv[e]) * wf[e] : 0.f;
+                    gg[r][e] = g;
+                    sg += g;
+                    sgx = fmaf(g, xh, sgx);
+                }
+                gs[2 * r] = sg;
+                gs[2 * r + 1] = sgx;
+            }
+            warp_sums<2 * RW>(gs);
+            // ---- v2 (fp32, for the outputs and hb) and W = -eta_last v2 in three bf16 terms (exact), MN-major
+            float *V2F = reinterpret_cast<float *>(sm + L::V2F + p * BT * D * 4);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int i = i0 + r;
+                float v2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v2[e] = rs[r] * (1.f / D) * (D * gg[r][e] - gs[2 * r] - x[r][e] * gs[2 * r + 1]);
+                *reinterpret_cast<float4 *>(V2F + i * D + f0) = make_float4(v2[0], v2[1], v2[2], v2[3]);
+                uint32_t wa[3], wb[3];
+                split3(-el * v2[0], -el * v2[1], wa[0], wa[1], wa[2]);
+                split3(-el * v2[2], -el * v2[3], wb[0], wb[1], wb[2]);
+                const uint32_t off = (f0 >> 6) * L::V2H + tc::sw128(i, f0 & 63);
+#pragma unroll
+                for (int tt = 0; tt < 3; ++tt)
+                    *reinterpret_cast<uint2 *>(sm + L::V2T + p * L::V2P + tt * 2 * L::V2H + off) =
+                        make_uint2(wa[tt], wb[tt]);
             }
             if (ctid <= BT) {   // the learning rates and eta_last for the output warps (the rates' slot is
                                 // refilled before the outputs run)
                 float *E2 = reinterpret_cast<float *>(sm + L::E2 + p * (BT + 4) * 4);
                 E2[ctid] = ctid < BT ? ET[ctid] : el;
-            }
-            // -eta_last v2 in three bf16 terms (exact), MN-major: row i, feature m (two rows per split)
-#pragma unroll
-            for (int u = 0; u < HB; u += 2) {
-                const int i = r0h + u;
-                uint32_t wv[3];
-                split3(-el * v2[u], -el * v2[u + 1], wv[0], wv[1], wv[2]);
-                const uint32_t off0 = (m >> 6) * L::V2H + tc::sw128(i, m & 63);
-                const uint32_t off1 = (m >> 6) * L::V2H + tc::sw128(i + 1, m & 63);
-#pragma unroll
-                for (int tt = 0; tt < 3; ++tt) {
-                    *reinterpret_cast<uint16_t *>(sm + L::V2T + tt * 2 * L::V2H + off0) = (uint16_t)(wv[tt] & 0xFFFFu);
-                    *reinterpret_cast<uint16_t *>(sm + L::V2T + tt * 2 * L::V2H + off1) = (uint16_t)(wv[tt] >> 16);
-                }
             }
             tc::fence_proxy_async();
             tc::fence_before();
