@@ -53,21 +53,21 @@ struct TtcLayout {
     static constexpr int V2T = VR + 3 * BT * D * 2;  // [2][3] terms of -eta_last v2 by parity, MN-major: [BT rows][2 halves]
     static constexpr int V2H = BT * 128;             // one 64-column half of a term
     static constexpr int V2P = 3 * 2 * V2H;          // one parity's three terms
-    static constexpr int V2F = V2T + 2 * V2P;        // [2][BT][D] v2 fp32, by parity
+    static constexpr int V2F = V2T + 2 * V2P;        // [BT][D] v2 fp32 (the chain's sums over rows for hb)
     // the B operands of the small products with W = -eta_last v2 (K-major, 128-byte swizzle, BT rows of BT
     // K values): two bf16 terms of k_{t+1} k_t^T (the next correction), two of the outputs' scaled scores
     static constexpr int TB = BT * 128;
-    static constexpr int MT = (V2F + 2 * BT * D * 4 + 1023) / 1024 * 1024;
+    static constexpr int MT = (V2F + BT * D * 4 + 1023) / 1024 * 1024;
     static constexpr int KKT = MT, MST = MT + 2 * TB;
     static constexpr int KH = MT + 4 * TB;           // [BT][D] k_t h_t + hb (fp32): the chain's rows
     static constexpr int ET = KH + BT * D * 4;       // [3][BT] learning rates (0 past the end)
-    static constexpr int E2 = ET + 3 * BT * 4;       // [2][BT + 1] the outputs' learning rates and eta_last
-    static constexpr int RED2 = E2 + 2 * (BT + 4) * 4;   // [4][BT][2] the output warps' partial statistics
-    // prod, upd, hs_ready, v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3], kk_ready, tail[2], corr,
-    // rows; TMEM address; abort word
-    static constexpr int BAR = (RED2 + 4 * BT * 2 * 4 + 7) / 8 * 8;
+    static constexpr int HBP = ET + 3 * BT * 4;      // [2][D] hb at the start of a mini-batch, by parity
+    static constexpr int OV = HBP + 2 * D * 4;       // [BT][D] the outputs before their LayerNorm (fp32)
+    // prod, upd, hs_half[0], v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3], kk_ready, tail[2], corr,
+    // rows, hs_half[1]; TMEM address; abort word
+    static constexpr int BAR = (OV + BT * D * 4 + 7) / 8 * 8;
     // the row products read rows 0..127 of a tile with K-halves XH apart: keep that span allocated
-    static constexpr int END = BAR + 160 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 160 : X0 + 2 * XB + XH + 128 * 128;
+    static constexpr int END = BAR + 176 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 176 : X0 + 2 * XB + XH + 128 * 128;
     static constexpr int BYTES = END + 1024;
     // TMEM columns: the state, its two bf16 terms (64 columns each), [q h_t, k_{t+1} h_t]^T by parity, the row
     // products by parity, the outputs' score-weighted sums of v2 by parity
@@ -118,48 +118,7 @@ __device__ __forceinline__ void split2_rn(float a, float b, uint32_t &w1, uint32
     const __nv_bfloat162 l = __floats2bfloat162_rn(ra, rb);
     w2 = *reinterpret_cast<const uint32_t *>(&l);
 }
-__device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
 
-// merge the four quadrants' (mean, M2) of 32 values each: mean and 1 / sqrt(var + eps)
-__device__ __forceinline__ void merge4(const float *red, int BT, int i, float eps, float &mean, float &rstd)
-{
-    float m = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        m += red[(q * BT + i) * 2];
-    m *= 0.25f;
-    float s = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float d = red[(q * BT + i) * 2] - m;
-        s += red[(q * BT + i) * 2 + 1] + 32.f * d * d;
-    }
-    mean = m;
-    rstd = rsqrtf(fmaf(s, 1.f / D, eps));
-}
-
-// Reduce-scatter over the warp: every lane brings V values (V = 16 or 32); lane l ends with the sum over the
-// 32 lanes of value q = l >> (V == 16 ? 1 : 0) (with V = 16, lanes 2q and 2q + 1 hold the same sum).  Halving
-// the values at each exchange takes V - 1 shuffles where V separate sums would take 5 V.
-template <int V>
-__device__ __forceinline__ float warp_rs(float (&v)[V], int lane)
-{
-    int o = 16;
-#pragma unroll
-    for (int n = V; n > 1; n >>= 1, o >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int k = 0; k < n / 2; ++k) {
-            const float keep = up ? v[n / 2 + k] : v[k], send = up ? v[k] : v[n / 2 + k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    float x = v[0];
-#pragma unroll
-    for (; o > 0; o >>= 1)
-        x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
 // x[n] <- its sum over the warp's 32 lanes, the N sums interleaved
 template <int N>
 __device__ __forceinline__ void warp_sums(float (&x)[N])
@@ -169,48 +128,6 @@ __device__ __forceinline__ void warp_sums(float (&x)[N])
 #pragma unroll
         for (int n = 0; n < N; ++n)
             x[n] += __shfl_xor_sync(0xffffffffu, x[n], o);
-}
-// This warp's (mean, M2) over its 32 lanes of each of HB rows (x[u] belongs to row r0 + u) into
-// red[(qd BT + r0 + u) 2 + {0, 1}]: the sums of d = x - s (s the row's value in lane 0, so that the sum of
-// squares does not cancel) and of d^2, reduce-scattered; one lane per row writes.
-template <int HB>
-__device__ __forceinline__ void warp_row_stats(const float (&x)[HB], float *red, int qd, int BT, int r0, int lane)
-{
-    constexpr int V = 2 * HB, SH = V == 16 ? 1 : 0;
-    float v[V], s[HB];
-#pragma unroll
-    for (int u = 0; u < HB; ++u) {
-        s[u] = __shfl_sync(0xffffffffu, x[u], 0);
-        const float d = x[u] - s[u];
-        v[2 * u] = d;
-        v[2 * u + 1] = d * d;
-    }
-    const float tot = warp_rs<V>(v, lane);
-    const float sq = __shfl_xor_sync(0xffffffffu, tot, 1 << SH);   // the row's sum of squares (odd q)
-    const int q = lane >> SH, u = q >> 1;
-    float su = 0.f;
-#pragma unroll
-    for (int w = 0; w < HB; ++w)
-        su = w == u ? s[w] : su;
-    if ((q & 1) == 0 && (lane & ((1 << SH) - 1)) == 0) {
-        red[(qd * BT + r0 + u) * 2] = fmaf(tot, 1.f / 32, su);
-        red[(qd * BT + r0 + u) * 2 + 1] = fmaf(-tot, tot * (1.f / 32), sq);
-    }
-}
-// mean and 1 / sqrt(var + eps) of rows r0 .. r0 + HB - 1 over the four quadrants: lane u merges row r0 + u,
-// then every lane takes all HB rows
-template <int HB>
-__device__ __forceinline__ void rows_merged(const float *red, int BT, int r0, float eps, int lane, float (&mean)[HB],
-                                            float (&rstd)[HB])
-{
-    float mm = 0.f, rr = 0.f;
-    if (lane < HB)
-        merge4(red, BT, r0 + lane, eps, mm, rr);
-#pragma unroll
-    for (int u = 0; u < HB; ++u) {
-        mean[u] = __shfl_sync(0xffffffffu, mm, u);
-        rstd[u] = __shfl_sync(0xffffffffu, rr, u);
-    }
 }
 // x[0..N) = N consecutive 32-bit TMEM columns of this thread's lane (N = 4, 8, 16 or 32)
 template <int N>
@@ -258,14 +175,17 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char *sm = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
-    uint64_t *prod = bar, *upd = bar + 1, *hs_ready = bar + 2, *v2t_ready = bar + 3;
+    uint64_t *prod = bar, *upd = bar + 1, *v2t_ready = bar + 3;
+    // the state's two terms of columns c (K of the state products) in two chunks: c in [0, 32) + [64, 96), then
+    // the rest (each split thread takes 32 columns of its row half at a time)
+    uint64_t *const hs_half[2] = {bar + 2, bar + 19};
     uint64_t *v2_full = bar + 4, *out_free = bar + 6;
     uint64_t *xfull = bar + 8, *slot_free = bar + 11;   // [3] by mini-batch mod 3: the tile's rows landed / free
     uint64_t *kk_ready = bar + 14, *tail = bar + 15;    // the small products' B operands staged / done [2]
     uint64_t *corr = bar + 17;                           // the correction onto the next k h is done
     uint64_t *rows = bar + 18;                           // the row products of a tile are done
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 152);
-    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 156);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 160);
+    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 164);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, qd = warp & 3, rh = (warp >> 2) & 1;
     const int ctid = tid & 255;                          // index within the role
     const int m = 32 * qd + lane;                        // this thread's TMEM lane: output feature m
@@ -291,7 +211,8 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     if (tid == 0) {
         tc::bar_init(prod, 1);
         tc::bar_init(upd, 1);
-        tc::bar_init(hs_ready, 1);
+        tc::bar_init(hs_half[0], 256);
+        tc::bar_init(hs_half[1], 256);
         tc::bar_init(v2t_ready, 1);
         for (int b = 0; b < 2; ++b) {
             tc::bar_init(&v2_full[b], 256);
@@ -349,27 +270,39 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             for (int t = 0; t < nmb && ok; ++t) {
                 const int p = t & 1;
                 const uint32_t xs = sb + L::X0 + (t % 3) * L::XB;
-                // h_t in two terms is in place (the tile's rows were seen with its row products); the outputs
-                // of t - 2 are done with this parity's columns
-                ok = tc::bar_wait(hs_ready, t & 1, abort_w);
+                // the first chunk of h_t's two terms is in place (the tile's rows were seen with its row
+                // products); the outputs of t - 2 are done with this parity's columns
+                ok = tc::bar_wait(hs_half[0], t & 1, abort_w);
                 if (ok && t >= 2)
                     ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w);
                 if (!ok)
                     break;
                 tc::fence_after();
-                if (t == 0)   // k_0 h_0, the first mini-batch's rows (columns BT.. of the other parity)
-                    for (int tt = 0; tt < 2; ++tt)
-                        for (int ks = 0; ks < D / 16; ++ks)
-                            tc::mma_ts(tmem + L::DA + 64 + BT, tmem + L::HS + 64 * tt + 8 * ks,
-                                       tc::sdesc_sw128(xs + (ks >> 2) * L::XH + (ks & 3) * 32), ID_C,
-                                       (tt | ks) ? 1u : 0u);
-                // [q_t h_t, k_{t+1} h_t]^T: tile rows BT .. 3 BT - 1
+                // [q_t h_t, k_{t+1} h_t]^T: tile rows BT .. 3 BT - 1, K steps of the first chunk (c / 16 = 0, 1, 4,
+                // 5), then of the second while it is being split
 #pragma unroll 1
-                for (int tt = 0; tt < 2; ++tt)
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        tc::mma_ts(tmem + L::DA + 64 * p, tmem + L::HS + 64 * tt + 8 * ks,
-                                   tc::sdesc_sw128(xs + BT * 128 + (ks >> 2) * L::XH + (ks & 3) * 32), ID_Q,
-                                   (tt | ks) ? 1u : 0u);
+                for (int half = 0; half < 2; ++half) {
+                    if (half == 1) {
+                        if (!(ok = tc::bar_wait(hs_half[1], t & 1, abort_w)))
+                            break;
+                        tc::fence_after();
+                        if (t == 0)   // k_0 h_0, the first mini-batch's rows (columns BT.. of the other parity)
+                            for (int tt = 0; tt < 2; ++tt)
+                                for (int ks = 0; ks < D / 16; ++ks)
+                                    tc::mma_ts(tmem + L::DA + 64 + BT, tmem + L::HS + 64 * tt + 8 * ks,
+                                               tc::sdesc_sw128(xs + (ks >> 2) * L::XH + (ks & 3) * 32), ID_C,
+                                               (tt | ks) ? 1u : 0u);
+                    }
+                    for (int tt = 0; tt < 2; ++tt)
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const int ks = (kk & 1) + 2 * half + 4 * (kk >> 1);
+                            tc::mma_ts(tmem + L::DA + 64 * p, tmem + L::HS + 64 * tt + 8 * ks,
+                                       tc::sdesc_sw128(xs + BT * 128 + (ks >> 2) * L::XH + (ks & 3) * 32), ID_Q,
+                                       (half | tt | kk) ? 1u : 0u);
+                        }
+                }
+                if (!ok)
+                    break;
                 tc::mma_commit(prod);
                 // W_t's terms (the chain) and the small products' B operands (the staging warps) are in place
                 if (!(ok = tc::bar_wait(v2t_ready, t & 1, abort_w) && tc::bar_wait(kk_ready, t & 1, abort_w)))
@@ -577,7 +510,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             }
             warp_sums<2 * RW>(gs);
             // ---- v2 (fp32, for the outputs and hb) and W = -eta_last v2 in three bf16 terms (exact), MN-major
-            float *V2F = reinterpret_cast<float *>(sm + L::V2F + p * BT * D * 4);
+            float *V2F = reinterpret_cast<float *>(sm + L::V2F);
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
                 const int i = i0 + r;
@@ -595,11 +528,8 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     *reinterpret_cast<uint2 *>(sm + L::V2T + p * L::V2P + tt * 2 * L::V2H + off) =
                         make_uint2(wa[tt], wb[tt]);
             }
-            if (ctid <= BT) {   // the learning rates and eta_last for the output warps (the rates' slot is
-                                // refilled before the outputs run)
-                float *E2 = reinterpret_cast<float *>(sm + L::E2 + p * (BT + 4) * 4);
-                E2[ctid] = ctid < BT ? ET[ctid] : el;
-            }
+            if (rh == 0)   // hb of this mini-batch (feature m) for the outputs
+                reinterpret_cast<float *>(sm + L::HBP)[p * D + m] = hb;
             tc::fence_proxy_async();
             tc::fence_before();
             chain_sync();
@@ -610,7 +540,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             for (int j = 0; j < BT; ++j)
                 sv += V2F[j * D + m];
             hb = fmaf(-el, sv, hb);
-            tc::bar_arrive(&v2_full[p]);   // this mini-batch's v2 and rates: to the outputs
+            tc::bar_arrive(&v2_full[p]);   // this mini-batch's hb: to the outputs
         }
         if (nmb > 0) {
             ok = tc::bar_wait(upd, (nmb - 1) & 1, abort_w) && ok;   // the last update
@@ -637,8 +567,6 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             a.hbt[st * D + m] = hb;
     } else if (warp < 16) {
         // ============ warps 8-15: the state split, and the outputs one mini-batch behind ============
-        float hb = a.hb0 ? a.hb0[st * D + m] : 0.f;   // kept here too, updated as the chain's
-        const float wm = a.w[(size_t)h * D + m], bm = a.b[(size_t)h * D + m];
         // h^T (fp32, this thread's 64 columns) -> its two bf16 terms
         auto split_state = [&]() {
 #pragma unroll 1
@@ -652,8 +580,10 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     split2_rn(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]), w1[u], w2[u]);
                 tc::tmem_st16(tl + L::HS + 0 * 64 + c0 / 2, w1);
                 tc::tmem_st16(tl + L::HS + 1 * 64 + c0 / 2, w2);
+                tc::tmem_wait_st();
+                tc::fence_before();
+                tc::bar_arrive(c32 ? hs_half[1] : hs_half[0]);   // this chunk of the terms: to the state products
             }
-            tc::tmem_wait_st();
         };
         // initial state: h^T[m][c] = h0[c][m] for this thread's 64 columns c (row half rh), and its two terms
 #pragma unroll 1
@@ -666,16 +596,21 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             tc::tmem_st32(tl + L::HT + c0, r);
         }
         tc::tmem_wait_st();
-        if (nmb > 0) {
+        if (nmb > 0)
             split_state();
-            tc::fence_before();
-            out_sync();
-            if (ctid == 0)
-                tc::bar_arrive(hs_ready);
-        }
         // q h + hb - eta_i sum_{j<=i} (scale q_i.k_j + 1) v2_j from the mini-batch's q h columns and the
-        // score-weighted sums of v2 (both in TMEM), then o + LN(o) w + b
-        float *RED2 = reinterpret_cast<float *>(sm + L::RED2);
+        // score-weighted sums of v2 (both in TMEM, transposed: feature m of rows r0h ..), then through shared
+        // memory to rows (warp w - 8 takes rows RW (w - 8) .., lane l the features 4 l .. 4 l + 3):
+        // o + LN(o) w + b with the row statistics reduced within the warp
+        constexpr int RW = BT / 8;
+        const int i0 = RW * (warp - 8), f0 = 4 * lane;
+        float wf[4], bv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            wf[e] = a.w[(size_t)h * D + f0 + e];
+            bv[e] = a.b[(size_t)h * D + f0 + e];
+        }
+        float *OV = reinterpret_cast<float *>(sm + L::OV);
         for (int t = 0; t < nmb && ok; ++t) {
             const int p = t & 1, r0 = bos + t * BT, len = min(BT, eos - r0);
             // h_{t+1} = h_t + k_t^T W_t is complete (and with it the products that read h_t's terms): its terms
@@ -685,46 +620,59 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 ok = role_all(ok, 2);
                 tc::fence_after();
                 split_state();
-                tc::fence_before();
-                out_sync();
-                if (ctid == 0)
-                    tc::bar_arrive(hs_ready);
             }
             ok = tc::bar_wait(&v2_full[p], (t >> 1) & 1, abort_w) && ok;
             if (ctid == 0)
                 ok = tc::bar_wait(&tail[p], (t >> 1) & 1, abort_w) && ok;   // the score-weighted sums of v2
-            ok = role_all(ok, 2);
+            ok = role_all(ok, 2);   // (also: the last mini-batch's rows of OV have been read)
             tc::fence_after();
-            uint32_t r[HB], dz[HB];
-            tmem_ldn<HB>(tl + L::DA + 64 * p + r0h, r);
-            tmem_ldn<HB>(tl + L::DO + 32 * p + r0h, dz);
-            const float *V2F = reinterpret_cast<const float *>(sm + L::V2F + p * BT * D * 4);
-            const float *E2 = reinterpret_cast<const float *>(sm + L::E2 + p * (BT + 4) * 4);
-            float ov[HB];
-#pragma unroll
-            for (int u = 0; u < HB; ++u)   // q h + hb - eta_i sum_{j<=i} (scale q_i.k_j + 1) v2_j
-                ov[u] = fmaf(scale, __uint_as_float(r[u]), hb) + __uint_as_float(dz[u]);
-            warp_row_stats<HB>(ov, RED2, qd, BT, r0h, lane);
-            const float el = E2[BT];
-            float sv = 0.f;
-#pragma unroll
-            for (int j = 0; j < BT; ++j)
-                sv += V2F[j * D + m];
-            out_sync();
             {
-                float mean[HB], rstd[HB];
-                rows_merged<HB>(RED2, BT, r0h, eps, lane, mean, rstd);
+                uint32_t r[HB], dz[HB];
+                tmem_ldn<HB>(tl + L::DA + 64 * p + r0h, r);
+                tmem_ldn<HB>(tl + L::DO + 32 * p + r0h, dz);
+                const float hbm = reinterpret_cast<const float *>(sm + L::HBP)[p * D + m];
 #pragma unroll
-                for (int u = 0; u < HB; ++u) {
-                    const int i = r0h + u;
-                    if (i < len)
-                        a.o[((size_t)(r0 + i) * H + h) * D + m] = ov[u] + fmaf((ov[u] - mean[u]) * rstd[u], wm, bm);
-                }
+                for (int u = 0; u < HB; ++u)
+                    OV[(r0h + u) * D + m] = fmaf(scale, __uint_as_float(r[u]), hbm) + __uint_as_float(dz[u]);
             }
-            hb = fmaf(-el, sv, hb);
             tc::fence_before();
-            out_sync();   // RED2 is free again
-            tc::bar_arrive(&out_free[p]);
+            tc::bar_arrive(&out_free[p]);   // this parity's TMEM columns and hb are read
+            out_sync();
+            float x[RW][4], s1[RW], s2[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(OV + (i0 + r) * D + f0);
+                x[r][0] = q4.x;
+                x[r][1] = q4.y;
+                x[r][2] = q4.z;
+                x[r][3] = q4.w;
+                s1[r] = (q4.x + q4.y) + (q4.z + q4.w);
+            }
+            warp_sums<RW>(s1);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const float mean = s1[r] * (1.f / D);
+                s2[r] = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float d = x[r][e] - mean;
+                    s2[r] = fmaf(d, d, s2[r]);
+                }
+                s1[r] = mean;
+            }
+            warp_sums<RW>(s2);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int i = i0 + r;
+                const float rstd = rsqrtf(fmaf(s2[r], 1.f / D, eps));
+                float y[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    y[e] = x[r][e] + fmaf((x[r][e] - s1[r]) * rstd, wf[e], bv[e]);
+                if (i < len)
+                    *reinterpret_cast<float4 *>(a.o + ((size_t)(r0 + i) * H + h) * D + f0) =
+                        make_float4(y[0], y[1], y[2], y[3]);
+            }
         }
     }
     tc::fence_before();
