@@ -386,21 +386,28 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         // ================================ row copies ================================
         // mini-batch t's rows into tile t mod 3: k_t (rows 0..BT-1), q_t (BT..), k_{t+1} (2 BT..), zero past the
         // end; its v rows and learning rates.  Each lane's copies arrive on the tile's barrier as they land.
+        // Lane l copies the 16-byte chunk l mod 16 (eight features) of every other row, starting at row l / 16.
+        const int c = lane & 15, ib = lane >> 4;
+        const size_t rs = (size_t)H * D;   // elements from one row to the next
+        const size_t col = (size_t)h * D + 8 * c;
         for (int t = 0; t < nmb && ok; ++t) {
             const int r0 = bos + t * BT, slot = t % 3;
             if (t >= 3 && !(ok = tc::bar_wait(&slot_free[slot], ((t / 3) - 1) & 1, abort_w)))
                 break;
-            unsigned char *xt = sm + L::X0 + slot * L::XB;
-            for (int e = lane; e < 4 * BT * 16; e += 32) {
-                const int which = e / (BT * 16), rem = e - which * (BT * 16), i = rem >> 4, c = rem & 15;
-                const int row = r0 + (which == 2 ? BT : 0) + i;
-                const bool in = row < eos;
-                const size_t gr = (size_t)(in ? row : r0) * H + h;
-                if (which < 3) {
-                    const __nv_bfloat16 *src = (which == 1 ? gq : gk) + gr * D + 8 * c;
-                    cp_async16(xt + (c >> 3) * L::XH + tc::sw128(which * BT + i, 8 * (c & 7)), src, in ? 16u : 0u);
-                } else {
-                    cp_async16(sm + L::VR + slot * BT * D * 2 + i * D * 2 + 16 * c, gv + gr * D + 8 * c, in ? 16u : 0u);
+            unsigned char *xt = sm + L::X0 + slot * L::XB + (c >> 3) * L::XH;
+            unsigned char *vt = sm + L::VR + slot * BT * D * 2 + 16 * c;
+            const size_t g0 = (size_t)r0 * rs + col;   // this lane's chunk of row r0 (in every tensor)
+#pragma unroll 1
+            for (int which = 0; which < 4; ++which) {   // k_t, q_t, k_{t+1}, v_t
+                const __nv_bfloat16 *src = which == 1 ? gq : which == 3 ? gv : gk;
+                const int roff = which == 2 ? BT : 0;
+#pragma unroll
+                for (int u = 0; u < BT / 2; ++u) {
+                    const int i = ib + 2 * u;
+                    const bool in = r0 + roff + i < eos;
+                    const __nv_bfloat16 *g = src + g0 + (in ? (size_t)(roff + i) * rs : 0);
+                    unsigned char *dst = which < 3 ? xt + tc::sw128(which * BT + i, 8 * (c & 7)) : vt + i * D * 2;
+                    cp_async16(dst, g, in ? 16u : 0u);
                 }
             }
             if (lane < BT) {
