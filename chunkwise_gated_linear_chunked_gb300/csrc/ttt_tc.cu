@@ -63,11 +63,11 @@ struct TtcLayout {
     static constexpr int ET = KH + BT * D * 4;       // [3][BT] learning rates (0 past the end)
     static constexpr int HBP = ET + 3 * BT * 4;      // [2][D] hb at the start of a mini-batch, by parity
     static constexpr int OV = HBP + 2 * D * 4;       // [BT][D] the outputs before their LayerNorm (fp32)
-    // prod, upd, hs_half[0], v2t_ready, v2_full[2], out_free[2], xfull[3], slot_free[3], kk_ready, tail[2], corr,
-    // rows, hs_half[1]; TMEM address; abort word
+    // prod, upd, hs_half[0], v2t(0), v2_full[2], out_free[2], xfull[3], slot_free[3], kk(0), tail[2], corr, rows,
+    // hs_half[1], v2t(1), kk(1); TMEM address; abort word
     static constexpr int BAR = (OV + BT * D * 4 + 7) / 8 * 8;
     // the row products read rows 0..127 of a tile with K-halves XH apart: keep that span allocated
-    static constexpr int END = BAR + 176 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 176 : X0 + 2 * XB + XH + 128 * 128;
+    static constexpr int END = BAR + 192 > X0 + 2 * XB + XH + 128 * 128 ? BAR + 192 : X0 + 2 * XB + XH + 128 * 128;
     static constexpr int BYTES = END + 1024;
     // TMEM columns: the state, its two bf16 terms (64 columns each), [q h_t, k_{t+1} h_t]^T by parity, the row
     // products by parity, the outputs' score-weighted sums of v2 by parity
@@ -175,17 +175,19 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
     extern __shared__ __align__(16) unsigned char smraw[];
     unsigned char *sm = smraw + ((1024u - (tc::smem_u32(smraw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::BAR);
-    uint64_t *prod = bar, *upd = bar + 1, *v2t_ready = bar + 3;
+    uint64_t *prod = bar, *upd = bar + 1;
+    auto v2t = [bar](int q) { return bar + (q ? 20 : 3); };   // W_t's terms written, by parity
     // the state's two terms of columns c (K of the state products) in two chunks: c in [0, 32) + [64, 96), then
     // the rest (each split thread takes 32 columns of its row half at a time)
     uint64_t *const hs_half[2] = {bar + 2, bar + 19};
     uint64_t *v2_full = bar + 4, *out_free = bar + 6;
     uint64_t *xfull = bar + 8, *slot_free = bar + 11;   // [3] by mini-batch mod 3: the tile's rows landed / free
-    uint64_t *kk_ready = bar + 14, *tail = bar + 15;    // the small products' B operands staged / done [2]
+    auto kk = [bar](int q) { return bar + (q ? 21 : 14); };   // the small products' B operands staged, by parity
+    uint64_t *tail = bar + 15;                           // [2] the small products with W_t done, by parity
     uint64_t *corr = bar + 17;                           // the correction onto the next k h is done
     uint64_t *rows = bar + 18;                           // the row products of a tile are done
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 160);
-    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 164);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::BAR + 176);
+    volatile int *abort_w = reinterpret_cast<volatile int *>(sm + L::BAR + 180);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, qd = warp & 3, rh = (warp >> 2) & 1;
     const int ctid = tid & 255;                          // index within the role
     const int m = 32 * qd + lane;                        // this thread's TMEM lane: output feature m
@@ -213,16 +215,18 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         tc::bar_init(upd, 1);
         tc::bar_init(hs_half[0], 256);
         tc::bar_init(hs_half[1], 256);
-        tc::bar_init(v2t_ready, 1);
+        tc::bar_init(v2t(0), 1);
+        tc::bar_init(v2t(1), 1);
         for (int b = 0; b < 2; ++b) {
             tc::bar_init(&v2_full[b], 256);
             tc::bar_init(&out_free[b], 256);
         }
         for (int b = 0; b < 3; ++b) {
             tc::bar_init(&xfull[b], 32);   // one completion-tracked arrival per lane of the copy warp
-            tc::bar_init(&slot_free[b], 1);
+            tc::bar_init(&slot_free[b], 2);   // the row products, and the update
         }
-        tc::bar_init(kk_ready, 2);   // one arrival per staging warp
+        tc::bar_init(kk(0), 2);   // one arrival per staging warp
+        tc::bar_init(kk(1), 2);
         tc::bar_init(&tail[0], 1);
         tc::bar_init(&tail[1], 1);
         tc::bar_init(corr, 1);
@@ -250,34 +254,18 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             constexpr uint32_t ID_Q = idesc_bf16(128, 2 * BT), ID_C = idesc_bf16(128, BT);
             constexpr uint32_t ID_B = idesc_bf16(128, D) | tc::kIdescAMajorMN | tc::kIdescBMajorMN;
             constexpr uint32_t ID_W = idesc_bf16(128, BT) | tc::kIdescAMajorMN;
-            // the row products of tile tt (they need no state): its rows times k_tt, lanes BT.. q_tt k_tt^T, lanes
-            // 2 BT.. k_{tt+1} k_tt^T, for the staging warps.  Issued a mini-batch ahead.
-            auto row_products = [&](int tt) {
-                const uint32_t xr = sb + L::X0 + (tt % 3) * L::XB;
-                if (!tc::bar_wait(&xfull[tt % 3], (tt / 3) & 1, abort_w))
-                    return false;
-                tc::fence_after();
-                tc::fence_proxy_async();   // the copied rows -> the tensor cores
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t dx = tc::sdesc_sw128(xr + (ks >> 2) * L::XH + (ks & 3) * 32);
-                    tc::mma_ss(tmem + L::DC + 32 * (tt & 1), dx, dx, ID_C, ks ? 1u : 0u);
-                }
-                tc::mma_commit(rows);
-                return true;
-            };
-            if (nmb > 0)
-                ok = row_products(0);
             for (int t = 0; t < nmb && ok; ++t) {
                 const int p = t & 1;
                 const uint32_t xs = sb + L::X0 + (t % 3) * L::XB;
-                // the first chunk of h_t's two terms is in place (the tile's rows were seen with its row
-                // products); the outputs of t - 2 are done with this parity's columns
-                ok = tc::bar_wait(hs_half[0], t & 1, abort_w);
+                // the first chunk of h_t's two terms and the tile's rows are in place; the outputs of t - 2 are
+                // done with this parity's columns
+                ok = tc::bar_wait(hs_half[0], t & 1, abort_w) && tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w);
                 if (ok && t >= 2)
                     ok = tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w);
                 if (!ok)
                     break;
                 tc::fence_after();
+                tc::fence_proxy_async();   // the copied rows -> the tensor cores
                 // [q_t h_t, k_{t+1} h_t]^T: tile rows BT .. 3 BT - 1, K steps of the first chunk (c / 16 = 0, 1, 4,
                 // 5), then of the second while it is being split
 #pragma unroll 1
@@ -305,7 +293,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     break;
                 tc::mma_commit(prod);
                 // W_t's terms (the chain) and the small products' B operands (the staging warps) are in place
-                if (!(ok = tc::bar_wait(v2t_ready, t & 1, abort_w) && tc::bar_wait(kk_ready, t & 1, abort_w)))
+                if (!(ok = tc::bar_wait(v2t(p), (t >> 1) & 1, abort_w) && tc::bar_wait(kk(p), (t >> 1) & 1, abort_w)))
                     break;
                 tc::fence_after();
                 // first the correction (k_{t+1} k_t^T) W_t onto k_{t+1} h_t, which the chain waits for: W_t's
@@ -325,18 +313,6 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                                    tc::sdesc_mn_sw128(xs + ks * 2048, L::XH), ID_B, 1u);
                 tc::mma_commit(upd);
                 tc::mma_commit(&slot_free[t % 3]);
-                // the outputs' sums -eta_i sum_j (scale q_i.k_j + 1) v2_j (W_t's first two terms)
-                for (int tw = 0; tw < 2; ++tw)
-                    for (int tb = 0; tb < 2; ++tb)
-                        for (int ks = 0; ks < BT / 16; ++ks)
-                            tc::mma_ss(tmem + L::DO + 32 * p,
-                                       tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tw * 2 * L::V2H + ks * 2048, L::V2H),
-                                       tc::sdesc_sw128(sb + L::MST + tb * L::TB + ks * 32), ID_W,
-                                       (tw | tb | ks) ? 1u : 0u);
-                tc::mma_commit(&tail[p]);
-                // the next tile's row products (their buffer's last reader, staging t - 1, is done)
-                if (t + 1 < nmb)
-                    ok = row_products(t + 1);
             }
         }
     } else if (warp == W_SC || warp == W_KK) {
@@ -344,11 +320,38 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         // to shared memory in two bf16 terms: the outputs' scores (eta_i / eta_last)(scale q_i.k_j + 1) for
         // j <= i (0 above the diagonal), and k_{t+1} k_t^T, once the mini-batch's row products are complete
         // and the last mini-batch's small products (which read these buffers) are done
+        // Lane 0 of the k_{t+1} k_t^T warp is the second MMA issuer: per mini-batch the outputs' sums
+        // -eta_i sum_j (scale q_i.k_j + 1) v2_j (W_t's first two terms) and the next tile's row products, so
+        // that the main issuer keeps only the state products, the correction and the update (each issuing
+        // thread waits about 120 cycles per tcgen05.mma, whatever its size; issuers in different warps overlap)
         const bool sc = warp == W_SC;
+        constexpr uint32_t ID_C = idesc_bf16(128, BT), ID_W = idesc_bf16(128, BT) | tc::kIdescAMajorMN;
+        // the row products of tile tt (they need no state): its rows times k_tt, lanes BT.. q_tt k_tt^T, lanes
+        // 2 BT.. k_{tt+1} k_tt^T.  Issued a mini-batch ahead; with the update they release the tile.
+        auto row_products = [&](int tt) {
+            const uint32_t xr = sb + L::X0 + (tt % 3) * L::XB;
+            if (!tc::bar_wait(&xfull[tt % 3], (tt / 3) & 1, abort_w))
+                return false;
+            tc::fence_after();
+            tc::fence_proxy_async();   // the copied rows -> the tensor cores
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t dx = tc::sdesc_sw128(xr + (ks >> 2) * L::XH + (ks & 3) * 32);
+                tc::mma_ss(tmem + L::DC + 32 * (tt & 1), dx, dx, ID_C, ks ? 1u : 0u);
+            }
+            tc::mma_commit(rows);
+            tc::mma_commit(&slot_free[tt % 3]);
+            return true;
+        };
+        if (!sc && lane == 0 && nmb > 0)
+            ok = row_products(0);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         for (int t = 0; t < nmb && ok; ++t) {
             const int p = t & 1, len = min(BT, eos - (bos + t * BT));
+            // (the last mini-batch's small products: the outputs' sums from the second issuer, the correction
+            // from the first)
             ok = tc::bar_wait(&xfull[t % 3], (t / 3) & 1, abort_w) && tc::bar_wait(rows, t & 1, abort_w) &&
-                 (t == 0 || tc::bar_wait(&tail[p ^ 1], ((t - 1) >> 1) & 1, abort_w));
+                 (t == 0 || (tc::bar_wait(&tail[p ^ 1], ((t - 1) >> 1) & 1, abort_w) &&
+                             tc::bar_wait(corr, (t - 1) & 1, abort_w)));
             if (!ok)
                 break;
             tc::fence_after();
@@ -380,7 +383,30 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             tc::fence_before();
             __syncwarp();
             if (lane == 0)
-                tc::bar_arrive(kk_ready);
+                tc::bar_arrive(kk(p));
+            if (!sc) {
+                // W_t's terms are in place, both B operands staged, and the outputs of t - 2 are done with this
+                // parity's columns
+                if (lane == 0) {
+                    ok = tc::bar_wait(v2t(p), (t >> 1) & 1, abort_w) && tc::bar_wait(kk(p), (t >> 1) & 1, abort_w) &&
+                         (t < 2 || tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w));
+                    if (ok) {
+                        tc::fence_after();
+                        for (int tw = 0; tw < 2; ++tw)
+                            for (int tb = 0; tb < 2; ++tb)
+                                for (int ks = 0; ks < BT / 16; ++ks)
+                                    tc::mma_ss(tmem + L::DO + 32 * p,
+                                               tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tw * 2 * L::V2H + ks * 2048,
+                                                                  L::V2H),
+                                               tc::sdesc_sw128(sb + L::MST + tb * L::TB + ks * 32), ID_W,
+                                               (tw | tb | ks) ? 1u : 0u);
+                        tc::mma_commit(&tail[p]);
+                        if (t + 1 < nmb)
+                            ok = row_products(t + 1);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            }
         }
     } else if (warp == W_COPY) {
         // ================================ row copies ================================
@@ -541,7 +567,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             tc::fence_before();
             chain_sync();
             if (ctid == 0)
-                tc::bar_arrive(v2t_ready);
+                tc::bar_arrive(v2t(p));
             float sv = 0.f;
 #pragma unroll
             for (int j = 0; j < BT; ++j)
@@ -620,14 +646,14 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
         float *OV = reinterpret_cast<float *>(sm + L::OV);
         for (int t = 0; t < nmb && ok; ++t) {
             const int p = t & 1, r0 = bos + t * BT, len = min(BT, eos - r0);
-            // h_{t+1} = h_t + k_t^T W_t is complete (and with it the products that read h_t's terms): its terms
-            if (t + 1 < nmb) {
-                if (ctid == 0)
-                    ok = tc::bar_wait(upd, t & 1, abort_w) && ok;
-                ok = role_all(ok, 2);
-                tc::fence_after();
+            // h_{t+1} = h_t + k_t^T W_t is complete (and with it the products that read h_t's terms, among them
+            // this mini-batch's q h columns): its terms
+            if (ctid == 0)
+                ok = tc::bar_wait(upd, t & 1, abort_w) && ok;
+            ok = role_all(ok, 2);
+            tc::fence_after();
+            if (t + 1 < nmb)
                 split_state();
-            }
             ok = tc::bar_wait(&v2_full[p], (t >> 1) & 1, abort_w) && ok;
             if (ctid == 0)
                 ok = tc::bar_wait(&tail[p], (t >> 1) & 1, abort_w) && ok;   // the score-weighted sums of v2
