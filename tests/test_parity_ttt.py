@@ -52,6 +52,13 @@ CASES = [
     ("bf16", 2, 200, 2, 128, True, None, 16),     # ragged last mini-batch
     ("bf16", 1, 0, 2, 128, True, [1, 15, 16, 17, 0, 130, 300], 16),
     ("bf16", 1, 0, 1, 128, False, [33, 64, 7], 32),
+    # the tensor-core kernel's pipeline edges: sequences of one, two and three mini-batches (whole and
+    # ragged), at both mini-batch sizes, a dense batch with a ragged tail, and a pack of many short and
+    # empty sequences (each CTA then runs at most a few mini-batches)
+    ("bf16", 1, 0, 2, 128, True, [16, 32, 48, 1, 2, 3, 31, 33, 47, 49], 16),
+    ("bf16", 1, 0, 1, 128, True, [32, 64, 96, 1, 65, 97], 32),
+    ("bf16", 3, 50, 4, 128, False, None, 16),
+    ("bf16", 1, 0, 2, 128, True, [5] * 40 + [0] * 5 + [16] * 10, 16),
 ]
 
 
