@@ -94,6 +94,24 @@ def test_ttt_tensor_core_kernel_runs_for_bf16_d128():
     assert [n for n, _ in timer.results()] == ["ttt_linear_tc"]
 
 
+@pytest.mark.parametrize("chunk", [16, 32])
+def test_ttt_tensor_core_kernel_is_deterministic(chunk):
+    """Repeated calls give bitwise-equal o, ht, hbt: every reduction has a fixed order and the issuing threads'
+    products land in their own accumulators, so no result depends on how the roles happen to interleave."""
+    from chunkwise_gated_linear_chunked_gb300 import binding
+    q, k, v, w, b, eta, s0, sb0, cu = make_ttt("bf16", 1, 0, 4, 128, True, [700, 33, 1, 512, 96], 11 + chunk)
+    args = [x.cuda() for x in (q, k, v, w, b, eta)]
+    outs = []
+    for _ in range(3):
+        o, ht, hbt = binding.ttt_linear_fwd(*args, chunk=chunk, initial_state=s0.cuda(),
+                                            initial_state_bias=sb0.cuda(), cu_seqlens=cu.cuda())
+        torch.cuda.synchronize()
+        outs.append([x.cpu() for x in (o, ht, hbt)])
+    for other in outs[1:]:
+        for x, y in zip(outs[0], other):
+            assert torch.equal(x, y)
+
+
 def test_ttt_bad_offsets_are_reported_not_faulted():
     from chunkwise_gated_linear_chunked_gb300 import binding
     q, k, v, w, b, eta, *_ = make_ttt("f32", 1, 40, 1, 64, False, None, 1)
