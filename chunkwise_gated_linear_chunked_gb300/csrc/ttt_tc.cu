@@ -297,10 +297,11 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                     break;
                 tc::fence_after();
                 // first the correction (k_{t+1} k_t^T) W_t onto k_{t+1} h_t, which the chain waits for: W_t's
-                // first two terms (MN-major A; they leave at most 2^-18 |W_t|), k_{t+1} k_t^T in two
+                // first two terms (MN-major A; they leave at most 2^-18 |W_t|) by k_{t+1} k_t^T's two, without
+                // the product of the two second terms (at most 2^-18 of the whole)
                 if (t + 1 < nmb)
                     for (int tw = 0; tw < 2; ++tw)
-                        for (int tb = 0; tb < 2; ++tb)
+                        for (int tb = 0; tb < 2 - tw; ++tb)
                             for (int ks = 0; ks < BT / 16; ++ks)
                                 tc::mma_ss(tmem + L::DA + 64 * p + BT,
                                            tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tw * 2 * L::V2H + ks * 2048, L::V2H),
@@ -392,8 +393,8 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                          (t < 2 || tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w));
                     if (ok) {
                         tc::fence_after();
-                        for (int tw = 0; tw < 2; ++tw)
-                            for (int tb = 0; tb < 2; ++tb)
+                        for (int tw = 0; tw < 2; ++tw)   // (without the product of the two second terms)
+                            for (int tb = 0; tb < 2 - tw; ++tb)
                                 for (int ks = 0; ks < BT / 16; ++ks)
                                     tc::mma_ss(tmem + L::DO + 32 * p,
                                                tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tw * 2 * L::V2H + ks * 2048,
