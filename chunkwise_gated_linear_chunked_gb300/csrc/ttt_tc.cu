@@ -82,6 +82,28 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// A shared-memory descriptor advanced by `bytes` (the start-address field holds address >> 4 and shared
+// addresses stay below 2^18, so the add cannot carry out of it).  The MMA loops below are fully unrolled over
+// descriptors formed once: an issuing thread then spends about half the cycles per tcgen05.mma that a loop
+// forming each descriptor from its address does (44 against 88 cycles at N = 32, measured).
+__device__ __forceinline__ uint64_t sd_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+// Half `HALF` of the state products [q_t h_t, k_{t+1} h_t]^T: the K steps c / 16 = HALF*2 + {0, 1} and
+// 4 + HALF*2 + {0, 1} of both terms of h_t (A from TMEM), B the tile's rows BT .. 3 BT - 1 (dq: descriptor of
+// those rows' first K-half)
+template <int BT, int HALF>
+__device__ __forceinline__ void state_products(uint32_t d, uint32_t hs, uint64_t dq, uint32_t idesc, int xh)
+{
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const int ks = (kk & 1) + 2 * HALF + 4 * (kk >> 1);
+            tc::mma_ts(d, hs + 64 * tt + 8 * ks, sd_add(dq, (uint32_t)((ks >> 2) * xh + (ks & 3) * 32)), idesc,
+                       (HALF | tt | kk) ? 1u : 0u);
+        }
+}
+
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
@@ -254,6 +276,7 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
             constexpr uint32_t ID_Q = idesc_bf16(128, 2 * BT), ID_C = idesc_bf16(128, BT);
             constexpr uint32_t ID_B = idesc_bf16(128, D) | tc::kIdescAMajorMN | tc::kIdescBMajorMN;
             constexpr uint32_t ID_W = idesc_bf16(128, BT) | tc::kIdescAMajorMN;
+            const uint64_t dkk = tc::sdesc_sw128(sb + L::KKT);   // k_{t+1} k_t^T's two terms
             for (int t = 0; t < nmb && ok; ++t) {
                 const int p = t & 1;
                 const uint32_t xs = sb + L::X0 + (t % 3) * L::XB;
@@ -268,29 +291,22 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 tc::fence_proxy_async();   // the copied rows -> the tensor cores
                 // [q_t h_t, k_{t+1} h_t]^T: tile rows BT .. 3 BT - 1, K steps of the first chunk (c / 16 = 0, 1, 4,
                 // 5), then of the second while it is being split
-#pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    if (half == 1) {
-                        if (!(ok = tc::bar_wait(hs_half[1], t & 1, abort_w)))
-                            break;
-                        tc::fence_after();
-                        if (t == 0)   // k_0 h_0, the first mini-batch's rows (columns BT.. of the other parity)
-                            for (int tt = 0; tt < 2; ++tt)
-                                for (int ks = 0; ks < D / 16; ++ks)
-                                    tc::mma_ts(tmem + L::DA + 64 + BT, tmem + L::HS + 64 * tt + 8 * ks,
-                                               tc::sdesc_sw128(xs + (ks >> 2) * L::XH + (ks & 3) * 32), ID_C,
-                                               (tt | ks) ? 1u : 0u);
-                    }
-                    for (int tt = 0; tt < 2; ++tt)
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const int ks = (kk & 1) + 2 * half + 4 * (kk >> 1);
-                            tc::mma_ts(tmem + L::DA + 64 * p, tmem + L::HS + 64 * tt + 8 * ks,
-                                       tc::sdesc_sw128(xs + BT * 128 + (ks >> 2) * L::XH + (ks & 3) * 32), ID_Q,
-                                       (half | tt | kk) ? 1u : 0u);
-                        }
-                }
-                if (!ok)
+                const uint64_t dq = tc::sdesc_sw128(xs + BT * 128);
+                state_products<BT, 0>(tmem + L::DA + 64 * p, tmem + L::HS, dq, ID_Q, L::XH);
+                if (!(ok = tc::bar_wait(hs_half[1], t & 1, abort_w)))
                     break;
+                tc::fence_after();
+                if (t == 0) {   // k_0 h_0, the first mini-batch's rows (columns BT.. of the other parity)
+                    const uint64_t dk = tc::sdesc_sw128(xs);
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            tc::mma_ts(tmem + L::DA + 64 + BT, tmem + L::HS + 64 * tt + 8 * ks,
+                                       sd_add(dk, (uint32_t)((ks >> 2) * L::XH + (ks & 3) * 32)), ID_C,
+                                       (tt | ks) ? 1u : 0u);
+                }
+                state_products<BT, 1>(tmem + L::DA + 64 * p, tmem + L::HS, dq, ID_Q, L::XH);
                 tc::mma_commit(prod);
                 // W_t's terms (the chain) and the small products' B operands (the staging warps) are in place
                 if (!(ok = tc::bar_wait(v2t(p), (t >> 1) & 1, abort_w) && tc::bar_wait(kk(p), (t >> 1) & 1, abort_w)))
@@ -299,19 +315,28 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 // first the correction (k_{t+1} k_t^T) W_t onto k_{t+1} h_t, which the chain waits for: W_t's
                 // first two terms (MN-major A; they leave at most 2^-18 |W_t|) by k_{t+1} k_t^T's two, without
                 // the product of the two second terms (at most 2^-18 of the whole)
-                if (t + 1 < nmb)
+                const uint64_t dw = tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P, L::V2H);   // W_t's terms
+                if (t + 1 < nmb) {
+#pragma unroll
                     for (int tw = 0; tw < 2; ++tw)
+#pragma unroll
                         for (int tb = 0; tb < 2 - tw; ++tb)
+#pragma unroll
                             for (int ks = 0; ks < BT / 16; ++ks)
-                                tc::mma_ss(tmem + L::DA + 64 * p + BT,
-                                           tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tw * 2 * L::V2H + ks * 2048, L::V2H),
-                                           tc::sdesc_sw128(sb + L::KKT + tb * L::TB + ks * 32), ID_W, 1u);
+                                tc::mma_ss(tmem + L::DA + 64 * p + BT, sd_add(dw, tw * 2 * L::V2H + ks * 2048),
+                                           sd_add(dkk, tb * L::TB + ks * 32), ID_W, 1u);
+                }
                 tc::mma_commit(corr);
                 // the update h^T += W_t^T k_t into the fp32 state, on all three (exact) terms
-                for (int tt = 0; tt < 3; ++tt)
-                    for (int ks = 0; ks < BT / 16; ++ks)
-                        tc::mma_ss(tmem + L::HT, tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tt * 2 * L::V2H + ks * 2048, L::V2H),
-                                   tc::sdesc_mn_sw128(xs + ks * 2048, L::XH), ID_B, 1u);
+                {
+                    const uint64_t dkr = tc::sdesc_mn_sw128(xs, L::XH);   // the tile's k_t rows, MN-major
+#pragma unroll
+                    for (int tt = 0; tt < 3; ++tt)
+#pragma unroll
+                        for (int ks = 0; ks < BT / 16; ++ks)
+                            tc::mma_ss(tmem + L::HT, sd_add(dw, tt * 2 * L::V2H + ks * 2048), sd_add(dkr, ks * 2048),
+                                       ID_B, 1u);
+                }
                 tc::mma_commit(upd);
                 tc::mma_commit(&slot_free[t % 3]);
             }
@@ -335,8 +360,10 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                 return false;
             tc::fence_after();
             tc::fence_proxy_async();   // the copied rows -> the tensor cores
+            const uint64_t d0 = tc::sdesc_sw128(xr);
+#pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                const uint64_t dx = tc::sdesc_sw128(xr + (ks >> 2) * L::XH + (ks & 3) * 32);
+                const uint64_t dx = sd_add(d0, (uint32_t)((ks >> 2) * L::XH + (ks & 3) * 32));
                 tc::mma_ss(tmem + L::DC + 32 * (tt & 1), dx, dx, ID_C, ks ? 1u : 0u);
             }
             tc::mma_commit(rows);
@@ -393,14 +420,16 @@ __global__ void __launch_bounds__(NTH, 1) ttt_linear_tc(TttArgs a)
                          (t < 2 || tc::bar_wait(&out_free[p], ((t >> 1) - 1) & 1, abort_w));
                     if (ok) {
                         tc::fence_after();
+                        const uint64_t dw = tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P, L::V2H);
+                        const uint64_t dm = tc::sdesc_sw128(sb + L::MST);
+#pragma unroll
                         for (int tw = 0; tw < 2; ++tw)   // (without the product of the two second terms)
+#pragma unroll
                             for (int tb = 0; tb < 2 - tw; ++tb)
+#pragma unroll
                                 for (int ks = 0; ks < BT / 16; ++ks)
-                                    tc::mma_ss(tmem + L::DO + 32 * p,
-                                               tc::sdesc_mn_sw128(sb + L::V2T + p * L::V2P + tw * 2 * L::V2H + ks * 2048,
-                                                                  L::V2H),
-                                               tc::sdesc_sw128(sb + L::MST + tb * L::TB + ks * 32), ID_W,
-                                               (tw | tb | ks) ? 1u : 0u);
+                                    tc::mma_ss(tmem + L::DO + 32 * p, sd_add(dw, tw * 2 * L::V2H + ks * 2048),
+                                               sd_add(dm, tb * L::TB + ks * 32), ID_W, (tw | tb | ks) ? 1u : 0u);
                         tc::mma_commit(&tail[p]);
                         if (t + 1 < nmb)
                             ok = row_products(t + 1);
