@@ -141,15 +141,20 @@ __device__ __forceinline__ void quad_transpose(float (&a)[4], int p)
 }
 
 // K-major operand whose K index runs over two 64-element halves `hs` bytes apart: K step kk (16 elements)
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, uint32_t hs)
-{
-    return tc::sdesc_sw128(base + (kk >> 2) * hs + (kk & 3) * 32);
-}
-// MN-major operand (MN blocks of 64 `lbo` bytes apart, K = rows of 128 bytes): K step kk (16 rows)
-__device__ __forceinline__ uint64_t mdesc(uint32_t base, int kk, uint32_t lbo)
-{
-    return tc::sdesc_mn_sw128(base + kk * 2048, lbo);
-}
+// Shared-memory descriptors of the operand tiles, formed from bases computed once: K-major (step kk of 16 keys:
+// 32 bytes inside a 128-byte row, 64-key halves `hs` bytes apart) and MN-major (step kk: 16 rows of 128 bytes;
+// 64-element blocks `lbo` bytes apart).  The start-address field holds address >> 4 and shared addresses stay
+// below 2^18, so adding an offset cannot carry out of it; with the MMA loops unrolled the offsets are constants
+// and an issuing thread spends about half the cycles per tcgen05.mma that forming each descriptor anew costs.
+struct Descs {
+    uint64_t k, m8, m16;
+    __device__ __forceinline__ uint64_t kd(uint32_t ofs, int kk, uint32_t hs) const
+    {
+        return k + ((ofs + (kk >> 2) * hs + (kk & 3) * 32) >> 4);
+    }
+    __device__ __forceinline__ uint64_t md8(uint32_t ofs, int kk) const { return m8 + ((ofs + kk * 2048) >> 4); }
+    __device__ __forceinline__ uint64_t md16(uint32_t ofs, int kk) const { return m16 + ((ofs + kk * 2048) >> 4); }
+};
 
 // One (chunk, head) item: rows [bos, bos + len) of head h; row t of the chunk is row-head index rb + t * rs.
 struct Item {
@@ -240,6 +245,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
 
         bool ok = true;
         uint32_t mph = 0;   // completed waits on bar_mma
+        const Descs dsc{tc::sdesc_sw128(sb), tc::sdesc_mn_sw128(sb, 8192), tc::sdesc_mn_sw128(sb, 16384)};
         auto wait_mma = [&]() {
             const bool got = tc::bar_wait(bar_mma, mph & 1, abort_w);
             ++mph;
@@ -365,14 +371,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
 
             // ---- AM = q~ k~^T (six term products), BM = do v^T
             if (tid == 0) {
-#pragma unroll 1
+#pragma unroll
                 for (int ta = 0; ta < 3; ++ta)
                     for (int tb = 0; ta + tb < 3; ++tb)
                         for (int kk = 0; kk < 8; ++kk)
-                            tc::mma_ss(tmem + TM_AM, kdesc(sb + Q3 + ta * 16384, kk, 8192),
-                                       kdesc(sb + K3 + tb * 16384, kk, 8192), ID, (ta | tb | kk) ? 1u : 0u);
+                            tc::mma_ss(tmem + TM_AM, dsc.kd(Q3 + ta * 16384, kk, 8192),
+                                       dsc.kd(K3 + tb * 16384, kk, 8192), ID, (ta | tb | kk) ? 1u : 0u);
                 for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_ss(tmem + TM_BM, kdesc(sb + DO, kk, 8192), kdesc(sb + VV, kk, 8192), ID, kk ? 1u : 0u);
+                    tc::mma_ss(tmem + TM_BM, dsc.kd(DO, kk, 8192), dsc.kd(VV, kk, 8192), ID, kk ? 1u : 0u);
                 tc::mma_commit(bar_mma);
             }
             wait_mma();
@@ -416,24 +422,24 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
             const uint32_t acc = tmem;
             if (tid == 0 && (nit == 0 || tc::bar_wait(acc_empty, (nit - 1) & 1, abort_w))) {
                 tc::fence_after();
-#pragma unroll 1
+#pragma unroll
                 for (int ta = 0; ta < 3; ++ta)
                     for (int tb = 0; ta + tb < 3; ++tb)
                         for (int kk = 0; kk < 4; ++kk)
-                            tc::mma_ss(acc + TM_DQ, mdesc(sb + K3 + ta * 16384, kk, 8192),
-                                       kdesc(sb + BM3 + tb * 8192, kk, 0), ID | tc::kIdescAMajorMN,
+                            tc::mma_ss(acc + TM_DQ, dsc.md8(K3 + ta * 16384, kk),
+                                       dsc.kd(BM3 + tb * 8192, kk, 0), ID | tc::kIdescAMajorMN,
                                        (ta | tb | kk) ? 1u : 0u);
-#pragma unroll 1
+#pragma unroll
                 for (int ta = 0; ta < 3; ++ta)
                     for (int tb = 0; ta + tb < 3; ++tb)
                         for (int kk = 0; kk < 4; ++kk)
-                            tc::mma_ss(acc + TM_DK, mdesc(sb + Q3 + ta * 16384, kk, 8192),
-                                       mdesc(sb + BM3 + tb * 8192, kk, 8192),
+                            tc::mma_ss(acc + TM_DK, dsc.md8(Q3 + ta * 16384, kk),
+                                       dsc.md8(BM3 + tb * 8192, kk),
                                        ID | tc::kIdescAMajorMN | tc::kIdescBMajorMN, (ta | tb | kk) ? 1u : 0u);
-#pragma unroll 1
+#pragma unroll
                 for (int t = 0; t < 3; ++t)
                     for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ss(acc + TM_DV, mdesc(sb + DO, kk, 8192), mdesc(sb + AM3 + t * 8192, kk, 8192),
+                        tc::mma_ss(acc + TM_DV, dsc.md8(DO, kk), dsc.md8(AM3 + t * 8192, kk),
                                    ID | tc::kIdescAMajorMN | tc::kIdescBMajorMN, (t | kk) ? 1u : 0u);
                 tc::mma_commit(bar_mma);
             }
@@ -445,17 +451,17 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
             // ---- R' = 2^(G_l - G_a) R_c: dk^T += R' v^T, dv^T += R'^T k~^T
             split_state(FR);
             if (tid == 0) {
-#pragma unroll 1
+#pragma unroll
                 for (int t = 0; t < 3; ++t)
                     for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ss(acc + TM_DK, kdesc(sb + ST3 + t * 32768, kk, 16384), kdesc(sb + VV, kk, 8192),
+                        tc::mma_ss(acc + TM_DK, dsc.kd(ST3 + t * 32768, kk, 16384), dsc.kd(VV, kk, 8192),
                                    ID, 1u);
-#pragma unroll 1
+#pragma unroll
                 for (int ta = 0; ta < 3; ++ta)
                     for (int tb = 0; ta + tb < 3; ++tb)
                         for (int kk = 0; kk < 8; ++kk)
-                            tc::mma_ss(acc + TM_DV, mdesc(sb + ST3 + ta * 32768, kk, 16384),
-                                       kdesc(sb + K3 + tb * 16384, kk, 8192), ID | tc::kIdescAMajorMN, 1u);
+                            tc::mma_ss(acc + TM_DV, dsc.md16(ST3 + ta * 32768, kk),
+                                       dsc.kd(K3 + tb * 16384, kk, 8192), ID | tc::kIdescAMajorMN, 1u);
                 tc::mma_commit(bar_mma);
             }
             fetch_state(a.dS, cur);
@@ -466,10 +472,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_grads_tc(BwdArgs a, int nitems)
             // ---- S' = scale 2^(G_a) S_c: dq^T += S' do^T; the accumulator set goes to the epilogue
             split_state(FA);
             if (tid == 0) {
-#pragma unroll 1
+#pragma unroll
                 for (int t = 0; t < 3; ++t)
                     for (int kk = 0; kk < 8; ++kk)
-                        tc::mma_ss(acc + TM_DQ, kdesc(sb + ST3 + t * 32768, kk, 16384), kdesc(sb + DO, kk, 8192),
+                        tc::mma_ss(acc + TM_DQ, dsc.kd(ST3 + t * 32768, kk, 16384), dsc.kd(DO, kk, 8192),
                                    ID, 1u);
                 tc::mma_commit(bar_mma);
                 tc::mma_commit(acc_full);
