@@ -16,19 +16,20 @@
 //   * the split warps (which also form the outputs) cut h_t into two bf16 terms as soon as the update that
 //     made it is complete (h = h1 + h2 + e, |e| <= 2^-18 |h|, each term rounded to nearest by conversion);
 //   * one issuing thread then takes h_t^T [q_t; k_{t+1}]^T (tcgen05 kind::f16, A the two terms from TMEM,
-//     M = 128, N = 2 BT, K = D: the outputs' q h and the next mini-batch's k h_t); the row products of the
-//     tile [k_t; q_t; k_{t+1}] with k_t (q k^T for the outputs, k_{t+1} k_t^T for the next correction) need
-//     no state and are issued a mini-batch ahead, and two staging warps turn them into the B operands of the
-//     small products with W_t (two bf16 terms each);
-//   * the chain warps take the rows' LayerNorm statistics and the two gradient sums over the 128 lanes (four
-//     warps of 32, merged through shared memory) and v2_t; W_t = -eta_last v2_t is split exactly into three
-//     bf16 terms (MN-major A): the update h^T += W^T k is one more product accumulating into the fp32 state
-//     on all three (B: the k rows of the tile, MN-major), so the state itself is never rewritten by the CUDA
-//     cores, and the small products (the correction, the outputs' score-weighted sums) take the first two,
-//     which leave at most 2^-18 |W_t|;
-//   * the outputs of a mini-batch are formed one mini-batch behind from its q h columns, v2, learning rates
-//     and the product of its masked scores with W_t, kept in buffers by parity and released through
-//     mbarriers.
+//     M = 128, N = 2 BT, K = D: the outputs' q h and the next mini-batch's k h_t), the correction and the
+//     update; the row products of the tile [k_t; q_t; k_{t+1}] with k_t (q k^T for the outputs, k_{t+1} k_t^T
+//     for the next correction) need no state and are issued a mini-batch ahead by a second issuing thread
+//     (which also issues the outputs' small products), and two staging warps turn them into the B operands of
+//     the small products with W_t (two bf16 terms each);
+//   * the chain warps move k h (transposed in TMEM) to shared memory once and run the rest of the step on rows,
+//     so the LayerNorm statistics and the two gradient sums are reductions within a warp; W_t = -eta_last v2_t
+//     is split exactly into three bf16 terms (MN-major A): the update h^T += W^T k is one more product
+//     accumulating into the fp32 state on all three (B: the k rows of the tile, MN-major), so the state itself
+//     is never rewritten by the CUDA cores, and the small products (the correction, the outputs'
+//     score-weighted sums) take the first two, which leave at most 2^-18 |W_t|;
+//   * the outputs of a mini-batch are formed one mini-batch behind from its q h columns, hb and the product
+//     of its masked scores with W_t, through shared memory to rows for their LayerNorm, with the buffers kept
+//     by parity and released through mbarriers.
 // Rows arrive by asynchronous copies two mini-batches ahead (three tiles in turn); rows past the end of a
 // sequence are zero in k and q and take no part in the update (as the CUDA-core path).
 #include <cuda_bf16.h>
